@@ -1,0 +1,210 @@
+/*
+ * qsa.h -- C ABI of the GB300 (sm_103a) QSA block-sparse GQA decode / verify
+ * library over an NVFP4 paged KV cache.
+ *
+ * One decode or speculative-verify step is three calls on one stream:
+ *
+ *   qsa_index_scores   exact int8 index dot products -> one int32 score per
+ *                      (query row, KV block)
+ *   qsa_select_topk    canonical top-k block selection per query row
+ *   qsa_sparse_decode  split-KV GQA attention over the selected NVFP4 pages,
+ *                      dequantised in registers, partials merged by log-sum-exp
+ *
+ * Sources (TensorRT-LLM pull-request pages):
+ *   [F]  PR #20276 "Qwen3.8-Flash-Next NVFP4 target", Features table: NVFP4 KV
+ *        cache = uint8 e2m1 pages + e4m3 block scales, QSA side planes packed
+ *        so that one page index addresses every pool; canonical QSA selection.
+ *   [D]  PR #20276, Decisions: canonical selection is a pure function of the
+ *        scores, the window and k, identical from launch to launch.
+ *   [W]  PR #20937 "GB300 perf work on qwen3_8_flash_next_nvfp4__sm_103__tp1",
+ *        What changes: NVFP4 sparse GQA decode as split-K + merge with a lean
+ *        one-split variant; verify as request-grouped sparse GQA with a
+ *        per-row merge; request-tiled index scores.
+ *   [Q]  PR #20937, Per-File QA: invalid-page handling and masking.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Geometry (qsa_geom_t, host values): B requests, R = rows_per_req query rows
+ * per request (1 for decode, 1 + drafts for verify), T = B*R rows, row r =
+ * b*R + j.  Hq query heads, Hkv KV heads, G = Hq/Hkv; query head h reads KV
+ * head h / G.  D = head_dim = 128, Di = index_dim = 64, P = page_size (64 or
+ * 128 tokens), MB = max_blocks (page-table row stride), NP = num_pages.
+ *
+ * Visibility: seqlens[b] = L_b counts the request's cached tokens including
+ * its R newest rows; row j sees n = clamp(L_b - R + 1 + j, 0, MB*P) tokens
+ * (causal among the R rows).  Block beta holds tokens [beta*P, beta*P + P).
+ *
+ * Page table: page_table[b*MB + beta] is the physical page of block beta of
+ * request b; an entry < 0 or >= NP marks an invalid block, which is masked,
+ * never dereferenced.
+ *
+ * Memory: every pointer argument is DEVICE memory owned by the caller; the
+ * library never allocates, frees or keeps global state.  Calls are
+ * asynchronous on `stream`, read no device data on the host, and size their
+ * grids from the geometry alone, so a step can be captured in a CUDA graph.
+ *
+ * Errors: each call validates its arguments on the host and returns a status
+ * before launching anything; QSA_ERR_CUDA reports a launch failure.  Bad
+ * device data (page ids, seqlens, sel entries) is masked, never trapped.
+ */
+#ifndef QSA_H_
+#define QSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QSA_OK = 0,
+    QSA_ERR_INVALID_ARG = 1,   /* null pointer or inconsistent geometry      */
+    QSA_ERR_UNSUPPORTED = 2,   /* shape outside the built kernels, or not sm_103 */
+    QSA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed        */
+    QSA_ERR_WORKSPACE = 4,     /* workspace missing or too small              */
+    QSA_ERR_DEVICE_TIMEOUT = 5 /* a bounded device-side wait gave up (status word) */
+} qsa_status_t;
+
+typedef struct {
+    int batch;          /* B                                    */
+    int rows_per_req;   /* R = 1 + draft rows, 1..8             */
+    int num_q_heads;    /* Hq, 1..256                           */
+    int num_kv_heads;   /* Hkv, divides Hq                      */
+    int head_dim;       /* D, must be 128                       */
+    int index_dim;      /* Di, must be 64                       */
+    int page_size;      /* P, 64 or 128                         */
+    int max_blocks;     /* MB, page-table row stride, >= 1      */
+    int num_pages;      /* NP, pages in every pool, >= 1        */
+} qsa_geom_t;
+
+/* Human-readable name of a status. Never NULL. */
+const char *qsa_status_string(qsa_status_t status);
+
+/*
+ * A1 -- index scores ([W] request-tiled index scores; [F] index keys share the
+ * page index of the K/V pools).
+ *
+ *   iq        int8  [T, Hq, Di]   index query of every row and query head
+ *   ik_pool   int8  [NP, P, Di]   index key of every cached token
+ *   page_table int32 [B, MB]
+ *   seqlens   int32 [B]
+ *   scores    int32 [T, MB]       output
+ *
+ * scores[r, beta] = max over the visible tokens t of block beta of
+ *                   sum_h sum_d iq[r, h, d] * ik[page, t - beta*P, d],
+ * exact in int32 (|value| <= 64*64*127*127 for Hq <= 64; Hq <= 256 keeps it
+ * below 2^31), or INT32_MIN when the block's page is invalid or the block has
+ * no token visible to row r (all beta >= ceil(n/P) included).
+ */
+qsa_status_t qsa_index_scores(const qsa_geom_t *geom, const int8_t *iq,
+                              const int8_t *ik_pool, const int32_t *page_table,
+                              const int32_t *seqlens, int32_t *scores,
+                              cudaStream_t stream);
+
+/*
+ * A2 -- canonical top-k selection ([F] Features table; [D] Decisions).
+ *
+ *   scores    int32 [T, MB]  as written by qsa_index_scores (INT32_MIN =
+ *                            invalid block)
+ *   seqlens   int32 [B]
+ *   k         blocks per row, window included, 1..1024
+ *   window    always-kept recent blocks, 0..k
+ *   sel       int32 [T, k]   output: selected block indices, ascending,
+ *                            padded with -1
+ *   nsel      int32 [T]      output: number of selected blocks
+ *
+ * Per row with nb = ceil(n/P) visible blocks: the valid blocks among the last
+ * `window` visible ones are always kept; the remaining slots (k minus those)
+ * go to the other valid visible blocks ranked by score, higher first, ties to
+ * the higher block index -- every block strictly above the k-th score, then
+ * the highest-index blocks at the k-th score.  An invalid window block frees
+ * its slot.  A pure function of (scores, seqlens, k, window): identical bits
+ * on every launch.
+ */
+qsa_status_t qsa_select_topk(const qsa_geom_t *geom, const int32_t *scores,
+                             const int32_t *seqlens, int k, int window,
+                             int32_t *sel, int32_t *nsel, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace qsa_sparse_decode needs for this geometry and k
+ * with the automatic split count (num_splits = 0), or for an explicit
+ * num_splits >= 1 with the _ex variant below.  Returns 0 for an invalid
+ * geometry.  Host-only; launches nothing.
+ */
+size_t qsa_sparse_decode_workspace_bytes(const qsa_geom_t *geom, int k);
+size_t qsa_sparse_decode_workspace_bytes_ex(const qsa_geom_t *geom, int k,
+                                            int num_splits);
+
+/*
+ * Zero-fills a workspace (its split-merge tickets and status word must start
+ * at zero). Call once after allocating it; every qsa_sparse_decode leaves the
+ * tickets at zero again, so a workspace is reusable across steps as long as
+ * calls using it do not overlap on the GPU.  Asynchronous on `stream`.
+ */
+qsa_status_t qsa_workspace_init(void *workspace, size_t workspace_bytes,
+                                cudaStream_t stream);
+
+/*
+ * A3 -- split-KV sparse GQA over the selected NVFP4 pages ([W] split-K +
+ * merge, lean one-split variant, request-grouped verify with a per-row merge;
+ * [F] NVFP4 page format; [Q] invalid-page masking).
+ *
+ *   q         bf16  [T, Hq, D]
+ *   k_pool, v_pool  uint8 [NP, Hkv, P, D/2]  two e2m1 codes per byte, low
+ *                                            nibble = even element
+ *   k_sf, v_sf      uint8 [NP, Hkv, P, D/16] e4m3 scale per 16 elements
+ *   k_scale, v_scale  fp32 per-tensor dequant multipliers:
+ *                     K = e2m1 * e4m3 * k_scale, V likewise
+ *   sm_scale  softmax scale applied to q.K (1/sqrt(D) conventionally)
+ *   page_table, seqlens as above
+ *   sel       int32 [T, k]   ascending block ids padded with -1 (the output of
+ *                            qsa_select_topk)
+ *   out       bf16  [T, Hq, D]   output
+ *   lse       fp32  [T, Hq]      output, natural-log sum of exp(sm_scale*q.K)
+ *   workspace device memory of at least qsa_sparse_decode_workspace_bytes(),
+ *             zero-filled once by qsa_workspace_init().
+ *
+ * For row r and head h, the attended tokens are those of the distinct blocks
+ * listed in sel[r, :] whose page is valid, restricted to the row's n visible
+ * tokens.  Each (request, KV head) pass reads every page in the union of its
+ * rows' selections once and serves all G*R query vectors.  A row with no
+ * tokens gets out = 0 and lse = -inf.  Rounding: fp32 accumulation, bf16 RNE
+ * output.
+ */
+qsa_status_t qsa_sparse_decode(const qsa_geom_t *geom, const void *q_bf16,
+                               const uint8_t *k_pool, const uint8_t *k_sf,
+                               const uint8_t *v_pool, const uint8_t *v_sf,
+                               float k_scale, float v_scale, float sm_scale,
+                               const int32_t *page_table, const int32_t *seqlens,
+                               const int32_t *sel, int k, void *out_bf16,
+                               float *lse, void *workspace,
+                               size_t workspace_bytes, cudaStream_t stream);
+
+/* As qsa_sparse_decode, with the number of KV splits per (request, KV head)
+ * forced to num_splits (>= 1), or chosen automatically when 0.  Results agree
+ * across split counts within fp32 rounding. */
+qsa_status_t qsa_sparse_decode_ex(const qsa_geom_t *geom, const void *q_bf16,
+                                  const uint8_t *k_pool, const uint8_t *k_sf,
+                                  const uint8_t *v_pool, const uint8_t *v_sf,
+                                  float k_scale, float v_scale, float sm_scale,
+                                  const int32_t *page_table,
+                                  const int32_t *seqlens, const int32_t *sel,
+                                  int k, void *out_bf16, float *lse,
+                                  void *workspace, size_t workspace_bytes,
+                                  int num_splits, cudaStream_t stream);
+
+/*
+ * Reads the workspace's device status word (synchronising `stream`): 0 when
+ * every bounded wait since qsa_workspace_init() completed, otherwise a
+ * nonzero code and QSA_ERR_DEVICE_TIMEOUT is returned.  Diagnostic only.
+ */
+qsa_status_t qsa_workspace_status(const void *workspace, int *device_code,
+                                  cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSA_H_ */

@@ -1,0 +1,68 @@
+"""QSA block-sparse GQA decode / speculative verify over an NVFP4 paged KV
+cache, for one GB300 (sm_103a).
+
+The compute lives in libqsa.so (hand-written CUDA kernels behind the C ABI of
+include/qsa.h); this package is its ctypes binding plus a small helper that
+owns the per-step output buffers.  Importing the package does not load the
+library; the first call does, and raises if it is not built.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from .binding import (EXPORTS, QsaError, load, make_geom, qsa_geom_t, qsa_index_scores,
+                      qsa_select_topk, qsa_sparse_decode, qsa_sparse_decode_ex,
+                      qsa_sparse_decode_workspace_bytes, qsa_sparse_decode_workspace_bytes_ex,
+                      qsa_status_string, qsa_workspace_init, qsa_workspace_status)
+
+__all__ = [
+    "EXPORTS", "QsaError", "load", "make_geom", "qsa_geom_t", "qsa_index_scores",
+    "qsa_select_topk", "qsa_sparse_decode", "qsa_sparse_decode_ex",
+    "qsa_sparse_decode_workspace_bytes", "qsa_sparse_decode_workspace_bytes_ex",
+    "qsa_status_string", "qsa_workspace_init", "qsa_workspace_status", "DecodeStep",
+]
+
+GEOM_FIELDS = [n for n, _ in qsa_geom_t._fields_]
+
+
+class DecodeStep:
+    """Device buffers for one QSA step of a fixed geometry, and the three
+    library calls that fill them: index scores -> top-k selection -> sparse
+    decode.  ``num_splits`` = 0 lets the library choose the KV split count."""
+
+    def __init__(self, geom: dict, k: int, window: int, device="cuda", num_splits: int = 0):
+        self.geom = {n: int(geom[n]) for n in GEOM_FIELDS}
+        self.cg = make_geom(**self.geom)
+        self.k, self.window, self.num_splits = int(k), int(window), int(num_splits)
+        T = self.geom["batch"] * self.geom["rows_per_req"]
+        Hq, D, MB = self.geom["num_q_heads"], self.geom["head_dim"], self.geom["max_blocks"]
+        dev = torch.device(device)
+        self.scores = torch.empty((T, MB), dtype=torch.int32, device=dev)
+        self.sel = torch.empty((T, self.k), dtype=torch.int32, device=dev)
+        self.nsel = torch.empty((T,), dtype=torch.int32, device=dev)
+        self.out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
+        nbytes = qsa_sparse_decode_workspace_bytes_ex(self.cg, self.k, self.num_splits)
+        if nbytes == 0:
+            raise QsaError("qsa_sparse_decode_workspace_bytes", 1, "invalid geometry")
+        self.workspace = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
+        qsa_workspace_init(self.workspace)
+
+    def run(self, w: dict, stream=None, sm_scale=None):
+        """One step over workload tensors ``w`` (the generator's layout)."""
+        sm = float(w["sm_scale"]) if sm_scale is None else float(sm_scale)
+        qsa_index_scores(self.cg, w["iq"], w["ik_pool"], w["page_table"], w["seqlens"],
+                         self.scores, stream)
+        qsa_select_topk(self.cg, self.scores, w["seqlens"], self.k, self.window, self.sel,
+                        self.nsel, stream)
+        qsa_sparse_decode_ex(self.cg, w["q"], w["k_pool"], w["k_sf"], w["v_pool"], w["v_sf"],
+                             w["k_scale"], w["v_scale"], sm, w["page_table"], w["seqlens"],
+                             self.sel, self.k, self.out, self.lse, self.workspace,
+                             self.num_splits, stream)
+        return self
+
+    @staticmethod
+    def default_sm_scale(head_dim: int = 128) -> float:
+        return 1.0 / math.sqrt(head_dim)

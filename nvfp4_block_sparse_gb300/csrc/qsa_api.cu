@@ -1,0 +1,190 @@
+// qsa_api.cu -- the library's C ABI (declared in include/qsa.h): host-side
+// argument validation, the sm_103 gate and the launches on the caller's
+// stream.  Nothing here allocates, synchronises (except the diagnostic
+// qsa_workspace_status) or reads device data.
+//
+// TensorRT-LLM PR #20937 ("GB300 perf work on
+// qwen3_8_flash_next_nvfp4__sm_103__tp1"), review of the grouped-verify
+// tests: the grouped NVFP4 path runs on SM 10.3 only; callers pass their own
+// buffers (Per-File QA: caller-provided buffers).
+#include "qsa_common.cuh"
+
+#include <stdint.h>
+
+namespace {
+
+using qsa::Geom;
+
+bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+qsa_status_t check_geom(const qsa_geom_t* g) {
+  if (!g) return QSA_ERR_INVALID_ARG;
+  if (g->batch < 1 || g->batch > 65535) return QSA_ERR_INVALID_ARG;
+  if (g->rows_per_req < 1) return QSA_ERR_INVALID_ARG;
+  if (g->num_q_heads < 1 || g->num_kv_heads < 1) return QSA_ERR_INVALID_ARG;
+  if (g->num_q_heads % g->num_kv_heads != 0) return QSA_ERR_INVALID_ARG;
+  if (g->max_blocks < 1 || g->num_pages < 1) return QSA_ERR_INVALID_ARG;
+  if (g->head_dim != qsa::kHeadDim || g->index_dim != qsa::kIndexDim) return QSA_ERR_UNSUPPORTED;
+  if (g->page_size != 64 && g->page_size != 128) return QSA_ERR_UNSUPPORTED;
+  if (g->rows_per_req > qsa::kMaxRows) return QSA_ERR_UNSUPPORTED;
+  if (g->num_q_heads > qsa::kMaxQHeads) return QSA_ERR_UNSUPPORTED;
+  if (g->max_blocks > qsa::kMaxBlocks) return QSA_ERR_UNSUPPORTED;
+  if ((long long)g->batch * g->rows_per_req > (1LL << 24)) return QSA_ERR_UNSUPPORTED;
+  return QSA_OK;
+}
+
+Geom to_geom(const qsa_geom_t* g) {
+  Geom r;
+  r.B = g->batch;
+  r.R = g->rows_per_req;
+  r.Hq = g->num_q_heads;
+  r.Hkv = g->num_kv_heads;
+  r.D = g->head_dim;
+  r.Di = g->index_dim;
+  r.P = g->page_size;
+  r.MB = g->max_blocks;
+  r.NP = g->num_pages;
+  return r;
+}
+
+// The kernels use sm_103a instructions (tcgen05-era conversions, bulk copies).
+qsa_status_t check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return QSA_ERR_CUDA;
+  }
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return QSA_ERR_CUDA;
+  }
+  if (major != 10 || minor != 3) return QSA_ERR_UNSUPPORTED;
+  return QSA_OK;
+}
+
+qsa_status_t from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) e = cudaGetLastError();
+  else cudaGetLastError();
+  return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
+}
+
+qsa_status_t check_decode_args(const qsa_geom_t* geom, int k) {
+  qsa_status_t st = check_geom(geom);
+  if (st != QSA_OK) return st;
+  if (k < 1) return QSA_ERR_INVALID_ARG;
+  if (k > qsa::kMaxK) return QSA_ERR_UNSUPPORTED;
+  if ((long long)geom->rows_per_req * k > qsa::kMaxUnion) return QSA_ERR_UNSUPPORTED;
+  return QSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qsa_status_string(qsa_status_t s) {
+  switch (s) {
+    case QSA_OK: return "ok";
+    case QSA_ERR_INVALID_ARG: return "invalid argument";
+    case QSA_ERR_UNSUPPORTED: return "unsupported shape or device (needs sm_103)";
+    case QSA_ERR_CUDA: return "CUDA error";
+    case QSA_ERR_WORKSPACE: return "workspace missing or too small";
+    case QSA_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+qsa_status_t qsa_index_scores(const qsa_geom_t* geom, const int8_t* iq, const int8_t* ik_pool,
+                              const int32_t* page_table, const int32_t* seqlens,
+                              int32_t* scores, cudaStream_t stream) {
+  qsa_status_t st = check_geom(geom);
+  if (st != QSA_OK) return st;
+  if (!iq || !ik_pool || !page_table || !seqlens || !scores) return QSA_ERR_INVALID_ARG;
+  if (!aligned(ik_pool, 16)) return QSA_ERR_INVALID_ARG;
+  st = check_device();
+  if (st != QSA_OK) return st;
+  return from_cuda(qsa::launch_index_scores(to_geom(geom), iq, ik_pool, page_table, seqlens,
+                                            scores, true, stream));
+}
+
+qsa_status_t qsa_select_topk(const qsa_geom_t* geom, const int32_t* scores,
+                             const int32_t* seqlens, int k, int window, int32_t* sel,
+                             int32_t* nsel, cudaStream_t stream) {
+  qsa_status_t st = check_geom(geom);
+  if (st != QSA_OK) return st;
+  if (!scores || !seqlens || !sel || !nsel) return QSA_ERR_INVALID_ARG;
+  if (k < 1 || window < 0 || window > k) return QSA_ERR_INVALID_ARG;
+  if (k > qsa::kMaxK) return QSA_ERR_UNSUPPORTED;
+  st = check_device();
+  if (st != QSA_OK) return st;
+  return from_cuda(qsa::launch_select_topk(to_geom(geom), scores, seqlens, k, window, sel, nsel,
+                                           true, stream));
+}
+
+size_t qsa_sparse_decode_workspace_bytes_ex(const qsa_geom_t* geom, int k, int num_splits) {
+  if (check_decode_args(geom, k) != QSA_OK || num_splits < 0) return 0;
+  return qsa::plan_sparse_decode(to_geom(geom), k, num_splits).ws_bytes;
+}
+
+size_t qsa_sparse_decode_workspace_bytes(const qsa_geom_t* geom, int k) {
+  return qsa_sparse_decode_workspace_bytes_ex(geom, k, 0);
+}
+
+qsa_status_t qsa_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!workspace || workspace_bytes == 0) return QSA_ERR_INVALID_ARG;
+  return from_cuda(cudaMemsetAsync(workspace, 0, workspace_bytes, stream));
+}
+
+qsa_status_t qsa_sparse_decode_ex(const qsa_geom_t* geom, const void* q_bf16,
+                                  const uint8_t* k_pool, const uint8_t* k_sf,
+                                  const uint8_t* v_pool, const uint8_t* v_sf, float k_scale,
+                                  float v_scale, float sm_scale, const int32_t* page_table,
+                                  const int32_t* seqlens, const int32_t* sel, int k,
+                                  void* out_bf16, float* lse, void* workspace,
+                                  size_t workspace_bytes, int num_splits, cudaStream_t stream) {
+  qsa_status_t st = check_decode_args(geom, k);
+  if (st != QSA_OK) return st;
+  if (num_splits < 0) return QSA_ERR_INVALID_ARG;
+  if (!q_bf16 || !k_pool || !k_sf || !v_pool || !v_sf || !page_table || !seqlens || !sel ||
+      !out_bf16 || !lse)
+    return QSA_ERR_INVALID_ARG;
+  if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(k_sf, 16) || !aligned(v_sf, 16) ||
+      !aligned(q_bf16, 8))
+    return QSA_ERR_INVALID_ARG;
+  const Geom g = to_geom(geom);
+  const qsa::DecodePlan plan = qsa::plan_sparse_decode(g, k, num_splits);
+  if (!workspace || workspace_bytes < plan.ws_bytes || !aligned(workspace, 256))
+    return QSA_ERR_WORKSPACE;
+  st = check_device();
+  if (st != QSA_OK) return st;
+  return from_cuda(qsa::launch_sparse_decode(g, plan, q_bf16, k_pool, k_sf, v_pool, v_sf, k_scale,
+                                             v_scale, sm_scale, page_table, seqlens, sel, k,
+                                             out_bf16, lse, workspace, true, stream));
+}
+
+qsa_status_t qsa_sparse_decode(const qsa_geom_t* geom, const void* q_bf16, const uint8_t* k_pool,
+                               const uint8_t* k_sf, const uint8_t* v_pool, const uint8_t* v_sf,
+                               float k_scale, float v_scale, float sm_scale,
+                               const int32_t* page_table, const int32_t* seqlens,
+                               const int32_t* sel, int k, void* out_bf16, float* lse,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return qsa_sparse_decode_ex(geom, q_bf16, k_pool, k_sf, v_pool, v_sf, k_scale, v_scale,
+                              sm_scale, page_table, seqlens, sel, k, out_bf16, lse, workspace,
+                              workspace_bytes, 0, stream);
+}
+
+qsa_status_t qsa_workspace_status(const void* workspace, int* device_code, cudaStream_t stream) {
+  if (!workspace || !device_code) return QSA_ERR_INVALID_ARG;
+  int v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return QSA_ERR_CUDA;
+  }
+  *device_code = v;
+  return v == 0 ? QSA_OK : QSA_ERR_DEVICE_TIMEOUT;
+}
+
+}  // extern "C"

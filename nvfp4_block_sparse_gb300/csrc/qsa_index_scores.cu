@@ -1,0 +1,194 @@
+// qsa_index_scores.cu -- A1: exact int8 index scores per (query row, KV block).
+//
+// TensorRT-LLM PR #20937 ("GB300 perf work on
+// qwen3_8_flash_next_nvfp4__sm_103__tp1"), What changes / Verify:
+// request-tiled index scores; PR #20276 ("Qwen3.8-Flash-Next NVFP4 target"),
+// Features table: the QSA index plane is addressed by the same page index as
+// the K/V pools.
+//
+// score(r, beta) = max over visible tokens t of block beta of
+//                  sum_h sum_d iq[r,h,d] * ik[page, t, d]
+//
+// Design (HBM-bound streaming of 64 B per token):
+//  * The head sum is taken first: sum_h iq[r,h,:] . ik = (sum_h iq[r,h,:]) . ik.
+//    Both sides are exact integer arithmetic, so the result is bit-identical to
+//    the per-head sum, and one 64-long int16 x int8 dot product per (row,
+//    token) replaces Hq of them.
+//  * Request tiling: a CTA serves one request; each warp streams whole blocks
+//    (P tokens x 64 B, contiguous in the pool) with 16-byte loads, 4 lanes per
+//    token, and scores every one of the request's R rows from the same loads,
+//    so verify rows share one read of the keys.
+//  * dp2a (int16 pair x int8 pair) accumulates each lane's 16 dims in int32;
+//    two xor-shuffles finish the token's dot product and three more the
+//    block max.  Invalid pages and invisible blocks are never read.
+#include "qsa_common.cuh"
+
+namespace qsa {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+__device__ __forceinline__ int4 ld_stream_v4(const int4* p) {
+  int4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// RB: compile-time bound on rows per request (R <= RB).
+template <int P, int RB>
+__global__ void __launch_bounds__(kThreads)
+index_scores_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __restrict__ ik_pool,
+                    const int32_t* __restrict__ page_table, const int32_t* __restrict__ seqlens,
+                    int32_t* __restrict__ scores, int blocks_per_warp) {
+  __shared__ int32_t wpart[4][RB][kIndexDim];
+  __shared__ uint32_t wpack[RB][kIndexDim / 2];
+
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int R = g.R;
+
+  pdl_wait();
+
+  // Head sums of the request's index queries: w[j][d] = sum_h iq[b*R+j][h][d].
+  for (int idx = threadIdx.x; idx < 4 * RB * kIndexDim; idx += kThreads) {
+    const int hg = idx / (RB * kIndexDim);
+    const int j = (idx / kIndexDim) % RB;
+    const int d = idx % kIndexDim;
+    int s = 0;
+    if (j < R) {
+      const int8_t* src = iq + ((size_t)(b * R + j) * g.Hq) * kIndexDim + d;
+      for (int h = hg; h < g.Hq; h += 4) s += src[(size_t)h * kIndexDim];
+    }
+    wpart[hg][j][d] = s;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < RB * (kIndexDim / 2); idx += kThreads) {
+    const int j = idx / (kIndexDim / 2), i = idx % (kIndexDim / 2);
+    int w0 = 0, w1 = 0;
+#pragma unroll
+    for (int hg = 0; hg < 4; ++hg) {
+      w0 += wpart[hg][j][2 * i];
+      w1 += wpart[hg][j][2 * i + 1];
+    }
+    wpack[j][i] = ((uint32_t)w0 & 0xFFFFu) | ((uint32_t)w1 << 16);
+  }
+  __syncthreads();
+  pdl_trigger();
+
+  // Lane (token group lane>>2, part lane&3) covers dims [16*part, 16*part+16).
+  const int part = lane & 3;
+  uint32_t wr[RB][8];
+#pragma unroll
+  for (int j = 0; j < RB; ++j)
+#pragma unroll
+    for (int q = 0; q < 8; ++q) wr[j][q] = wpack[j][8 * part + q];
+
+  const int L = seqlens[b];
+  const int cap = g.MB * P;
+  int nrow[RB];
+#pragma unroll
+  for (int j = 0; j < RB; ++j) nrow[j] = (j < R) ? visible_tokens(L, R, j, cap) : 0;
+  const int nmax = visible_tokens(L, R, R - 1, cap);
+
+  for (int it = 0; it < blocks_per_warp; ++it) {
+    const int beta = (blockIdx.x * blocks_per_warp + it) * kWarps + warp;
+    if (beta >= g.MB) break;
+    const int page = page_table[(size_t)b * g.MB + beta];
+    const bool live = page >= 0 && page < g.NP && beta * P < nmax;
+    int32_t* dst = scores + (size_t)b * R * g.MB + beta;
+    if (!live) {
+      if (lane < R) dst[(size_t)lane * g.MB] = kSentinel;
+      continue;
+    }
+    const int4* src = reinterpret_cast<const int4*>(ik_pool + (size_t)page * P * kIndexDim) + lane;
+    int4 kv[P / 8];
+#pragma unroll
+    for (int i = 0; i < P / 8; ++i) kv[i] = ld_stream_v4(src + 32 * i);
+
+    int best[RB];
+#pragma unroll
+    for (int j = 0; j < RB; ++j) best[j] = kSentinel;
+#pragma unroll
+    for (int i = 0; i < P / 8; ++i) {
+      const int t_abs = beta * P + 8 * i + (lane >> 2);
+      const int words[4] = {kv[i].x, kv[i].y, kv[i].z, kv[i].w};
+#pragma unroll
+      for (int j = 0; j < RB; ++j) {
+        if (j < R) {
+          int acc = 0;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            acc = __dp2a_lo((int)wr[j][2 * m], words[m], acc);
+            acc = __dp2a_hi((int)wr[j][2 * m + 1], words[m], acc);
+          }
+          acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+          acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+          if (t_abs < nrow[j]) best[j] = max(best[j], acc);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < RB; ++j) {
+      if (j < R) {
+        int v = best[j];
+        v = max(v, __shfl_xor_sync(0xffffffffu, v, 4));
+        v = max(v, __shfl_xor_sync(0xffffffffu, v, 8));
+        v = max(v, __shfl_xor_sync(0xffffffffu, v, 16));
+        if (lane == j) dst[(size_t)j * g.MB] = (beta * P < nrow[j]) ? v : kSentinel;
+      }
+    }
+  }
+}
+
+template <int P, int RB>
+cudaError_t launch_t(const Geom& g, const int8_t* iq, const int8_t* ik_pool,
+                     const int32_t* page_table, const int32_t* seqlens, int32_t* scores,
+                     bool pdl, cudaStream_t stream) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // Enough warps in flight to cover HBM latency; more blocks per warp only
+  // when the grid would exceed ~4 resident CTAs per SM.
+  const long long warps_needed = (long long)g.B * g.MB;
+  const long long warp_slots = (long long)sms * 4 * kWarps;
+  int bpw = (int)((warps_needed + warp_slots - 1) / warp_slots);
+  bpw = bpw < 1 ? 1 : (bpw > 4 ? 4 : bpw);
+  dim3 grid((g.MB + kWarps * bpw - 1) / (kWarps * bpw), g.B);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, index_scores_kernel<P, RB>, g, iq, ik_pool, page_table,
+                            seqlens, scores, bpw);
+}
+
+template <int P>
+cudaError_t launch_p(const Geom& g, const int8_t* iq, const int8_t* ik_pool,
+                     const int32_t* page_table, const int32_t* seqlens, int32_t* scores,
+                     bool pdl, cudaStream_t stream) {
+  if (g.R <= 1) return launch_t<P, 1>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
+  if (g.R <= 2) return launch_t<P, 2>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
+  if (g.R <= 4) return launch_t<P, 4>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
+  return launch_t<P, 8>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_index_scores(const Geom& g, const int8_t* iq, const int8_t* ik_pool,
+                                const int32_t* page_table, const int32_t* seqlens,
+                                int32_t* scores, bool pdl, cudaStream_t stream) {
+  if (g.P == 64) return launch_p<64>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
+  return launch_p<128>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
+}
+
+}  // namespace qsa

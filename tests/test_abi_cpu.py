@@ -1,0 +1,110 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/qsa.h declares, and its host-side validation rejects bad arguments
+before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import nvfp4_block_sparse_gb300 as qsa
+from nvfp4_block_sparse_gb300 import binding
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "qsa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return qsa.load(build_if_missing=True)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qsa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declarations_match_binding():
+    assert declared_functions() == sorted(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert qsa.qsa_status_string(s)
+    assert "unknown" in qsa.qsa_status_string(99)
+
+
+def geom(**kw):
+    base = dict(batch=2, rows_per_req=1, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                index_dim=64, page_size=64, max_blocks=16, num_pages=32)
+    base.update(kw)
+    return qsa.make_geom(**base)
+
+
+FAKE = ctypes.c_void_p(256)   # never dereferenced: validation fails first
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(num_q_heads=7), 1), (dict(batch=0), 1), (dict(rows_per_req=0), 1),
+    (dict(max_blocks=0), 1), (dict(num_pages=0), 1), (dict(head_dim=64), 2),
+    (dict(index_dim=128), 2), (dict(page_size=32), 2), (dict(rows_per_req=9), 2),
+    (dict(num_q_heads=512, num_kv_heads=2), 2),
+])
+def test_geometry_validation(lib, bad, status):
+    g = geom(**bad)
+    st = lib.qsa_index_scores(ctypes.byref(g), FAKE, FAKE, FAKE, FAKE, FAKE, None)
+    assert st == status
+
+
+def test_null_pointers_rejected(lib):
+    g = geom()
+    assert lib.qsa_index_scores(ctypes.byref(g), None, FAKE, FAKE, FAKE, FAKE, None) == 1
+    assert lib.qsa_select_topk(ctypes.byref(g), FAKE, FAKE, 4, 1, None, FAKE, None) == 1
+    assert lib.qsa_index_scores(None, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 1
+
+
+@pytest.mark.parametrize("k,window,status", [(0, 0, 1), (4, -1, 1), (4, 5, 1), (2000, 2, 2)])
+def test_select_argument_validation(lib, k, window, status):
+    g = geom()
+    assert lib.qsa_select_topk(ctypes.byref(g), FAKE, FAKE, k, window, FAKE, FAKE, None) == status
+
+
+def test_unaligned_pool_rejected(lib):
+    g = geom()
+    odd = ctypes.c_void_p(257)
+    assert lib.qsa_index_scores(ctypes.byref(g), FAKE, odd, FAKE, FAKE, FAKE, None) == 1
+
+
+def test_workspace_sizes(lib):
+    g = geom(rows_per_req=4)
+    assert qsa.qsa_sparse_decode_workspace_bytes_ex(g, 8, 1) > 0
+    one = qsa.qsa_sparse_decode_workspace_bytes_ex(g, 8, 1)
+    four = qsa.qsa_sparse_decode_workspace_bytes_ex(g, 8, 4)
+    assert four > one
+    assert qsa.qsa_sparse_decode_workspace_bytes_ex(g, 0, 1) == 0          # k < 1
+    assert qsa.qsa_sparse_decode_workspace_bytes_ex(geom(rows_per_req=8), 512, 1) == 0
+
+
+def test_decode_rejects_small_workspace(lib):
+    g = geom()
+    need = qsa.qsa_sparse_decode_workspace_bytes_ex(g, 8, 4)
+    args = [ctypes.byref(g)] + [FAKE] * 5 + [1.0, 1.0, 0.1] + [FAKE] * 3 + [8] + [FAKE] * 2
+    st = lib.qsa_sparse_decode_ex(*args, FAKE, need - 1, 4, None)
+    assert st == 4
+    st = lib.qsa_sparse_decode_ex(*args, None, need, 4, None)
+    assert st == 4
+
+
+def test_no_cpu_fallback_without_library(monkeypatch, tmp_path):
+    # The binding refuses to run when the library is absent instead of
+    # computing anything on the host.
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding._build, "LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        binding.load()
