@@ -1,0 +1,496 @@
+"""Benchmark: QSA block-sparse GQA decode step (index scores -> canonical top-k
+-> split-KV sparse decode over NVFP4 pages) on one GB300, as query rows/s and
+achieved HBM bandwidth.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl qsa|reference]
+
+Prints one JSON line (rank 0).  A step is one pass of all three kernels over
+one batch of synthetic, seeded input (the "batched decode" workload by
+default).  Steps rotate over input replicas held in distinct HBM buffers whose
+touched bytes add up to at least 4x the L2 size, so every step reads HBM.
+Timing: CUDA graph replays bracketed by CUDA events on the launching stream,
+with a barrier and synchronize on both sides; per-kernel durations come from
+event-record nodes around each kernel in a second, separately timed pass.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import qsa_workloads as qw  # noqa: E402
+
+METRIC = "sparse decode query-rows/s per GPU; achieved HBM GB/s vs GB300 peak"
+L2_BYTES_DEFAULT = 129 * 1024 * 1024
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def workload_label(case: qw.Case) -> str:
+    ctx = (str(case.ctx_lo) if case.ctx_lo == case.ctx_hi
+           else "U[%d,%d]" % (case.ctx_lo, case.ctx_hi))
+    s = ("%s (seed %d): %d requests x %d rows, %d q heads / %d KV heads, head_dim %d, "
+         "context %s tokens, %d-token NVFP4 pages, k=%d blocks incl. %d-block window"
+         % (case.name, case.seed, case.batch, case.rows_per_req, case.num_q_heads,
+            case.num_kv_heads, case.head_dim, ctx, case.page_size, case.k, case.window))
+    if case.invalid_frac:
+        s += ", %g%% invalid page entries" % (100 * case.invalid_frac)
+    if case.tie_frac:
+        s += ", %g%% duplicated index-key blocks" % (100 * case.tie_frac)
+    return s
+
+
+def algorithmic_bytes(w: dict, sel: np.ndarray) -> dict:
+    """Bytes the method must move per step (per kernel), from the inputs and
+    the step's selection: index keys of every visible valid token, NVFP4 K/V
+    + scales of every selected token per KV head (union over a request's
+    rows), q, iq, out, lse and the page-table entries read."""
+    B, R, P, MB = w["batch"], w["rows_per_req"], w["page_size"], w["max_blocks"]
+    Hq, Hkv, D, Di = w["num_q_heads"], w["num_kv_heads"], w["head_dim"], w["index_dim"]
+    pt = w["page_table_np"]
+    sl = w["seqlens_np"]
+    T = B * R
+    key_tokens = 0
+    page_tokens = 0
+    union_entries = 0
+    for b in range(B):
+        n_last = max(0, min(int(sl[b]), MB * P))          # row R-1 sees L tokens
+        nb = -(-n_last // P)
+        for beta in range(nb):
+            if pt[b, beta] >= 0:
+                key_tokens += min(P, n_last - beta * P)
+        u = set()
+        for j in range(R):
+            u.update(int(x) for x in sel[b * R + j] if x >= 0)
+        union_entries += len(u)
+        for beta in u:
+            page_tokens += min(P, n_last - beta * P)
+    idx = key_tokens * Di + T * Hq * Di + B * MB * 4 + B * 4
+    dec = page_tokens * Hkv * (D // 2 + D // 16) * 2 + 2 * T * Hq * D * 2 + T * Hq * 4 \
+        + union_entries * 4
+    return dict(index_scores=idx, select_topk=0, sparse_decode=dec, step=idx + dec,
+                key_bytes=key_tokens * Di, page_bytes=page_tokens * Hkv * (D // 2 + D // 16) * 2,
+                touched=idx + dec + T * MB * 4 * 2 + T * w["k"] * 4 * 2)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_record(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = os.path.join(ROOT, "nvfp4_block_sparse_gb300", "csrc", kernel + ".cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] if os.path.exists(src) else ""
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            parts = line.split("|")
+            if len(parts) >= 4 and parts[0].strip() == kernel and parts[1].strip() == workload:
+                if parts[3].strip() == sha:
+                    return float(parts[2])
+    return None
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle, timed on host cores
+# ---------------------------------------------------------------------------
+
+def time_oracle(case: qw.Case, w_np: dict, budget_s: float = 10.0, nreq=None):
+    """Times the oracle's whole path (index scores, selection, attention) on
+    the first requests of the workload: as many as fit in ``budget_s`` (at
+    least one), unless ``nreq`` fixes the count."""
+    import oracle
+    oracle.build()
+    R = case.rows_per_req
+    if nreq is None:
+        t0 = time.perf_counter()
+        oracle.step(w_np, rows=(0, R))
+        t1 = time.perf_counter() - t0
+        nreq = int(max(1, min(case.batch, math.floor(budget_s / max(t1, 1e-6)))))
+    t0 = time.perf_counter()
+    oracle.step(w_np, rows=(0, nreq * R))
+    t = time.perf_counter() - t0
+    rows = nreq * R
+    return dict(value=rows / t, unit="rows/s", cores=oracle.num_threads(), kind="oracle",
+                sample="%d of %d requests (%d query rows) of the workload per step, whole "
+                "path (index scores, selection, attention), fp64 C + OpenMP"
+                % (nreq, case.batch, rows), seconds=t, nreq=nreq)
+
+
+def run_reference(args, case):
+    """The reference arm: the CPU oracle as it stands, on this host's cores,
+    on the GPU arm's workload, metric and unit.  Each step is a bounded sample
+    (whole requests) sized so warm-up + steps fit in about three minutes."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = qw.make_workload(case, "cpu")
+    w_np = qw.to_numpy(w)
+    total_budget = 150.0
+    probe = time_oracle(case, w_np, nreq=1)
+    per_step = total_budget / (args.steps + args.warmup)
+    nreq = int(max(1, min(case.batch, math.floor(per_step / max(probe["seconds"], 1e-6)))))
+    for _ in range(args.warmup):
+        if probe["seconds"] * nreq * args.warmup > 30.0:
+            break
+        time_oracle(case, w_np, nreq=nreq)
+    steps, spent = [], 0.0
+    for _ in range(args.steps):
+        r = time_oracle(case, w_np, nreq=nreq)
+        steps.append(r)
+        spent += r["seconds"]
+        if spent > total_budget:
+            break
+    tot_rows = sum(r["nreq"] * case.rows_per_req for r in steps)
+    tot_t = sum(r["seconds"] for r in steps)
+    v = tot_rows / tot_t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "rows/s",
+        "n_gpus": args.gpus, "steps": len(steps), "steps_requested": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1000.0 * tot_t / len(steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": workload_label(case), "config_index": args.config,
+                   "query_rows_per_step": nreq * case.rows_per_req},
+        "cpu_baseline": {"value": v, "unit": "rows/s", "cores": steps[0]["cores"],
+                         "kind": "oracle", "sample": steps[0]["sample"]},
+        "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def make_events(n):
+    try:
+        return [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n)]
+    except TypeError:
+        return None
+
+
+def run_qsa(args, case):
+    import nvfp4_block_sparse_gb300 as qsa
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    qsa.load()
+
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or L2_BYTES_DEFAULT)
+    peak_gbs, peak_kind = measured_peaks()
+
+    # Replica 0 carries the workload's own seed; others shift it (and the rank).
+    def replica(i):
+        seed = case.seed + 7919 * i + 104729 * rank
+        w = qw.make_workload(case, dev, seed=seed)
+        w["page_table_np"] = w["page_table"].cpu().numpy()
+        w["seqlens_np"] = w["seqlens"].cpu().numpy()
+        return w
+
+    w0 = replica(0)
+    step = qsa.DecodeStep(qw.geometry(w0), case.k, case.window, device=dev)
+    step.run(w0)
+    torch.cuda.synchronize()
+    by0 = algorithmic_bytes(w0, step.sel.cpu().numpy())
+    nrep = int(min(64, max(2, math.ceil(4 * l2 / max(1, by0["touched"])))))
+    reps = [w0] + [replica(i) for i in range(1, nrep)]
+    sels = []
+    for w in reps:
+        step.run(w)
+        torch.cuda.synchronize()
+        sels.append(step.sel.cpu().numpy())
+    bys = [algorithmic_bytes(w, s) for w, s in zip(reps, sels)]
+    mean = {k: float(np.mean([b[k] for b in bys])) for k in bys[0]}
+    T = case.rows
+
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))
+
+    # Warm-up (eager), then capture one graph over every replica in turn.
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step.run(reps[i % nrep], stream=stream)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for w in reps:
+                step.run(w, stream=stream)
+        rem = args.steps % nrep
+        graph_rem = None
+        if rem:
+            graph_rem = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph_rem, stream=stream):
+                for w in reps[:rem]:
+                    step.run(w, stream=stream)
+        for _ in range(2):
+            graph.replay()
+        stream.synchronize()
+
+    # ---- timed region -----------------------------------------------------
+    full, rem = divmod(args.steps, nrep)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(full):
+                graph.replay()
+            if rem:
+                graph_rem.replay()
+            ev1.record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    clocks = clk.summary()
+    ms_step = ms / args.steps
+    rows_s = world * T * args.steps / (ms / 1000.0)
+    step_gbs = mean["step"] / (ms_step / 1000.0) / 1e9
+
+    # ---- per-kernel durations: event nodes around each kernel ---------------
+    kern_ms = {}
+    evs = make_events(6 * nrep)
+    if evs is not None:
+        kg = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(kg, stream=stream):
+                for i, w in enumerate(reps):
+                    e = evs[6 * i: 6 * i + 6]
+                    e[0].record(stream)
+                    qsa.qsa_index_scores(step.cg, w["iq"], w["ik_pool"], w["page_table"],
+                                         w["seqlens"], step.scores, stream)
+                    e[1].record(stream)
+                    e[2].record(stream)
+                    qsa.qsa_select_topk(step.cg, step.scores, w["seqlens"], step.k, step.window,
+                                        step.sel, step.nsel, stream)
+                    e[3].record(stream)
+                    e[4].record(stream)
+                    qsa.qsa_sparse_decode_ex(step.cg, w["q"], w["k_pool"], w["k_sf"],
+                                             w["v_pool"], w["v_sf"], w["k_scale"],
+                                             w["v_scale"], w["sm_scale"], w["page_table"],
+                                             w["seqlens"], step.sel, step.k, step.out, step.lse,
+                                             step.workspace, step.num_splits, stream)
+                    e[5].record(stream)
+            acc = {"index_scores": [], "select_topk": [], "sparse_decode": []}
+            for _ in range(5):
+                kg.replay()
+                stream.synchronize()
+                for i in range(nrep):
+                    e = evs[6 * i: 6 * i + 6]
+                    acc["index_scores"].append(e[0].elapsed_time(e[1]))
+                    acc["select_topk"].append(e[2].elapsed_time(e[3]))
+                    acc["sparse_decode"].append(e[4].elapsed_time(e[5]))
+        kern_ms = {k: float(np.mean(v)) for k, v in acc.items()}
+
+    # ---- end to end through host buffers ----------------------------------
+    e2e = run_e2e(qsa, step, reps, stream, args, dev, T, world)
+
+    # ---- CPU baseline (rank 0, N = 1 only) -----------------------------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        w_np = qw.to_numpy({k: v for k, v in w0.items() if not k.endswith("_np")})
+        cpu = time_oracle(case, w_np)
+        cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+
+    if rank != 0:
+        return
+    kernels = {}
+    for name, t in kern_ms.items():
+        b = mean[name]
+        kernels[name] = {"ms": t, "bytes": b,
+                         "gbs": (b / (t / 1000.0) / 1e9) if (t > 0 and b > 0) else None}
+    dom = max(kern_ms, key=kern_ms.get) if kern_ms else "sparse_decode"
+    dom_t = kern_ms.get(dom)
+    achieved = (mean[dom] / (dom_t / 1000.0) / 1e9) if dom_t else None
+    wl = "cfg%d" % args.config
+    traffic = traffic_record("qsa_" + dom, wl)
+    line = {
+        "metric": METRIC, "value": rows_s, "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "nvfp4 KV (e2m1+e4m3), bf16 q/out, int8 index, fp32 accumulate",
+        "data": "synthetic",
+        "config": {"workload": workload_label(case), "config_index": args.config,
+                   "query_rows_per_step": T, "replicas": nrep,
+                   "l2_defeat": "inputs rotate over %d HBM replicas; touched bytes per cycle "
+                   "%.0f MB >= 4x L2 (%d MB)" % (nrep, nrep * mean["touched"] / 1e6, l2 >> 20),
+                   "timing": "CUDA graph replay of %d steps, CUDA events on the launching "
+                   "stream" % nrep},
+        "step_hbm": {"bytes": mean["step"], "achieved_gbs": step_gbs, "peak_gbs": peak_gbs,
+                     "frac": step_gbs / peak_gbs, "peak_kind": peak_kind},
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak_gbs,
+                     "unit": "GB/s", "frac": (achieved / peak_gbs) if achieved else None,
+                     "traffic": traffic, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": mean[dom]},
+        "kernels": kernels,
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(qsa, step, reps, stream, args, dev, T, world):
+    """Same metric through the public API with HOST buffers: each step copies
+    its query-side inputs (q, iq, page table, seqlens) from pinned host memory
+    to the device, runs the three calls, and reads out + lse back.  The NVFP4
+    K/V pages and index keys are the cache: resident in HBM."""
+    keys = ("q", "iq", "page_table", "seqlens")
+    host = [{k: w[k].cpu().pin_memory() for k in keys} for w in reps]
+    out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    lse_h = torch.empty(step.lse.shape, dtype=step.lse.dtype).pin_memory()
+    h2d = sum(host[0][k].numel() * host[0][k].element_size() for k in keys)
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    n = max(1, min(args.steps, 2000))
+    nrep = len(reps)
+
+    def one(i):
+        w = reps[i % nrep]
+        hs = host[i % nrep]
+        for k in keys:
+            w[k].copy_(hs[k], non_blocking=True)
+        step.run(w, stream=stream)
+        out_h.copy_(step.out, non_blocking=True)
+        lse_h.copy_(step.lse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(min(args.warmup, 8)):
+            one(i)
+        stream.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            one(i)
+        e1.record(stream)
+        stream.synchronize()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": world * T * n / (ms / 1000.0), "unit": "rows/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--impl", default="qsa", choices=["qsa", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    case = qw.CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, case)
+        return
+    run_qsa(args, case)
+
+
+if __name__ == "__main__":
+    main()
