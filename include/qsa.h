@@ -196,6 +196,37 @@ qsa_status_t qsa_sparse_decode_ex(const qsa_geom_t *geom, const void *q_bf16,
                                   int num_splits, cudaStream_t stream);
 
 /*
+ * qsa_sparse_decode for callers that cannot allocate device memory (no
+ * counterpart in the method's description: it exists for deployment).  Some
+ * callers never get to call cudaMalloc -- an allocator-free runtime, a memory
+ * pool that must not grow once serving starts, a plugin that is only handed
+ * input and output pointers -- so they have no workspace to pass.  This call
+ * takes the same inputs and outputs as qsa_sparse_decode minus the workspace
+ * and uses a 4 MiB scratch array built into the library instead; it allocates
+ * and frees nothing.
+ *
+ *  - The array lives on every GPU that loads the library, until the process
+ *    exits, and all calls on a GPU share it: calls that overlap on the GPU
+ *    (different streams or host threads) race and must be serialised by the
+ *    caller.  Each call clears the part that must start at zero.
+ *  - The first call on a device looks up the array's device address; make
+ *    that first call before capturing any stream into a CUDA graph.
+ *  - The KV split count is lowered until the split partials fit the array;
+ *    when even one split does not fit (more than about a million
+ *    (request, KV head, column group) units), the call returns
+ *    QSA_ERR_WORKSPACE without launching.
+ *  - Other arguments are validated as in qsa_sparse_decode.
+ */
+qsa_status_t qsa_sparse_decode_noalloc(const qsa_geom_t *geom, const void *q_bf16,
+                                       const uint8_t *k_pool, const uint8_t *k_sf,
+                                       const uint8_t *v_pool, const uint8_t *v_sf,
+                                       float k_scale, float v_scale, float sm_scale,
+                                       const int32_t *page_table,
+                                       const int32_t *seqlens, const int32_t *sel,
+                                       int k, void *out_bf16, float *lse,
+                                       cudaStream_t stream);
+
+/*
  * Reads the workspace's device status word (synchronising `stream`): 0 when
  * every bounded wait since qsa_workspace_init() completed, otherwise a
  * nonzero code and QSA_ERR_DEVICE_TIMEOUT is returned.  Diagnostic only.

@@ -30,6 +30,7 @@ EXPORTS = (
     "qsa_workspace_init",
     "qsa_sparse_decode",
     "qsa_sparse_decode_ex",
+    "qsa_sparse_decode_noalloc",
     "qsa_workspace_status",
 )
 
@@ -86,6 +87,10 @@ def load(build_if_missing: bool = False):
     lib.qsa_sparse_decode.argtypes = dec + [_vp]
     lib.qsa_sparse_decode_ex.restype = st
     lib.qsa_sparse_decode_ex.argtypes = dec + [ctypes.c_int, _vp]
+    lib.qsa_sparse_decode_noalloc.restype = st
+    lib.qsa_sparse_decode_noalloc.argtypes = [G, _vp, _vp, _vp, _vp, _vp, ctypes.c_float,
+                                              ctypes.c_float, ctypes.c_float, _vp, _vp, _vp,
+                                              ctypes.c_int, _vp, _vp, _vp]
     lib.qsa_workspace_status.restype = st
     lib.qsa_workspace_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int), _vp]
     _lib = lib
@@ -183,6 +188,21 @@ def qsa_sparse_decode_ex(geom, q, k_pool, k_sf, v_pool, v_sf, k_scale, v_scale, 
                             page_table, seqlens, sel, k, out, lse, workspace)
     _check("qsa_sparse_decode_ex",
            load().qsa_sparse_decode_ex(*args, int(num_splits), _stream(stream)))
+
+
+def qsa_sparse_decode_noalloc(geom, q, k_pool, k_sf, v_pool, v_sf, k_scale, v_scale, sm_scale,
+                              page_table, seqlens, sel, k, out, lse, stream=None):
+    """qsa_sparse_decode without a workspace, for callers that cannot
+    allocate device memory: the library's built-in scratch array is used
+    instead (shared by every call on the device, so overlapping calls race)."""
+    g = _geom(geom)
+    _check("qsa_sparse_decode_noalloc", load().qsa_sparse_decode_noalloc(
+        ctypes.byref(g), _ptr(q, torch.bfloat16, "q"), _ptr(k_pool, torch.uint8, "k_pool"),
+        _ptr(k_sf, torch.uint8, "k_sf"), _ptr(v_pool, torch.uint8, "v_pool"),
+        _ptr(v_sf, torch.uint8, "v_sf"), float(k_scale), float(v_scale), float(sm_scale),
+        _ptr(page_table, torch.int32, "page_table"), _ptr(seqlens, torch.int32, "seqlens"),
+        _ptr(sel, torch.int32, "sel"), int(k), _ptr(out, torch.bfloat16, "out"),
+        _ptr(lse, torch.float32, "lse"), _stream(stream)))
 
 
 def qsa_workspace_status(workspace, stream=None) -> int:
