@@ -392,6 +392,11 @@ def run_qsa(args, case):
 
     if rank != 0:
         return
+    # Every bounded wait in the timed steps must have succeeded.
+    wst = qsa.qsa_workspace_status(step.workspace)
+    if wst != 0:
+        raise RuntimeError("sparse decode reported status %d (%s) during the bench"
+                           % (wst, qsa.qsa_status_string(wst)))
     kernels = {}
     for name, t in kern_ms.items():
         b = mean[name]

@@ -37,8 +37,9 @@ __device__ __forceinline__ int4 ld_stream_v4(const int4* p) {
   return v;
 }
 
-// RB: compile-time bound on rows per request (R <= RB).
-template <int P, int RB>
+// RB: compile-time bound on rows per request (R <= RB).  PIPE: a warp owns
+// several blocks and loads the next block's keys while scoring the current.
+template <int P, int RB, bool PIPE>
 __global__ void __launch_bounds__(kThreads)
 index_scores_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __restrict__ ik_pool,
                     const int32_t* __restrict__ page_table, const int32_t* __restrict__ seqlens,
@@ -53,6 +54,32 @@ index_scores_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __restr
 
   pdl_wait();
 
+  const int L = seqlens[b];
+  const int cap = g.MB * P;
+  const int nmax = visible_tokens(L, R, R - 1, cap);
+
+  // Block `it` of this warp: page id and whether it has a visible token.
+  auto block_of = [&](int it, int& beta, int& page) -> bool {
+    beta = (blockIdx.x * blocks_per_warp + it) * kWarps + warp;
+    page = -1;
+    if (beta >= g.MB) return false;
+    page = page_table[(size_t)b * g.MB + beta];
+    return page >= 0 && page < g.NP && beta * P < nmax;
+  };
+  // Lane (token group lane>>2, part lane&3) loads 16 B of 8 tokens per step.
+  auto load_keys = [&](int page, int4 (&kv)[P / 8]) {
+    const int4* src = reinterpret_cast<const int4*>(ik_pool + (size_t)page * P * kIndexDim) + lane;
+#pragma unroll
+    for (int i = 0; i < P / 8; ++i) kv[i] = ld_stream_v4(src + 32 * i);
+  };
+
+  // The first block's keys are requested before the query head sums, so the
+  // two latencies overlap.
+  int beta0, page0;
+  bool live0 = block_of(0, beta0, page0);
+  int4 kv[P / 8];
+  if (live0) load_keys(page0, kv);
+
   // Head sums of the request's index queries: w[j][d] = sum_h iq[b*R+j][h][d].
   for (int idx = threadIdx.x; idx < 4 * RB * kIndexDim; idx += kThreads) {
     const int hg = idx / (RB * kIndexDim);
@@ -61,7 +88,16 @@ index_scores_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __restr
     int s = 0;
     if (j < R) {
       const int8_t* src = iq + ((size_t)(b * R + j) * g.Hq) * kIndexDim + d;
-      for (int h = hg; h < g.Hq; h += 4) s += src[(size_t)h * kIndexDim];
+      int h = hg;
+      // Batches of eight independent loads keep several L2 requests in flight.
+      for (; h + 28 < g.Hq; h += 32) {
+        int v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = src[(size_t)(h + 4 * u) * kIndexDim];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) s += v[u];
+      }
+      for (; h < g.Hq; h += 4) s += src[(size_t)h * kIndexDim];
     }
     wpart[hg][j][d] = s;
   }
@@ -79,7 +115,7 @@ index_scores_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __restr
   __syncthreads();
   pdl_trigger();
 
-  // Lane (token group lane>>2, part lane&3) covers dims [16*part, 16*part+16).
+  // Lane part covers dims [16*part, 16*part+16).
   const int part = lane & 3;
   uint32_t wr[RB][8];
 #pragma unroll
@@ -87,76 +123,93 @@ index_scores_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __restr
 #pragma unroll
     for (int q = 0; q < 8; ++q) wr[j][q] = wpack[j][8 * part + q];
 
-  const int L = seqlens[b];
-  const int cap = g.MB * P;
   int nrow[RB];
 #pragma unroll
   for (int j = 0; j < RB; ++j) nrow[j] = (j < R) ? visible_tokens(L, R, j, cap) : 0;
-  const int nmax = visible_tokens(L, R, R - 1, cap);
 
+  int beta = beta0, page = page0;
+  bool live = live0;
   for (int it = 0; it < blocks_per_warp; ++it) {
-    const int beta = (blockIdx.x * blocks_per_warp + it) * kWarps + warp;
     if (beta >= g.MB) break;
-    const int page = page_table[(size_t)b * g.MB + beta];
-    const bool live = page >= 0 && page < g.NP && beta * P < nmax;
+    // Next block's keys go out before this block is scored.
+    int beta_n = g.MB, page_n = -1;
+    bool live_n = false;
+    int4 kv_n[PIPE ? P / 8 : 1];
+    if constexpr (PIPE) {
+      if (it + 1 < blocks_per_warp) {
+        live_n = block_of(it + 1, beta_n, page_n);
+        if (live_n) load_keys(page_n, kv_n);
+      }
+    } else if (it + 1 < blocks_per_warp) {
+      live_n = block_of(it + 1, beta_n, page_n);
+    }
     int32_t* dst = scores + (size_t)b * R * g.MB + beta;
     if (!live) {
       if (lane < R) dst[(size_t)lane * g.MB] = kSentinel;
-      continue;
-    }
-    const int4* src = reinterpret_cast<const int4*>(ik_pool + (size_t)page * P * kIndexDim) + lane;
-    int4 kv[P / 8];
+    } else {
+      int best[RB];
 #pragma unroll
-    for (int i = 0; i < P / 8; ++i) kv[i] = ld_stream_v4(src + 32 * i);
-
-    int best[RB];
+      for (int j = 0; j < RB; ++j) best[j] = kSentinel;
 #pragma unroll
-    for (int j = 0; j < RB; ++j) best[j] = kSentinel;
+      for (int i = 0; i < P / 8; ++i) {
+        const int t_abs = beta * P + 8 * i + (lane >> 2);
+        const int words[4] = {kv[i].x, kv[i].y, kv[i].z, kv[i].w};
 #pragma unroll
-    for (int i = 0; i < P / 8; ++i) {
-      const int t_abs = beta * P + 8 * i + (lane >> 2);
-      const int words[4] = {kv[i].x, kv[i].y, kv[i].z, kv[i].w};
+        for (int j = 0; j < RB; ++j) {
+          if (j < R) {
+            int acc = 0;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              acc = __dp2a_lo((int)wr[j][2 * m], words[m], acc);
+              acc = __dp2a_hi((int)wr[j][2 * m + 1], words[m], acc);
+            }
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            if (t_abs < nrow[j]) best[j] = max(best[j], acc);
+          }
+        }
+      }
 #pragma unroll
       for (int j = 0; j < RB; ++j) {
         if (j < R) {
-          int acc = 0;
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            acc = __dp2a_lo((int)wr[j][2 * m], words[m], acc);
-            acc = __dp2a_hi((int)wr[j][2 * m + 1], words[m], acc);
-          }
-          acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-          acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-          if (t_abs < nrow[j]) best[j] = max(best[j], acc);
+          int v = best[j];
+          v = max(v, __shfl_xor_sync(0xffffffffu, v, 4));
+          v = max(v, __shfl_xor_sync(0xffffffffu, v, 8));
+          v = max(v, __shfl_xor_sync(0xffffffffu, v, 16));
+          if (lane == j) dst[(size_t)j * g.MB] = (beta * P < nrow[j]) ? v : kSentinel;
         }
       }
     }
+    beta = beta_n;
+    page = page_n;
+    live = live_n;
+    if constexpr (PIPE) {
 #pragma unroll
-    for (int j = 0; j < RB; ++j) {
-      if (j < R) {
-        int v = best[j];
-        v = max(v, __shfl_xor_sync(0xffffffffu, v, 4));
-        v = max(v, __shfl_xor_sync(0xffffffffu, v, 8));
-        v = max(v, __shfl_xor_sync(0xffffffffu, v, 16));
-        if (lane == j) dst[(size_t)j * g.MB] = (beta * P < nrow[j]) ? v : kSentinel;
-      }
+      for (int i = 0; i < P / 8; ++i) kv[i] = kv_n[i];
+    } else {
+      if (live) load_keys(page, kv);
     }
   }
+  (void)page;
 }
 
-template <int P, int RB>
-cudaError_t launch_t(const Geom& g, const int8_t* iq, const int8_t* ik_pool,
-                     const int32_t* page_table, const int32_t* seqlens, int32_t* scores,
-                     bool pdl, cudaStream_t stream) {
+// Blocks each warp scores: one, unless the grid would exceed about four
+// resident CTAs per SM.
+int blocks_per_warp_for(const Geom& g) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  // Enough warps in flight to cover HBM latency; more blocks per warp only
-  // when the grid would exceed ~4 resident CTAs per SM.
   const long long warps_needed = (long long)g.B * g.MB;
   const long long warp_slots = (long long)sms * 4 * kWarps;
   int bpw = (int)((warps_needed + warp_slots - 1) / warp_slots);
-  bpw = bpw < 1 ? 1 : (bpw > 4 ? 4 : bpw);
+  return bpw < 1 ? 1 : (bpw > 4 ? 4 : bpw);
+}
+
+template <int P, int RB, bool PIPE>
+cudaError_t launch_t(const Geom& g, const int8_t* iq, const int8_t* ik_pool,
+                     const int32_t* page_table, const int32_t* seqlens, int32_t* scores,
+                     bool pdl, cudaStream_t stream) {
+  const int bpw = blocks_per_warp_for(g);
   dim3 grid((g.MB + kWarps * bpw - 1) / (kWarps * bpw), g.B);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -168,18 +221,27 @@ cudaError_t launch_t(const Geom& g, const int8_t* iq, const int8_t* ik_pool,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, index_scores_kernel<P, RB>, g, iq, ik_pool, page_table,
+  return cudaLaunchKernelEx(&cfg, index_scores_kernel<P, RB, PIPE>, g, iq, ik_pool, page_table,
                             seqlens, scores, bpw);
+}
+
+template <int P, int RB>
+cudaError_t launch_rb(const Geom& g, const int8_t* iq, const int8_t* ik_pool,
+                      const int32_t* page_table, const int32_t* seqlens, int32_t* scores,
+                      bool pdl, cudaStream_t stream) {
+  if (blocks_per_warp_for(g) > 1)
+    return launch_t<P, RB, true>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
+  return launch_t<P, RB, false>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
 }
 
 template <int P>
 cudaError_t launch_p(const Geom& g, const int8_t* iq, const int8_t* ik_pool,
                      const int32_t* page_table, const int32_t* seqlens, int32_t* scores,
                      bool pdl, cudaStream_t stream) {
-  if (g.R <= 1) return launch_t<P, 1>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
-  if (g.R <= 2) return launch_t<P, 2>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
-  if (g.R <= 4) return launch_t<P, 4>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
-  return launch_t<P, 8>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
+  if (g.R <= 1) return launch_rb<P, 1>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
+  if (g.R <= 2) return launch_rb<P, 2>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
+  if (g.R <= 4) return launch_rb<P, 4>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
+  return launch_rb<P, 8>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
 }
 
 }  // namespace

@@ -8,16 +8,22 @@
 // invalid-page handling and masking.  PR #20276 ("Qwen3.8-Flash-Next NVFP4
 // target"), Features table: uint8 e2m1 pages + e4m3 block scales.
 //
-// One CTA = (request b, KV head g, query-column group, KV split s).  Its
-// query columns are the G*R query vectors (row j, head g*G + hh) of the
-// request that read KV head g, so every page is read once per KV head for all
-// of them.  The pages are the union of the rows' selections (each page carries
-// a mask of the rows that selected it); the split takes a contiguous share of
-// that union's 64-token chunks.
+// One CTA = (request b, KV head g, head slice, KV split s).  Its query columns
+// are the (row j, head) pairs of the request's R rows for a slice of up to
+// 8*NTR of the G query heads that read KV head g.  The pages it reads are the
+// union of the rows' selections (each page carries a mask of the rows that
+// selected it), so each page is read from HBM once per KV head; the split
+// takes a contiguous share of that union's 64-token chunks.
 //
-// Per chunk (K 4 KB + K scales 512 B + V 4 KB + V scales 512 B, contiguous in
-// the pools) a TMA bulk copy lands it in shared memory; the consuming warps
-// dequantise straight into mma.sync fragments:
+// Warp roles.  A producer warp streams the chunks (K 4 KB + K scales 512 B +
+// V 4 KB + V scales 512 B, contiguous in the pools) into shared-memory stages
+// with TMA bulk copies and full/empty mbarriers.  Each consumer warp owns one
+// row's columns and processes a chunk completely and alone: with one row
+// (decode) the consumers take chunks round-robin; with R rows (verify) there
+// is one consumer per row and it processes exactly the chunks its row
+// selected.  No warp waits on another inside a chunk.
+//
+// Per chunk the consumer dequantises straight into mma.sync fragments:
 //   S^T = K . Q^T     A = K tile (tokens x dims) from e2m1 bytes * e4m3 scale,
 //                     B = Q^T (fp16, pre-scaled by a power of two per column)
 //   O^T += V^T . P^T  A = V^T tile (dims x tokens) built from two tokens'
@@ -28,22 +34,22 @@
 // and shared-memory wavefronts stay conflict-free; the contraction is
 // invariant under those permutations and the output un-permutes them.
 //
-// A team of TEAM warps shares each chunk: QK is split by 16-token tiles and
-// PV by 16-dim tiles, the chunk max and P fragments are exchanged through
-// shared memory, so no element is dequantised twice and each warp keeps only
-// its share of the accumulators.  Query-column tiles whose rows did not select
-// the chunk's page are skipped (verify rows mostly select different pages).
+// Every wait is bounded: a wait that gives up records a status word in the
+// workspace and the kernel still finishes.
 #include "qsa_common.cuh"
 
+#include <cooperative_groups.h>
 #include <math.h>
+
+#include <mutex>
+#include <vector>
+
+namespace cg = cooperative_groups;
 
 namespace qsa {
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kWarps = kThreads / 32;
 constexpr int kChunk = 64;                   // tokens per pipeline stage
-constexpr int kMaxCols = 32;                 // query columns per CTA
 constexpr int kKBytes = kChunk * kHeadDim / 2;     // 4096
 constexpr int kSfBytes = kChunk * kHeadDim / 16;   // 512
 constexpr int kStageBytes = 2 * kKBytes + 2 * kSfBytes;  // 9216
@@ -51,13 +57,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per bounded wait
 constexpr int kPartStride = 4 + kHeadDim;    // m, l, pad, pad, O[128] per column
-
-#ifndef QSA_DECODE_TEAM_NT1
-#define QSA_DECODE_TEAM_NT1 4
-#endif
-#ifndef QSA_DECODE_STAGES_NT1
-#define QSA_DECODE_STAGES_NT1 4
-#endif
+constexpr int kMaxCluster = 8;               // portable cluster size
+constexpr int kPtRowMax = 4096;              // page-table rows up to this stay in smem
 
 struct Params {
   Geom g;
@@ -74,9 +75,11 @@ struct Params {
   __nv_bfloat16* out;
   float* lse;
   int* status;          // workspace status word
-  int* tickets;         // [B * Hkv * QG]
-  float* partials;      // [B * Hkv * QG][S][kMaxCols][kPartStride]
-  int splits, qgroups, cols;
+  int* tickets;         // [units]
+  float* partials;      // [units][splits][R * 8 * NTR][kPartStride]
+  int splits;           // KV splits per unit
+  int slices;           // head slices per KV head
+  int cluster;          // 1: ticket merge through partials; >1: cluster (DSMEM) merge
 };
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
@@ -85,13 +88,17 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   return t;
 }
 
-__device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (globaltimer_ns() - t0 > kWaitNs) return false;
   }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // Four bytes of e2m1 pairs -> four fp16 pairs (byte i -> o[i], low nibble in
@@ -104,150 +111,172 @@ __device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&o)[4]) 
       : "r"(w));
 }
 
-__device__ __forceinline__ void named_bar(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-template <int TEAM>
-__device__ __forceinline__ void team_sync(int team) {
-  if constexpr (TEAM == 1) {
-    __syncwarp();
-  } else if constexpr (TEAM == kWarps) {
-    __syncthreads();
-  } else {
-    named_bar(1 + team, TEAM * 32);
-  }
-}
-
 // Shared-memory layout (bytes), shared by host sizing and the kernel.
-template <int NT, int TEAM, int STAGES>
+template <int NTR, int W, int S>
 struct Layout {
-  static constexpr int kTeams = kWarps / TEAM;
-  static constexpr int kMtPerWarp = 4 / TEAM;
-  static constexpr int kStagesSz = kTeams * STAGES * kStageBytes;
-  // After the main loop the stage region holds the team partials, and in the
-  // merging CTA the split weights.
-  static constexpr int kCombineSz = kTeams * kMaxCols * kHeadDim * 4 + kTeams * kMaxCols * 4 +
-                                    kWarps * kMaxCols * 4;
-  static constexpr int kMergeSz = kMaxCols * 64 * 4 + kMaxCols * 8;
-  static constexpr int kRegion0 = kStagesSz > kCombineSz ? kStagesSz : kCombineSz;
-  static constexpr int kRegionSz = kRegion0 > kMergeSz ? kRegion0 : kMergeSz;
-  static constexpr int kBarOff = kRegionSz;
-  static constexpr int kBarSz = kTeams * STAGES * 8;
-  static constexpr int kQOff = kBarOff + kBarSz;                 // half [NT*8][128]
-  static constexpr int kQSz = NT * 8 * kHeadDim * 2;
-  static constexpr int kColOff = kQOff + kQSz;                   // cq, n, row bit, tile rows
-  static constexpr int kColSz = 3 * kMaxCols * 4 + 4 * 4;
-  static constexpr int kXmaxOff = kColOff + kColSz;              // [teams][TEAM][32] float
-  static constexpr int kXmaxSz = (TEAM > 1) ? kTeams * TEAM * kMaxCols * 4 : 0;
-  static constexpr int kXpSlots = kMtPerWarp * NT * 2;
-  static constexpr int kXpOff = kXmaxOff + kXmaxSz;              // [teams][TEAM][slots][32]
-  static constexpr int kXpSz = (TEAM > 1) ? kTeams * TEAM * kXpSlots * 32 * 4 : 0;
-  static constexpr int kMiscOff = kXpOff + kXpSz;
-  static constexpr int kMiscSz = 64 * 4;
-  static constexpr int kSelOff = kMiscOff + kMiscSz;             // sel rows, union, pages
-  static size_t bytes(int rows, int k) { return (size_t)kSelOff + (size_t)rows * k * 4 * 3; }
+  static constexpr int kHsp = 8 * NTR;                            // padded head slice
+  static constexpr int kStagesSz = S * kStageBytes;
+  // After the main loop the stage region holds the consumers' partials (co,
+  // cm, cl), the CTA partial (cp) and the cluster merge weights.
+  static constexpr int kCoSz = W * kHsp * kHeadDim * 4;
+  static constexpr int kCmSz = W * kHsp * 4;
+  static constexpr int kClSz = W * kHsp * 4;
+  static constexpr int kCpOff = kCoSz + kCmSz + kClSz;
+  __host__ __device__ static int cp_bytes(int R) { return R * kHsp * kPartStride * 4; }
+  __host__ __device__ static int region_bytes(int R, int splits) {
+    const int combine = kCpOff + cp_bytes(R) + R * kHsp * (kMaxCluster + 2) * 4;
+    const int merge = R * kHsp * (splits + 2) * 4;
+    int r = kStagesSz > combine ? kStagesSz : combine;
+    return r > merge ? r : merge;
+  }
+  static size_t bytes(int R, int k, int mb, int splits) {
+    size_t off = (size_t)region_bytes(R, splits);
+    off += 2 * S * 8;                                   // full + empty barriers
+    off += (size_t)R * kHsp * kHeadDim * 2;             // q (fp16)
+    off += (size_t)R * kHsp * 4 * 2;                    // cq, n per column
+    off += 64 * 4;                                      // scalars
+    off += (size_t)R * k * 4 * 3;                       // sel rows, union ids, pages
+    off += mb <= kPtRowMax ? (size_t)mb * 4 : 0;        // page-table row
+    return off;
+  }
 };
 
-template <int NT, int TEAM, int STAGES>
-__global__ void __launch_bounds__(kThreads)
-sparse_decode_kernel(Params p) {
-  using Lay = Layout<NT, TEAM, STAGES>;
-  constexpr int kTeams = Lay::kTeams;
-  constexpr int kMtPerWarp = 4 / TEAM;   // QK 16-token tiles per warp per chunk
-  constexpr int kDtPerWarp = 8 / TEAM;   // PV 16-dim tiles per warp
-  constexpr int kSlots = Lay::kXpSlots;
+// Register budget: about 136 per thread for 8-column rows with up to four
+// consumers (three CTAs per SM), unconstrained otherwise.
+template <int NTR, int W>
+constexpr int decode_min_blocks() { return NTR == 1 ? (W <= 4 ? 3 : 1) : 1; }
 
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* region = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
-  __half* qs = reinterpret_cast<__half*>(smem + Lay::kQOff);
-  float* col_cq = reinterpret_cast<float*>(smem + Lay::kColOff);
-  int* col_n = reinterpret_cast<int*>(smem + Lay::kColOff + kMaxCols * 4);
-  int* col_bit = reinterpret_cast<int*>(smem + Lay::kColOff + 2 * kMaxCols * 4);
-  int* tile_rows = reinterpret_cast<int*>(smem + Lay::kColOff + 3 * kMaxCols * 4);
-  float* xmax = reinterpret_cast<float*>(smem + Lay::kXmaxOff);
-  uint32_t* xp = reinterpret_cast<uint32_t*>(smem + Lay::kXpOff);
-  int* misc = reinterpret_cast<int*>(smem + Lay::kMiscOff);
-  int32_t* s_sel = reinterpret_cast<int32_t*>(smem + Lay::kSelOff);
+template <int NTR, int W, int S>
+__global__ void __launch_bounds__((W + 1) * 32, (decode_min_blocks<NTR, W>()))
+sparse_decode_kernel(Params p) {
+  using Lay = Layout<NTR, W, S>;
+  constexpr int kHsp = Lay::kHsp;
+  constexpr int kThreads = (W + 1) * 32;
 
   const Geom& g = p.g;
+  const int R = g.R;
+  const int G = g.Hq / g.Hkv;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
-  const int team = warp / TEAM, rank = warp % TEAM;
+  const bool producer = warp == W;
 
   const int s = blockIdx.x;
-  const int gq = blockIdx.y;
-  const int kvh = gq / p.qgroups, qg = gq % p.qgroups;
+  const int kvh = blockIdx.y / p.slices, slice = blockIdx.y % p.slices;
   const int b = blockIdx.z;
-  const int G = g.Hq / g.Hkv;
-  const int R = g.R;
-  const int c0 = qg * kMaxCols;
-  const int ncols = min(kMaxCols, p.cols - c0);
-  const int j_lo = c0 / G, j_hi = (c0 + ncols - 1) / G;
-  const int nrows = j_hi - j_lo + 1;
+  const int hs0 = slice * kHsp;                       // first head of the slice
+  const int hs = min(kHsp, G - hs0);                  // real heads in the slice
+  const int ncols = R * kHsp;                         // padded columns (j, hh)
   const int k = p.k;
-  int32_t* s_union = s_sel + nrows * k;
-  int32_t* s_upage = s_union + nrows * k;
 
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* region = smem;
+  size_t off = (size_t)Lay::region_bytes(R, p.splits);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + off);
+  uint64_t* empty = full + S;
+  off += 2 * S * 8;
+  __half* qs = reinterpret_cast<__half*>(smem + off);
+  off += (size_t)R * kHsp * kHeadDim * 2;
+  float* col_cq = reinterpret_cast<float*>(smem + off);
+  int* col_n = reinterpret_cast<int*>(col_cq + ncols);
+  off += (size_t)ncols * 4 * 2;
+  int* misc = reinterpret_cast<int*>(smem + off);
+  off += 64 * 4;
+  int32_t* s_sel = reinterpret_cast<int32_t*>(smem + off);
+  int32_t* s_union = s_sel + R * k;
+  int32_t* s_upage = s_union + R * k;
+  int32_t* s_pt = s_upage + R * k;
+
+  // Consumers per stage: decode (one row) gives each chunk to one consumer;
+  // verify gives every chunk to all row consumers (each skips what its row did
+  // not select) so that stage reuse waits for all of them.
+  const int empty_count = (R == 1) ? 1 : W;
   if (tid == 0) {
-    for (int i = 0; i < kTeams * STAGES; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], empty_count);
+    }
     fence_mbar_init();
   }
 
   pdl_wait();   // every global read below may depend on the preceding kernel
 
-  // ---- union of the rows' selections (first occurrence, valid pages) -------
-  for (int i = tid; i < nrows * k; i += kThreads) {
-    const int v = p.sel[(size_t)(b * R + j_lo + i / k) * k + (i % k)];
+  // ---- one round trip: selections, the request's page-table row, queries ---
+  const bool pt_in_smem = g.MB <= kPtRowMax;
+  for (int i = tid; i < R * k; i += kThreads) {
+    const int v = p.sel[(size_t)b * R * k + i];
     s_sel[i] = (v >= 0 && v < g.MB) ? v : -1;
   }
-  __syncthreads();
-  const int ne = nrows * k;
-  const int per = (ne + kThreads - 1) / kThreads;   // <= 16 (union bound 2048)
-  const int e_lo = min(ne, tid * per), e_hi = min(ne, e_lo + per);
-  // Each thread marks its entries: kept (first occurrence, valid page) with
-  // the mask of rows that selected the block.
-  int flags[16];
-  int keep_cnt = 0;
+  if (pt_in_smem)
+    for (int i = tid; i < g.MB; i += kThreads) s_pt[i] = p.page_table[(size_t)b * g.MB + i];
+  constexpr int kQPerWarp = (8 * kHsp + (W + 1) - 1) / (W + 1);   // columns per warp, R <= 8
+  float qv[kQPerWarp][4];
 #pragma unroll
-  for (int q = 0; q < 16; ++q) {
-    const int e = e_lo + q;
-    int flag = 0;
-    if (e < e_hi) {
-      const int beta = s_sel[e];
-      if (beta >= 0) {
-        const int jj = e / k;
-        bool first = true;
-        int mask = 1 << jj;
-        for (int j2 = 0; j2 < nrows; ++j2) {
-          if (j2 == jj) continue;
-          const int32_t* row = s_sel + j2 * k;
-          int lo2 = 0, hi2 = k;
-          while (lo2 < hi2) {
-            const int mid = (lo2 + hi2) >> 1;
-            const int x = row[mid] < 0 ? 0x7FFFFFFF : row[mid];
-            if (x < beta) lo2 = mid + 1; else hi2 = mid;
+  for (int ci = 0; ci < kQPerWarp; ++ci) {
+    const int c = warp + ci * (W + 1);
+    qv[ci][0] = qv[ci][1] = qv[ci][2] = qv[ci][3] = 0.f;
+    if (c < ncols) {
+      const int j = c / kHsp, hh = c % kHsp;
+      if (hh < hs) {
+        const int h = kvh * G + hs0 + hh;
+        const __nv_bfloat16* src = p.q + ((size_t)(b * R + j) * g.Hq + h) * kHeadDim + lane * 4;
+        const uint2 raw = *reinterpret_cast<const uint2*>(src);
+        const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+        const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+        qv[ci][0] = __low2float(lo); qv[ci][1] = __high2float(lo);
+        qv[ci][2] = __low2float(hi); qv[ci][3] = __high2float(hi);
+      }
+    }
+  }
+  const int L = p.seqlens[b];
+  __syncthreads();
+
+  // ---- union of the rows' selections (first occurrence, valid pages) -------
+  {
+    const int ne = R * k;
+    constexpr int kPer = (kMaxUnion + kThreads - 1) / kThreads;
+    const int per = (ne + kThreads - 1) / kThreads;   // <= kPer
+    const int e_lo = min(ne, tid * per), e_hi = min(ne, e_lo + per);
+    int flags[kPer];
+    int pages[kPer];
+    int keep_cnt = 0;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int e = e_lo + q;
+      int flag = 0;
+      pages[q] = 0;
+      if (e < e_hi) {
+        const int beta = s_sel[e];
+        if (beta >= 0) {
+          const int jj = e / k;
+          bool first = true;
+          int mask = 1 << jj;
+          for (int j2 = 0; j2 < R; ++j2) {
+            if (j2 == jj) continue;
+            const int32_t* row = s_sel + j2 * k;
+            int lo2 = 0, hi2 = k;
+            while (lo2 < hi2) {
+              const int mid = (lo2 + hi2) >> 1;
+              const int x = row[mid] < 0 ? 0x7FFFFFFF : row[mid];
+              if (x < beta) lo2 = mid + 1; else hi2 = mid;
+            }
+            if (lo2 < k && row[lo2] == beta) {
+              mask |= 1 << j2;
+              if (j2 < jj) first = false;
+            }
           }
-          if (lo2 < k && row[lo2] == beta) {
-            mask |= 1 << j2;
-            if (j2 < jj) first = false;
-          }
-        }
-        if (first) {
-          const int page = p.page_table[(size_t)b * g.MB + beta];
-          if (page >= 0 && page < g.NP) {
-            flag = 0x100 | (mask & 0xFF);
-            s_upage[e] = page;   // staged at the entry index, compacted below
-            ++keep_cnt;
+          if (first) {
+            const int page = pt_in_smem ? s_pt[beta] : p.page_table[(size_t)b * g.MB + beta];
+            if (page >= 0 && page < g.NP) {
+              flag = 0x100 | (mask & 0xFF);
+              pages[q] = page;
+              ++keep_cnt;
+            }
           }
         }
       }
+      flags[q] = flag;
     }
-    flags[q] = flag;
-  }
-  {
     int x = keep_cnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -257,126 +286,135 @@ sparse_decode_kernel(Params p) {
     if (lane == 31) misc[warp] = x;
     __syncthreads();
     int base = 0, tot = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w <= W; ++w) {
       base += (w < warp) ? misc[w] : 0;
       tot += misc[w];
     }
     int pos = base + x - keep_cnt;
-    int pages[16];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) pages[q] = flags[q] ? s_upage[e_lo + q] : 0;
-    __syncthreads();   // every staged page read before compaction overwrites
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
+    for (int q = 0; q < kPer; ++q) {
       if (!flags[q]) continue;
-      const int beta = s_sel[e_lo + q];
-      s_union[pos] = beta | ((flags[q] & 0xFF) << 24);
+      s_union[pos] = s_sel[e_lo + q] | ((flags[q] & 0xFF) << 24);
       s_upage[pos] = pages[q];
       ++pos;
     }
-    if (tid == 0) misc[8] = tot;
+    if (tid == 0) misc[16] = tot;
   }
   __syncthreads();
 
-  const int U = misc[8];
+  const int U = misc[16];
   const int cpp = g.P / kChunk;               // chunks per page
   const int C = U * cpp;
   const int per_split = (C + p.splits - 1) / p.splits;
   const int ch_lo = min(C, s * per_split);
-  const int ch_hi = min(C, ch_lo + per_split);
-  const int all_rows = (1 << nrows) - 1;
+  const int n_ch = min(C, ch_lo + per_split) - ch_lo;
 
-  const uint64_t pol = policy_evict_first();
-  const bool leader = (rank == 0) && (lane == 0);
-  uint8_t* my_stages = region + team * STAGES * kStageBytes;
-  uint64_t* my_bars = bars + team * STAGES;
-  const int first_ch = ch_lo + team;
-  const int n_my = (ch_hi > first_ch) ? (ch_hi - first_ch + kTeams - 1) / kTeams : 0;
-
-  auto issue = [&](int i) {   // this team's chunk i into stage i % STAGES
-    const int c = first_ch + i * kTeams;
+  // ---- producer: stream this split's chunks through the stages -------------
+  // The first S chunks need no stage to drain, so they go out before the
+  // prologue barrier; the rest wait for consumers and so are issued after it.
+  const uint64_t pol = producer ? policy_evict_first() : 0ull;
+  auto issue = [&](int i) {
+    const int st = i % S;
+    const int c = ch_lo + i;
     const int u = c / cpp, sub = c % cpp;
     const size_t row0 = ((size_t)s_upage[u] * g.Hkv + kvh) * g.P + (size_t)sub * kChunk;
-    uint8_t* st = my_stages + (i % STAGES) * kStageBytes;
-    uint64_t* bar = &my_bars[i % STAGES];
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar, kStageBytes);
-    bulk_g2s(st, p.k_pool + row0 * (kHeadDim / 2), kKBytes, bar, pol);
-    bulk_g2s(st + kKBytes, p.v_pool + row0 * (kHeadDim / 2), kKBytes, bar, pol);
-    bulk_g2s(st + 2 * kKBytes, p.k_sf + row0 * (kHeadDim / 16), kSfBytes, bar, pol);
-    bulk_g2s(st + 2 * kKBytes + kSfBytes, p.v_sf + row0 * (kHeadDim / 16), kSfBytes, bar, pol);
+    uint8_t* dst = region + st * kStageBytes;
+    mbar_arrive_expect_tx(&full[st], kStageBytes);
+    bulk_g2s(dst, p.k_pool + row0 * (kHeadDim / 2), kKBytes, &full[st], pol);
+    bulk_g2s(dst + kKBytes, p.v_pool + row0 * (kHeadDim / 2), kKBytes, &full[st], pol);
+    bulk_g2s(dst + 2 * kKBytes, p.k_sf + row0 * (kHeadDim / 16), kSfBytes, &full[st], pol);
+    bulk_g2s(dst + 2 * kKBytes + kSfBytes, p.v_sf + row0 * (kHeadDim / 16), kSfBytes, &full[st],
+             pol);
   };
-  if (leader)
-    for (int i = 0; i < STAGES && i < n_my; ++i) issue(i);
+  const int n_pre = min(n_ch, S);
+  if (producer && lane == 0)
+    for (int i = 0; i < n_pre; ++i) issue(i);
 
-  // ---- queries (overlapping the first copies) -----------------------------
-  const int L = p.seqlens[b];
+  // ---- queries: pre-scaled fp16 and per-column constants -------------------
   const int cap = g.MB * g.P;
-  for (int c = warp; c < NT * 8; c += kWarps) {
-    float amax = 0.f;
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
-    int jrow = 0;
-    if (c < ncols) {
-      const int col = c0 + c;
-      jrow = col / G;
-      const int h = kvh * G + col % G;
-      const __nv_bfloat16* src = p.q + ((size_t)(b * R + jrow) * g.Hq + h) * kHeadDim + lane * 4;
-      const uint2 raw = *reinterpret_cast<const uint2*>(src);
-      const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-      const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-      v[0] = __low2float(lo); v[1] = __high2float(lo);
-      v[2] = __low2float(hi); v[3] = __high2float(hi);
-      amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-    }
+#pragma unroll
+  for (int ci = 0; ci < kQPerWarp; ++ci) {
+    const int c = warp + ci * (W + 1);
+    if (c >= ncols) break;
+    const float* v = qv[ci];
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
     for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     // Power-of-two pre-scale mapping |q|max into [256, 512): exact, and keeps
-    // bf16 queries of any magnitude inside fp16 range.
-    int e = 0;
-    if (amax > 0.f) frexpf(amax, &e);
-    const int sq = (amax > 0.f) ? 9 - e : 0;
+    // bf16 queries of any magnitude inside fp16 range.  The scale 2^sq and its
+    // inverse are built from exponent bits (|sq| <= 126 keeps both normal).
+    const int ebits = (int)((__float_as_uint(amax) >> 23) & 0xFF);
+    int sq = (amax > 0.f) ? 135 - ebits : 0;
+    sq = sq > 126 ? 126 : (sq < -126 ? -126 : sq);
+    const float up = __uint_as_float((uint32_t)(sq + 127) << 23);
+    const float down = __uint_as_float((uint32_t)(127 - sq) << 23);
     __half2* dst = reinterpret_cast<__half2*>(qs + c * kHeadDim + lane * 4);
-    dst[0] = __floats2half2_rn(ldexpf(v[0], sq), ldexpf(v[1], sq));
-    dst[1] = __floats2half2_rn(ldexpf(v[2], sq), ldexpf(v[3], sq));
+    dst[0] = __floats2half2_rn(v[0] * up, v[1] * up);
+    dst[1] = __floats2half2_rn(v[2] * up, v[3] * up);
     if (lane == 0) {
-      col_cq[c] = (c < ncols) ? p.k_scale * p.sm_scale * kLog2e * ldexpf(1.f, -sq) : 0.f;
-      col_n[c] = (c < ncols) ? visible_tokens(L, R, jrow, cap) : 0;
-      col_bit[c] = (c < ncols) ? (jrow - j_lo) : 31;
+      const int j = c / kHsp;
+      col_cq[c] = ((c % kHsp) < hs) ? p.k_scale * p.sm_scale * kLog2e * down : 0.f;
+      col_n[c] = visible_tokens(L, R, j, cap);
     }
   }
   __syncthreads();
-  if (tid < NT) {
-    int m = 0;
-    for (int c = tid * 8; c < tid * 8 + 8; ++c)
-      if (c < ncols) m |= 1 << col_bit[c];
-    tile_rows[tid] = m;
-  }
-  int min_n = 0x7FFFFFFF;
-  for (int c = 0; c < ncols; ++c) min_n = min(min_n, col_n[c]);
-  __syncthreads();
   pdl_trigger();
 
-  float cq[NT][2];
-  int trows[NT];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    trows[nt] = tile_rows[nt];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) cq[nt][e] = col_cq[nt * 8 + 2 * tig + e];
+  if (producer) {
+    if (lane == 0) {
+      int dead = 0, issued = n_pre;
+      for (int i = n_pre; i < n_ch; ++i) {
+        if (!wait_bounded(&empty[i % S], ((i / S) - 1) & 1)) {
+          dead = 1;
+          break;
+        }
+        fence_proxy_async_smem();   // consumers' reads of the stage come first
+        issue(i);
+        issued = i + 1;
+      }
+      if (dead) atomicExch(p.status, kStatusWaitTimeout);
+      // Every issued copy lands before the stage memory is reused below (older
+      // ones were consumed before their stage was refilled).
+      for (int i = max(0, issued - S); i < issued; ++i)
+        if (!wait_bounded(&full[i % S], (i / S) & 1)) atomicExch(p.status, kStatusWaitTimeout);
+    }
+    __syncwarp();
   }
-  int all_tiles = 0;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) all_tiles |= (trows[nt] != 0) << nt;
 
-  // Q^T fragments (column nt*8+gid, dims [32*tig, 32*tig+32)) in registers for
-  // up to two column tiles; wider tiles are read from shared memory per use.
-  constexpr bool kQInRegs = NT <= 2;
-  uint32_t qf[kQInRegs ? NT : 1][16];
-  if constexpr (kQInRegs) {
+  // ---- consumers -------------------------------------------------------------
+  // Decode: every consumer on row 0, chunks round-robin.  Verify: consumer w
+  // owns row w % R and, of that row's chunks, those with index = w / R modulo
+  // the W / R consumers per row.
+  const int gper = (R == 1) ? W : W / R;        // consumers per row
+  const int jw = (R == 1) ? 0 : warp % R;       // the row this warp owns
+  const int gw = (R == 1) ? 0 : warp / R;
+  float m_run[NTR][2], l_run[NTR][2];
+  float o_acc[8][NTR][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const uint4* src = reinterpret_cast<const uint4*>(qs + (nt * 8 + gid) * kHeadDim + 32 * tig);
+  for (int nt = 0; nt < NTR; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) { m_run[nt][e] = -INFINITY; l_run[nt][e] = 0.f; }
+#pragma unroll
+  for (int dt = 0; dt < 8; ++dt)
+#pragma unroll
+    for (int nt = 0; nt < NTR; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o_acc[dt][nt][e] = 0.f;
+
+  if (!producer && jw < R) {
+    const int cbase = jw * kHsp;
+    float cq[NTR][2];
+#pragma unroll
+    for (int nt = 0; nt < NTR; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) cq[nt][e] = col_cq[cbase + nt * 8 + 2 * tig + e];
+    const int nrow = col_n[cbase];              // tokens this row sees
+    // Q^T fragments: column nt*8+gid of the row, dims [32*tig, 32*tig+32).
+    uint32_t qf[NTR][16];
+#pragma unroll
+    for (int nt = 0; nt < NTR; ++nt) {
+      const uint4* src =
+          reinterpret_cast<const uint4*>(qs + (cbase + nt * 8 + gid) * kHeadDim + 32 * tig);
 #pragma unroll
       for (int v4 = 0; v4 < 4; ++v4) {
         const uint4 x = src[v4];
@@ -384,314 +422,213 @@ sparse_decode_kernel(Params p) {
         qf[nt][4 * v4 + 2] = x.z; qf[nt][4 * v4 + 3] = x.w;
       }
     }
-  }
 
-  // Online-softmax state (log2 domain) for the thread's columns.
-  float m_run[NT][2], l_run[NT][2];
-  float o_acc[kDtPerWarp][NT][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) { m_run[nt][e] = -INFINITY; l_run[nt][e] = 0.f; }
-#pragma unroll
-  for (int dt = 0; dt < kDtPerWarp; ++dt)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o_acc[dt][nt][e] = 0.f;
+    bool dead = false;
+    const int i0 = (R == 1) ? warp : 0;
+    const int di = (R == 1) ? W : 1;
+    for (int i = i0; i < n_ch; i += di) {
+      const int st = i % S;
+      const int c = ch_lo + i;
+      const int u = c / cpp, sub = c % cpp;
+      const int ue = s_union[u];
+      const bool mine = (R == 1) || (((ue >> (24 + jw)) & 1) && (i % gper) == gw);
+      if (!dead && !wait_bounded(&full[st], (i / S) & 1)) {
+        dead = true;
+        if (lane == 0) atomicExch(p.status, kStatusWaitTimeout);
+      }
+      if (mine && !dead) {
+        const int beta = ue & 0xFFFFFF;
+        const int tok0 = beta * g.P + sub * kChunk;
+        const bool partial = tok0 + kChunk > nrow;
+        const uint8_t* sk = region + st * kStageBytes;
+        const uint8_t* sv = sk + kKBytes;
+        const uint8_t* sks = sk + 2 * kKBytes;
+        const uint8_t* svs = sks + kSfBytes;
 
-  bool dead = false;
-  int i = 0;
-  for (; i < n_my; ++i) {
-    const int c = first_ch + i * kTeams;
-    const int u = c / cpp, sub = c % cpp;
-    const int ue = s_union[u];
-    const int beta = ue & 0xFFFFFF;
-    const int rmask = (ue >> 24) & 0xFF;
-    const int tok0 = beta * g.P + sub * kChunk;
-    const bool full = (rmask == all_rows) && (tok0 + kChunk <= min_n);
-    int act = 0;   // column tiles with a row that selected this page
+        // ---- S^T = K . Q^T over the chunk's four 16-token tiles ------------
+        // Tiles go in pairs: k-steps outside and the pair inside, so
+        // consecutive MMAs feed different accumulators.
+        float sacc[4][NTR][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) act |= ((trows[nt] & rmask) != 0) << nt;
-    if (full) act = all_tiles;
-    const uint8_t* st = my_stages + (i % STAGES) * kStageBytes;
-    const bool ok = wait_stage(&my_bars[i % STAGES], (i / STAGES) & 1);
-    if constexpr (TEAM == 1) {
-      if (!ok) { dead = true; break; }
-    } else {
-      if (lane == 0) misc[16 + warp] = ok ? 0 : 1;
-    }
-    const uint8_t* sk = st;
-    const uint8_t* sv = st + kKBytes;
-    const uint8_t* sks = st + 2 * kKBytes;
-    const uint8_t* svs = st + 2 * kKBytes + kSfBytes;
-
-    // ---- S^T = K . Q^T over this warp's 16-token tiles ---------------------
-    float sacc[kMtPerWarp][NT][4];
+        for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-    for (int mi = 0; mi < kMtPerWarp; ++mi) {
-      const int mt = rank * kMtPerWarp + mi;
-      const int rA = 16 * mt + (gid >> 1) + 4 * (gid & 1);
-      const int rB = rA + 8;
-      const uint4 kA = *reinterpret_cast<const uint4*>(sk + rA * 64 + 16 * tig);
-      const uint4 kB = *reinterpret_cast<const uint4*>(sk + rB * 64 + 16 * tig);
-      const uint32_t sA = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sks + rA * 8 + 2 * tig));
-      const uint32_t sB = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sks + rB * 8 + 2 * tig));
-      const uint32_t scA[2] = {prmt(sA, 0, 0x1010), prmt(sA, 0, 0x3232)};
-      const uint32_t scB[2] = {prmt(sB, 0, 0x1010), prmt(sB, 0, 0x3232)};
-      const uint32_t wA[4] = {kA.x, kA.y, kA.z, kA.w};
-      const uint32_t wB[4] = {kB.x, kB.y, kB.z, kB.w};
+          for (int nt = 0; nt < NTR; ++nt)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+            for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[mi][nt][e] = 0.f;
+        for (int m0 = 0; m0 < 4; m0 += 2) {
+          uint32_t wA[2][4], wB[2][4], scA[2][2], scB[2][2];
 #pragma unroll
-      for (int wd = 0; wd < 4; ++wd) {
-        uint32_t fa[4], fb[4];
-        e2m1x8_to_f16x2x4(wA[wd], fa);
-        e2m1x8_to_f16x2x4(wB[wd], fb);
-        const uint32_t sa = scA[wd >> 1], sb = scB[wd >> 1];
+          for (int gi = 0; gi < 2; ++gi) {
+            const int mt = m0 + gi;
+            const int rA = 16 * mt + (gid >> 1) + 4 * (gid & 1);
+            const int rB = rA + 8;
+            const uint4 kA = *reinterpret_cast<const uint4*>(sk + rA * 64 + 16 * tig);
+            const uint4 kB = *reinterpret_cast<const uint4*>(sk + rB * 64 + 16 * tig);
+            const uint32_t sA = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sks + rA * 8 + 2 * tig));
+            const uint32_t sB = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sks + rB * 8 + 2 * tig));
+            scA[gi][0] = prmt(sA, 0, 0x1010); scA[gi][1] = prmt(sA, 0, 0x3232);
+            scB[gi][0] = prmt(sB, 0, 0x1010); scB[gi][1] = prmt(sB, 0, 0x3232);
+            wA[gi][0] = kA.x; wA[gi][1] = kA.y; wA[gi][2] = kA.z; wA[gi][3] = kA.w;
+            wB[gi][0] = kB.x; wB[gi][1] = kB.y; wB[gi][2] = kB.z; wB[gi][3] = kB.w;
+          }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int kk = 2 * wd + h;
-          uint32_t a[4];
-          a[0] = hmul2_u32(fa[2 * h], sa);
-          a[2] = hmul2_u32(fa[2 * h + 1], sa);
-          a[1] = hmul2_u32(fb[2 * h], sb);
-          a[3] = hmul2_u32(fb[2 * h + 1], sb);
+          for (int wd = 0; wd < 4; ++wd) {
+            uint32_t fa[2][4], fb[2][4];
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            if (act & (1 << nt)) {
-              uint32_t b0, b1;
-              if constexpr (kQInRegs) {
-                b0 = qf[kQInRegs ? nt : 0][2 * kk];
-                b1 = qf[kQInRegs ? nt : 0][2 * kk + 1];
-              } else {
-                const uint2 qv = *reinterpret_cast<const uint2*>(
-                    qs + (nt * 8 + gid) * kHeadDim + 32 * tig + 4 * kk);
-                b0 = qv.x;
-                b1 = qv.y;
+            for (int gi = 0; gi < 2; ++gi) {
+              e2m1x8_to_f16x2x4(wA[gi][wd], fa[gi]);
+              e2m1x8_to_f16x2x4(wB[gi][wd], fb[gi]);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int kk = 2 * wd + h;
+#pragma unroll
+              for (int gi = 0; gi < 2; ++gi) {
+                const uint32_t sa = scA[gi][wd >> 1], sb = scB[gi][wd >> 1];
+                uint32_t a[4];
+                a[0] = hmul2_u32(fa[gi][2 * h], sa);
+                a[2] = hmul2_u32(fa[gi][2 * h + 1], sa);
+                a[1] = hmul2_u32(fb[gi][2 * h], sb);
+                a[3] = hmul2_u32(fb[gi][2 * h + 1], sb);
+#pragma unroll
+                for (int nt = 0; nt < NTR; ++nt)
+                  mma_f16_16816(sacc[m0 + gi][nt], a, qf[nt][2 * kk], qf[nt][2 * kk + 1]);
               }
-              mma_f16_16816(sacc[mi][nt], a, b0, b1);
+            }
+          }
+        }
+
+        // ---- logits, causal mask, chunk max --------------------------------
+        float cmax[NTR][2];
+#pragma unroll
+        for (int nt = 0; nt < NTR; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) cmax[nt][e] = -INFINITY;
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+          const int tA = tok0 + 16 * mt + (gid >> 1) + 4 * (gid & 1);
+          const int tB = tA + 8;
+#pragma unroll
+          for (int nt = 0; nt < NTR; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float zA = sacc[mt][nt][e] * cq[nt][e];
+              float zB = sacc[mt][nt][2 + e] * cq[nt][e];
+              if (partial) {
+                if (tA >= nrow) zA = -INFINITY;
+                if (tB >= nrow) zB = -INFINITY;
+              }
+              sacc[mt][nt][e] = zA;
+              sacc[mt][nt][2 + e] = zB;
+              cmax[nt][e] = fmaxf(cmax[nt][e], fmaxf(zA, zB));
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NTR; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float v = cmax[nt][e];
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+            cmax[nt][e] = v;
+          }
+
+        // ---- online softmax update -----------------------------------------
+        float base[NTR][2];
+        bool rescale = false;
+#pragma unroll
+        for (int nt = 0; nt < NTR; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float mn = fmaxf(m_run[nt][e], cmax[nt][e]);
+            rescale |= (mn != m_run[nt][e]) && (m_run[nt][e] != -INFINITY);
+            base[nt][e] = (mn == -INFINITY) ? 0.f : mn;
+          }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int nt = 0; nt < NTR; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float alpha = exp2f(m_run[nt][e] - base[nt][e]);
+              l_run[nt][e] *= alpha;
+#pragma unroll
+              for (int dt = 0; dt < 8; ++dt) {
+                o_acc[dt][nt][e] *= alpha;
+                o_acc[dt][nt][2 + e] *= alpha;
+              }
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NTR; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) m_run[nt][e] = fmaxf(m_run[nt][e], cmax[nt][e]);
+
+        // P = exp2(z - base) -> fp16 -> transposed B fragments for P^T.
+        uint32_t pf[4][NTR][2];
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < NTR; ++nt) {
+            const float p0 = exp2f(sacc[mt][nt][0] - base[nt][0]);
+            const float p1 = exp2f(sacc[mt][nt][1] - base[nt][1]);
+            const float p2 = exp2f(sacc[mt][nt][2] - base[nt][0]);
+            const float p3 = exp2f(sacc[mt][nt][3] - base[nt][1]);
+            l_run[nt][0] += p0 + p2;
+            l_run[nt][1] += p1 + p3;
+            pf[mt][nt][0] = movmatrix_trans(pack_half2(p0, p1));
+            pf[mt][nt][1] = movmatrix_trans(pack_half2(p2, p3));
+          }
+
+        // ---- O^T += V^T . P^T over the eight 16-dim tiles -------------------
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const int t0 = 16 * ks + tig;
+          const uint32_t sv01 = e4m3x2_to_f16x2((uint32_t)svs[t0 * 8 + gid] |
+                                                ((uint32_t)svs[(t0 + 4) * 8 + gid] << 8));
+          const uint32_t sv23 = e4m3x2_to_f16x2((uint32_t)svs[(t0 + 8) * 8 + gid] |
+                                                ((uint32_t)svs[(t0 + 12) * 8 + gid] << 8));
+#pragma unroll
+          for (int w4 = 0; w4 < 2; ++w4) {
+            // bytes [8*gid + 4*w4, +4) of the four token rows of this k-step
+            const int boff = 8 * gid + 4 * w4;
+            const uint32_t X = *reinterpret_cast<const uint32_t*>(sv + t0 * 64 + boff);
+            const uint32_t Y = *reinterpret_cast<const uint32_t*>(sv + (t0 + 4) * 64 + boff);
+            const uint32_t X2 = *reinterpret_cast<const uint32_t*>(sv + (t0 + 8) * 64 + boff);
+            const uint32_t Y2 = *reinterpret_cast<const uint32_t*>(sv + (t0 + 12) * 64 + boff);
+            const uint32_t LO = (X & 0x0F0F0F0Fu) | ((Y << 4) & 0xF0F0F0F0u);
+            const uint32_t HI = ((X >> 4) & 0x0F0F0F0Fu) | (Y & 0xF0F0F0F0u);
+            const uint32_t LO2 = (X2 & 0x0F0F0F0Fu) | ((Y2 << 4) & 0xF0F0F0F0u);
+            const uint32_t HI2 = ((X2 >> 4) & 0x0F0F0F0Fu) | (Y2 & 0xF0F0F0F0u);
+            uint32_t f0[4], f1[4], f2[4], f3[4];
+            e2m1x8_to_f16x2x4(LO, f0);
+            e2m1x8_to_f16x2x4(HI, f1);
+            e2m1x8_to_f16x2x4(LO2, f2);
+            e2m1x8_to_f16x2x4(HI2, f3);
+#pragma unroll
+            for (int bi = 0; bi < 4; ++bi) {
+              const int dt = 4 * w4 + bi;
+              uint32_t a[4];
+              a[0] = hmul2_u32(f0[bi], sv01);
+              a[1] = hmul2_u32(f1[bi], sv01);
+              a[2] = hmul2_u32(f2[bi], sv23);
+              a[3] = hmul2_u32(f3[bi], sv23);
+#pragma unroll
+              for (int nt = 0; nt < NTR; ++nt)
+                mma_f16_16816(o_acc[dt][nt], a, pf[ks][nt][0], pf[ks][nt][1]);
             }
           }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
     }
-
-    // ---- logits, masking, chunk max --------------------------------------
-    float cmax[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) cmax[nt][e] = -INFINITY;
-#pragma unroll
-    for (int mi = 0; mi < kMtPerWarp; ++mi) {
-      const int mt = rank * kMtPerWarp + mi;
-      const int tA = tok0 + 16 * mt + (gid >> 1) + 4 * (gid & 1);
-      const int tB = tA + 8;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        if (!(act & (1 << nt))) continue;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float zA = sacc[mi][nt][e] * cq[nt][e];
-          float zB = sacc[mi][nt][2 + e] * cq[nt][e];
-          if (!full) {
-            const int cc = nt * 8 + 2 * tig + e;
-            const int lim = ((rmask >> col_bit[cc]) & 1) ? col_n[cc] : 0;
-            if (tA >= lim) zA = -INFINITY;
-            if (tB >= lim) zB = -INFINITY;
-          }
-          sacc[mi][nt][e] = zA;
-          sacc[mi][nt][2 + e] = zB;
-          cmax[nt][e] = fmaxf(cmax[nt][e], fmaxf(zA, zB));
-        }
-      }
-    }
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      if (!(act & (1 << nt))) continue;
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float v = cmax[nt][e];
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-        cmax[nt][e] = v;
-      }
-    }
-    if constexpr (TEAM > 1) {
-      float* xm = xmax + team * TEAM * kMaxCols;
-      if (gid == 0) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) xm[rank * kMaxCols + nt * 8 + 2 * tig + e] = cmax[nt][e];
-      }
-      team_sync<TEAM>(team);
-      int dead_any = 0;
-#pragma unroll
-      for (int r2 = 0; r2 < TEAM; ++r2) dead_any |= misc[16 + team * TEAM + r2];
-      if (dead_any) { dead = true; break; }
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        if (!(act & (1 << nt))) continue;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float v = -INFINITY;
-#pragma unroll
-          for (int r2 = 0; r2 < TEAM; ++r2) v = fmaxf(v, xm[r2 * kMaxCols + nt * 8 + 2 * tig + e]);
-          cmax[nt][e] = v;
-        }
-      }
-    }
-
-    // ---- online softmax update -------------------------------------------
-    float base[NT][2];
-    bool rescale = false;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float mn = fmaxf(m_run[nt][e], cmax[nt][e]);
-        rescale |= (mn != m_run[nt][e]) && (m_run[nt][e] != -INFINITY);
-        base[nt][e] = (mn == -INFINITY) ? 0.f : mn;
-      }
-    if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float alpha = exp2f(m_run[nt][e] - base[nt][e]);
-          l_run[nt][e] *= alpha;
-#pragma unroll
-          for (int dt = 0; dt < kDtPerWarp; ++dt) {
-            o_acc[dt][nt][e] *= alpha;
-            o_acc[dt][nt][2 + e] *= alpha;
-          }
-        }
-    }
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) m_run[nt][e] = fmaxf(m_run[nt][e], cmax[nt][e]);
-
-    // P = exp2(z - base) -> fp16 -> transposed B fragments for P^T.  Slot q
-    // holds 16-token tile ((q / kMtPerWarp + rank) % TEAM) * kMtPerWarp +
-    // q % kMtPerWarp: this warp's own tiles first.
-    uint32_t pf[4][NT][2];
-#pragma unroll
-    for (int mi = 0; mi < kMtPerWarp; ++mi) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        if (!(act & (1 << nt))) continue;
-        const float p0 = exp2f(sacc[mi][nt][0] - base[nt][0]);
-        const float p1 = exp2f(sacc[mi][nt][1] - base[nt][1]);
-        const float p2 = exp2f(sacc[mi][nt][2] - base[nt][0]);
-        const float p3 = exp2f(sacc[mi][nt][3] - base[nt][1]);
-        l_run[nt][0] += p0 + p2;
-        l_run[nt][1] += p1 + p3;
-        pf[mi][nt][0] = movmatrix_trans(pack_half2(p0, p1));
-        pf[mi][nt][1] = movmatrix_trans(pack_half2(p2, p3));
-      }
-    }
-    if constexpr (TEAM > 1) {
-      uint32_t* mine = xp + ((team * TEAM + rank) * kSlots) * 32 + lane;
-#pragma unroll
-      for (int mi = 0; mi < kMtPerWarp; ++mi)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          if (!(act & (1 << nt))) continue;
-          mine[((mi * NT + nt) * 2 + 0) * 32] = pf[mi][nt][0];
-          mine[((mi * NT + nt) * 2 + 1) * 32] = pf[mi][nt][1];
-        }
-      team_sync<TEAM>(team);
-#pragma unroll
-      for (int r2 = 1; r2 < TEAM; ++r2) {
-        const int other = (rank + r2) % TEAM;
-        const uint32_t* theirs = xp + ((team * TEAM + other) * kSlots) * 32 + lane;
-#pragma unroll
-        for (int mi = 0; mi < kMtPerWarp; ++mi)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            if (!(act & (1 << nt))) continue;
-            pf[r2 * kMtPerWarp + mi][nt][0] = theirs[((mi * NT + nt) * 2 + 0) * 32];
-            pf[r2 * kMtPerWarp + mi][nt][1] = theirs[((mi * NT + nt) * 2 + 1) * 32];
-          }
-      }
-    }
-
-    // ---- O^T += V^T . P^T over this warp's 16-dim tiles ---------------------
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int ks = ((q / kMtPerWarp + rank) % TEAM) * kMtPerWarp + q % kMtPerWarp;
-      const int t0 = 16 * ks + tig;
-      const uint32_t sv01 = e4m3x2_to_f16x2((uint32_t)svs[t0 * 8 + gid] |
-                                            ((uint32_t)svs[(t0 + 4) * 8 + gid] << 8));
-      const uint32_t sv23 = e4m3x2_to_f16x2((uint32_t)svs[(t0 + 8) * 8 + gid] |
-                                            ((uint32_t)svs[(t0 + 12) * 8 + gid] << 8));
-#pragma unroll
-      for (int w4 = 0; w4 < (kDtPerWarp + 3) / 4; ++w4) {
-        // bytes [8*gid + dbase, +kNb) of the four token rows of this k-step
-        constexpr int kNb = kDtPerWarp < 4 ? kDtPerWarp : 4;
-        const int dbase = rank * kDtPerWarp + 4 * w4;
-        uint32_t X, Y, X2, Y2;
-        if constexpr (kNb == 4) {
-          X = *reinterpret_cast<const uint32_t*>(sv + t0 * 64 + 8 * gid + dbase);
-          Y = *reinterpret_cast<const uint32_t*>(sv + (t0 + 4) * 64 + 8 * gid + dbase);
-          X2 = *reinterpret_cast<const uint32_t*>(sv + (t0 + 8) * 64 + 8 * gid + dbase);
-          Y2 = *reinterpret_cast<const uint32_t*>(sv + (t0 + 12) * 64 + 8 * gid + dbase);
-        } else {
-          X = *reinterpret_cast<const uint16_t*>(sv + t0 * 64 + 8 * gid + dbase);
-          Y = *reinterpret_cast<const uint16_t*>(sv + (t0 + 4) * 64 + 8 * gid + dbase);
-          X2 = *reinterpret_cast<const uint16_t*>(sv + (t0 + 8) * 64 + 8 * gid + dbase);
-          Y2 = *reinterpret_cast<const uint16_t*>(sv + (t0 + 12) * 64 + 8 * gid + dbase);
-        }
-        const uint32_t LO = (X & 0x0F0F0F0Fu) | ((Y << 4) & 0xF0F0F0F0u);
-        const uint32_t HI = ((X >> 4) & 0x0F0F0F0Fu) | (Y & 0xF0F0F0F0u);
-        const uint32_t LO2 = (X2 & 0x0F0F0F0Fu) | ((Y2 << 4) & 0xF0F0F0F0u);
-        const uint32_t HI2 = ((X2 >> 4) & 0x0F0F0F0Fu) | (Y2 & 0xF0F0F0F0u);
-        uint32_t f0[4], f1[4], f2[4], f3[4];
-        e2m1x8_to_f16x2x4(LO, f0);
-        e2m1x8_to_f16x2x4(HI, f1);
-        e2m1x8_to_f16x2x4(LO2, f2);
-        e2m1x8_to_f16x2x4(HI2, f3);
-#pragma unroll
-        for (int bi = 0; bi < kNb; ++bi) {
-          const int dl = 4 * w4 + bi;
-          uint32_t a[4];
-          a[0] = hmul2_u32(f0[bi], sv01);
-          a[1] = hmul2_u32(f1[bi], sv01);
-          a[2] = hmul2_u32(f2[bi], sv23);
-          a[3] = hmul2_u32(f3[bi], sv23);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            if (act & (1 << nt)) mma_f16_16816(o_acc[dl][nt], a, pf[q][nt][0], pf[q][nt][1]);
-        }
-      }
-    }
-
-    // Release the stage and refill it with this team's chunk i + STAGES.
-    team_sync<TEAM>(team);
-    if (leader && i + STAGES < n_my) issue(i + STAGES);
   }
 
-  if (dead) {
-    // A copy never completed: record it, then drain this team's other
-    // in-flight copies (bounded) before the stage memory is reused.
-    if (lane == 0) atomicExch(p.status, kStatusWaitTimeout);
-    for (int i2 = i; i2 < n_my && i2 < i + STAGES; ++i2)
-      (void)wait_stage(&my_bars[i2 % STAGES], (i2 / STAGES) & 1);
+  // Row sums over the 8 token lanes of the warp.
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) { m_run[nt][e] = -INFINITY; l_run[nt][e] = 0.f; }
-  }
-
-  // Row sums over the 8 token lanes of this warp.
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
+  for (int nt = 0; nt < NTR; ++nt)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       float v = l_run[nt][e];
@@ -701,59 +638,69 @@ sparse_decode_kernel(Params p) {
       l_run[nt][e] = v;
     }
 
-  // ---- combine the warps and teams of this CTA ----------------------------
-  __syncthreads();   // every stage consumed: the region holds the partials now
-  float* co = reinterpret_cast<float*>(region);                  // [teams][32][128]
-  float* cm = co + kTeams * kMaxCols * kHeadDim;                  // [teams][32]
-  float* cl = cm + kTeams * kMaxCols;                             // [warps][32]
-  if (gid == 0) {
+  // ---- combine the consumers of this CTA ------------------------------------
+  __syncthreads();   // every copy landed and was consumed: reuse the stage region
+  float* co = reinterpret_cast<float*>(region);                  // [W][kHsp][128]
+  float* cm = co + W * kHsp * kHeadDim;                           // [W][kHsp]
+  float* cl = cm + W * kHsp;                                      // [W][kHsp]
+  float* cp = reinterpret_cast<float*>(region + Lay::kCpOff);     // [ncols][kPartStride]
+  if (!producer) {
+    if (gid == 0) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+      for (int nt = 0; nt < NTR; ++nt)
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int cc = nt * 8 + 2 * tig + e;
-        if (rank == 0) cm[team * kMaxCols + cc] = m_run[nt][e];
-        cl[warp * kMaxCols + cc] = l_run[nt][e];
-      }
-  }
-  // O^T accumulators: dim 16*gid + 2*dt (+1 for c2/c3), column nt*8 + 2*tig + e.
+        for (int e = 0; e < 2; ++e) {
+          const int cc = nt * 8 + 2 * tig + e;
+          cm[warp * kHsp + cc] = m_run[nt][e];
+          cl[warp * kHsp + cc] = l_run[nt][e];
+        }
+    }
+    // O^T accumulators: dim 16*gid + 2*dt (+1 for c2/c3), column nt*8+2*tig+e.
 #pragma unroll
-  for (int dl = 0; dl < kDtPerWarp; ++dl) {
-    const int dt = rank * kDtPerWarp + dl;
+    for (int dt = 0; dt < 8; ++dt)
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+      for (int nt = 0; nt < NTR; ++nt)
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int cc = nt * 8 + 2 * tig + e;
-        const float2 v2 = make_float2(o_acc[dl][nt][e], o_acc[dl][nt][2 + e]);
-        *reinterpret_cast<float2*>(co + ((size_t)team * kMaxCols + cc) * kHeadDim + 16 * gid +
-                                   2 * dt) = v2;
-      }
+        for (int e = 0; e < 2; ++e) {
+          const int cc = nt * 8 + 2 * tig + e;
+          *reinterpret_cast<float2*>(co + ((size_t)warp * kHsp + cc) * kHeadDim + 16 * gid +
+                                     2 * dt) = make_float2(o_acc[dt][nt][e], o_acc[dt][nt][2 + e]);
+        }
   }
   __syncthreads();
 
-  const int units_idx = (b * g.Hkv + kvh) * p.qgroups + qg;
-  // Team weights exp2(m_team - M) for column cc; returns M (0 when empty) and
-  // the combined row sum.
-  auto team_weights = [&](int cc, float& M, float& Lsum, float (&wt)[kTeams]) {
+  // CTA partial per column (j, hh): m (log2 domain, -inf when empty), l, O,
+  // merged over the consumers of row j (warps j, j + R, ...).
+  const int wstep = (R == 1) ? 1 : R;
+  for (int idx = tid; idx < ncols * (kHeadDim / 4); idx += kThreads) {
+    const int c = idx / (kHeadDim / 4), d4 = (idx % (kHeadDim / 4)) * 4;
+    const int j = c / kHsp, cc = c % kHsp;
+    const int w_lo = (R == 1) ? 0 : j;
     float mx = -INFINITY;
-#pragma unroll
-    for (int t = 0; t < kTeams; ++t) mx = fmaxf(mx, cm[t * kMaxCols + cc]);
-    M = (mx == -INFINITY) ? 0.f : mx;
-    Lsum = 0.f;
-#pragma unroll
-    for (int t = 0; t < kTeams; ++t) {
-      wt[t] = exp2f(cm[t * kMaxCols + cc] - M);
-      float lt = 0.f;
-#pragma unroll
-      for (int r2 = 0; r2 < TEAM; ++r2) lt += cl[(t * TEAM + r2) * kMaxCols + cc];
-      Lsum += lt * wt[t];
+    for (int w = w_lo; w < W; w += wstep) mx = fmaxf(mx, cm[w * kHsp + cc]);
+    const float M = (mx == -INFINITY) ? 0.f : mx;
+    float Lsum = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int w = w_lo; w < W; w += wstep) {
+      const float wt = exp2f(cm[w * kHsp + cc] - M);
+      Lsum += cl[w * kHsp + cc] * wt;
+      const float4 v = *reinterpret_cast<const float4*>(co + ((size_t)w * kHsp + cc) * kHeadDim + d4);
+      O.x += v.x * wt; O.y += v.y * wt; O.z += v.z * wt; O.w += v.w * wt;
     }
-  };
-  auto store_out = [&](int cc, int d4, float4 O, float Lsum, float M) {
-    const int col = c0 + cc;
-    const int jrow = col / G, h = kvh * G + col % G;
-    const size_t orow = (size_t)(b * R + jrow) * g.Hq + h;
+    float* pc = cp + (size_t)c * kPartStride;
+    *reinterpret_cast<float4*>(pc + 4 + d4) = O;
+    if (d4 == 0) {
+      pc[0] = (Lsum > 0.f) ? M : -INFINITY;
+      pc[1] = Lsum;
+    }
+  }
+  __syncthreads();
+
+  auto store_out = [&](int c, int d4, float4 O, float Lsum, float M) {
+    const int j = c / kHsp, hh = c % kHsp;
+    if (hh >= hs) return;   // padding column
+    const int h = kvh * G + hs0 + hh;
+    const size_t orow = (size_t)(b * R + j) * g.Hq + h;
     const float sc = Lsum > 0.f ? p.v_scale / Lsum : 0.f;
     __nv_bfloat162 o01 = __floats2bfloat162_rn(O.x * sc, O.y * sc);
     __nv_bfloat162 o23 = __floats2bfloat162_rn(O.z * sc, O.w * sc);
@@ -766,89 +713,124 @@ sparse_decode_kernel(Params p) {
 
   if (p.splits == 1) {
     for (int idx = tid; idx < ncols * (kHeadDim / 4); idx += kThreads) {
-      const int cc = idx / (kHeadDim / 4), d4 = (idx % (kHeadDim / 4)) * 4;
-      float M, Lsum, wt[kTeams];
-      team_weights(cc, M, Lsum, wt);
-      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int t = 0; t < kTeams; ++t) {
-        const float4 v = *reinterpret_cast<const float4*>(co + ((size_t)t * kMaxCols + cc) * kHeadDim + d4);
-        O.x += v.x * wt[t]; O.y += v.y * wt[t]; O.z += v.z * wt[t]; O.w += v.w * wt[t];
-      }
-      store_out(cc, d4, O, Lsum, M);
+      const int c = idx / (kHeadDim / 4), d4 = (idx % (kHeadDim / 4)) * 4;
+      const float* pc = cp + (size_t)c * kPartStride;
+      store_out(c, d4, *reinterpret_cast<const float4*>(pc + 4 + d4), pc[1], pc[0]);
     }
     return;
   }
 
-  // Split partial (log2 domain), then a ticket: the last split of this
-  // (request, KV head, group) to arrive merges all of them in split order
-  // (deterministic) and resets the ticket.
-  float* part = p.partials + ((size_t)units_idx * p.splits + s) * kMaxCols * kPartStride;
-  for (int idx = tid; idx < ncols * (kHeadDim / 4); idx += kThreads) {
-    const int cc = idx / (kHeadDim / 4), d4 = (idx % (kHeadDim / 4)) * 4;
-    float M, Lsum, wt[kTeams];
-    team_weights(cc, M, Lsum, wt);
-    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (p.cluster > 1) {
+    // The splits of this unit form one thread-block cluster: merge their
+    // partials through distributed shared memory, each CTA finishing a slice
+    // of the (column, dim) items.  Split order is fixed (deterministic).
+    cg::cluster_group cluster = cg::this_cluster();
+    const int CL = p.cluster;
+    const int crank = (int)cluster.block_rank();
+    float* wt = cp + (size_t)ncols * kPartStride;                    // [ncols][kMaxCluster]
+    float* wM = wt + ncols * kMaxCluster;
+    float* wL = wM + ncols;
+    cluster.sync();   // every CTA's partial is in its shared memory
+    for (int c = tid; c < ncols; c += kThreads) {
+      float mx = -INFINITY;
+      float mr[kMaxCluster], lr[kMaxCluster];
 #pragma unroll
-    for (int t = 0; t < kTeams; ++t) {
-      const float4 v = *reinterpret_cast<const float4*>(co + ((size_t)t * kMaxCols + cc) * kHeadDim + d4);
-      O.x += v.x * wt[t]; O.y += v.y * wt[t]; O.z += v.z * wt[t]; O.w += v.w * wt[t];
+      for (int r2 = 0; r2 < kMaxCluster; ++r2) {
+        if (r2 < CL) {
+          const float* rp = cluster.map_shared_rank(cp, r2) + (size_t)c * kPartStride;
+          mr[r2] = rp[0];
+          lr[r2] = rp[1];
+          mx = fmaxf(mx, mr[r2]);
+        }
+      }
+      const float M = (mx == -INFINITY) ? 0.f : mx;
+      float Lsum = 0.f;
+#pragma unroll
+      for (int r2 = 0; r2 < kMaxCluster; ++r2) {
+        if (r2 < CL) {
+          const float w = exp2f(mr[r2] - M);
+          wt[c * kMaxCluster + r2] = w;
+          Lsum += lr[r2] * w;
+        }
+      }
+      wM[c] = M;
+      wL[c] = Lsum;
     }
-    float* pc = part + (size_t)cc * kPartStride;
-    *reinterpret_cast<float4*>(pc + 4 + d4) = O;
-    if (d4 == 0) {
-      pc[0] = (Lsum > 0.f) ? M : -INFINITY;
-      pc[1] = Lsum;
+    __syncthreads();
+    for (int idx = crank * kThreads + tid; idx < ncols * (kHeadDim / 4); idx += CL * kThreads) {
+      const int c = idx / (kHeadDim / 4), d4 = (idx % (kHeadDim / 4)) * 4;
+      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int r2 = 0; r2 < kMaxCluster; ++r2) {
+        if (r2 < CL) {
+          const float4 v = *reinterpret_cast<const float4*>(
+              cluster.map_shared_rank(cp, r2) + (size_t)c * kPartStride + 4 + d4);
+          const float w = wt[c * kMaxCluster + r2];
+          O.x += v.x * w; O.y += v.y * w; O.z += v.z * w; O.w += v.w * w;
+        }
+      }
+      store_out(c, d4, O, wL[c], wM[c]);
     }
+    cluster.sync();   // no CTA leaves while its partial may still be read
+    return;
   }
+
+  // Ticket merge: partials go to the workspace; the last split of this
+  // (request, KV head, slice) to arrive merges them in split order
+  // (deterministic) and resets the ticket.
+  const int units_idx = (b * g.Hkv + kvh) * p.slices + slice;
+  const size_t split_floats = (size_t)ncols * kPartStride;
+  float* part = p.partials + ((size_t)units_idx * p.splits + s) * split_floats;
+  for (int idx = tid; idx < ncols * (kPartStride / 4); idx += kThreads)
+    reinterpret_cast<float4*>(part)[idx] = reinterpret_cast<const float4*>(cp)[idx];
   __threadfence();
   __syncthreads();
   if (tid == 0) {
     const int prev = atomicAdd(&p.tickets[units_idx], 1);
-    misc[9] = (prev == p.splits - 1);
+    misc[17] = (prev == p.splits - 1);
   }
   __syncthreads();
-  if (!misc[9]) return;
+  if (!misc[17]) return;
   __threadfence();
 
   // Merge: per-column max and weights first, then float4 sums over splits.
-  const float* parts = p.partials + (size_t)units_idx * p.splits * kMaxCols * kPartStride;
-  float* wsplit = reinterpret_cast<float*>(region);                 // [32][splits]
-  float* lcol = wsplit + kMaxCols * p.splits;                       // [32]
-  float* mcol = lcol + kMaxCols;                                    // [32]
-  for (int cc = warp; cc < ncols; cc += kWarps) {
+  const float* parts = p.partials + (size_t)units_idx * p.splits * split_floats;
+  float* wsplit = reinterpret_cast<float*>(region);                 // [ncols][splits]
+  float* lcol = wsplit + (size_t)ncols * p.splits;                  // [ncols]
+  float* mcol = lcol + ncols;                                       // [ncols]
+  for (int c = warp; c < ncols; c += W + 1) {
     float mloc = -INFINITY;
     for (int t = lane; t < p.splits; t += 32)
-      mloc = fmaxf(mloc, __ldcg(parts + ((size_t)t * kMaxCols + cc) * kPartStride));
+      mloc = fmaxf(mloc, __ldcg(parts + t * split_floats + (size_t)c * kPartStride));
 #pragma unroll
     for (int o = 16; o; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
     const float base = (mloc == -INFINITY) ? 0.f : mloc;
     float lsum = 0.f;
     for (int t = lane; t < p.splits; t += 32) {
-      const float* pc = parts + ((size_t)t * kMaxCols + cc) * kPartStride;
+      const float* pc = parts + t * split_floats + (size_t)c * kPartStride;
       const float wgt = exp2f(__ldcg(pc) - base);
-      wsplit[cc * p.splits + t] = wgt;
+      wsplit[c * p.splits + t] = wgt;
       lsum += __ldcg(pc + 1) * wgt;
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
     if (lane == 0) {
-      lcol[cc] = lsum;
-      mcol[cc] = base;
+      lcol[c] = lsum;
+      mcol[c] = base;
     }
   }
   __syncthreads();
   for (int idx = tid; idx < ncols * (kHeadDim / 4); idx += kThreads) {
-    const int cc = idx / (kHeadDim / 4), d4 = (idx % (kHeadDim / 4)) * 4;
+    const int c = idx / (kHeadDim / 4), d4 = (idx % (kHeadDim / 4)) * 4;
     float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float* src = parts + (size_t)cc * kPartStride + 4 + d4;
-    const float* wrow = wsplit + cc * p.splits;
+    const float* src = parts + (size_t)c * kPartStride + 4 + d4;
+    const float* wrow = wsplit + c * p.splits;
     int t = 0;
     for (; t + 4 <= p.splits; t += 4) {
       float4 v[4];
 #pragma unroll
       for (int u2 = 0; u2 < 4; ++u2)
-        v[u2] = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(t + u2) * kMaxCols * kPartStride));
+        v[u2] = __ldcg(reinterpret_cast<const float4*>(src + (t + u2) * split_floats));
 #pragma unroll
       for (int u2 = 0; u2 < 4; ++u2) {
         const float wgt = wrow[t + u2];
@@ -856,11 +838,11 @@ sparse_decode_kernel(Params p) {
       }
     }
     for (; t < p.splits; ++t) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (size_t)t * kMaxCols * kPartStride));
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(src + t * split_floats));
       const float wgt = wrow[t];
       O.x += v.x * wgt; O.y += v.y * wgt; O.z += v.z * wgt; O.w += v.w * wgt;
     }
-    store_out(cc, d4, O, lcol[cc], mcol[cc]);
+    store_out(c, d4, O, lcol[c], mcol[c]);
   }
   if (tid == 0) atomicExch(&p.tickets[units_idx], 0);
 }
@@ -869,61 +851,114 @@ constexpr size_t kWsHeader = 256;
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-template <int NT, int TEAM, int STAGES>
-cudaError_t launch_t(const Params& prm, dim3 grid, int rows, int k, bool pdl,
-                     cudaStream_t stream) {
-  const size_t smem = Layout<NT, TEAM, STAGES>::bytes(rows, k);
-  cudaError_t e = cudaFuncSetAttribute(sparse_decode_kernel<NT, TEAM, STAGES>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+template <int NTR, int W, int S>
+cudaLaunchConfig_t make_config(dim3 grid, size_t smem, cudaStream_t stream,
+                               cudaLaunchAttribute* attr, bool pdl, int cluster) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3((W + 1) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, sparse_decode_kernel<NT, TEAM, STAGES>, prm);
+  cfg.numAttrs = n;
+  return cfg;
+}
+
+// Whether a cluster of `cl` CTAs of this variant can be resident at all.
+template <int NTR, int W, int S>
+bool cluster_fits(int cl, size_t smem, dim3 grid) {
+  struct Entry { int dev, cl; size_t smem; bool ok; };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  if (cl < 2 || cl > kMaxCluster) return false;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry& e : cache)
+      if (e.dev == dev && e.cl == cl && e.smem == smem) return e.ok;
+  }
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = make_config<NTR, W, S>(grid, smem, 0, attr, false, cl);
+  int n = 0;
+  const bool ok = cudaOccupancyMaxActiveClusters(&n, sparse_decode_kernel<NTR, W, S>, &cfg) ==
+                      cudaSuccess && n > 0;
+  cudaGetLastError();
+  std::lock_guard<std::mutex> lock(mu);
+  cache.push_back({dev, cl, smem, ok});
+  return ok;
+}
+
+template <int NTR, int W, int S>
+cudaError_t launch_t(Params prm, dim3 grid, int R, int k, int mb, bool pdl,
+                     cudaStream_t stream) {
+  const size_t smem = Layout<NTR, W, S>::bytes(R, k, mb, prm.splits);
+  cudaError_t e = cudaFuncSetAttribute(sparse_decode_kernel<NTR, W, S>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  prm.cluster = 1;
+  if (prm.splits > 1 && cluster_fits<NTR, W, S>(prm.splits, smem, grid))
+    prm.cluster = prm.splits;
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = make_config<NTR, W, S>(grid, smem, stream, attr, pdl, prm.cluster);
+  return cudaLaunchKernelEx(&cfg, sparse_decode_kernel<NTR, W, S>, prm);
 }
 
 // Resident CTAs per SM of a variant, for split sizing.
-template <int NT, int TEAM, int STAGES>
-int resident_ctas(int rows, int k) {
-  const size_t smem = Layout<NT, TEAM, STAGES>::bytes(rows, k);
-  cudaFuncSetAttribute(sparse_decode_kernel<NT, TEAM, STAGES>,
+template <int NTR, int W, int S>
+int resident_ctas(int R, int k, int mb, int splits) {
+  const size_t smem = Layout<NTR, W, S>::bytes(R, k, mb, splits);
+  cudaFuncSetAttribute(sparse_decode_kernel<NTR, W, S>,
                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sparse_decode_kernel<NT, TEAM, STAGES>,
-                                                    kThreads, smem) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sparse_decode_kernel<NTR, W, S>,
+                                                    (W + 1) * 32, smem) != cudaSuccess) {
     cudaGetLastError();
-    n = 2;
+    n = 1;
   }
   return n < 1 ? 1 : n;
 }
 
-int cols_tiles(const Geom& g) {
-  const int cols = (g.Hq / g.Hkv) * g.R;
-  const int cta_cols = cols < kMaxCols ? cols : kMaxCols;
-  return (cta_cols + 7) / 8;
-}
+// Variant by (tiles per row, rows): decode rows use W consumers sharing the
+// chunks (S a multiple of W); verify rows W / R consumers per row.
+#ifndef QSA_DECODE_STAGES_R1
+#define QSA_DECODE_STAGES_R1 8
+#endif
+#ifndef QSA_DECODE_WARPS_R1
+#define QSA_DECODE_WARPS_R1 4
+#endif
+#define QSA_DECODE_VARIANTS(X)                                            \
+  X(1, 1, QSA_DECODE_WARPS_R1, QSA_DECODE_STAGES_R1)                      \
+  X(2, 1, QSA_DECODE_WARPS_R1, QSA_DECODE_STAGES_R1)                      \
+  X(1, 2, 4, 8) X(2, 2, 4, 8)                                             \
+  X(1, 3, 6, 8) X(2, 3, 6, 8)                                             \
+  X(1, 4, 4, 8) X(2, 4, 4, 8)                                             \
+  X(1, 5, 5, 8) X(2, 5, 5, 8)                                             \
+  X(1, 6, 6, 8) X(2, 6, 6, 8)                                             \
+  X(1, 7, 7, 8) X(2, 7, 7, 8)                                             \
+  X(1, 8, 8, 8) X(2, 8, 8, 8)
 
-int rows_per_cta(const Geom& g, int qgroups) {
+int tiles_per_row(const Geom& g) {
   const int G = g.Hq / g.Hkv;
-  return qgroups == 1 ? g.R : min(g.R, (kMaxCols + G - 1) / G + 1);
+  return G <= 8 ? 1 : 2;
 }
 
-#define QSA_DECODE_VARIANTS(X)                     \
-  X(1, QSA_DECODE_TEAM_NT1, QSA_DECODE_STAGES_NT1) \
-  X(2, 2, 4)                                       \
-  X(3, 4, 4)                                       \
-  X(4, 4, 4)
-
-int variant_resident(int nt, int rows, int k) {
-#define X(NT_, TEAM_, ST_) \
-  if (nt == NT_) return resident_ctas<NT_, TEAM_, ST_>(rows, k);
+int variant_resident(int ntr, int R, int k, int mb, int splits) {
+#define X(NTR_, R_, W_, S_) \
+  if (ntr == NTR_ && R == R_) return resident_ctas<NTR_, W_, S_>(R, k, mb, splits);
   QSA_DECODE_VARIANTS(X)
 #undef X
   return 1;
@@ -934,11 +969,11 @@ int variant_resident(int nt, int rows, int k) {
 DecodePlan plan_sparse_decode(const Geom& g, int k, int num_splits) {
   DecodePlan pl;
   const int G = g.Hq / g.Hkv;
-  pl.cols = G * g.R;
-  pl.qgroups = (pl.cols + kMaxCols - 1) / kMaxCols;
+  const int ntr = tiles_per_row(g);
+  pl.qgroups = (G + 8 * ntr - 1) / (8 * ntr);           // head slices per KV head
+  pl.cols = g.R * 8 * ntr;                               // padded columns per CTA
   const long long units = (long long)g.B * g.Hkv * pl.qgroups;
-  const int rows = rows_per_cta(g, pl.qgroups);
-  const int max_union = min(rows * k, g.MB);
+  const int max_union = min(g.R * k, g.MB);
   const int max_chunks = max(1, max_union * (g.P / kChunk));
   int splits = num_splits;
   if (splits <= 0) {
@@ -946,16 +981,27 @@ DecodePlan plan_sparse_decode(const Geom& g, int k, int num_splits) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaGetLastError();
-    const int resident = variant_resident(cols_tiles(g), rows, k);
+    const int resident = variant_resident(ntr, g.R, k, g.MB, kMaxCluster);
     const long long slots = (long long)sms * resident;
-    // Fill every resident slot once; a CTA keeps at least 2 chunks.
-    splits = (int)((slots + units - 1) / units);
+    // Enough CTAs for about four waves of work per resident slot when the
+    // problem is large, one wave when it is small; each CTA keeps at least
+    // two chunks.  Up to a portable cluster the splits merge in distributed
+    // shared memory, so prefer a power of two there.
+    const long long total_chunks = (long long)units * max_chunks;
+    long long want = slots;
+    if (total_chunks > 64 * slots) want = 4 * slots;
+    splits = (int)(want / units);
     splits = min(splits, max(1, max_chunks / 2));
     splits = max(1, min(splits, 64));
+    if (splits < 2 * kMaxCluster) {
+      int p2 = 1;
+      while (p2 * 2 <= splits && p2 * 2 <= kMaxCluster) p2 *= 2;
+      splits = p2;
+    }
   }
   pl.splits = splits;
   size_t ws = kWsHeader + align256((size_t)units * sizeof(int));
-  if (splits > 1) ws += (size_t)units * splits * kMaxCols * kPartStride * sizeof(float);
+  if (splits > 1) ws += (size_t)units * splits * pl.cols * kPartStride * sizeof(float);
   pl.ws_bytes = ws;
   return pl;
 }
@@ -980,13 +1026,15 @@ cudaError_t launch_sparse_decode(const Geom& g, const DecodePlan& plan, const vo
   prm.tickets = reinterpret_cast<int*>(ws + kWsHeader);
   prm.partials = reinterpret_cast<float*>(ws + kWsHeader + align256((size_t)units * sizeof(int)));
   prm.splits = plan.splits;
-  prm.qgroups = plan.qgroups;
-  prm.cols = plan.cols;
-  const int rows = rows_per_cta(g, plan.qgroups);
+  prm.slices = plan.qgroups;
+  prm.cluster = 1;
   dim3 grid(plan.splits, g.Hkv * plan.qgroups, g.B);
-  const int nt = cols_tiles(g);
-#define X(NT_, TEAM_, ST_) \
-  if (nt == NT_) return launch_t<NT_, TEAM_, ST_>(prm, grid, rows, k, pdl, stream);
+  const int ntr = tiles_per_row(g);
+  // With one row a stage must always belong to the same consumer (S % W == 0).
+#define X(NTR_, R_, W_, S_)                                           \
+  static_assert(R_ != 1 || (S_ % W_) == 0, "decode stages per consumer"); \
+  if (ntr == NTR_ && g.R == R_)                                        \
+    return launch_t<NTR_, W_, S_>(prm, grid, g.R, k, g.MB, pdl, stream);
   QSA_DECODE_VARIANTS(X)
 #undef X
   return cudaErrorInvalidValue;

@@ -28,6 +28,8 @@ def run_gpu(qsa, w, num_splits=0, window=None, k=None):
                           device=w["q"].device, num_splits=num_splits)
     step.run(w)
     torch.cuda.synchronize()
+    # A bounded wait that gave up leaves a status in the workspace.
+    assert qsa.qsa_workspace_status(step.workspace) == 0
     return step
 
 
