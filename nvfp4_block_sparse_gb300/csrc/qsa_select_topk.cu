@@ -31,11 +31,13 @@ select_topk_kernel(Geom g, const int32_t* __restrict__ scores, const int32_t* __
   const int r = blockIdx.x;
   const int b = r / g.R, j = r % g.R;
   pdl_wait();
+  // Dependents may start their own prologue now: it reads only step inputs,
+  // which are complete once this wait has returned.
+  pdl_trigger();
   const int n = visible_tokens(seqlens[b], g.R, j, g.MB * g.P);
   const int nb = (n + g.P - 1) / g.P;
   select_row<kThreads>(scores + (size_t)r * g.MB, nb, W, k, sel + (size_t)r * k, nsel + r,
                        smem_sel);
-  pdl_trigger();
 }
 
 }  // namespace

@@ -111,57 +111,280 @@ __device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&o)[4]) 
       : "r"(w));
 }
 
-// Shared-memory layout (bytes), shared by host sizing and the kernel.
-template <int NTR, int W, int S>
+// Shared-memory layout (bytes), shared by host sizing and the kernel.  ONE:
+// the single-row specialisation (no producer warp; W consumer warps).
+template <int NTR, int W, int S, bool ONE>
 struct Layout {
   static constexpr int kHsp = 8 * NTR;                            // padded head slice
+  static constexpr int kWarps = ONE ? W : W + 1;
+  static constexpr int kThreads = kWarps * 32;
   static constexpr int kStagesSz = S * kStageBytes;
   // After the main loop the stage region holds the consumers' partials (co,
-  // cm, cl), the CTA partial (cp) and the cluster merge weights.
+  // cm, cl) and the CTA partial (cp); the ticket merge then reuses it for its
+  // weights.  Before the main loop it holds the union's temporaries.
   static constexpr int kCoSz = W * kHsp * kHeadDim * 4;
   static constexpr int kCmSz = W * kHsp * 4;
   static constexpr int kClSz = W * kHsp * 4;
   static constexpr int kCpOff = kCoSz + kCmSz + kClSz;
   __host__ __device__ static int cp_bytes(int R) { return R * kHsp * kPartStride * 4; }
-  __host__ __device__ static int region_bytes(int R, int splits) {
-    const int combine = kCpOff + cp_bytes(R) + R * kHsp * (kMaxCluster + 2) * 4;
+  __host__ __device__ static int region_bytes(int R, int k, int splits) {
+    const int combine = kCpOff + cp_bytes(R);
     const int merge = R * kHsp * (splits + 2) * 4;
-    int r = kStagesSz > combine ? kStagesSz : combine;
-    return r > merge ? r : merge;
+    const int uni = R * k * 4 * 2;
+    int r = kStagesSz;
+    r = r > combine ? r : combine;
+    r = r > merge ? r : merge;
+    r = r > uni ? r : uni;
+    return (r + 15) & ~15;
+  }
+  // Receive buffer of the cluster merge: [splits][ceil(ncols / splits)] partials.
+  __host__ __device__ static int rb_bytes(int R, int splits) {
+    if (splits < 2 || splits > kMaxCluster) return 0;
+    const int per = (R * kHsp + splits - 1) / splits;
+    return splits * per * kPartStride * 4;
   }
   static size_t bytes(int R, int k, int mb, int splits) {
-    size_t off = (size_t)region_bytes(R, splits);
+    size_t off = (size_t)region_bytes(R, k, splits) + rb_bytes(R, splits);
     off += 2 * S * 8;                                   // full + empty barriers
     off += (size_t)R * kHsp * kHeadDim * 2;             // q (fp16)
     off += (size_t)R * kHsp * 4 * 2;                    // cq, n per column
     off += 64 * 4;                                      // scalars
-    off += (size_t)R * k * 4 * 3;                       // sel rows, union ids, pages
+    off += (size_t)R * k * 4 * 4 + 16;                  // sel rows, union ids, pages, scan
     off += mb <= kPtRowMax ? (size_t)mb * 4 : 0;        // page-table row
     return off;
   }
 };
 
-// Register budget: about 136 per thread for 8-column rows with up to four
-// consumers (three CTAs per SM), unconstrained otherwise.
-template <int NTR, int W>
-constexpr int decode_min_blocks() { return NTR == 1 ? (W <= 4 ? 3 : 1) : 1; }
+// Register budget: 128 per thread for single-row 8-column CTAs (two CTAs of
+// 256 threads or four of 128 per SM), about 136 for 8-column verify CTAs with
+// up to four row consumers, unconstrained otherwise.
+template <int NTR, int W, bool ONE>
+constexpr int decode_min_blocks() {
+  return NTR != 1 ? 1 : (ONE ? (W <= 4 ? 4 : 2) : (W <= 4 ? 3 : 1));
+}
 
-template <int NTR, int W, int S>
-__global__ void __launch_bounds__((W + 1) * 32, (decode_min_blocks<NTR, W>()))
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// One 64-token chunk (K, V and their scales at sk, contiguous) into the
+// online-softmax state of 8*NTR columns.  tok0: the chunk's first token;
+// tokens at or past nrow are masked.
+template <int NTR>
+__device__ __forceinline__ void consume_chunk(const uint8_t* __restrict__ sk, int tok0, int nrow,
+                                              const uint32_t (&qf)[NTR][16],
+                                              const float (&cq)[NTR][2], float (&m_run)[NTR][2],
+                                              float (&l_run)[NTR][2],
+                                              float (&o_acc)[8][NTR][4]) {
+  const int lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const bool partial = tok0 + kChunk > nrow;
+  const uint8_t* sv = sk + kKBytes;
+  const uint8_t* sks = sk + 2 * kKBytes;
+  const uint8_t* svs = sks + kSfBytes;
+
+  // ---- S^T = K . Q^T over the chunk's four 16-token tiles ------------
+  // Tiles go in pairs: k-steps outside and the pair inside, so
+  // consecutive MMAs feed different accumulators.
+  float sacc[4][NTR][4];
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NTR; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.f;
+#pragma unroll
+  for (int m0 = 0; m0 < 4; m0 += 2) {
+    uint32_t wA[2][4], wB[2][4], scA[2][2], scB[2][2];
+#pragma unroll
+    for (int gi = 0; gi < 2; ++gi) {
+      const int mt = m0 + gi;
+      const int rA = 16 * mt + (gid >> 1) + 4 * (gid & 1);
+      const int rB = rA + 8;
+      const uint4 kA = *reinterpret_cast<const uint4*>(sk + rA * 64 + 16 * tig);
+      const uint4 kB = *reinterpret_cast<const uint4*>(sk + rB * 64 + 16 * tig);
+      const uint32_t sA = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sks + rA * 8 + 2 * tig));
+      const uint32_t sB = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sks + rB * 8 + 2 * tig));
+      scA[gi][0] = prmt(sA, 0, 0x1010); scA[gi][1] = prmt(sA, 0, 0x3232);
+      scB[gi][0] = prmt(sB, 0, 0x1010); scB[gi][1] = prmt(sB, 0, 0x3232);
+      wA[gi][0] = kA.x; wA[gi][1] = kA.y; wA[gi][2] = kA.z; wA[gi][3] = kA.w;
+      wB[gi][0] = kB.x; wB[gi][1] = kB.y; wB[gi][2] = kB.z; wB[gi][3] = kB.w;
+    }
+#pragma unroll
+    for (int wd = 0; wd < 4; ++wd) {
+      uint32_t fa[2][4], fb[2][4];
+#pragma unroll
+      for (int gi = 0; gi < 2; ++gi) {
+        e2m1x8_to_f16x2x4(wA[gi][wd], fa[gi]);
+        e2m1x8_to_f16x2x4(wB[gi][wd], fb[gi]);
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int kk = 2 * wd + h;
+#pragma unroll
+        for (int gi = 0; gi < 2; ++gi) {
+          const uint32_t sa = scA[gi][wd >> 1], sb = scB[gi][wd >> 1];
+          uint32_t a[4];
+          a[0] = hmul2_u32(fa[gi][2 * h], sa);
+          a[2] = hmul2_u32(fa[gi][2 * h + 1], sa);
+          a[1] = hmul2_u32(fb[gi][2 * h], sb);
+          a[3] = hmul2_u32(fb[gi][2 * h + 1], sb);
+#pragma unroll
+          for (int nt = 0; nt < NTR; ++nt)
+            mma_f16_16816(sacc[m0 + gi][nt], a, qf[nt][2 * kk], qf[nt][2 * kk + 1]);
+        }
+      }
+    }
+  }
+
+  // ---- logits, causal mask, chunk max --------------------------------
+  float cmax[NTR][2];
+#pragma unroll
+  for (int nt = 0; nt < NTR; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) cmax[nt][e] = -INFINITY;
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt) {
+    const int tA = tok0 + 16 * mt + (gid >> 1) + 4 * (gid & 1);
+    const int tB = tA + 8;
+#pragma unroll
+    for (int nt = 0; nt < NTR; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float zA = sacc[mt][nt][e] * cq[nt][e];
+        float zB = sacc[mt][nt][2 + e] * cq[nt][e];
+        if (partial) {
+          if (tA >= nrow) zA = -INFINITY;
+          if (tB >= nrow) zB = -INFINITY;
+        }
+        sacc[mt][nt][e] = zA;
+        sacc[mt][nt][2 + e] = zB;
+        cmax[nt][e] = fmaxf(cmax[nt][e], fmaxf(zA, zB));
+      }
+  }
+#pragma unroll
+  for (int nt = 0; nt < NTR; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float v = cmax[nt][e];
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+      cmax[nt][e] = v;
+    }
+
+  // ---- online softmax update -----------------------------------------
+  float base[NTR][2];
+  bool rescale = false;
+#pragma unroll
+  for (int nt = 0; nt < NTR; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float mn = fmaxf(m_run[nt][e], cmax[nt][e]);
+      rescale |= (mn != m_run[nt][e]) && (m_run[nt][e] != -INFINITY);
+      base[nt][e] = (mn == -INFINITY) ? 0.f : mn;
+    }
+  if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+    for (int nt = 0; nt < NTR; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float alpha = exp2f(m_run[nt][e] - base[nt][e]);
+        l_run[nt][e] *= alpha;
+#pragma unroll
+        for (int dt = 0; dt < 8; ++dt) {
+          o_acc[dt][nt][e] *= alpha;
+          o_acc[dt][nt][2 + e] *= alpha;
+        }
+      }
+  }
+#pragma unroll
+  for (int nt = 0; nt < NTR; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) m_run[nt][e] = fmaxf(m_run[nt][e], cmax[nt][e]);
+
+  // P = exp2(z - base) -> fp16 -> transposed B fragments for P^T.
+  uint32_t pf[4][NTR][2];
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NTR; ++nt) {
+      const float p0 = exp2f(sacc[mt][nt][0] - base[nt][0]);
+      const float p1 = exp2f(sacc[mt][nt][1] - base[nt][1]);
+      const float p2 = exp2f(sacc[mt][nt][2] - base[nt][0]);
+      const float p3 = exp2f(sacc[mt][nt][3] - base[nt][1]);
+      l_run[nt][0] += p0 + p2;
+      l_run[nt][1] += p1 + p3;
+      pf[mt][nt][0] = movmatrix_trans(pack_half2(p0, p1));
+      pf[mt][nt][1] = movmatrix_trans(pack_half2(p2, p3));
+    }
+
+  // ---- O^T += V^T . P^T over the eight 16-dim tiles -------------------
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks) {
+    const int t0 = 16 * ks + tig;
+    const uint32_t sv01 = e4m3x2_to_f16x2((uint32_t)svs[t0 * 8 + gid] |
+                                          ((uint32_t)svs[(t0 + 4) * 8 + gid] << 8));
+    const uint32_t sv23 = e4m3x2_to_f16x2((uint32_t)svs[(t0 + 8) * 8 + gid] |
+                                          ((uint32_t)svs[(t0 + 12) * 8 + gid] << 8));
+#pragma unroll
+    for (int w4 = 0; w4 < 2; ++w4) {
+      // bytes [8*gid + 4*w4, +4) of the four token rows of this k-step
+      const int boff = 8 * gid + 4 * w4;
+      const uint32_t X = *reinterpret_cast<const uint32_t*>(sv + t0 * 64 + boff);
+      const uint32_t Y = *reinterpret_cast<const uint32_t*>(sv + (t0 + 4) * 64 + boff);
+      const uint32_t X2 = *reinterpret_cast<const uint32_t*>(sv + (t0 + 8) * 64 + boff);
+      const uint32_t Y2 = *reinterpret_cast<const uint32_t*>(sv + (t0 + 12) * 64 + boff);
+      const uint32_t LO = (X & 0x0F0F0F0Fu) | ((Y << 4) & 0xF0F0F0F0u);
+      const uint32_t HI = ((X >> 4) & 0x0F0F0F0Fu) | (Y & 0xF0F0F0F0u);
+      const uint32_t LO2 = (X2 & 0x0F0F0F0Fu) | ((Y2 << 4) & 0xF0F0F0F0u);
+      const uint32_t HI2 = ((X2 >> 4) & 0x0F0F0F0Fu) | (Y2 & 0xF0F0F0F0u);
+      uint32_t f0[4], f1[4], f2[4], f3[4];
+      e2m1x8_to_f16x2x4(LO, f0);
+      e2m1x8_to_f16x2x4(HI, f1);
+      e2m1x8_to_f16x2x4(LO2, f2);
+      e2m1x8_to_f16x2x4(HI2, f3);
+#pragma unroll
+      for (int bi = 0; bi < 4; ++bi) {
+        const int dt = 4 * w4 + bi;
+        uint32_t a[4];
+        a[0] = hmul2_u32(f0[bi], sv01);
+        a[1] = hmul2_u32(f1[bi], sv01);
+        a[2] = hmul2_u32(f2[bi], sv23);
+        a[3] = hmul2_u32(f3[bi], sv23);
+#pragma unroll
+        for (int nt = 0; nt < NTR; ++nt)
+          mma_f16_16816(o_acc[dt][nt], a, pf[ks][nt][0], pf[ks][nt][1]);
+      }
+    }
+  }
+}
+
+template <int NTR, int W, int S, bool ONE>
+__global__ void __launch_bounds__(Layout<NTR, W, S, ONE>::kThreads,
+                                  (decode_min_blocks<NTR, W, ONE>()))
 sparse_decode_kernel(Params p) {
-  using Lay = Layout<NTR, W, S>;
+  using Lay = Layout<NTR, W, S, ONE>;
   constexpr int kHsp = Lay::kHsp;
-  constexpr int kThreads = (W + 1) * 32;
+  constexpr int kWarps = Lay::kWarps;
+  constexpr int kThreads = Lay::kThreads;
+  static_assert(!ONE || S % W == 0, "a single-row stage must always belong to one consumer");
 
   const Geom& g = p.g;
-  const int R = g.R;
+  const int R = ONE ? 1 : g.R;
   const int G = g.Hq / g.Hkv;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
-  const bool producer = warp == W;
+  const bool producer = !ONE && warp == W;
 
-  const int s = blockIdx.x;
+  const int s = blockIdx.x;                           // KV split (= cluster rank)
   const int kvh = blockIdx.y / p.slices, slice = blockIdx.y % p.slices;
   const int b = blockIdx.z;
   const int hs0 = slice * kHsp;                       // first head of the slice
@@ -171,7 +394,9 @@ sparse_decode_kernel(Params p) {
 
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* region = smem;
-  size_t off = (size_t)Lay::region_bytes(R, p.splits);
+  size_t off = (size_t)Lay::region_bytes(R, k, p.splits);
+  float* rb = reinterpret_cast<float*>(smem + off);   // cluster merge receive buffer
+  off += (size_t)Lay::rb_bytes(R, p.splits);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + off);
   uint64_t* empty = full + S;
   off += 2 * S * 8;
@@ -185,98 +410,141 @@ sparse_decode_kernel(Params p) {
   int32_t* s_sel = reinterpret_cast<int32_t*>(smem + off);
   int32_t* s_union = s_sel + R * k;
   int32_t* s_upage = s_union + R * k;
-  int32_t* s_pt = s_upage + R * k;
+  int32_t* s_scan = s_upage + R * k;                  // [R * k + 1]
+  int32_t* s_pt = s_scan + R * k + 4;
 
-  // Consumers per stage: decode (one row) gives each chunk to one consumer;
-  // verify gives every chunk to all row consumers (each skips what its row did
-  // not select) so that stage reuse waits for all of them.
-  const int empty_count = (R == 1) ? 1 : W;
+  // full[st]: one arrival (the copy issuer) plus the copies' bytes.  empty[st]
+  // (verify only): every row consumer arrives, so stage reuse waits for all.
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], empty_count);
+      if (!ONE) mbar_init(&empty[i], W);
     }
     fence_mbar_init();
   }
+  // Cluster merge: this arrival is matched by the wait before the first
+  // remote write, which so only starts once every CTA of the cluster runs.
+  if (p.cluster > 1) cluster_arrive_relaxed();
 
-  pdl_wait();   // every global read below may depend on the preceding kernel
-
-  // ---- one round trip: selections, the request's page-table row, queries ---
+  // ---- before the dependency wait: what does not depend on the selection ---
+  // The queries, the request's page-table row and its length are step inputs
+  // that no kernel of the step writes; the selection kernel triggers its
+  // dependents only after its own wait returned, so they are complete here.
   const bool pt_in_smem = g.MB <= kPtRowMax;
+  if (pt_in_smem)
+    for (int i = tid; i < g.MB; i += kThreads) s_pt[i] = p.page_table[(size_t)b * g.MB + i];
+  const int L = p.seqlens[b];
+  const int cap = g.MB * g.P;
+  {
+    // Queries -> fp16 pre-scaled by a power of two per column, one warp per
+    // column.  The scale maps |q|max into [256, 512): exact, and keeps bf16
+    // queries of any magnitude inside fp16 range.  2^sq and its inverse are
+    // built from exponent bits (|sq| <= 126 keeps both normal).
+    constexpr int kMaxCols = (ONE ? 1 : kMaxRows) * kHsp;
+    constexpr int kQPerWarp = (kMaxCols + kWarps - 1) / kWarps;
+    uint2 raw[kQPerWarp];
+#pragma unroll
+    for (int ci = 0; ci < kQPerWarp; ++ci) {
+      const int c = warp + ci * kWarps;
+      raw[ci] = make_uint2(0u, 0u);
+      if (c < ncols && (c % kHsp) < hs) {
+        const int j = c / kHsp;
+        const int h = kvh * G + hs0 + c % kHsp;
+        raw[ci] = *reinterpret_cast<const uint2*>(
+            p.q + ((size_t)(b * R + j) * g.Hq + h) * kHeadDim + lane * 4);
+      }
+    }
+#pragma unroll
+    for (int ci = 0; ci < kQPerWarp; ++ci) {
+      const int c = warp + ci * kWarps;
+      if (c >= ncols) break;
+      const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw[ci].x);
+      const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw[ci].y);
+      const float v0 = __low2float(lo), v1 = __high2float(lo);
+      const float v2 = __low2float(hi), v3 = __high2float(hi);
+      float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+#pragma unroll
+      for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const int ebits = (int)((__float_as_uint(amax) >> 23) & 0xFF);
+      int sq = (amax > 0.f) ? 135 - ebits : 0;
+      sq = sq > 126 ? 126 : (sq < -126 ? -126 : sq);
+      const float up = __uint_as_float((uint32_t)(sq + 127) << 23);
+      const float down = __uint_as_float((uint32_t)(127 - sq) << 23);
+      __half2* dst = reinterpret_cast<__half2*>(qs + c * kHeadDim + lane * 4);
+      dst[0] = __floats2half2_rn(v0 * up, v1 * up);
+      dst[1] = __floats2half2_rn(v2 * up, v3 * up);
+      if (lane == 0) {
+        col_cq[c] = ((c % kHsp) < hs) ? p.k_scale * p.sm_scale * kLog2e * down : 0.f;
+        col_n[c] = visible_tokens(L, R, c / kHsp, cap);
+      }
+    }
+  }
+
+  pdl_wait();   // the selections come from the preceding kernel
+
   for (int i = tid; i < R * k; i += kThreads) {
     const int v = p.sel[(size_t)b * R * k + i];
     s_sel[i] = (v >= 0 && v < g.MB) ? v : -1;
   }
-  if (pt_in_smem)
-    for (int i = tid; i < g.MB; i += kThreads) s_pt[i] = p.page_table[(size_t)b * g.MB + i];
-  constexpr int kQPerWarp = (8 * kHsp + (W + 1) - 1) / (W + 1);   // columns per warp, R <= 8
-  float qv[kQPerWarp][4];
-#pragma unroll
-  for (int ci = 0; ci < kQPerWarp; ++ci) {
-    const int c = warp + ci * (W + 1);
-    qv[ci][0] = qv[ci][1] = qv[ci][2] = qv[ci][3] = 0.f;
-    if (c < ncols) {
-      const int j = c / kHsp, hh = c % kHsp;
-      if (hh < hs) {
-        const int h = kvh * G + hs0 + hh;
-        const __nv_bfloat16* src = p.q + ((size_t)(b * R + j) * g.Hq + h) * kHeadDim + lane * 4;
-        const uint2 raw = *reinterpret_cast<const uint2*>(src);
-        const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-        const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-        qv[ci][0] = __low2float(lo); qv[ci][1] = __high2float(lo);
-        qv[ci][2] = __low2float(hi); qv[ci][3] = __high2float(hi);
-      }
-    }
-  }
-  const int L = p.seqlens[b];
   __syncthreads();
 
-  // ---- union of the rows' selections (first occurrence, valid pages) -------
+  // ---- union of the rows' selections: distinct valid pages, ascending ------
+  // Entry e = (row jj, block beta) is kept when no earlier row holds beta and
+  // its page is valid; its mask marks every row that holds beta.  Rows are
+  // ascending (padding last), so a kept entry's union position is the number
+  // of kept entries, over all rows, with smaller blocks: per row, a prefix
+  // count of kept entries up to the binary-search bound.  The union is thus
+  // in block order and each row's pages spread across the whole of it.
+  // Each thread takes a contiguous run of entries; flags and pages wait in
+  // the (still idle) stage region.
   {
     const int ne = R * k;
-    constexpr int kPer = (kMaxUnion + kThreads - 1) / kThreads;
-    const int per = (ne + kThreads - 1) / kThreads;   // <= kPer
+    const int per = (ne + kThreads - 1) / kThreads;
     const int e_lo = min(ne, tid * per), e_hi = min(ne, e_lo + per);
-    int flags[kPer];
-    int pages[kPer];
+    int32_t* t_flag = reinterpret_cast<int32_t*>(region);   // [ne]
+    int32_t* t_page = t_flag + ne;                          // [ne]
+    // lower bound of beta in row j2 (padding counts as +inf)
+    auto lower = [&](int j2, int beta) {
+      const int32_t* row = s_sel + j2 * k;
+      int lo2 = 0, hi2 = k;
+      while (lo2 < hi2) {
+        const int mid = (lo2 + hi2) >> 1;
+        const int x = row[mid] < 0 ? 0x7FFFFFFF : row[mid];
+        if (x < beta) lo2 = mid + 1; else hi2 = mid;
+      }
+      return lo2;
+    };
+    const int jj0 = e_lo / k, ii0 = e_lo - jj0 * k;
     int keep_cnt = 0;
-#pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-      const int e = e_lo + q;
-      int flag = 0;
-      pages[q] = 0;
-      if (e < e_hi) {
-        const int beta = s_sel[e];
-        if (beta >= 0) {
-          const int jj = e / k;
-          bool first = true;
-          int mask = 1 << jj;
+    for (int e = e_lo, jj = jj0, ii = ii0; e < e_hi; ++e) {
+      int flag = 0, page = 0;
+      const int beta = s_sel[e];
+      if (beta >= 0) {
+        bool first = true;
+        int mask = 1 << jj;
+        if (!ONE) {
           for (int j2 = 0; j2 < R; ++j2) {
             if (j2 == jj) continue;
-            const int32_t* row = s_sel + j2 * k;
-            int lo2 = 0, hi2 = k;
-            while (lo2 < hi2) {
-              const int mid = (lo2 + hi2) >> 1;
-              const int x = row[mid] < 0 ? 0x7FFFFFFF : row[mid];
-              if (x < beta) lo2 = mid + 1; else hi2 = mid;
-            }
-            if (lo2 < k && row[lo2] == beta) {
+            const int lb = lower(j2, beta);
+            if (lb < k && s_sel[j2 * k + lb] == beta) {
               mask |= 1 << j2;
               if (j2 < jj) first = false;
             }
           }
-          if (first) {
-            const int page = pt_in_smem ? s_pt[beta] : p.page_table[(size_t)b * g.MB + beta];
-            if (page >= 0 && page < g.NP) {
-              flag = 0x100 | (mask & 0xFF);
-              pages[q] = page;
-              ++keep_cnt;
-            }
+        }
+        if (first) {
+          page = pt_in_smem ? s_pt[beta] : p.page_table[(size_t)b * g.MB + beta];
+          if (page >= 0 && page < g.NP) {
+            flag = 0x100 | (mask & 0xFF);
+            ++keep_cnt;
           }
         }
       }
-      flags[q] = flag;
+      t_flag[e] = flag;
+      t_page[e] = page;
+      if (++ii == k) { ii = 0; ++jj; }
     }
+    // exclusive prefix of kept entries over the flat entry order
     int x = keep_cnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -285,38 +553,44 @@ sparse_decode_kernel(Params p) {
     }
     if (lane == 31) misc[warp] = x;
     __syncthreads();
-    int base = 0, tot = 0;
-    for (int w = 0; w <= W; ++w) {
-      base += (w < warp) ? misc[w] : 0;
-      tot += misc[w];
+    int run = x - keep_cnt;
+    for (int w = 0; w < warp; ++w) run += misc[w];
+    for (int e = e_lo; e < e_hi; ++e) {
+      s_scan[e] = run;
+      run += t_flag[e] ? 1 : 0;
     }
-    int pos = base + x - keep_cnt;
-#pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-      if (!flags[q]) continue;
-      s_union[pos] = s_sel[e_lo + q] | ((flags[q] & 0xFF) << 24);
-      s_upage[pos] = pages[q];
-      ++pos;
+    if (tid == kThreads - 1) s_scan[ne] = run;   // the last thread's run is the total
+    __syncthreads();
+    for (int e = e_lo, jj = jj0, ii = ii0; e < e_hi; ++e) {
+      const int flag = t_flag[e];
+      if (flag) {
+        const int beta = s_sel[e];
+        int pos = s_scan[e] - s_scan[jj * k];
+        if (!ONE)
+          for (int j2 = 0; j2 < R; ++j2)
+            if (j2 != jj) pos += s_scan[j2 * k + lower(j2, beta)] - s_scan[j2 * k];
+        s_union[pos] = beta | ((flag & 0xFF) << 24);
+        s_upage[pos] = t_page[e];
+      }
+      if (++ii == k) { ii = 0; ++jj; }
     }
-    if (tid == 0) misc[16] = tot;
   }
   __syncthreads();
+  pdl_trigger();
 
-  const int U = misc[16];
-  const int cpp = g.P / kChunk;               // chunks per page
-  const int C = U * cpp;
-  const int per_split = (C + p.splits - 1) / p.splits;
-  const int ch_lo = min(C, s * per_split);
-  const int n_ch = min(C, ch_lo + per_split) - ch_lo;
+  const int U = s_scan[R * k];
+  const int csh = (g.P == 2 * kChunk) ? 1 : 0;  // chunks per page: 1 << csh
+  const int C = U << csh;
+  // Split s takes union chunks s, s + splits, ... so every split gets an even
+  // share of every row's pages.
+  const int n_ch = (C > s) ? (C - s + p.splits - 1) / p.splits : 0;
 
-  // ---- producer: stream this split's chunks through the stages -------------
-  // The first S chunks need no stage to drain, so they go out before the
-  // prologue barrier; the rest wait for consumers and so are issued after it.
-  const uint64_t pol = producer ? policy_evict_first() : 0ull;
+  const uint64_t pol = (ONE || producer) ? policy_evict_first() : 0ull;
+  // Chunk i of this split into stage i % S (one lane).
   auto issue = [&](int i) {
     const int st = i % S;
-    const int c = ch_lo + i;
-    const int u = c / cpp, sub = c % cpp;
+    const int c = s + i * p.splits;
+    const int u = c >> csh, sub = c & csh;
     const size_t row0 = ((size_t)s_upage[u] * g.Hkv + kvh) * g.P + (size_t)sub * kChunk;
     uint8_t* dst = region + st * kStageBytes;
     mbar_arrive_expect_tx(&full[st], kStageBytes);
@@ -326,49 +600,20 @@ sparse_decode_kernel(Params p) {
     bulk_g2s(dst + 2 * kKBytes + kSfBytes, p.v_sf + row0 * (kHeadDim / 16), kSfBytes, &full[st],
              pol);
   };
-  const int n_pre = min(n_ch, S);
-  if (producer && lane == 0)
-    for (int i = 0; i < n_pre; ++i) issue(i);
 
-  // ---- queries: pre-scaled fp16 and per-column constants -------------------
-  const int cap = g.MB * g.P;
-#pragma unroll
-  for (int ci = 0; ci < kQPerWarp; ++ci) {
-    const int c = warp + ci * (W + 1);
-    if (c >= ncols) break;
-    const float* v = qv[ci];
-    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-#pragma unroll
-    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    // Power-of-two pre-scale mapping |q|max into [256, 512): exact, and keeps
-    // bf16 queries of any magnitude inside fp16 range.  The scale 2^sq and its
-    // inverse are built from exponent bits (|sq| <= 126 keeps both normal).
-    const int ebits = (int)((__float_as_uint(amax) >> 23) & 0xFF);
-    int sq = (amax > 0.f) ? 135 - ebits : 0;
-    sq = sq > 126 ? 126 : (sq < -126 ? -126 : sq);
-    const float up = __uint_as_float((uint32_t)(sq + 127) << 23);
-    const float down = __uint_as_float((uint32_t)(127 - sq) << 23);
-    __half2* dst = reinterpret_cast<__half2*>(qs + c * kHeadDim + lane * 4);
-    dst[0] = __floats2half2_rn(v[0] * up, v[1] * up);
-    dst[1] = __floats2half2_rn(v[2] * up, v[3] * up);
-    if (lane == 0) {
-      const int j = c / kHsp;
-      col_cq[c] = ((c % kHsp) < hs) ? p.k_scale * p.sm_scale * kLog2e * down : 0.f;
-      col_n[c] = visible_tokens(L, R, j, cap);
-    }
-  }
-  __syncthreads();
-  pdl_trigger();
-
+  // ---- producer (verify): stream this split's chunks through the stages ----
   if (producer) {
     if (lane == 0) {
-      int dead = 0, issued = n_pre;
-      for (int i = n_pre; i < n_ch; ++i) {
-        if (!wait_bounded(&empty[i % S], ((i / S) - 1) & 1)) {
-          dead = 1;
-          break;
+      fence_proxy_async_smem();   // after the union's temporaries in the stage region
+      int dead = 0, issued = 0;
+      for (int i = 0; i < n_ch; ++i) {
+        if (i >= S) {
+          if (!wait_bounded(&empty[i % S], ((i / S) - 1) & 1)) {
+            dead = 1;
+            break;
+          }
+          fence_proxy_async_smem();   // consumers' reads of the stage come first
         }
-        fence_proxy_async_smem();   // consumers' reads of the stage come first
         issue(i);
         issued = i + 1;
       }
@@ -382,12 +627,14 @@ sparse_decode_kernel(Params p) {
   }
 
   // ---- consumers -------------------------------------------------------------
-  // Decode: every consumer on row 0, chunks round-robin.  Verify: consumer w
-  // owns row w % R and, of that row's chunks, those with index = w / R modulo
-  // the W / R consumers per row.
-  const int gper = (R == 1) ? W : W / R;        // consumers per row
-  const int jw = (R == 1) ? 0 : warp % R;       // the row this warp owns
-  const int gw = (R == 1) ? 0 : warp / R;
+  // Decode: consumer w takes chunks w, w + W, ... and itself refills the stage
+  // it has just read with its chunk S further on (S % W == 0 keeps a stage
+  // with one consumer), so no warp waits on another.  Verify: consumer w owns
+  // row w % R and, of the chunks of this split that its row selected, every
+  // (W / R)-th starting at the (w / R)-th.
+  const int gper = ONE ? W : W / R;             // consumers per row
+  const int jw = ONE ? 0 : warp % R;            // the row this warp owns
+  const int gw = ONE ? 0 : warp / R;
   float m_run[NTR][2], l_run[NTR][2];
   float o_acc[8][NTR][4];
 #pragma unroll
@@ -401,7 +648,14 @@ sparse_decode_kernel(Params p) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) o_acc[dt][nt][e] = 0.f;
 
-  if (!producer && jw < R) {
+  // The stage region held the union's temporaries (generic-proxy writes):
+  // order them before the first copies into it.
+  if (ONE && lane == 0) {
+    fence_proxy_async_smem();
+    for (int i = warp; i < min(S, n_ch); i += W) issue(i);
+  }
+
+  if (!producer) {
     const int cbase = jw * kHsp;
     float cq[NTR][2];
 #pragma unroll
@@ -423,206 +677,50 @@ sparse_decode_kernel(Params p) {
       }
     }
 
-    bool dead = false;
-    const int i0 = (R == 1) ? warp : 0;
-    const int di = (R == 1) ? W : 1;
-    for (int i = i0; i < n_ch; i += di) {
-      const int st = i % S;
-      const int c = ch_lo + i;
-      const int u = c / cpp, sub = c % cpp;
-      const int ue = s_union[u];
-      const bool mine = (R == 1) || (((ue >> (24 + jw)) & 1) && (i % gper) == gw);
-      if (!dead && !wait_bounded(&full[st], (i / S) & 1)) {
-        dead = true;
-        if (lane == 0) atomicExch(p.status, kStatusWaitTimeout);
-      }
-      if (mine && !dead) {
-        const int beta = ue & 0xFFFFFF;
-        const int tok0 = beta * g.P + sub * kChunk;
-        const bool partial = tok0 + kChunk > nrow;
-        const uint8_t* sk = region + st * kStageBytes;
-        const uint8_t* sv = sk + kKBytes;
-        const uint8_t* sks = sk + 2 * kKBytes;
-        const uint8_t* svs = sks + kSfBytes;
-
-        // ---- S^T = K . Q^T over the chunk's four 16-token tiles ------------
-        // Tiles go in pairs: k-steps outside and the pair inside, so
-        // consecutive MMAs feed different accumulators.
-        float sacc[4][NTR][4];
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-          for (int nt = 0; nt < NTR; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.f;
-#pragma unroll
-        for (int m0 = 0; m0 < 4; m0 += 2) {
-          uint32_t wA[2][4], wB[2][4], scA[2][2], scB[2][2];
-#pragma unroll
-          for (int gi = 0; gi < 2; ++gi) {
-            const int mt = m0 + gi;
-            const int rA = 16 * mt + (gid >> 1) + 4 * (gid & 1);
-            const int rB = rA + 8;
-            const uint4 kA = *reinterpret_cast<const uint4*>(sk + rA * 64 + 16 * tig);
-            const uint4 kB = *reinterpret_cast<const uint4*>(sk + rB * 64 + 16 * tig);
-            const uint32_t sA = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sks + rA * 8 + 2 * tig));
-            const uint32_t sB = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sks + rB * 8 + 2 * tig));
-            scA[gi][0] = prmt(sA, 0, 0x1010); scA[gi][1] = prmt(sA, 0, 0x3232);
-            scB[gi][0] = prmt(sB, 0, 0x1010); scB[gi][1] = prmt(sB, 0, 0x3232);
-            wA[gi][0] = kA.x; wA[gi][1] = kA.y; wA[gi][2] = kA.z; wA[gi][3] = kA.w;
-            wB[gi][0] = kB.x; wB[gi][1] = kB.y; wB[gi][2] = kB.z; wB[gi][3] = kB.w;
-          }
-#pragma unroll
-          for (int wd = 0; wd < 4; ++wd) {
-            uint32_t fa[2][4], fb[2][4];
-#pragma unroll
-            for (int gi = 0; gi < 2; ++gi) {
-              e2m1x8_to_f16x2x4(wA[gi][wd], fa[gi]);
-              e2m1x8_to_f16x2x4(wB[gi][wd], fb[gi]);
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int kk = 2 * wd + h;
-#pragma unroll
-              for (int gi = 0; gi < 2; ++gi) {
-                const uint32_t sa = scA[gi][wd >> 1], sb = scB[gi][wd >> 1];
-                uint32_t a[4];
-                a[0] = hmul2_u32(fa[gi][2 * h], sa);
-                a[2] = hmul2_u32(fa[gi][2 * h + 1], sa);
-                a[1] = hmul2_u32(fb[gi][2 * h], sb);
-                a[3] = hmul2_u32(fb[gi][2 * h + 1], sb);
-#pragma unroll
-                for (int nt = 0; nt < NTR; ++nt)
-                  mma_f16_16816(sacc[m0 + gi][nt], a, qf[nt][2 * kk], qf[nt][2 * kk + 1]);
-              }
-            }
-          }
+    if (ONE) {
+      int i_dead = -1;
+      for (int i = warp; i < n_ch; i += W) {
+        const int st = i % S;
+        if (!wait_bounded(&full[st], (i / S) & 1)) {
+          i_dead = i;
+          if (lane == 0) atomicExch(p.status, kStatusWaitTimeout);
+          break;
         }
-
-        // ---- logits, causal mask, chunk max --------------------------------
-        float cmax[NTR][2];
-#pragma unroll
-        for (int nt = 0; nt < NTR; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) cmax[nt][e] = -INFINITY;
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-          const int tA = tok0 + 16 * mt + (gid >> 1) + 4 * (gid & 1);
-          const int tB = tA + 8;
-#pragma unroll
-          for (int nt = 0; nt < NTR; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              float zA = sacc[mt][nt][e] * cq[nt][e];
-              float zB = sacc[mt][nt][2 + e] * cq[nt][e];
-              if (partial) {
-                if (tA >= nrow) zA = -INFINITY;
-                if (tB >= nrow) zB = -INFINITY;
-              }
-              sacc[mt][nt][e] = zA;
-              sacc[mt][nt][2 + e] = zB;
-              cmax[nt][e] = fmaxf(cmax[nt][e], fmaxf(zA, zB));
-            }
-        }
-#pragma unroll
-        for (int nt = 0; nt < NTR; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float v = cmax[nt][e];
-            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
-            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-            cmax[nt][e] = v;
-          }
-
-        // ---- online softmax update -----------------------------------------
-        float base[NTR][2];
-        bool rescale = false;
-#pragma unroll
-        for (int nt = 0; nt < NTR; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float mn = fmaxf(m_run[nt][e], cmax[nt][e]);
-            rescale |= (mn != m_run[nt][e]) && (m_run[nt][e] != -INFINITY);
-            base[nt][e] = (mn == -INFINITY) ? 0.f : mn;
-          }
-        if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-          for (int nt = 0; nt < NTR; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float alpha = exp2f(m_run[nt][e] - base[nt][e]);
-              l_run[nt][e] *= alpha;
-#pragma unroll
-              for (int dt = 0; dt < 8; ++dt) {
-                o_acc[dt][nt][e] *= alpha;
-                o_acc[dt][nt][2 + e] *= alpha;
-              }
-            }
-        }
-#pragma unroll
-        for (int nt = 0; nt < NTR; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) m_run[nt][e] = fmaxf(m_run[nt][e], cmax[nt][e]);
-
-        // P = exp2(z - base) -> fp16 -> transposed B fragments for P^T.
-        uint32_t pf[4][NTR][2];
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-          for (int nt = 0; nt < NTR; ++nt) {
-            const float p0 = exp2f(sacc[mt][nt][0] - base[nt][0]);
-            const float p1 = exp2f(sacc[mt][nt][1] - base[nt][1]);
-            const float p2 = exp2f(sacc[mt][nt][2] - base[nt][0]);
-            const float p3 = exp2f(sacc[mt][nt][3] - base[nt][1]);
-            l_run[nt][0] += p0 + p2;
-            l_run[nt][1] += p1 + p3;
-            pf[mt][nt][0] = movmatrix_trans(pack_half2(p0, p1));
-            pf[mt][nt][1] = movmatrix_trans(pack_half2(p2, p3));
-          }
-
-        // ---- O^T += V^T . P^T over the eight 16-dim tiles -------------------
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const int t0 = 16 * ks + tig;
-          const uint32_t sv01 = e4m3x2_to_f16x2((uint32_t)svs[t0 * 8 + gid] |
-                                                ((uint32_t)svs[(t0 + 4) * 8 + gid] << 8));
-          const uint32_t sv23 = e4m3x2_to_f16x2((uint32_t)svs[(t0 + 8) * 8 + gid] |
-                                                ((uint32_t)svs[(t0 + 12) * 8 + gid] << 8));
-#pragma unroll
-          for (int w4 = 0; w4 < 2; ++w4) {
-            // bytes [8*gid + 4*w4, +4) of the four token rows of this k-step
-            const int boff = 8 * gid + 4 * w4;
-            const uint32_t X = *reinterpret_cast<const uint32_t*>(sv + t0 * 64 + boff);
-            const uint32_t Y = *reinterpret_cast<const uint32_t*>(sv + (t0 + 4) * 64 + boff);
-            const uint32_t X2 = *reinterpret_cast<const uint32_t*>(sv + (t0 + 8) * 64 + boff);
-            const uint32_t Y2 = *reinterpret_cast<const uint32_t*>(sv + (t0 + 12) * 64 + boff);
-            const uint32_t LO = (X & 0x0F0F0F0Fu) | ((Y << 4) & 0xF0F0F0F0u);
-            const uint32_t HI = ((X >> 4) & 0x0F0F0F0Fu) | (Y & 0xF0F0F0F0u);
-            const uint32_t LO2 = (X2 & 0x0F0F0F0Fu) | ((Y2 << 4) & 0xF0F0F0F0u);
-            const uint32_t HI2 = ((X2 >> 4) & 0x0F0F0F0Fu) | (Y2 & 0xF0F0F0F0u);
-            uint32_t f0[4], f1[4], f2[4], f3[4];
-            e2m1x8_to_f16x2x4(LO, f0);
-            e2m1x8_to_f16x2x4(HI, f1);
-            e2m1x8_to_f16x2x4(LO2, f2);
-            e2m1x8_to_f16x2x4(HI2, f3);
-#pragma unroll
-            for (int bi = 0; bi < 4; ++bi) {
-              const int dt = 4 * w4 + bi;
-              uint32_t a[4];
-              a[0] = hmul2_u32(f0[bi], sv01);
-              a[1] = hmul2_u32(f1[bi], sv01);
-              a[2] = hmul2_u32(f2[bi], sv23);
-              a[3] = hmul2_u32(f3[bi], sv23);
-#pragma unroll
-              for (int nt = 0; nt < NTR; ++nt)
-                mma_f16_16816(o_acc[dt][nt], a, pf[ks][nt][0], pf[ks][nt][1]);
-            }
-          }
+        const int c = s + i * p.splits;
+        const int beta = s_union[c >> csh] & 0xFFFFFF;
+        consume_chunk<NTR>(region + st * kStageBytes, beta * g.P + (c & csh) * kChunk, nrow, qf,
+                           cq, m_run, l_run, o_acc);
+        __syncwarp();   // every lane's reads of the stage are done
+        if (lane == 0 && i + S < n_ch) {
+          fence_proxy_async_smem();
+          issue(i + S);
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
+      // After a wait gave up, let this warp's copies still in flight land
+      // before the stage memory is reused.
+      if (i_dead >= 0 && lane == 0)
+        for (int i = i_dead; i < min(n_ch, i_dead + S); i += W)
+          if (!wait_bounded(&full[i % S], (i / S) & 1)) break;
+    } else {
+      bool dead = false;
+      int rc = 0;                               // this row's chunks seen so far
+      for (int i = 0; i < n_ch; ++i) {
+        const int st = i % S;
+        const int c = s + i * p.splits;
+        const int ue = s_union[c >> csh];
+        const bool rowbit = (ue >> (24 + jw)) & 1;
+        const bool mine = rowbit && (rc % gper) == gw;
+        rc += rowbit ? 1 : 0;
+        if (!dead && !wait_bounded(&full[st], (i / S) & 1)) {
+          dead = true;
+          if (lane == 0) atomicExch(p.status, kStatusWaitTimeout);
+        }
+        if (mine && !dead)
+          consume_chunk<NTR>(region + st * kStageBytes, (ue & 0xFFFFFF) * g.P + (c & csh) * kChunk,
+                             nrow, qf, cq, m_run, l_run, o_acc);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+      }
     }
   }
 
@@ -669,33 +767,6 @@ sparse_decode_kernel(Params p) {
   }
   __syncthreads();
 
-  // CTA partial per column (j, hh): m (log2 domain, -inf when empty), l, O,
-  // merged over the consumers of row j (warps j, j + R, ...).
-  const int wstep = (R == 1) ? 1 : R;
-  for (int idx = tid; idx < ncols * (kHeadDim / 4); idx += kThreads) {
-    const int c = idx / (kHeadDim / 4), d4 = (idx % (kHeadDim / 4)) * 4;
-    const int j = c / kHsp, cc = c % kHsp;
-    const int w_lo = (R == 1) ? 0 : j;
-    float mx = -INFINITY;
-    for (int w = w_lo; w < W; w += wstep) mx = fmaxf(mx, cm[w * kHsp + cc]);
-    const float M = (mx == -INFINITY) ? 0.f : mx;
-    float Lsum = 0.f;
-    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int w = w_lo; w < W; w += wstep) {
-      const float wt = exp2f(cm[w * kHsp + cc] - M);
-      Lsum += cl[w * kHsp + cc] * wt;
-      const float4 v = *reinterpret_cast<const float4*>(co + ((size_t)w * kHsp + cc) * kHeadDim + d4);
-      O.x += v.x * wt; O.y += v.y * wt; O.z += v.z * wt; O.w += v.w * wt;
-    }
-    float* pc = cp + (size_t)c * kPartStride;
-    *reinterpret_cast<float4*>(pc + 4 + d4) = O;
-    if (d4 == 0) {
-      pc[0] = (Lsum > 0.f) ? M : -INFINITY;
-      pc[1] = Lsum;
-    }
-  }
-  __syncthreads();
-
   auto store_out = [&](int c, int d4, float4 O, float Lsum, float M) {
     const int j = c / kHsp, hh = c % kHsp;
     if (hh >= hs) return;   // padding column
@@ -711,67 +782,91 @@ sparse_decode_kernel(Params p) {
     if (d4 == 0) p.lse[orow] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
   };
 
-  if (p.splits == 1) {
-    for (int idx = tid; idx < ncols * (kHeadDim / 4); idx += kThreads) {
-      const int c = idx / (kHeadDim / 4), d4 = (idx % (kHeadDim / 4)) * 4;
-      const float* pc = cp + (size_t)c * kPartStride;
-      store_out(c, d4, *reinterpret_cast<const float4*>(pc + 4 + d4), pc[1], pc[0]);
+  // CTA partial per column (j, hh): m (log2 domain, -inf when empty), l, O,
+  // merged over the consumers of row j (warps j, j + R, ...).  With one split
+  // it is the result.
+  for (int idx = tid; idx < ncols * (kHeadDim / 4); idx += kThreads) {
+    const int c = idx / (kHeadDim / 4), d4 = (idx % (kHeadDim / 4)) * 4;
+    const int j = c / kHsp, cc = c % kHsp;
+    float mv[W];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      mv[w] = (ONE || w % R == j) ? cm[w * kHsp + cc] : -INFINITY;
+      mx = fmaxf(mx, mv[w]);
     }
-    return;
+    const float M = (mx == -INFINITY) ? 0.f : mx;
+    float Lsum = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      if (ONE || w % R == j) {
+        const float wt = exp2f(mv[w] - M);
+        Lsum += cl[w * kHsp + cc] * wt;
+        const float4 v =
+            *reinterpret_cast<const float4*>(co + ((size_t)w * kHsp + cc) * kHeadDim + d4);
+        O.x += v.x * wt; O.y += v.y * wt; O.z += v.z * wt; O.w += v.w * wt;
+      }
+    }
+    const float Mc = (Lsum > 0.f) ? M : -INFINITY;
+    if (p.splits == 1) {
+      store_out(c, d4, O, Lsum, Mc);
+    } else {
+      float* pc = cp + (size_t)c * kPartStride;
+      *reinterpret_cast<float4*>(pc + 4 + d4) = O;
+      if (d4 == 0) {
+        pc[0] = Mc;
+        pc[1] = Lsum;
+      }
+    }
   }
+  if (p.splits == 1) return;
+  __syncthreads();
 
   if (p.cluster > 1) {
-    // The splits of this unit form one thread-block cluster: merge their
-    // partials through distributed shared memory, each CTA finishing a slice
-    // of the (column, dim) items.  Split order is fixed (deterministic).
+    // The splits of this unit form one thread-block cluster.  Column c is
+    // merged by rank c % CL: every CTA pushes its partial of c into that
+    // rank's receive buffer (slot [split][c / CL]), one cluster barrier
+    // publishes the writes, and each rank merges its columns from local
+    // shared memory in split order (deterministic).
     cg::cluster_group cluster = cg::this_cluster();
     const int CL = p.cluster;
-    const int crank = (int)cluster.block_rank();
-    float* wt = cp + (size_t)ncols * kPartStride;                    // [ncols][kMaxCluster]
-    float* wM = wt + ncols * kMaxCluster;
-    float* wL = wM + ncols;
-    cluster.sync();   // every CTA's partial is in its shared memory
-    for (int c = tid; c < ncols; c += kThreads) {
+    const int per = (ncols + CL - 1) / CL;
+    cluster_wait_acquire();   // pairs with the arrival at the start
+    for (int idx = tid; idx < ncols * (kPartStride / 4); idx += kThreads) {
+      const int c = idx / (kPartStride / 4), w4 = (idx % (kPartStride / 4)) * 4;
+      float* dst = cluster.map_shared_rank(rb, c % CL) +
+                   ((size_t)s * per + c / CL) * kPartStride + w4;
+      *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(cp + c * kPartStride + w4);
+    }
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    for (int idx = tid; idx < per * (kHeadDim / 4); idx += kThreads) {
+      const int q = idx / (kHeadDim / 4), d4 = (idx % (kHeadDim / 4)) * 4;
+      const int c = q * CL + s;
+      if (c >= ncols) continue;
+      float mr[kMaxCluster];
       float mx = -INFINITY;
-      float mr[kMaxCluster], lr[kMaxCluster];
 #pragma unroll
       for (int r2 = 0; r2 < kMaxCluster; ++r2) {
-        if (r2 < CL) {
-          const float* rp = cluster.map_shared_rank(cp, r2) + (size_t)c * kPartStride;
-          mr[r2] = rp[0];
-          lr[r2] = rp[1];
-          mx = fmaxf(mx, mr[r2]);
-        }
+        mr[r2] = (r2 < CL) ? rb[((size_t)r2 * per + q) * kPartStride] : -INFINITY;
+        mx = fmaxf(mx, mr[r2]);
       }
       const float M = (mx == -INFINITY) ? 0.f : mx;
       float Lsum = 0.f;
-#pragma unroll
-      for (int r2 = 0; r2 < kMaxCluster; ++r2) {
-        if (r2 < CL) {
-          const float w = exp2f(mr[r2] - M);
-          wt[c * kMaxCluster + r2] = w;
-          Lsum += lr[r2] * w;
-        }
-      }
-      wM[c] = M;
-      wL[c] = Lsum;
-    }
-    __syncthreads();
-    for (int idx = crank * kThreads + tid; idx < ncols * (kHeadDim / 4); idx += CL * kThreads) {
-      const int c = idx / (kHeadDim / 4), d4 = (idx % (kHeadDim / 4)) * 4;
       float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int r2 = 0; r2 < kMaxCluster; ++r2) {
         if (r2 < CL) {
-          const float4 v = *reinterpret_cast<const float4*>(
-              cluster.map_shared_rank(cp, r2) + (size_t)c * kPartStride + 4 + d4);
-          const float w = wt[c * kMaxCluster + r2];
+          const float* pr = rb + ((size_t)r2 * per + q) * kPartStride;
+          const float w = exp2f(mr[r2] - M);
+          Lsum += pr[1] * w;
+          const float4 v = *reinterpret_cast<const float4*>(pr + 4 + d4);
           O.x += v.x * w; O.y += v.y * w; O.z += v.z * w; O.w += v.w * w;
         }
       }
-      store_out(c, d4, O, wL[c], wM[c]);
+      store_out(c, d4, O, Lsum, M);
     }
-    cluster.sync();   // no CTA leaves while its partial may still be read
     return;
   }
 
@@ -798,7 +893,7 @@ sparse_decode_kernel(Params p) {
   float* wsplit = reinterpret_cast<float*>(region);                 // [ncols][splits]
   float* lcol = wsplit + (size_t)ncols * p.splits;                  // [ncols]
   float* mcol = lcol + ncols;                                       // [ncols]
-  for (int c = warp; c < ncols; c += W + 1) {
+  for (int c = warp; c < ncols; c += kWarps) {
     float mloc = -INFINITY;
     for (int t = lane; t < p.splits; t += 32)
       mloc = fmaxf(mloc, __ldcg(parts + t * split_floats + (size_t)c * kPartStride));
@@ -851,12 +946,12 @@ constexpr size_t kWsHeader = 256;
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-template <int NTR, int W, int S>
+template <int NTR, int W, int S, bool ONE>
 cudaLaunchConfig_t make_config(dim3 grid, size_t smem, cudaStream_t stream,
                                cudaLaunchAttribute* attr, bool pdl, int cluster) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3((W + 1) * 32);
+  cfg.blockDim = dim3(Layout<NTR, W, S, ONE>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   int n = 0;
@@ -878,7 +973,7 @@ cudaLaunchConfig_t make_config(dim3 grid, size_t smem, cudaStream_t stream,
 }
 
 // Whether a cluster of `cl` CTAs of this variant can be resident at all.
-template <int NTR, int W, int S>
+template <int NTR, int W, int S, bool ONE>
 bool cluster_fits(int cl, size_t smem, dim3 grid) {
   struct Entry { int dev, cl; size_t smem; bool ok; };
   static std::mutex mu;
@@ -892,40 +987,42 @@ bool cluster_fits(int cl, size_t smem, dim3 grid) {
       if (e.dev == dev && e.cl == cl && e.smem == smem) return e.ok;
   }
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = make_config<NTR, W, S>(grid, smem, 0, attr, false, cl);
+  cudaLaunchConfig_t cfg = make_config<NTR, W, S, ONE>(grid, smem, 0, attr, false, cl);
   int n = 0;
-  const bool ok = cudaOccupancyMaxActiveClusters(&n, sparse_decode_kernel<NTR, W, S>, &cfg) ==
-                      cudaSuccess && n > 0;
+  const bool ok = cudaOccupancyMaxActiveClusters(&n, sparse_decode_kernel<NTR, W, S, ONE>,
+                                                 &cfg) == cudaSuccess && n > 0;
   cudaGetLastError();
   std::lock_guard<std::mutex> lock(mu);
   cache.push_back({dev, cl, smem, ok});
   return ok;
 }
 
-template <int NTR, int W, int S>
+template <int NTR, int W, int S, bool ONE>
 cudaError_t launch_t(Params prm, dim3 grid, int R, int k, int mb, bool pdl,
                      cudaStream_t stream) {
-  const size_t smem = Layout<NTR, W, S>::bytes(R, k, mb, prm.splits);
-  cudaError_t e = cudaFuncSetAttribute(sparse_decode_kernel<NTR, W, S>,
+  const size_t smem = Layout<NTR, W, S, ONE>::bytes(R, k, mb, prm.splits);
+  cudaError_t e = cudaFuncSetAttribute(sparse_decode_kernel<NTR, W, S, ONE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   prm.cluster = 1;
-  if (prm.splits > 1 && cluster_fits<NTR, W, S>(prm.splits, smem, grid))
+  if (prm.splits > 1 && cluster_fits<NTR, W, S, ONE>(prm.splits, smem, grid))
     prm.cluster = prm.splits;
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = make_config<NTR, W, S>(grid, smem, stream, attr, pdl, prm.cluster);
-  return cudaLaunchKernelEx(&cfg, sparse_decode_kernel<NTR, W, S>, prm);
+  cudaLaunchConfig_t cfg =
+      make_config<NTR, W, S, ONE>(grid, smem, stream, attr, pdl, prm.cluster);
+  return cudaLaunchKernelEx(&cfg, sparse_decode_kernel<NTR, W, S, ONE>, prm);
 }
 
 // Resident CTAs per SM of a variant, for split sizing.
-template <int NTR, int W, int S>
+template <int NTR, int W, int S, bool ONE>
 int resident_ctas(int R, int k, int mb, int splits) {
-  const size_t smem = Layout<NTR, W, S>::bytes(R, k, mb, splits);
-  cudaFuncSetAttribute(sparse_decode_kernel<NTR, W, S>,
+  const size_t smem = Layout<NTR, W, S, ONE>::bytes(R, k, mb, splits);
+  cudaFuncSetAttribute(sparse_decode_kernel<NTR, W, S, ONE>,
                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sparse_decode_kernel<NTR, W, S>,
-                                                    (W + 1) * 32, smem) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sparse_decode_kernel<NTR, W, S, ONE>,
+                                                    Layout<NTR, W, S, ONE>::kThreads,
+                                                    smem) != cudaSuccess) {
     cudaGetLastError();
     n = 1;
   }
@@ -933,23 +1030,24 @@ int resident_ctas(int R, int k, int mb, int splits) {
 }
 
 // Variant by (tiles per row, rows): decode rows use W consumers sharing the
-// chunks (S a multiple of W); verify rows W / R consumers per row.
+// chunks (S a multiple of W); verify rows a producer warp and W / R
+// consumers per row.
 #ifndef QSA_DECODE_STAGES_R1
 #define QSA_DECODE_STAGES_R1 8
 #endif
 #ifndef QSA_DECODE_WARPS_R1
-#define QSA_DECODE_WARPS_R1 4
+#define QSA_DECODE_WARPS_R1 8
 #endif
 #define QSA_DECODE_VARIANTS(X)                                            \
-  X(1, 1, QSA_DECODE_WARPS_R1, QSA_DECODE_STAGES_R1)                      \
-  X(2, 1, QSA_DECODE_WARPS_R1, QSA_DECODE_STAGES_R1)                      \
-  X(1, 2, 4, 8) X(2, 2, 4, 8)                                             \
-  X(1, 3, 6, 8) X(2, 3, 6, 8)                                             \
-  X(1, 4, 4, 8) X(2, 4, 4, 8)                                             \
-  X(1, 5, 5, 8) X(2, 5, 5, 8)                                             \
-  X(1, 6, 6, 8) X(2, 6, 6, 8)                                             \
-  X(1, 7, 7, 8) X(2, 7, 7, 8)                                             \
-  X(1, 8, 8, 8) X(2, 8, 8, 8)
+  X(1, 1, QSA_DECODE_WARPS_R1, QSA_DECODE_STAGES_R1, true)                \
+  X(2, 1, QSA_DECODE_WARPS_R1, QSA_DECODE_STAGES_R1, true)                \
+  X(1, 2, 4, 8, false) X(2, 2, 4, 8, false)                               \
+  X(1, 3, 6, 8, false) X(2, 3, 6, 8, false)                               \
+  X(1, 4, 4, 8, false) X(2, 4, 4, 8, false)                               \
+  X(1, 5, 5, 8, false) X(2, 5, 5, 8, false)                               \
+  X(1, 6, 6, 8, false) X(2, 6, 6, 8, false)                               \
+  X(1, 7, 7, 8, false) X(2, 7, 7, 8, false)                               \
+  X(1, 8, 8, 8, false) X(2, 8, 8, 8, false)
 
 int tiles_per_row(const Geom& g) {
   const int G = g.Hq / g.Hkv;
@@ -957,8 +1055,8 @@ int tiles_per_row(const Geom& g) {
 }
 
 int variant_resident(int ntr, int R, int k, int mb, int splits) {
-#define X(NTR_, R_, W_, S_) \
-  if (ntr == NTR_ && R == R_) return resident_ctas<NTR_, W_, S_>(R, k, mb, splits);
+#define X(NTR_, R_, W_, S_, ONE_) \
+  if (ntr == NTR_ && R == R_) return resident_ctas<NTR_, W_, S_, ONE_>(R, k, mb, splits);
   QSA_DECODE_VARIANTS(X)
 #undef X
   return 1;
@@ -1030,11 +1128,9 @@ cudaError_t launch_sparse_decode(const Geom& g, const DecodePlan& plan, const vo
   prm.cluster = 1;
   dim3 grid(plan.splits, g.Hkv * plan.qgroups, g.B);
   const int ntr = tiles_per_row(g);
-  // With one row a stage must always belong to the same consumer (S % W == 0).
-#define X(NTR_, R_, W_, S_)                                           \
-  static_assert(R_ != 1 || (S_ % W_) == 0, "decode stages per consumer"); \
+#define X(NTR_, R_, W_, S_, ONE_)                                    \
   if (ntr == NTR_ && g.R == R_)                                        \
-    return launch_t<NTR_, W_, S_>(prm, grid, g.R, k, g.MB, pdl, stream);
+    return launch_t<NTR_, W_, S_, ONE_>(prm, grid, g.R, k, g.MB, pdl, stream);
   QSA_DECODE_VARIANTS(X)
 #undef X
   return cudaErrorInvalidValue;
