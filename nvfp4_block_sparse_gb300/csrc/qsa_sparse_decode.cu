@@ -496,8 +496,54 @@ sparse_decode_kernel(Params p) {
   // count of kept entries up to the binary-search bound.  The union is thus
   // in block order and each row's pages spread across the whole of it.
   // Each thread takes a contiguous run of entries; flags and pages wait in
-  // the (still idle) stage region.
-  {
+  // the (still idle) stage region.  Verify rows whose page-table row fits in
+  // shared memory use a per-block row mask instead (below).
+  if (!ONE && pt_in_smem) {
+    // Row mask per block (one byte per block, four per word): every entry
+    // ors its row bit in; the union is then the blocks with a mask and a
+    // valid page, compacted in block order.
+    uint32_t* s_rm = reinterpret_cast<uint32_t*>(region);   // [ceil(MB / 4)]
+    const int nw = (g.MB + 3) >> 2;
+    for (int i = tid; i < nw; i += kThreads) s_rm[i] = 0u;
+    __syncthreads();
+    const int ne = R * k;
+    const int per_e = (ne + kThreads - 1) / kThreads;
+    const int e_lo = min(ne, tid * per_e), e_hi = min(ne, e_lo + per_e);
+    for (int e = e_lo, jj = e_lo / k, ii = e_lo - (e_lo / k) * k; e < e_hi; ++e) {
+      const int beta = s_sel[e];
+      if (beta >= 0) atomicOr(&s_rm[beta >> 2], (1u << jj) << (8 * (beta & 3)));
+      if (++ii == k) { ii = 0; ++jj; }
+    }
+    __syncthreads();
+    const uint8_t* rm = reinterpret_cast<const uint8_t*>(s_rm);
+    const int per_b = (g.MB + kThreads - 1) / kThreads;
+    const int b_lo = min(g.MB, tid * per_b), b_hi = min(g.MB, b_lo + per_b);
+    int cnt = 0;
+    for (int beta = b_lo; beta < b_hi; ++beta) {
+      const int page = s_pt[beta];
+      cnt += (rm[beta] != 0 && page >= 0 && page < g.NP) ? 1 : 0;
+    }
+    int x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) misc[warp] = x;
+    __syncthreads();
+    int pos = x - cnt;
+    for (int w = 0; w < warp; ++w) pos += misc[w];
+    for (int beta = b_lo; beta < b_hi; ++beta) {
+      const int mask = rm[beta];
+      const int page = s_pt[beta];
+      if (mask != 0 && page >= 0 && page < g.NP) {
+        s_union[pos] = beta | (mask << 24);
+        s_upage[pos] = page;
+        ++pos;
+      }
+    }
+    if (tid == kThreads - 1) s_scan[R * k] = pos;   // the last thread's end is the total
+  } else {
     const int ne = R * k;
     const int per = (ne + kThreads - 1) / kThreads;
     const int e_lo = min(ne, tid * per), e_hi = min(ne, e_lo + per);
@@ -1081,21 +1127,17 @@ DecodePlan plan_sparse_decode(const Geom& g, int k, int num_splits) {
     cudaGetLastError();
     const int resident = variant_resident(ntr, g.R, k, g.MB, kMaxCluster);
     const long long slots = (long long)sms * resident;
-    // Enough CTAs for about four waves of work per resident slot when the
-    // problem is large, one wave when it is small; each CTA keeps at least
-    // two chunks.  Up to a portable cluster the splits merge in distributed
-    // shared memory, so prefer a power of two there.
-    const long long total_chunks = (long long)units * max_chunks;
-    long long want = slots;
-    if (total_chunks > 64 * slots) want = 4 * slots;
-    splits = (int)(want / units);
+    // One wave: the largest power of two up to a portable cluster (whose
+    // splits merge in distributed shared memory) with units * splits within
+    // the resident CTA slots.  Each CTA carries a fixed cost (prologue, union,
+    // merge), so more waves of smaller CTAs lose.  Only when even a full
+    // cluster per unit fills under a quarter of the slots (a handful of
+    // requests) do more splits, merged by ticket, pay.
+    splits = 1;
+    while (splits * 2 <= kMaxCluster && units * splits * 2 <= slots) splits *= 2;
+    if (units * kMaxCluster * 4 < slots) splits = (int)min(64LL, slots / units);
     splits = min(splits, max(1, max_chunks / 2));
-    splits = max(1, min(splits, 64));
-    if (splits < 2 * kMaxCluster) {
-      int p2 = 1;
-      while (p2 * 2 <= splits && p2 * 2 <= kMaxCluster) p2 *= 2;
-      splits = p2;
-    }
+    splits = max(1, splits);
   }
   pl.splits = splits;
   size_t ws = kWsHeader + align256((size_t)units * sizeof(int));
