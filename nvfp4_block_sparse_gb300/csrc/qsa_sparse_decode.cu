@@ -160,7 +160,7 @@ struct Layout {
 // up to four row consumers, unconstrained otherwise.
 template <int NTR, int W, bool ONE>
 constexpr int decode_min_blocks() {
-  return NTR != 1 ? 1 : (ONE ? (W <= 4 ? 4 : 2) : (W <= 4 ? 3 : 1));
+  return NTR != 1 ? 1 : (ONE ? (W <= 4 ? 4 : 2) : (W <= 4 ? 3 : 2));
 }
 
 __device__ __forceinline__ void cluster_arrive_relaxed() {
@@ -1084,16 +1084,27 @@ int resident_ctas(int R, int k, int mb, int splits) {
 #ifndef QSA_DECODE_WARPS_R1
 #define QSA_DECODE_WARPS_R1 8
 #endif
+#ifndef QSA_DECODE_STAGES_RN
+#define QSA_DECODE_STAGES_RN 4
+#endif
+#ifndef QSA_DECODE_WARPS_R2
+#define QSA_DECODE_WARPS_R2 4
+#endif
+#ifndef QSA_DECODE_WARPS_R4
+#define QSA_DECODE_WARPS_R4 4
+#endif
 #define QSA_DECODE_VARIANTS(X)                                            \
   X(1, 1, QSA_DECODE_WARPS_R1, QSA_DECODE_STAGES_R1, true)                \
   X(2, 1, QSA_DECODE_WARPS_R1, QSA_DECODE_STAGES_R1, true)                \
-  X(1, 2, 4, 8, false) X(2, 2, 4, 8, false)                               \
-  X(1, 3, 6, 8, false) X(2, 3, 6, 8, false)                               \
-  X(1, 4, 4, 8, false) X(2, 4, 4, 8, false)                               \
-  X(1, 5, 5, 8, false) X(2, 5, 5, 8, false)                               \
-  X(1, 6, 6, 8, false) X(2, 6, 6, 8, false)                               \
-  X(1, 7, 7, 8, false) X(2, 7, 7, 8, false)                               \
-  X(1, 8, 8, 8, false) X(2, 8, 8, 8, false)
+  X(1, 2, QSA_DECODE_WARPS_R2, QSA_DECODE_STAGES_RN, false)              \
+  X(2, 2, 4, QSA_DECODE_STAGES_RN, false)                                 \
+  X(1, 3, 6, QSA_DECODE_STAGES_RN, false) X(2, 3, 6, QSA_DECODE_STAGES_RN, false) \
+  X(1, 4, QSA_DECODE_WARPS_R4, QSA_DECODE_STAGES_RN, false)              \
+  X(2, 4, 4, QSA_DECODE_STAGES_RN, false)                                 \
+  X(1, 5, 5, QSA_DECODE_STAGES_RN, false) X(2, 5, 5, QSA_DECODE_STAGES_RN, false) \
+  X(1, 6, 6, QSA_DECODE_STAGES_RN, false) X(2, 6, 6, QSA_DECODE_STAGES_RN, false) \
+  X(1, 7, 7, QSA_DECODE_STAGES_RN, false) X(2, 7, 7, QSA_DECODE_STAGES_RN, false) \
+  X(1, 8, 8, QSA_DECODE_STAGES_RN, false) X(2, 8, 8, QSA_DECODE_STAGES_RN, false)
 
 int tiles_per_row(const Geom& g) {
   const int G = g.Hq / g.Hkv;
@@ -1127,14 +1138,14 @@ DecodePlan plan_sparse_decode(const Geom& g, int k, int num_splits) {
     cudaGetLastError();
     const int resident = variant_resident(ntr, g.R, k, g.MB, kMaxCluster);
     const long long slots = (long long)sms * resident;
-    // One wave: the largest power of two up to a portable cluster (whose
-    // splits merge in distributed shared memory) with units * splits within
+    // One wave: the most splits up to a portable cluster (whose splits
+    // merge in distributed shared memory) with units * splits within
     // the resident CTA slots.  Each CTA carries a fixed cost (prologue, union,
     // merge), so more waves of smaller CTAs lose.  Only when even a full
     // cluster per unit fills under a quarter of the slots (a handful of
     // requests) do more splits, merged by ticket, pay.
     splits = 1;
-    while (splits * 2 <= kMaxCluster && units * splits * 2 <= slots) splits *= 2;
+    while (splits + 1 <= kMaxCluster && units * (splits + 1) <= slots) ++splits;
     if (units * kMaxCluster * 4 < slots) splits = (int)min(64LL, slots / units);
     splits = min(splits, max(1, max_chunks / 2));
     splits = max(1, splits);
