@@ -14,12 +14,15 @@
 //   out    = window U taken, ascending, padded with -1
 //
 // Layout: block i of the row belongs to thread i mod NTHREADS ("round"
-// i / NTHREADS), so shared-memory accesses are conflict-free.  The
-// take-th largest candidate key is found by radix selection on (key - min key)
-// with 11-bit digits starting at the highest bit where candidates differ (two
-// passes for ranges below 2^22).  Ordered steps -- the tie ranks (highest
-// index first) and the ascending compaction -- use warp ballots plus one table
-// of per-(round, warp) counts, so each costs one barrier.
+// i / NTHREADS), so shared-memory accesses are conflict-free.  The take-th
+// largest candidate key is located by radix selection on (key - min key) with
+// 11-bit digits starting at the highest bit where candidates differ.  As soon
+// as the digit bin that holds it has at most kSelMaxMembers candidates, those
+// members are ranked exactly by (key, block) against each other and the
+// remaining digits are never visited (one pass for typical score ranges).
+// When the last digit is reached instead, the threshold key is exact and ties
+// go to the highest block indices by per-(round, warp) ballot counts.  The
+// ascending compaction uses the same ballot counts, one barrier.
 #pragma once
 
 #include "qsa_common.cuh"
@@ -28,6 +31,7 @@ namespace qsa {
 
 constexpr int kSelDigitBits = 11;
 constexpr int kSelBins = 1 << kSelDigitBits;
+constexpr int kSelMaxMembers = 256;   // boundary-bin members ranked directly
 
 // Shared memory a CTA of NTHREADS needs for rows of up to `mb` blocks.
 template <int NTHREADS>
@@ -35,6 +39,7 @@ __host__ __device__ constexpr size_t select_row_smem(int mb) {
   return (size_t)kSelBins * 4                                      // histogram
          + (size_t)((mb + NTHREADS - 1) / NTHREADS) * (NTHREADS / 32) * 4 * 2  // round counts
          + 64 * 4                                                  // scalars
+         + (size_t)kSelMaxMembers * 8                              // boundary members
          + (size_t)mb * 4;                                         // the row
 }
 
@@ -54,18 +59,20 @@ __device__ void select_row(const int32_t* __restrict__ src, int nb, int W, int k
   int* cnt_eq = reinterpret_cast<int*>(smem + kSelBins * 4);
   int* cnt_pick = cnt_eq + rounds * kWarps;
   int* sc = cnt_pick + rounds * kWarps;           // 64 scalars
-  int32_t* row = sc + 64;
+  uint2* mlist = reinterpret_cast<uint2*>(sc + 64);   // (rel, block) of boundary members
+  int32_t* row = reinterpret_cast<int32_t*>(mlist + kSelMaxMembers);
   const int wlo = nb - W > 0 ? nb - W : 0;
   const unsigned lt_mask = (1u << lane) - 1u;
 
-  for (int i = tid; i < nb; i += NTHREADS) row[i] = src[i];
-  // (row visibility for other threads comes with the next barrier)
-
-  // Window and candidate counts; candidate key range.
+  // Row into shared memory; window and candidate counts and the candidate key
+  // range straight from the loaded values.  The first histogram is cleared
+  // here too.
+  for (int q = tid; q < kSelBins; q += NTHREADS) hist[q] = 0;
   int nwin = 0, ncand = 0;
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
   for (int i = tid; i < nb; i += NTHREADS) {
-    const int s = row[i];
+    const int s = src[i];
+    row[i] = s;
     if (s == kSentinel) continue;
     if (i >= wlo) {
       ++nwin;
@@ -86,6 +93,7 @@ __device__ void select_row(const int32_t* __restrict__ src, int nb, int W, int k
     sc[16 + warp] = (int)kmin;
     sc[24 + warp] = (int)kmax;
   }
+  if (tid == 0) sc[50] = 0;   // boundary-member counter
   __syncthreads();
   int tot_win = 0, tot_cand = 0;
   kmin = 0xFFFFFFFFu;
@@ -101,20 +109,28 @@ __device__ void select_row(const int32_t* __restrict__ src, int nb, int W, int k
   const int take = min(k - tot_win, tot_cand);
   const bool none = take <= 0;
   const bool all = !none && take >= tot_cand;
-  uint32_t thr_rel = 0;   // candidates with rel > thr_rel are taken ...
-  int need = 0;           // ... and, at rel == thr_rel, the need highest indices
+  // Result of the search: candidates whose rel >> shift exceeds prefix are
+  // taken; at rel >> shift == prefix, `need` more are taken -- the highest
+  // (rel, block) members (ranked, by_rank) or, at shift 0, the highest blocks.
+  uint32_t prefix = 0;
+  int shift = 0;
+  int need = 0;
+  bool by_rank = false;
   if (!none && !all) {
     const uint32_t range = kmax - kmin;
-    int shift = range ? 32 - __clz(range) : 0;
-    uint32_t prefix = 0;
+    shift = range ? 32 - __clz(range) : 0;
     int remaining = take;
+    bool first = true;
     while (shift > 0) {
       const int bits = shift < kSelDigitBits ? shift : kSelDigitBits;
       shift -= bits;
       const int nbins = 1 << bits;
       const uint32_t dmask = (uint32_t)nbins - 1u;
-      for (int q = tid; q < nbins; q += NTHREADS) hist[q] = 0;
-      __syncthreads();
+      if (!first) {
+        for (int q = tid; q < nbins; q += NTHREADS) hist[q] = 0;
+        __syncthreads();
+      }
+      first = false;
       for (int i = tid; i < wlo; i += NTHREADS) {
         const int s = row[i];
         if (s == kSentinel) continue;
@@ -151,59 +167,102 @@ __device__ void select_row(const int32_t* __restrict__ src, int nb, int W, int k
         if (above < remaining && remaining <= above + c[q]) {
           sc[48] = tid * kPer + q;
           sc[49] = above;
+          sc[51] = c[q];
         }
         above += c[q];
       }
       __syncthreads();
       remaining -= sc[49];
       prefix = (prefix << bits) | (uint32_t)sc[48];
+      if (shift > 0 && sc[51] <= kSelMaxMembers) {
+        by_rank = true;
+        break;
+      }
     }
-    thr_rel = prefix;
     need = remaining;
   }
 
-  // Tie ranks: equal candidates per (round, warp) first.
-  for (int rd = 0; rd < rounds; ++rd) {
-    const int i = rd * NTHREADS + tid;
-    bool eq = false;
-    if (!none && !all && i < wlo) {
+  if (by_rank) {
+    // Boundary members into a list (any order), then each ranks itself.
+    for (int i = tid; i < wlo; i += NTHREADS) {
       const int s = row[i];
-      eq = s != kSentinel && sel_order_key(s) - kmin == thr_rel;
+      if (s == kSentinel) continue;
+      const uint32_t rel = sel_order_key(s) - kmin;
+      if ((rel >> shift) == prefix) mlist[atomicAdd(&sc[50], 1)] = make_uint2(rel, (uint32_t)i);
     }
-    const unsigned b = __ballot_sync(kFull, eq);
-    if (lane == 0) cnt_eq[rd * kWarps + warp] = __popc(b);
-  }
-  __syncthreads();
-  // Picks, from the highest round down: an equal candidate is taken when fewer
-  // than `need` equal candidates sit at higher block indices.  The pick flag
-  // replaces the score in place.
-  int eq_above = 0;   // equal candidates in rounds above the current one
-  for (int rd = rounds - 1; rd >= 0; --rd) {
-    const int i = rd * NTHREADS + tid;
-    const int s = i < nb ? row[i] : kSentinel;
-    bool pick = false, eq = false;
-    if (s != kSentinel) {
-      if (i >= wlo || all) {
-        pick = true;
-      } else if (!none) {
-        const uint32_t rel = sel_order_key(s) - kmin;
-        pick = rel > thr_rel;
-        eq = rel == thr_rel;
+    __syncthreads();
+    const int m = sc[50];
+    for (int rd = 0; rd < rounds; ++rd) {
+      const int i = rd * NTHREADS + tid;
+      const int s = i < nb ? row[i] : kSentinel;
+      bool pick = false;
+      if (s != kSentinel) {
+        if (i >= wlo) {
+          pick = true;
+        } else {
+          const uint32_t rel = sel_order_key(s) - kmin;
+          const uint32_t hi = rel >> shift;
+          if (hi > prefix) {
+            pick = true;
+          } else if (hi == prefix) {
+            int rank = 0;   // members above this one in (rel, block) order
+            for (int t = 0; t < m; ++t) {
+              const uint2 y = mlist[t];
+              rank += (y.x > rel || (y.x == rel && (int)y.y > i)) ? 1 : 0;
+            }
+            pick = rank < need;
+          }
+        }
       }
+      const unsigned pb = __ballot_sync(kFull, pick);
+      if (lane == 0) cnt_pick[rd * kWarps + warp] = __popc(pb);
+      if (i < nb) row[i] = pick ? 1 : 0;
     }
-    const unsigned b = __ballot_sync(kFull, eq);
-    int in_round = 0, round_tot = 0;
+  } else {
+    const uint32_t thr_rel = prefix;   // exact threshold key (shift 0)
+    // Tie ranks: equal candidates per (round, warp) first.
+    for (int rd = 0; rd < rounds; ++rd) {
+      const int i = rd * NTHREADS + tid;
+      bool eq = false;
+      if (!none && !all && i < wlo) {
+        const int s = row[i];
+        eq = s != kSentinel && sel_order_key(s) - kmin == thr_rel;
+      }
+      const unsigned b = __ballot_sync(kFull, eq);
+      if (lane == 0) cnt_eq[rd * kWarps + warp] = __popc(b);
+    }
+    __syncthreads();
+    // Picks, from the highest round down: an equal candidate is taken when
+    // fewer than `need` equal candidates sit at higher block indices.  The
+    // pick flag replaces the score in place.
+    int eq_above = 0;   // equal candidates in rounds above the current one
+    for (int rd = rounds - 1; rd >= 0; --rd) {
+      const int i = rd * NTHREADS + tid;
+      const int s = i < nb ? row[i] : kSentinel;
+      bool pick = false, eq = false;
+      if (s != kSentinel) {
+        if (i >= wlo || all) {
+          pick = true;
+        } else if (!none) {
+          const uint32_t rel = sel_order_key(s) - kmin;
+          pick = rel > thr_rel;
+          eq = rel == thr_rel;
+        }
+      }
+      const unsigned b = __ballot_sync(kFull, eq);
+      int in_round = 0, round_tot = 0;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const int cw = cnt_eq[rd * kWarps + w];
-      round_tot += cw;
-      if (w > warp) in_round += cw;
+      for (int w = 0; w < kWarps; ++w) {
+        const int cw = cnt_eq[rd * kWarps + w];
+        round_tot += cw;
+        if (w > warp) in_round += cw;
+      }
+      if (eq) pick = eq_above + in_round + __popc(b & ~lt_mask & ~(1u << lane)) < need;
+      eq_above += round_tot;
+      const unsigned pb = __ballot_sync(kFull, pick);
+      if (lane == 0) cnt_pick[rd * kWarps + warp] = __popc(pb);
+      if (i < nb) row[i] = pick ? 1 : 0;
     }
-    if (eq) pick = eq_above + in_round + __popc(b & ~lt_mask & ~(1u << lane)) < need;
-    eq_above += round_tot;
-    const unsigned pb = __ballot_sync(kFull, pick);
-    if (lane == 0) cnt_pick[rd * kWarps + warp] = __popc(pb);
-    if (i < nb) row[i] = pick ? 1 : 0;
   }
   __syncthreads();
   // Ascending compaction: position = picks at lower indices.
