@@ -103,6 +103,49 @@ def algorithmic_bytes(w: dict, sel: np.ndarray) -> dict:
                 touched=idx + dec + T * MB * 4 * 2 + T * w["k"] * 4 * 2)
 
 
+def time_prologue(qsa, step, reps, stream, nrep):
+    """qsa_store_kv_tokens (the decode prologue) per replica, graph-replayed
+    between CUDA events: us per call and its algorithmic bytes (new K/V rows
+    and index keys read; NVFP4 codes, scales and keys written; one page-table
+    entry per row and the lengths read)."""
+    news = [qw.make_new_tokens(w, seed=7 + i) for i, w in enumerate(reps)]
+    w = reps[0]
+    T, Hkv = w["batch"] * w["rows_per_req"], w["num_kv_heads"]
+    D, Di = w["head_dim"], w["index_dim"]
+    nbytes = (T * Hkv * 2 * (D * 2 + D // 2 + D // 16) + T * Di * 2 + T * 4
+              + w["batch"] * 4)
+
+    def run(i):
+        n = news[i]
+        r = reps[i]
+        qsa.qsa_store_kv_tokens(step.cg, n["k_new"], n["v_new"], n["ik_new"], r["k_scale"],
+                                r["v_scale"], r["page_table"], r["seqlens"], r["k_pool"],
+                                r["k_sf"], r["v_pool"], r["v_sf"], r["ik_pool"], stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(nrep):
+            run(i)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(nrep):
+                run(i)
+        g.replay()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        n_rep = max(20, 2000 // nrep)
+        e0.record(stream)
+        for _ in range(n_rep):
+            g.replay()
+        e1.record(stream)
+        stream.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (n_rep * nrep)
+    return {"call": "qsa_store_kv_tokens", "us_per_call": us, "bytes_per_call": nbytes,
+            "gbs": nbytes / (us * 1e-6) / 1e9, "bound": "latency (a few KB per call)",
+            "launches_per_call": 1}
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling while the timed region runs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -383,6 +426,10 @@ def run_qsa(args, case):
     # ---- end to end through host buffers ----------------------------------
     e2e = run_e2e(qsa, step, reps, stream, args, dev, T, world)
 
+    # ---- decode prologue (store the step's new tokens), after every other
+    # measurement because it writes into the replicas' caches ---------------
+    prologue = time_prologue(qsa, step, reps, stream, nrep)
+
     # ---- CPU baseline (rank 0, N = 1 only) -----------------------------------
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -430,6 +477,7 @@ def run_qsa(args, case):
         "e2e": e2e,
         "gpu_launches": 3 * args.steps,
         "cpu_baseline": cpu,
+        "prologue": prologue,
     }
     print(json.dumps(line), flush=True)
 

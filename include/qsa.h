@@ -227,6 +227,46 @@ qsa_status_t qsa_sparse_decode_noalloc(const qsa_geom_t *geom, const void *q_bf1
                                        cudaStream_t stream);
 
 /*
+ * Decode prologue: store the step's new tokens into the cache before A1.
+ * TensorRT-LLM PR #20937 ("GB300 perf work on
+ * qwen3_8_flash_next_nvfp4__sm_103__tp1"), What changes: a decode prologue over
+ * the NVFP4 KV cache that also serves verify steps; Walkthrough, changes
+ * table: NVFP4 storage in the decode prologue.  [F]: e2m1 pages with e4m3
+ * block scales, one page index for every pool.
+ *
+ *   k_new, v_new  bf16 [T, Hkv, 128]  the new rows' keys and values
+ *   ik_new        int8 [T, 64]        the new rows' index keys
+ *   k_scale,
+ *   v_scale       fp32 > 0            per-tensor dequant multipliers (the same
+ *                                     values qsa_sparse_decode is given)
+ *   page_table, seqlens               as above; seqlens already count the R
+ *                                     new rows
+ *   k_pool, k_sf, v_pool, v_sf, ik_pool   the cache pools (layouts as in
+ *                                     qsa_sparse_decode / qsa_index_scores),
+ *                                     written in place
+ *
+ * Row j of request b is the token at position L_b - R + j: block
+ * (L_b - R + j) / P, slot (L_b - R + j) % P of its page; rows whose position
+ * is negative, at or past MB*P, or whose page is invalid are skipped.  Each
+ * 16-element block of a K or V row is quantised as
+ *   sf = e4m3_rne_satfinite((max|x| / 6) / scale)
+ *   code_i = e2m1_rne_satfinite(x_i / (e4m3(sf) * scale))
+ * (every division and product in IEEE fp32, in that order; all codes 0 when
+ * e4m3(sf) * scale is 0; a code rounded to magnitude zero is stored as +0).
+ * The index key is copied as is.  Only the written slots change.
+ * Returns QSA_ERR_INVALID_ARG for null pointers, non-positive or non-finite
+ * scales, k_new / v_new not 8-byte aligned, ik_new / ik_pool not 4-byte
+ * aligned or k_pool / v_pool not 2-byte aligned; geometry and device checks
+ * as for the other calls.
+ */
+qsa_status_t qsa_store_kv_tokens(const qsa_geom_t *geom, const void *k_new_bf16,
+                                 const void *v_new_bf16, const int8_t *ik_new,
+                                 float k_scale, float v_scale,
+                                 const int32_t *page_table, const int32_t *seqlens,
+                                 uint8_t *k_pool, uint8_t *k_sf, uint8_t *v_pool,
+                                 uint8_t *v_sf, int8_t *ik_pool, cudaStream_t stream);
+
+/*
  * Reads the workspace's device status word (synchronising `stream`): 0 when
  * every bounded wait since qsa_workspace_init() completed, otherwise a
  * nonzero code and QSA_ERR_DEVICE_TIMEOUT is returned.  Diagnostic only.

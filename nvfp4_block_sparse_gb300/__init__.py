@@ -15,13 +15,15 @@ import torch
 from .binding import (EXPORTS, QsaError, load, make_geom, qsa_geom_t, qsa_index_scores,
                       qsa_select_topk, qsa_sparse_decode, qsa_sparse_decode_ex, qsa_sparse_decode_noalloc,
                       qsa_sparse_decode_workspace_bytes, qsa_sparse_decode_workspace_bytes_ex,
-                      qsa_status_string, qsa_workspace_init, qsa_workspace_status)
+                      qsa_status_string, qsa_store_kv_tokens, qsa_workspace_init,
+                      qsa_workspace_status)
 
 __all__ = [
     "EXPORTS", "QsaError", "load", "make_geom", "qsa_geom_t", "qsa_index_scores",
     "qsa_select_topk", "qsa_sparse_decode", "qsa_sparse_decode_ex", "qsa_sparse_decode_noalloc",
     "qsa_sparse_decode_workspace_bytes", "qsa_sparse_decode_workspace_bytes_ex",
-    "qsa_status_string", "qsa_workspace_init", "qsa_workspace_status", "DecodeStep",
+    "qsa_status_string", "qsa_store_kv_tokens", "qsa_workspace_init", "qsa_workspace_status",
+    "DecodeStep",
 ]
 
 GEOM_FIELDS = [n for n, _ in qsa_geom_t._fields_]

@@ -32,6 +32,7 @@ EXPORTS = (
     "qsa_sparse_decode_ex",
     "qsa_sparse_decode_noalloc",
     "qsa_workspace_status",
+    "qsa_store_kv_tokens",
 )
 
 
@@ -91,6 +92,9 @@ def load(build_if_missing: bool = False):
     lib.qsa_sparse_decode_noalloc.argtypes = [G, _vp, _vp, _vp, _vp, _vp, ctypes.c_float,
                                               ctypes.c_float, ctypes.c_float, _vp, _vp, _vp,
                                               ctypes.c_int, _vp, _vp, _vp]
+    lib.qsa_store_kv_tokens.restype = st
+    lib.qsa_store_kv_tokens.argtypes = [G, _vp, _vp, _vp, ctypes.c_float, ctypes.c_float, _vp,
+                                        _vp, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.qsa_workspace_status.restype = st
     lib.qsa_workspace_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int), _vp]
     _lib = lib
@@ -138,6 +142,18 @@ def qsa_index_scores(geom, iq, ik_pool, page_table, seqlens, scores, stream=None
         ctypes.byref(g), _ptr(iq, torch.int8, "iq"), _ptr(ik_pool, torch.int8, "ik_pool"),
         _ptr(page_table, torch.int32, "page_table"), _ptr(seqlens, torch.int32, "seqlens"),
         _ptr(scores, torch.int32, "scores"), _stream(stream)))
+
+
+def qsa_store_kv_tokens(geom, k_new, v_new, ik_new, k_scale, v_scale, page_table, seqlens,
+                        k_pool, k_sf, v_pool, v_sf, ik_pool, stream=None):
+    g = _geom(geom)
+    _check("qsa_store_kv_tokens", load().qsa_store_kv_tokens(
+        ctypes.byref(g), _ptr(k_new, torch.bfloat16, "k_new"), _ptr(v_new, torch.bfloat16, "v_new"),
+        _ptr(ik_new, torch.int8, "ik_new"), float(k_scale), float(v_scale),
+        _ptr(page_table, torch.int32, "page_table"), _ptr(seqlens, torch.int32, "seqlens"),
+        _ptr(k_pool, torch.uint8, "k_pool"), _ptr(k_sf, torch.uint8, "k_sf"),
+        _ptr(v_pool, torch.uint8, "v_pool"), _ptr(v_sf, torch.uint8, "v_sf"),
+        _ptr(ik_pool, torch.int8, "ik_pool"), _stream(stream)))
 
 
 def qsa_select_topk(geom, scores, seqlens, k, window, sel, nsel, stream=None):

@@ -9,6 +9,7 @@
 // buffers (Per-File QA: caller-provided buffers).
 #include "qsa_common.cuh"
 
+#include <math.h>
 #include <stdint.h>
 
 namespace {
@@ -93,6 +94,29 @@ const char* qsa_status_string(qsa_status_t s) {
     case QSA_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
   }
   return "unknown status";
+}
+
+qsa_status_t qsa_store_kv_tokens(const qsa_geom_t* geom, const void* k_new_bf16,
+                                 const void* v_new_bf16, const int8_t* ik_new, float k_scale,
+                                 float v_scale, const int32_t* page_table,
+                                 const int32_t* seqlens, uint8_t* k_pool, uint8_t* k_sf,
+                                 uint8_t* v_pool, uint8_t* v_sf, int8_t* ik_pool,
+                                 cudaStream_t stream) {
+  qsa_status_t st = check_geom(geom);
+  if (st != QSA_OK) return st;
+  if (!k_new_bf16 || !v_new_bf16 || !ik_new || !page_table || !seqlens || !k_pool || !k_sf ||
+      !v_pool || !v_sf || !ik_pool)
+    return QSA_ERR_INVALID_ARG;
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || !isfinite(k_scale) || !isfinite(v_scale))
+    return QSA_ERR_INVALID_ARG;
+  if (!aligned(k_new_bf16, 8) || !aligned(v_new_bf16, 8) || !aligned(ik_new, 4) ||
+      !aligned(ik_pool, 4) || !aligned(k_pool, 2) || !aligned(v_pool, 2))
+    return QSA_ERR_INVALID_ARG;
+  st = check_device();
+  if (st != QSA_OK) return st;
+  return from_cuda(qsa::launch_store_tokens(to_geom(geom), k_new_bf16, v_new_bf16, ik_new,
+                                            k_scale, v_scale, page_table, seqlens, k_pool, k_sf,
+                                            v_pool, v_sf, ik_pool, true, stream));
 }
 
 qsa_status_t qsa_index_scores(const qsa_geom_t* geom, const int8_t* iq, const int8_t* ik_pool,

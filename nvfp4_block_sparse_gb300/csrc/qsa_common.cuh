@@ -186,6 +186,11 @@ struct Geom {
   int B, R, Hq, Hkv, D, Di, P, MB, NP;
 };
 
+cudaError_t launch_store_tokens(const Geom& g, const void* k_new, const void* v_new,
+                                const int8_t* ik_new, float k_scale, float v_scale,
+                                const int32_t* page_table, const int32_t* seqlens,
+                                uint8_t* k_pool, uint8_t* k_sf, uint8_t* v_pool, uint8_t* v_sf,
+                                int8_t* ik_pool, bool pdl, cudaStream_t stream);
 cudaError_t launch_index_scores(const Geom& g, const int8_t* iq, const int8_t* ik_pool,
                                 const int32_t* page_table, const int32_t* seqlens,
                                 int32_t* scores, bool pdl, cudaStream_t stream);

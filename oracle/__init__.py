@@ -30,7 +30,7 @@ def build(force: bool = False) -> str:
     """Compile the oracle with the host C compiler (OpenMP, -O2, no fast-math)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + ".tmp%d" % os.getpid()
-        subprocess.run(["gcc", "-O2", "-std=c99", "-fopenmp", "-fPIC", "-shared",
+        subprocess.run(["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared",
                         "-o", tmp, _SRC, "-lm"], check=True)
         os.replace(tmp, _LIB)
     return _LIB
@@ -46,6 +46,16 @@ def _load():
         lib.qsa_oracle_e4m3.restype = ctypes.c_double
         lib.qsa_oracle_e4m3.argtypes = [ctypes.c_int]
         lib.qsa_oracle_num_threads.restype = ctypes.c_int
+        lib.qsa_oracle_e4m3_encode.restype = ctypes.c_int
+        lib.qsa_oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.qsa_oracle_e2m1_encode.restype = ctypes.c_int
+        lib.qsa_oracle_e2m1_encode.argtypes = [ctypes.c_float]
+        lib.qsa_oracle_quantize_block.restype = None
+        lib.qsa_oracle_quantize_block.argtypes = [ctypes.c_void_p, ctypes.c_float,
+                                                  ctypes.c_void_p, ctypes.c_void_p]
+        lib.qsa_oracle_store_kv.restype = ctypes.c_int
+        lib.qsa_oracle_store_kv.argtypes = ([ctypes.c_int] * 8 + [ctypes.c_void_p] * 3 +
+                                            [ctypes.c_float] * 2 + [ctypes.c_void_p] * 7)
         for name in ("qsa_oracle_index_scores", "qsa_oracle_select",
                      "qsa_oracle_attention"):
             getattr(lib, name).restype = ctypes.c_int
@@ -148,3 +158,48 @@ def step(w: dict, rows=None):
     sel, nsel = select(w, sc, rows)
     out, lse = attention(w, sel, rows)
     return dict(scores=sc, sel=sel, nsel=nsel, out=out, lse=lse)
+
+
+# ---------------------------------------------------------------------------
+# decode prologue: NVFP4 quantiser and token store
+# ---------------------------------------------------------------------------
+
+def e4m3_encode(q: float) -> int:
+    """e4m3 byte nearest to fp32 ``q`` >= 0 (ties to even, saturating)."""
+    return _load().qsa_oracle_e4m3_encode(float(q))
+
+
+def e2m1_encode(y: float) -> int:
+    """e2m1 code nearest to fp32 ``y`` (ties to even, saturating, zero as +0)."""
+    return _load().qsa_oracle_e2m1_encode(float(y))
+
+
+def quantize_block(x: np.ndarray, scale: float):
+    """16 fp32 values -> (16 e2m1 codes, e4m3 scale byte)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    assert x.shape == (16,)
+    codes = np.zeros(16, dtype=np.uint8)
+    sf = np.zeros(1, dtype=np.uint8)
+    _load().qsa_oracle_quantize_block(_p(x), float(scale), _p(codes), _p(sf))
+    return codes, int(sf[0])
+
+
+def store_kv(w: dict, new: dict) -> dict:
+    """The decode prologue on host copies of the pools: returns new k_pool,
+    k_sf, v_pool, v_sf and ik_pool with the step's tokens stored.  ``new``
+    holds k_new / v_new (bf16 bits as uint16 [T, Hkv, D]) and ik_new (int8
+    [T, Di])."""
+    out = {n: np.ascontiguousarray(w[n]).copy() for n in ("k_pool", "k_sf", "v_pool", "v_sf",
+                                                           "ik_pool")}
+    B, R, Hkv = w["batch"], w["rows_per_req"], w["num_kv_heads"]
+    st = _load().qsa_oracle_store_kv(
+        B, R, Hkv, w["head_dim"], w["index_dim"], w["page_size"], w["max_blocks"],
+        w["num_pages"], _p(np.ascontiguousarray(new["k_new"], dtype=np.uint16)),
+        _p(np.ascontiguousarray(new["v_new"], dtype=np.uint16)),
+        _p(np.ascontiguousarray(new["ik_new"], dtype=np.int8)), float(w["k_scale"]),
+        float(w["v_scale"]), _p(np.ascontiguousarray(w["page_table"], dtype=np.int32)),
+        _p(np.ascontiguousarray(w["seqlens"], dtype=np.int32)), _p(out["k_pool"]),
+        _p(out["k_sf"]), _p(out["v_pool"]), _p(out["v_sf"]), _p(out["ik_pool"]))
+    if st != 0:
+        raise RuntimeError("qsa_oracle_store_kv failed (%d)" % st)
+    return out

@@ -22,7 +22,7 @@
  *     with a per-row merge.
  *   - e2m1 / e4m3 bit fields: OCP Microscaling Formats v1.0 (element formats).
  *
- * Readings where the pages are silent (each one is listed in the design doc):
+ * Readings where the pages are silent:
  *   R1 block score = max over the block's visible tokens of the token score;
  *   R2 token score = sum over all query heads of the int8 dot product;
  *   R3 one selection per query row, shared by every head;
@@ -341,4 +341,134 @@ int qsa_oracle_attention(int B, int R, int Hq, int Hkv, int D, int P, int MB,
         }
     }
     return oom ? -2 : 0;
+}
+
+/* ---- decode prologue: NVFP4 quantiser and token store ------------------
+ *
+ * TensorRT-LLM PR #20937 "GB300 perf work on
+ * qwen3_8_flash_next_nvfp4__sm_103__tp1", What changes: a decode prologue over
+ * the NVFP4 KV cache that also serves verify steps; Walkthrough, changes
+ * table: NVFP4 storage in the decode prologue.  The pages print no quantiser;
+ * the recipe below is the plain per-16-element NVFP4 reading:
+ *   sf     = e4m3_rne_satfinite((max|x| / 6) / scale)
+ *   code_i = e2m1_rne_satfinite(x_i / (e4m3(sf) * scale))
+ * Where floating point decides a code, the decision is taken in IEEE fp32
+ * (the pages fix no precision; fp32 is what the library computes in), with
+ * the divisions and the product in that order.  The encoders are written from
+ * the element definitions: the nearest representable magnitude, a tie going
+ * to the code whose lowest bit is 0 (the even mantissa), saturating at the
+ * largest finite value.  A code whose magnitude is zero is stored as +0.
+ */
+
+/* e4m3 byte (sign 0) nearest to q >= 0. */
+int qsa_oracle_e4m3_encode(float q)
+{
+    int best = 0;
+    double bd = INFINITY;
+    for (int c = 0; c <= 0x7E; c++) {                 /* 0x7F is NaN */
+        double d = fabs((double)q - qsa_oracle_e4m3(c));
+        if (d < bd || (d == bd && (c & 1) == 0)) {
+            best = c;
+            bd = d;
+        }
+    }
+    return best;
+}
+
+/* e2m1 code nearest to y (sign bit 3; magnitude zero stored as +0). */
+int qsa_oracle_e2m1_encode(float y)
+{
+    double a = fabs((double)y);
+    int best = 0;
+    double bd = INFINITY;
+    for (int c = 0; c <= 7; c++) {
+        double d = fabs(a - qsa_oracle_e2m1(c));
+        if (d < bd || (d == bd && (c & 1) == 0)) {
+            best = c;
+            bd = d;
+        }
+    }
+    if (best != 0 && y < 0.0f)
+        best |= 8;
+    return best;
+}
+
+/* One 16-element block: 16 codes and the scale byte. */
+void qsa_oracle_quantize_block(const float *x, float scale, uint8_t *codes, uint8_t *sf_out)
+{
+    float a = 0.0f;
+    for (int i = 0; i < 16; i++) {
+        float v = fabsf(x[i]);
+        if (v > a)
+            a = v;
+    }
+    float q = (a / 6.0f) / scale;     /* ISO C, no contraction: each op rounds */
+    int sf = qsa_oracle_e4m3_encode(q);
+    float den = (float)qsa_oracle_e4m3(sf) * scale;
+    for (int i = 0; i < 16; i++) {
+        if (den == 0.0f) {
+            codes[i] = 0;
+        } else {
+            codes[i] = (uint8_t)qsa_oracle_e2m1_encode(x[i] / den);
+        }
+    }
+    *sf_out = (uint8_t)sf;
+}
+
+static float bf16_to_float(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/*
+ * Row r = b*R + j is the token at position L_b - R + j of request b: block
+ * pos / P, slot pos % P of page page_table[b, pos / P]; skipped when
+ * pos < 0, pos >= MB*P or the page is invalid.  k_new / v_new: bf16
+ * [T, Hkv, D]; ik_new: int8 [T, Di].  The pools are updated in place.
+ */
+int qsa_oracle_store_kv(int B, int R, int Hkv, int D, int Di, int P, int MB, int NP,
+                        const uint16_t *k_new, const uint16_t *v_new, const int8_t *ik_new,
+                        float k_scale, float v_scale, const int32_t *page_table,
+                        const int32_t *seqlens, uint8_t *k_pool, uint8_t *k_sf,
+                        uint8_t *v_pool, uint8_t *v_sf, int8_t *ik_pool)
+{
+    if (D % 16 != 0)
+        return -1;
+    for (int b = 0; b < B; b++) {
+        for (int j = 0; j < R; j++) {
+            int64_t pos = (int64_t)seqlens[b] - R + j;
+            if (pos < 0 || pos >= (int64_t)MB * P)
+                continue;
+            int beta = (int)(pos / P), slot = (int)(pos % P);
+            int32_t page = page_table[(int64_t)b * MB + beta];
+            if (page < 0 || page >= NP)
+                continue;
+            int64_t r = (int64_t)b * R + j;
+            for (int g = 0; g < Hkv; g++) {
+                int64_t row = ((int64_t)page * Hkv + g) * P + slot;
+                for (int kv = 0; kv < 2; kv++) {
+                    const uint16_t *src = (kv ? v_new : k_new) + (r * Hkv + g) * D;
+                    uint8_t *pool = kv ? v_pool : k_pool;
+                    uint8_t *sfp = kv ? v_sf : k_sf;
+                    float scale = kv ? v_scale : k_scale;
+                    for (int blk = 0; blk < D / 16; blk++) {
+                        float x[16];
+                        uint8_t codes[16], sf;
+                        for (int i = 0; i < 16; i++)
+                            x[i] = bf16_to_float(src[blk * 16 + i]);
+                        qsa_oracle_quantize_block(x, scale, codes, &sf);
+                        for (int i = 0; i < 16; i += 2)
+                            pool[row * (D / 2) + blk * 8 + i / 2] =
+                                (uint8_t)(codes[i] | (codes[i + 1] << 4));
+                        sfp[row * (D / 16) + blk] = sf;
+                    }
+                }
+            }
+            memcpy(ik_pool + ((int64_t)page * P + slot) * Di, ik_new + r * Di, (size_t)Di);
+        }
+    }
+    return 0;
 }

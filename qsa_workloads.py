@@ -282,6 +282,22 @@ def geometry(w: dict) -> dict:
                                    "page_size", "max_blocks", "num_pages")}
 
 
+def make_new_tokens(w: dict, seed: Optional[int] = None) -> dict:
+    """The step's new rows for the decode prologue: k_new, v_new ~ N(0, 1) as
+    bf16 [T, Hkv, D] and ik_new uniform int8 [T, Di] in [-127, 127], drawn in
+    that order from their own seeded generator (inputs only; the quantiser
+    lives in the library and in the oracle)."""
+    T = w["batch"] * w["rows_per_req"]
+    Hkv, D, Di = w["num_kv_heads"], w["head_dim"], w["index_dim"]
+    device = w["q"].device
+    gen = torch.Generator(device=device)
+    gen.manual_seed((w["case"].seed if seed is None else seed) + 1000003)
+    k_new = torch.randn((T, Hkv, D), generator=gen, device=device).to(torch.bfloat16)
+    v_new = torch.randn((T, Hkv, D), generator=gen, device=device).to(torch.bfloat16)
+    ik_new = _uniform_int(gen, -127, 127, (T, Di), device).to(torch.int8)
+    return {"k_new": k_new, "v_new": v_new, "ik_new": ik_new}
+
+
 def to_numpy(w: dict) -> dict:
     """Host copies of a workload's tensors (bf16 as raw uint16 bits)."""
     out = {}

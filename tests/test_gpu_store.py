@@ -1,0 +1,107 @@
+"""GPU parity of the decode prologue (qsa_store_kv_tokens) against the oracle.
+
+Every byte of every pool must match the oracle (stored codes, scales and index
+keys, and the untouched remainder), so the quantiser's rounding decisions are
+checked one by one.  A last test stores a step's tokens and then runs the
+step on the updated cache, against the oracle on the oracle's updated cache.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import qsa_workloads as qw
+
+pytestmark = pytest.mark.gpu
+
+POOLS = ("k_pool", "k_sf", "v_pool", "v_sf", "ik_pool")
+
+
+@pytest.fixture(scope="module")
+def qsa():
+    import nvfp4_block_sparse_gb300 as m
+    m.load(build_if_missing=True)
+    return m
+
+
+def store_gpu(qsa, w, new):
+    pools = {n: w[n].clone() for n in POOLS}
+    qsa.qsa_store_kv_tokens(qw.geometry(w), new["k_new"], new["v_new"], new["ik_new"],
+                            w["k_scale"], w["v_scale"], w["page_table"], w["seqlens"],
+                            pools["k_pool"], pools["k_sf"], pools["v_pool"], pools["v_sf"],
+                            pools["ik_pool"])
+    torch.cuda.synchronize()
+    return pools
+
+
+def check_store(qsa, w, new):
+    got = store_gpu(qsa, w, new)
+    ref = oracle.store_kv(qw.to_numpy(w), qw.to_numpy(new))
+    for n in POOLS:
+        np.testing.assert_array_equal(got[n].cpu().numpy(), ref[n], err_msg=n)
+    return got
+
+
+@pytest.mark.parametrize("cfg", range(5))
+def test_store_small_configs(qsa, cfg):
+    w = qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cuda")
+    check_store(qsa, w, qw.make_new_tokens(w))
+
+
+@pytest.mark.parametrize("cfg", [1, 4])
+def test_store_full_size(qsa, cfg):
+    w = qw.make_workload(qw.CONFIGS[cfg], "cuda")
+    check_store(qsa, w, qw.make_new_tokens(w))
+
+
+def _case(**kw):
+    base = dict(name="edge", seed=31, batch=3, rows_per_req=1, num_q_heads=8, num_kv_heads=2,
+                page_size=64, ctx_lo=700, ctx_hi=1300, k=6, window=2, max_blocks=21,
+                pool="perm")
+    base.update(kw)
+    return qw.Case(**base)
+
+
+STORE_CASES = {
+    "p128_verify": _case(page_size=128, rows_per_req=4, ctx_lo=129, ctx_hi=2600),
+    "tiny_contexts_verify": _case(rows_per_req=4, ctx_lo=1, ctx_hi=6, max_blocks=2, k=2, window=1),
+    "mostly_invalid": _case(invalid_frac=0.9, rows_per_req=3),
+    "eight_rows_one_kv_head": _case(rows_per_req=8, num_q_heads=4, num_kv_heads=1, k=5),
+}
+
+
+@pytest.mark.parametrize("name", sorted(STORE_CASES))
+def test_store_edge_cases(qsa, name):
+    w = qw.make_workload(STORE_CASES[name], "cuda")
+    check_store(qsa, w, qw.make_new_tokens(w))
+
+
+@pytest.mark.parametrize("mult", [1e4, 1e-7, 0.0])
+def test_store_saturation_underflow_and_zeros(qsa, mult):
+    # Values far above the tensor scale saturate the block scale (448) and
+    # the codes (6); values far below it flush the block to zero.
+    w = qw.make_workload(qw.small(qw.CONFIGS[2]), "cuda")
+    new = qw.make_new_tokens(w)
+    new["k_new"] = (new["k_new"].float() * mult).to(torch.bfloat16)
+    new["v_new"] = (new["v_new"].float() * mult).to(torch.bfloat16)
+    check_store(qsa, w, new)
+
+
+def test_store_then_step_matches_the_oracle(qsa):
+    w = qw.make_workload(qw.small(qw.CONFIGS[2]), "cuda")
+    new = qw.make_new_tokens(w)
+    got = store_gpu(qsa, w, new)
+    for n in POOLS:
+        w[n] = got[n]
+    step = qsa.DecodeStep(qw.geometry(w), w["k"], w["window"], device=w["q"].device)
+    step.run(w)
+    torch.cuda.synchronize()
+    assert qsa.qsa_workspace_status(step.workspace) == 0
+    ref = oracle.step(qw.to_numpy(w))
+    np.testing.assert_array_equal(step.scores.cpu().numpy(), ref["scores"])
+    np.testing.assert_array_equal(step.sel.cpu().numpy(), ref["sel"])
+    out = step.out.float().cpu().numpy().astype(np.float64)
+    assert np.abs(out - ref["out"]).max() <= 1e-2
+    lse = step.lse.cpu().numpy().astype(np.float64)
+    fin = np.isfinite(ref["lse"])
+    assert np.abs(lse[fin] - ref["lse"][fin]).max() <= 1e-3

@@ -413,3 +413,124 @@ def test_step_invariant_under_page_permutation():
     res2 = oracle.step(w2)
     for key in ("scores", "sel", "nsel", "out", "lse"):
         np.testing.assert_array_equal(res[key], res2[key])
+
+
+# ---------------------------------------------------------------------------
+# decode prologue: the NVFP4 quantiser and the token store
+# ---------------------------------------------------------------------------
+
+def test_e4m3_encode_round_trips_every_finite_code():
+    for c in range(0x7F):                       # 0x7F is NaN
+        assert oracle.e4m3_encode(oracle.e4m3(c)) == c
+
+
+def test_e4m3_encode_midpoints_go_to_the_even_code():
+    for c in range(0x7E):
+        lo, hi = oracle.e4m3(c), oracle.e4m3(c + 1)
+        mid = (lo + hi) / 2                      # exact in fp32 (5 significant bits)
+        assert oracle.e4m3_encode(mid) == (c if c % 2 == 0 else c + 1)
+        assert oracle.e4m3_encode(np.nextafter(np.float32(mid), np.float32(0))) == c
+        assert oracle.e4m3_encode(np.nextafter(np.float32(mid), np.float32(1e9))) == c + 1
+
+
+def test_e4m3_encode_saturates_and_flushes():
+    assert oracle.e4m3_encode(448.0) == 0x7E
+    assert oracle.e4m3_encode(1e30) == 0x7E
+    assert oracle.e4m3_encode(0.0) == 0
+    assert oracle.e4m3_encode(2.0 ** -10) == 0    # half the smallest subnormal: tie to 0
+    assert oracle.e4m3_encode(2.0 ** -10 * 1.0001) == 1
+
+
+def test_e4m3_encode_matches_torch_float8_cast():
+    rng = np.random.default_rng(5)
+    v = np.exp(rng.uniform(np.log(2.0 ** -12), np.log(448.0), 4000)).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(float(x)) for x in v], dtype=np.uint8)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_e2m1_encode_from_the_definition():
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for c, m in enumerate(mags):
+        assert oracle.e2m1_encode(m) == c
+        if c:
+            assert oracle.e2m1_encode(-m) == c | 8
+    # midpoints between neighbours go to the even code
+    for (a, b), want in zip(zip(mags, mags[1:]), [0, 2, 2, 4, 4, 6, 6]):
+        assert oracle.e2m1_encode((a + b) / 2) == want
+    assert oracle.e2m1_encode(7.5) == 7 and oracle.e2m1_encode(1e9) == 7
+    assert oracle.e2m1_encode(-1e9) == 15
+    assert oracle.e2m1_encode(-0.2) == 0        # rounds to zero: stored as +0
+    assert oracle.e2m1_encode(-0.3) == 9
+
+
+def test_quantize_block_round_trips_grid_values():
+    rng = np.random.default_rng(6)
+    mags = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    for _ in range(300):
+        scale = 2.0 ** int(rng.integers(-8, 3))
+        sf = int(rng.integers(0x08, 0x7E))      # a normal e4m3 scale
+        codes = rng.integers(1, 16, 16)
+        codes[codes == 8] = 1                   # no -0
+        codes[int(rng.integers(0, 16))] = 7 | (8 if rng.random() < 0.5 else 0)  # |x|max = 6
+        x = np.array([(-1 if c & 8 else 1) * mags[c & 7] for c in codes]) * oracle.e4m3(sf) * scale
+        got_codes, got_sf = oracle.quantize_block(x.astype(np.float32), scale)
+        assert got_sf == sf
+        np.testing.assert_array_equal(got_codes, codes)
+
+
+def test_quantize_block_zero_and_underflow():
+    codes, sf = oracle.quantize_block(np.zeros(16, np.float32), 0.5)
+    assert sf == 0 and not codes.any()
+    x = np.full(16, 1e-6, np.float32)
+    codes, sf = oracle.quantize_block(x, 1.0)    # (1e-6 / 6) / 1 is below half of 2^-9
+    assert sf == 0 and not codes.any()
+
+
+def test_quantize_matches_the_generators_encoder():
+    # The input generator's torch encoder (midpoint thresholds + torch's
+    # float8 cast) is an independent implementation of the same recipe.
+    g = torch.Generator().manual_seed(7)
+    x = torch.randn((64, 128), generator=g).to(torch.bfloat16).float()
+    packed, sfs, ts = qw.nvfp4_encode(x)
+    for r in range(64):
+        for blk in range(8):
+            codes, sf = oracle.quantize_block(x[r, 16 * blk:16 * blk + 16].numpy(), ts)
+            assert sf == int(sfs[r, blk])
+            np.testing.assert_array_equal(codes[0::2] | (codes[1::2] << 4),
+                                          packed[r, 8 * blk:8 * blk + 8].numpy())
+
+
+@pytest.mark.parametrize("cfg", [2, 4])
+def test_store_kv_writes_exactly_the_new_slots(cfg):
+    w = qw.to_numpy(qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cpu"))
+    new = qw.to_numpy(qw.make_new_tokens(qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cpu")))
+    out = oracle.store_kv(w, new)
+    B, R, P, MB, Hkv = w["batch"], w["rows_per_req"], w["page_size"], w["max_blocks"], w["num_kv_heads"]
+    rows = np.zeros((w["num_pages"], Hkv, P), bool)
+    keys = np.zeros((w["num_pages"], P), bool)
+    for b in range(B):
+        for j in range(R):
+            pos = int(w["seqlens"][b]) - R + j
+            if pos < 0 or pos >= MB * P:
+                continue
+            page = int(w["page_table"][b, pos // P])
+            if page < 0 or page >= w["num_pages"]:
+                continue
+            rows[page, :, pos % P] = True
+            keys[page, pos % P] = True
+            # the stored row decodes to the quantised new values
+            for g in range(Hkv):
+                xk = new["k_new"][b * R + j, g].astype(np.uint32) << 16
+                xk = xk.view(np.float32)
+                for blk in range(8):
+                    codes, sf = oracle.quantize_block(xk[16 * blk:16 * blk + 16], w["k_scale"])
+                    assert out["k_sf"].reshape(-1, Hkv, P, 8)[page, g, pos % P, blk] == sf
+            np.testing.assert_array_equal(out["ik_pool"].reshape(-1, P, 64)[page, pos % P],
+                                          new["ik_new"][b * R + j])
+    for name, mask in (("k_pool", rows), ("v_pool", rows), ("k_sf", rows), ("v_sf", rows),
+                       ("ik_pool", keys)):
+        before = w[name].reshape(mask.shape + (-1,))
+        after = out[name].reshape(mask.shape + (-1,))
+        np.testing.assert_array_equal(after[~mask], before[~mask])
+    assert rows.any()
