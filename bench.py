@@ -146,6 +146,51 @@ def time_prologue(qsa, step, reps, stream, nrep):
             "launches_per_call": 1}
 
 
+def time_rollback(qsa, step, reps, stream, nrep):
+    """qsa_rollback_gather and qsa_rollback_restore (every other row rejected)
+    per replica, graph-replayed between CUDA events: us per call and bytes
+    moved (each saved row is read once and written once)."""
+    w = reps[0]
+    T = w["batch"] * w["rows_per_req"]
+    nb = qsa.qsa_rollback_state_bytes(step.cg)
+    saved = [torch.zeros(nb, dtype=torch.uint8, device=w["q"].device) for _ in range(nrep)]
+    rejected = (torch.arange(T, device=w["q"].device) % 2 == 1).to(torch.int32)
+    out = {}
+    for name in ("gather", "restore"):
+        def run(i, name=name):
+            r = reps[i]
+            if name == "gather":
+                qsa.qsa_rollback_gather(step.cg, r["page_table"], r["seqlens"], r["k_pool"],
+                                        r["k_sf"], r["v_pool"], r["v_sf"], r["ik_pool"],
+                                        saved[i], stream)
+            else:
+                qsa.qsa_rollback_restore(step.cg, r["page_table"], r["seqlens"], rejected,
+                                         saved[i], r["k_pool"], r["k_sf"], r["v_pool"], r["v_sf"],
+                                         r["ik_pool"], stream)
+        with torch.cuda.stream(stream):
+            for i in range(nrep):
+                run(i)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(nrep):
+                    run(i)
+            g.replay()
+            stream.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            n_rep = max(20, 2000 // nrep)
+            e0.record(stream)
+            for _ in range(n_rep):
+                g.replay()
+            e1.record(stream)
+            stream.synchronize()
+        out[name + "_us_per_call"] = e0.elapsed_time(e1) * 1e3 / (n_rep * nrep)
+    out["saved_bytes_per_call"] = nb
+    out["bound"] = "latency (one saved row per query row)"
+    return out
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling while the timed region runs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -428,6 +473,7 @@ def run_qsa(args, case):
 
     # ---- decode prologue (store the step's new tokens), after every other
     # measurement because it writes into the replicas' caches ---------------
+    rollback = time_rollback(qsa, step, reps, stream, nrep)
     prologue = time_prologue(qsa, step, reps, stream, nrep)
 
     # ---- CPU baseline (rank 0, N = 1 only) -----------------------------------
@@ -478,6 +524,7 @@ def run_qsa(args, case):
         "gpu_launches": 3 * args.steps,
         "cpu_baseline": cpu,
         "prologue": prologue,
+        "rollback": rollback,
     }
     print(json.dumps(line), flush=True)
 

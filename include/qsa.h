@@ -267,6 +267,44 @@ qsa_status_t qsa_store_kv_tokens(const qsa_geom_t *geom, const void *k_new_bf16,
                                  uint8_t *v_sf, int8_t *ik_pool, cudaStream_t stream);
 
 /*
+ * Speculative rollback of the cache for rejected draft rows.  TensorRT-LLM PR
+ * #20937 ("GB300 perf work on qwen3_8_flash_next_nvfp4__sm_103__tp1"), What
+ * changes (Rollback and PLE): batched rollback of the QSA index planes; the
+ * rollback gather / restore operations; review of their test: rejected rows
+ * get their old values back, kept rows stay untouched.
+ *
+ * A verify step stores its R new rows into the slots at positions
+ * L_b - R + j (qsa_store_kv_tokens).  Call qsa_rollback_gather with the
+ * step's page_table and seqlens BEFORE that store: it copies what those slots
+ * hold now into `saved`.  After the step, qsa_rollback_restore writes the
+ * saved bytes back for every row r with rejected[r] != 0 and leaves the other
+ * rows' slots as the step left them.  Rows without a slot (negative position,
+ * position at or past MB*P, invalid page) are skipped by both calls.
+ *
+ *   saved     device bytes, qsa_rollback_state_bytes(geom) long, 4-byte
+ *             aligned, owned by the caller; row r's part starts at
+ *             r * (144 * Hkv + 64) and holds, per KV head, the K codes (64 B),
+ *             K scales (8), V codes (64), V scales (8), then the index key (64)
+ *   rejected  int32 [T], nonzero for a rejected row
+ *   pools     as in qsa_store_kv_tokens (4-byte aligned here)
+ *
+ * The caller updates seqlens for the accepted prefix itself.  Returns
+ * QSA_ERR_INVALID_ARG for null or misaligned pointers; geometry and device
+ * checks as for the other calls.
+ */
+size_t qsa_rollback_state_bytes(const qsa_geom_t *geom);
+qsa_status_t qsa_rollback_gather(const qsa_geom_t *geom, const int32_t *page_table,
+                                 const int32_t *seqlens, const uint8_t *k_pool,
+                                 const uint8_t *k_sf, const uint8_t *v_pool,
+                                 const uint8_t *v_sf, const int8_t *ik_pool, void *saved,
+                                 cudaStream_t stream);
+qsa_status_t qsa_rollback_restore(const qsa_geom_t *geom, const int32_t *page_table,
+                                  const int32_t *seqlens, const int32_t *rejected,
+                                  const void *saved, uint8_t *k_pool, uint8_t *k_sf,
+                                  uint8_t *v_pool, uint8_t *v_sf, int8_t *ik_pool,
+                                  cudaStream_t stream);
+
+/*
  * Reads the workspace's device status word (synchronising `stream`): 0 when
  * every bounded wait since qsa_workspace_init() completed, otherwise a
  * nonzero code and QSA_ERR_DEVICE_TIMEOUT is returned.  Diagnostic only.

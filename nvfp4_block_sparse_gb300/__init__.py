@@ -15,6 +15,7 @@ import torch
 from .binding import (EXPORTS, QsaError, load, make_geom, qsa_geom_t, qsa_index_scores,
                       qsa_select_topk, qsa_sparse_decode, qsa_sparse_decode_ex, qsa_sparse_decode_noalloc,
                       qsa_sparse_decode_workspace_bytes, qsa_sparse_decode_workspace_bytes_ex,
+                      qsa_rollback_gather, qsa_rollback_restore, qsa_rollback_state_bytes,
                       qsa_status_string, qsa_store_kv_tokens, qsa_workspace_init,
                       qsa_workspace_status)
 
@@ -22,6 +23,7 @@ __all__ = [
     "EXPORTS", "QsaError", "load", "make_geom", "qsa_geom_t", "qsa_index_scores",
     "qsa_select_topk", "qsa_sparse_decode", "qsa_sparse_decode_ex", "qsa_sparse_decode_noalloc",
     "qsa_sparse_decode_workspace_bytes", "qsa_sparse_decode_workspace_bytes_ex",
+    "qsa_rollback_gather", "qsa_rollback_restore", "qsa_rollback_state_bytes",
     "qsa_status_string", "qsa_store_kv_tokens", "qsa_workspace_init", "qsa_workspace_status",
     "DecodeStep",
 ]

@@ -33,6 +33,9 @@ EXPORTS = (
     "qsa_sparse_decode_noalloc",
     "qsa_workspace_status",
     "qsa_store_kv_tokens",
+    "qsa_rollback_state_bytes",
+    "qsa_rollback_gather",
+    "qsa_rollback_restore",
 )
 
 
@@ -95,6 +98,12 @@ def load(build_if_missing: bool = False):
     lib.qsa_store_kv_tokens.restype = st
     lib.qsa_store_kv_tokens.argtypes = [G, _vp, _vp, _vp, ctypes.c_float, ctypes.c_float, _vp,
                                         _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.qsa_rollback_state_bytes.restype = ctypes.c_size_t
+    lib.qsa_rollback_state_bytes.argtypes = [G]
+    lib.qsa_rollback_gather.restype = st
+    lib.qsa_rollback_gather.argtypes = [G] + [_vp] * 9
+    lib.qsa_rollback_restore.restype = st
+    lib.qsa_rollback_restore.argtypes = [G] + [_vp] * 10
     lib.qsa_workspace_status.restype = st
     lib.qsa_workspace_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int), _vp]
     _lib = lib
@@ -154,6 +163,33 @@ def qsa_store_kv_tokens(geom, k_new, v_new, ik_new, k_scale, v_scale, page_table
         _ptr(k_pool, torch.uint8, "k_pool"), _ptr(k_sf, torch.uint8, "k_sf"),
         _ptr(v_pool, torch.uint8, "v_pool"), _ptr(v_sf, torch.uint8, "v_sf"),
         _ptr(ik_pool, torch.int8, "ik_pool"), _stream(stream)))
+
+
+def qsa_rollback_state_bytes(geom) -> int:
+    g = _geom(geom)
+    return int(load().qsa_rollback_state_bytes(ctypes.byref(g)))
+
+
+def qsa_rollback_gather(geom, page_table, seqlens, k_pool, k_sf, v_pool, v_sf, ik_pool, saved,
+                        stream=None):
+    g = _geom(geom)
+    _check("qsa_rollback_gather", load().qsa_rollback_gather(
+        ctypes.byref(g), _ptr(page_table, torch.int32, "page_table"),
+        _ptr(seqlens, torch.int32, "seqlens"), _ptr(k_pool, torch.uint8, "k_pool"),
+        _ptr(k_sf, torch.uint8, "k_sf"), _ptr(v_pool, torch.uint8, "v_pool"),
+        _ptr(v_sf, torch.uint8, "v_sf"), _ptr(ik_pool, torch.int8, "ik_pool"),
+        _ptr(saved, torch.uint8, "saved"), _stream(stream)))
+
+
+def qsa_rollback_restore(geom, page_table, seqlens, rejected, saved, k_pool, k_sf, v_pool, v_sf,
+                         ik_pool, stream=None):
+    g = _geom(geom)
+    _check("qsa_rollback_restore", load().qsa_rollback_restore(
+        ctypes.byref(g), _ptr(page_table, torch.int32, "page_table"),
+        _ptr(seqlens, torch.int32, "seqlens"), _ptr(rejected, torch.int32, "rejected"),
+        _ptr(saved, torch.uint8, "saved"), _ptr(k_pool, torch.uint8, "k_pool"),
+        _ptr(k_sf, torch.uint8, "k_sf"), _ptr(v_pool, torch.uint8, "v_pool"),
+        _ptr(v_sf, torch.uint8, "v_sf"), _ptr(ik_pool, torch.int8, "ik_pool"), _stream(stream)))
 
 
 def qsa_select_topk(geom, scores, seqlens, k, window, sel, nsel, stream=None):

@@ -119,6 +119,51 @@ qsa_status_t qsa_store_kv_tokens(const qsa_geom_t* geom, const void* k_new_bf16,
                                             v_pool, v_sf, ik_pool, true, stream));
 }
 
+size_t qsa_rollback_state_bytes(const qsa_geom_t* geom) {
+  if (check_geom(geom) != QSA_OK) return 0;
+  return (size_t)geom->batch * geom->rows_per_req * qsa::rollback_row_bytes(geom->num_kv_heads);
+}
+
+qsa_status_t qsa_rollback_gather(const qsa_geom_t* geom, const int32_t* page_table,
+                                 const int32_t* seqlens, const uint8_t* k_pool,
+                                 const uint8_t* k_sf, const uint8_t* v_pool, const uint8_t* v_sf,
+                                 const int8_t* ik_pool, void* saved, cudaStream_t stream) {
+  qsa_status_t st = check_geom(geom);
+  if (st != QSA_OK) return st;
+  if (!page_table || !seqlens || !k_pool || !k_sf || !v_pool || !v_sf || !ik_pool || !saved)
+    return QSA_ERR_INVALID_ARG;
+  if (!aligned(k_pool, 4) || !aligned(k_sf, 4) || !aligned(v_pool, 4) || !aligned(v_sf, 4) ||
+      !aligned(ik_pool, 4) || !aligned(saved, 4))
+    return QSA_ERR_INVALID_ARG;
+  st = check_device();
+  if (st != QSA_OK) return st;
+  return from_cuda(qsa::launch_rollback(
+      to_geom(geom), false, page_table, seqlens, nullptr, const_cast<uint8_t*>(k_pool),
+      const_cast<uint8_t*>(k_sf), const_cast<uint8_t*>(v_pool), const_cast<uint8_t*>(v_sf),
+      const_cast<int8_t*>(ik_pool), reinterpret_cast<uint8_t*>(saved), true, stream));
+}
+
+qsa_status_t qsa_rollback_restore(const qsa_geom_t* geom, const int32_t* page_table,
+                                  const int32_t* seqlens, const int32_t* rejected,
+                                  const void* saved, uint8_t* k_pool, uint8_t* k_sf,
+                                  uint8_t* v_pool, uint8_t* v_sf, int8_t* ik_pool,
+                                  cudaStream_t stream) {
+  qsa_status_t st = check_geom(geom);
+  if (st != QSA_OK) return st;
+  if (!page_table || !seqlens || !rejected || !saved || !k_pool || !k_sf || !v_pool || !v_sf ||
+      !ik_pool)
+    return QSA_ERR_INVALID_ARG;
+  if (!aligned(k_pool, 4) || !aligned(k_sf, 4) || !aligned(v_pool, 4) || !aligned(v_sf, 4) ||
+      !aligned(ik_pool, 4) || !aligned(saved, 4))
+    return QSA_ERR_INVALID_ARG;
+  st = check_device();
+  if (st != QSA_OK) return st;
+  return from_cuda(qsa::launch_rollback(to_geom(geom), true, page_table, seqlens, rejected,
+                                        k_pool, k_sf, v_pool, v_sf, ik_pool,
+                                        const_cast<uint8_t*>(reinterpret_cast<const uint8_t*>(saved)),
+                                        true, stream));
+}
+
 qsa_status_t qsa_index_scores(const qsa_geom_t* geom, const int8_t* iq, const int8_t* ik_pool,
                               const int32_t* page_table, const int32_t* seqlens,
                               int32_t* scores, cudaStream_t stream) {

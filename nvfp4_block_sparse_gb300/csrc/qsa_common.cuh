@@ -186,6 +186,11 @@ struct Geom {
   int B, R, Hq, Hkv, D, Di, P, MB, NP;
 };
 
+size_t rollback_row_bytes(int hkv);
+cudaError_t launch_rollback(const Geom& g, bool restore, const int32_t* page_table,
+                            const int32_t* seqlens, const int32_t* rejected, uint8_t* k_pool,
+                            uint8_t* k_sf, uint8_t* v_pool, uint8_t* v_sf, int8_t* ik_pool,
+                            uint8_t* saved, bool pdl, cudaStream_t stream);
 cudaError_t launch_store_tokens(const Geom& g, const void* k_new, const void* v_new,
                                 const int8_t* ik_new, float k_scale, float v_scale,
                                 const int32_t* page_table, const int32_t* seqlens,

@@ -53,6 +53,8 @@ def _load():
         lib.qsa_oracle_quantize_block.restype = None
         lib.qsa_oracle_quantize_block.argtypes = [ctypes.c_void_p, ctypes.c_float,
                                                   ctypes.c_void_p, ctypes.c_void_p]
+        lib.qsa_oracle_rollback.restype = ctypes.c_int
+        lib.qsa_oracle_rollback.argtypes = [ctypes.c_int] * 9 + [ctypes.c_void_p] * 9
         lib.qsa_oracle_store_kv.restype = ctypes.c_int
         lib.qsa_oracle_store_kv.argtypes = ([ctypes.c_int] * 8 + [ctypes.c_void_p] * 3 +
                                             [ctypes.c_float] * 2 + [ctypes.c_void_p] * 7)
@@ -203,3 +205,40 @@ def store_kv(w: dict, new: dict) -> dict:
     if st != 0:
         raise RuntimeError("qsa_oracle_store_kv failed (%d)" % st)
     return out
+
+
+def rollback_state_bytes(w: dict) -> int:
+    return (w["batch"] * w["rows_per_req"] *
+            (w["num_kv_heads"] * 2 * (w["head_dim"] // 2 + w["head_dim"] // 16) + w["index_dim"]))
+
+
+def rollback_gather(w: dict, pools: dict, saved: np.ndarray = None) -> np.ndarray:
+    """Saved state of the slots the step's rows own (bytes the rows own no
+    slot for are left as given, zero by default)."""
+    saved = (np.zeros(rollback_state_bytes(w), np.uint8) if saved is None
+             else np.ascontiguousarray(saved, dtype=np.uint8).copy())
+    p = {n: np.ascontiguousarray(pools[n]).copy() for n in ("k_pool", "k_sf", "v_pool", "v_sf",
+                                                             "ik_pool")}
+    _rollback(0, w, None, p, saved)
+    return saved
+
+
+def rollback_restore(w: dict, pools: dict, rejected: np.ndarray, saved: np.ndarray) -> dict:
+    """Pools with the rejected rows' slots set back to ``saved``."""
+    p = {n: np.ascontiguousarray(pools[n]).copy() for n in ("k_pool", "k_sf", "v_pool", "v_sf",
+                                                             "ik_pool")}
+    _rollback(1, w, np.ascontiguousarray(rejected, dtype=np.int32), p,
+              np.ascontiguousarray(saved, dtype=np.uint8).copy())
+    return p
+
+
+def _rollback(restore, w, rejected, p, saved):
+    rej = rejected if rejected is not None else np.zeros(1, np.int32)
+    st = _load().qsa_oracle_rollback(
+        restore, w["batch"], w["rows_per_req"], w["num_kv_heads"], w["head_dim"],
+        w["index_dim"], w["page_size"], w["max_blocks"], w["num_pages"],
+        _p(np.ascontiguousarray(w["page_table"], dtype=np.int32)),
+        _p(np.ascontiguousarray(w["seqlens"], dtype=np.int32)), _p(rej), _p(p["k_pool"]),
+        _p(p["k_sf"]), _p(p["v_pool"]), _p(p["v_sf"]), _p(p["ik_pool"]), _p(saved))
+    if st != 0:
+        raise RuntimeError("qsa_oracle_rollback failed (%d)" % st)

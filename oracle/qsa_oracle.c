@@ -472,3 +472,68 @@ int qsa_oracle_store_kv(int B, int R, int Hkv, int D, int Di, int P, int MB, int
     }
     return 0;
 }
+
+/* ---- speculative rollback of the cache planes ---------------------------
+ *
+ * TensorRT-LLM PR #20937 "GB300 perf work on
+ * qwen3_8_flash_next_nvfp4__sm_103__tp1", What changes (Rollback and PLE):
+ * batched rollback of the QSA index planes; rollback gather / restore of the
+ * planes, whose test restores the rejected rows' old values and leaves kept
+ * rows untouched.  Row r = b*R + j owns the slot at position L_b - R + j
+ * (skipped when negative, at or past MB*P, or on an invalid page).  Saved
+ * state of row r, at r * (144*Hkv + 64): per KV head K codes (D/2), K scales
+ * (D/16), V codes (D/2), V scales (D/16); then the index key (Di).
+ */
+static int row_slot(int b, int R, int j, int P, int MB, int NP, const int32_t *page_table,
+                    const int32_t *seqlens, int32_t *page, int *slot)
+{
+    int64_t pos = (int64_t)seqlens[b] - R + j;
+    if (pos < 0 || pos >= (int64_t)MB * P)
+        return 0;
+    *page = page_table[(int64_t)b * MB + pos / P];
+    if (*page < 0 || *page >= NP)
+        return 0;
+    *slot = (int)(pos % P);
+    return 1;
+}
+
+/* restore == 0: pools -> saved (every row with a slot);
+ * restore != 0: saved -> pools (rows with a slot and rejected[r] != 0). */
+int qsa_oracle_rollback(int restore, int B, int R, int Hkv, int D, int Di, int P, int MB, int NP,
+                        const int32_t *page_table, const int32_t *seqlens,
+                        const int32_t *rejected, uint8_t *k_pool, uint8_t *k_sf,
+                        uint8_t *v_pool, uint8_t *v_sf, int8_t *ik_pool, uint8_t *saved)
+{
+    int64_t row_bytes = (int64_t)Hkv * (2 * (D / 2 + D / 16)) + Di;
+    for (int b = 0; b < B; b++) {
+        for (int j = 0; j < R; j++) {
+            int64_t r = (int64_t)b * R + j;
+            int32_t page;
+            int slot;
+            if (!row_slot(b, R, j, P, MB, NP, page_table, seqlens, &page, &slot))
+                continue;
+            if (restore && rejected[r] == 0)
+                continue;
+            uint8_t *s = saved + r * row_bytes;
+            for (int g = 0; g < Hkv; g++) {
+                int64_t row = ((int64_t)page * Hkv + g) * P + slot;
+                uint8_t *parts[4] = {k_pool + row * (D / 2), k_sf + row * (D / 16),
+                                     v_pool + row * (D / 2), v_sf + row * (D / 16)};
+                int sizes[4] = {D / 2, D / 16, D / 2, D / 16};
+                for (int q = 0; q < 4; q++) {
+                    if (restore)
+                        memcpy(parts[q], s, (size_t)sizes[q]);
+                    else
+                        memcpy(s, parts[q], (size_t)sizes[q]);
+                    s += sizes[q];
+                }
+            }
+            int8_t *key = ik_pool + ((int64_t)page * P + slot) * Di;
+            if (restore)
+                memcpy(key, s, (size_t)Di);
+            else
+                memcpy(s, key, (size_t)Di);
+        }
+    }
+    return 0;
+}

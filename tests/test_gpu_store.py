@@ -105,3 +105,53 @@ def test_store_then_step_matches_the_oracle(qsa):
     lse = step.lse.cpu().numpy().astype(np.float64)
     fin = np.isfinite(ref["lse"])
     assert np.abs(lse[fin] - ref["lse"][fin]).max() <= 1e-3
+
+
+# ---------------------------------------------------------------------------
+# speculative rollback: gather before the store, restore the rejected rows
+# ---------------------------------------------------------------------------
+
+def gather_gpu(qsa, w, pools):
+    saved = torch.zeros(qsa.qsa_rollback_state_bytes(qw.geometry(w)), dtype=torch.uint8,
+                        device=w["q"].device)
+    qsa.qsa_rollback_gather(qw.geometry(w), w["page_table"], w["seqlens"], pools["k_pool"],
+                            pools["k_sf"], pools["v_pool"], pools["v_sf"], pools["ik_pool"], saved)
+    return saved
+
+
+def restore_gpu(qsa, w, pools, rejected, saved):
+    qsa.qsa_rollback_restore(qw.geometry(w), w["page_table"], w["seqlens"], rejected, saved,
+                             pools["k_pool"], pools["k_sf"], pools["v_pool"], pools["v_sf"],
+                             pools["ik_pool"])
+    torch.cuda.synchronize()
+
+
+ROLLBACK_CASES = [("cfg2", lambda: qw.small(qw.CONFIGS[2])), ("cfg4", lambda: qw.small(qw.CONFIGS[4])),
+                  ("tiny", lambda: STORE_CASES["tiny_contexts_verify"]),
+                  ("invalid", lambda: STORE_CASES["mostly_invalid"]),
+                  ("full4", lambda: qw.CONFIGS[4])]
+
+
+@pytest.mark.parametrize("name,make", ROLLBACK_CASES, ids=[c[0] for c in ROLLBACK_CASES])
+def test_rollback_matches_oracle(qsa, name, make):
+    w = qw.make_workload(make(), "cuda")
+    new = qw.make_new_tokens(w)
+    T = w["batch"] * w["rows_per_req"]
+    w_np = qw.to_numpy(w)
+    saved = gather_gpu(qsa, w, {n: w[n] for n in POOLS})
+    torch.cuda.synchronize()
+    ref_saved = oracle.rollback_gather(w_np, w_np)
+    # bytes of rows without a slot stay as allocated (zero) on both sides
+    np.testing.assert_array_equal(saved.cpu().numpy(), ref_saved)
+    stored = store_gpu(qsa, w, new)
+    ref_stored = oracle.store_kv(w_np, qw.to_numpy(new))
+    for rej_np in (np.ones(T, np.int32), np.zeros(T, np.int32),
+                   (np.arange(T) % 2 == 1).astype(np.int32)):
+        pools = {n: stored[n].clone() for n in POOLS}
+        restore_gpu(qsa, w, pools, torch.from_numpy(rej_np).to(w["q"].device), saved)
+        ref = oracle.rollback_restore(w_np, ref_stored, rej_np, ref_saved)
+        for n in POOLS:
+            np.testing.assert_array_equal(pools[n].cpu().numpy(), ref[n], err_msg=n)
+        if rej_np.all():
+            for n in POOLS:      # everything rejected: the cache is back, byte for byte
+                np.testing.assert_array_equal(pools[n].cpu().numpy(), w_np[n], err_msg=n)

@@ -534,3 +534,72 @@ def test_store_kv_writes_exactly_the_new_slots(cfg):
         after = out[name].reshape(mask.shape + (-1,))
         np.testing.assert_array_equal(after[~mask], before[~mask])
     assert rows.any()
+
+
+# ---------------------------------------------------------------------------
+# speculative rollback of the cache planes
+# ---------------------------------------------------------------------------
+
+def _half_rejected(T):
+    # exactly half the rows rejected, interleaved (kept and rejected both occur)
+    return (np.arange(T) % 2 == 1).astype(np.int32)
+
+
+@pytest.mark.parametrize("cfg", [2, 4])
+def test_rollback_round_trip(cfg):
+    w = qw.to_numpy(qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cpu"))
+    new = qw.to_numpy(qw.make_new_tokens(qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cpu")))
+    names = ("k_pool", "k_sf", "v_pool", "v_sf", "ik_pool")
+    saved = oracle.rollback_gather(w, w)
+    stored = oracle.store_kv(w, new)
+    T = w["batch"] * w["rows_per_req"]
+    # every row rejected: the cache is back to what it was, byte for byte
+    back = oracle.rollback_restore(w, stored, np.ones(T, np.int32), saved)
+    for n in names:
+        np.testing.assert_array_equal(back[n], w[n])
+    # no row rejected: the step's stores stay
+    keep = oracle.rollback_restore(w, stored, np.zeros(T, np.int32), saved)
+    for n in names:
+        np.testing.assert_array_equal(keep[n], stored[n])
+    # half rejected: exactly the rejected rows' slots go back
+    rej = _half_rejected(T)
+    mixed = oracle.rollback_restore(w, stored, rej, saved)
+    # slots of rejected rows equal the original, those of kept rows the store
+    rows_rej = np.zeros(T, bool)
+    rows_rej[rej == 1] = True
+    P, R, Hkv = w["page_size"], w["rows_per_req"], w["num_kv_heads"]
+    for r in range(T):
+        b, j = divmod(r, R)
+        pos = int(w["seqlens"][b]) - R + j
+        if pos < 0 or pos >= w["max_blocks"] * P:
+            continue
+        page = int(w["page_table"][b, pos // P])
+        if page < 0 or page >= w["num_pages"]:
+            continue
+        want = w if rows_rej[r] else stored
+        kp = mixed["k_pool"].reshape(-1, Hkv, P, 64)[page, :, pos % P]
+        np.testing.assert_array_equal(kp, want["k_pool"].reshape(-1, Hkv, P, 64)[page, :, pos % P])
+        ik = mixed["ik_pool"].reshape(-1, P, 64)[page, pos % P]
+        np.testing.assert_array_equal(ik, want["ik_pool"].reshape(-1, P, 64)[page, pos % P])
+    assert rows_rej.any() and (~rows_rej).any()
+
+
+def test_rollback_saved_layout():
+    # the saved bytes of a row are its slots' bytes in the documented order
+    w = qw.to_numpy(qw.make_workload(qw.small(qw.CONFIGS[2]), "cpu"))
+    saved = oracle.rollback_gather(w, w)
+    Hkv, P, R = w["num_kv_heads"], w["page_size"], w["rows_per_req"]
+    row_bytes = Hkv * 144 + 64
+    b, j = 1, 2
+    r = b * R + j
+    pos = int(w["seqlens"][b]) - R + j
+    page = int(w["page_table"][b, pos // P])
+    s = saved[r * row_bytes:(r + 1) * row_bytes]
+    for g in range(Hkv):
+        part = s[g * 144:(g + 1) * 144]
+        np.testing.assert_array_equal(part[:64], w["k_pool"].reshape(-1, Hkv, P, 64)[page, g, pos % P])
+        np.testing.assert_array_equal(part[64:72], w["k_sf"].reshape(-1, Hkv, P, 8)[page, g, pos % P])
+        np.testing.assert_array_equal(part[72:136], w["v_pool"].reshape(-1, Hkv, P, 64)[page, g, pos % P])
+        np.testing.assert_array_equal(part[136:144], w["v_sf"].reshape(-1, Hkv, P, 8)[page, g, pos % P])
+    np.testing.assert_array_equal(s[Hkv * 144:].view(np.int8),
+                                  w["ik_pool"].reshape(-1, P, 64)[page, pos % P])
