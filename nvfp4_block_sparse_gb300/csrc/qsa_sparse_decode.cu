@@ -111,6 +111,12 @@ __device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&o)[4]) 
       : "r"(w));
 }
 
+// Chunks a decode warp can own: the row's k entries of up to two 64-token
+// chunks, dealt over splits * W warps.
+__host__ __device__ inline int decode_list_cap(int k, int splits, int W) {
+  return (2 * k + splits * W - 1) / (splits * W);
+}
+
 // Shared-memory layout (bytes), shared by host sizing and the kernel.  ONE:
 // the single-row specialisation (no producer warp; W consumer warps).
 template <int NTR, int W, int S, bool ONE>
@@ -149,7 +155,13 @@ struct Layout {
     off += (size_t)R * kHsp * kHeadDim * 2;             // q (fp16)
     off += (size_t)R * kHsp * 4 * 2;                    // cq, n per column
     off += 64 * 4;                                      // scalars
-    off += (size_t)R * k * 4 * 4 + 16;                  // sel rows, union ids, pages, scan
+    // sel rows, union ids, pages, scan (verify) / per-warp chunk lists (decode)
+    size_t sel_bytes = (size_t)R * k * 4 * 4 + 16;
+    if (ONE) {
+      const size_t lists = (size_t)W * 2 * decode_list_cap(k, splits, W) * 4;
+      if (lists > sel_bytes) sel_bytes = lists;
+    }
+    off += sel_bytes;
     off += mb <= kPtRowMax ? (size_t)mb * 4 : 0;        // page-table row
     return off;
   }
@@ -411,7 +423,8 @@ sparse_decode_kernel(Params p) {
   int32_t* s_union = s_sel + R * k;
   int32_t* s_upage = s_union + R * k;
   int32_t* s_scan = s_upage + R * k;                  // [R * k + 1]
-  int32_t* s_pt = s_scan + R * k + 4;
+  const int list_ints = ONE ? W * 2 * decode_list_cap(k, p.splits, W) : 0;
+  int32_t* s_pt = s_sel + (list_ints > R * k * 4 + 4 ? list_ints : R * k * 4 + 4);
 
   // full[st]: one arrival (the copy issuer) plus the copies' bytes.  empty[st]
   // (verify only): every row consumer arrives, so stage reuse waits for all.
@@ -480,8 +493,45 @@ sparse_decode_kernel(Params p) {
     }
   }
 
-  pdl_wait();   // the selections come from the preceding kernel
+  __syncthreads();   // barriers, page-table row and queries visible to every warp
+  pdl_wait();        // the selections come from the preceding kernel
 
+  const int csh = (g.P == 2 * kChunk) ? 1 : 0;  // chunks per page: 1 << csh
+  // Decode: each warp lists its own chunks straight from the selection (no
+  // union and no CTA-wide barrier before the first copies).  Candidate chunk c
+  // of the row (entry c >> csh, part c & csh) belongs to split c mod splits and,
+  // within it, to warp (c / splits) mod W.  An entry equal to its predecessor
+  // (the selection is ascending) or on an invalid page is dropped.
+  int* wl = s_sel + warp * 2 * decode_list_cap(k, p.splits, W);   // (page, tok0) pairs
+  int wcnt = 0;
+  if (ONE) {
+    const int nc = k << csh;
+    for (int t0 = 0;; t0 += 32) {
+      if (s + (long long)p.splits * (warp + (long long)W * t0) >= nc) break;
+      const long long c = s + (long long)p.splits * (warp + (long long)W * (t0 + lane));
+      int page = -1, tok0 = 0;
+      if (c < nc) {
+        const int e = (int)(c >> csh);
+        const int beta = p.sel[(size_t)b * k + e];
+        const int prev = e > 0 ? p.sel[(size_t)b * k + e - 1] : -1;
+        if (beta >= 0 && beta < g.MB && beta != prev) {
+          const int pg = pt_in_smem ? s_pt[beta] : p.page_table[(size_t)b * g.MB + beta];
+          if (pg >= 0 && pg < g.NP) {
+            page = pg;
+            tok0 = beta * g.P + (int)(c & csh) * kChunk;
+          }
+        }
+      }
+      const unsigned vm = __ballot_sync(0xffffffffu, page >= 0);
+      if (page >= 0) {
+        const int q = wcnt + __popc(vm & ((1u << lane) - 1u));
+        wl[2 * q] = page;
+        wl[2 * q + 1] = tok0;
+      }
+      wcnt += __popc(vm);
+    }
+    __syncwarp();
+  } else {
   for (int i = tid; i < R * k; i += kThreads) {
     const int v = p.sel[(size_t)b * R * k + i];
     s_sel[i] = (v >= 0 && v < g.MB) ? v : -1;
@@ -622,10 +672,10 @@ sparse_decode_kernel(Params p) {
     }
   }
   __syncthreads();
+  }   // verify union
   pdl_trigger();
 
-  const int U = s_scan[R * k];
-  const int csh = (g.P == 2 * kChunk) ? 1 : 0;  // chunks per page: 1 << csh
+  const int U = ONE ? 0 : s_scan[R * k];
   const int C = U << csh;
   // Split s takes union chunks s, s + splits, ... so every split gets an even
   // share of every row's pages.
@@ -694,12 +744,22 @@ sparse_decode_kernel(Params p) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) o_acc[dt][nt][e] = 0.f;
 
-  // The stage region held the union's temporaries (generic-proxy writes):
-  // order them before the first copies into it.
-  if (ONE && lane == 0) {
-    fence_proxy_async_smem();
-    for (int i = warp; i < min(S, n_ch); i += W) issue(i);
-  }
+  // Decode: this warp's q-th chunk goes to stage warp + W * (q mod S/W).
+  constexpr int kSpw = ONE ? S / W : 1;          // stages per decode warp
+  auto issue_one = [&](int q) {
+    const int st = warp + W * (q % kSpw);
+    const int page = wl[2 * q], tok0 = wl[2 * q + 1];
+    const size_t row0 = ((size_t)page * g.Hkv + kvh) * g.P + (size_t)(tok0 & (g.P - 1));
+    uint8_t* dst = region + st * kStageBytes;
+    mbar_arrive_expect_tx(&full[st], kStageBytes);
+    bulk_g2s(dst, p.k_pool + row0 * (kHeadDim / 2), kKBytes, &full[st], pol);
+    bulk_g2s(dst + kKBytes, p.v_pool + row0 * (kHeadDim / 2), kKBytes, &full[st], pol);
+    bulk_g2s(dst + 2 * kKBytes, p.k_sf + row0 * (kHeadDim / 16), kSfBytes, &full[st], pol);
+    bulk_g2s(dst + 2 * kKBytes + kSfBytes, p.v_sf + row0 * (kHeadDim / 16), kSfBytes, &full[st],
+             pol);
+  };
+  if (ONE && lane == 0)
+    for (int q = 0; q < min(kSpw, wcnt); ++q) issue_one(q);
 
   if (!producer) {
     const int cbase = jw * kHsp;
@@ -724,29 +784,27 @@ sparse_decode_kernel(Params p) {
     }
 
     if (ONE) {
-      int i_dead = -1;
-      for (int i = warp; i < n_ch; i += W) {
-        const int st = i % S;
-        if (!wait_bounded(&full[st], (i / S) & 1)) {
-          i_dead = i;
+      int q_dead = -1;
+      for (int q = 0; q < wcnt; ++q) {
+        const int st = warp + W * (q % kSpw);
+        if (!wait_bounded(&full[st], (q / kSpw) & 1)) {
+          q_dead = q;
           if (lane == 0) atomicExch(p.status, kStatusWaitTimeout);
           break;
         }
-        const int c = s + i * p.splits;
-        const int beta = s_union[c >> csh] & 0xFFFFFF;
-        consume_chunk<NTR>(region + st * kStageBytes, beta * g.P + (c & csh) * kChunk, nrow, qf,
-                           cq, m_run, l_run, o_acc);
+        consume_chunk<NTR>(region + st * kStageBytes, wl[2 * q + 1], nrow, qf, cq, m_run, l_run,
+                           o_acc);
         __syncwarp();   // every lane's reads of the stage are done
-        if (lane == 0 && i + S < n_ch) {
+        if (lane == 0 && q + kSpw < wcnt) {
           fence_proxy_async_smem();
-          issue(i + S);
+          issue_one(q + kSpw);
         }
       }
       // After a wait gave up, let this warp's copies still in flight land
       // before the stage memory is reused.
-      if (i_dead >= 0 && lane == 0)
-        for (int i = i_dead; i < min(n_ch, i_dead + S); i += W)
-          if (!wait_bounded(&full[i % S], (i / S) & 1)) break;
+      if (q_dead >= 0 && lane == 0)
+        for (int q = q_dead; q < min(wcnt, q_dead + kSpw); ++q)
+          if (!wait_bounded(&full[warp + W * (q % kSpw)], (q / kSpw) & 1)) break;
     } else {
       bool dead = false;
       int rc = 0;                               // this row's chunks seen so far
