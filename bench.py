@@ -434,6 +434,9 @@ def run_qsa(args, case):
     step_gbs = mean["step"] / (ms_step / 1000.0) / 1e9
 
     # ---- per-kernel durations: event nodes around each kernel ---------------
+    # When the step runs selection and attention as one launch (DecodeStep
+    # fused), sparse_decode below times that fused kernel.
+    fused = step.fused and qsa.qsa_select_sparse_decode_fused(step.cg)
     kern_ms = {}
     evs = make_events(6 * nrep)
     if evs is not None:
@@ -447,15 +450,24 @@ def run_qsa(args, case):
                                          w["seqlens"], step.scores, stream)
                     e[1].record(stream)
                     e[2].record(stream)
-                    qsa.qsa_select_topk(step.cg, step.scores, w["seqlens"], step.k, step.window,
-                                        step.sel, step.nsel, stream)
+                    if not fused:
+                        qsa.qsa_select_topk(step.cg, step.scores, w["seqlens"], step.k,
+                                            step.window, step.sel, step.nsel, stream)
                     e[3].record(stream)
                     e[4].record(stream)
-                    qsa.qsa_sparse_decode_ex(step.cg, w["q"], w["k_pool"], w["k_sf"],
-                                             w["v_pool"], w["v_sf"], w["k_scale"],
-                                             w["v_scale"], w["sm_scale"], w["page_table"],
-                                             w["seqlens"], step.sel, step.k, step.out, step.lse,
-                                             step.workspace, step.num_splits, stream)
+                    if fused:
+                        qsa.qsa_select_sparse_decode(
+                            step.cg, step.scores, step.window, w["q"], w["k_pool"], w["k_sf"],
+                            w["v_pool"], w["v_sf"], w["k_scale"], w["v_scale"], w["sm_scale"],
+                            w["page_table"], w["seqlens"], step.k, step.sel, step.nsel,
+                            step.out, step.lse, step.workspace, step.num_splits, stream)
+                    else:
+                        qsa.qsa_sparse_decode_ex(step.cg, w["q"], w["k_pool"], w["k_sf"],
+                                                 w["v_pool"], w["v_sf"], w["k_scale"],
+                                                 w["v_scale"], w["sm_scale"], w["page_table"],
+                                                 w["seqlens"], step.sel, step.k, step.out,
+                                                 step.lse, step.workspace, step.num_splits,
+                                                 stream)
                     e[5].record(stream)
             acc = {"index_scores": [], "select_topk": [], "sparse_decode": []}
             for _ in range(5):
@@ -467,6 +479,8 @@ def run_qsa(args, case):
                     acc["select_topk"].append(e[2].elapsed_time(e[3]))
                     acc["sparse_decode"].append(e[4].elapsed_time(e[5]))
         kern_ms = {k: float(np.mean(v)) for k, v in acc.items()}
+        if fused:
+            kern_ms.pop("select_topk")
 
     # ---- end to end through host buffers ----------------------------------
     e2e = run_e2e(qsa, step, reps, stream, args, dev, T, world)
@@ -495,6 +509,8 @@ def run_qsa(args, case):
         b = mean[name]
         kernels[name] = {"ms": t, "bytes": b,
                          "gbs": (b / (t / 1000.0) / 1e9) if (t > 0 and b > 0) else None}
+    if fused:
+        kernels["select_topk"] = {"ms": None, "fused_into": "sparse_decode"}
     dom = max(kern_ms, key=kern_ms.get) if kern_ms else "sparse_decode"
     dom_t = kern_ms.get(dom)
     achieved = (mean[dom] / (dom_t / 1000.0) / 1e9) if dom_t else None
@@ -521,7 +537,7 @@ def run_qsa(args, case):
         "kernels": kernels,
         "clocks": clocks,
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (2 if fused else 3) * args.steps,
         "cpu_baseline": cpu,
         "prologue": prologue,
         "rollback": rollback,

@@ -196,6 +196,36 @@ qsa_status_t qsa_sparse_decode_ex(const qsa_geom_t *geom, const void *q_bf16,
                                   int num_splits, cudaStream_t stream);
 
 /*
+ * qsa_select_topk followed by qsa_sparse_decode as one call (same arguments,
+ * same sel / nsel / out / lse results, bit for bit).  For decode rows (R = 1)
+ * whose selection scratch fits the attention kernel's staging memory (MB up
+ * to about 15,000 blocks) it is ONE launch: every attention CTA selects its
+ * row from the scores itself and one CTA per row writes sel and nsel, so the
+ * selection's separate launch and its round trip through memory leave the
+ * step; otherwise it launches the two kernels.  TensorRT-LLM PR #20276
+ * ("Qwen3.8-Flash-Next NVFP4 target"), Decisions worth knowing: canonical
+ * selection as a separate composition costs a decode step 2-4%; the fast
+ * paths produce the same rows from one fused launch, and the composition
+ * remains for wide score tables.  `window` as in qsa_select_topk; the
+ * workspace and num_splits as in qsa_sparse_decode_ex (0 = the library's
+ * choice; size the workspace with qsa_sparse_decode_workspace_bytes_ex).
+ */
+/* 1 when qsa_select_sparse_decode runs as one launch for this geometry, 0
+ * when it launches the selection and the attention kernels (or the geometry
+ * is invalid). */
+int qsa_select_sparse_decode_fused(const qsa_geom_t *geom);
+
+qsa_status_t qsa_select_sparse_decode(const qsa_geom_t *geom, const int32_t *scores,
+                                      int window, const void *q_bf16,
+                                      const uint8_t *k_pool, const uint8_t *k_sf,
+                                      const uint8_t *v_pool, const uint8_t *v_sf,
+                                      float k_scale, float v_scale, float sm_scale,
+                                      const int32_t *page_table, const int32_t *seqlens,
+                                      int k, int32_t *sel, int32_t *nsel, void *out_bf16,
+                                      float *lse, void *workspace, size_t workspace_bytes,
+                                      int num_splits, cudaStream_t stream);
+
+/*
  * qsa_sparse_decode for callers that cannot allocate device memory (no
  * counterpart in the method's description: it exists for deployment).  Some
  * callers never get to call cudaMalloc -- an allocator-free runtime, a memory

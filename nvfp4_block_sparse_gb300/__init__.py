@@ -13,6 +13,7 @@ import math
 import torch
 
 from .binding import (EXPORTS, QsaError, load, make_geom, qsa_geom_t, qsa_index_scores,
+                      qsa_select_sparse_decode, qsa_select_sparse_decode_fused,
                       qsa_select_topk, qsa_sparse_decode, qsa_sparse_decode_ex, qsa_sparse_decode_noalloc,
                       qsa_sparse_decode_workspace_bytes, qsa_sparse_decode_workspace_bytes_ex,
                       qsa_rollback_gather, qsa_rollback_restore, qsa_rollback_state_bytes,
@@ -21,6 +22,7 @@ from .binding import (EXPORTS, QsaError, load, make_geom, qsa_geom_t, qsa_index_
 
 __all__ = [
     "EXPORTS", "QsaError", "load", "make_geom", "qsa_geom_t", "qsa_index_scores",
+    "qsa_select_sparse_decode", "qsa_select_sparse_decode_fused",
     "qsa_select_topk", "qsa_sparse_decode", "qsa_sparse_decode_ex", "qsa_sparse_decode_noalloc",
     "qsa_sparse_decode_workspace_bytes", "qsa_sparse_decode_workspace_bytes_ex",
     "qsa_rollback_gather", "qsa_rollback_restore", "qsa_rollback_state_bytes",
@@ -32,11 +34,16 @@ GEOM_FIELDS = [n for n, _ in qsa_geom_t._fields_]
 
 
 class DecodeStep:
-    """Device buffers for one QSA step of a fixed geometry, and the three
-    library calls that fill them: index scores -> top-k selection -> sparse
-    decode.  ``num_splits`` = 0 lets the library choose the KV split count."""
+    """Device buffers for one QSA step of a fixed geometry, and the library
+    calls that fill them: index scores -> top-k selection -> sparse decode,
+    chained by programmatic dependent launch.  ``fused`` runs selection and
+    decode through qsa_select_sparse_decode instead (one launch for decode
+    rows; bit-identical results).  ``num_splits`` = 0 lets the library choose
+    the KV split count."""
 
-    def __init__(self, geom: dict, k: int, window: int, device="cuda", num_splits: int = 0):
+    def __init__(self, geom: dict, k: int, window: int, device="cuda", num_splits: int = 0,
+                 fused: bool = False):
+        self.fused = bool(fused)
         self.geom = {n: int(geom[n]) for n in GEOM_FIELDS}
         self.cg = make_geom(**self.geom)
         self.k, self.window, self.num_splits = int(k), int(window), int(num_splits)
@@ -59,12 +66,19 @@ class DecodeStep:
         sm = float(w["sm_scale"]) if sm_scale is None else float(sm_scale)
         qsa_index_scores(self.cg, w["iq"], w["ik_pool"], w["page_table"], w["seqlens"],
                          self.scores, stream)
-        qsa_select_topk(self.cg, self.scores, w["seqlens"], self.k, self.window, self.sel,
-                        self.nsel, stream)
-        qsa_sparse_decode_ex(self.cg, w["q"], w["k_pool"], w["k_sf"], w["v_pool"], w["v_sf"],
-                             w["k_scale"], w["v_scale"], sm, w["page_table"], w["seqlens"],
-                             self.sel, self.k, self.out, self.lse, self.workspace,
-                             self.num_splits, stream)
+        if not self.fused:
+            qsa_select_topk(self.cg, self.scores, w["seqlens"], self.k, self.window, self.sel,
+                            self.nsel, stream)
+            qsa_sparse_decode_ex(self.cg, w["q"], w["k_pool"], w["k_sf"], w["v_pool"],
+                                 w["v_sf"], w["k_scale"], w["v_scale"], sm, w["page_table"],
+                                 w["seqlens"], self.sel, self.k, self.out, self.lse,
+                                 self.workspace, self.num_splits, stream)
+        else:
+            qsa_select_sparse_decode(self.cg, self.scores, self.window, w["q"], w["k_pool"],
+                                     w["k_sf"], w["v_pool"], w["v_sf"], w["k_scale"],
+                                     w["v_scale"], sm, w["page_table"], w["seqlens"], self.k,
+                                     self.sel, self.nsel, self.out, self.lse, self.workspace,
+                                     self.num_splits, stream)
         return self
 
     @staticmethod

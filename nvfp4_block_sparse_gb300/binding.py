@@ -33,6 +33,8 @@ EXPORTS = (
     "qsa_sparse_decode_noalloc",
     "qsa_workspace_status",
     "qsa_store_kv_tokens",
+    "qsa_select_sparse_decode",
+    "qsa_select_sparse_decode_fused",
     "qsa_rollback_state_bytes",
     "qsa_rollback_gather",
     "qsa_rollback_restore",
@@ -91,6 +93,13 @@ def load(build_if_missing: bool = False):
     lib.qsa_sparse_decode.argtypes = dec + [_vp]
     lib.qsa_sparse_decode_ex.restype = st
     lib.qsa_sparse_decode_ex.argtypes = dec + [ctypes.c_int, _vp]
+    lib.qsa_select_sparse_decode_fused.restype = ctypes.c_int
+    lib.qsa_select_sparse_decode_fused.argtypes = [G]
+    lib.qsa_select_sparse_decode.restype = st
+    lib.qsa_select_sparse_decode.argtypes = [G, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp,
+                                             ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                             _vp, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp,
+                                             ctypes.c_size_t, ctypes.c_int, _vp]
     lib.qsa_sparse_decode_noalloc.restype = st
     lib.qsa_sparse_decode_noalloc.argtypes = [G, _vp, _vp, _vp, _vp, _vp, ctypes.c_float,
                                               ctypes.c_float, ctypes.c_float, _vp, _vp, _vp,
@@ -190,6 +199,27 @@ def qsa_rollback_restore(geom, page_table, seqlens, rejected, saved, k_pool, k_s
         _ptr(saved, torch.uint8, "saved"), _ptr(k_pool, torch.uint8, "k_pool"),
         _ptr(k_sf, torch.uint8, "k_sf"), _ptr(v_pool, torch.uint8, "v_pool"),
         _ptr(v_sf, torch.uint8, "v_sf"), _ptr(ik_pool, torch.int8, "ik_pool"), _stream(stream)))
+
+
+def qsa_select_sparse_decode_fused(geom) -> bool:
+    g = _geom(geom)
+    return bool(load().qsa_select_sparse_decode_fused(ctypes.byref(g)))
+
+
+def qsa_select_sparse_decode(geom, scores, window, q, k_pool, k_sf, v_pool, v_sf, k_scale,
+                             v_scale, sm_scale, page_table, seqlens, k, sel, nsel, out, lse,
+                             workspace, num_splits=0, stream=None):
+    g = _geom(geom)
+    _check("qsa_select_sparse_decode", load().qsa_select_sparse_decode(
+        ctypes.byref(g), _ptr(scores, torch.int32, "scores"), int(window),
+        _ptr(q, torch.bfloat16, "q"), _ptr(k_pool, torch.uint8, "k_pool"),
+        _ptr(k_sf, torch.uint8, "k_sf"), _ptr(v_pool, torch.uint8, "v_pool"),
+        _ptr(v_sf, torch.uint8, "v_sf"), float(k_scale), float(v_scale), float(sm_scale),
+        _ptr(page_table, torch.int32, "page_table"), _ptr(seqlens, torch.int32, "seqlens"),
+        int(k), _ptr(sel, torch.int32, "sel"), _ptr(nsel, torch.int32, "nsel"),
+        _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
+        _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), int(num_splits),
+        _stream(stream)))
 
 
 def qsa_select_topk(geom, scores, seqlens, k, window, sel, nsel, stream=None):

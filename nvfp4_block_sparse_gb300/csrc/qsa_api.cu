@@ -232,6 +232,47 @@ qsa_status_t qsa_sparse_decode_ex(const qsa_geom_t* geom, const void* q_bf16,
                                              out_bf16, lse, workspace, true, stream));
 }
 
+int qsa_select_sparse_decode_fused(const qsa_geom_t* geom) {
+  if (check_geom(geom) != QSA_OK) return 0;
+  return qsa::decode_can_fuse_select(to_geom(geom)) ? 1 : 0;
+}
+
+qsa_status_t qsa_select_sparse_decode(const qsa_geom_t* geom, const int32_t* scores, int window,
+                                      const void* q_bf16, const uint8_t* k_pool,
+                                      const uint8_t* k_sf, const uint8_t* v_pool,
+                                      const uint8_t* v_sf, float k_scale, float v_scale,
+                                      float sm_scale, const int32_t* page_table,
+                                      const int32_t* seqlens, int k, int32_t* sel, int32_t* nsel,
+                                      void* out_bf16, float* lse, void* workspace,
+                                      size_t workspace_bytes, int num_splits,
+                                      cudaStream_t stream) {
+  qsa_status_t st = check_decode_args(geom, k);
+  if (st != QSA_OK) return st;
+  if (window < 0 || window > k || num_splits < 0) return QSA_ERR_INVALID_ARG;
+  if (!scores || !q_bf16 || !k_pool || !k_sf || !v_pool || !v_sf || !page_table || !seqlens ||
+      !sel || !nsel || !out_bf16 || !lse)
+    return QSA_ERR_INVALID_ARG;
+  if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(k_sf, 16) || !aligned(v_sf, 16) ||
+      !aligned(q_bf16, 8))
+    return QSA_ERR_INVALID_ARG;
+  const Geom g = to_geom(geom);
+  const qsa::DecodePlan plan = qsa::plan_sparse_decode(g, k, num_splits);
+  if (!workspace || workspace_bytes < plan.ws_bytes || !aligned(workspace, 256))
+    return QSA_ERR_WORKSPACE;
+  st = check_device();
+  if (st != QSA_OK) return st;
+  if (qsa::decode_can_fuse_select(g))
+    return from_cuda(qsa::launch_sparse_decode(g, plan, q_bf16, k_pool, k_sf, v_pool, v_sf,
+                                               k_scale, v_scale, sm_scale, page_table, seqlens,
+                                               nullptr, k, out_bf16, lse, workspace, true, stream,
+                                               scores, window, sel, nsel));
+  cudaError_t e = qsa::launch_select_topk(g, scores, seqlens, k, window, sel, nsel, true, stream);
+  if (e != cudaSuccess) return from_cuda(e);
+  return from_cuda(qsa::launch_sparse_decode(g, plan, q_bf16, k_pool, k_sf, v_pool, v_sf, k_scale,
+                                             v_scale, sm_scale, page_table, seqlens, sel, k,
+                                             out_bf16, lse, workspace, true, stream));
+}
+
 qsa_status_t qsa_sparse_decode(const qsa_geom_t* geom, const void* q_bf16, const uint8_t* k_pool,
                                const uint8_t* k_sf, const uint8_t* v_pool, const uint8_t* v_sf,
                                float k_scale, float v_scale, float sm_scale,

@@ -212,6 +212,7 @@ struct DecodePlan {
 };
 
 DecodePlan plan_sparse_decode(const Geom& g, int k, int num_splits);
+bool decode_can_fuse_select(const Geom& g);
 
 cudaError_t launch_sparse_decode(const Geom& g, const DecodePlan& plan, const void* q,
                                  const uint8_t* k_pool, const uint8_t* k_sf,
@@ -219,6 +220,8 @@ cudaError_t launch_sparse_decode(const Geom& g, const DecodePlan& plan, const vo
                                  float v_scale, float sm_scale, const int32_t* page_table,
                                  const int32_t* seqlens, const int32_t* sel, int k,
                                  void* out, float* lse, void* workspace, bool pdl,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream,
+                                 const int32_t* scores = nullptr, int window = 0,
+                                 int32_t* sel_out = nullptr, int32_t* nsel_out = nullptr);
 
 }  // namespace qsa

@@ -37,6 +37,7 @@
 // Every wait is bounded: a wait that gives up records a status word in the
 // workspace and the kernel still finishes.
 #include "qsa_common.cuh"
+#include "qsa_select_row.cuh"
 
 #include <cooperative_groups.h>
 #include <math.h>
@@ -80,6 +81,13 @@ struct Params {
   int splits;           // KV splits per unit
   int slices;           // head slices per KV head
   int cluster;          // 1: ticket merge through partials; >1: cluster (DSMEM) merge
+  // Fused selection (decode rows only): when scores is set, each CTA selects
+  // its row from the scores itself instead of reading sel; the CTA of split
+  // 0, KV head 0, slice 0 writes the row's sel_out / nsel_out.
+  const int32_t* scores;
+  int window;
+  int32_t* sel_out;
+  int32_t* nsel_out;
 };
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
@@ -157,8 +165,8 @@ struct Layout {
     off += 64 * 4;                                      // scalars
     // sel rows, union ids, pages, scan (verify) / per-warp chunk lists (decode)
     size_t sel_bytes = (size_t)R * k * 4 * 4 + 16;
-    if (ONE) {
-      const size_t lists = (size_t)W * 2 * decode_list_cap(k, splits, W) * 4;
+    if (ONE) {   // per-warp chunk lists, then the fused selection's row
+      const size_t lists = ((size_t)W * 2 * decode_list_cap(k, splits, W) + k) * 4;
       if (lists > sel_bytes) sel_bytes = lists;
     }
     off += sel_bytes;
@@ -423,7 +431,7 @@ sparse_decode_kernel(Params p) {
   int32_t* s_union = s_sel + R * k;
   int32_t* s_upage = s_union + R * k;
   int32_t* s_scan = s_upage + R * k;                  // [R * k + 1]
-  const int list_ints = ONE ? W * 2 * decode_list_cap(k, p.splits, W) : 0;
+  const int list_ints = ONE ? W * 2 * decode_list_cap(k, p.splits, W) + k : 0;
   int32_t* s_pt = s_sel + (list_ints > R * k * 4 + 4 ? list_ints : R * k * 4 + 4);
 
   // full[st]: one arrival (the copy issuer) plus the copies' bytes.  empty[st]
@@ -506,14 +514,29 @@ sparse_decode_kernel(Params p) {
   int wcnt = 0;
   if (ONE) {
     const int nc = k << csh;
+    const int32_t* selrow = p.sel + (size_t)b * k;
+    if (p.scores) {
+      // Fused selection: this CTA selects its row from the scores, with the
+      // (still idle) stage region as the selection's scratch.
+      int32_t* s_row = s_sel + W * 2 * decode_list_cap(k, p.splits, W);
+      const int n = visible_tokens(L, 1, 0, cap);
+      select_row<kThreads>(p.scores + (size_t)b * g.MB, (n + g.P - 1) / g.P, p.window, k, s_row,
+                           misc + 20, region);
+      __syncthreads();   // the row is complete and the scratch is free
+      if (s == 0 && kvh == 0 && slice == 0) {
+        for (int i = tid; i < k; i += kThreads) p.sel_out[(size_t)b * k + i] = s_row[i];
+        if (tid == 0) p.nsel_out[b] = misc[20];
+      }
+      selrow = s_row;
+    }
     for (int t0 = 0;; t0 += 32) {
       if (s + (long long)p.splits * (warp + (long long)W * t0) >= nc) break;
       const long long c = s + (long long)p.splits * (warp + (long long)W * (t0 + lane));
       int page = -1, tok0 = 0;
       if (c < nc) {
         const int e = (int)(c >> csh);
-        const int beta = p.sel[(size_t)b * k + e];
-        const int prev = e > 0 ? p.sel[(size_t)b * k + e - 1] : -1;
+        const int beta = selrow[e];
+        const int prev = e > 0 ? selrow[e - 1] : -1;
         if (beta >= 0 && beta < g.MB && beta != prev) {
           const int pg = pt_in_smem ? s_pt[beta] : p.page_table[(size_t)b * g.MB + beta];
           if (pg >= 0 && pg < g.NP) {
@@ -758,8 +781,10 @@ sparse_decode_kernel(Params p) {
     bulk_g2s(dst + 2 * kKBytes + kSfBytes, p.v_sf + row0 * (kHeadDim / 16), kSfBytes, &full[st],
              pol);
   };
-  if (ONE && lane == 0)
+  if (ONE && lane == 0) {
+    fence_proxy_async_smem();   // after the fused selection's scratch in the region
     for (int q = 0; q < min(kSpw, wcnt); ++q) issue_one(q);
+  }
 
   if (!producer) {
     const int cbase = jw * kHsp;
@@ -1179,6 +1204,20 @@ int variant_resident(int ntr, int R, int k, int mb, int splits) {
 
 }  // namespace
 
+// The decode variant can select its row itself when the selection's scratch
+// fits in its stage region.
+bool decode_can_fuse_select(const Geom& g) {
+  if (g.R != 1) return false;
+  const int ntr = tiles_per_row(g);
+#define X(NTR_, R_, W_, S_, ONE_)                                                   \
+  if (ONE_ && ntr == NTR_ && R_ == 1)                                               \
+    return select_row_smem<Layout<NTR_, W_, S_, ONE_>::kThreads>(g.MB) <=           \
+           (size_t)Layout<NTR_, W_, S_, ONE_>::kStagesSz;
+  QSA_DECODE_VARIANTS(X)
+#undef X
+  return false;
+}
+
 DecodePlan plan_sparse_decode(const Geom& g, int k, int num_splits) {
   DecodePlan pl;
   const int G = g.Hq / g.Hkv;
@@ -1220,8 +1259,14 @@ cudaError_t launch_sparse_decode(const Geom& g, const DecodePlan& plan, const vo
                                  const uint8_t* v_pool, const uint8_t* v_sf, float k_scale,
                                  float v_scale, float sm_scale, const int32_t* page_table,
                                  const int32_t* seqlens, const int32_t* sel, int k, void* out,
-                                 float* lse, void* workspace, bool pdl, cudaStream_t stream) {
+                                 float* lse, void* workspace, bool pdl, cudaStream_t stream,
+                                 const int32_t* scores, int window, int32_t* sel_out,
+                                 int32_t* nsel_out) {
   Params prm;
+  prm.scores = scores;
+  prm.window = window;
+  prm.sel_out = sel_out;
+  prm.nsel_out = nsel_out;
   prm.g = g;
   prm.q = reinterpret_cast<const __nv_bfloat16*>(q);
   prm.k_pool = k_pool; prm.k_sf = k_sf; prm.v_pool = v_pool; prm.v_sf = v_sf;

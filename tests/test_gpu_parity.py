@@ -250,3 +250,39 @@ def test_full_size_sampled_rows(qsa, cfg):
     picks = sorted({0, (case.batch // 2) * R, T - R})
     for r0 in picks:
         check_against_oracle(res, w_np, rows=(r0, r0 + R))
+
+
+# ---------------------------------------------------------------------------
+# fused selection + decode against the composed calls (bit for bit)
+# ---------------------------------------------------------------------------
+
+FUSED_CASES = [("cfg0", lambda: qw.small(qw.CONFIGS[0]), 0),
+               ("cfg1", lambda: qw.small(qw.CONFIGS[1]), 0),
+               ("cfg3", lambda: qw.small(qw.CONFIGS[3]), 0),
+               ("cfg1_full", lambda: qw.CONFIGS[1], 0),
+               ("cfg3_full", lambda: qw.CONFIGS[3], 0),
+               ("cfg1_split1", lambda: qw.small(qw.CONFIGS[1]), 1),
+               ("cfg1_split7", lambda: qw.small(qw.CONFIGS[1]), 7),
+               ("cfg1_split64", lambda: qw.small(qw.CONFIGS[1]), 64),
+               ("window0", lambda: EDGE_CASES["window_zero"], 0),
+               ("k_one", lambda: EDGE_CASES["k_one"], 0),
+               ("ties", lambda: _case(tie_frac=0.5), 0),
+               ("invalid", lambda: _case(invalid_frac=0.3), 0),
+               ("gqa12", lambda: EDGE_CASES["gqa12_nt2"], 0),
+               ("cfg2_composed_inside", lambda: qw.small(qw.CONFIGS[2]), 0)]
+
+
+@pytest.mark.parametrize("name,make,splits", FUSED_CASES, ids=[c[0] for c in FUSED_CASES])
+def test_fused_selection_matches_composed(qsa, name, make, splits):
+    w = qw.make_workload(make(), "cuda")
+    c = run_gpu(qsa, w, num_splits=splits)
+    step_f = qsa.DecodeStep(qw.geometry(w), w["k"], w["window"], device=w["q"].device,
+                            num_splits=splits, fused=True)
+    step_f.run(w)
+    torch.cuda.synchronize()
+    assert qsa.qsa_workspace_status(step_f.workspace) == 0
+    ra, rc = host(step_f), host(c)
+    for key in ("scores", "sel", "nsel", "out", "lse"):
+        np.testing.assert_array_equal(ra[key], rc[key], err_msg=key)
+    if w["rows_per_req"] == 1 and name not in ("gqa12",):
+        assert qsa.qsa_select_sparse_decode_fused(qw.geometry(w))
