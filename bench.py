@@ -47,6 +47,27 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The timed region's duration as the job sees it: the maximum over ranks
+    (each rank times the same steps between barriers)."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rows_per_second(world: int, rows_per_step: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: every rank processes its own rows (weak scaling)."""
+    return world * rows_per_step * steps / (ms / 1000.0)
+
+
+def replica_seed(case: qw.Case, i: int, rank: int) -> int:
+    """Seed of input replica i on a rank: replica 0 of rank 0 is the workload's
+    own seed; ranks and replicas draw distinct inputs."""
+    return case.seed + 7919 * i + 104729 * rank
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -359,7 +380,7 @@ def run_qsa(args, case):
 
     # Replica 0 carries the workload's own seed; others shift it (and the rank).
     def replica(i):
-        seed = case.seed + 7919 * i + 104729 * rank
+        seed = replica_seed(case, i, rank)
         w = qw.make_workload(case, dev, seed=seed)
         w["page_table_np"] = w["page_table"].cpu().numpy()
         w["seqlens_np"] = w["seqlens"].cpu().numpy()
@@ -423,14 +444,10 @@ def run_qsa(args, case):
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     clocks = clk.summary()
     ms_step = ms / args.steps
-    rows_s = world * T * args.steps / (ms / 1000.0)
+    rows_s = job_rows_per_second(world, T, args.steps, ms)
     step_gbs = mean["step"] / (ms_step / 1000.0) / 1e9
 
     # ---- per-kernel durations: event nodes around each kernel ---------------
@@ -581,12 +598,8 @@ def run_e2e(qsa, step, reps, stream, args, dev, T, world):
             one(i)
         e1.record(stream)
         stream.synchronize()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": world * T * n / (ms / 1000.0), "unit": "rows/s",
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    return {"value": job_rows_per_second(world, T, n, ms), "unit": "rows/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
 
 
