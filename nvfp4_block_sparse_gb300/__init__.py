@@ -53,8 +53,13 @@ class DecodeStep:
         self.scores = torch.empty((T, MB), dtype=torch.int32, device=dev)
         self.sel = torch.empty((T, self.k), dtype=torch.int32, device=dev)
         self.nsel = torch.empty((T,), dtype=torch.int32, device=dev)
-        self.out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)
-        self.lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
+        # out and lse share one allocation (lse right after out, 256-byte
+        # aligned) so that a host can read a step's results in one copy.
+        out_bytes = T * Hq * D * 2
+        lse_off = (out_bytes + 255) // 256 * 256
+        self.results = torch.empty((lse_off + T * Hq * 4,), dtype=torch.uint8, device=dev)
+        self.out = self.results[:out_bytes].view(torch.bfloat16).view(T, Hq, D)
+        self.lse = self.results[lse_off:].view(torch.float32).view(T, Hq)
         nbytes = qsa_sparse_decode_workspace_bytes_ex(self.cg, self.k, self.num_splits)
         if nbytes == 0:
             raise QsaError("qsa_sparse_decode_workspace_bytes", 1, "invalid geometry")
