@@ -29,6 +29,10 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
+#ifndef QSA_INDEX_MMA
+#define QSA_INDEX_MMA 1
+#endif
+
 __device__ __forceinline__ int4 ld_stream_v4(const int4* p) {
   int4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
@@ -193,6 +197,190 @@ index_scores_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __restr
   (void)page;
 }
 
+// ---- verify rows (R >= 2): the dot products on the tensor cores ------------
+//
+// Per request the head-summed weights w[j][d] (|w| <= 127 * Hq) are split as
+// w = 128*a + b with b in [-64, 63] and |a| <= 254: both exact in fp16, as is
+// every int8 key.  Per 16 tokens, two mma.sync m16n8k16 (fp16 x fp16 -> fp32)
+// give S_a = K . a^T and S_b = K . b^T for all rows at once (the rows are the
+// 8 MMA columns); every partial sum stays below 2^24 in magnitude, so both are
+// exact integers and 128*S_a + S_b is the exact int32 token score.  Keys
+// become fp16 by one byte permute against 0x64 (1024 + (x + 128)) and one
+// subtraction of 1152.  Dims are taken in the order each lane holds them
+// (lane part tig: dims 16*tig..16*tig+15, k-step kk: 4 of them), the same on
+// both operands, so the contraction is unchanged.
+
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Four int8 -> two fp16 pairs (bytes 0,1 and bytes 2,3), exact.
+__device__ __forceinline__ void s8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;                 // x + 128, as unsigned bytes
+  const uint32_t bias = 0x64806480u;                  // fp16 pair (1152, 1152)
+  lo = hsub2_u32(__byte_perm(u, 0x64646464u, 0x4140), bias);
+  hi = hsub2_u32(__byte_perm(u, 0x64646464u, 0x4342), bias);
+}
+
+template <int P, bool PIPE>
+__global__ void __launch_bounds__(kThreads)
+index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __restrict__ ik_pool,
+                        const int32_t* __restrict__ page_table,
+                        const int32_t* __restrict__ seqlens, int32_t* __restrict__ scores,
+                        int blocks_per_warp) {
+  constexpr int RB = kMaxRows;                 // the 8 MMA columns hold the rows
+  __shared__ int32_t wpart[4][RB][kIndexDim];
+  __shared__ __half wsplit[2][RB][kIndexDim];   // a, b
+
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int R = g.R;
+
+  pdl_wait();
+
+  const int L = seqlens[b];
+  const int cap = g.MB * P;
+  const int nmax = visible_tokens(L, R, R - 1, cap);
+
+  auto block_of = [&](int it, int& beta, int& page) -> bool {
+    beta = (blockIdx.x * blocks_per_warp + it) * kWarps + warp;
+    page = -1;
+    if (beta >= g.MB) return false;
+    page = page_table[(size_t)b * g.MB + beta];
+    return page >= 0 && page < g.NP && beta * P < nmax;
+  };
+  // Lane (gid, tig) loads 16 B (dims 16*tig..) of token 8*i + gid per step.
+  auto load_keys = [&](int page, int4 (&kv)[P / 8]) {
+    const int4* src = reinterpret_cast<const int4*>(ik_pool + (size_t)page * P * kIndexDim) + lane;
+#pragma unroll
+    for (int i = 0; i < P / 8; ++i) kv[i] = ld_stream_v4(src + 32 * i);
+  };
+
+  int beta0, page0;
+  bool live0 = block_of(0, beta0, page0);
+  int4 kv[P / 8];
+  if (live0) load_keys(page0, kv);
+
+  // Head sums w[j][d], then the exact split w = 128*a + b.
+  for (int idx = threadIdx.x; idx < 4 * RB * kIndexDim; idx += kThreads) {
+    const int hg = idx / (RB * kIndexDim);
+    const int j = (idx / kIndexDim) % RB;
+    const int d = idx % kIndexDim;
+    int s = 0;
+    if (j < R) {
+      const int8_t* src = iq + ((size_t)(b * R + j) * g.Hq) * kIndexDim + d;
+      int h = hg;
+      for (; h + 28 < g.Hq; h += 32) {
+        int v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = src[(size_t)(h + 4 * u) * kIndexDim];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) s += v[u];
+      }
+      for (; h < g.Hq; h += 4) s += src[(size_t)h * kIndexDim];
+    }
+    wpart[hg][j][d] = s;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < RB * kIndexDim; idx += kThreads) {
+    const int j = idx / kIndexDim, d = idx % kIndexDim;
+    const int w = wpart[0][j][d] + wpart[1][j][d] + wpart[2][j][d] + wpart[3][j][d];
+    const int lo = ((w + 64) & 127) - 64;
+    wsplit[0][j][d] = __int2half_rn((w - lo) / 128);
+    wsplit[1][j][d] = __int2half_rn(lo);
+  }
+  __syncthreads();
+  pdl_trigger();
+
+  // B fragments (column gid = row gid): k-step kk, halves 0/1 -> dims
+  // 16*tig + 4*kk + {0,1} / {2,3}.
+  uint32_t bw[2][4][2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const __half* src = &wsplit[q][gid][16 * tig + 4 * kk];
+      bw[q][kk][0] = *reinterpret_cast<const uint32_t*>(src);
+      bw[q][kk][1] = *reinterpret_cast<const uint32_t*>(src + 2);
+    }
+  // This lane's two columns (rows 2*tig, 2*tig + 1).
+  int ncol[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int j = 2 * tig + e;
+    ncol[e] = (j < R) ? visible_tokens(L, R, j, cap) : 0;
+  }
+
+  int beta = beta0, page = page0;
+  bool live = live0;
+  for (int it = 0; it < blocks_per_warp; ++it) {
+    if (beta >= g.MB) break;
+    int beta_n = g.MB, page_n = -1;
+    bool live_n = false;
+    int4 kv_n[PIPE ? P / 8 : 1];
+    if constexpr (PIPE) {
+      if (it + 1 < blocks_per_warp) {
+        live_n = block_of(it + 1, beta_n, page_n);
+        if (live_n) load_keys(page_n, kv_n);
+      }
+    } else if (it + 1 < blocks_per_warp) {
+      live_n = block_of(it + 1, beta_n, page_n);
+    }
+    int32_t* dst = scores + (size_t)b * R * g.MB + beta;
+    if (!live) {
+      if (lane < R) dst[(size_t)lane * g.MB] = kSentinel;
+    } else {
+      int best[2] = {kSentinel, kSentinel};
+#pragma unroll
+      for (int mt = 0; mt < P / 16; ++mt) {
+        const int4 ka = kv[2 * mt], kb = kv[2 * mt + 1];   // tokens gid and gid + 8
+        const uint32_t wa[4] = {(uint32_t)ka.x, (uint32_t)ka.y, (uint32_t)ka.z, (uint32_t)ka.w};
+        const uint32_t wb[4] = {(uint32_t)kb.x, (uint32_t)kb.y, (uint32_t)kb.z, (uint32_t)kb.w};
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          uint32_t a[4];
+          s8x4_to_f16x2x2(wa[kk], a[0], a[2]);
+          s8x4_to_f16x2x2(wb[kk], a[1], a[3]);
+          mma_f16_16816(sa, a, bw[0][kk][0], bw[0][kk][1]);
+          mma_f16_16816(sb, a, bw[1][kk][0], bw[1][kk][1]);
+        }
+        const int tA = beta * P + 16 * mt + gid, tB = tA + 8;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int vA = __float2int_rn(sa[e]) * 128 + __float2int_rn(sb[e]);
+          const int vB = __float2int_rn(sa[2 + e]) * 128 + __float2int_rn(sb[2 + e]);
+          if (tA < ncol[e]) best[e] = max(best[e], vA);
+          if (tB < ncol[e]) best[e] = max(best[e], vB);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        int v = best[e];
+        v = max(v, __shfl_xor_sync(0xffffffffu, v, 4));
+        v = max(v, __shfl_xor_sync(0xffffffffu, v, 8));
+        v = max(v, __shfl_xor_sync(0xffffffffu, v, 16));
+        const int j = 2 * tig + e;
+        if (gid == 0 && j < R) dst[(size_t)j * g.MB] = (beta * P < ncol[e]) ? v : kSentinel;
+      }
+    }
+    beta = beta_n;
+    page = page_n;
+    live = live_n;
+    if constexpr (PIPE) {
+#pragma unroll
+      for (int i = 0; i < P / 8; ++i) kv[i] = kv_n[i];
+    } else {
+      if (live) load_keys(page, kv);
+    }
+  }
+  (void)page;
+}
+
 // Blocks each warp scores: one, unless the grid would exceed about four
 // resident CTAs per SM.
 int blocks_per_warp_for(const Geom& g) {
@@ -237,10 +425,37 @@ cudaError_t launch_rb(const Geom& g, const int8_t* iq, const int8_t* ik_pool,
   return launch_t<P, RB, false>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
 }
 
+template <int P, bool PIPE>
+cudaError_t launch_mma_t(const Geom& g, const int8_t* iq, const int8_t* ik_pool,
+                         const int32_t* page_table, const int32_t* seqlens, int32_t* scores,
+                         bool pdl, cudaStream_t stream) {
+  const int bpw = blocks_per_warp_for(g);
+  dim3 grid((g.MB + kWarps * bpw - 1) / (kWarps * bpw), g.B);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, index_scores_mma_kernel<P, PIPE>, g, iq, ik_pool, page_table,
+                            seqlens, scores, bpw);
+}
+
 template <int P>
 cudaError_t launch_p(const Geom& g, const int8_t* iq, const int8_t* ik_pool,
                      const int32_t* page_table, const int32_t* seqlens, int32_t* scores,
                      bool pdl, cudaStream_t stream) {
+#if QSA_INDEX_MMA
+  if (g.R >= 2) {
+    if (blocks_per_warp_for(g) > 1)
+      return launch_mma_t<P, true>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
+    return launch_mma_t<P, false>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
+  }
+#endif
   if (g.R <= 1) return launch_rb<P, 1>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
   if (g.R <= 2) return launch_rb<P, 2>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
   if (g.R <= 4) return launch_rb<P, 4>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
