@@ -27,8 +27,11 @@
  * Geometry (qsa_geom_t, host values): B requests, R = rows_per_req query rows
  * per request (1 for decode, 1 + drafts for verify), T = B*R rows, row r =
  * b*R + j.  Hq query heads, Hkv KV heads, G = Hq/Hkv; query head h reads KV
- * head h / G.  D = head_dim = 128, Di = index_dim = 64, P = page_size (64 or
- * 128 tokens), MB = max_blocks (page-table row stride), NP = num_pages.
+ * head h / G.  D = head_dim (128, or 256: the geometry of PR #20276,
+ * Performance / shared code touched, 24 q / 2 KV heads at head_dim 256),
+ * Di = index_dim = 64, P = page_size (64 or 128 tokens at D = 128; 32 or 64
+ * at D = 256, 32 being the page size of PR #20276, Known limitations),
+ * MB = max_blocks (page-table row stride), NP = num_pages.
  *
  * Visibility: seqlens[b] = L_b counts the request's cached tokens including
  * its R newest rows; row j sees n = clamp(L_b - R + 1 + j, 0, MB*P) tokens
@@ -72,9 +75,9 @@ typedef struct {
     int rows_per_req;   /* R = 1 + draft rows, 1..8             */
     int num_q_heads;    /* Hq, 1..256                           */
     int num_kv_heads;   /* Hkv, divides Hq                      */
-    int head_dim;       /* D, must be 128                       */
+    int head_dim;       /* D, 128 or 256                        */
     int index_dim;      /* Di, must be 64                       */
-    int page_size;      /* P, 64 or 128                         */
+    int page_size;      /* P, 64|128 (D = 128), 32|64 (D = 256) */
     int max_blocks;     /* MB, page-table row stride, >= 1      */
     int num_pages;      /* NP, pages in every pool, >= 1        */
 } qsa_geom_t;
@@ -264,7 +267,7 @@ qsa_status_t qsa_sparse_decode_noalloc(const qsa_geom_t *geom, const void *q_bf1
  * table: NVFP4 storage in the decode prologue.  [F]: e2m1 pages with e4m3
  * block scales, one page index for every pool.
  *
- *   k_new, v_new  bf16 [T, Hkv, 128]  the new rows' keys and values
+ *   k_new, v_new  bf16 [T, Hkv, D]    the new rows' keys and values
  *   ik_new        int8 [T, 64]        the new rows' index keys
  *   k_scale,
  *   v_scale       fp32 > 0            per-tensor dequant multipliers (the same
@@ -285,9 +288,9 @@ qsa_status_t qsa_sparse_decode_noalloc(const qsa_geom_t *geom, const void *q_bf1
  * e4m3(sf) * scale is 0; a code rounded to magnitude zero is stored as +0).
  * The index key is copied as is.  Only the written slots change.
  * Returns QSA_ERR_INVALID_ARG for null pointers, non-positive or non-finite
- * scales, k_new / v_new not 8-byte aligned, ik_new / ik_pool not 4-byte
- * aligned or k_pool / v_pool not 2-byte aligned; geometry and device checks
- * as for the other calls.
+ * scales, k_new / v_new not D/16-byte aligned, ik_new / ik_pool not 4-byte
+ * aligned or k_pool / v_pool not D/64-byte aligned; geometry and device
+ * checks as for the other calls.
  */
 qsa_status_t qsa_store_kv_tokens(const qsa_geom_t *geom, const void *k_new_bf16,
                                  const void *v_new_bf16, const int8_t *ik_new,
@@ -313,8 +316,9 @@ qsa_status_t qsa_store_kv_tokens(const qsa_geom_t *geom, const void *k_new_bf16,
  *
  *   saved     device bytes, qsa_rollback_state_bytes(geom) long, 4-byte
  *             aligned, owned by the caller; row r's part starts at
- *             r * (144 * Hkv + 64) and holds, per KV head, the K codes (64 B),
- *             K scales (8), V codes (64), V scales (8), then the index key (64)
+ *             r * ((D + D/8) * Hkv + 64) and holds, per KV head, the K codes
+ *             (D/2 bytes), K scales (D/16), V codes (D/2), V scales (D/16),
+ *             then the index key (64)
  *   rejected  int32 [T], nonzero for a rejected row
  *   pools     as in qsa_store_kv_tokens (4-byte aligned here)
  *

@@ -25,8 +25,17 @@ qsa_status_t check_geom(const qsa_geom_t* g) {
   if (g->num_q_heads < 1 || g->num_kv_heads < 1) return QSA_ERR_INVALID_ARG;
   if (g->num_q_heads % g->num_kv_heads != 0) return QSA_ERR_INVALID_ARG;
   if (g->max_blocks < 1 || g->num_pages < 1) return QSA_ERR_INVALID_ARG;
-  if (g->head_dim != qsa::kHeadDim || g->index_dim != qsa::kIndexDim) return QSA_ERR_UNSUPPORTED;
-  if (g->page_size != 64 && g->page_size != 128) return QSA_ERR_UNSUPPORTED;
+  // head_dim 128 with 64/128-token pages; head_dim 256 (PR #20276, Performance,
+  // shared code touched: the target's 24 q / 2 KV heads at head_dim 256) with
+  // 32-token pages (Known limitations: tokens_per_block 32) or 64.
+  if (g->index_dim != qsa::kIndexDim) return QSA_ERR_UNSUPPORTED;
+  if (g->head_dim == 128) {
+    if (g->page_size != 64 && g->page_size != 128) return QSA_ERR_UNSUPPORTED;
+  } else if (g->head_dim == 256) {
+    if (g->page_size != 32 && g->page_size != 64) return QSA_ERR_UNSUPPORTED;
+  } else {
+    return QSA_ERR_UNSUPPORTED;
+  }
   if (g->rows_per_req > qsa::kMaxRows) return QSA_ERR_UNSUPPORTED;
   if (g->num_q_heads > qsa::kMaxQHeads) return QSA_ERR_UNSUPPORTED;
   if (g->max_blocks > qsa::kMaxBlocks) return QSA_ERR_UNSUPPORTED;
@@ -109,8 +118,10 @@ qsa_status_t qsa_store_kv_tokens(const qsa_geom_t* geom, const void* k_new_bf16,
     return QSA_ERR_INVALID_ARG;
   if (!(k_scale > 0.f) || !(v_scale > 0.f) || !isfinite(k_scale) || !isfinite(v_scale))
     return QSA_ERR_INVALID_ARG;
-  if (!aligned(k_new_bf16, 8) || !aligned(v_new_bf16, 8) || !aligned(ik_new, 4) ||
-      !aligned(ik_pool, 4) || !aligned(k_pool, 2) || !aligned(v_pool, 2))
+  // A lane moves D/32 values: 8 or 16 bytes of bf16 in, 2 or 4 code bytes out.
+  const uintptr_t in_al = geom->head_dim / 16, out_al = geom->head_dim / 64;
+  if (!aligned(k_new_bf16, in_al) || !aligned(v_new_bf16, in_al) || !aligned(ik_new, 4) ||
+      !aligned(ik_pool, 4) || !aligned(k_pool, out_al) || !aligned(v_pool, out_al))
     return QSA_ERR_INVALID_ARG;
   st = check_device();
   if (st != QSA_OK) return st;
@@ -121,7 +132,7 @@ qsa_status_t qsa_store_kv_tokens(const qsa_geom_t* geom, const void* k_new_bf16,
 
 size_t qsa_rollback_state_bytes(const qsa_geom_t* geom) {
   if (check_geom(geom) != QSA_OK) return 0;
-  return (size_t)geom->batch * geom->rows_per_req * qsa::rollback_row_bytes(geom->num_kv_heads);
+  return (size_t)geom->batch * geom->rows_per_req * qsa::rollback_row_bytes(geom->num_kv_heads, geom->head_dim);
 }
 
 qsa_status_t qsa_rollback_gather(const qsa_geom_t* geom, const int32_t* page_table,

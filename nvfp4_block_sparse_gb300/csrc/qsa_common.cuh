@@ -13,7 +13,6 @@
 
 namespace qsa {
 
-constexpr int kHeadDim = 128;
 constexpr int kIndexDim = 64;
 constexpr int kMaxRows = 8;           // rows per request (1 + drafts)
 constexpr int kMaxQHeads = 256;
@@ -186,7 +185,7 @@ struct Geom {
   int B, R, Hq, Hkv, D, Di, P, MB, NP;
 };
 
-size_t rollback_row_bytes(int hkv);
+size_t rollback_row_bytes(int hkv, int d);
 cudaError_t launch_rollback(const Geom& g, bool restore, const int32_t* page_table,
                             const int32_t* seqlens, const int32_t* rejected, uint8_t* k_pool,
                             uint8_t* k_sf, uint8_t* v_pool, uint8_t* v_sf, int8_t* ik_pool,

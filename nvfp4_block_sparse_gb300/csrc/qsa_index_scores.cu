@@ -467,6 +467,7 @@ cudaError_t launch_p(const Geom& g, const int8_t* iq, const int8_t* ik_pool,
 cudaError_t launch_index_scores(const Geom& g, const int8_t* iq, const int8_t* ik_pool,
                                 const int32_t* page_table, const int32_t* seqlens,
                                 int32_t* scores, bool pdl, cudaStream_t stream) {
+  if (g.P == 32) return launch_p<32>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
   if (g.P == 64) return launch_p<64>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
   return launch_p<128>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
 }

@@ -12,27 +12,34 @@
 // Row j of request b owns the slot at position L_b - R + j (block / P, slot
 // % P of its page); rows whose position is negative, at or past MB*P, or
 // whose page is invalid own no slot and are skipped.  A row's saved state is
-// kSavedRowBytes(Hkv) contiguous bytes:
-//   for each KV head: K codes (64) | K scales (8) | V codes (64) | V scales (8)
+// rollback_row_bytes(Hkv, D) contiguous bytes:
+//   for each KV head: K codes (D/2) | K scales (D/16) | V codes (D/2) |
+//   V scales (D/16)
 //   then the index key (64)
-// One warp per (row, KV head) moves its 144 bytes as 36 words; the KV-head-0
-// warp also moves the 64-byte index key.
+// One warp per (row, KV head) moves its 9D/8 bytes as 9D/32 words; the
+// KV-head-0 warp also moves the 64-byte index key.
 #include "qsa_common.cuh"
 
 namespace qsa {
 namespace {
 
 constexpr int kWarpsPerCta = 8;
-constexpr int kKvWords = (2 * (kHeadDim / 2 + kHeadDim / 16)) / 4;   // 36
 constexpr int kIkWords = kIndexDim / 4;                              // 16
 
-// Word w of the (row, KV head) state: its address in the pools.
-__device__ __forceinline__ uint32_t* pool_word(int w, size_t row, uint8_t* k_pool, uint8_t* k_sf,
-                                               uint8_t* v_pool, uint8_t* v_sf) {
-  if (w < 16) return reinterpret_cast<uint32_t*>(k_pool + row * (kHeadDim / 2)) + w;
-  if (w < 18) return reinterpret_cast<uint32_t*>(k_sf + row * (kHeadDim / 16)) + (w - 16);
-  if (w < 34) return reinterpret_cast<uint32_t*>(v_pool + row * (kHeadDim / 2)) + (w - 18);
-  return reinterpret_cast<uint32_t*>(v_sf + row * (kHeadDim / 16)) + (w - 34);
+// Words of one (row, KV head) state: K codes, K scales, V codes, V scales.
+__host__ __device__ __forceinline__ int kv_words(int d) { return 2 * (d / 8 + d / 64); }
+
+// Word w of the (row, KV head) state: its address in the pools (cw = D/8 code
+// words, sw = D/64 scale words per pool row).
+__device__ __forceinline__ uint32_t* pool_word(int w, int cw, int sw, size_t row, uint8_t* k_pool,
+                                               uint8_t* k_sf, uint8_t* v_pool, uint8_t* v_sf) {
+  if (w < cw) return reinterpret_cast<uint32_t*>(k_pool + row * 4 * cw) + w;
+  w -= cw;
+  if (w < sw) return reinterpret_cast<uint32_t*>(k_sf + row * 4 * sw) + w;
+  w -= sw;
+  if (w < cw) return reinterpret_cast<uint32_t*>(v_pool + row * 4 * cw) + w;
+  w -= cw;
+  return reinterpret_cast<uint32_t*>(v_sf + row * 4 * sw) + w;
 }
 
 template <bool RESTORE>
@@ -55,22 +62,23 @@ rollback_kernel(Geom g, const int32_t* __restrict__ page_table, const int32_t* _
   if (page < 0 || page >= g.NP) return;
   const int slot = (int)(pos % g.P);
   const size_t row = ((size_t)page * g.Hkv + kvh) * g.P + slot;
-  const size_t row_bytes = (size_t)g.Hkv * kKvWords * 4 + kIkWords * 4;
-  uint32_t* sv = reinterpret_cast<uint32_t*>(saved + (size_t)r * row_bytes) + kvh * kKvWords;
-  for (int w = lane; w < kKvWords; w += 32) {
-    uint32_t* p = pool_word(w, row, k_pool, k_sf, v_pool, v_sf);
+  const int kw = kv_words(g.D), cw = g.D / 8, sw = g.D / 64;
+  const size_t row_bytes = (size_t)g.Hkv * kw * 4 + kIkWords * 4;
+  uint32_t* sv = reinterpret_cast<uint32_t*>(saved + (size_t)r * row_bytes) + kvh * kw;
+  for (int w = lane; w < kw; w += 32) {
+    uint32_t* p = pool_word(w, cw, sw, row, k_pool, k_sf, v_pool, v_sf);
     if (RESTORE) *p = sv[w]; else sv[w] = *p;
   }
   if (kvh == 0 && lane < kIkWords) {
     uint32_t* p = reinterpret_cast<uint32_t*>(ik_pool + ((size_t)page * g.P + slot) * kIndexDim) + lane;
-    uint32_t* s = reinterpret_cast<uint32_t*>(saved + (size_t)r * row_bytes) + g.Hkv * kKvWords + lane;
+    uint32_t* s = reinterpret_cast<uint32_t*>(saved + (size_t)r * row_bytes) + g.Hkv * kw + lane;
     if (RESTORE) *p = *s; else *s = *p;
   }
 }
 
 }  // namespace
 
-size_t rollback_row_bytes(int hkv) { return (size_t)hkv * kKvWords * 4 + kIkWords * 4; }
+size_t rollback_row_bytes(int hkv, int d) { return (size_t)hkv * kv_words(d) * 4 + kIkWords * 4; }
 
 cudaError_t launch_rollback(const Geom& g, bool restore, const int32_t* page_table,
                             const int32_t* seqlens, const int32_t* rejected, uint8_t* k_pool,

@@ -50,14 +50,28 @@ namespace cg = cooperative_groups;
 namespace qsa {
 namespace {
 
-constexpr int kChunk = 64;                   // tokens per pipeline stage
-constexpr int kKBytes = kChunk * kHeadDim / 2;     // 4096
-constexpr int kSfBytes = kChunk * kHeadDim / 16;   // 512
-constexpr int kStageBytes = 2 * kKBytes + 2 * kSfBytes;  // 9216
+// Per head dimension D (128 or 256): a stage holds 8192 elements of K and of
+// V, i.e. 64 tokens at D = 128 and 32 tokens at D = 256, so every stage is
+// K codes 4 KB | V codes 4 KB | K scales 512 B | V scales 512 B.
+template <int D>
+struct Hd {
+  static_assert(D == 128 || D == 256, "head_dim 128 or 256");
+  static constexpr int kChunk = 8192 / D;            // tokens per pipeline stage
+  static constexpr int kRow = D / 2;                 // code bytes per token row
+  static constexpr int kSfRow = D / 16;              // scale bytes per token row
+  static constexpr int kKBytes = kChunk * kRow;      // 4096
+  static constexpr int kSfBytes = kChunk * kSfRow;   // 512
+  static constexpr int kPartStride = 4 + D;          // m, l, pad, pad, O[D] per column
+  static constexpr int kMt = kChunk / 16;            // 16-token tiles per stage
+  static constexpr int kDt = D / 16;                 // 16-dim tiles
+  static constexpr int kRuns = D / 128;              // 16-byte runs of a row per lane
+};
+constexpr int kStageBytes = 9216;
+static_assert(2 * Hd<128>::kKBytes + 2 * Hd<128>::kSfBytes == kStageBytes, "stage size");
+static_assert(2 * Hd<256>::kKBytes + 2 * Hd<256>::kSfBytes == kStageBytes, "stage size");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per bounded wait
-constexpr int kPartStride = 4 + kHeadDim;    // m, l, pad, pad, O[128] per column
 constexpr int kMaxCluster = 8;               // portable cluster size
 constexpr int kPtRowMax = 4096;              // page-table rows up to this stay in smem
 
@@ -77,7 +91,7 @@ struct Params {
   float* lse;
   int* status;          // workspace status word
   int* tickets;         // [units]
-  float* partials;      // [units][splits][R * 8 * NTR][kPartStride]
+  float* partials;      // [units][splits][R * 8 * NTR][4 + D]
   int splits;           // KV splits per unit
   int slices;           // head slices per KV head
   int cluster;          // 1: ticket merge through partials; >1: cluster (DSMEM) merge
@@ -119,30 +133,34 @@ __device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&o)[4]) 
       : "r"(w));
 }
 
-// Chunks a decode warp can own: the row's k entries of up to two 64-token
-// chunks, dealt over splits * W warps.
+// Chunks a decode warp can own: the row's k entries of up to two stages
+// each, dealt over splits * W warps.
 __host__ __device__ inline int decode_list_cap(int k, int splits, int W) {
   return (2 * k + splits * W - 1) / (splits * W);
 }
 
 // Shared-memory layout (bytes), shared by host sizing and the kernel.  ONE:
 // the single-row specialisation (no producer warp; W consumer warps).
-template <int NTR, int W, int S, bool ONE>
+template <int NTR, int W, int S, bool ONE, int D>
 struct Layout {
   static constexpr int kHsp = 8 * NTR;                            // padded head slice
   static constexpr int kWarps = ONE ? W : W + 1;
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kStagesSz = S * kStageBytes;
+  static constexpr int kPartStride = Hd<D>::kPartStride;
   // After the main loop the stage region holds the consumers' partials (co,
   // cm, cl) and the CTA partial (cp); the ticket merge then reuses it for its
-  // weights.  Before the main loop it holds the union's temporaries.
-  static constexpr int kCoSz = W * kHsp * kHeadDim * 4;
+  // weights.  Before the main loop it holds the union's temporaries.  With one
+  // consumer per row (direct) each consumer writes its row's partial straight
+  // into cp and co, cm, cl are not used.
+  static constexpr int kCoSz = W * kHsp * D * 4;
   static constexpr int kCmSz = W * kHsp * 4;
   static constexpr int kClSz = W * kHsp * 4;
-  static constexpr int kCpOff = kCoSz + kCmSz + kClSz;
+  __host__ __device__ static bool direct(int R) { return !ONE && W == R; }
+  __host__ __device__ static int cp_off(int R) { return direct(R) ? 0 : kCoSz + kCmSz + kClSz; }
   __host__ __device__ static int cp_bytes(int R) { return R * kHsp * kPartStride * 4; }
   __host__ __device__ static int region_bytes(int R, int k, int splits) {
-    const int combine = kCpOff + cp_bytes(R);
+    const int combine = cp_off(R) + cp_bytes(R);
     const int merge = R * kHsp * (splits + 2) * 4;
     const int uni = R * k * 4 * 2;
     int r = kStagesSz;
@@ -160,7 +178,7 @@ struct Layout {
   static size_t bytes(int R, int k, int mb, int splits) {
     size_t off = (size_t)region_bytes(R, k, splits) + rb_bytes(R, splits);
     off += 2 * S * 8;                                   // full + empty barriers
-    off += (size_t)R * kHsp * kHeadDim * 2;             // q (fp16)
+    off += (size_t)R * kHsp * D * 2;                    // q (fp16)
     off += (size_t)R * kHsp * 4 * 2;                    // cq, n per column
     off += 64 * 4;                                      // scalars
     // sel rows, union ids, pages, scan (verify) / per-warp chunk lists (decode)
@@ -175,12 +193,16 @@ struct Layout {
   }
 };
 
-// Register budget: 128 per thread for single-row 8-column CTAs (two CTAs of
-// 256 threads or four of 128 per SM), about 136 for 8-column verify CTAs with
-// up to four row consumers, unconstrained otherwise.
-template <int NTR, int W, bool ONE>
+// Register budget: at D = 128, 128 per thread for single-row 8-column CTAs
+// (two CTAs of 256 threads or four of 128 per SM), about 136 for 8-column
+// verify CTAs with up to four row consumers, unconstrained otherwise; at
+// D = 256 (twice the output and query fragments) two CTAs per SM of up to
+// five warps, unconstrained for wider ones.
+template <int NTR, int W, bool ONE, int D>
 constexpr int decode_min_blocks() {
-  return NTR != 1 ? 1 : (ONE ? (W <= 4 ? 4 : 2) : (W <= 4 ? 3 : 2));
+  return NTR != 1 ? 1
+                  : (D != 128 ? (W <= 4 ? 2 : 1)
+                              : (ONE ? (W <= 4 ? 4 : 2) : (W <= 4 ? 3 : 2)));
 }
 
 __device__ __forceinline__ void cluster_arrive_relaxed() {
@@ -193,71 +215,85 @@ __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// One 64-token chunk (K, V and their scales at sk, contiguous) into the
-// online-softmax state of 8*NTR columns.  tok0: the chunk's first token;
-// tokens at or past nrow are masked.
-template <int NTR>
+// One stage (K, V and their scales at sk, contiguous) into the online-softmax
+// state of 8*NTR columns.  tok0: the stage's first token; tokens at or past
+// nrow are masked.
+//
+// Lane (gid, tig) reads, for QK, bytes [D/8 * tig, D/8 * (tig+1)) of two token
+// rows per 16-token tile (D/4 dims, in D/128 runs of 16 bytes): k-step kk
+// covers dims D/4 * tig + 4*kk + {0..3} on both operands.  For PV it reads
+// bytes [D/16 * gid, D/16 * (gid+1)) of four token rows per k-step: dim tile
+// dt holds dims D/8 * gid + 2*dt (+1 in the upper eight rows).
+template <int NTR, int D>
 __device__ __forceinline__ void consume_chunk(const uint8_t* __restrict__ sk, int tok0, int nrow,
-                                              const uint32_t (&qf)[NTR][16],
+                                              const uint32_t (&qf)[NTR][D / 8],
                                               const float (&cq)[NTR][2], float (&m_run)[NTR][2],
                                               float (&l_run)[NTR][2],
-                                              float (&o_acc)[8][NTR][4]) {
+                                              float (&o_acc)[D / 16][NTR][4]) {
+  using H = Hd<D>;
+  constexpr int kMt = H::kMt;
   const int lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
-  const bool partial = tok0 + kChunk > nrow;
-  const uint8_t* sv = sk + kKBytes;
-  const uint8_t* sks = sk + 2 * kKBytes;
-  const uint8_t* svs = sks + kSfBytes;
+  const bool partial = tok0 + H::kChunk > nrow;
+  const uint8_t* sv = sk + H::kKBytes;
+  const uint8_t* sks = sk + 2 * H::kKBytes;
+  const uint8_t* svs = sks + H::kSfBytes;
 
-  // ---- S^T = K . Q^T over the chunk's four 16-token tiles ------------
+  // ---- S^T = K . Q^T over the stage's 16-token tiles -----------------
   // Tiles go in pairs: k-steps outside and the pair inside, so
   // consecutive MMAs feed different accumulators.
-  float sacc[4][NTR][4];
+  float sacc[kMt][NTR][4];
 #pragma unroll
-  for (int mt = 0; mt < 4; ++mt)
+  for (int mt = 0; mt < kMt; ++mt)
 #pragma unroll
     for (int nt = 0; nt < NTR; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.f;
 #pragma unroll
-  for (int m0 = 0; m0 < 4; m0 += 2) {
-    uint32_t wA[2][4], wB[2][4], scA[2][2], scB[2][2];
+  for (int m0 = 0; m0 < kMt; m0 += 2) {
 #pragma unroll
-    for (int gi = 0; gi < 2; ++gi) {
-      const int mt = m0 + gi;
-      const int rA = 16 * mt + (gid >> 1) + 4 * (gid & 1);
-      const int rB = rA + 8;
-      const uint4 kA = *reinterpret_cast<const uint4*>(sk + rA * 64 + 16 * tig);
-      const uint4 kB = *reinterpret_cast<const uint4*>(sk + rB * 64 + 16 * tig);
-      const uint32_t sA = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sks + rA * 8 + 2 * tig));
-      const uint32_t sB = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sks + rB * 8 + 2 * tig));
-      scA[gi][0] = prmt(sA, 0, 0x1010); scA[gi][1] = prmt(sA, 0, 0x3232);
-      scB[gi][0] = prmt(sB, 0, 0x1010); scB[gi][1] = prmt(sB, 0, 0x3232);
-      wA[gi][0] = kA.x; wA[gi][1] = kA.y; wA[gi][2] = kA.z; wA[gi][3] = kA.w;
-      wB[gi][0] = kB.x; wB[gi][1] = kB.y; wB[gi][2] = kB.z; wB[gi][3] = kB.w;
-    }
-#pragma unroll
-    for (int wd = 0; wd < 4; ++wd) {
-      uint32_t fa[2][4], fb[2][4];
+    for (int run = 0; run < H::kRuns; ++run) {
+      uint32_t wA[2][4], wB[2][4], scA[2][2], scB[2][2];
 #pragma unroll
       for (int gi = 0; gi < 2; ++gi) {
-        e2m1x8_to_f16x2x4(wA[gi][wd], fa[gi]);
-        e2m1x8_to_f16x2x4(wB[gi][wd], fb[gi]);
+        const int mt = m0 + gi;
+        const int rA = 16 * mt + (gid >> 1) + 4 * (gid & 1);
+        const int rB = rA + 8;
+        const int kb = (D / 8) * tig + 16 * run;          // byte of the run in a row
+        const uint4 kA = *reinterpret_cast<const uint4*>(sk + rA * H::kRow + kb);
+        const uint4 kB = *reinterpret_cast<const uint4*>(sk + rB * H::kRow + kb);
+        const uint32_t sA =
+            e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sks + rA * H::kSfRow + kb / 8));
+        const uint32_t sB =
+            e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sks + rB * H::kSfRow + kb / 8));
+        scA[gi][0] = prmt(sA, 0, 0x1010); scA[gi][1] = prmt(sA, 0, 0x3232);
+        scB[gi][0] = prmt(sB, 0, 0x1010); scB[gi][1] = prmt(sB, 0, 0x3232);
+        wA[gi][0] = kA.x; wA[gi][1] = kA.y; wA[gi][2] = kA.z; wA[gi][3] = kA.w;
+        wB[gi][0] = kB.x; wB[gi][1] = kB.y; wB[gi][2] = kB.z; wB[gi][3] = kB.w;
       }
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int kk = 2 * wd + h;
+      for (int wd = 0; wd < 4; ++wd) {
+        uint32_t fa[2][4], fb[2][4];
 #pragma unroll
         for (int gi = 0; gi < 2; ++gi) {
-          const uint32_t sa = scA[gi][wd >> 1], sb = scB[gi][wd >> 1];
-          uint32_t a[4];
-          a[0] = hmul2_u32(fa[gi][2 * h], sa);
-          a[2] = hmul2_u32(fa[gi][2 * h + 1], sa);
-          a[1] = hmul2_u32(fb[gi][2 * h], sb);
-          a[3] = hmul2_u32(fb[gi][2 * h + 1], sb);
+          e2m1x8_to_f16x2x4(wA[gi][wd], fa[gi]);
+          e2m1x8_to_f16x2x4(wB[gi][wd], fb[gi]);
+        }
 #pragma unroll
-          for (int nt = 0; nt < NTR; ++nt)
-            mma_f16_16816(sacc[m0 + gi][nt], a, qf[nt][2 * kk], qf[nt][2 * kk + 1]);
+        for (int h = 0; h < 2; ++h) {
+          const int kk = 8 * run + 2 * wd + h;
+#pragma unroll
+          for (int gi = 0; gi < 2; ++gi) {
+            const uint32_t sa = scA[gi][wd >> 1], sb = scB[gi][wd >> 1];
+            uint32_t a[4];
+            a[0] = hmul2_u32(fa[gi][2 * h], sa);
+            a[2] = hmul2_u32(fa[gi][2 * h + 1], sa);
+            a[1] = hmul2_u32(fb[gi][2 * h], sb);
+            a[3] = hmul2_u32(fb[gi][2 * h + 1], sb);
+#pragma unroll
+            for (int nt = 0; nt < NTR; ++nt)
+              mma_f16_16816(sacc[m0 + gi][nt], a, qf[nt][2 * kk], qf[nt][2 * kk + 1]);
+          }
         }
       }
     }
@@ -270,7 +306,7 @@ __device__ __forceinline__ void consume_chunk(const uint8_t* __restrict__ sk, in
 #pragma unroll
     for (int e = 0; e < 2; ++e) cmax[nt][e] = -INFINITY;
 #pragma unroll
-  for (int mt = 0; mt < 4; ++mt) {
+  for (int mt = 0; mt < kMt; ++mt) {
     const int tA = tok0 + 16 * mt + (gid >> 1) + 4 * (gid & 1);
     const int tB = tA + 8;
 #pragma unroll
@@ -318,7 +354,7 @@ __device__ __forceinline__ void consume_chunk(const uint8_t* __restrict__ sk, in
         const float alpha = exp2f(m_run[nt][e] - base[nt][e]);
         l_run[nt][e] *= alpha;
 #pragma unroll
-        for (int dt = 0; dt < 8; ++dt) {
+        for (int dt = 0; dt < H::kDt; ++dt) {
           o_acc[dt][nt][e] *= alpha;
           o_acc[dt][nt][2 + e] *= alpha;
         }
@@ -330,9 +366,9 @@ __device__ __forceinline__ void consume_chunk(const uint8_t* __restrict__ sk, in
     for (int e = 0; e < 2; ++e) m_run[nt][e] = fmaxf(m_run[nt][e], cmax[nt][e]);
 
   // P = exp2(z - base) -> fp16 -> transposed B fragments for P^T.
-  uint32_t pf[4][NTR][2];
+  uint32_t pf[kMt][NTR][2];
 #pragma unroll
-  for (int mt = 0; mt < 4; ++mt)
+  for (int mt = 0; mt < kMt; ++mt)
 #pragma unroll
     for (int nt = 0; nt < NTR; ++nt) {
       const float p0 = exp2f(sacc[mt][nt][0] - base[nt][0]);
@@ -345,52 +381,60 @@ __device__ __forceinline__ void consume_chunk(const uint8_t* __restrict__ sk, in
       pf[mt][nt][1] = movmatrix_trans(pack_half2(p2, p3));
     }
 
-  // ---- O^T += V^T . P^T over the eight 16-dim tiles -------------------
+  // ---- O^T += V^T . P^T over the 16-dim tiles -------------------------
 #pragma unroll
-  for (int ks = 0; ks < 4; ++ks) {
+  for (int ks = 0; ks < kMt; ++ks) {
     const int t0 = 16 * ks + tig;
-    const uint32_t sv01 = e4m3x2_to_f16x2((uint32_t)svs[t0 * 8 + gid] |
-                                          ((uint32_t)svs[(t0 + 4) * 8 + gid] << 8));
-    const uint32_t sv23 = e4m3x2_to_f16x2((uint32_t)svs[(t0 + 8) * 8 + gid] |
-                                          ((uint32_t)svs[(t0 + 12) * 8 + gid] << 8));
 #pragma unroll
-    for (int w4 = 0; w4 < 2; ++w4) {
-      // bytes [8*gid + 4*w4, +4) of the four token rows of this k-step
-      const int boff = 8 * gid + 4 * w4;
-      const uint32_t X = *reinterpret_cast<const uint32_t*>(sv + t0 * 64 + boff);
-      const uint32_t Y = *reinterpret_cast<const uint32_t*>(sv + (t0 + 4) * 64 + boff);
-      const uint32_t X2 = *reinterpret_cast<const uint32_t*>(sv + (t0 + 8) * 64 + boff);
-      const uint32_t Y2 = *reinterpret_cast<const uint32_t*>(sv + (t0 + 12) * 64 + boff);
-      const uint32_t LO = (X & 0x0F0F0F0Fu) | ((Y << 4) & 0xF0F0F0F0u);
-      const uint32_t HI = ((X >> 4) & 0x0F0F0F0Fu) | (Y & 0xF0F0F0F0u);
-      const uint32_t LO2 = (X2 & 0x0F0F0F0Fu) | ((Y2 << 4) & 0xF0F0F0F0u);
-      const uint32_t HI2 = ((X2 >> 4) & 0x0F0F0F0Fu) | (Y2 & 0xF0F0F0F0u);
-      uint32_t f0[4], f1[4], f2[4], f3[4];
-      e2m1x8_to_f16x2x4(LO, f0);
-      e2m1x8_to_f16x2x4(HI, f1);
-      e2m1x8_to_f16x2x4(LO2, f2);
-      e2m1x8_to_f16x2x4(HI2, f3);
+    for (int run = 0; run < H::kRuns; ++run) {
+      // scale block of bytes [D/16 * gid + 8 * run, +8) of the four token rows
+      const int blk = (D / 128) * gid + run;
+      const uint32_t sv01 = e4m3x2_to_f16x2((uint32_t)svs[t0 * H::kSfRow + blk] |
+                                            ((uint32_t)svs[(t0 + 4) * H::kSfRow + blk] << 8));
+      const uint32_t sv23 = e4m3x2_to_f16x2((uint32_t)svs[(t0 + 8) * H::kSfRow + blk] |
+                                            ((uint32_t)svs[(t0 + 12) * H::kSfRow + blk] << 8));
 #pragma unroll
-      for (int bi = 0; bi < 4; ++bi) {
-        const int dt = 4 * w4 + bi;
-        uint32_t a[4];
-        a[0] = hmul2_u32(f0[bi], sv01);
-        a[1] = hmul2_u32(f1[bi], sv01);
-        a[2] = hmul2_u32(f2[bi], sv23);
-        a[3] = hmul2_u32(f3[bi], sv23);
+      for (int w4 = 0; w4 < 2; ++w4) {
+        // bytes [D/16 * gid + 8 * run + 4 * w4, +4) of the four token rows
+        const int boff = (D / 16) * gid + 8 * run + 4 * w4;
+        const uint32_t X = *reinterpret_cast<const uint32_t*>(sv + t0 * H::kRow + boff);
+        const uint32_t Y = *reinterpret_cast<const uint32_t*>(sv + (t0 + 4) * H::kRow + boff);
+        const uint32_t X2 = *reinterpret_cast<const uint32_t*>(sv + (t0 + 8) * H::kRow + boff);
+        const uint32_t Y2 = *reinterpret_cast<const uint32_t*>(sv + (t0 + 12) * H::kRow + boff);
+        const uint32_t LO = (X & 0x0F0F0F0Fu) | ((Y << 4) & 0xF0F0F0F0u);
+        const uint32_t HI = ((X >> 4) & 0x0F0F0F0Fu) | (Y & 0xF0F0F0F0u);
+        const uint32_t LO2 = (X2 & 0x0F0F0F0Fu) | ((Y2 << 4) & 0xF0F0F0F0u);
+        const uint32_t HI2 = ((X2 >> 4) & 0x0F0F0F0Fu) | (Y2 & 0xF0F0F0F0u);
+        uint32_t f0[4], f1[4], f2[4], f3[4];
+        e2m1x8_to_f16x2x4(LO, f0);
+        e2m1x8_to_f16x2x4(HI, f1);
+        e2m1x8_to_f16x2x4(LO2, f2);
+        e2m1x8_to_f16x2x4(HI2, f3);
 #pragma unroll
-        for (int nt = 0; nt < NTR; ++nt)
-          mma_f16_16816(o_acc[dt][nt], a, pf[ks][nt][0], pf[ks][nt][1]);
+        for (int bi = 0; bi < 4; ++bi) {
+          const int dt = 8 * run + 4 * w4 + bi;
+          uint32_t a[4];
+          a[0] = hmul2_u32(f0[bi], sv01);
+          a[1] = hmul2_u32(f1[bi], sv01);
+          a[2] = hmul2_u32(f2[bi], sv23);
+          a[3] = hmul2_u32(f3[bi], sv23);
+#pragma unroll
+          for (int nt = 0; nt < NTR; ++nt)
+            mma_f16_16816(o_acc[dt][nt], a, pf[ks][nt][0], pf[ks][nt][1]);
+        }
       }
     }
   }
 }
 
-template <int NTR, int W, int S, bool ONE>
-__global__ void __launch_bounds__(Layout<NTR, W, S, ONE>::kThreads,
-                                  (decode_min_blocks<NTR, W, ONE>()))
+template <int NTR, int W, int S, bool ONE, int D>
+__global__ void __launch_bounds__(Layout<NTR, W, S, ONE, D>::kThreads,
+                                  (decode_min_blocks<NTR, W, ONE, D>()))
 sparse_decode_kernel(Params p) {
-  using Lay = Layout<NTR, W, S, ONE>;
+  using Lay = Layout<NTR, W, S, ONE, D>;
+  using H = Hd<D>;
+  constexpr int kPartStride = H::kPartStride;
+  constexpr int kChunk = H::kChunk;
   constexpr int kHsp = Lay::kHsp;
   constexpr int kWarps = Lay::kWarps;
   constexpr int kThreads = Lay::kThreads;
@@ -421,7 +465,7 @@ sparse_decode_kernel(Params p) {
   uint64_t* empty = full + S;
   off += 2 * S * 8;
   __half* qs = reinterpret_cast<__half*>(smem + off);
-  off += (size_t)R * kHsp * kHeadDim * 2;
+  off += (size_t)R * kHsp * D * 2;
   float* col_cq = reinterpret_cast<float*>(smem + off);
   int* col_n = reinterpret_cast<int*>(col_cq + ncols);
   off += (size_t)ncols * 4 * 2;
@@ -461,29 +505,40 @@ sparse_decode_kernel(Params p) {
     // column.  The scale maps |q|max into [256, 512): exact, and keeps bf16
     // queries of any magnitude inside fp16 range.  2^sq and its inverse are
     // built from exponent bits (|sq| <= 126 keeps both normal).
+    // Lane holds D/32 consecutive dims (4 or 8), read as D/128 8-byte words.
     constexpr int kMaxCols = (ONE ? 1 : kMaxRows) * kHsp;
     constexpr int kQPerWarp = (kMaxCols + kWarps - 1) / kWarps;
-    uint2 raw[kQPerWarp];
+    constexpr int kQw = D / 128;
+    uint2 raw[kQPerWarp][kQw];
 #pragma unroll
     for (int ci = 0; ci < kQPerWarp; ++ci) {
       const int c = warp + ci * kWarps;
-      raw[ci] = make_uint2(0u, 0u);
+#pragma unroll
+      for (int u = 0; u < kQw; ++u) raw[ci][u] = make_uint2(0u, 0u);
       if (c < ncols && (c % kHsp) < hs) {
         const int j = c / kHsp;
         const int h = kvh * G + hs0 + c % kHsp;
-        raw[ci] = *reinterpret_cast<const uint2*>(
-            p.q + ((size_t)(b * R + j) * g.Hq + h) * kHeadDim + lane * 4);
+        const uint2* src = reinterpret_cast<const uint2*>(
+            p.q + ((size_t)(b * R + j) * g.Hq + h) * D + lane * (D / 32));
+#pragma unroll
+        for (int u = 0; u < kQw; ++u) raw[ci][u] = src[u];
       }
     }
 #pragma unroll
     for (int ci = 0; ci < kQPerWarp; ++ci) {
       const int c = warp + ci * kWarps;
       if (c >= ncols) break;
-      const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw[ci].x);
-      const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw[ci].y);
-      const float v0 = __low2float(lo), v1 = __high2float(lo);
-      const float v2 = __low2float(hi), v3 = __high2float(hi);
-      float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+      float v[4 * kQw];
+#pragma unroll
+      for (int u = 0; u < kQw; ++u) {
+        const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw[ci][u].x);
+        const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw[ci][u].y);
+        v[4 * u + 0] = __low2float(lo); v[4 * u + 1] = __high2float(lo);
+        v[4 * u + 2] = __low2float(hi); v[4 * u + 3] = __high2float(hi);
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4 * kQw; ++i) amax = fmaxf(amax, fabsf(v[i]));
 #pragma unroll
       for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       const int ebits = (int)((__float_as_uint(amax) >> 23) & 0xFF);
@@ -491,9 +546,9 @@ sparse_decode_kernel(Params p) {
       sq = sq > 126 ? 126 : (sq < -126 ? -126 : sq);
       const float up = __uint_as_float((uint32_t)(sq + 127) << 23);
       const float down = __uint_as_float((uint32_t)(127 - sq) << 23);
-      __half2* dst = reinterpret_cast<__half2*>(qs + c * kHeadDim + lane * 4);
-      dst[0] = __floats2half2_rn(v0 * up, v1 * up);
-      dst[1] = __floats2half2_rn(v2 * up, v3 * up);
+      __half2* dst = reinterpret_cast<__half2*>(qs + c * D + lane * (D / 32));
+#pragma unroll
+      for (int i = 0; i < 2 * kQw; ++i) dst[i] = __floats2half2_rn(v[2 * i] * up, v[2 * i + 1] * up);
       if (lane == 0) {
         col_cq[c] = ((c % kHsp) < hs) ? p.k_scale * p.sm_scale * kLog2e * down : 0.f;
         col_n[c] = visible_tokens(L, R, c / kHsp, cap);
@@ -504,7 +559,7 @@ sparse_decode_kernel(Params p) {
   __syncthreads();   // barriers, page-table row and queries visible to every warp
   pdl_wait();        // the selections come from the preceding kernel
 
-  const int csh = (g.P == 2 * kChunk) ? 1 : 0;  // chunks per page: 1 << csh
+  const int csh = (g.P == 2 * kChunk) ? 1 : 0;  // stages per page: 1 << csh
   // Decode: each warp lists its own chunks straight from the selection (no
   // union and no CTA-wide barrier before the first copies).  Candidate chunk c
   // of the row (entry c >> csh, part c & csh) belongs to split c mod splits and,
@@ -713,11 +768,11 @@ sparse_decode_kernel(Params p) {
     const size_t row0 = ((size_t)s_upage[u] * g.Hkv + kvh) * g.P + (size_t)sub * kChunk;
     uint8_t* dst = region + st * kStageBytes;
     mbar_arrive_expect_tx(&full[st], kStageBytes);
-    bulk_g2s(dst, p.k_pool + row0 * (kHeadDim / 2), kKBytes, &full[st], pol);
-    bulk_g2s(dst + kKBytes, p.v_pool + row0 * (kHeadDim / 2), kKBytes, &full[st], pol);
-    bulk_g2s(dst + 2 * kKBytes, p.k_sf + row0 * (kHeadDim / 16), kSfBytes, &full[st], pol);
-    bulk_g2s(dst + 2 * kKBytes + kSfBytes, p.v_sf + row0 * (kHeadDim / 16), kSfBytes, &full[st],
-             pol);
+    bulk_g2s(dst, p.k_pool + row0 * H::kRow, H::kKBytes, &full[st], pol);
+    bulk_g2s(dst + H::kKBytes, p.v_pool + row0 * H::kRow, H::kKBytes, &full[st], pol);
+    bulk_g2s(dst + 2 * H::kKBytes, p.k_sf + row0 * H::kSfRow, H::kSfBytes, &full[st], pol);
+    bulk_g2s(dst + 2 * H::kKBytes + H::kSfBytes, p.v_sf + row0 * H::kSfRow, H::kSfBytes,
+             &full[st], pol);
   };
 
   // ---- producer (verify): stream this split's chunks through the stages ----
@@ -755,13 +810,13 @@ sparse_decode_kernel(Params p) {
   const int jw = ONE ? 0 : warp % R;            // the row this warp owns
   const int gw = ONE ? 0 : warp / R;
   float m_run[NTR][2], l_run[NTR][2];
-  float o_acc[8][NTR][4];
+  float o_acc[H::kDt][NTR][4];
 #pragma unroll
   for (int nt = 0; nt < NTR; ++nt)
 #pragma unroll
     for (int e = 0; e < 2; ++e) { m_run[nt][e] = -INFINITY; l_run[nt][e] = 0.f; }
 #pragma unroll
-  for (int dt = 0; dt < 8; ++dt)
+  for (int dt = 0; dt < H::kDt; ++dt)
 #pragma unroll
     for (int nt = 0; nt < NTR; ++nt)
 #pragma unroll
@@ -775,11 +830,11 @@ sparse_decode_kernel(Params p) {
     const size_t row0 = ((size_t)page * g.Hkv + kvh) * g.P + (size_t)(tok0 & (g.P - 1));
     uint8_t* dst = region + st * kStageBytes;
     mbar_arrive_expect_tx(&full[st], kStageBytes);
-    bulk_g2s(dst, p.k_pool + row0 * (kHeadDim / 2), kKBytes, &full[st], pol);
-    bulk_g2s(dst + kKBytes, p.v_pool + row0 * (kHeadDim / 2), kKBytes, &full[st], pol);
-    bulk_g2s(dst + 2 * kKBytes, p.k_sf + row0 * (kHeadDim / 16), kSfBytes, &full[st], pol);
-    bulk_g2s(dst + 2 * kKBytes + kSfBytes, p.v_sf + row0 * (kHeadDim / 16), kSfBytes, &full[st],
-             pol);
+    bulk_g2s(dst, p.k_pool + row0 * H::kRow, H::kKBytes, &full[st], pol);
+    bulk_g2s(dst + H::kKBytes, p.v_pool + row0 * H::kRow, H::kKBytes, &full[st], pol);
+    bulk_g2s(dst + 2 * H::kKBytes, p.k_sf + row0 * H::kSfRow, H::kSfBytes, &full[st], pol);
+    bulk_g2s(dst + 2 * H::kKBytes + H::kSfBytes, p.v_sf + row0 * H::kSfRow, H::kSfBytes,
+             &full[st], pol);
   };
   if (ONE && lane == 0) {
     fence_proxy_async_smem();   // after the fused selection's scratch in the region
@@ -794,14 +849,14 @@ sparse_decode_kernel(Params p) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) cq[nt][e] = col_cq[cbase + nt * 8 + 2 * tig + e];
     const int nrow = col_n[cbase];              // tokens this row sees
-    // Q^T fragments: column nt*8+gid of the row, dims [32*tig, 32*tig+32).
-    uint32_t qf[NTR][16];
+    // Q^T fragments: column nt*8+gid of the row, dims [D/4*tig, D/4*(tig+1)).
+    uint32_t qf[NTR][D / 8];
 #pragma unroll
     for (int nt = 0; nt < NTR; ++nt) {
       const uint4* src =
-          reinterpret_cast<const uint4*>(qs + (cbase + nt * 8 + gid) * kHeadDim + 32 * tig);
+          reinterpret_cast<const uint4*>(qs + (cbase + nt * 8 + gid) * D + (D / 4) * tig);
 #pragma unroll
-      for (int v4 = 0; v4 < 4; ++v4) {
+      for (int v4 = 0; v4 < D / 32; ++v4) {
         const uint4 x = src[v4];
         qf[nt][4 * v4 + 0] = x.x; qf[nt][4 * v4 + 1] = x.y;
         qf[nt][4 * v4 + 2] = x.z; qf[nt][4 * v4 + 3] = x.w;
@@ -817,7 +872,7 @@ sparse_decode_kernel(Params p) {
           if (lane == 0) atomicExch(p.status, kStatusWaitTimeout);
           break;
         }
-        consume_chunk<NTR>(region + st * kStageBytes, wl[2 * q + 1], nrow, qf, cq, m_run, l_run,
+        consume_chunk<NTR, D>(region + st * kStageBytes, wl[2 * q + 1], nrow, qf, cq, m_run, l_run,
                            o_acc);
         __syncwarp();   // every lane's reads of the stage are done
         if (lane == 0 && q + kSpw < wcnt) {
@@ -845,7 +900,7 @@ sparse_decode_kernel(Params p) {
           if (lane == 0) atomicExch(p.status, kStatusWaitTimeout);
         }
         if (mine && !dead)
-          consume_chunk<NTR>(region + st * kStageBytes, (ue & 0xFFFFFF) * g.P + (c & csh) * kChunk,
+          consume_chunk<NTR, D>(region + st * kStageBytes, (ue & 0xFFFFFF) * g.P + (c & csh) * kChunk,
                              nrow, qf, cq, m_run, l_run, o_acc);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
@@ -867,31 +922,42 @@ sparse_decode_kernel(Params p) {
 
   // ---- combine the consumers of this CTA ------------------------------------
   __syncthreads();   // every copy landed and was consumed: reuse the stage region
-  float* co = reinterpret_cast<float*>(region);                  // [W][kHsp][128]
-  float* cm = co + W * kHsp * kHeadDim;                           // [W][kHsp]
+  const bool direct = Lay::direct(R);
+  float* co = reinterpret_cast<float*>(region);                  // [W][kHsp][D]
+  float* cm = co + W * kHsp * D;                                  // [W][kHsp]
   float* cl = cm + W * kHsp;                                      // [W][kHsp]
-  float* cp = reinterpret_cast<float*>(region + Lay::kCpOff);     // [ncols][kPartStride]
+  float* cp = reinterpret_cast<float*>(region + Lay::cp_off(R));  // [ncols][kPartStride]
   if (!producer) {
+    // Direct: consumer `warp` is row `warp`'s only consumer, and its state is
+    // the CTA partial of the row's columns.
+    float* dsto = direct ? cp + (size_t)warp * kHsp * kPartStride + 4 : co + (size_t)warp * kHsp * D;
+    const int cstride = direct ? kPartStride : D;
     if (gid == 0) {
 #pragma unroll
       for (int nt = 0; nt < NTR; ++nt)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int cc = nt * 8 + 2 * tig + e;
-          cm[warp * kHsp + cc] = m_run[nt][e];
-          cl[warp * kHsp + cc] = l_run[nt][e];
+          if (direct) {
+            float* pc = cp + ((size_t)warp * kHsp + cc) * kPartStride;
+            pc[0] = (l_run[nt][e] > 0.f) ? m_run[nt][e] : -INFINITY;
+            pc[1] = l_run[nt][e];
+          } else {
+            cm[warp * kHsp + cc] = m_run[nt][e];
+            cl[warp * kHsp + cc] = l_run[nt][e];
+          }
         }
     }
-    // O^T accumulators: dim 16*gid + 2*dt (+1 for c2/c3), column nt*8+2*tig+e.
+    // O^T accumulators: dim D/8*gid + 2*dt (+1 for c2/c3), column nt*8+2*tig+e.
 #pragma unroll
-    for (int dt = 0; dt < 8; ++dt)
+    for (int dt = 0; dt < H::kDt; ++dt)
 #pragma unroll
       for (int nt = 0; nt < NTR; ++nt)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int cc = nt * 8 + 2 * tig + e;
-          *reinterpret_cast<float2*>(co + ((size_t)warp * kHsp + cc) * kHeadDim + 16 * gid +
-                                     2 * dt) = make_float2(o_acc[dt][nt][e], o_acc[dt][nt][2 + e]);
+          *reinterpret_cast<float2*>(dsto + (size_t)cc * cstride + (D / 8) * gid + 2 * dt) =
+              make_float2(o_acc[dt][nt][e], o_acc[dt][nt][2 + e]);
         }
   }
   __syncthreads();
@@ -907,15 +973,24 @@ sparse_decode_kernel(Params p) {
     uint2 packed;
     packed.x = *reinterpret_cast<uint32_t*>(&o01);
     packed.y = *reinterpret_cast<uint32_t*>(&o23);
-    *reinterpret_cast<uint2*>(p.out + orow * kHeadDim + d4) = packed;
+    *reinterpret_cast<uint2*>(p.out + orow * D + d4) = packed;
     if (d4 == 0) p.lse[orow] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
   };
 
+  if (direct) {
+    if (p.splits == 1) {
+      for (int idx = tid; idx < ncols * (D / 4); idx += kThreads) {
+        const int c = idx / (D / 4), d4 = (idx % (D / 4)) * 4;
+        const float* pc = cp + (size_t)c * kPartStride;
+        store_out(c, d4, *reinterpret_cast<const float4*>(pc + 4 + d4), pc[1], pc[0]);
+      }
+    }
+  } else {
   // CTA partial per column (j, hh): m (log2 domain, -inf when empty), l, O,
   // merged over the consumers of row j (warps j, j + R, ...).  With one split
   // it is the result.
-  for (int idx = tid; idx < ncols * (kHeadDim / 4); idx += kThreads) {
-    const int c = idx / (kHeadDim / 4), d4 = (idx % (kHeadDim / 4)) * 4;
+  for (int idx = tid; idx < ncols * (D / 4); idx += kThreads) {
+    const int c = idx / (D / 4), d4 = (idx % (D / 4)) * 4;
     const int j = c / kHsp, cc = c % kHsp;
     float mv[W];
     float mx = -INFINITY;
@@ -933,7 +1008,7 @@ sparse_decode_kernel(Params p) {
         const float wt = exp2f(mv[w] - M);
         Lsum += cl[w * kHsp + cc] * wt;
         const float4 v =
-            *reinterpret_cast<const float4*>(co + ((size_t)w * kHsp + cc) * kHeadDim + d4);
+            *reinterpret_cast<const float4*>(co + ((size_t)w * kHsp + cc) * D + d4);
         O.x += v.x * wt; O.y += v.y * wt; O.z += v.z * wt; O.w += v.w * wt;
       }
     }
@@ -948,6 +1023,7 @@ sparse_decode_kernel(Params p) {
         pc[1] = Lsum;
       }
     }
+  }
   }
   if (p.splits == 1) return;
   __syncthreads();
@@ -970,8 +1046,8 @@ sparse_decode_kernel(Params p) {
     }
     cluster_arrive_release();
     cluster_wait_acquire();
-    for (int idx = tid; idx < per * (kHeadDim / 4); idx += kThreads) {
-      const int q = idx / (kHeadDim / 4), d4 = (idx % (kHeadDim / 4)) * 4;
+    for (int idx = tid; idx < per * (D / 4); idx += kThreads) {
+      const int q = idx / (D / 4), d4 = (idx % (D / 4)) * 4;
       const int c = q * CL + s;
       if (c >= ncols) continue;
       float mr[kMaxCluster];
@@ -1044,8 +1120,8 @@ sparse_decode_kernel(Params p) {
     }
   }
   __syncthreads();
-  for (int idx = tid; idx < ncols * (kHeadDim / 4); idx += kThreads) {
-    const int c = idx / (kHeadDim / 4), d4 = (idx % (kHeadDim / 4)) * 4;
+  for (int idx = tid; idx < ncols * (D / 4); idx += kThreads) {
+    const int c = idx / (D / 4), d4 = (idx % (D / 4)) * 4;
     float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
     const float* src = parts + (size_t)c * kPartStride + 4 + d4;
     const float* wrow = wsplit + c * p.splits;
@@ -1075,12 +1151,12 @@ constexpr size_t kWsHeader = 256;
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-template <int NTR, int W, int S, bool ONE>
+template <int NTR, int W, int S, bool ONE, int D>
 cudaLaunchConfig_t make_config(dim3 grid, size_t smem, cudaStream_t stream,
                                cudaLaunchAttribute* attr, bool pdl, int cluster) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(Layout<NTR, W, S, ONE>::kThreads);
+  cfg.blockDim = dim3(Layout<NTR, W, S, ONE, D>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   int n = 0;
@@ -1102,7 +1178,7 @@ cudaLaunchConfig_t make_config(dim3 grid, size_t smem, cudaStream_t stream,
 }
 
 // Whether a cluster of `cl` CTAs of this variant can be resident at all.
-template <int NTR, int W, int S, bool ONE>
+template <int NTR, int W, int S, bool ONE, int D>
 bool cluster_fits(int cl, size_t smem, dim3 grid) {
   struct Entry { int dev, cl; size_t smem; bool ok; };
   static std::mutex mu;
@@ -1116,9 +1192,9 @@ bool cluster_fits(int cl, size_t smem, dim3 grid) {
       if (e.dev == dev && e.cl == cl && e.smem == smem) return e.ok;
   }
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = make_config<NTR, W, S, ONE>(grid, smem, 0, attr, false, cl);
+  cudaLaunchConfig_t cfg = make_config<NTR, W, S, ONE, D>(grid, smem, 0, attr, false, cl);
   int n = 0;
-  const bool ok = cudaOccupancyMaxActiveClusters(&n, sparse_decode_kernel<NTR, W, S, ONE>,
+  const bool ok = cudaOccupancyMaxActiveClusters(&n, sparse_decode_kernel<NTR, W, S, ONE, D>,
                                                  &cfg) == cudaSuccess && n > 0;
   cudaGetLastError();
   std::lock_guard<std::mutex> lock(mu);
@@ -1126,31 +1202,31 @@ bool cluster_fits(int cl, size_t smem, dim3 grid) {
   return ok;
 }
 
-template <int NTR, int W, int S, bool ONE>
+template <int NTR, int W, int S, bool ONE, int D>
 cudaError_t launch_t(Params prm, dim3 grid, int R, int k, int mb, bool pdl,
                      cudaStream_t stream) {
-  const size_t smem = Layout<NTR, W, S, ONE>::bytes(R, k, mb, prm.splits);
-  cudaError_t e = cudaFuncSetAttribute(sparse_decode_kernel<NTR, W, S, ONE>,
+  const size_t smem = Layout<NTR, W, S, ONE, D>::bytes(R, k, mb, prm.splits);
+  cudaError_t e = cudaFuncSetAttribute(sparse_decode_kernel<NTR, W, S, ONE, D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   prm.cluster = 1;
-  if (prm.splits > 1 && cluster_fits<NTR, W, S, ONE>(prm.splits, smem, grid))
+  if (prm.splits > 1 && cluster_fits<NTR, W, S, ONE, D>(prm.splits, smem, grid))
     prm.cluster = prm.splits;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg =
-      make_config<NTR, W, S, ONE>(grid, smem, stream, attr, pdl, prm.cluster);
-  return cudaLaunchKernelEx(&cfg, sparse_decode_kernel<NTR, W, S, ONE>, prm);
+      make_config<NTR, W, S, ONE, D>(grid, smem, stream, attr, pdl, prm.cluster);
+  return cudaLaunchKernelEx(&cfg, sparse_decode_kernel<NTR, W, S, ONE, D>, prm);
 }
 
 // Resident CTAs per SM of a variant, for split sizing.
-template <int NTR, int W, int S, bool ONE>
+template <int NTR, int W, int S, bool ONE, int D>
 int resident_ctas(int R, int k, int mb, int splits) {
-  const size_t smem = Layout<NTR, W, S, ONE>::bytes(R, k, mb, splits);
-  cudaFuncSetAttribute(sparse_decode_kernel<NTR, W, S, ONE>,
+  const size_t smem = Layout<NTR, W, S, ONE, D>::bytes(R, k, mb, splits);
+  cudaFuncSetAttribute(sparse_decode_kernel<NTR, W, S, ONE, D>,
                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sparse_decode_kernel<NTR, W, S, ONE>,
-                                                    Layout<NTR, W, S, ONE>::kThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sparse_decode_kernel<NTR, W, S, ONE, D>,
+                                                    Layout<NTR, W, S, ONE, D>::kThreads,
                                                     smem) != cudaSuccess) {
     cudaGetLastError();
     n = 1;
@@ -1176,27 +1252,41 @@ int resident_ctas(int R, int k, int mb, int splits) {
 #ifndef QSA_DECODE_WARPS_R4
 #define QSA_DECODE_WARPS_R4 4
 #endif
+// head_dim 256: one 8-column tile per row (the output and query fragments are
+// twice as large; wider head groups take several slices), four decode
+// consumers.
 #define QSA_DECODE_VARIANTS(X)                                            \
-  X(1, 1, QSA_DECODE_WARPS_R1, QSA_DECODE_STAGES_R1, true)                \
-  X(2, 1, QSA_DECODE_WARPS_R1, QSA_DECODE_STAGES_R1, true)                \
-  X(1, 2, QSA_DECODE_WARPS_R2, QSA_DECODE_STAGES_RN, false)              \
-  X(2, 2, 4, QSA_DECODE_STAGES_RN, false)                                 \
-  X(1, 3, 6, QSA_DECODE_STAGES_RN, false) X(2, 3, 6, QSA_DECODE_STAGES_RN, false) \
-  X(1, 4, QSA_DECODE_WARPS_R4, QSA_DECODE_STAGES_RN, false)              \
-  X(2, 4, 4, QSA_DECODE_STAGES_RN, false)                                 \
-  X(1, 5, 5, QSA_DECODE_STAGES_RN, false) X(2, 5, 5, QSA_DECODE_STAGES_RN, false) \
-  X(1, 6, 6, QSA_DECODE_STAGES_RN, false) X(2, 6, 6, QSA_DECODE_STAGES_RN, false) \
-  X(1, 7, 7, QSA_DECODE_STAGES_RN, false) X(2, 7, 7, QSA_DECODE_STAGES_RN, false) \
-  X(1, 8, 8, QSA_DECODE_STAGES_RN, false) X(2, 8, 8, QSA_DECODE_STAGES_RN, false)
+  X(1, 1, QSA_DECODE_WARPS_R1, QSA_DECODE_STAGES_R1, true, 128)           \
+  X(2, 1, QSA_DECODE_WARPS_R1, QSA_DECODE_STAGES_R1, true, 128)           \
+  X(1, 2, QSA_DECODE_WARPS_R2, QSA_DECODE_STAGES_RN, false, 128)         \
+  X(2, 2, 4, QSA_DECODE_STAGES_RN, false, 128)                            \
+  X(1, 3, 6, QSA_DECODE_STAGES_RN, false, 128)                            \
+  X(2, 3, 6, QSA_DECODE_STAGES_RN, false, 128)                            \
+  X(1, 4, QSA_DECODE_WARPS_R4, QSA_DECODE_STAGES_RN, false, 128)         \
+  X(2, 4, 4, QSA_DECODE_STAGES_RN, false, 128)                            \
+  X(1, 5, 5, QSA_DECODE_STAGES_RN, false, 128) X(2, 5, 5, QSA_DECODE_STAGES_RN, false, 128) \
+  X(1, 6, 6, QSA_DECODE_STAGES_RN, false, 128) X(2, 6, 6, QSA_DECODE_STAGES_RN, false, 128) \
+  X(1, 7, 7, QSA_DECODE_STAGES_RN, false, 128) X(2, 7, 7, QSA_DECODE_STAGES_RN, false, 128) \
+  X(1, 8, 8, QSA_DECODE_STAGES_RN, false, 128) X(2, 8, 8, QSA_DECODE_STAGES_RN, false, 128) \
+  X(1, 1, 4, 8, true, 256)                                                \
+  X(1, 2, 4, QSA_DECODE_STAGES_RN, false, 256)                            \
+  X(1, 3, 6, QSA_DECODE_STAGES_RN, false, 256)                            \
+  X(1, 4, 4, QSA_DECODE_STAGES_RN, false, 256)                            \
+  X(1, 5, 5, QSA_DECODE_STAGES_RN, false, 256)                            \
+  X(1, 6, 6, QSA_DECODE_STAGES_RN, false, 256)                            \
+  X(1, 7, 7, QSA_DECODE_STAGES_RN, false, 256)                            \
+  X(1, 8, 8, QSA_DECODE_STAGES_RN, false, 256)
 
 int tiles_per_row(const Geom& g) {
   const int G = g.Hq / g.Hkv;
-  return G <= 8 ? 1 : 2;
+  return (G <= 8 || g.D != 128) ? 1 : 2;
 }
 
-int variant_resident(int ntr, int R, int k, int mb, int splits) {
-#define X(NTR_, R_, W_, S_, ONE_) \
-  if (ntr == NTR_ && R == R_) return resident_ctas<NTR_, W_, S_, ONE_>(R, k, mb, splits);
+int stage_tokens(const Geom& g) { return 8192 / g.D; }
+
+int variant_resident(int ntr, int R, int d, int k, int mb, int splits) {
+#define X(NTR_, R_, W_, S_, ONE_, D_) \
+  if (ntr == NTR_ && R == R_ && d == D_) return resident_ctas<NTR_, W_, S_, ONE_, D_>(R, k, mb, splits);
   QSA_DECODE_VARIANTS(X)
 #undef X
   return 1;
@@ -1209,10 +1299,10 @@ int variant_resident(int ntr, int R, int k, int mb, int splits) {
 bool decode_can_fuse_select(const Geom& g) {
   if (g.R != 1) return false;
   const int ntr = tiles_per_row(g);
-#define X(NTR_, R_, W_, S_, ONE_)                                                   \
-  if (ONE_ && ntr == NTR_ && R_ == 1)                                               \
-    return select_row_smem<Layout<NTR_, W_, S_, ONE_>::kThreads>(g.MB) <=           \
-           (size_t)Layout<NTR_, W_, S_, ONE_>::kStagesSz;
+#define X(NTR_, R_, W_, S_, ONE_, D_)                                                 \
+  if (ONE_ && ntr == NTR_ && R_ == 1 && g.D == D_)                                      \
+    return select_row_smem<Layout<NTR_, W_, S_, ONE_, D_>::kThreads>(g.MB) <=           \
+           (size_t)Layout<NTR_, W_, S_, ONE_, D_>::kStagesSz;
   QSA_DECODE_VARIANTS(X)
 #undef X
   return false;
@@ -1226,14 +1316,14 @@ DecodePlan plan_sparse_decode(const Geom& g, int k, int num_splits) {
   pl.cols = g.R * 8 * ntr;                               // padded columns per CTA
   const long long units = (long long)g.B * g.Hkv * pl.qgroups;
   const int max_union = min(g.R * k, g.MB);
-  const int max_chunks = max(1, max_union * (g.P / kChunk));
+  const int max_chunks = max(1, max_union * (g.P / stage_tokens(g)));
   int splits = num_splits;
   if (splits <= 0) {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaGetLastError();
-    const int resident = variant_resident(ntr, g.R, k, g.MB, kMaxCluster);
+    const int resident = variant_resident(ntr, g.R, g.D, k, g.MB, kMaxCluster);
     const long long slots = (long long)sms * resident;
     // One wave: the most splits up to a portable cluster (whose splits
     // merge in distributed shared memory) with units * splits within
@@ -1249,7 +1339,7 @@ DecodePlan plan_sparse_decode(const Geom& g, int k, int num_splits) {
   }
   pl.splits = splits;
   size_t ws = kWsHeader + align256((size_t)units * sizeof(int));
-  if (splits > 1) ws += (size_t)units * splits * pl.cols * kPartStride * sizeof(float);
+  if (splits > 1) ws += (size_t)units * splits * pl.cols * (4 + g.D) * sizeof(float);
   pl.ws_bytes = ws;
   return pl;
 }
@@ -1284,9 +1374,9 @@ cudaError_t launch_sparse_decode(const Geom& g, const DecodePlan& plan, const vo
   prm.cluster = 1;
   dim3 grid(plan.splits, g.Hkv * plan.qgroups, g.B);
   const int ntr = tiles_per_row(g);
-#define X(NTR_, R_, W_, S_, ONE_)                                    \
-  if (ntr == NTR_ && g.R == R_)                                        \
-    return launch_t<NTR_, W_, S_, ONE_>(prm, grid, g.R, k, g.MB, pdl, stream);
+#define X(NTR_, R_, W_, S_, ONE_, D_)                                \
+  if (ntr == NTR_ && g.R == R_ && g.D == D_)                           \
+    return launch_t<NTR_, W_, S_, ONE_, D_>(prm, grid, g.R, k, g.MB, pdl, stream);
   QSA_DECODE_VARIANTS(X)
 #undef X
   return cudaErrorInvalidValue;

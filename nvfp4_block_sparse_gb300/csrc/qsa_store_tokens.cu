@@ -19,9 +19,10 @@
 // with every division and product an IEEE fp32 operation in that order.
 // The row's int8 index key is copied into the index pool at the same slot.
 //
-// One warp per (row, KV head, K|V): lane l holds elements 4l..4l+3, so the
-// four lanes of a 16-element block reduce its maximum with two shuffles and
-// each lane writes two code bytes; lane 4g writes block g's scale byte.
+// One warp per (row, KV head, K|V): lane l holds the E = D/32 elements
+// E*l..E*l+E-1 (4 at head_dim 128, 8 at 256), so the 16/E lanes of a
+// 16-element block reduce its maximum with shuffles and each lane writes E/2
+// code bytes; the first lane of block g writes its scale byte.
 #include "qsa_common.cuh"
 
 namespace qsa {
@@ -57,6 +58,7 @@ __device__ __forceinline__ uint32_t canon_zero(uint32_t byte) {
   return byte;
 }
 
+template <int D>
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
 store_tokens_kernel(Geom g, const __nv_bfloat16* __restrict__ k_new,
                     const __nv_bfloat16* __restrict__ v_new, const int8_t* __restrict__ ik_new,
@@ -81,28 +83,41 @@ store_tokens_kernel(Geom g, const __nv_bfloat16* __restrict__ k_new,
   const int page = page_table[(size_t)b * g.MB + beta];
   if (page < 0 || page >= g.NP) return;
 
-  const __nv_bfloat16* src = (is_v ? v_new : k_new) + ((size_t)r * g.Hkv + kvh) * kHeadDim;
+  constexpr int E = D / 32;        // elements per lane
+  constexpr int LPB = 16 / E;      // lanes per 16-element block
+  const __nv_bfloat16* src = (is_v ? v_new : k_new) + ((size_t)r * g.Hkv + kvh) * D;
   const float s = is_v ? v_scale : k_scale;
-  const uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * lane);
-  const __nv_bfloat162 p01 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-  const __nv_bfloat162 p23 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-  const float x0 = __low2float(p01), x1 = __high2float(p01);
-  const float x2 = __low2float(p23), x3 = __high2float(p23);
-  float a = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
-  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+  float x[E];
+#pragma unroll
+  for (int u = 0; u < E / 4; ++u) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(src + E * lane + 4 * u);
+    const __nv_bfloat162 p01 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+    const __nv_bfloat162 p23 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+    x[4 * u + 0] = __low2float(p01); x[4 * u + 1] = __high2float(p01);
+    x[4 * u + 2] = __low2float(p23); x[4 * u + 3] = __high2float(p23);
+  }
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < E; ++i) a = fmaxf(a, fabsf(x[i]));
+#pragma unroll
+  for (int o = 1; o < LPB; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
   const uint32_t sf = f32_to_e4m3(__fdiv_rn(__fdiv_rn(a, 6.0f), s));
   const float den = __fmul_rn(e4m3_to_f32(sf), s);
-  uint32_t b0 = 0, b1 = 0;
+  uint32_t codes = 0;   // E/2 code bytes, element 2i in the low nibble of byte i
   if (den != 0.f) {
-    b0 = canon_zero(f32x2_to_e2m1x2(__fdiv_rn(x0, den), __fdiv_rn(x1, den)));
-    b1 = canon_zero(f32x2_to_e2m1x2(__fdiv_rn(x2, den), __fdiv_rn(x3, den)));
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i)
+      codes |= canon_zero(f32x2_to_e2m1x2(__fdiv_rn(x[2 * i], den),
+                                          __fdiv_rn(x[2 * i + 1], den))) << (8 * i);
   }
   const size_t row = ((size_t)page * g.Hkv + kvh) * g.P + slot;   // token row in the pool
   uint8_t* pool = is_v ? v_pool : k_pool;
   uint8_t* sfp = is_v ? v_sf : k_sf;
-  *reinterpret_cast<uint16_t*>(pool + row * (kHeadDim / 2) + 2 * lane) = (uint16_t)(b0 | (b1 << 8));
-  if ((lane & 3) == 0) sfp[row * (kHeadDim / 16) + (lane >> 2)] = (uint8_t)sf;
+  if constexpr (E == 4)
+    *reinterpret_cast<uint16_t*>(pool + row * (D / 2) + 2 * lane) = (uint16_t)codes;
+  else
+    *reinterpret_cast<uint32_t*>(pool + row * (D / 2) + 4 * lane) = codes;
+  if (lane % LPB == 0) sfp[row * (D / 16) + lane / LPB] = (uint8_t)sf;
   // The index key: one warp per row (K side of KV head 0), 16 lanes x 4 B.
   if (!is_v && kvh == 0 && lane < kIndexDim / 4) {
     const uint32_t w = *reinterpret_cast<const uint32_t*>(ik_new + (size_t)r * kIndexDim + 4 * lane);
@@ -128,8 +143,8 @@ cudaError_t launch_store_tokens(const Geom& g, const void* k_new, const void* v_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, store_tokens_kernel, g,
-                            reinterpret_cast<const __nv_bfloat16*>(k_new),
+  auto* kern = g.D == 256 ? store_tokens_kernel<256> : store_tokens_kernel<128>;
+  return cudaLaunchKernelEx(&cfg, kern, g, reinterpret_cast<const __nv_bfloat16*>(k_new),
                             reinterpret_cast<const __nv_bfloat16*>(v_new), ik_new, k_scale,
                             v_scale, page_table, seqlens, k_pool, k_sf, v_pool, v_sf, ik_pool);
 }

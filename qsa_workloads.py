@@ -72,7 +72,9 @@ class Case:
         return dataclasses.replace(self, **kw)
 
 
-# The five workloads the method is measured on.
+# The workloads the method is measured on: five at head_dim 128, then one in
+# the geometry the pages tune their kernels on (24 q / 2 KV heads, head_dim
+# 256, 32-token pages, four rows per request as in an MTP-3 verify step).
 CONFIGS = [
     Case("tiny decode", seed=0, batch=1, rows_per_req=1, num_q_heads=8,
          num_kv_heads=1, page_size=64, ctx_lo=4096, ctx_hi=4096, k=16,
@@ -91,6 +93,10 @@ CONFIGS = [
          num_q_heads=32, num_kv_heads=4, page_size=64, ctx_lo=4096,
          ctx_hi=32768, k=48, window=4, max_blocks=512, pool="perm",
          invalid_frac=0.05, tie_frac=0.10),
+    Case("head_dim-256 verify", seed=5, batch=32, rows_per_req=4,
+         num_q_heads=24, num_kv_heads=2, page_size=32, ctx_lo=8192,
+         ctx_hi=16384, k=64, window=4, max_blocks=512, pool="perm",
+         head_dim=256),
 ]
 
 

@@ -67,10 +67,10 @@ def check_against_oracle(res, w_np, rows=None):
 
 
 # ---------------------------------------------------------------------------
-# the five workloads, reduced to oracle speed (several tiles + ragged tails)
+# the workloads, reduced to oracle speed (several tiles + ragged tails)
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("cfg", range(5))
+@pytest.mark.parametrize("cfg", range(len(qw.CONFIGS)))
 def test_small_configs(qsa, cfg):
     case = qw.small(qw.CONFIGS[cfg])
     w = qw.make_workload(case, "cuda")
@@ -79,7 +79,8 @@ def test_small_configs(qsa, cfg):
 
 
 @pytest.mark.parametrize("cfg,splits", [(1, 1), (1, 2), (1, 7), (1, 64), (2, 1), (2, 3),
-                                        (4, 1), (4, 5), (3, 1), (3, 16)])
+                                        (4, 1), (4, 5), (3, 1), (3, 16), (5, 1), (5, 2),
+                                        (5, 8), (5, 24)])
 def test_forced_splits(qsa, cfg, splits):
     case = qw.small(qw.CONFIGS[cfg])
     w = qw.make_workload(case, "cuda")
@@ -115,6 +116,21 @@ EDGE_CASES = {
     "cols_24_team": _case(num_q_heads=24, num_kv_heads=4, rows_per_req=4),
     "mqa_64_heads": _case(num_q_heads=64, num_kv_heads=1, rows_per_req=1, batch=2),
     "ties": _case(tie_frac=0.5, rows_per_req=2),
+    # head_dim 256 (32-token stages): decode and verify rows, 32- and 64-token
+    # pages, head groups wider than one 8-column slice, masks and tails
+    "hd256_decode_p32": _case(head_dim=256, page_size=32, max_blocks=41, k=9, window=2,
+                              num_q_heads=24, num_kv_heads=2),
+    "hd256_decode_p64": _case(head_dim=256, num_q_heads=16, num_kv_heads=2),
+    "hd256_verify2_p64": _case(head_dim=256, rows_per_req=2, num_q_heads=12, num_kv_heads=1),
+    "hd256_verify3": _case(head_dim=256, page_size=32, max_blocks=41, rows_per_req=3, k=10),
+    "hd256_verify4_g12": _case(head_dim=256, page_size=32, max_blocks=41, rows_per_req=4, k=12,
+                               num_q_heads=24, num_kv_heads=2, invalid_frac=0.2),
+    "hd256_eight_rows": _case(head_dim=256, page_size=32, max_blocks=41, rows_per_req=8,
+                              num_q_heads=4, num_kv_heads=1, k=7),
+    "hd256_ragged_tiny": _case(head_dim=256, page_size=32, rows_per_req=4, ctx_lo=1, ctx_hi=70,
+                               max_blocks=3, k=2, window=1),
+    "hd256_ties": _case(head_dim=256, page_size=32, max_blocks=41, tie_frac=0.5, rows_per_req=2,
+                        k=8),
 }
 
 
@@ -237,7 +253,7 @@ def _selection_properties(res, w_np):
         assert np.all(res["sel"][r, res["nsel"][r]:] == -1)
 
 
-@pytest.mark.parametrize("cfg", range(5))
+@pytest.mark.parametrize("cfg", range(len(qw.CONFIGS)))
 def test_full_size_sampled_rows(qsa, cfg):
     case = qw.CONFIGS[cfg]
     w = qw.make_workload(case, "cuda")
@@ -269,6 +285,8 @@ FUSED_CASES = [("cfg0", lambda: qw.small(qw.CONFIGS[0]), 0),
                ("ties", lambda: _case(tie_frac=0.5), 0),
                ("invalid", lambda: _case(invalid_frac=0.3), 0),
                ("gqa12", lambda: EDGE_CASES["gqa12_nt2"], 0),
+               ("hd256_p32", lambda: EDGE_CASES["hd256_decode_p32"], 0),
+               ("hd256_p64_split3", lambda: EDGE_CASES["hd256_decode_p64"], 3),
                ("cfg2_composed_inside", lambda: qw.small(qw.CONFIGS[2]), 0)]
 
 

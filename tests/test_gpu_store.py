@@ -42,13 +42,13 @@ def check_store(qsa, w, new):
     return got
 
 
-@pytest.mark.parametrize("cfg", range(5))
+@pytest.mark.parametrize("cfg", range(len(qw.CONFIGS)))
 def test_store_small_configs(qsa, cfg):
     w = qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cuda")
     check_store(qsa, w, qw.make_new_tokens(w))
 
 
-@pytest.mark.parametrize("cfg", [1, 4])
+@pytest.mark.parametrize("cfg", [1, 4, 5])
 def test_store_full_size(qsa, cfg):
     w = qw.make_workload(qw.CONFIGS[cfg], "cuda")
     check_store(qsa, w, qw.make_new_tokens(w))
@@ -67,6 +67,10 @@ STORE_CASES = {
     "tiny_contexts_verify": _case(rows_per_req=4, ctx_lo=1, ctx_hi=6, max_blocks=2, k=2, window=1),
     "mostly_invalid": _case(invalid_frac=0.9, rows_per_req=3),
     "eight_rows_one_kv_head": _case(rows_per_req=8, num_q_heads=4, num_kv_heads=1, k=5),
+    "hd256_p32_verify": _case(head_dim=256, page_size=32, max_blocks=41, rows_per_req=4,
+                              num_q_heads=24, num_kv_heads=2),
+    "hd256_p64_tiny": _case(head_dim=256, rows_per_req=4, ctx_lo=1, ctx_hi=6, max_blocks=2,
+                            k=2, window=1),
 }
 
 
@@ -76,19 +80,20 @@ def test_store_edge_cases(qsa, name):
     check_store(qsa, w, qw.make_new_tokens(w))
 
 
-@pytest.mark.parametrize("mult", [1e4, 1e-7, 0.0])
-def test_store_saturation_underflow_and_zeros(qsa, mult):
+@pytest.mark.parametrize("mult,cfg", [(1e4, 2), (1e-7, 2), (0.0, 2), (1e4, 5), (1e-7, 5)])
+def test_store_saturation_underflow_and_zeros(qsa, mult, cfg):
     # Values far above the tensor scale saturate the block scale (448) and
     # the codes (6); values far below it flush the block to zero.
-    w = qw.make_workload(qw.small(qw.CONFIGS[2]), "cuda")
+    w = qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cuda")
     new = qw.make_new_tokens(w)
     new["k_new"] = (new["k_new"].float() * mult).to(torch.bfloat16)
     new["v_new"] = (new["v_new"].float() * mult).to(torch.bfloat16)
     check_store(qsa, w, new)
 
 
-def test_store_then_step_matches_the_oracle(qsa):
-    w = qw.make_workload(qw.small(qw.CONFIGS[2]), "cuda")
+@pytest.mark.parametrize("cfg", [2, 5])
+def test_store_then_step_matches_the_oracle(qsa, cfg):
+    w = qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cuda")
     new = qw.make_new_tokens(w)
     got = store_gpu(qsa, w, new)
     for n in POOLS:
@@ -129,7 +134,9 @@ def restore_gpu(qsa, w, pools, rejected, saved):
 ROLLBACK_CASES = [("cfg2", lambda: qw.small(qw.CONFIGS[2])), ("cfg4", lambda: qw.small(qw.CONFIGS[4])),
                   ("tiny", lambda: STORE_CASES["tiny_contexts_verify"]),
                   ("invalid", lambda: STORE_CASES["mostly_invalid"]),
-                  ("full4", lambda: qw.CONFIGS[4])]
+                  ("full4", lambda: qw.CONFIGS[4]),
+                  ("cfg5", lambda: qw.small(qw.CONFIGS[5])),
+                  ("hd256_tiny", lambda: STORE_CASES["hd256_p64_tiny"])]
 
 
 @pytest.mark.parametrize("name,make", ROLLBACK_CASES, ids=[c[0] for c in ROLLBACK_CASES])

@@ -126,11 +126,11 @@ def test_encoder_recipe_and_error_bound():
 # A1 index scores
 # ---------------------------------------------------------------------------
 
-def _tiny_case(R=1, invalid=0.0, P=64, Hq=4, Hkv=2, B=2, lo=300, hi=333, k=4, W=1):
+def _tiny_case(R=1, invalid=0.0, P=64, Hq=4, Hkv=2, B=2, lo=300, hi=333, k=4, W=1, D=128):
     mb = -(-hi // P)
     return qw.Case("pin", seed=11, batch=B, rows_per_req=R, num_q_heads=Hq,
                    num_kv_heads=Hkv, page_size=P, ctx_lo=lo, ctx_hi=hi, k=k,
-                   window=W, max_blocks=mb, pool="perm", invalid_frac=invalid)
+                   window=W, max_blocks=mb, pool="perm", invalid_frac=invalid, head_dim=D)
 
 
 def test_index_scores_closed_form():
@@ -333,11 +333,13 @@ def _sdpa_reference(w, golden_dir):
     return out.numpy(), lse.numpy()
 
 
-@pytest.mark.parametrize("R,Hq,Hkv,P,invalid", [(1, 8, 2, 64, 0.0), (4, 4, 2, 64, 0.15),
-                                                 (2, 6, 3, 128, 0.1)])
-def test_attention_dense_when_k_covers_all(golden_dir, R, Hq, Hkv, P, invalid):
-    case = _tiny_case(R=R, invalid=invalid, P=P, Hq=Hq, Hkv=Hkv, B=2, lo=150, hi=2 * P + 70,
-                      k=16, W=2)
+@pytest.mark.parametrize("R,Hq,Hkv,P,invalid,D", [(1, 8, 2, 64, 0.0, 128), (4, 4, 2, 64, 0.15, 128),
+                                                   (2, 6, 3, 128, 0.1, 128),
+                                                   (4, 12, 1, 32, 0.1, 256), (1, 6, 2, 64, 0.0, 256)])
+def test_attention_dense_when_k_covers_all(golden_dir, R, Hq, Hkv, P, invalid, D):
+    hi = 2 * P + 70 if P >= 64 else 6 * P + 10      # several blocks, a ragged tail
+    case = _tiny_case(R=R, invalid=invalid, P=P, Hq=Hq, Hkv=Hkv, B=2, lo=150, hi=hi,
+                      k=16, W=2, D=D)
     w = qw.to_numpy(qw.make_workload(case, "cpu"))
     res = oracle.step(w)
     out_ref, lse_ref = _sdpa_reference(w, golden_dir)
@@ -501,12 +503,13 @@ def test_quantize_matches_the_generators_encoder():
                                           packed[r, 8 * blk:8 * blk + 8].numpy())
 
 
-@pytest.mark.parametrize("cfg", [2, 4])
+@pytest.mark.parametrize("cfg", [2, 4, 5])
 def test_store_kv_writes_exactly_the_new_slots(cfg):
     w = qw.to_numpy(qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cpu"))
     new = qw.to_numpy(qw.make_new_tokens(qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cpu")))
     out = oracle.store_kv(w, new)
     B, R, P, MB, Hkv = w["batch"], w["rows_per_req"], w["page_size"], w["max_blocks"], w["num_kv_heads"]
+    D = w["head_dim"]
     rows = np.zeros((w["num_pages"], Hkv, P), bool)
     keys = np.zeros((w["num_pages"], P), bool)
     for b in range(B):
@@ -523,9 +526,13 @@ def test_store_kv_writes_exactly_the_new_slots(cfg):
             for g in range(Hkv):
                 xk = new["k_new"][b * R + j, g].astype(np.uint32) << 16
                 xk = xk.view(np.float32)
-                for blk in range(8):
+                for blk in range(D // 16):
                     codes, sf = oracle.quantize_block(xk[16 * blk:16 * blk + 16], w["k_scale"])
-                    assert out["k_sf"].reshape(-1, Hkv, P, 8)[page, g, pos % P, blk] == sf
+                    assert out["k_sf"].reshape(-1, Hkv, P, D // 16)[page, g, pos % P, blk] == sf
+                    np.testing.assert_array_equal(
+                        out["k_pool"].reshape(-1, Hkv, P, D // 2)[page, g, pos % P,
+                                                                   8 * blk:8 * blk + 8],
+                        codes[0::2] | (codes[1::2] << 4))
             np.testing.assert_array_equal(out["ik_pool"].reshape(-1, P, 64)[page, pos % P],
                                           new["ik_new"][b * R + j])
     for name, mask in (("k_pool", rows), ("v_pool", rows), ("k_sf", rows), ("v_sf", rows),
@@ -545,7 +552,7 @@ def _half_rejected(T):
     return (np.arange(T) % 2 == 1).astype(np.int32)
 
 
-@pytest.mark.parametrize("cfg", [2, 4])
+@pytest.mark.parametrize("cfg", [2, 4, 5])
 def test_rollback_round_trip(cfg):
     w = qw.to_numpy(qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cpu"))
     new = qw.to_numpy(qw.make_new_tokens(qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cpu")))
@@ -567,7 +574,7 @@ def test_rollback_round_trip(cfg):
     # slots of rejected rows equal the original, those of kept rows the store
     rows_rej = np.zeros(T, bool)
     rows_rej[rej == 1] = True
-    P, R, Hkv = w["page_size"], w["rows_per_req"], w["num_kv_heads"]
+    P, R, Hkv, D = w["page_size"], w["rows_per_req"], w["num_kv_heads"], w["head_dim"]
     for r in range(T):
         b, j = divmod(r, R)
         pos = int(w["seqlens"][b]) - R + j
@@ -577,29 +584,34 @@ def test_rollback_round_trip(cfg):
         if page < 0 or page >= w["num_pages"]:
             continue
         want = w if rows_rej[r] else stored
-        kp = mixed["k_pool"].reshape(-1, Hkv, P, 64)[page, :, pos % P]
-        np.testing.assert_array_equal(kp, want["k_pool"].reshape(-1, Hkv, P, 64)[page, :, pos % P])
+        kp = mixed["k_pool"].reshape(-1, Hkv, P, D // 2)[page, :, pos % P]
+        np.testing.assert_array_equal(kp, want["k_pool"].reshape(-1, Hkv, P, D // 2)[page, :, pos % P])
         ik = mixed["ik_pool"].reshape(-1, P, 64)[page, pos % P]
         np.testing.assert_array_equal(ik, want["ik_pool"].reshape(-1, P, 64)[page, pos % P])
     assert rows_rej.any() and (~rows_rej).any()
 
 
-def test_rollback_saved_layout():
+@pytest.mark.parametrize("cfg", [2, 5])
+def test_rollback_saved_layout(cfg):
     # the saved bytes of a row are its slots' bytes in the documented order
-    w = qw.to_numpy(qw.make_workload(qw.small(qw.CONFIGS[2]), "cpu"))
+    w = qw.to_numpy(qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cpu"))
     saved = oracle.rollback_gather(w, w)
-    Hkv, P, R = w["num_kv_heads"], w["page_size"], w["rows_per_req"]
-    row_bytes = Hkv * 144 + 64
+    Hkv, P, R, D = w["num_kv_heads"], w["page_size"], w["rows_per_req"], w["head_dim"]
+    c, f = D // 2, D // 16            # code and scale bytes per token row
+    per = 2 * (c + f)
+    row_bytes = Hkv * per + 64
     b, j = 1, 2
     r = b * R + j
     pos = int(w["seqlens"][b]) - R + j
     page = int(w["page_table"][b, pos // P])
     s = saved[r * row_bytes:(r + 1) * row_bytes]
     for g in range(Hkv):
-        part = s[g * 144:(g + 1) * 144]
-        np.testing.assert_array_equal(part[:64], w["k_pool"].reshape(-1, Hkv, P, 64)[page, g, pos % P])
-        np.testing.assert_array_equal(part[64:72], w["k_sf"].reshape(-1, Hkv, P, 8)[page, g, pos % P])
-        np.testing.assert_array_equal(part[72:136], w["v_pool"].reshape(-1, Hkv, P, 64)[page, g, pos % P])
-        np.testing.assert_array_equal(part[136:144], w["v_sf"].reshape(-1, Hkv, P, 8)[page, g, pos % P])
-    np.testing.assert_array_equal(s[Hkv * 144:].view(np.int8),
+        part = s[g * per:(g + 1) * per]
+        np.testing.assert_array_equal(part[:c], w["k_pool"].reshape(-1, Hkv, P, c)[page, g, pos % P])
+        np.testing.assert_array_equal(part[c:c + f], w["k_sf"].reshape(-1, Hkv, P, f)[page, g, pos % P])
+        np.testing.assert_array_equal(part[c + f:2 * c + f],
+                                      w["v_pool"].reshape(-1, Hkv, P, c)[page, g, pos % P])
+        np.testing.assert_array_equal(part[2 * c + f:per],
+                                      w["v_sf"].reshape(-1, Hkv, P, f)[page, g, pos % P])
+    np.testing.assert_array_equal(s[Hkv * per:].view(np.int8),
                                   w["ik_pool"].reshape(-1, P, 64)[page, pos % P])
