@@ -116,6 +116,9 @@ EDGE_CASES = {
     "cols_24_team": _case(num_q_heads=24, num_kv_heads=4, rows_per_req=4),
     "mqa_64_heads": _case(num_q_heads=64, num_kv_heads=1, rows_per_req=1, batch=2),
     "ties": _case(tie_frac=0.5, rows_per_req=2),
+    # page-table rows far wider than the requests' blocks
+    "wide_table": _case(max_blocks=2100, rows_per_req=2, tie_frac=0.3),
+    "wide_table_verify4": _case(max_blocks=2049, rows_per_req=4, k=9),
     # head_dim 256 (32-token stages): decode and verify rows, 32- and 64-token
     # pages, head groups wider than one 8-column slice, masks and tails
     "hd256_decode_p32": _case(head_dim=256, page_size=32, max_blocks=41, k=9, window=2,
