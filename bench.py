@@ -77,6 +77,18 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def measured_tensor_peak():
+    """Dense 16-bit tensor throughput (TFLOP/s): the measured bf16 burst figure
+    (fp16 inputs with fp32 accumulation run at the same rate)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
 def workload_label(case: qw.Case) -> str:
     ctx = (str(case.ctx_lo) if case.ctx_lo == case.ctx_hi
            else "U[%d,%d]" % (case.ctx_lo, case.ctx_hi))
@@ -104,7 +116,13 @@ def algorithmic_bytes(w: dict, sel: np.ndarray) -> dict:
     key_tokens = 0
     page_tokens = 0
     union_entries = 0
+    att_tokens = 0          # (row, selected visible token) pairs: the attention's work
     for b in range(B):
+        for j in range(R):
+            n = max(0, min(int(sl[b]) - R + 1 + j, MB * P))
+            for beta in sel[b * R + j]:
+                if beta >= 0 and 0 <= pt[b, beta] < w["num_pages"]:
+                    att_tokens += max(0, min(P, n - int(beta) * P))
         n_last = max(0, min(int(sl[b]), MB * P))          # row R-1 sees L tokens
         nb = -(-n_last // P)
         for beta in range(nb):
@@ -119,7 +137,8 @@ def algorithmic_bytes(w: dict, sel: np.ndarray) -> dict:
     idx = key_tokens * Di + T * Hq * Di + B * MB * 4 + B * 4
     dec = page_tokens * Hkv * (D // 2 + D // 16) * 2 + 2 * T * Hq * D * 2 + T * Hq * 4 \
         + union_entries * 4
-    return dict(index_scores=idx, select_topk=0, sparse_decode=dec, step=idx + dec,
+    return dict(index_scores=idx, select_topk=0, sparse_decode=dec, sparse_prefill=dec,
+                step=idx + dec, flops=4.0 * D * Hq * att_tokens,
                 key_bytes=key_tokens * Di, page_bytes=page_tokens * Hkv * (D // 2 + D // 16) * 2,
                 touched=idx + dec + T * MB * 4 * 2 + T * w["k"] * 4 * 2)
 
@@ -454,6 +473,7 @@ def run_qsa(args, case):
     # When the step runs selection and attention as one launch (DecodeStep
     # fused), sparse_decode below times that fused kernel.
     fused = step.fused and qsa.qsa_select_sparse_decode_fused(step.cg)
+    att = "sparse_prefill" if step.prefill else "sparse_decode"
     kern_ms = {}
     evs = make_events(6 * nrep)
     if evs is not None:
@@ -472,7 +492,13 @@ def run_qsa(args, case):
                                             step.window, step.sel, step.nsel, stream)
                     e[3].record(stream)
                     e[4].record(stream)
-                    if fused:
+                    if step.prefill:
+                        qsa.qsa_sparse_prefill(step.cg, w["q"], w["k_pool"], w["k_sf"],
+                                               w["v_pool"], w["v_sf"], w["k_scale"],
+                                               w["v_scale"], w["sm_scale"], w["page_table"],
+                                               w["seqlens"], step.sel, step.k, step.out,
+                                               step.lse, step.workspace, stream)
+                    elif fused:
                         qsa.qsa_select_sparse_decode(
                             step.cg, step.scores, step.window, w["q"], w["k_pool"], w["k_sf"],
                             w["v_pool"], w["v_sf"], w["k_scale"], w["v_scale"], w["sm_scale"],
@@ -486,7 +512,7 @@ def run_qsa(args, case):
                                                  step.lse, step.workspace, step.num_splits,
                                                  stream)
                     e[5].record(stream)
-            acc = {"index_scores": [], "select_topk": [], "sparse_decode": []}
+            acc = {"index_scores": [], "select_topk": [], att: []}
             for _ in range(5):
                 kg.replay()
                 stream.synchronize()
@@ -494,7 +520,7 @@ def run_qsa(args, case):
                     e = evs[6 * i: 6 * i + 6]
                     acc["index_scores"].append(e[0].elapsed_time(e[1]))
                     acc["select_topk"].append(e[2].elapsed_time(e[3]))
-                    acc["sparse_decode"].append(e[4].elapsed_time(e[5]))
+                    acc[att].append(e[4].elapsed_time(e[5]))
         kern_ms = {k: float(np.mean(v)) for k, v in acc.items()}
         if fused:
             kern_ms.pop("select_topk")
@@ -504,7 +530,8 @@ def run_qsa(args, case):
 
     # ---- decode prologue (store the step's new tokens), after every other
     # measurement because it writes into the replicas' caches ---------------
-    rollback = time_rollback(qsa, step, reps, stream, nrep)
+    rollback = (time_rollback(qsa, step, reps, stream, nrep) if not step.prefill else
+                {"skipped": "context row groups are not speculative rows"})
     prologue = time_prologue(qsa, step, reps, stream, nrep)
 
     # ---- CPU baseline (rank 0, N = 1 only) -----------------------------------
@@ -528,11 +555,27 @@ def run_qsa(args, case):
                          "gbs": (b / (t / 1000.0) / 1e9) if (t > 0 and b > 0) else None}
     if fused:
         kernels["select_topk"] = {"ms": None, "fused_into": "sparse_decode"}
-    dom = max(kern_ms, key=kern_ms.get) if kern_ms else "sparse_decode"
+    dom = max(kern_ms, key=kern_ms.get) if kern_ms else att
     dom_t = kern_ms.get(dom)
-    achieved = (mean[dom] / (dom_t / 1000.0) / 1e9) if dom_t else None
     wl = "cfg%d" % args.config
     traffic = traffic_record("qsa_" + dom, wl)
+    if dom == "sparse_prefill":
+        # A contraction: useful FLOPs (4 * D per (row, head, attended token))
+        # against the measured dense 16-bit tensor throughput.
+        tpeak, tkind = measured_tensor_peak()
+        achieved = (mean["flops"] / (dom_t / 1000.0) / 1e12) if dom_t else None
+        roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tpeak,
+                    "unit": "TFLOP/s", "frac": (achieved / tpeak) if achieved else None,
+                    "traffic": traffic, "peak_kind": tkind,
+                    "algorithmic_flops_per_launch": mean["flops"],
+                    "algorithmic_bytes_per_launch": mean[dom],
+                    "hbm_gbs": (mean[dom] / (dom_t / 1000.0) / 1e9) if dom_t else None}
+    else:
+        achieved = (mean[dom] / (dom_t / 1000.0) / 1e9) if dom_t else None
+        roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak_gbs,
+                    "unit": "GB/s", "frac": (achieved / peak_gbs) if achieved else None,
+                    "traffic": traffic, "peak_kind": peak_kind,
+                    "algorithmic_bytes_per_launch": mean[dom]}
     line = {
         "metric": METRIC, "value": rows_s, "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -547,10 +590,7 @@ def run_qsa(args, case):
                    "stream" % nrep},
         "step_hbm": {"bytes": mean["step"], "achieved_gbs": step_gbs, "peak_gbs": peak_gbs,
                      "frac": step_gbs / peak_gbs, "peak_kind": peak_kind},
-        "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak_gbs,
-                     "unit": "GB/s", "frac": (achieved / peak_gbs) if achieved else None,
-                     "traffic": traffic, "peak_kind": peak_kind,
-                     "algorithmic_bytes_per_launch": mean[dom]},
+        "roofline": roofline,
         "kernels": kernels,
         "clocks": clocks,
         "e2e": e2e,

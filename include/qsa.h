@@ -72,7 +72,10 @@ typedef enum {
 
 typedef struct {
     int batch;          /* B                                    */
-    int rows_per_req;   /* R = 1 + draft rows, 1..8             */
+    int rows_per_req;   /* R = 1 + draft rows, 1..8; up to 4096
+                           (a context row group) for the index
+                           scores, the selection, the prologue
+                           and qsa_sparse_prefill             */
     int num_q_heads;    /* Hq, 1..256                           */
     int num_kv_heads;   /* Hkv, divides Hq                      */
     int head_dim;       /* D, 128 or 256                        */
@@ -337,6 +340,45 @@ qsa_status_t qsa_rollback_restore(const qsa_geom_t *geom, const int32_t *page_ta
                                   const void *saved, uint8_t *k_pool, uint8_t *k_sf,
                                   uint8_t *v_pool, uint8_t *v_sf, int8_t *ik_pool,
                                   cudaStream_t stream);
+
+/*
+ * Context (prefill) row groups: row-tile sparse GQA on the tensor cores.
+ * TensorRT-LLM PR #20276 ("Qwen3.8-Flash-Next NVFP4 target"), Performance
+ * (what runs on the fast paths): context steps run a row-tile sparse GQA on
+ * tcgen05 that reads K/V tiles once per group of rows of one request; Known
+ * limitations: context rows read the NVFP4 pages dequantised to bf16 through
+ * the row-tile pass.  PR #20937, What changes: the page conversion and the
+ * row-tile planning.
+ *
+ * Same arguments, layouts and result as qsa_sparse_decode (out = softmax
+ * attention of every row and head over the tokens of the blocks its row
+ * selected that it sees; lse the natural log of the softmax sum, -inf and
+ * out = 0 for a row with no such token), for rows_per_req up to 4096: the
+ * rows of a request are taken in tiles of floor(128 / G) consecutive rows
+ * (the 128 query vectors of one tensor-core tile), each tile reading the
+ * union of its rows' selected pages once.  The pages are dequantised on chip
+ * to fp16 (e2m1 x e4m3 is exact; the per-tensor scales are applied in fp32),
+ * so no converted copy of the cache is written.
+ *
+ *   workspace   >= qsa_sparse_prefill_workspace_bytes() bytes (its status
+ *               word), 256-byte aligned, zero-filled once by
+ *               qsa_workspace_init().
+ *
+ * Returns QSA_ERR_UNSUPPORTED for head_dim != 128, more than 128 query heads
+ * per KV head, or a tile (floor(128 / G) rows x k selections plus their union)
+ * beyond one CTA's shared memory; QSA_ERR_INVALID_ARG for null pointers, k <
+ * 1, pools / scales / q / out not 16-byte aligned; QSA_ERR_WORKSPACE for a
+ * missing, short or misaligned workspace.  A bounded device wait that gives
+ * up is reported through qsa_workspace_status().
+ */
+size_t qsa_sparse_prefill_workspace_bytes(const qsa_geom_t *geom, int k);
+qsa_status_t qsa_sparse_prefill(const qsa_geom_t *geom, const void *q_bf16,
+                                const uint8_t *k_pool, const uint8_t *k_sf,
+                                const uint8_t *v_pool, const uint8_t *v_sf, float k_scale,
+                                float v_scale, float sm_scale, const int32_t *page_table,
+                                const int32_t *seqlens, const int32_t *sel, int k,
+                                void *out_bf16, float *lse, void *workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Reads the workspace's device status word (synchronising `stream`): 0 when

@@ -17,6 +17,7 @@ from .binding import (EXPORTS, QsaError, load, make_geom, qsa_geom_t, qsa_index_
                       qsa_select_topk, qsa_sparse_decode, qsa_sparse_decode_ex, qsa_sparse_decode_noalloc,
                       qsa_sparse_decode_workspace_bytes, qsa_sparse_decode_workspace_bytes_ex,
                       qsa_rollback_gather, qsa_rollback_restore, qsa_rollback_state_bytes,
+                      qsa_sparse_prefill, qsa_sparse_prefill_workspace_bytes,
                       qsa_status_string, qsa_store_kv_tokens, qsa_workspace_init,
                       qsa_workspace_status)
 
@@ -26,9 +27,14 @@ __all__ = [
     "qsa_select_topk", "qsa_sparse_decode", "qsa_sparse_decode_ex", "qsa_sparse_decode_noalloc",
     "qsa_sparse_decode_workspace_bytes", "qsa_sparse_decode_workspace_bytes_ex",
     "qsa_rollback_gather", "qsa_rollback_restore", "qsa_rollback_state_bytes",
+    "qsa_sparse_prefill", "qsa_sparse_prefill_workspace_bytes",
     "qsa_status_string", "qsa_store_kv_tokens", "qsa_workspace_init", "qsa_workspace_status",
-    "DecodeStep",
+    "DecodeStep", "MAX_DECODE_ROWS",
 ]
+
+# Rows per request the decode / verify attention takes; longer row groups
+# (context chunks) go to the row-tile path, qsa_sparse_prefill.
+MAX_DECODE_ROWS = 8
 
 GEOM_FIELDS = [n for n, _ in qsa_geom_t._fields_]
 
@@ -39,7 +45,8 @@ class DecodeStep:
     chained by programmatic dependent launch.  ``fused`` runs selection and
     decode through qsa_select_sparse_decode instead (one launch for decode
     rows; bit-identical results).  ``num_splits`` = 0 lets the library choose
-    the KV split count."""
+    the KV split count.  A geometry with more than MAX_DECODE_ROWS rows per
+    request (a context row group) runs qsa_sparse_prefill as its attention."""
 
     def __init__(self, geom: dict, k: int, window: int, device="cuda", num_splits: int = 0,
                  fused: bool = False):
@@ -60,7 +67,11 @@ class DecodeStep:
         self.results = torch.empty((lse_off + T * Hq * 4,), dtype=torch.uint8, device=dev)
         self.out = self.results[:out_bytes].view(torch.bfloat16).view(T, Hq, D)
         self.lse = self.results[lse_off:].view(torch.float32).view(T, Hq)
-        nbytes = qsa_sparse_decode_workspace_bytes_ex(self.cg, self.k, self.num_splits)
+        self.prefill = self.geom["rows_per_req"] > MAX_DECODE_ROWS
+        if self.prefill:
+            nbytes = qsa_sparse_prefill_workspace_bytes(self.cg, self.k)
+        else:
+            nbytes = qsa_sparse_decode_workspace_bytes_ex(self.cg, self.k, self.num_splits)
         if nbytes == 0:
             raise QsaError("qsa_sparse_decode_workspace_bytes", 1, "invalid geometry")
         self.workspace = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
@@ -71,7 +82,13 @@ class DecodeStep:
         sm = float(w["sm_scale"]) if sm_scale is None else float(sm_scale)
         qsa_index_scores(self.cg, w["iq"], w["ik_pool"], w["page_table"], w["seqlens"],
                          self.scores, stream)
-        if not self.fused:
+        if self.prefill:
+            qsa_select_topk(self.cg, self.scores, w["seqlens"], self.k, self.window, self.sel,
+                            self.nsel, stream)
+            qsa_sparse_prefill(self.cg, w["q"], w["k_pool"], w["k_sf"], w["v_pool"], w["v_sf"],
+                               w["k_scale"], w["v_scale"], sm, w["page_table"], w["seqlens"],
+                               self.sel, self.k, self.out, self.lse, self.workspace, stream)
+        elif not self.fused:
             qsa_select_topk(self.cg, self.scores, w["seqlens"], self.k, self.window, self.sel,
                             self.nsel, stream)
             qsa_sparse_decode_ex(self.cg, w["q"], w["k_pool"], w["k_sf"], w["v_pool"],

@@ -38,6 +38,8 @@ EXPORTS = (
     "qsa_rollback_state_bytes",
     "qsa_rollback_gather",
     "qsa_rollback_restore",
+    "qsa_sparse_prefill_workspace_bytes",
+    "qsa_sparse_prefill",
 )
 
 
@@ -113,6 +115,10 @@ def load(build_if_missing: bool = False):
     lib.qsa_rollback_gather.argtypes = [G] + [_vp] * 9
     lib.qsa_rollback_restore.restype = st
     lib.qsa_rollback_restore.argtypes = [G] + [_vp] * 10
+    lib.qsa_sparse_prefill_workspace_bytes.restype = ctypes.c_size_t
+    lib.qsa_sparse_prefill_workspace_bytes.argtypes = [G, ctypes.c_int]
+    lib.qsa_sparse_prefill.restype = st
+    lib.qsa_sparse_prefill.argtypes = dec + [_vp]
     lib.qsa_workspace_status.restype = st
     lib.qsa_workspace_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int), _vp]
     _lib = lib
@@ -270,6 +276,18 @@ def qsa_sparse_decode_ex(geom, q, k_pool, k_sf, v_pool, v_sf, k_scale, v_scale, 
                             page_table, seqlens, sel, k, out, lse, workspace)
     _check("qsa_sparse_decode_ex",
            load().qsa_sparse_decode_ex(*args, int(num_splits), _stream(stream)))
+
+
+def qsa_sparse_prefill_workspace_bytes(geom, k) -> int:
+    g = _geom(geom)
+    return int(load().qsa_sparse_prefill_workspace_bytes(ctypes.byref(g), int(k)))
+
+
+def qsa_sparse_prefill(geom, q, k_pool, k_sf, v_pool, v_sf, k_scale, v_scale, sm_scale,
+                       page_table, seqlens, sel, k, out, lse, workspace, stream=None):
+    args, _g = _decode_args(geom, q, k_pool, k_sf, v_pool, v_sf, k_scale, v_scale, sm_scale,
+                            page_table, seqlens, sel, k, out, lse, workspace)
+    _check("qsa_sparse_prefill", load().qsa_sparse_prefill(*args, _stream(stream)))
 
 
 def qsa_sparse_decode_noalloc(geom, q, k_pool, k_sf, v_pool, v_sf, k_scale, v_scale, sm_scale,

@@ -18,7 +18,10 @@ using qsa::Geom;
 
 bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
-qsa_status_t check_geom(const qsa_geom_t* g) {
+// max_rows: 8 for the decode / verify attention and the rollback; the index
+// scores, the selection, the prologue and the context row-tile attention also
+// take long context row groups.
+qsa_status_t check_geom(const qsa_geom_t* g, int max_rows = qsa::kMaxRows) {
   if (!g) return QSA_ERR_INVALID_ARG;
   if (g->batch < 1 || g->batch > 65535) return QSA_ERR_INVALID_ARG;
   if (g->rows_per_req < 1) return QSA_ERR_INVALID_ARG;
@@ -36,7 +39,7 @@ qsa_status_t check_geom(const qsa_geom_t* g) {
   } else {
     return QSA_ERR_UNSUPPORTED;
   }
-  if (g->rows_per_req > qsa::kMaxRows) return QSA_ERR_UNSUPPORTED;
+  if (g->rows_per_req > max_rows) return QSA_ERR_UNSUPPORTED;
   if (g->num_q_heads > qsa::kMaxQHeads) return QSA_ERR_UNSUPPORTED;
   if (g->max_blocks > qsa::kMaxBlocks) return QSA_ERR_UNSUPPORTED;
   if ((long long)g->batch * g->rows_per_req > (1LL << 24)) return QSA_ERR_UNSUPPORTED;
@@ -111,7 +114,7 @@ qsa_status_t qsa_store_kv_tokens(const qsa_geom_t* geom, const void* k_new_bf16,
                                  const int32_t* seqlens, uint8_t* k_pool, uint8_t* k_sf,
                                  uint8_t* v_pool, uint8_t* v_sf, int8_t* ik_pool,
                                  cudaStream_t stream) {
-  qsa_status_t st = check_geom(geom);
+  qsa_status_t st = check_geom(geom, qsa::kMaxContextRows);
   if (st != QSA_OK) return st;
   if (!k_new_bf16 || !v_new_bf16 || !ik_new || !page_table || !seqlens || !k_pool || !k_sf ||
       !v_pool || !v_sf || !ik_pool)
@@ -178,7 +181,7 @@ qsa_status_t qsa_rollback_restore(const qsa_geom_t* geom, const int32_t* page_ta
 qsa_status_t qsa_index_scores(const qsa_geom_t* geom, const int8_t* iq, const int8_t* ik_pool,
                               const int32_t* page_table, const int32_t* seqlens,
                               int32_t* scores, cudaStream_t stream) {
-  qsa_status_t st = check_geom(geom);
+  qsa_status_t st = check_geom(geom, qsa::kMaxContextRows);
   if (st != QSA_OK) return st;
   if (!iq || !ik_pool || !page_table || !seqlens || !scores) return QSA_ERR_INVALID_ARG;
   if (!aligned(ik_pool, 16)) return QSA_ERR_INVALID_ARG;
@@ -191,7 +194,7 @@ qsa_status_t qsa_index_scores(const qsa_geom_t* geom, const int8_t* iq, const in
 qsa_status_t qsa_select_topk(const qsa_geom_t* geom, const int32_t* scores,
                              const int32_t* seqlens, int k, int window, int32_t* sel,
                              int32_t* nsel, cudaStream_t stream) {
-  qsa_status_t st = check_geom(geom);
+  qsa_status_t st = check_geom(geom, qsa::kMaxContextRows);
   if (st != QSA_OK) return st;
   if (!scores || !seqlens || !sel || !nsel) return QSA_ERR_INVALID_ARG;
   if (k < 1 || window < 0 || window > k) return QSA_ERR_INVALID_ARG;
@@ -241,6 +244,47 @@ qsa_status_t qsa_sparse_decode_ex(const qsa_geom_t* geom, const void* q_bf16,
   return from_cuda(qsa::launch_sparse_decode(g, plan, q_bf16, k_pool, k_sf, v_pool, v_sf, k_scale,
                                              v_scale, sm_scale, page_table, seqlens, sel, k,
                                              out_bf16, lse, workspace, true, stream));
+}
+
+// Context row groups: head_dim 128, a head group of at most 128 heads, and a
+// tile's selections + union within the CTA's shared memory.
+qsa_status_t check_prefill_args(const qsa_geom_t* geom, int k) {
+  qsa_status_t st = check_geom(geom, qsa::kMaxContextRows);
+  if (st != QSA_OK) return st;
+  if (k < 1) return QSA_ERR_INVALID_ARG;
+  if (k > qsa::kMaxK || geom->head_dim != 128) return QSA_ERR_UNSUPPORTED;
+  const Geom g = to_geom(geom);
+  if (qsa::prefill_rows_per_tile(g) < 1) return QSA_ERR_UNSUPPORTED;
+  if (qsa::prefill_smem_bytes(g, k) > 227 * 1024) return QSA_ERR_UNSUPPORTED;
+  return QSA_OK;
+}
+
+size_t qsa_sparse_prefill_workspace_bytes(const qsa_geom_t* geom, int k) {
+  return check_prefill_args(geom, k) == QSA_OK ? 256 : 0;
+}
+
+qsa_status_t qsa_sparse_prefill(const qsa_geom_t* geom, const void* q_bf16,
+                                const uint8_t* k_pool, const uint8_t* k_sf,
+                                const uint8_t* v_pool, const uint8_t* v_sf, float k_scale,
+                                float v_scale, float sm_scale, const int32_t* page_table,
+                                const int32_t* seqlens, const int32_t* sel, int k,
+                                void* out_bf16, float* lse, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
+  qsa_status_t st = check_prefill_args(geom, k);
+  if (st != QSA_OK) return st;
+  if (!q_bf16 || !k_pool || !k_sf || !v_pool || !v_sf || !page_table || !seqlens || !sel ||
+      !out_bf16 || !lse)
+    return QSA_ERR_INVALID_ARG;
+  if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(k_sf, 16) || !aligned(v_sf, 16) ||
+      !aligned(q_bf16, 16) || !aligned(out_bf16, 16))
+    return QSA_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < 256 || !aligned(workspace, 256)) return QSA_ERR_WORKSPACE;
+  st = check_device();
+  if (st != QSA_OK) return st;
+  return from_cuda(qsa::launch_sparse_prefill(to_geom(geom), q_bf16, k_pool, k_sf, v_pool, v_sf,
+                                              k_scale, v_scale, sm_scale, page_table, seqlens,
+                                              sel, k, out_bf16, lse,
+                                              reinterpret_cast<int*>(workspace), stream));
 }
 
 int qsa_select_sparse_decode_fused(const qsa_geom_t* geom) {

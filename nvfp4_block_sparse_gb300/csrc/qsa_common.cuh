@@ -15,6 +15,7 @@ namespace qsa {
 
 constexpr int kIndexDim = 64;
 constexpr int kMaxRows = 8;           // rows per request (1 + drafts)
+constexpr int kMaxContextRows = 4096; // rows per request of a context (prefill) row group
 constexpr int kMaxQHeads = 256;
 constexpr int kMaxK = 1024;
 constexpr int kMaxUnion = 2048;       // R * k bound for the decode union
@@ -212,6 +213,17 @@ struct DecodePlan {
 
 DecodePlan plan_sparse_decode(const Geom& g, int k, int num_splits);
 bool decode_can_fuse_select(const Geom& g);
+
+// Context row groups (qsa_sparse_prefill): rows per 128-vector tile, dynamic
+// shared memory of a CTA, and the launch.
+int prefill_rows_per_tile(const Geom& g);
+size_t prefill_smem_bytes(const Geom& g, int k);
+cudaError_t launch_sparse_prefill(const Geom& g, const void* q, const uint8_t* k_pool,
+                                  const uint8_t* k_sf, const uint8_t* v_pool, const uint8_t* v_sf,
+                                  float k_scale, float v_scale, float sm_scale,
+                                  const int32_t* page_table, const int32_t* seqlens,
+                                  const int32_t* sel, int k, void* out, float* lse,
+                                  int* status, cudaStream_t stream);
 
 cudaError_t launch_sparse_decode(const Geom& g, const DecodePlan& plan, const void* q,
                                  const uint8_t* k_pool, const uint8_t* k_sf,

@@ -29,9 +29,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
-#ifndef QSA_INDEX_MMA
-#define QSA_INDEX_MMA 1
-#endif
 
 __device__ __forceinline__ int4 ld_stream_v4(const int4* p) {
   int4 v;
@@ -208,7 +205,8 @@ index_scores_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __restr
 // become fp16 by one byte permute against 0x64 (1024 + (x + 128)) and one
 // subtraction of 1152.  Dims are taken in the order each lane holds them
 // (lane part tig: dims 16*tig..16*tig+15, k-step kk: 4 of them), the same on
-// both operands, so the contraction is unchanged.
+// both operands, so the contraction is unchanged.  Requests with more than 8
+// rows (context row groups) take one CTA row per group of 8 rows (grid z).
 
 __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
   uint32_t r;
@@ -235,6 +233,7 @@ index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __r
   __shared__ __half wsplit[2][RB][kIndexDim];   // a, b
 
   const int b = blockIdx.y;
+  const int r0 = blockIdx.z * RB;              // first row of this CTA's group
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
@@ -244,7 +243,7 @@ index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __r
 
   const int L = seqlens[b];
   const int cap = g.MB * P;
-  const int nmax = visible_tokens(L, R, R - 1, cap);
+  const int nmax = visible_tokens(L, R, min(R - 1, r0 + RB - 1), cap);
 
   auto block_of = [&](int it, int& beta, int& page) -> bool {
     beta = (blockIdx.x * blocks_per_warp + it) * kWarps + warp;
@@ -271,8 +270,8 @@ index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __r
     const int j = (idx / kIndexDim) % RB;
     const int d = idx % kIndexDim;
     int s = 0;
-    if (j < R) {
-      const int8_t* src = iq + ((size_t)(b * R + j) * g.Hq) * kIndexDim + d;
+    if (r0 + j < R) {
+      const int8_t* src = iq + ((size_t)((size_t)b * R + r0 + j) * g.Hq) * kIndexDim + d;
       int h = hg;
       for (; h + 28 < g.Hq; h += 32) {
         int v[8];
@@ -307,11 +306,11 @@ index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __r
       bw[q][kk][0] = *reinterpret_cast<const uint32_t*>(src);
       bw[q][kk][1] = *reinterpret_cast<const uint32_t*>(src + 2);
     }
-  // This lane's two columns (rows 2*tig, 2*tig + 1).
+  // This lane's two columns (rows r0 + 2*tig, r0 + 2*tig + 1).
   int ncol[2];
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
-    const int j = 2 * tig + e;
+    const int j = r0 + 2 * tig + e;
     ncol[e] = (j < R) ? visible_tokens(L, R, j, cap) : 0;
   }
 
@@ -330,9 +329,9 @@ index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __r
     } else if (it + 1 < blocks_per_warp) {
       live_n = block_of(it + 1, beta_n, page_n);
     }
-    int32_t* dst = scores + (size_t)b * R * g.MB + beta;
+    int32_t* dst = scores + ((size_t)b * R + r0) * g.MB + beta;
     if (!live) {
-      if (lane < R) dst[(size_t)lane * g.MB] = kSentinel;
+      if (lane < RB && r0 + lane < R) dst[(size_t)lane * g.MB] = kSentinel;
     } else {
       int best[2] = {kSentinel, kSentinel};
 #pragma unroll
@@ -365,7 +364,7 @@ index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __r
         v = max(v, __shfl_xor_sync(0xffffffffu, v, 8));
         v = max(v, __shfl_xor_sync(0xffffffffu, v, 16));
         const int j = 2 * tig + e;
-        if (gid == 0 && j < R) dst[(size_t)j * g.MB] = (beta * P < ncol[e]) ? v : kSentinel;
+        if (gid == 0 && r0 + j < R) dst[(size_t)j * g.MB] = (beta * P < ncol[e]) ? v : kSentinel;
       }
     }
     beta = beta_n;
@@ -430,7 +429,7 @@ cudaError_t launch_mma_t(const Geom& g, const int8_t* iq, const int8_t* ik_pool,
                          const int32_t* page_table, const int32_t* seqlens, int32_t* scores,
                          bool pdl, cudaStream_t stream) {
   const int bpw = blocks_per_warp_for(g);
-  dim3 grid((g.MB + kWarps * bpw - 1) / (kWarps * bpw), g.B);
+  dim3 grid((g.MB + kWarps * bpw - 1) / (kWarps * bpw), g.B, (g.R + kMaxRows - 1) / kMaxRows);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);
@@ -449,17 +448,13 @@ template <int P>
 cudaError_t launch_p(const Geom& g, const int8_t* iq, const int8_t* ik_pool,
                      const int32_t* page_table, const int32_t* seqlens, int32_t* scores,
                      bool pdl, cudaStream_t stream) {
-#if QSA_INDEX_MMA
+  // Decode rows: int16 x int8 dp2a.  Two rows and more: the tensor cores.
   if (g.R >= 2) {
     if (blocks_per_warp_for(g) > 1)
       return launch_mma_t<P, true>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
     return launch_mma_t<P, false>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
   }
-#endif
-  if (g.R <= 1) return launch_rb<P, 1>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
-  if (g.R <= 2) return launch_rb<P, 2>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
-  if (g.R <= 4) return launch_rb<P, 4>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
-  return launch_rb<P, 8>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
+  return launch_rb<P, 1>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
 }
 
 }  // namespace

@@ -1,0 +1,620 @@
+// qsa_sparse_prefill.cu -- context (prefill) rows: row-tile sparse GQA on the
+// fifth-generation tensor cores (tcgen05, accumulators in tensor memory).
+//
+// TensorRT-LLM PR #20276 ("Qwen3.8-Flash-Next NVFP4 target"), Performance /
+// what runs on the fast paths: context and mixed steps run a row-tile sparse
+// GQA on tcgen05 whose K/V tiles are read once per group of rows of one
+// request; Known limitations: the context rows read NVFP4 pages dequantised
+// to bf16 through the row-tile pass.  PR #20937 ("GB300 perf work on
+// qwen3_8_flash_next_nvfp4__sm_103__tp1"), What changes: the NVFP4 page
+// conversion and the row-tile planning and scheduling.
+//
+// One CTA = (request b, KV head g, row tile): TR = floor(128 / G) consecutive
+// rows of the request, whose TR*G query vectors (row j, head h) are the 128
+// rows of the MMA tile (padding rows are zero and never stored).  The tile
+// visits the union of its rows' selected blocks in 64-token chunks; every
+// query vector takes the logits of a chunk only if its row selected the
+// block and only for tokens it sees (causal, n_j = L - R + 1 + j).
+//
+// Per chunk (one pipeline step; the NVFP4 bytes of the next chunk are in
+// flight on the bulk-copy engine meanwhile):
+//   1. dequantise K (64 tokens x 128 dims) and V^T (128 dims x 64 tokens)
+//      from the staged NVFP4 bytes into fp16 tiles in shared memory, K-major
+//      with the 128-byte swizzle; e2m1 x e4m3 is exact in fp16 and the
+//      per-tensor scales are applied in fp32 outside the MMAs, so the tiles
+//      hold the cache's values exactly (the page conversion, on chip);
+//   2. S = Q . K^T     tcgen05.mma kind::f16, M = 128, N = 64, K = 128,
+//                      fp32 accumulator in tensor memory;
+//   3. each thread owns one query vector (one tensor-memory lane): masks,
+//      log2-domain online softmax with a lazy rescale (the running base only
+//      moves when the maximum grows by more than 2^8; O and l are then
+//      rescaled), P = exp2(z - base) as fp16 into a swizzled P tile;
+//   4. O += P . V      tcgen05.mma kind::f16, M = 128, N = 128, K = 64.
+// After the last chunk every thread reads its O row from tensor memory,
+// divides by l, applies the V tensor scale and writes out (bf16) and lse.
+//
+// Queries enter as fp16 pre-scaled by a power of two per vector (|q|max in
+// [256, 512)); the scale is undone in fp32 with the logit scale.  Every wait
+// is bounded (2 s); a wait that gives up records a status word in the
+// workspace, lets the copies and MMAs in flight finish and frees tensor memory.
+#include "qsa_common.cuh"
+
+namespace qsa {
+namespace {
+
+constexpr int kD = 128;                 // head dim
+constexpr int kTok = 64;                // tokens per chunk
+constexpr int kThreads = 128;           // four warps: one thread per tile row
+constexpr int kStage = 2 * kTok * kD / 2 + 2 * kTok * kD / 16;   // 9216 B of NVFP4
+constexpr int kQBytes = 128 * kD * 2;   // Q tile, fp16: two 64-dim halves of 16 KB
+constexpr int kKBytes = kTok * kD * 2;  // K tile: two halves of 8 KB
+constexpr int kVBytes = kD * kTok * 2;  // V^T tile: 128 rows of 128 B
+constexpr int kPBytes = 128 * kTok * 2; // P tile: 128 rows of 128 B
+constexpr uint32_t kTmemCols = 256;     // S: columns [0, 64), O: [64, 192)
+constexpr uint32_t kOCol = 64;
+constexpr unsigned long long kWaitNs = 2000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleGap = 8.f;      // log2 units the base may trail the maximum
+
+struct Params {
+  Geom g;
+  const __nv_bfloat16* q;
+  const uint8_t* k_pool;
+  const uint8_t* k_sf;
+  const uint8_t* v_pool;
+  const uint8_t* v_sf;
+  float k_scale, v_scale, sm_scale;
+  const int32_t* page_table;
+  const int32_t* seqlens;
+  const int32_t* sel;
+  int k;
+  int tr;                 // rows per tile
+  int ucap;               // union capacity (blocks)
+  __nv_bfloat16* out;
+  float* lse;
+  int* status;
+};
+
+// Byte offset of (row r, element e) of a K-major fp16 tile whose rows are 64
+// elements (128 B), in 8-row atoms of 1024 B with the 128-byte swizzle (the
+// 16-byte chunk index is xor-ed with the row within the atom).
+__host__ __device__ __forceinline__ int sw128(int r, int chunk16) {
+  return (r >> 3) * 1024 + (r & 7) * 128 + ((chunk16 ^ (r & 7)) << 4);
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 B apart (the leading offset is unused in this layout).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1 << 16;                 // leading byte offset 16 B (unused)
+  d |= (uint64_t)(1024 >> 4) << 32;       // stride byte offset
+  d |= (uint64_t)1 << 46;                 // descriptor version
+  d |= (uint64_t)2 << 61;                 // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B (K-major), fp32 D, M x N.
+__host__ __device__ constexpr uint32_t f16_idesc(int m, int n) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ unsigned long long now_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = now_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (now_ns() - t0 > kWaitNs) return false;
+  }
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Eight e2m1 codes (one word, element 2i in the low nibble of byte i) times
+// one fp16 scale pair -> four fp16 pairs.
+__device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t s2) {
+  uint32_t o[4];
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
+  return make_uint4(hmul2_u32(o[0], s2), hmul2_u32(o[1], s2), hmul2_u32(o[2], s2),
+                    hmul2_u32(o[3], s2));
+}
+
+// Lower bound of beta in an ascending selection row padded with -1 (+inf).
+__device__ __forceinline__ bool row_holds(const int32_t* row, int k, int beta) {
+  int lo = 0, hi = k;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    const int x = row[mid] < 0 ? 0x7FFFFFFF : row[mid];
+    if (x < beta) lo = mid + 1; else hi = mid;
+  }
+  return lo < k && row[lo] == beta;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+sparse_prefill_kernel(Params p) {
+  const Geom& g = p.g;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int G = g.Hq / g.Hkv;
+  const int TR = p.tr;
+  const int tile = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int r0 = tile * TR;                   // first row of the tile
+  const int rows = min(TR, g.R - r0);
+  const int k = p.k;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // The swizzle atoms need 1024-byte alignment (one spare KB is allocated).
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;                           // 32 KB
+  uint8_t* sK = sQ + kQBytes;                   // 16 KB
+  uint8_t* sV = sK + kKBytes;                   // 16 KB
+  uint8_t* sP = sV + kVBytes;                   // 16 KB
+  uint8_t* sStage = sP + kPBytes;               // 2 x 9216 B
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + 2 * kStage);
+  uint64_t* mbar = full + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mbar + 1);
+  int* s_misc = reinterpret_cast<int*>(s_tmem + 1);            // [8]
+  int32_t* s_sel = s_misc + 8;                                  // [TR][k]
+  int32_t* s_union = s_sel + TR * k;                            // [ucap]
+  int32_t* s_upage = s_union + p.ucap;                          // [ucap]
+  uint32_t* s_bits = reinterpret_cast<uint32_t*>(s_upage + p.ucap);   // [ceil(MB/32)]
+  const int nwords = (g.MB + 31) >> 5;
+
+  // ---- barriers, tensor memory ---------------------------------------------
+  if (tid == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    mbar_init(mbar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(s_tmem)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+
+  // ---- this thread's query vector: Q row into the swizzled tile -------------
+  const int jj = tid / G, hh = tid % G;
+  const bool vec = jj < rows;                   // a real (row, head) vector
+  const int j = r0 + jj;
+  const int L = p.seqlens[b];
+  const int cap = g.MB * g.P;
+  const int nrow = vec ? visible_tokens(L, g.R, j, cap) : 0;
+  float cq = 0.f;                               // logit scale, log2 domain
+  {
+    uint4 raw[16];
+    const size_t qrow = ((size_t)b * g.R + j) * g.Hq + (size_t)kvh * G + hh;
+    float amax = 0.f;
+    if (vec) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow * kD);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) raw[i] = src[i];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          amax = fmaxf(amax, fabsf(__uint_as_float(w4[u] << 16)));
+          amax = fmaxf(amax, fabsf(__uint_as_float(w4[u] & 0xFFFF0000u)));
+        }
+      }
+    }
+    const int ebits = (int)((__float_as_uint(amax) >> 23) & 0xFF);
+    int sq = (amax > 0.f) ? 135 - ebits : 0;
+    sq = sq > 126 ? 126 : (sq < -126 ? -126 : sq);
+    const float up = __uint_as_float((uint32_t)(sq + 127) << 23);
+    const float down = __uint_as_float((uint32_t)(127 - sq) << 23);
+    cq = p.k_scale * p.sm_scale * kLog2e * down;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      uint4 h = make_uint4(0u, 0u, 0u, 0u);
+      if (vec) {
+        const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          o[u] = pack_half2(__uint_as_float(w4[u] << 16) * up,
+                            __uint_as_float(w4[u] & 0xFFFF0000u) * up);
+        h = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      // dims 8i..8i+7: half i / 8, 16-byte chunk i % 8 of row tid
+      *reinterpret_cast<uint4*>(sQ + (i >> 3) * (kQBytes / 2) + sw128(tid, i & 7)) = h;
+    }
+  }
+
+  // ---- the tile's rows' selections and their union ----------------------------
+  for (int i = tid; i < TR * k; i += kThreads) {
+    const int jr = i / k;
+    int v = -1;
+    if (jr < rows) {
+      v = p.sel[((size_t)b * g.R + r0 + jr) * k + (i - jr * k)];
+      if (v < 0 || v >= g.MB) v = -1;
+    }
+    s_sel[i] = v;
+  }
+  for (int i = tid; i < nwords; i += kThreads) s_bits[i] = 0u;
+  __syncthreads();
+  for (int i = tid; i < rows * k; i += kThreads) {
+    const int v = s_sel[i];
+    if (v >= 0) atomicOr(&s_bits[v >> 5], 1u << (v & 31));
+  }
+  __syncthreads();
+  {
+    // Blocks with a valid page, ascending: thread t scans words [t*per, ...).
+    const int per = (nwords + kThreads - 1) / kThreads;
+    const int w0 = min(nwords, tid * per), w1 = min(nwords, w0 + per);
+    const int32_t* pt = p.page_table + (size_t)b * g.MB;
+    int cnt = 0;
+    for (int w = w0; w < w1; ++w) {
+      uint32_t m = s_bits[w];
+      while (m) {
+        const int beta = (w << 5) + __ffs(m) - 1;
+        m &= m - 1;
+        const int pg = pt[beta];
+        if (pg >= 0 && pg < g.NP) ++cnt; else s_bits[w] &= ~(1u << (beta & 31));
+      }
+    }
+    int x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if ((tid & 31) >= o) x += y;
+    }
+    if ((tid & 31) == 31) s_misc[warp] = x;
+    __syncthreads();
+    int pos = x - cnt;
+    for (int w = 0; w < warp; ++w) pos += s_misc[w];
+    for (int w = w0; w < w1; ++w) {
+      uint32_t m = s_bits[w];
+      while (m) {
+        const int beta = (w << 5) + __ffs(m) - 1;
+        m &= m - 1;
+        s_union[pos] = beta;
+        s_upage[pos] = pt[beta];
+        ++pos;
+      }
+    }
+    if (tid == kThreads - 1) s_misc[4] = pos;
+  }
+  fence_proxy_async_smem();       // Q tile (generic stores) before the MMAs read it
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const int U = s_misc[4];
+  const int csh = (g.P == 2 * kTok) ? 1 : 0;    // chunks per block: 1 << csh
+  const int C = U << csh;
+  const int32_t* myrow = s_sel + jj * k;
+
+  const uint64_t pol = policy_evict_first();
+  auto issue = [&](int c) {
+    uint8_t* dst = sStage + (c & 1) * kStage;
+    const int u = c >> csh, sub = c & csh;
+    const size_t row0 = ((size_t)s_upage[u] * g.Hkv + kvh) * g.P + (size_t)sub * kTok;
+    mbar_arrive_expect_tx(&full[c & 1], kStage);
+    bulk_g2s(dst, p.k_pool + row0 * (kD / 2), kTok * kD / 2, &full[c & 1], pol);
+    bulk_g2s(dst + kTok * kD / 2, p.v_pool + row0 * (kD / 2), kTok * kD / 2, &full[c & 1], pol);
+    bulk_g2s(dst + kTok * kD, p.k_sf + row0 * (kD / 16), kTok * kD / 16, &full[c & 1], pol);
+    bulk_g2s(dst + kTok * kD + kTok * kD / 16, p.v_sf + row0 * (kD / 16), kTok * kD / 16,
+             &full[c & 1], pol);
+  };
+  if (tid == 0 && C > 0) issue(0);
+
+  float m_base = -INFINITY, l_run = 0.f;
+  uint32_t mma_phase = 0;
+  bool dead = false;
+  int issued = C > 0 ? 1 : 0;
+  const uint32_t tS = tmem, tO = tmem + kOCol;
+  const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+
+  for (int c = 0; c < C && !dead; ++c) {
+    if (tid == 0 && c + 1 < C) {
+      fence_proxy_async_smem();   // the stage's last readers (chunk c - 1) came first
+      issue(c + 1);
+      issued = c + 2;
+    }
+    // Every wait is agreed on by the whole CTA, so no thread is left in a barrier.
+    if (__syncthreads_or(!wait_bounded(&full[c & 1], (c >> 1) & 1))) { dead = true; break; }
+    const uint8_t* st = sStage + (c & 1) * kStage;
+    const uint8_t* kc = st;
+    const uint8_t* vc = st + kTok * kD / 2;
+    const uint8_t* ks = st + kTok * kD;
+    const uint8_t* vs = ks + kTok * kD / 16;
+
+    // ---- 1. dequantise: K rows = tokens, V^T rows = dims --------------------
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int pc = tid + kThreads * i;      // (token, 8-dim group)
+      const int t = pc >> 4, c8 = pc & 15;
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(kc + t * 64 + c8 * 4);
+      const uint32_t s = e4m3x2_to_f16x2(ks[t * 8 + (c8 >> 1)]);
+      const uint32_t s2 = prmt(s, 0, 0x1010);
+      *reinterpret_cast<uint4*>(sK + (c8 >> 3) * (kKBytes / 2) + sw128(t, c8 & 7)) =
+          dequant8(w, s2);
+    }
+    {
+      const int tg = tid & 7, c8 = tid >> 3;  // 8 tokens x 8 dims per thread
+      uint32_t X[8], sf[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        X[u] = *reinterpret_cast<const uint32_t*>(vc + (8 * tg + u) * 64 + c8 * 4);
+        sf[u] = vs[(8 * tg + u) * 8 + (c8 >> 1)];
+      }
+      uint32_t rowv[8][4];   // [dim e][token pair]
+#pragma unroll
+      for (int pr = 0; pr < 4; ++pr) {
+        const uint32_t x0 = X[2 * pr], x1 = X[2 * pr + 1];
+        const uint32_t s2 = e4m3x2_to_f16x2(sf[2 * pr] | (sf[2 * pr + 1] << 8));
+        const uint32_t LO = (x0 & 0x0F0F0F0Fu) | ((x1 << 4) & 0xF0F0F0F0u);    // even dims
+        const uint32_t HI = ((x0 >> 4) & 0x0F0F0F0Fu) | (x1 & 0xF0F0F0F0u);    // odd dims
+        const uint4 el = dequant8(LO, s2), od = dequant8(HI, s2);
+        rowv[0][pr] = el.x; rowv[2][pr] = el.y; rowv[4][pr] = el.z; rowv[6][pr] = el.w;
+        rowv[1][pr] = od.x; rowv[3][pr] = od.y; rowv[5][pr] = od.z; rowv[7][pr] = od.w;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        *reinterpret_cast<uint4*>(sV + sw128(8 * c8 + e, tg)) =
+            make_uint4(rowv[e][0], rowv[e][1], rowv[e][2], rowv[e][3]);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- 2. S = Q . K^T ------------------------------------------------------
+    if (tid == 0) {
+      const uint32_t id = f16_idesc(128, kTok);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int ks2 = 0; ks2 < 4; ++ks2)
+          mma_f16(tS, sw128_desc(smem_u32(sQ + h * (kQBytes / 2)) + 32 * ks2),
+                  sw128_desc(smem_u32(sK + h * (kKBytes / 2)) + 32 * ks2), id,
+                  (h | ks2) ? 1u : 0u);
+      mma_commit(mbar);
+    }
+    if (__syncthreads_or(!wait_bounded(mbar, mma_phase & 1))) { dead = true; break; }
+    ++mma_phase;
+    tc_fence_after();
+
+    // ---- 3. masks and online softmax for this thread's vector ----------------
+    const int ue = s_union[c >> csh];
+    const int tok0 = ue * g.P + (c & csh) * kTok;
+    const bool member = vec && tok0 < nrow && row_holds(myrow, k, ue);
+    float z[64];
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      float v16[16];
+      tmem_ld16(tS + lane_off + 16 * q4, v16);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) z[16 * q4 + i] = v16[i];
+    }
+    tmem_wait_ld();
+    float cmax = -INFINITY;
+    if (member) {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        z[i] = (tok0 + i < nrow) ? z[i] * cq : -INFINITY;
+        cmax = fmaxf(cmax, z[i]);
+      }
+    }
+    bool rescale = false;
+    float alpha = 1.f;
+    if (cmax != -INFINITY) {
+      if (m_base == -INFINITY) {
+        m_base = cmax;
+      } else if (cmax > m_base + kRescaleGap) {
+        alpha = exp2f(m_base - cmax);
+        m_base = cmax;
+        rescale = true;
+      }
+    }
+    uint32_t pk[32];
+    {
+      float ls = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float p0 = 0.f, p1 = 0.f;
+        if (member) {
+          p0 = exp2f(z[2 * i] - m_base);
+          p1 = exp2f(z[2 * i + 1] - m_base);
+        }
+        ls += p0 + p1;
+        pk[i] = pack_half2(p0, p1);
+      }
+      l_run = l_run * alpha + ls;
+    }
+#pragma unroll
+    for (int c16 = 0; c16 < 8; ++c16)
+      *reinterpret_cast<uint4*>(sP + sw128(tid, c16)) =
+          make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
+    // O (complete: the previous chunk's MMA was waited for).  Tensor-memory
+    // loads and stores are warp-wide: a warp rescales when any of its lanes
+    // must (alpha = 1 for the others).
+    if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+      for (int q8 = 0; q8 < 8; ++q8) {
+        float o16[16];
+        tmem_ld16(tO + lane_off + 16 * q8, o16);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o16[i] *= alpha;
+        tmem_st16(tO + lane_off + 16 * q8, o16);
+      }
+      tmem_wait_st();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- 4. O += P . V ---------------------------------------------------------
+    if (tid == 0) {
+      const uint32_t id = f16_idesc(128, kD);
+#pragma unroll
+      for (int ks2 = 0; ks2 < 4; ++ks2)
+        mma_f16(tO, sw128_desc(smem_u32(sP) + 32 * ks2), sw128_desc(smem_u32(sV) + 32 * ks2), id,
+                (c | ks2) ? 1u : 0u);
+      mma_commit(mbar);
+    }
+    if (__syncthreads_or(!wait_bounded(mbar, mma_phase & 1))) { dead = true; break; }
+    ++mma_phase;
+    tc_fence_after();
+  }
+
+  if (dead) {
+    if (tid == 0) atomicExch(p.status, kStatusWaitTimeout);
+    // Let this CTA's copies in flight land before the CTA's memory goes away.
+    if (tid == 0)
+      for (int c = max(0, issued - 2); c < issued; ++c) wait_bounded(&full[c & 1], (c >> 1) & 1);
+  }
+
+  // ---- epilogue: out = O / l * v_scale, lse -------------------------------------
+  // (tensor-memory loads by every lane of every warp; O holds no value when no
+  // chunk was visited, and rows without a token write zeros)
+  if (!dead) {
+    const size_t orow = ((size_t)b * g.R + j) * g.Hq + (size_t)kvh * G + hh;
+    uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kD);
+    const bool has = l_run > 0.f && C > 0;
+    const float sc = has ? p.v_scale / l_run : 0.f;
+#pragma unroll
+    for (int q8 = 0; q8 < 8; ++q8) {
+      float o16[16];
+      if (C > 0) {
+        tmem_ld16(tO + lane_off + 16 * q8, o16);
+        tmem_wait_ld();
+      }
+      uint32_t h[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        __nv_bfloat162 x = __floats2bfloat162_rn(has ? o16[2 * i] * sc : 0.f,
+                                                 has ? o16[2 * i + 1] * sc : 0.f);
+        h[i] = *reinterpret_cast<uint32_t*>(&x);
+      }
+      if (vec) {
+        dst[2 * q8] = make_uint4(h[0], h[1], h[2], h[3]);
+        dst[2 * q8 + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+      }
+    }
+    if (vec) p.lse[orow] = has ? (m_base + log2f(l_run)) * kLn2 : -INFINITY;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols));
+}
+
+}  // namespace
+
+int prefill_rows_per_tile(const Geom& g) {
+  const int G = g.Hq / g.Hkv;
+  return G <= 128 ? 128 / G : 0;
+}
+
+size_t prefill_smem_bytes(const Geom& g, int k) {
+  const int tr = prefill_rows_per_tile(g);
+  const int ucap = min(g.MB, tr * k);
+  return (size_t)1024 + kQBytes + kKBytes + kVBytes + kPBytes + 2 * kStage + 3 * 8 + 4 + 8 * 4 +
+         (size_t)tr * k * 4 + (size_t)ucap * 8 + (size_t)((g.MB + 31) / 32) * 4;
+}
+
+cudaError_t launch_sparse_prefill(const Geom& g, const void* q, const uint8_t* k_pool,
+                                  const uint8_t* k_sf, const uint8_t* v_pool, const uint8_t* v_sf,
+                                  float k_scale, float v_scale, float sm_scale,
+                                  const int32_t* page_table, const int32_t* seqlens,
+                                  const int32_t* sel, int k, void* out, float* lse,
+                                  int* status, cudaStream_t stream) {
+  Params prm;
+  prm.g = g;
+  prm.q = reinterpret_cast<const __nv_bfloat16*>(q);
+  prm.k_pool = k_pool; prm.k_sf = k_sf; prm.v_pool = v_pool; prm.v_sf = v_sf;
+  prm.k_scale = k_scale; prm.v_scale = v_scale; prm.sm_scale = sm_scale;
+  prm.page_table = page_table; prm.seqlens = seqlens; prm.sel = sel; prm.k = k;
+  prm.tr = prefill_rows_per_tile(g);
+  prm.ucap = min(g.MB, prm.tr * k);
+  prm.out = reinterpret_cast<__nv_bfloat16*>(out);
+  prm.lse = lse;
+  prm.status = status;
+  const size_t smem = prefill_smem_bytes(g, k);
+  cudaError_t e = cudaFuncSetAttribute(sparse_prefill_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((g.R + prm.tr - 1) / prm.tr, g.Hkv, g.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 0;
+  return cudaLaunchKernelEx(&cfg, sparse_prefill_kernel, prm);
+}
+
+}  // namespace qsa

@@ -63,6 +63,10 @@ class Case:
     tie_frac: float = 0.0
     head_dim: int = 128
     index_dim: int = 64
+    # 0: every row's index query is drawn independently.  n > 0: one base
+    # query per request plus per-row integer noise in [-n, n] (clipped to
+    # int8), so that the rows of a context chunk select overlapping blocks.
+    iq_row_noise: int = 0
 
     @property
     def rows(self) -> int:
@@ -97,7 +101,13 @@ CONFIGS = [
          num_q_heads=24, num_kv_heads=2, page_size=32, ctx_lo=8192,
          ctx_hi=16384, k=64, window=4, max_blocks=512, pool="perm",
          head_dim=256),
+    Case("context prefill", seed=6, batch=2, rows_per_req=512, num_q_heads=32,
+         num_kv_heads=4, page_size=64, ctx_lo=32768, ctx_hi=32768, k=64,
+         window=4, max_blocks=512, pool="perm", iq_row_noise=24),
 ]
+
+# Workloads whose rows are context row groups (served by the row-tile path).
+PREFILL_CONFIGS = (6,)
 
 
 def small(case: Case, batch: Optional[int] = None, ctx_lo: Optional[int] = None,
@@ -226,7 +236,12 @@ def make_workload(case: Case, device="cpu", seed: Optional[int] = None) -> dict:
     v_pool, v_sf, v_scale = nvfp4_encode(vb)
     del vb
     # 5./6. index query and keys
-    iq = _uniform_int(gen, -127, 127, (T, Hq, Di), device).to(torch.int8)
+    if case.iq_row_noise > 0:
+        base = _uniform_int(gen, -127, 127, (B, 1, Hq, Di), device)
+        noise = _uniform_int(gen, -case.iq_row_noise, case.iq_row_noise, (B, R, Hq, Di), device)
+        iq = (base + noise).clamp(-127, 127).reshape(T, Hq, Di).to(torch.int8)
+    else:
+        iq = _uniform_int(gen, -127, 127, (T, Hq, Di), device).to(torch.int8)
     ik_pool = _uniform_int(gen, -127, 127, (NP, P, Di), device).to(torch.int8)
 
     # 7. page table

@@ -53,7 +53,7 @@ FAKE = ctypes.c_void_p(256)   # never dereferenced: validation fails first
 @pytest.mark.parametrize("bad,status", [
     (dict(num_q_heads=7), 1), (dict(batch=0), 1), (dict(rows_per_req=0), 1),
     (dict(max_blocks=0), 1), (dict(num_pages=0), 1), (dict(head_dim=64), 2),
-    (dict(index_dim=128), 2), (dict(page_size=32), 2), (dict(rows_per_req=9), 2),
+    (dict(index_dim=128), 2), (dict(page_size=32), 2), (dict(rows_per_req=4097), 2),
     (dict(head_dim=192), 2), (dict(head_dim=256, page_size=128), 2),
     (dict(head_dim=256, page_size=16), 2),
     (dict(num_q_heads=512, num_kv_heads=2), 2),
