@@ -103,6 +103,9 @@ const char *qsa_status_string(qsa_status_t status);
  * exact in int32 (|value| <= 64*64*127*127 for Hq <= 64; Hq <= 256 keeps it
  * below 2^31), or INT32_MIN when the block's page is invalid or the block has
  * no token visible to row r (all beta >= ceil(n/P) included).
+ * Returns QSA_ERR_INVALID_ARG for null pointers or iq / ik_pool not 16-byte
+ * aligned; geometry and device checks as for the other calls (rows_per_req up
+ * to 4096).
  */
 qsa_status_t qsa_index_scores(const qsa_geom_t *geom, const int8_t *iq,
                               const int8_t *ik_pool, const int32_t *page_table,
@@ -367,7 +370,8 @@ qsa_status_t qsa_rollback_restore(const qsa_geom_t *geom, const int32_t *page_ta
  * Returns QSA_ERR_UNSUPPORTED for head_dim != 128, more than 128 query heads
  * per KV head, or a tile (floor(128 / G) rows x k selections plus their union)
  * beyond one CTA's shared memory; QSA_ERR_INVALID_ARG for null pointers, k <
- * 1, pools / scales / q / out not 16-byte aligned; QSA_ERR_WORKSPACE for a
+ * 1, k_scale or sm_scale not positive and finite, v_scale not finite, pools /
+ * scales / q / out not 16-byte aligned; QSA_ERR_WORKSPACE for a
  * missing, short or misaligned workspace.  A bounded device wait that gives
  * up is reported through qsa_workspace_status().
  */

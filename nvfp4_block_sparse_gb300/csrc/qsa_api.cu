@@ -184,7 +184,7 @@ qsa_status_t qsa_index_scores(const qsa_geom_t* geom, const int8_t* iq, const in
   qsa_status_t st = check_geom(geom, qsa::kMaxContextRows);
   if (st != QSA_OK) return st;
   if (!iq || !ik_pool || !page_table || !seqlens || !scores) return QSA_ERR_INVALID_ARG;
-  if (!aligned(ik_pool, 16)) return QSA_ERR_INVALID_ARG;
+  if (!aligned(ik_pool, 16) || !aligned(iq, 16)) return QSA_ERR_INVALID_ARG;
   st = check_device();
   if (st != QSA_OK) return st;
   return from_cuda(qsa::launch_index_scores(to_geom(geom), iq, ik_pool, page_table, seqlens,
@@ -277,6 +277,9 @@ qsa_status_t qsa_sparse_prefill(const qsa_geom_t* geom, const void* q_bf16,
     return QSA_ERR_INVALID_ARG;
   if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(k_sf, 16) || !aligned(v_sf, 16) ||
       !aligned(q_bf16, 16) || !aligned(out_bf16, 16))
+    return QSA_ERR_INVALID_ARG;
+  if (!(k_scale > 0.f) || !(sm_scale > 0.f) || !isfinite(k_scale) || !isfinite(sm_scale) ||
+      !isfinite(v_scale))
     return QSA_ERR_INVALID_ARG;
   if (!workspace || workspace_bytes < 256 || !aligned(workspace, 256)) return QSA_ERR_WORKSPACE;
   st = check_device();

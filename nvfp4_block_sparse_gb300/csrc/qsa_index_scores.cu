@@ -380,6 +380,163 @@ index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __r
   (void)page;
 }
 
+// ---- long row groups (R > 8): 64 rows per CTA ----------------------------
+//
+// The same exact tensor-core dot products, for eight 8-row groups per CTA: a
+// warp converts a block's keys to fp16 A fragments once and runs the MMAs of
+// all eight groups from those registers, so the keys are read once per 64
+// rows instead of once per 8.  Head sums: thread (row, part) adds the Hq
+// 16-byte slices of its row's index queries (all loads in flight at once).
+constexpr int kGroupRows = 64;
+
+template <int P>
+__global__ void __launch_bounds__(kThreads)
+index_scores_rows_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __restrict__ ik_pool,
+                         const int32_t* __restrict__ page_table,
+                         const int32_t* __restrict__ seqlens, int32_t* __restrict__ scores,
+                         int blocks_per_warp) {
+  __shared__ __half wsplit[2][kGroupRows][kIndexDim];   // a, b of w = 128 a + b
+  static_assert(kThreads == 4 * kGroupRows, "one thread per (row, 16-dim part)");
+  const int b = blockIdx.y;
+  const int r0 = blockIdx.z * kGroupRows;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int R = g.R;
+
+  pdl_wait();
+
+  const int L = seqlens[b];
+  const int cap = g.MB * P;
+  const int nmax = visible_tokens(L, R, min(R - 1, r0 + kGroupRows - 1), cap);
+
+  auto block_of = [&](int it, int& beta, int& page) -> bool {
+    beta = (blockIdx.x * blocks_per_warp + it) * kWarps + warp;
+    page = -1;
+    if (beta >= g.MB) return false;
+    page = page_table[(size_t)b * g.MB + beta];
+    return page >= 0 && page < g.NP && beta * P < nmax;
+  };
+
+  {
+    const int rr = threadIdx.x >> 2, part = threadIdx.x & 3;
+    int acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = 0;
+    if (r0 + rr < R) {
+      const int4* src = reinterpret_cast<const int4*>(
+                            iq + ((size_t)b * R + r0 + rr) * g.Hq * kIndexDim) + part;
+      int h = 0;
+      for (; h + 8 <= g.Hq; h += 8) {
+        int4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __ldg(src + (size_t)(h + u) * (kIndexDim / 16));
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[4 * q + e] += (int)(int8_t)(w4[q] >> (8 * e));
+        }
+      }
+      for (; h < g.Hq; ++h) {
+        const int4 v = __ldg(src + (size_t)h * (kIndexDim / 16));
+        const int w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[4 * q + e] += (int)(int8_t)(w4[q] >> (8 * e));
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int w = acc[i];
+      const int lo = ((w + 64) & 127) - 64;
+      wsplit[0][rr][16 * part + i] = __int2half_rn((w - lo) / 128);
+      wsplit[1][rr][16 * part + i] = __int2half_rn(lo);
+    }
+  }
+  __syncthreads();
+  pdl_trigger();
+
+  // This lane's columns in every group: rows r0 + 8*grp + 2*tig + e.
+  int beta = 0, page = -1;
+  for (int it = 0; it < blocks_per_warp; ++it) {
+    const bool live = block_of(it, beta, page);
+    if (beta >= g.MB) break;
+    int32_t* dst = scores + ((size_t)b * R + r0) * g.MB + beta;
+    if (!live) {
+      for (int jr = lane; jr < kGroupRows; jr += 32)
+        if (r0 + jr < R) dst[(size_t)jr * g.MB] = kSentinel;
+      continue;
+    }
+    int4 kv[P / 8];
+    const int4* src = reinterpret_cast<const int4*>(ik_pool + (size_t)page * P * kIndexDim) + lane;
+#pragma unroll
+    for (int i = 0; i < P / 8; ++i) kv[i] = ld_stream_v4(src + 32 * i);
+    // A fragments of the block, once: [m-tile][k-step][4]
+    uint32_t af[P / 16][4][4];
+#pragma unroll
+    for (int mt = 0; mt < P / 16; ++mt) {
+      const int4 ka = kv[2 * mt], kb = kv[2 * mt + 1];   // tokens gid and gid + 8
+      const uint32_t wa[4] = {(uint32_t)ka.x, (uint32_t)ka.y, (uint32_t)ka.z, (uint32_t)ka.w};
+      const uint32_t wb[4] = {(uint32_t)kb.x, (uint32_t)kb.y, (uint32_t)kb.z, (uint32_t)kb.w};
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        s8x4_to_f16x2x2(wa[kk], af[mt][kk][0], af[mt][kk][2]);
+        s8x4_to_f16x2x2(wb[kk], af[mt][kk][1], af[mt][kk][3]);
+      }
+    }
+    for (int grp = 0; grp < kGroupRows / 8; ++grp) {
+      const int jbase = 8 * grp;
+      if (r0 + jbase >= R) break;
+      uint32_t bw[2][4][2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const __half* w = &wsplit[q][jbase + gid][16 * tig + 4 * kk];
+          bw[q][kk][0] = *reinterpret_cast<const uint32_t*>(w);
+          bw[q][kk][1] = *reinterpret_cast<const uint32_t*>(w + 2);
+        }
+      int ncol[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int j = r0 + jbase + 2 * tig + e;
+        ncol[e] = (j < R) ? visible_tokens(L, R, j, cap) : 0;
+      }
+      int best[2] = {kSentinel, kSentinel};
+#pragma unroll
+      for (int mt = 0; mt < P / 16; ++mt) {
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          mma_f16_16816(sa, af[mt][kk], bw[0][kk][0], bw[0][kk][1]);
+          mma_f16_16816(sb, af[mt][kk], bw[1][kk][0], bw[1][kk][1]);
+        }
+        const int tA = beta * P + 16 * mt + gid, tB = tA + 8;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int vA = __float2int_rn(sa[e]) * 128 + __float2int_rn(sb[e]);
+          const int vB = __float2int_rn(sa[2 + e]) * 128 + __float2int_rn(sb[2 + e]);
+          if (tA < ncol[e]) best[e] = max(best[e], vA);
+          if (tB < ncol[e]) best[e] = max(best[e], vB);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        int v = best[e];
+        v = max(v, __shfl_xor_sync(0xffffffffu, v, 4));
+        v = max(v, __shfl_xor_sync(0xffffffffu, v, 8));
+        v = max(v, __shfl_xor_sync(0xffffffffu, v, 16));
+        const int j = jbase + 2 * tig + e;
+        if (gid == 0 && r0 + j < R) dst[(size_t)j * g.MB] = (beta * P < ncol[e]) ? v : kSentinel;
+      }
+    }
+  }
+}
+
 // Blocks each warp scores: one, unless the grid would exceed about four
 // resident CTAs per SM.
 int blocks_per_warp_for(const Geom& g) {
@@ -445,10 +602,39 @@ cudaError_t launch_mma_t(const Geom& g, const int8_t* iq, const int8_t* ik_pool,
 }
 
 template <int P>
+cudaError_t launch_rows(const Geom& g, const int8_t* iq, const int8_t* ik_pool,
+                        const int32_t* page_table, const int32_t* seqlens, int32_t* scores,
+                        bool pdl, cudaStream_t stream) {
+  // Blocks per warp: about four resident CTAs per SM over the whole grid.
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long groups = (g.R + kGroupRows - 1) / kGroupRows;
+  const long long warps_needed = (long long)g.B * g.MB * groups;
+  const long long warp_slots = (long long)sms * 4 * kWarps;
+  int bpw = (int)((warps_needed + warp_slots - 1) / warp_slots);
+  bpw = bpw < 1 ? 1 : (bpw > 8 ? 8 : bpw);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((g.MB + kWarps * bpw - 1) / (kWarps * bpw), g.B, (unsigned)groups);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, index_scores_rows_kernel<P>, g, iq, ik_pool, page_table,
+                            seqlens, scores, bpw);
+}
+
+template <int P>
 cudaError_t launch_p(const Geom& g, const int8_t* iq, const int8_t* ik_pool,
                      const int32_t* page_table, const int32_t* seqlens, int32_t* scores,
                      bool pdl, cudaStream_t stream) {
-  // Decode rows: int16 x int8 dp2a.  Two rows and more: the tensor cores.
+  // Decode rows: int16 x int8 dp2a.  Two rows and more: the tensor cores,
+  // 8 rows per CTA for verify rows, 64 for long row groups.
+  if (g.R > kMaxRows) return launch_rows<P>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);
   if (g.R >= 2) {
     if (blocks_per_warp_for(g) > 1)
       return launch_mma_t<P, true>(g, iq, ik_pool, page_table, seqlens, scores, pdl, stream);

@@ -114,6 +114,19 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// A CTA-wide bounded wait on one mbarrier phase: every thread polls, then
+// the CTA agrees on the outcome.  True when the wait gave up, in every thread.
+__device__ __forceinline__ bool cta_wait_failed(uint64_t* bar, uint32_t parity) {
+  return __syncthreads_or(!wait_bounded(bar, parity));
+}
+
+// 2^x, hardware approximation (flushes subnormal results to zero).
+__device__ __forceinline__ float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                         uint32_t accumulate) {
   asm volatile(
@@ -214,8 +227,9 @@ sparse_prefill_kernel(Params p) {
   uint8_t* sP = sV + kVBytes;                   // 16 KB
   uint8_t* sStage = sP + kPBytes;               // 2 x 9216 B
   uint64_t* full = reinterpret_cast<uint64_t*>(sStage + 2 * kStage);
-  uint64_t* mbar = full + 2;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mbar + 1);
+  uint64_t* barS = full + 2;                    // S = Q K^T complete
+  uint64_t* barO = full + 3;                    // O += P V complete
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(full + 4);
   int* s_misc = reinterpret_cast<int*>(s_tmem + 1);            // [8]
   int32_t* s_sel = s_misc + 8;                                  // [TR][k]
   int32_t* s_union = s_sel + TR * k;                            // [ucap]
@@ -227,7 +241,8 @@ sparse_prefill_kernel(Params p) {
   if (tid == 0) {
     mbar_init(&full[0], 1);
     mbar_init(&full[1], 1);
-    mbar_init(mbar, 1);
+    mbar_init(barS, 1);
+    mbar_init(barO, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -362,86 +377,116 @@ sparse_prefill_kernel(Params p) {
     bulk_g2s(dst + kTok * kD + kTok * kD / 16, p.v_sf + row0 * (kD / 16), kTok * kD / 16,
              &full[c & 1], pol);
   };
-  if (tid == 0 && C > 0) issue(0);
-
-  float m_base = -INFINITY, l_run = 0.f;
-  uint32_t mma_phase = 0;
-  bool dead = false;
-  int issued = C > 0 ? 1 : 0;
   const uint32_t tS = tmem, tO = tmem + kOCol;
   const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
 
-  for (int c = 0; c < C && !dead; ++c) {
-    if (tid == 0 && c + 1 < C) {
-      fence_proxy_async_smem();   // the stage's last readers (chunk c - 1) came first
-      issue(c + 1);
-      issued = c + 2;
-    }
-    // Every wait is agreed on by the whole CTA, so no thread is left in a barrier.
-    if (__syncthreads_or(!wait_bounded(&full[c & 1], (c >> 1) & 1))) { dead = true; break; }
-    const uint8_t* st = sStage + (c & 1) * kStage;
+  // ---- stage helpers ---------------------------------------------------------
+  // K rows = tokens (two 64-dim halves), V^T rows = dims; 8 pieces per thread.
+  auto dequant_k = [&](const uint8_t* st) {
     const uint8_t* kc = st;
-    const uint8_t* vc = st + kTok * kD / 2;
     const uint8_t* ks = st + kTok * kD;
-    const uint8_t* vs = ks + kTok * kD / 16;
-
-    // ---- 1. dequantise: K rows = tokens, V^T rows = dims --------------------
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int pc = tid + kThreads * i;      // (token, 8-dim group)
       const int t = pc >> 4, c8 = pc & 15;
       const uint32_t w = *reinterpret_cast<const uint32_t*>(kc + t * 64 + c8 * 4);
       const uint32_t s = e4m3x2_to_f16x2(ks[t * 8 + (c8 >> 1)]);
-      const uint32_t s2 = prmt(s, 0, 0x1010);
       *reinterpret_cast<uint4*>(sK + (c8 >> 3) * (kKBytes / 2) + sw128(t, c8 & 7)) =
-          dequant8(w, s2);
+          dequant8(w, prmt(s, 0, 0x1010));
     }
-    {
-      const int tg = tid & 7, c8 = tid >> 3;  // 8 tokens x 8 dims per thread
-      uint32_t X[8], sf[8];
+  };
+  auto dequant_v = [&](const uint8_t* st) {
+    const uint8_t* vc = st + kTok * kD / 2;
+    const uint8_t* vs = st + kTok * kD + kTok * kD / 16;
+    // 8 tokens x 8 dims per thread: lane = dim group (16) + half-warp bit, the
+    // two half-warps on neighbouring 8-token groups.  The upper half loads each
+    // token pair in swapped order, so that one load instruction touches tokens
+    // of both parities: 32 distinct banks (token rows are 64 B apart).
+    const int lane = tid & 31, hw = lane >> 4;
+    const int c8 = lane & 15, tg = 2 * warp + hw;
+    uint32_t X[8], sf[8];   // X[u]: token 8*tg + (u ^ hw)
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        X[u] = *reinterpret_cast<const uint32_t*>(vc + (8 * tg + u) * 64 + c8 * 4);
-        sf[u] = vs[(8 * tg + u) * 8 + (c8 >> 1)];
-      }
-      uint32_t rowv[8][4];   // [dim e][token pair]
-#pragma unroll
-      for (int pr = 0; pr < 4; ++pr) {
-        const uint32_t x0 = X[2 * pr], x1 = X[2 * pr + 1];
-        const uint32_t s2 = e4m3x2_to_f16x2(sf[2 * pr] | (sf[2 * pr + 1] << 8));
-        const uint32_t LO = (x0 & 0x0F0F0F0Fu) | ((x1 << 4) & 0xF0F0F0F0u);    // even dims
-        const uint32_t HI = ((x0 >> 4) & 0x0F0F0F0Fu) | (x1 & 0xF0F0F0F0u);    // odd dims
-        const uint4 el = dequant8(LO, s2), od = dequant8(HI, s2);
-        rowv[0][pr] = el.x; rowv[2][pr] = el.y; rowv[4][pr] = el.z; rowv[6][pr] = el.w;
-        rowv[1][pr] = od.x; rowv[3][pr] = od.y; rowv[5][pr] = od.z; rowv[7][pr] = od.w;
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        *reinterpret_cast<uint4*>(sV + sw128(8 * c8 + e, tg)) =
-            make_uint4(rowv[e][0], rowv[e][1], rowv[e][2], rowv[e][3]);
+    for (int u = 0; u < 8; ++u) {
+      const int t = 8 * tg + (u ^ hw);
+      X[u] = *reinterpret_cast<const uint32_t*>(vc + t * 64 + c8 * 4);
+      sf[u] = vs[t * 8 + (c8 >> 1)];
     }
+    uint32_t rowv[8][4];   // [dim e][token pair]
+#pragma unroll
+    for (int pr = 0; pr < 4; ++pr) {
+      const uint32_t x0 = hw ? X[2 * pr + 1] : X[2 * pr];        // token 8*tg + 2*pr
+      const uint32_t x1 = hw ? X[2 * pr] : X[2 * pr + 1];        // token 8*tg + 2*pr + 1
+      const uint32_t f0 = hw ? sf[2 * pr + 1] : sf[2 * pr];
+      const uint32_t f1 = hw ? sf[2 * pr] : sf[2 * pr + 1];
+      const uint32_t s2 = e4m3x2_to_f16x2(f0 | (f1 << 8));
+      const uint32_t LO = (x0 & 0x0F0F0F0Fu) | ((x1 << 4) & 0xF0F0F0F0u);    // even dims
+      const uint32_t HI = ((x0 >> 4) & 0x0F0F0F0Fu) | (x1 & 0xF0F0F0F0u);    // odd dims
+      const uint4 el = dequant8(LO, s2), od = dequant8(HI, s2);
+      rowv[0][pr] = el.x; rowv[2][pr] = el.y; rowv[4][pr] = el.z; rowv[6][pr] = el.w;
+      rowv[1][pr] = od.x; rowv[3][pr] = od.y; rowv[5][pr] = od.z; rowv[7][pr] = od.w;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      *reinterpret_cast<uint4*>(sV + sw128(8 * c8 + e, tg)) =
+          make_uint4(rowv[e][0], rowv[e][1], rowv[e][2], rowv[e][3]);
+  };
+  // Generic-proxy shared-memory writes become visible to the tensor core and
+  // every thread's tensor-memory accesses are ordered around the barrier.
+  auto publish = [&]() {
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+  };
+  auto issue_s = [&]() {       // S = Q . K^T, then the S barrier
+    const uint32_t id = f16_idesc(128, kTok);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int ks2 = 0; ks2 < 4; ++ks2)
+        mma_f16(tS, sw128_desc(smem_u32(sQ + h * (kQBytes / 2)) + 32 * ks2),
+                sw128_desc(smem_u32(sK + h * (kKBytes / 2)) + 32 * ks2), id,
+                (h | ks2) ? 1u : 0u);
+    mma_commit(barS);
+  };
+  auto issue_o = [&](int c) {  // O += P . V, then the O barrier
+    const uint32_t id = f16_idesc(128, kD);
+#pragma unroll
+    for (int ks2 = 0; ks2 < 4; ++ks2)
+      mma_f16(tO, sw128_desc(smem_u32(sP) + 32 * ks2), sw128_desc(smem_u32(sV) + 32 * ks2), id,
+              (c | ks2) ? 1u : 0u);
+    mma_commit(barO);
+  };
 
-    // ---- 2. S = Q . K^T ------------------------------------------------------
-    if (tid == 0) {
-      const uint32_t id = f16_idesc(128, kTok);
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int ks2 = 0; ks2 < 4; ++ks2)
-          mma_f16(tS, sw128_desc(smem_u32(sQ + h * (kQBytes / 2)) + 32 * ks2),
-                  sw128_desc(smem_u32(sK + h * (kKBytes / 2)) + 32 * ks2), id,
-                  (h | ks2) ? 1u : 0u);
-      mma_commit(mbar);
+  // ---- pipeline ----------------------------------------------------------------
+  // Chunk c:  softmax(c) -> [O += P(c) V(c)  ||  dequantise K(c+1)]
+  //           -> [S(c+1) = Q K(c+1)^T  ||  dequantise V(c+1) once O(c) is done]
+  // The NVFP4 bytes of chunk c+2 are requested when chunk c's stage is free.
+  float m_base = -INFINITY, l_run = 0.f;
+  uint32_t phS = 0, phO = 0;
+  bool dead = false;
+  int issued = 0;
+  if (tid == 0) {
+    for (int c = 0; c < min(C, 2); ++c) issue(c);
+  }
+  issued = min(C, 2);
+  if (C > 0) {
+    if (cta_wait_failed(&full[0], 0)) {
+      dead = true;
+    } else {
+      dequant_k(sStage);
+      dequant_v(sStage);
+      publish();
+      if (tid == 0) issue_s();
     }
-    if (__syncthreads_or(!wait_bounded(mbar, mma_phase & 1))) { dead = true; break; }
-    ++mma_phase;
+  }
+
+  for (int c = 0; c < C && !dead; ++c) {
+    if (cta_wait_failed(barS, phS & 1)) { dead = true; break; }   // S(c) and all before it
+    ++phS;
     tc_fence_after();
 
-    // ---- 3. masks and online softmax for this thread's vector ----------------
+    // ---- softmax(c): masks, online softmax, P tile, O rescale ------------------
     const int ue = s_union[c >> csh];
     const int tok0 = ue * g.P + (c & csh) * kTok;
     const bool member = vec && tok0 < nrow && row_holds(myrow, k, ue);
@@ -454,13 +499,17 @@ sparse_prefill_kernel(Params p) {
       for (int i = 0; i < 16; ++i) z[16 * q4 + i] = v16[i];
     }
     tmem_wait_ld();
-    float cmax = -INFINITY;
+    float cmax = -INFINITY;   // log2 units
     if (member) {
+      if (tok0 + kTok > nrow) {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        z[i] = (tok0 + i < nrow) ? z[i] * cq : -INFINITY;
-        cmax = fmaxf(cmax, z[i]);
+        for (int i = 0; i < 64; ++i)
+          if (tok0 + i >= nrow) z[i] = -INFINITY;
       }
+      float mx = z[0];
+#pragma unroll
+      for (int i = 1; i < 64; ++i) mx = fmaxf(mx, z[i]);
+      cmax = mx * cq;         // cq > 0: the scale keeps the order
     }
     bool rescale = false;
     float alpha = 1.f;
@@ -468,31 +517,31 @@ sparse_prefill_kernel(Params p) {
       if (m_base == -INFINITY) {
         m_base = cmax;
       } else if (cmax > m_base + kRescaleGap) {
-        alpha = exp2f(m_base - cmax);
+        alpha = exp2_approx(m_base - cmax);
         m_base = cmax;
         rescale = true;
       }
     }
     uint32_t pk[32];
-    {
+    if (member) {
       float ls = 0.f;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        float p0 = 0.f, p1 = 0.f;
-        if (member) {
-          p0 = exp2f(z[2 * i] - m_base);
-          p1 = exp2f(z[2 * i + 1] - m_base);
-        }
+        const float p0 = exp2_approx(fmaf(z[2 * i], cq, -m_base));
+        const float p1 = exp2_approx(fmaf(z[2 * i + 1], cq, -m_base));
         ls += p0 + p1;
         pk[i] = pack_half2(p0, p1);
       }
       l_run = l_run * alpha + ls;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) pk[i] = 0u;
     }
 #pragma unroll
     for (int c16 = 0; c16 < 8; ++c16)
       *reinterpret_cast<uint4*>(sP + sw128(tid, c16)) =
           make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
-    // O (complete: the previous chunk's MMA was waited for).  Tensor-memory
+    // O (complete: O(c-1) finished before V(c) was dequantised).  Tensor-memory
     // loads and stores are warp-wide: a warp rescales when any of its lanes
     // must (alpha = 1 for the others).
     if (__any_sync(0xffffffffu, rescale)) {
@@ -507,24 +556,32 @@ sparse_prefill_kernel(Params p) {
       }
       tmem_wait_st();
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
+    publish();   // P(c), V(c), the rescaled O; S(c) has been read
 
-    // ---- 4. O += P . V ---------------------------------------------------------
     if (tid == 0) {
-      const uint32_t id = f16_idesc(128, kD);
-#pragma unroll
-      for (int ks2 = 0; ks2 < 4; ++ks2)
-        mma_f16(tO, sw128_desc(smem_u32(sP) + 32 * ks2), sw128_desc(smem_u32(sV) + 32 * ks2), id,
-                (c | ks2) ? 1u : 0u);
-      mma_commit(mbar);
+      issue_o(c);
+      if (c + 2 < C) {
+        fence_proxy_async_smem();   // stage c & 1 was last read by V(c)
+        issue(c + 2);
+      }
     }
-    if (__syncthreads_or(!wait_bounded(mbar, mma_phase & 1))) { dead = true; break; }
-    ++mma_phase;
-    tc_fence_after();
+    if (tid == 0 && c + 2 < C) issued = c + 3;
+    if (c + 1 < C) {
+      // K(c+1) while O(c) runs (S(c) is done, so sK is free).
+      if (cta_wait_failed(&full[(c + 1) & 1], ((c + 1) >> 1) & 1)) { dead = true; break; }
+      dequant_k(sStage + ((c + 1) & 1) * kStage);
+      publish();
+      if (tid == 0) issue_s();
+      // V(c+1) once O(c) has read sV; S(c+1) runs meanwhile.
+      if (cta_wait_failed(barO, phO & 1)) { dead = true; break; }
+      ++phO;
+      dequant_v(sStage + ((c + 1) & 1) * kStage);
+    } else {
+      if (cta_wait_failed(barO, phO & 1)) { dead = true; break; }
+      ++phO;
+    }
   }
+  tc_fence_after();
 
   if (dead) {
     if (tid == 0) atomicExch(p.status, kStatusWaitTimeout);
@@ -579,7 +636,7 @@ int prefill_rows_per_tile(const Geom& g) {
 size_t prefill_smem_bytes(const Geom& g, int k) {
   const int tr = prefill_rows_per_tile(g);
   const int ucap = min(g.MB, tr * k);
-  return (size_t)1024 + kQBytes + kKBytes + kVBytes + kPBytes + 2 * kStage + 3 * 8 + 4 + 8 * 4 +
+  return (size_t)1024 + kQBytes + kKBytes + kVBytes + kPBytes + 2 * kStage + 4 * 8 + 4 + 8 * 4 +
          (size_t)tr * k * 4 + (size_t)ucap * 8 + (size_t)((g.MB + 31) / 32) * 4;
 }
 
