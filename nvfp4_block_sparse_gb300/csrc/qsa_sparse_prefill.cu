@@ -366,6 +366,7 @@ sparse_prefill_kernel(Params p) {
   const int32_t* myrow = s_sel + jj * k;
 
   const uint64_t pol = policy_evict_first();
+  // Chunk c's four bulk copies (K codes, V codes, K scales, V scales).
   auto issue = [&](int c) {
     uint8_t* dst = sStage + (c & 1) * kStage;
     const int u = c >> csh, sub = c & csh;
@@ -485,6 +486,13 @@ sparse_prefill_kernel(Params p) {
     if (cta_wait_failed(barS, phS & 1)) { dead = true; break; }   // S(c) and all before it
     ++phS;
     tc_fence_after();
+    // Every thread is past V(c) (the barrier above), so chunk c's stage is
+    // free: request chunk c + 2 now, a whole chunk ahead of its use.
+    if (tid == 0 && c + 2 < C) {
+      fence_proxy_async_smem();
+      issue(c + 2);
+      issued = c + 3;
+    }
 
     // ---- softmax(c): masks, online softmax, P tile, O rescale ------------------
     const int ue = s_union[c >> csh];
@@ -506,10 +514,16 @@ sparse_prefill_kernel(Params p) {
         for (int i = 0; i < 64; ++i)
           if (tok0 + i >= nrow) z[i] = -INFINITY;
       }
-      float mx = z[0];
+      float mx8[8];           // eight independent chains, then a tree
 #pragma unroll
-      for (int i = 1; i < 64; ++i) mx = fmaxf(mx, z[i]);
-      cmax = mx * cq;         // cq > 0: the scale keeps the order
+      for (int i = 0; i < 8; ++i) mx8[i] = z[i];
+#pragma unroll
+      for (int i = 8; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], z[i]);
+#pragma unroll
+      for (int h = 4; h >= 1; h >>= 1)
+#pragma unroll
+        for (int i = 0; i < h; ++i) mx8[i] = fmaxf(mx8[i], mx8[i + h]);
+      cmax = mx8[0] * cq;     // cq > 0: the scale keeps the order
     }
     bool rescale = false;
     float alpha = 1.f;
@@ -524,15 +538,15 @@ sparse_prefill_kernel(Params p) {
     }
     uint32_t pk[32];
     if (member) {
-      float ls = 0.f;
+      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const float p0 = exp2_approx(fmaf(z[2 * i], cq, -m_base));
         const float p1 = exp2_approx(fmaf(z[2 * i + 1], cq, -m_base));
-        ls += p0 + p1;
+        ls4[i & 3] += p0 + p1;
         pk[i] = pack_half2(p0, p1);
       }
-      l_run = l_run * alpha + ls;
+      l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i) pk[i] = 0u;
@@ -558,14 +572,7 @@ sparse_prefill_kernel(Params p) {
     }
     publish();   // P(c), V(c), the rescaled O; S(c) has been read
 
-    if (tid == 0) {
-      issue_o(c);
-      if (c + 2 < C) {
-        fence_proxy_async_smem();   // stage c & 1 was last read by V(c)
-        issue(c + 2);
-      }
-    }
-    if (tid == 0 && c + 2 < C) issued = c + 3;
+    if (tid == 0) issue_o(c);
     if (c + 1 < C) {
       // K(c+1) while O(c) runs (S(c) is done, so sK is free).
       if (cta_wait_failed(&full[(c + 1) & 1], ((c + 1) >> 1) & 1)) { dead = true; break; }
