@@ -110,3 +110,28 @@ def test_no_cpu_fallback_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding._build, "LIB", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         binding.load()
+
+
+def test_context_row_groups_validation(lib):
+    # Long row groups: index scores / selection / row-tile attention accept up
+    # to 4096 rows per request; the decode attention keeps its 8.
+    long = geom(rows_per_req=512, num_q_heads=32, num_kv_heads=4)
+    assert qsa.qsa_sparse_prefill_workspace_bytes(long, 64) > 0
+    assert qsa.qsa_sparse_decode_workspace_bytes_ex(long, 64, 0) == 0
+    assert qsa.qsa_sparse_decode_workspace_bytes_ex(geom(rows_per_req=9), 8, 0) == 0
+    assert qsa.qsa_sparse_prefill_workspace_bytes(long, 0) == 0                    # k < 1
+    assert qsa.qsa_sparse_prefill_workspace_bytes(geom(head_dim=256, page_size=32), 8) == 0
+    assert qsa.qsa_sparse_prefill_workspace_bytes(
+        geom(num_q_heads=256, num_kv_heads=1), 8) == 0                            # G > 128
+    assert qsa.qsa_sparse_prefill_workspace_bytes(geom(rows_per_req=4097), 8) == 0
+    ws = qsa.qsa_sparse_prefill_workspace_bytes(long, 64)
+    args = [ctypes.byref(long)] + [FAKE] * 5
+    tail = [FAKE, FAKE, FAKE, 64, FAKE, FAKE, FAKE, ws, None]
+    # non-positive or non-finite scales are rejected before any launch
+    for ks, vs, sm in ((0.0, 1.0, 0.1), (1.0, 1.0, -0.1), (float("nan"), 1.0, 0.1),
+                       (1.0, float("inf"), 0.1)):
+        assert lib.qsa_sparse_prefill(*args, ks, vs, sm, *tail) == 1
+    # a missing or short workspace
+    good = [ctypes.byref(long)] + [FAKE] * 5 + [1.0, 1.0, 0.1, FAKE, FAKE, FAKE, 64, FAKE, FAKE]
+    assert lib.qsa_sparse_prefill(*good, None, ws, None) == 4
+    assert lib.qsa_sparse_prefill(*good, FAKE, ws - 1, None) == 4
