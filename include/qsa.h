@@ -367,7 +367,10 @@ qsa_status_t qsa_rollback_restore(const qsa_geom_t *geom, const int32_t *page_ta
  *               word), 256-byte aligned, zero-filled once by
  *               qsa_workspace_init().
  *
- * Returns QSA_ERR_UNSUPPORTED for head_dim != 128, more than 128 query heads
+ * head_dim 256 (the geometry above, 32-token pages) runs 32-token chunks with
+ * 512 tensor-memory columns per tile.
+ *
+ * Returns QSA_ERR_UNSUPPORTED for more than 128 query heads
  * per KV head, or a tile (floor(128 / G) rows x k selections plus their union)
  * beyond one CTA's shared memory; QSA_ERR_INVALID_ARG for null pointers, k <
  * 1, k_scale or sm_scale not positive and finite, v_scale not finite, pools /

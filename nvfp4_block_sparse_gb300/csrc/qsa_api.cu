@@ -246,13 +246,14 @@ qsa_status_t qsa_sparse_decode_ex(const qsa_geom_t* geom, const void* q_bf16,
                                              out_bf16, lse, workspace, true, stream));
 }
 
-// Context row groups: head_dim 128, a head group of at most 128 heads, and a
-// tile's selections + union within the CTA's shared memory.
+// Context row groups: head_dim 128 or 256, a head group of at most 128 heads,
+// and a tile's selections + union within the CTA's shared memory.
 qsa_status_t check_prefill_args(const qsa_geom_t* geom, int k) {
   qsa_status_t st = check_geom(geom, qsa::kMaxContextRows);
   if (st != QSA_OK) return st;
   if (k < 1) return QSA_ERR_INVALID_ARG;
-  if (k > qsa::kMaxK || geom->head_dim != 128) return QSA_ERR_UNSUPPORTED;
+  if (k > qsa::kMaxK || (geom->head_dim != 128 && geom->head_dim != 256))
+    return QSA_ERR_UNSUPPORTED;
   const Geom g = to_geom(geom);
   if (qsa::prefill_rows_per_tile(g) < 1) return QSA_ERR_UNSUPPORTED;
   if (qsa::prefill_smem_bytes(g, k) > 227 * 1024) return QSA_ERR_UNSUPPORTED;

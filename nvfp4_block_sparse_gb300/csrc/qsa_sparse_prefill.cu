@@ -42,16 +42,25 @@
 namespace qsa {
 namespace {
 
-constexpr int kD = 128;                 // head dim
-constexpr int kTok = 64;                // tokens per chunk
 constexpr int kThreads = 128;           // four warps: one thread per tile row
-constexpr int kStage = 2 * kTok * kD / 2 + 2 * kTok * kD / 16;   // 9216 B of NVFP4
-constexpr int kQBytes = 128 * kD * 2;   // Q tile, fp16: two 64-dim halves of 16 KB
-constexpr int kKBytes = kTok * kD * 2;  // K tile: two halves of 8 KB
-constexpr int kVBytes = kD * kTok * 2;  // V^T tile: 128 rows of 128 B
-constexpr int kPBytes = 128 * kTok * 2; // P tile: 128 rows of 128 B
-constexpr uint32_t kTmemCols = 256;     // S: columns [0, 64), O: [64, 192)
-constexpr uint32_t kOCol = 64;
+constexpr int kStage = 9216;            // NVFP4 bytes of one chunk (8192 K and V values)
+
+// Per head dim D: a chunk is 8192 / D tokens (64 at D = 128, 32 at D = 256).
+// Every fp16 tile is K-major in 64-element (128-byte) column blocks of rows.
+template <int D>
+struct PT {
+  static_assert(D == 128 || D == 256, "head_dim 128 or 256");
+  static constexpr int kTok = 8192 / D;           // tokens per chunk
+  static constexpr int kQBytes = 128 * D * 2;     // Q: D/64 blocks of 128 rows x 128 B
+  static constexpr int kKBlk = kTok * 128;        // one 64-dim block of the K tile
+  static constexpr int kKBytes = (D / 64) * kKBlk;
+  static constexpr int kVBytes = D * 128;         // V^T: D rows of 64 tokens (zero-padded)
+  static constexpr int kPBytes = 128 * 128;       // P: 128 rows of 64 tokens (zero-padded)
+  static constexpr uint32_t kTmemCols = D == 128 ? 256 : 512;
+  static constexpr uint32_t kOCol = D == 128 ? 64 : 256;   // S at column 0, O here
+};
+static_assert(2 * PT<128>::kTok * 128 / 2 + 2 * PT<128>::kTok * 128 / 16 == kStage, "stage");
+static_assert(2 * PT<256>::kTok * 256 / 2 + 2 * PT<256>::kTok * 256 / 16 == kStage, "stage");
 constexpr unsigned long long kWaitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -206,8 +215,11 @@ __device__ __forceinline__ bool row_holds(const int32_t* row, int k, int beta) {
   return lo < k && row[lo] == beta;
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 sparse_prefill_kernel(Params p) {
+  using T = PT<D>;
+  constexpr int kTok = T::kTok;
   const Geom& g = p.g;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int G = g.Hq / g.Hkv;
@@ -221,11 +233,11 @@ sparse_prefill_kernel(Params p) {
   // The swizzle atoms need 1024-byte alignment (one spare KB is allocated).
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem;                           // 32 KB
-  uint8_t* sK = sQ + kQBytes;                   // 16 KB
-  uint8_t* sV = sK + kKBytes;                   // 16 KB
-  uint8_t* sP = sV + kVBytes;                   // 16 KB
-  uint8_t* sStage = sP + kPBytes;               // 2 x 9216 B
+  uint8_t* sQ = smem;                           // 32 / 64 KB
+  uint8_t* sK = sQ + T::kQBytes;                // 16 KB
+  uint8_t* sV = sK + T::kKBytes;                // 16 / 32 KB
+  uint8_t* sP = sV + T::kVBytes;                // 16 KB
+  uint8_t* sStage = sP + T::kPBytes;            // 2 x 9216 B
   uint64_t* full = reinterpret_cast<uint64_t*>(sStage + 2 * kStage);
   uint64_t* barS = full + 2;                    // S = Q K^T complete
   uint64_t* barO = full + 3;                    // O += P V complete
@@ -248,7 +260,7 @@ sparse_prefill_kernel(Params p) {
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(s_tmem)),
-                 "r"(kTmemCols));
+                 "r"(T::kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
 
@@ -261,16 +273,16 @@ sparse_prefill_kernel(Params p) {
   const int nrow = vec ? visible_tokens(L, g.R, j, cap) : 0;
   float cq = 0.f;                               // logit scale, log2 domain
   {
-    uint4 raw[16];
+    // Two passes over the row (L1/L2-resident the second time): the maximum,
+    // then the scaled fp16 copy into 16-byte chunks of the swizzled tile.
     const size_t qrow = ((size_t)b * g.R + j) * g.Hq + (size_t)kvh * G + hh;
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow * D);
     float amax = 0.f;
     if (vec) {
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow * kD);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) raw[i] = src[i];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll 4
+      for (int i = 0; i < D / 8; ++i) {
+        const uint4 r = src[i];
+        const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           amax = fmaxf(amax, fabsf(__uint_as_float(w4[u] << 16)));
@@ -284,11 +296,12 @@ sparse_prefill_kernel(Params p) {
     const float up = __uint_as_float((uint32_t)(sq + 127) << 23);
     const float down = __uint_as_float((uint32_t)(127 - sq) << 23);
     cq = p.k_scale * p.sm_scale * kLog2e * down;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
+#pragma unroll 4
+    for (int i = 0; i < D / 8; ++i) {
       uint4 h = make_uint4(0u, 0u, 0u, 0u);
       if (vec) {
-        const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+        const uint4 r = src[i];
+        const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
         uint32_t o[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u)
@@ -296,9 +309,15 @@ sparse_prefill_kernel(Params p) {
                             __uint_as_float(w4[u] & 0xFFFF0000u) * up);
         h = make_uint4(o[0], o[1], o[2], o[3]);
       }
-      // dims 8i..8i+7: half i / 8, 16-byte chunk i % 8 of row tid
-      *reinterpret_cast<uint4*>(sQ + (i >> 3) * (kQBytes / 2) + sw128(tid, i & 7)) = h;
+      // dims 8i..8i+7: column block i / 8, 16-byte chunk i % 8 of row tid
+      *reinterpret_cast<uint4*>(sQ + (i >> 3) * 16384 + sw128(tid, i & 7)) = h;
     }
+  }
+  // Tokens past a chunk (D = 256: 32 of the 64 token slots of the P and V^T
+  // tiles) stay zero: the tiles are cleared once and those slots never written.
+  if (kTok < 64) {
+    for (int i = tid; i < (T::kVBytes + T::kPBytes) / 16; i += kThreads)
+      reinterpret_cast<uint4*>(sV)[i] = make_uint4(0u, 0u, 0u, 0u);
   }
 
   // ---- the tile's rows' selections and their union ----------------------------
@@ -372,45 +391,49 @@ sparse_prefill_kernel(Params p) {
     const int u = c >> csh, sub = c & csh;
     const size_t row0 = ((size_t)s_upage[u] * g.Hkv + kvh) * g.P + (size_t)sub * kTok;
     mbar_arrive_expect_tx(&full[c & 1], kStage);
-    bulk_g2s(dst, p.k_pool + row0 * (kD / 2), kTok * kD / 2, &full[c & 1], pol);
-    bulk_g2s(dst + kTok * kD / 2, p.v_pool + row0 * (kD / 2), kTok * kD / 2, &full[c & 1], pol);
-    bulk_g2s(dst + kTok * kD, p.k_sf + row0 * (kD / 16), kTok * kD / 16, &full[c & 1], pol);
-    bulk_g2s(dst + kTok * kD + kTok * kD / 16, p.v_sf + row0 * (kD / 16), kTok * kD / 16,
+    bulk_g2s(dst, p.k_pool + row0 * (D / 2), kTok * D / 2, &full[c & 1], pol);
+    bulk_g2s(dst + kTok * D / 2, p.v_pool + row0 * (D / 2), kTok * D / 2, &full[c & 1], pol);
+    bulk_g2s(dst + kTok * D, p.k_sf + row0 * (D / 16), kTok * D / 16, &full[c & 1], pol);
+    bulk_g2s(dst + kTok * D + kTok * D / 16, p.v_sf + row0 * (D / 16), kTok * D / 16,
              &full[c & 1], pol);
   };
-  const uint32_t tS = tmem, tO = tmem + kOCol;
+  const uint32_t tS = tmem, tO = tmem + T::kOCol;
   const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
 
   // ---- stage helpers ---------------------------------------------------------
   // K rows = tokens (two 64-dim halves), V^T rows = dims; 8 pieces per thread.
   auto dequant_k = [&](const uint8_t* st) {
     const uint8_t* kc = st;
-    const uint8_t* ks = st + kTok * kD;
+    const uint8_t* ks = st + kTok * D;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int pc = tid + kThreads * i;      // (token, 8-dim group)
-      const int t = pc >> 4, c8 = pc & 15;
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(kc + t * 64 + c8 * 4);
-      const uint32_t s = e4m3x2_to_f16x2(ks[t * 8 + (c8 >> 1)]);
-      *reinterpret_cast<uint4*>(sK + (c8 >> 3) * (kKBytes / 2) + sw128(t, c8 & 7)) =
+      const int t = pc / (D / 8), c8 = pc % (D / 8);
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(kc + t * (D / 2) + c8 * 4);
+      const uint32_t s = e4m3x2_to_f16x2(ks[t * (D / 16) + (c8 >> 1)]);
+      *reinterpret_cast<uint4*>(sK + (c8 >> 3) * T::kKBlk + sw128(t, c8 & 7)) =
           dequant8(w, prmt(s, 0, 0x1010));
     }
   };
   auto dequant_v = [&](const uint8_t* st) {
-    const uint8_t* vc = st + kTok * kD / 2;
-    const uint8_t* vs = st + kTok * kD + kTok * kD / 16;
-    // 8 tokens x 8 dims per thread: lane = dim group (16) + half-warp bit, the
-    // two half-warps on neighbouring 8-token groups.  The upper half loads each
-    // token pair in swapped order, so that one load instruction touches tokens
-    // of both parities: 32 distinct banks (token rows are 64 B apart).
-    const int lane = tid & 31, hw = lane >> 4;
-    const int c8 = lane & 15, tg = 2 * warp + hw;
+    const uint8_t* vc = st + kTok * D / 2;
+    const uint8_t* vs = st + kTok * D + kTok * D / 16;
+    // 8 tokens x 8 dims per thread.  D = 128: lane = dim group (16) +
+    // half-warp bit, the two half-warps on neighbouring 8-token groups; the
+    // upper half loads each token pair in swapped order, so that one load
+    // instruction touches tokens of both parities (32 distinct banks: token
+    // rows are 64 B apart).  D = 256: warp w takes dim groups 8w..8w+7, lane
+    // bits 3-4 the 8-token group.
+    const int lane = tid & 31;
+    const int hw = D == 128 ? lane >> 4 : 0;
+    const int c8 = D == 128 ? lane & 15 : 8 * warp + (lane & 7);
+    const int tg = D == 128 ? 2 * warp + hw : lane >> 3;
     uint32_t X[8], sf[8];   // X[u]: token 8*tg + (u ^ hw)
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int t = 8 * tg + (u ^ hw);
-      X[u] = *reinterpret_cast<const uint32_t*>(vc + t * 64 + c8 * 4);
-      sf[u] = vs[t * 8 + (c8 >> 1)];
+      X[u] = *reinterpret_cast<const uint32_t*>(vc + t * (D / 2) + c8 * 4);
+      sf[u] = vs[t * (D / 16) + (c8 >> 1)];
     }
     uint32_t rowv[8][4];   // [dim e][token pair]
 #pragma unroll
@@ -442,16 +465,16 @@ sparse_prefill_kernel(Params p) {
   auto issue_s = [&]() {       // S = Q . K^T, then the S barrier
     const uint32_t id = f16_idesc(128, kTok);
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+    for (int h = 0; h < D / 64; ++h)
 #pragma unroll
       for (int ks2 = 0; ks2 < 4; ++ks2)
-        mma_f16(tS, sw128_desc(smem_u32(sQ + h * (kQBytes / 2)) + 32 * ks2),
-                sw128_desc(smem_u32(sK + h * (kKBytes / 2)) + 32 * ks2), id,
+        mma_f16(tS, sw128_desc(smem_u32(sQ + h * 16384) + 32 * ks2),
+                sw128_desc(smem_u32(sK + h * T::kKBlk) + 32 * ks2), id,
                 (h | ks2) ? 1u : 0u);
     mma_commit(barS);
   };
-  auto issue_o = [&](int c) {  // O += P . V, then the O barrier
-    const uint32_t id = f16_idesc(128, kD);
+  auto issue_o = [&](int c) {  // O += P . V (64 token slots), then the O barrier
+    const uint32_t id = f16_idesc(128, D);
 #pragma unroll
     for (int ks2 = 0; ks2 < 4; ++ks2)
       mma_f16(tO, sw128_desc(smem_u32(sP) + 32 * ks2), sw128_desc(smem_u32(sV) + 32 * ks2), id,
@@ -498,9 +521,9 @@ sparse_prefill_kernel(Params p) {
     const int ue = s_union[c >> csh];
     const int tok0 = ue * g.P + (c & csh) * kTok;
     const bool member = vec && tok0 < nrow && row_holds(myrow, k, ue);
-    float z[64];
+    float z[kTok];
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
+    for (int q4 = 0; q4 < kTok / 16; ++q4) {
       float v16[16];
       tmem_ld16(tS + lane_off + 16 * q4, v16);
 #pragma unroll
@@ -511,14 +534,14 @@ sparse_prefill_kernel(Params p) {
     if (member) {
       if (tok0 + kTok > nrow) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
+        for (int i = 0; i < kTok; ++i)
           if (tok0 + i >= nrow) z[i] = -INFINITY;
       }
       float mx8[8];           // eight independent chains, then a tree
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx8[i] = z[i];
 #pragma unroll
-      for (int i = 8; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], z[i]);
+      for (int i = 8; i < kTok; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], z[i]);
 #pragma unroll
       for (int h = 4; h >= 1; h >>= 1)
 #pragma unroll
@@ -536,11 +559,11 @@ sparse_prefill_kernel(Params p) {
         rescale = true;
       }
     }
-    uint32_t pk[32];
+    uint32_t pk[kTok / 2];
     if (member) {
       float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < kTok / 2; ++i) {
         const float p0 = exp2_approx(fmaf(z[2 * i], cq, -m_base));
         const float p1 = exp2_approx(fmaf(z[2 * i + 1], cq, -m_base));
         ls4[i & 3] += p0 + p1;
@@ -549,10 +572,10 @@ sparse_prefill_kernel(Params p) {
       l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
     } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) pk[i] = 0u;
+      for (int i = 0; i < kTok / 2; ++i) pk[i] = 0u;
     }
 #pragma unroll
-    for (int c16 = 0; c16 < 8; ++c16)
+    for (int c16 = 0; c16 < kTok / 8; ++c16)
       *reinterpret_cast<uint4*>(sP + sw128(tid, c16)) =
           make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
     // O (complete: O(c-1) finished before V(c) was dequantised).  Tensor-memory
@@ -560,7 +583,7 @@ sparse_prefill_kernel(Params p) {
     // must (alpha = 1 for the others).
     if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-      for (int q8 = 0; q8 < 8; ++q8) {
+      for (int q8 = 0; q8 < D / 16; ++q8) {
         float o16[16];
         tmem_ld16(tO + lane_off + 16 * q8, o16);
         tmem_wait_ld();
@@ -602,11 +625,11 @@ sparse_prefill_kernel(Params p) {
   // chunk was visited, and rows without a token write zeros)
   if (!dead) {
     const size_t orow = ((size_t)b * g.R + j) * g.Hq + (size_t)kvh * G + hh;
-    uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kD);
+    uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D);
     const bool has = l_run > 0.f && C > 0;
     const float sc = has ? p.v_scale / l_run : 0.f;
-#pragma unroll
-    for (int q8 = 0; q8 < 8; ++q8) {
+#pragma unroll 4
+    for (int q8 = 0; q8 < D / 16; ++q8) {
       float o16[16];
       if (C > 0) {
         tmem_ld16(tO + lane_off + 16 * q8, o16);
@@ -630,7 +653,7 @@ sparse_prefill_kernel(Params p) {
   __syncthreads();
   if (warp == 0)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(kTmemCols));
+                 "r"(T::kTmemCols));
 }
 
 }  // namespace
@@ -643,7 +666,10 @@ int prefill_rows_per_tile(const Geom& g) {
 size_t prefill_smem_bytes(const Geom& g, int k) {
   const int tr = prefill_rows_per_tile(g);
   const int ucap = min(g.MB, tr * k);
-  return (size_t)1024 + kQBytes + kKBytes + kVBytes + kPBytes + 2 * kStage + 4 * 8 + 4 + 8 * 4 +
+  const size_t tiles = g.D == 256
+                           ? (size_t)PT<256>::kQBytes + PT<256>::kKBytes + PT<256>::kVBytes + PT<256>::kPBytes
+                           : (size_t)PT<128>::kQBytes + PT<128>::kKBytes + PT<128>::kVBytes + PT<128>::kPBytes;
+  return (size_t)1024 + tiles + 2 * kStage + 4 * 8 + 4 + 8 * 4 +
          (size_t)tr * k * 4 + (size_t)ucap * 8 + (size_t)((g.MB + 31) / 32) * 4;
 }
 
@@ -665,8 +691,9 @@ cudaError_t launch_sparse_prefill(const Geom& g, const void* q, const uint8_t* k
   prm.lse = lse;
   prm.status = status;
   const size_t smem = prefill_smem_bytes(g, k);
-  cudaError_t e = cudaFuncSetAttribute(sparse_prefill_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto* kern = g.D == 256 ? sparse_prefill_kernel<256> : sparse_prefill_kernel<128>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((g.R + prm.tr - 1) / prm.tr, g.Hkv, g.B);
@@ -678,7 +705,7 @@ cudaError_t launch_sparse_prefill(const Geom& g, const void* q, const uint8_t* k
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 0;
-  return cudaLaunchKernelEx(&cfg, sparse_prefill_kernel, prm);
+  return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
 }  // namespace qsa

@@ -104,10 +104,14 @@ CONFIGS = [
     Case("context prefill", seed=6, batch=2, rows_per_req=512, num_q_heads=32,
          num_kv_heads=4, page_size=64, ctx_lo=32768, ctx_hi=32768, k=64,
          window=4, max_blocks=512, pool="perm", iq_row_noise=24),
+    Case("head_dim-256 context prefill", seed=7, batch=4, rows_per_req=256,
+         num_q_heads=24, num_kv_heads=2, page_size=32, ctx_lo=16384, ctx_hi=16384,
+         k=64, window=4, max_blocks=512, pool="perm", iq_row_noise=24,
+         head_dim=256),
 ]
 
 # Workloads whose rows are context row groups (served by the row-tile path).
-PREFILL_CONFIGS = (6,)
+PREFILL_CONFIGS = (6, 7)
 
 
 def small(case: Case, batch: Optional[int] = None, ctx_lo: Optional[int] = None,

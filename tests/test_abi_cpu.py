@@ -120,7 +120,8 @@ def test_context_row_groups_validation(lib):
     assert qsa.qsa_sparse_decode_workspace_bytes_ex(long, 64, 0) == 0
     assert qsa.qsa_sparse_decode_workspace_bytes_ex(geom(rows_per_req=9), 8, 0) == 0
     assert qsa.qsa_sparse_prefill_workspace_bytes(long, 0) == 0                    # k < 1
-    assert qsa.qsa_sparse_prefill_workspace_bytes(geom(head_dim=256, page_size=32), 8) == 0
+    assert qsa.qsa_sparse_prefill_workspace_bytes(geom(head_dim=256, page_size=32), 8) > 0
+    assert qsa.qsa_sparse_prefill_workspace_bytes(geom(head_dim=256, page_size=128), 8) == 0
     assert qsa.qsa_sparse_prefill_workspace_bytes(
         geom(num_q_heads=256, num_kv_heads=1), 8) == 0                            # G > 128
     assert qsa.qsa_sparse_prefill_workspace_bytes(geom(rows_per_req=4097), 8) == 0

@@ -81,6 +81,17 @@ CASES = {
     # one KV head, 128 query heads per KV head: one row per tile
     "mqa_g128": _case(num_q_heads=128, num_kv_heads=1, rows_per_req=9, ctx_lo=1500,
                       ctx_hi=1500, max_blocks=24),
+    # head_dim 256 (32-token chunks, 512 tensor-memory columns): the pages'
+    # geometry (12 heads per KV head, 10-row tiles, 32-token pages), 64-token
+    # pages with 8 heads, invalid pages and ties
+    "hd256_g12_p32": _case(head_dim=256, page_size=32, num_q_heads=24, num_kv_heads=2,
+                           rows_per_req=23, ctx_lo=1500, ctx_hi=1700, batch=2, max_blocks=54,
+                           k=12),
+    "hd256_g8_p64_ragged": _case(head_dim=256, num_q_heads=16, num_kv_heads=2, batch=2,
+                                 rows_per_req=37, ctx_lo=2400, ctx_hi=3100),
+    "hd256_invalid_ties": _case(head_dim=256, page_size=32, num_q_heads=8, num_kv_heads=1,
+                                rows_per_req=24, ctx_lo=1200, ctx_hi=1400, max_blocks=44,
+                                k=10, invalid_frac=0.15, tie_frac=0.3),
 }
 
 
@@ -121,14 +132,17 @@ def test_prefill_on_verify_rows_matches_decode(qsa):
     assert (lse[fin] - step.lse[fin]).abs().max().item() <= 2 * LSE_ABS
 
 
-def test_prefill_full_size_sampled_rows(qsa):
-    case = qw.CONFIGS[6]
+@pytest.mark.parametrize("cfg", qw.PREFILL_CONFIGS)
+def test_prefill_full_size_sampled_rows(qsa, cfg):
+    case = qw.CONFIGS[cfg]
     w = qw.make_workload(case, "cuda")
     step = run_step(qsa, w)
     w_np = qw.to_numpy(w)
-    R = case.rows_per_req
+    R, T = case.rows_per_req, case.rows
+    tr = 128 // (case.num_q_heads // case.num_kv_heads)
     # a tile at the start, one in the middle, the last rows of the last request
-    for r0, r1 in ((0, 16), (R + 248, R + 264), (2 * R - 16, 2 * R)):
+    mid = R + (R // 2 // tr) * tr
+    for r0, r1 in ((0, tr), (mid, mid + tr), (T - tr, T)):
         check(step, w_np, rows=(r0, r1))
 
 
