@@ -67,15 +67,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait: gives up after `limit` probes (each probe may suspend the
-// thread for a hardware-chosen interval) and returns false.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  uint32_t limit) {
-  for (uint32_t i = 0; i < limit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
-
 // Contiguous global -> shared copy on the TMA engine; completion is signalled
 // as transaction bytes on `bar`.  dst, src and bytes must be 16-byte aligned.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
@@ -102,15 +93,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // ---------------------------------------------------------------------------
 // NVFP4 element conversion
 // ---------------------------------------------------------------------------
-
-// Two e2m1 codes (low nibble -> low half) to two fp16 values.
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-      : "=r"(r)
-      : "r"(byte));
-  return r;
-}
 
 // Two e4m3 bytes (low byte -> low half) to two fp16 values.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {

@@ -546,9 +546,6 @@ int blocks_per_warp_for(const Geom& g) {
   const long long warps_needed = (long long)g.B * g.MB;
   const long long warp_slots = (long long)sms * 4 * kWarps;
   int bpw = (int)((warps_needed + warp_slots - 1) / warp_slots);
-#ifdef QSA_INDEX_MIN_BPW
-  if (bpw < QSA_INDEX_MIN_BPW) bpw = QSA_INDEX_MIN_BPW;
-#endif
   return bpw < 1 ? 1 : (bpw > 4 ? 4 : bpw);
 }
 
