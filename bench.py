@@ -608,13 +608,13 @@ def run_e2e(qsa, step, reps, stream, args, dev, T, world):
     to the device, runs the three calls, and reads out + lse back.  The NVFP4
     K/V pages and index keys are the cache: resident in HBM.
 
-    Steps are pipelined as a serving loop runs them: step i+1's inputs are
-    copied in (input stream) and step i-1's results copied out (output
-    stream) while step i computes (compute stream), with two DecodeStep
-    result buffers in turn; every step still moves its own inputs in and its
-    own results out inside the timed region.  The loop is captured as CUDA
-    graphs of 2 * replicas steps (forked and joined on the compute stream)
-    and replayed back to back."""
+    Steps are pipelined as a serving loop runs them: the inputs of a group of
+    steps (about 1 MB) are copied in on an input stream ahead of the group,
+    and each step's results are copied out on an output stream as soon as it
+    is done, while the next steps compute; every step still moves its own
+    inputs in and its own results out inside the timed region.  The loop is
+    captured as CUDA graphs of 2 * replicas steps (forked and joined on the
+    compute stream) and replayed back to back."""
     # A step's query-side inputs travel as one pinned host buffer into one
     # device buffer whose 256-byte-aligned slices are the step's tensors; the
     # results (out, then lse) come back in one copy of DecodeStep.results.
@@ -636,38 +636,49 @@ def run_e2e(qsa, step, reps, stream, args, dev, T, world):
         db.copy_(hb)
         host.append(hb)
         dev_in.append(db)
-    steps = [step, qsa.DecodeStep(step.geom, step.k, step.window, device=dev,
-                                  num_splits=step.num_splits, fused=step.fused)]
-    res_h = [torch.empty(step.results.shape, dtype=torch.uint8).pin_memory() for _ in range(2)]
-    h2d = total
-    d2h = res_h[0].numel()
     nrep = len(reps)
-    per_graph = 2 * nrep                 # replicas and result buffers both cycle
+    per_graph = 2 * nrep                 # every replica twice per graph
+    # One device result span (out, then lse) and one pinned host span per step
+    # of a graph, so that no step waits for an earlier step's result copy.
+    rbytes = step.results.numel()
+    rstride = (rbytes + 255) // 256 * 256    # every span 256-byte aligned
+    out_bytes = step.out.numel() * step.out.element_size()
+    lse_off = (out_bytes + 255) // 256 * 256
+    res_d = torch.empty((per_graph, rstride), dtype=torch.uint8, device=dev)[:, :rbytes]
+    res_h = torch.empty((per_graph, rstride), dtype=torch.uint8).pin_memory()[:, :rbytes]
+    outs = [res_d[i, :out_bytes].view(torch.bfloat16).view(step.out.shape) for i in range(per_graph)]
+    lses = [res_d[i, lse_off:].view(torch.float32).view(step.lse.shape) for i in range(per_graph)]
+    h2d = total
+    d2h = rbytes
     s_in = torch.cuda.Stream(device=dev)
     s_out = torch.cuda.Stream(device=dev)
 
+    # Inputs go in groups of about 1 MB of steps: the compute stream waits once
+    # per group (consecutive steps of a group keep their programmatic-launch
+    # overlap), and a large step's inputs are not queued behind its group's.
+    grp = max(1, min(nrep, (1 << 20) // max(1, total)))
+
     def body():
-        ev_in = [torch.cuda.Event() for _ in range(per_graph)]
         ev_run = [torch.cuda.Event() for _ in range(per_graph)]
-        ev_out = [torch.cuda.Event() for _ in range(per_graph)]
         s_in.wait_stream(stream)
         s_out.wait_stream(stream)
-        for i in range(per_graph):
-            r, b = i % nrep, i % 2
-            with torch.cuda.stream(s_in):
-                if i >= nrep:
-                    s_in.wait_event(ev_run[i - nrep])     # the replica's inputs are free
-                dev_in[r].copy_(host[r], non_blocking=True)
-                ev_in[i].record(s_in)
-            stream.wait_event(ev_in[i])
-            if i >= 2:
-                stream.wait_event(ev_out[i - 2])          # the result buffer was read
-            steps[b].run(reps[r], stream=stream)
-            ev_run[i].record(stream)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_run[i])
-                res_h[b].copy_(steps[b].results, non_blocking=True)
-                ev_out[i].record(s_out)
+        for half in range(2):
+            for g0 in range(0, nrep, grp):
+                ev_in = torch.cuda.Event()
+                with torch.cuda.stream(s_in):
+                    for r in range(g0, min(nrep, g0 + grp)):
+                        if half:
+                            s_in.wait_event(ev_run[r])    # replica r's inputs are free
+                        dev_in[r].copy_(host[r], non_blocking=True)
+                    ev_in.record(s_in)
+                stream.wait_event(ev_in)
+                for r in range(g0, min(nrep, g0 + grp)):
+                    i = half * nrep + r
+                    step.run(reps[r], stream=stream, out=outs[i], lse=lses[i])
+                    ev_run[i].record(stream)
+                    with torch.cuda.stream(s_out):
+                        s_out.wait_event(ev_run[i])
+                        res_h[i].copy_(res_d[i], non_blocking=True)
         stream.wait_stream(s_in)
         stream.wait_stream(s_out)
 
@@ -679,11 +690,9 @@ def run_e2e(qsa, step, reps, stream, args, dev, T, world):
             body()
         g.replay()
         stream.synchronize()
-        # The pipelined results are the steps' own: the last two result copies
-        # equal the two buffers they were read from.
-        for b in range(2):
-            if not torch.equal(res_h[b], steps[b].results.cpu()):
-                raise RuntimeError("pipelined result copy differs from its step's results")
+        # Every step's result copy equals that step's device results.
+        if not torch.equal(res_h, res_d.cpu()):
+            raise RuntimeError("pipelined result copies differ from the steps' results")
         replays = max(1, -(-min(args.steps, 2000) // per_graph))
         if world > 1:
             torch.distributed.barrier()
@@ -698,7 +707,9 @@ def run_e2e(qsa, step, reps, stream, args, dev, T, world):
     ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     return {"value": job_rows_per_second(world, T, n, ms), "unit": "rows/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
-            "pipelined": "inputs of step i+1 in and results of step i-1 out during step i"}
+            "pipelined": "inputs copied in per ~1 MB group of steps ahead of the group; "
+                         "each step's results copied out while the next steps run",
+            "input_group_steps": grp}
 
 
 def main():

@@ -77,9 +77,13 @@ class DecodeStep:
         self.workspace = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
         qsa_workspace_init(self.workspace)
 
-    def run(self, w: dict, stream=None, sm_scale=None):
-        """One step over workload tensors ``w`` (the generator's layout)."""
+    def run(self, w: dict, stream=None, sm_scale=None, out=None, lse=None):
+        """One step over workload tensors ``w`` (the generator's layout).
+        ``out`` / ``lse`` (optional) receive the results instead of the step's
+        own buffers, e.g. one span per step of a pipelined serving loop."""
         sm = float(w["sm_scale"]) if sm_scale is None else float(sm_scale)
+        out = self.out if out is None else out
+        lse = self.lse if lse is None else lse
         qsa_index_scores(self.cg, w["iq"], w["ik_pool"], w["page_table"], w["seqlens"],
                          self.scores, stream)
         if self.prefill:
@@ -87,19 +91,19 @@ class DecodeStep:
                             self.nsel, stream)
             qsa_sparse_prefill(self.cg, w["q"], w["k_pool"], w["k_sf"], w["v_pool"], w["v_sf"],
                                w["k_scale"], w["v_scale"], sm, w["page_table"], w["seqlens"],
-                               self.sel, self.k, self.out, self.lse, self.workspace, stream)
+                               self.sel, self.k, out, lse, self.workspace, stream)
         elif not self.fused:
             qsa_select_topk(self.cg, self.scores, w["seqlens"], self.k, self.window, self.sel,
                             self.nsel, stream)
             qsa_sparse_decode_ex(self.cg, w["q"], w["k_pool"], w["k_sf"], w["v_pool"],
                                  w["v_sf"], w["k_scale"], w["v_scale"], sm, w["page_table"],
-                                 w["seqlens"], self.sel, self.k, self.out, self.lse,
+                                 w["seqlens"], self.sel, self.k, out, lse,
                                  self.workspace, self.num_splits, stream)
         else:
             qsa_select_sparse_decode(self.cg, self.scores, self.window, w["q"], w["k_pool"],
                                      w["k_sf"], w["v_pool"], w["v_sf"], w["k_scale"],
                                      w["v_scale"], sm, w["page_table"], w["seqlens"], self.k,
-                                     self.sel, self.nsel, self.out, self.lse, self.workspace,
+                                     self.sel, self.nsel, out, lse, self.workspace,
                                      self.num_splits, stream)
         return self
 
