@@ -615,3 +615,29 @@ def test_rollback_saved_layout(cfg):
                                       w["v_sf"].reshape(-1, Hkv, P, f)[page, g, pos % P])
     np.testing.assert_array_equal(s[Hkv * per:].view(np.int8),
                                   w["ik_pool"].reshape(-1, P, 64)[page, pos % P])
+
+
+# ---------------------------------------------------------------------------
+# context row groups reduce to single rows
+# ---------------------------------------------------------------------------
+
+def test_row_group_rows_equal_single_rows():
+    # Row j of a request with R rows and L cached tokens sees L - R + 1 + j
+    # tokens; scored, selected and attended alone (one row, that length) it
+    # must give exactly the same scores, selection and outputs.
+    case = _tiny_case(R=24, B=1, lo=1500, hi=1500, P=64, Hq=4, Hkv=2, k=6, W=2)
+    w = qw.to_numpy(qw.make_workload(case, "cpu"))
+    ref = oracle.step(w)
+    R, L = w["rows_per_req"], int(w["seqlens"][0])
+    for j in (0, 1, 11, R - 2, R - 1):
+        w1 = dict(w)
+        w1["rows_per_req"] = 1
+        w1["seqlens"] = np.array([L - R + 1 + j], dtype=np.int32)
+        w1["q"] = w["q"][j:j + 1]
+        w1["iq"] = w["iq"][j:j + 1]
+        one = oracle.step(w1)
+        np.testing.assert_array_equal(one["scores"][0], ref["scores"][j])
+        np.testing.assert_array_equal(one["sel"][0], ref["sel"][j])
+        np.testing.assert_array_equal(one["nsel"][0], ref["nsel"][j])
+        np.testing.assert_array_equal(one["out"][0], ref["out"][j])
+        np.testing.assert_array_equal(one["lse"][0], ref["lse"][j])
