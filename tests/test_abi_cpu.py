@@ -136,3 +136,22 @@ def test_context_row_groups_validation(lib):
     good = [ctypes.byref(long)] + [FAKE] * 5 + [1.0, 1.0, 0.1, FAKE, FAKE, FAKE, 64, FAKE, FAKE]
     assert lib.qsa_sparse_prefill(*good, None, ws, None) == 4
     assert lib.qsa_sparse_prefill(*good, FAKE, ws - 1, None) == 4
+
+
+def test_prologue_and_rollback_row_limits(lib):
+    # The prologue stores context row groups (up to 4096 rows per request);
+    # the rollback serves speculative rows (up to 8).
+    ok_long = geom(rows_per_req=512, num_q_heads=32, num_kv_heads=4)
+    too_long = geom(rows_per_req=4097)
+    st = lib.qsa_store_kv_tokens(ctypes.byref(too_long), FAKE, FAKE, FAKE, 1.0, 1.0,
+                                 FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None)
+    assert st == 2
+    # (every call here is rejected by host validation before any launch: the
+    # pointers are placeholders)
+    assert lib.qsa_rollback_state_bytes(ctypes.byref(ok_long)) == 0
+    assert lib.qsa_rollback_state_bytes(ctypes.byref(geom(rows_per_req=9))) == 0
+    assert lib.qsa_rollback_gather(ctypes.byref(geom(rows_per_req=9)), *([FAKE] * 8), None) == 2
+    # non-positive scales are rejected by the prologue
+    st = lib.qsa_store_kv_tokens(ctypes.byref(geom()), FAKE, FAKE, FAKE, 0.0, 1.0,
+                                 FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None)
+    assert st == 1
