@@ -1,16 +1,23 @@
-"""Benchmark: QSA block-sparse GQA decode step (index scores -> canonical top-k
--> split-KV sparse decode over NVFP4 pages) on one GB300, as query rows/s and
-achieved HBM bandwidth.
+"""Benchmark: QSA block-sparse GQA decode / verify step (index scores ->
+canonical top-k -> split-KV sparse attention over NVFP4 pages) on one GB300,
+as query rows/s and achieved HBM bandwidth.
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl qsa|reference]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--config C]
+                [--per-config 1,2,3,4] [--impl qsa|reference]
 
-Prints one JSON line (rank 0).  A step is one pass of all three kernels over
-one batch of synthetic, seeded input (the "batched decode" workload by
-default).  Steps rotate over input replicas held in distinct HBM buffers whose
-touched bytes add up to at least 4x the L2 size, so every step reads HBM.
-Timing: CUDA graph replays bracketed by CUDA events on the launching stream,
-with a barrier and synchronize on both sides; per-kernel durations come from
-event-record nodes around each kernel in a second, separately timed pass.
+Prints one JSON line (rank 0).  A step is one pass of the whole path over one
+batch of synthetic, seeded input; the headline workload is the wide
+aggregated verify workload (the largest of the target set), and every other
+workload of the set is measured the same way into ``per_config``.  Steps
+rotate over input replicas held in distinct HBM buffers whose touched bytes
+add up to at least 4x the L2 size, so every step reads HBM.
+
+Timing: exactly K steps as CUDA graph replays (one step per replica) with CUDA
+events on the launching stream between replays, a barrier and synchronize on
+both sides; ``steady`` adds the median over many replays.  Per call: the call
+alone on every replica back to back in one graph (median over replays,
+divided by the replicas; the roofline uses this), and the same call isolated
+between CUDA event nodes.
 """
 from __future__ import annotations
 
@@ -284,25 +291,6 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def traffic_record(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel source changed since the counters were taken."""
-    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
-    if not os.path.exists(path):
-        return None
-    src = os.path.join(ROOT, "nvfp4_block_sparse_gb300", "csrc", kernel + ".cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] if os.path.exists(src) else ""
-    with open(path) as f:
-        for line in f:
-            if line.startswith("#") or not line.strip():
-                continue
-            parts = line.split("|")
-            if len(parts) >= 4 and parts[0].strip() == kernel and parts[1].strip() == workload:
-                if parts[3].strip() == sha:
-                    return float(parts[2])
-    return None
-
-
 # ---------------------------------------------------------------------------
 # reference arm: the CPU oracle, timed on host cores
 # ---------------------------------------------------------------------------
@@ -383,6 +371,252 @@ def make_events(n):
         return None
 
 
+def ncu_record(kernel: str, workload: str):
+    """(DRAM bytes, device us) per launch from the committed ncu summary, or
+    (None, None) when the kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None, None
+    src = os.path.join(ROOT, "nvfp4_block_sparse_gb300", "csrc", kernel + ".cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] if os.path.exists(src) else ""
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            parts = [x.strip() for x in line.split("|")]
+            if len(parts) >= 4 and parts[0] == kernel and parts[1] == workload and parts[3] == sha:
+                us = float(parts[4]) if len(parts) >= 5 and parts[4] else None
+                return float(parts[2]), us
+    return None, None
+
+
+# The library source that holds each timed call's dominant kernel.
+KERNEL_SOURCE = {"index_scores": "qsa_index_scores", "select_topk": "qsa_select_topk",
+                 "sparse_decode": "qsa_attend", "sparse_prefill": "qsa_sparse_prefill",
+                 "select_sparse_decode": "qsa_sparse_decode"}
+
+
+def source_of(name: str, case: qw.Case) -> str:
+    if name == "sparse_decode" and case.head_dim != 128:
+        return "qsa_sparse_decode"
+    return KERNEL_SOURCE.get(name, "")
+
+
+def measure(qsa, case, args, dev, rank, world, l2, peak_gbs, peak_kind, steps, headline):
+    """One workload: the timed steps, steady-state replays, per-call stream
+    timings, the roofline of the dominant call and the end-to-end figure."""
+    def replica(i):
+        w = qw.make_workload(case, dev, seed=replica_seed(case, i, rank))
+        w["page_table_np"] = w["page_table"].cpu().numpy()
+        w["seqlens_np"] = w["seqlens"].cpu().numpy()
+        return w
+
+    w0 = replica(0)
+    step = qsa.DecodeStep(qw.geometry(w0), case.k, case.window, device=dev)
+    step.run(w0)
+    torch.cuda.synchronize()
+    by0 = algorithmic_bytes(w0, step.sel.cpu().numpy())
+    nrep = int(min(64, max(2, math.ceil(4 * l2 / max(1, by0["touched"])))))
+    reps = [w0] + [replica(i) for i in range(1, nrep)]
+    bufs = [step.buffers() for _ in reps]
+    sels = []
+    for w, b in zip(reps, bufs):
+        step.run(w, bufs=b)
+        torch.cuda.synchronize()
+        sels.append(b["sel"].cpu().numpy())
+    bys = [algorithmic_bytes(w, s_) for w, s_ in zip(reps, sels)]
+    mean = {k: float(np.mean([b[k] for b in bys])) for k in bys[0]}
+    T = case.rows
+
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    # Warm-up (eager), then graphs of one step per replica in turn.
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step.run(reps[i % nrep], stream=stream, bufs=bufs[i % nrep])
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for w, b in zip(reps, bufs):
+                step.run(w, stream=stream, bufs=b)
+        rem = steps % nrep
+        graph_rem = None
+        if rem:
+            graph_rem = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph_rem, stream=stream):
+                for w, b in zip(reps[:rem], bufs[:rem]):
+                    step.run(w, stream=stream, bufs=b)
+        for _ in range(2):
+            graph.replay()
+        stream.synchronize()
+
+    # ---- timed region: exactly `steps` steps, events between graph replays --
+    full, rem = divmod(steps, nrep)
+    nseg = full + (1 if rem else 0)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(nseg + 1)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clk = ClockSampler(dev.index if dev.index is not None else 0) if headline else None
+    if clk:
+        clk.__enter__()
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for i in range(full):
+            graph.replay()
+            evs[i + 1].record(stream)
+        if rem:
+            graph_rem.replay()
+            evs[nseg].record(stream)
+    stream.synchronize()
+    if clk:
+        clk.__exit__(None, None, None)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    ms = max_over_ranks(evs[0].elapsed_time(evs[nseg]), world, dev)
+    seg_ms_per_step = [evs[i].elapsed_time(evs[i + 1]) / nrep for i in range(full)]
+    ms_step = ms / steps
+    rows_s = job_rows_per_second(world, T, steps, ms)
+
+    # ---- steady state: replays of the whole replica graph -------------------
+    n_steady = max(10, min(200, int(math.ceil(3000 / nrep))))
+    st_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_steady + 1)]
+    with torch.cuda.stream(stream):
+        st_ev[0].record(stream)
+        for i in range(n_steady):
+            graph.replay()
+            st_ev[i + 1].record(stream)
+    stream.synchronize()
+    steady = [st_ev[i].elapsed_time(st_ev[i + 1]) / nrep for i in range(n_steady)]
+    steady_med = statistics.median(steady)
+
+    # ---- per call, in stream: the call alone on every replica back to back ---
+    # (its inputs come from the warm-up steps above), and isolated: CUDA event
+    # nodes around each single launch.
+    calls = step.launches()
+    kern = {}
+    for name, fn in calls:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for w, b in zip(reps, bufs):
+                fn(w, b, stream)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for w, b in zip(reps, bufs):
+                    fn(w, b, stream)
+            g.replay()
+            stream.synchronize()
+            n_rep = max(10, min(100, int(math.ceil(2000 / nrep))))
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
+            ev[0].record(stream)
+            for i in range(n_rep):
+                g.replay()
+                ev[i + 1].record(stream)
+            stream.synchronize()
+        per = [ev[i].elapsed_time(ev[i + 1]) / nrep for i in range(n_rep)]
+        kern[name] = {"stream_ms": statistics.median(per)}
+    iso = make_events(2 * len(calls) * nrep)
+    if iso is not None:
+        kg = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(kg, stream=stream):
+                for i, (w, b) in enumerate(zip(reps, bufs)):
+                    for j, (name, fn) in enumerate(calls):
+                        e = iso[2 * (i * len(calls) + j): 2 * (i * len(calls) + j) + 2]
+                        e[0].record(stream)
+                        fn(w, b, stream)
+                        e[1].record(stream)
+            acc = {name: [] for name, _ in calls}
+            for _ in range(5):
+                kg.replay()
+                stream.synchronize()
+                for i in range(nrep):
+                    for j, (name, _) in enumerate(calls):
+                        e = iso[2 * (i * len(calls) + j): 2 * (i * len(calls) + j) + 2]
+                        acc[name].append(e[0].elapsed_time(e[1]))
+        for name in acc:
+            kern[name]["isolated_ms"] = float(np.mean(acc[name]))
+
+    # Every bounded wait in these launches must have succeeded.
+    for b in bufs + [step.own_buffers()]:
+        wst = qsa.qsa_workspace_status(b["workspace"])
+        if wst != 0:
+            raise RuntimeError("a bounded device wait gave up during the bench (%s)"
+                               % qsa.qsa_status_string(wst))
+
+    wl = "cfg%d" % case_index(case)
+    kernels = {}
+    for name, k in kern.items():
+        bkey = "sparse_decode" if name == "select_sparse_decode" else name
+        b = mean.get(bkey, 0.0)
+        t = k["stream_ms"]
+        traffic, ncu_us = ncu_record(source_of(name, case), wl)
+        kernels[name] = {"ms": t, "isolated_ms": k.get("isolated_ms"), "bytes": b,
+                         "gbs": (b / (t / 1000.0) / 1e9) if (t > 0 and b > 0) else None,
+                         "ncu_us": ncu_us}
+    dom = max(kern, key=lambda n: kern[n]["stream_ms"])
+    dom_t = kern[dom]["stream_ms"]
+    dkey = "sparse_decode" if dom == "select_sparse_decode" else dom
+    traffic, ncu_us = ncu_record(source_of(dom, case), wl)
+    if dom == "sparse_prefill":
+        # A contraction: useful FLOPs (4 * D per (row, head, attended token))
+        # against the measured dense 16-bit tensor throughput.
+        tpeak, tkind = measured_tensor_peak()
+        achieved = mean["flops"] / (dom_t / 1000.0) / 1e12
+        roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tpeak,
+                    "unit": "TFLOP/s", "frac": achieved / tpeak, "traffic": traffic,
+                    "peak_kind": tkind, "ncu_us": ncu_us,
+                    "algorithmic_flops_per_launch": mean["flops"],
+                    "algorithmic_bytes_per_launch": mean[dkey],
+                    "hbm_gbs": mean[dkey] / (dom_t / 1000.0) / 1e9,
+                    "timing": "median over graph replays of the call on every replica back "
+                    "to back, divided by the replicas"}
+    else:
+        achieved = mean[dkey] / (dom_t / 1000.0) / 1e9
+        roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak_gbs,
+                    "unit": "GB/s", "frac": achieved / peak_gbs, "traffic": traffic,
+                    "peak_kind": peak_kind, "ncu_us": ncu_us,
+                    "algorithmic_bytes_per_launch": mean[dkey],
+                    "timing": "median over graph replays of the call on every replica back "
+                    "to back, divided by the replicas"}
+    step_gbs = mean["step"] / (ms_step / 1000.0) / 1e9
+    steady_gbs = mean["step"] / (steady_med / 1000.0) / 1e9
+    e2e = run_e2e(qsa, step, reps, stream, args, dev, T, world)
+    res = {
+        "workload": workload_label(case), "config_index": case_index(case),
+        "value": rows_s, "unit": "rows/s", "ms_per_step": ms_step,
+        "ms_per_step_segments_median": (statistics.median(seg_ms_per_step)
+                                        if seg_ms_per_step else None),
+        "steady": {"ms_per_step_median": steady_med, "rows_s": world * T / (steady_med / 1e3),
+                   "replays": n_steady, "steps_per_replay": nrep},
+        "step_hbm": {"bytes": mean["step"], "achieved_gbs": step_gbs, "peak_gbs": peak_gbs,
+                     "frac": step_gbs / peak_gbs, "steady_gbs": steady_gbs,
+                     "steady_frac": steady_gbs / peak_gbs, "peak_kind": peak_kind},
+        "roofline": roofline, "kernels": kernels, "e2e": e2e,
+        "replicas": nrep, "query_rows_per_step": T,
+        "l2_defeat": "inputs rotate over %d HBM replicas; touched bytes per cycle %.0f MB >= 4x "
+                     "L2 (%d MB)" % (nrep, nrep * mean["touched"] / 1e6, l2 >> 20),
+        "launches_per_step": len(calls),
+    }
+    extra = {}
+    if headline:
+        extra["clocks"] = clk.summary()
+        extra["step"] = step
+        extra["reps"] = reps
+        extra["stream"] = stream
+        extra["w0"] = w0
+        extra["nrep"] = nrep
+    return res, extra
+
+
+def case_index(case: qw.Case) -> int:
+    for i, c in enumerate(qw.CONFIGS):
+        if c.name == case.name and c.seed == case.seed:
+            return i
+    return -1
+
+
 def run_qsa(args, case):
     import nvfp4_block_sparse_gb300 as qsa
     world, rank, local = dist_env()
@@ -397,207 +631,70 @@ def run_qsa(args, case):
     l2 = int(getattr(props, "L2_cache_size", 0) or L2_BYTES_DEFAULT)
     peak_gbs, peak_kind = measured_peaks()
 
-    # Replica 0 carries the workload's own seed; others shift it (and the rank).
-    def replica(i):
-        seed = replica_seed(case, i, rank)
-        w = qw.make_workload(case, dev, seed=seed)
-        w["page_table_np"] = w["page_table"].cpu().numpy()
-        w["seqlens_np"] = w["seqlens"].cpu().numpy()
-        return w
+    head, extra = measure(qsa, case, args, dev, rank, world, l2, peak_gbs, peak_kind,
+                          args.steps, headline=True)
+    step, reps, stream, w0, nrep = (extra["step"], extra["reps"], extra["stream"],
+                                    extra["w0"], extra["nrep"])
+    clocks = extra["clocks"]
 
-    w0 = replica(0)
-    step = qsa.DecodeStep(qw.geometry(w0), case.k, case.window, device=dev)
-    step.run(w0)
-    torch.cuda.synchronize()
-    by0 = algorithmic_bytes(w0, step.sel.cpu().numpy())
-    nrep = int(min(64, max(2, math.ceil(4 * l2 / max(1, by0["touched"])))))
-    reps = [w0] + [replica(i) for i in range(1, nrep)]
-    sels = []
-    for w in reps:
-        step.run(w)
-        torch.cuda.synchronize()
-        sels.append(step.sel.cpu().numpy())
-    bys = [algorithmic_bytes(w, s) for w, s in zip(reps, sels)]
-    mean = {k: float(np.mean([b[k] for b in bys])) for k in bys[0]}
-    T = case.rows
-
-    stream = torch.cuda.Stream(device=dev)
-    stream.wait_stream(torch.cuda.current_stream(dev))
-
-    # Warm-up (eager), then capture one graph over every replica in turn.
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            step.run(reps[i % nrep], stream=stream)
-        stream.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            for w in reps:
-                step.run(w, stream=stream)
-        rem = args.steps % nrep
-        graph_rem = None
-        if rem:
-            graph_rem = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph_rem, stream=stream):
-                for w in reps[:rem]:
-                    step.run(w, stream=stream)
-        for _ in range(2):
-            graph.replay()
-        stream.synchronize()
-
-    # ---- timed region -----------------------------------------------------
-    full, rem = divmod(args.steps, nrep)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for _ in range(full):
-                graph.replay()
-            if rem:
-                graph_rem.replay()
-            ev1.record(stream)
-        stream.synchronize()
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        torch.distributed.barrier()
-    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
-    clocks = clk.summary()
-    ms_step = ms / args.steps
-    rows_s = job_rows_per_second(world, T, args.steps, ms)
-    step_gbs = mean["step"] / (ms_step / 1000.0) / 1e9
-
-    # ---- per-kernel durations: event nodes around each kernel ---------------
-    # When the step runs selection and attention as one launch (DecodeStep
-    # fused), sparse_decode below times that fused kernel.
-    fused = step.fused and qsa.qsa_select_sparse_decode_fused(step.cg)
-    att = "sparse_prefill" if step.prefill else "sparse_decode"
-    kern_ms = {}
-    evs = make_events(6 * nrep)
-    if evs is not None:
-        kg = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(kg, stream=stream):
-                for i, w in enumerate(reps):
-                    e = evs[6 * i: 6 * i + 6]
-                    e[0].record(stream)
-                    qsa.qsa_index_scores(step.cg, w["iq"], w["ik_pool"], w["page_table"],
-                                         w["seqlens"], step.scores, stream)
-                    e[1].record(stream)
-                    e[2].record(stream)
-                    if not fused:
-                        qsa.qsa_select_topk(step.cg, step.scores, w["seqlens"], step.k,
-                                            step.window, step.sel, step.nsel, stream)
-                    e[3].record(stream)
-                    e[4].record(stream)
-                    if step.prefill:
-                        qsa.qsa_sparse_prefill(step.cg, w["q"], w["k_pool"], w["k_sf"],
-                                               w["v_pool"], w["v_sf"], w["k_scale"],
-                                               w["v_scale"], w["sm_scale"], w["page_table"],
-                                               w["seqlens"], step.sel, step.k, step.out,
-                                               step.lse, step.workspace, stream)
-                    elif fused:
-                        qsa.qsa_select_sparse_decode(
-                            step.cg, step.scores, step.window, w["q"], w["k_pool"], w["k_sf"],
-                            w["v_pool"], w["v_sf"], w["k_scale"], w["v_scale"], w["sm_scale"],
-                            w["page_table"], w["seqlens"], step.k, step.sel, step.nsel,
-                            step.out, step.lse, step.workspace, step.num_splits, stream)
-                    else:
-                        qsa.qsa_sparse_decode_ex(step.cg, w["q"], w["k_pool"], w["k_sf"],
-                                                 w["v_pool"], w["v_sf"], w["k_scale"],
-                                                 w["v_scale"], w["sm_scale"], w["page_table"],
-                                                 w["seqlens"], step.sel, step.k, step.out,
-                                                 step.lse, step.workspace, step.num_splits,
-                                                 stream)
-                    e[5].record(stream)
-            acc = {"index_scores": [], "select_topk": [], att: []}
-            for _ in range(5):
-                kg.replay()
-                stream.synchronize()
-                for i in range(nrep):
-                    e = evs[6 * i: 6 * i + 6]
-                    acc["index_scores"].append(e[0].elapsed_time(e[1]))
-                    acc["select_topk"].append(e[2].elapsed_time(e[3]))
-                    acc[att].append(e[4].elapsed_time(e[5]))
-        kern_ms = {k: float(np.mean(v)) for k, v in acc.items()}
-        if fused:
-            kern_ms.pop("select_topk")
-
-    # ---- end to end through host buffers ----------------------------------
-    e2e = run_e2e(qsa, step, reps, stream, args, dev, T, world)
-
-    # ---- decode prologue (store the step's new tokens), after every other
-    # measurement because it writes into the replicas' caches ---------------
+    # ---- decode prologue and rollback (they write into the replicas' caches) --
     rollback = (time_rollback(qsa, step, reps, stream, nrep) if not step.prefill else
                 {"skipped": "context row groups are not speculative rows"})
     prologue = time_prologue(qsa, step, reps, stream, nrep)
+    w0_np = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        w0_np = qw.to_numpy({k: v for k, v in w0.items() if not k.endswith("_np")})
+    del step, reps, extra, w0
+    torch.cuda.empty_cache()
+
+    # ---- the other workloads of the target set -----------------------------
+    per_config = {str(args.config): {k: v for k, v in head.items()}}
+    for c in [int(x) for x in args.per_config.split(",") if x.strip() != ""]:
+        if c == args.config:
+            continue
+        r, _ = measure(qsa, qw.CONFIGS[c], args, dev, rank, world, l2, peak_gbs, peak_kind,
+                       args.steps, headline=False)
+        per_config[str(c)] = r
+        torch.cuda.empty_cache()
 
     # ---- CPU baseline (rank 0, N = 1 only) -----------------------------------
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        w_np = qw.to_numpy({k: v for k, v in w0.items() if not k.endswith("_np")})
-        cpu = time_oracle(case, w_np)
-        cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    if w0_np is not None:
+        full = time_oracle(case, w0_np)
+        import oracle
+        nthr = oracle.num_threads()
+        oracle.set_threads(1)
+        one = time_oracle(case, w0_np, budget_s=8.0)
+        oracle.set_threads(nthr)
+        cpu = {k: full[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        cpu["single_thread"] = {"value": one["value"], "unit": one["unit"], "cores": 1,
+                                "sample": one["sample"]}
 
     if rank != 0:
         return
-    # Every bounded wait in the timed steps must have succeeded.
-    wst = qsa.qsa_workspace_status(step.workspace)
-    if wst != 0:
-        raise RuntimeError("sparse decode reported status %d (%s) during the bench"
-                           % (wst, qsa.qsa_status_string(wst)))
-    kernels = {}
-    for name, t in kern_ms.items():
-        b = mean[name]
-        kernels[name] = {"ms": t, "bytes": b,
-                         "gbs": (b / (t / 1000.0) / 1e9) if (t > 0 and b > 0) else None}
-    if fused:
-        kernels["select_topk"] = {"ms": None, "fused_into": "sparse_decode"}
-    dom = max(kern_ms, key=kern_ms.get) if kern_ms else att
-    dom_t = kern_ms.get(dom)
-    wl = "cfg%d" % args.config
-    traffic = traffic_record("qsa_" + dom, wl)
-    if dom == "sparse_prefill":
-        # A contraction: useful FLOPs (4 * D per (row, head, attended token))
-        # against the measured dense 16-bit tensor throughput.
-        tpeak, tkind = measured_tensor_peak()
-        achieved = (mean["flops"] / (dom_t / 1000.0) / 1e12) if dom_t else None
-        roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tpeak,
-                    "unit": "TFLOP/s", "frac": (achieved / tpeak) if achieved else None,
-                    "traffic": traffic, "peak_kind": tkind,
-                    "algorithmic_flops_per_launch": mean["flops"],
-                    "algorithmic_bytes_per_launch": mean[dom],
-                    "hbm_gbs": (mean[dom] / (dom_t / 1000.0) / 1e9) if dom_t else None}
-    else:
-        achieved = (mean[dom] / (dom_t / 1000.0) / 1e9) if dom_t else None
-        roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak_gbs,
-                    "unit": "GB/s", "frac": (achieved / peak_gbs) if achieved else None,
-                    "traffic": traffic, "peak_kind": peak_kind,
-                    "algorithmic_bytes_per_launch": mean[dom]}
     line = {
-        "metric": METRIC, "value": rows_s, "unit": "rows/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "metric": METRIC, "value": head["value"], "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "nvfp4 KV (e2m1+e4m3), bf16 q/out, int8 index, fp32 accumulate",
         "data": "synthetic",
-        "config": {"workload": workload_label(case), "config_index": args.config,
-                   "query_rows_per_step": T, "replicas": nrep,
-                   "l2_defeat": "inputs rotate over %d HBM replicas; touched bytes per cycle "
-                   "%.0f MB >= 4x L2 (%d MB)" % (nrep, nrep * mean["touched"] / 1e6, l2 >> 20),
-                   "timing": "CUDA graph replay of %d steps, CUDA events on the launching "
-                   "stream" % nrep},
-        "step_hbm": {"bytes": mean["step"], "achieved_gbs": step_gbs, "peak_gbs": peak_gbs,
-                     "frac": step_gbs / peak_gbs, "peak_kind": peak_kind},
-        "roofline": roofline,
-        "kernels": kernels,
+        "config": {"workload": head["workload"], "config_index": args.config,
+                   "query_rows_per_step": head["query_rows_per_step"],
+                   "replicas": head["replicas"], "l2_defeat": head["l2_defeat"],
+                   "timing": "CUDA graph replays of one step per replica; CUDA events on the "
+                   "launching stream between replays"},
+        "ms_per_step_segments_median": head["ms_per_step_segments_median"],
+        "steady": head["steady"],
+        "step_hbm": head["step_hbm"],
+        "roofline": head["roofline"],
+        "kernels": head["kernels"],
         "clocks": clocks,
-        "e2e": e2e,
-        "gpu_launches": (2 if fused else 3) * args.steps,
+        "e2e": head["e2e"],
+        "gpu_launches": head["launches_per_step"] * args.steps,
         "cpu_baseline": cpu,
         "prologue": prologue,
         "rollback": rollback,
+        "per_config": per_config,
     }
     print(json.dumps(line), flush=True)
 
@@ -715,9 +812,13 @@ def run_e2e(qsa, step, reps, stream, args, dev, T, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", type=int, default=1)
+    # The largest single-GPU workload of the target set is the headline; the
+    # others of the set are measured into per_config.
+    ap.add_argument("--config", type=int, default=4)
+    ap.add_argument("--per-config", default="1,2,3,4",
+                    help="comma-separated workload indices measured besides --config")
     ap.add_argument("--impl", default="qsa", choices=["qsa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

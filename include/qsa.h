@@ -42,9 +42,11 @@
  * never dereferenced.
  *
  * Memory: every pointer argument is DEVICE memory owned by the caller; the
- * library never allocates, frees or keeps global state.  Calls are
- * asynchronous on `stream`, read no device data on the host, and size their
- * grids from the geometry alone, so a step can be captured in a CUDA graph.
+ * library never allocates or frees device memory.  Its only global state is
+ * the fixed scratch array of qsa_sparse_decode_noalloc (and the diagnostic
+ * wait bound of qsa_debug_set_wait_ns).  Calls are asynchronous on `stream`,
+ * read no device data on the host, and size their grids from the geometry
+ * alone, so a step can be captured in a CUDA graph.
  *
  * Errors: each call validates its arguments on the host and returns a status
  * before launching anything; QSA_ERR_CUDA reports a launch failure.  Bad
@@ -247,13 +249,17 @@ qsa_status_t qsa_select_sparse_decode(const qsa_geom_t *geom, const int32_t *sco
  *  - The array lives on every GPU that loads the library, until the process
  *    exits, and all calls on a GPU share it: calls that overlap on the GPU
  *    (different streams or host threads) race and must be serialised by the
- *    caller.  Each call clears the part that must start at zero.
- *  - The first call on a device looks up the array's device address; make
- *    that first call before capturing any stream into a CUDA graph.
+ *    caller.  Its split tickets start at zero and every call leaves them at
+ *    zero, so nothing is cleared between calls.
+ *  - Every call looks up the array's device address (host-only); the first
+ *    call on a device may also load the library's device code, so make it
+ *    before capturing any stream into a CUDA graph.
  *  - The KV split count is lowered until the split partials fit the array;
  *    when even one split does not fit (more than about a million
  *    (request, KV head, column group) units), the call returns
  *    QSA_ERR_WORKSPACE without launching.
+ *  - A bounded device wait that gives up sets the array's status word, which
+ *    stays set until qsa_sparse_decode_noalloc_status() reads it.
  *  - Other arguments are validated as in qsa_sparse_decode.
  */
 qsa_status_t qsa_sparse_decode_noalloc(const qsa_geom_t *geom, const void *q_bf16,
@@ -264,6 +270,15 @@ qsa_status_t qsa_sparse_decode_noalloc(const qsa_geom_t *geom, const void *q_bf1
                                        const int32_t *seqlens, const int32_t *sel,
                                        int k, void *out_bf16, float *lse,
                                        cudaStream_t stream);
+
+/*
+ * Reads and clears the status word of the built-in scratch array of
+ * qsa_sparse_decode_noalloc on the current device (synchronising `stream`):
+ * *device_code = 0 and QSA_OK when every bounded device wait of the calls
+ * since the previous query completed, otherwise the nonzero code and
+ * QSA_ERR_DEVICE_TIMEOUT (the outputs of those calls are not valid).
+ */
+qsa_status_t qsa_sparse_decode_noalloc_status(int *device_code, cudaStream_t stream);
 
 /*
  * Decode prologue: store the step's new tokens into the cache before A1.
@@ -386,6 +401,18 @@ qsa_status_t qsa_sparse_prefill(const qsa_geom_t *geom, const void *q_bf16,
                                 const int32_t *seqlens, const int32_t *sel, int k,
                                 void *out_bf16, float *lse, void *workspace,
                                 size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Diagnostics: sets the bound, in nanoseconds, of the waits of the head_dim
+ * 128 sparse decode kernel for its page copies (2 s by default; 0 restores
+ * the default).  Process-wide, for tests of the timeout reporting: a bound
+ * below 1 us makes each wait one non-blocking probe, which gives up when the
+ * copy has not landed yet (the first probe follows the copy's request); the
+ * kernel records QSA_ERR_DEVICE_TIMEOUT in its status word, stops issuing
+ * copies, lets those in flight land (under the default bound) and finishes;
+ * that call's out and lse are not valid.
+ */
+void qsa_debug_set_wait_ns(unsigned long long ns);
 
 /*
  * Reads the workspace's device status word (synchronising `stream`): 0 when

@@ -15,6 +15,7 @@ import torch
 from .binding import (EXPORTS, QsaError, load, make_geom, qsa_geom_t, qsa_index_scores,
                       qsa_select_sparse_decode, qsa_select_sparse_decode_fused,
                       qsa_select_topk, qsa_sparse_decode, qsa_sparse_decode_ex, qsa_sparse_decode_noalloc,
+                      qsa_sparse_decode_noalloc_status, qsa_debug_set_wait_ns,
                       qsa_sparse_decode_workspace_bytes, qsa_sparse_decode_workspace_bytes_ex,
                       qsa_rollback_gather, qsa_rollback_restore, qsa_rollback_state_bytes,
                       qsa_sparse_prefill, qsa_sparse_prefill_workspace_bytes,
@@ -25,6 +26,7 @@ __all__ = [
     "EXPORTS", "QsaError", "load", "make_geom", "qsa_geom_t", "qsa_index_scores",
     "qsa_select_sparse_decode", "qsa_select_sparse_decode_fused",
     "qsa_select_topk", "qsa_sparse_decode", "qsa_sparse_decode_ex", "qsa_sparse_decode_noalloc",
+    "qsa_sparse_decode_noalloc_status", "qsa_debug_set_wait_ns",
     "qsa_sparse_decode_workspace_bytes", "qsa_sparse_decode_workspace_bytes_ex",
     "qsa_rollback_gather", "qsa_rollback_restore", "qsa_rollback_state_bytes",
     "qsa_sparse_prefill", "qsa_sparse_prefill_workspace_bytes",
@@ -77,34 +79,74 @@ class DecodeStep:
         self.workspace = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
         qsa_workspace_init(self.workspace)
 
-    def run(self, w: dict, stream=None, sm_scale=None, out=None, lse=None):
+    def buffers(self) -> dict:
+        """A fresh set of the step's intermediate and output buffers (scores,
+        sel, nsel, out, lse and a zero-filled workspace) on the step's device,
+        e.g. one per input replica of a benchmark."""
+        dev = self.scores.device
+        ws = torch.empty_like(self.workspace)
+        qsa_workspace_init(ws)
+        return dict(scores=torch.empty_like(self.scores), sel=torch.empty_like(self.sel),
+                    nsel=torch.empty_like(self.nsel), out=torch.empty_like(self.out),
+                    lse=torch.empty_like(self.lse), workspace=ws)
+
+    def own_buffers(self) -> dict:
+        return dict(scores=self.scores, sel=self.sel, nsel=self.nsel, out=self.out,
+                    lse=self.lse, workspace=self.workspace)
+
+    def launches(self):
+        """The step's library calls in order, as (name, fn) pairs; fn(w, bufs,
+        stream, sm_scale=None) issues that call for workload tensors ``w``
+        with the buffers ``bufs`` (the keys of buffers())."""
+        def sm_of(w, sm_scale):
+            return float(w["sm_scale"]) if sm_scale is None else float(sm_scale)
+
+        def index(w, bufs, stream, sm_scale=None):
+            qsa_index_scores(self.cg, w["iq"], w["ik_pool"], w["page_table"], w["seqlens"],
+                             bufs["scores"], stream)
+
+        def select(w, bufs, stream, sm_scale=None):
+            qsa_select_topk(self.cg, bufs["scores"], w["seqlens"], self.k, self.window,
+                            bufs["sel"], bufs["nsel"], stream)
+
+        def prefill(w, bufs, stream, sm_scale=None):
+            qsa_sparse_prefill(self.cg, w["q"], w["k_pool"], w["k_sf"], w["v_pool"], w["v_sf"],
+                               w["k_scale"], w["v_scale"], sm_of(w, sm_scale), w["page_table"],
+                               w["seqlens"], bufs["sel"], self.k, bufs["out"], bufs["lse"],
+                               bufs["workspace"], stream)
+
+        def decode(w, bufs, stream, sm_scale=None):
+            qsa_sparse_decode_ex(self.cg, w["q"], w["k_pool"], w["k_sf"], w["v_pool"],
+                                 w["v_sf"], w["k_scale"], w["v_scale"], sm_of(w, sm_scale),
+                                 w["page_table"], w["seqlens"], bufs["sel"], self.k, bufs["out"],
+                                 bufs["lse"], bufs["workspace"], self.num_splits, stream)
+
+        def select_decode(w, bufs, stream, sm_scale=None):
+            qsa_select_sparse_decode(self.cg, bufs["scores"], self.window, w["q"], w["k_pool"],
+                                     w["k_sf"], w["v_pool"], w["v_sf"], w["k_scale"],
+                                     w["v_scale"], sm_of(w, sm_scale), w["page_table"],
+                                     w["seqlens"], self.k, bufs["sel"], bufs["nsel"],
+                                     bufs["out"], bufs["lse"], bufs["workspace"],
+                                     self.num_splits, stream)
+
+        if self.prefill:
+            return [("index_scores", index), ("select_topk", select), ("sparse_prefill", prefill)]
+        if self.fused:
+            return [("index_scores", index), ("select_sparse_decode", select_decode)]
+        return [("index_scores", index), ("select_topk", select), ("sparse_decode", decode)]
+
+    def run(self, w: dict, stream=None, sm_scale=None, out=None, lse=None, bufs=None):
         """One step over workload tensors ``w`` (the generator's layout).
         ``out`` / ``lse`` (optional) receive the results instead of the step's
-        own buffers, e.g. one span per step of a pipelined serving loop."""
-        sm = float(w["sm_scale"]) if sm_scale is None else float(sm_scale)
-        out = self.out if out is None else out
-        lse = self.lse if lse is None else lse
-        qsa_index_scores(self.cg, w["iq"], w["ik_pool"], w["page_table"], w["seqlens"],
-                         self.scores, stream)
-        if self.prefill:
-            qsa_select_topk(self.cg, self.scores, w["seqlens"], self.k, self.window, self.sel,
-                            self.nsel, stream)
-            qsa_sparse_prefill(self.cg, w["q"], w["k_pool"], w["k_sf"], w["v_pool"], w["v_sf"],
-                               w["k_scale"], w["v_scale"], sm, w["page_table"], w["seqlens"],
-                               self.sel, self.k, out, lse, self.workspace, stream)
-        elif not self.fused:
-            qsa_select_topk(self.cg, self.scores, w["seqlens"], self.k, self.window, self.sel,
-                            self.nsel, stream)
-            qsa_sparse_decode_ex(self.cg, w["q"], w["k_pool"], w["k_sf"], w["v_pool"],
-                                 w["v_sf"], w["k_scale"], w["v_scale"], sm, w["page_table"],
-                                 w["seqlens"], self.sel, self.k, out, lse,
-                                 self.workspace, self.num_splits, stream)
-        else:
-            qsa_select_sparse_decode(self.cg, self.scores, self.window, w["q"], w["k_pool"],
-                                     w["k_sf"], w["v_pool"], w["v_sf"], w["k_scale"],
-                                     w["v_scale"], sm, w["page_table"], w["seqlens"], self.k,
-                                     self.sel, self.nsel, out, lse, self.workspace,
-                                     self.num_splits, stream)
+        own buffers, e.g. one span per step of a pipelined serving loop;
+        ``bufs`` (optional, from buffers()) replaces every buffer."""
+        b = dict(self.own_buffers() if bufs is None else bufs)
+        if out is not None:
+            b["out"] = out
+        if lse is not None:
+            b["lse"] = lse
+        for _, fn in self.launches():
+            fn(w, b, stream, sm_scale)
         return self
 
     @staticmethod

@@ -31,6 +31,8 @@ EXPORTS = (
     "qsa_sparse_decode",
     "qsa_sparse_decode_ex",
     "qsa_sparse_decode_noalloc",
+    "qsa_sparse_decode_noalloc_status",
+    "qsa_debug_set_wait_ns",
     "qsa_workspace_status",
     "qsa_store_kv_tokens",
     "qsa_select_sparse_decode",
@@ -119,6 +121,10 @@ def load(build_if_missing: bool = False):
     lib.qsa_sparse_prefill_workspace_bytes.argtypes = [G, ctypes.c_int]
     lib.qsa_sparse_prefill.restype = st
     lib.qsa_sparse_prefill.argtypes = dec + [_vp]
+    lib.qsa_sparse_decode_noalloc_status.restype = st
+    lib.qsa_sparse_decode_noalloc_status.argtypes = [ctypes.POINTER(ctypes.c_int), _vp]
+    lib.qsa_debug_set_wait_ns.restype = None
+    lib.qsa_debug_set_wait_ns.argtypes = [ctypes.c_ulonglong]
     lib.qsa_workspace_status.restype = st
     lib.qsa_workspace_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int), _vp]
     _lib = lib
@@ -303,6 +309,23 @@ def qsa_sparse_decode_noalloc(geom, q, k_pool, k_sf, v_pool, v_sf, k_scale, v_sc
         _ptr(page_table, torch.int32, "page_table"), _ptr(seqlens, torch.int32, "seqlens"),
         _ptr(sel, torch.int32, "sel"), int(k), _ptr(out, torch.bfloat16, "out"),
         _ptr(lse, torch.float32, "lse"), _stream(stream)))
+
+
+def qsa_sparse_decode_noalloc_status(stream=None) -> int:
+    """Reads and clears the built-in scratch array's status word on the
+    current device: 0, or the code of a bounded device wait that gave up in a
+    qsa_sparse_decode_noalloc call since the previous query."""
+    code = ctypes.c_int(0)
+    st = load().qsa_sparse_decode_noalloc_status(ctypes.byref(code), _stream(stream))
+    if st not in (QSA_OK, QSA_ERR_DEVICE_TIMEOUT):
+        _check("qsa_sparse_decode_noalloc_status", st)
+    return int(code.value)
+
+
+def qsa_debug_set_wait_ns(ns: int) -> None:
+    """Diagnostics: bound of the head_dim-128 decode kernel's copy waits in ns
+    (0 restores the 2 s default)."""
+    load().qsa_debug_set_wait_ns(int(ns))
 
 
 def qsa_workspace_status(workspace, stream=None) -> int:

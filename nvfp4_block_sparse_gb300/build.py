@@ -12,6 +12,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libqsa.so")
 SOURCES = ["qsa_api.cu", "qsa_index_scores.cu", "qsa_select_topk.cu", "qsa_sparse_decode.cu",
+           "qsa_attend.cu",
            "qsa_sparse_decode_noalloc.cu", "qsa_store_tokens.cu", "qsa_rollback.cu",
            "qsa_sparse_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -12,9 +12,14 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace {
 
 using qsa::Geom;
+
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
 
 bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
@@ -94,7 +99,15 @@ qsa_status_t check_decode_args(const qsa_geom_t* geom, int k) {
 
 }  // namespace
 
+namespace qsa {
+unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+}  // namespace qsa
+
 extern "C" {
+
+void qsa_debug_set_wait_ns(unsigned long long ns) {
+  g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns, std::memory_order_relaxed);
+}
 
 const char* qsa_status_string(qsa_status_t s) {
   switch (s) {

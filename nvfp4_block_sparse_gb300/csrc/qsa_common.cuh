@@ -67,6 +67,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// One probe of phase `parity` that never suspends the thread.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Contiguous global -> shared copy on the TMA engine; completion is signalled
 // as transaction bytes on `bar`.  dst, src and bytes must be 16-byte aligned.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
@@ -195,6 +208,21 @@ struct DecodePlan {
 
 DecodePlan plan_sparse_decode(const Geom& g, int k, int num_splits);
 bool decode_can_fuse_select(const Geom& g);
+
+// Bound of the attention kernels' waits for their chunk copies, in ns
+// (qsa_debug_set_wait_ns; 2 s unless a diagnostic changed it).
+unsigned long long wait_limit_ns();
+
+// head_dim 128 attention with one dequantisation per chunk for all of a
+// request's query columns (qsa_attend.cu).
+bool attend_supports(const Geom& g);
+DecodePlan plan_attend(const Geom& g, int k, int num_splits);
+cudaError_t launch_attend(const Geom& g, const DecodePlan& plan, const void* q,
+                          const uint8_t* k_pool, const uint8_t* k_sf, const uint8_t* v_pool,
+                          const uint8_t* v_sf, float k_scale, float v_scale, float sm_scale,
+                          const int32_t* page_table, const int32_t* seqlens, const int32_t* sel,
+                          int k, void* out, float* lse, void* workspace, bool pdl,
+                          cudaStream_t stream);
 
 // Context row groups (qsa_sparse_prefill): rows per 128-vector tile, dynamic
 // shared memory of a CTA, and the launch.

@@ -51,6 +51,9 @@ template <int NTHREADS>
 __device__ void select_row(const int32_t* __restrict__ src, int nb, int W, int k,
                            int32_t* __restrict__ out, int32_t* __restrict__ nsel,
                            uint8_t* smem) {
+  // The 64-int scalar area holds per-warp slots at sc[w], sc[8 + w], ...,
+  // sc[32 + w] next to fixed slots from sc[40] on: at most 8 warps.
+  static_assert(NTHREADS % 32 == 0 && NTHREADS <= 256, "select_row takes up to 8 warps");
   constexpr int kWarps = NTHREADS / 32;
   constexpr unsigned kFull = 0xffffffffu;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;

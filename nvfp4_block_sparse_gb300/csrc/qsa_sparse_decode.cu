@@ -567,7 +567,7 @@ sparse_decode_kernel(Params p) {
   // (the selection is ascending) or on an invalid page is dropped.
   int* wl = s_sel + warp * 2 * decode_list_cap(k, p.splits, W);   // (page, tok0) pairs
   int wcnt = 0;
-  if (ONE) {
+  if constexpr (ONE) {
     const int nc = k << csh;
     const int32_t* selrow = p.sel + (size_t)b * k;
     if (p.scores) {
@@ -1294,10 +1294,11 @@ int variant_resident(int ntr, int R, int d, int k, int mb, int splits) {
 
 }  // namespace
 
-// The decode variant can select its row itself when the selection's scratch
-// fits in its stage region.
+// The per-row-warp variant (head_dim 256) can select its row itself when the
+// selection's scratch fits in its stage region; head_dim 128 runs the shared-
+// dequantisation kernel, which reads a finished selection.
 bool decode_can_fuse_select(const Geom& g) {
-  if (g.R != 1) return false;
+  if (g.R != 1 || attend_supports(g)) return false;
   const int ntr = tiles_per_row(g);
 #define X(NTR_, R_, W_, S_, ONE_, D_)                                                 \
   if (ONE_ && ntr == NTR_ && R_ == 1 && g.D == D_)                                      \
@@ -1308,7 +1309,7 @@ bool decode_can_fuse_select(const Geom& g) {
   return false;
 }
 
-DecodePlan plan_sparse_decode(const Geom& g, int k, int num_splits) {
+DecodePlan plan_legacy_decode(const Geom& g, int k, int num_splits) {
   DecodePlan pl;
   const int G = g.Hq / g.Hkv;
   const int ntr = tiles_per_row(g);
@@ -1344,7 +1345,7 @@ DecodePlan plan_sparse_decode(const Geom& g, int k, int num_splits) {
   return pl;
 }
 
-cudaError_t launch_sparse_decode(const Geom& g, const DecodePlan& plan, const void* q,
+cudaError_t launch_legacy_decode(const Geom& g, const DecodePlan& plan, const void* q,
                                  const uint8_t* k_pool, const uint8_t* k_sf,
                                  const uint8_t* v_pool, const uint8_t* v_sf, float k_scale,
                                  float v_scale, float sm_scale, const int32_t* page_table,
@@ -1380,6 +1381,28 @@ cudaError_t launch_sparse_decode(const Geom& g, const DecodePlan& plan, const vo
   QSA_DECODE_VARIANTS(X)
 #undef X
   return cudaErrorInvalidValue;
+}
+
+// head_dim 128: the shared-dequantisation kernel (qsa_attend.cu); head_dim
+// 256: the per-row-warp kernel above.
+DecodePlan plan_sparse_decode(const Geom& g, int k, int num_splits) {
+  return attend_supports(g) ? plan_attend(g, k, num_splits) : plan_legacy_decode(g, k, num_splits);
+}
+
+cudaError_t launch_sparse_decode(const Geom& g, const DecodePlan& plan, const void* q,
+                                 const uint8_t* k_pool, const uint8_t* k_sf,
+                                 const uint8_t* v_pool, const uint8_t* v_sf, float k_scale,
+                                 float v_scale, float sm_scale, const int32_t* page_table,
+                                 const int32_t* seqlens, const int32_t* sel, int k, void* out,
+                                 float* lse, void* workspace, bool pdl, cudaStream_t stream,
+                                 const int32_t* scores, int window, int32_t* sel_out,
+                                 int32_t* nsel_out) {
+  if (!scores && attend_supports(g))
+    return launch_attend(g, plan, q, k_pool, k_sf, v_pool, v_sf, k_scale, v_scale, sm_scale,
+                         page_table, seqlens, sel, k, out, lse, workspace, pdl, stream);
+  return launch_legacy_decode(g, plan, q, k_pool, k_sf, v_pool, v_sf, k_scale, v_scale, sm_scale,
+                              page_table, seqlens, sel, k, out, lse, workspace, pdl, stream,
+                              scores, window, sel_out, nsel_out);
 }
 
 }  // namespace qsa

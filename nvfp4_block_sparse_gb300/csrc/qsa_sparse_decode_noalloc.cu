@@ -13,44 +13,34 @@
 // The array is a file-scope __device__ variable, so every GPU that loads the
 // library holds it until the process exits, and every call on that GPU shares
 // it: calls that overlap on the GPU (two streams, or two threads) race on it
-// and must be serialised by the caller.  Each call clears the tickets and
-// status word it relies on before launching, so whatever a previous call left
-// behind does no harm.
+// and must be serialised by the caller.  Its split tickets start at zero (a
+// __device__ array is zero-filled when the module loads) and every call leaves
+// them at zero again, so nothing is cleared between calls and the call keeps
+// the programmatic-launch overlap with the kernel before it.  Its status word
+// is sticky: a bounded device wait that gives up in any call sets it, and
+// qsa_sparse_decode_noalloc_status() reads and clears it.
 #include "qsa_common.cuh"
-
-#include <mutex>
 
 namespace {
 
 // 4 MiB: the status word and tickets always fit; the number of KV splits is
 // reduced until the split partials fit as well.
 constexpr size_t kNoAllocBytes = size_t(4) << 20;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
-std::mutex g_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Resolves the device address of the scratch array for the current device
-// (once per device).  The name g_noalloc_scratch is only a host-side handle;
-// the kernel must receive the address cudaGetSymbolAddress returns.
+// The device address of the scratch array on the current device.  The name
+// g_noalloc_scratch is only a host-side handle; kernels and copies must be
+// given the address cudaGetSymbolAddress returns.  It is looked up on every
+// call (host-only and cheap), so a context created anew on the device (after
+// cudaDeviceReset, say) gets its own array's address.
 qsa_status_t scratch_for_current_device(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
     cudaGetLastError();
     return QSA_ERR_CUDA;
   }
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-      cudaGetLastError();
-      return QSA_ERR_CUDA;
-    }
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return QSA_OK;
 }
 
@@ -88,14 +78,24 @@ extern "C" qsa_status_t qsa_sparse_decode_noalloc(
   void* scratch = nullptr;
   qsa_status_t st = scratch_for_current_device(&scratch);
   if (st != QSA_OK) return st;
-  // Status word and tickets must start at zero; they are the front of the
-  // layout, exactly the whole scratch of a one-split plan.
-  const size_t zero_bytes = qsa::plan_sparse_decode(g, k, 1).ws_bytes;
-  if (cudaMemsetAsync(scratch, 0, zero_bytes, stream) != cudaSuccess) {
-    cudaGetLastError();
-    return QSA_ERR_CUDA;
-  }
   return qsa_sparse_decode_ex(geom, q_bf16, k_pool, k_sf, v_pool, v_sf, k_scale, v_scale,
                               sm_scale, page_table, seqlens, sel, k, out_bf16, lse, scratch,
                               kNoAllocBytes, plan.splits, stream);
+}
+
+extern "C" qsa_status_t qsa_sparse_decode_noalloc_status(int* device_code, cudaStream_t stream) {
+  if (!device_code) return QSA_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  qsa_status_t st = scratch_for_current_device(&scratch);
+  if (st != QSA_OK) return st;
+  int v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, scratch, sizeof(int), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(scratch, 0, sizeof(int), stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return QSA_ERR_CUDA;
+  }
+  *device_code = v;
+  return v == 0 ? QSA_OK : QSA_ERR_DEVICE_TIMEOUT;
 }

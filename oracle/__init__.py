@@ -46,6 +46,8 @@ def _load():
         lib.qsa_oracle_e4m3.restype = ctypes.c_double
         lib.qsa_oracle_e4m3.argtypes = [ctypes.c_int]
         lib.qsa_oracle_num_threads.restype = ctypes.c_int
+        lib.qsa_oracle_set_threads.restype = None
+        lib.qsa_oracle_set_threads.argtypes = [ctypes.c_int]
         lib.qsa_oracle_e4m3_encode.restype = ctypes.c_int
         lib.qsa_oracle_e4m3_encode.argtypes = [ctypes.c_float]
         lib.qsa_oracle_e2m1_encode.restype = ctypes.c_int
@@ -72,6 +74,11 @@ def _p(a: np.ndarray):
 
 def num_threads() -> int:
     return int(_load().qsa_oracle_num_threads())
+
+
+def set_threads(n: int) -> None:
+    """Threads the following oracle calls use (OpenMP; n >= 1)."""
+    _load().qsa_oracle_set_threads(int(n))
 
 
 def e2m1(code: int) -> float:

@@ -92,6 +92,16 @@ int qsa_oracle_num_threads(void)
 #endif
 }
 
+/* Threads the following calls use (n >= 1); for single-thread timings. */
+void qsa_oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* Tokens visible to row j of a request with L cached tokens (R7). */
 static int64_t visible_tokens(int64_t L, int R, int j, int64_t cap)
 {

@@ -305,5 +305,7 @@ def test_fused_selection_matches_composed(qsa, name, make, splits):
     ra, rc = host(step_f), host(c)
     for key in ("scores", "sel", "nsel", "out", "lse"):
         np.testing.assert_array_equal(ra[key], rc[key], err_msg=key)
-    if w["rows_per_req"] == 1 and name not in ("gqa12",):
-        assert qsa.qsa_select_sparse_decode_fused(qw.geometry(w))
+    # One launch only where the per-row-warp kernel serves the geometry (head
+    # dim 256, decode rows); head dim 128 selects, then attends.
+    fused = qsa.qsa_select_sparse_decode_fused(qw.geometry(w))
+    assert bool(fused) == (w["rows_per_req"] == 1 and w["head_dim"] == 256)

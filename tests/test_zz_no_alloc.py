@@ -77,3 +77,88 @@ def test_noalloc_rejects_geometry_beyond_its_scratch(qsa):
                                        ctypes.c_float(0.1), fake, fake, fake, 1, fake, fake,
                                        ctypes.c_void_p(0))
     assert st == 4
+
+
+NOALLOC_BYTES = 4 << 20
+
+
+def _lowered_splits(qsa, geom, k):
+    """The split count qsa_sparse_decode_noalloc runs: the automatic one,
+    lowered until the workspace fits the 4 MiB array."""
+    auto = qsa.qsa_sparse_decode_workspace_bytes(geom, k)
+    splits = next(s for s in range(1, 65)
+                  if qsa.qsa_sparse_decode_workspace_bytes_ex(geom, k, s) == auto)
+    while splits > 1 and qsa.qsa_sparse_decode_workspace_bytes_ex(geom, k, splits) > NOALLOC_BYTES:
+        splits -= 1
+    return auto, splits
+
+
+def test_noalloc_lowers_splits_to_fit_its_scratch(qsa):
+    # Four rows per request, 8 query heads per KV head (32 query columns per
+    # CTA) and 38 (request, KV head) units: the automatic plan spreads every
+    # unit over 8 splits, whose partials need more than the 4 MiB array, so
+    # the call runs fewer splits.  Checked against the workspace entry point
+    # at that split count (the same bits) and against the oracle on sampled
+    # requests.
+    import oracle
+    case = qw.Case("noalloc lowering", seed=31, batch=19, rows_per_req=4, num_q_heads=16,
+                   num_kv_heads=2, page_size=64, ctx_lo=2600, ctx_hi=4100, k=12, window=2,
+                   max_blocks=65, pool="perm")
+    w = qw.make_workload(case, "cuda")
+    geom = qw.geometry(w)
+    auto, splits = _lowered_splits(qsa, geom, w["k"])
+    assert auto > NOALLOC_BYTES and splits >= 1
+    step = qsa.DecodeStep(geom, w["k"], w["window"], num_splits=splits)
+    step.run(w)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = step.out.clone(), step.lse.clone()
+    for _ in range(2):
+        out = torch.full_like(step.out, float("nan"))
+        lse = torch.full_like(step.lse, float("nan"))
+        qsa.qsa_sparse_decode_noalloc(step.cg, w["q"], w["k_pool"], w["k_sf"], w["v_pool"],
+                                      w["v_sf"], w["k_scale"], w["v_scale"], w["sm_scale"],
+                                      w["page_table"], w["seqlens"], step.sel, w["k"], out, lse)
+        torch.cuda.synchronize()
+        assert qsa.qsa_sparse_decode_noalloc_status() == 0
+        # same kernel, same split count: the same bits
+        assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+    w_np = qw.to_numpy(w)
+    R = case.rows_per_req
+    for b in (0, case.batch // 2, case.batch - 1):
+        ref = oracle.step(w_np, rows=(b * R, b * R + R))
+        _close(out[b * R:b * R + R], lse[b * R:b * R + R],
+               torch.from_numpy(ref["out"][b * R:b * R + R]),
+               torch.from_numpy(ref["lse"][b * R:b * R + R]))
+
+
+def test_noalloc_reports_a_wait_that_gave_up(qsa):
+    # A wait bound of a few nanoseconds makes the kernel's copy waits give up
+    # (the copies still land before it finishes): the built-in array's status
+    # word then reports QSA_ERR_DEVICE_TIMEOUT until it is read, and the next
+    # call under the default bound is correct again.
+    w = qw.make_workload(qw.small(qw.CONFIGS[1]), "cuda")
+    step = qsa.DecodeStep(qw.geometry(w), w["k"], w["window"])
+    step.run(w)
+    torch.cuda.synchronize()
+    assert qsa.qsa_sparse_decode_noalloc_status() == 0
+    out = torch.empty_like(step.out)
+    lse = torch.empty_like(step.lse)
+    args = (step.cg, w["q"], w["k_pool"], w["k_sf"], w["v_pool"], w["v_sf"], w["k_scale"],
+            w["v_scale"], w["sm_scale"], w["page_table"], w["seqlens"], step.sel, w["k"], out,
+            lse)
+    try:
+        qsa.qsa_debug_set_wait_ns(4)
+        qsa.qsa_sparse_decode_noalloc(*args)
+        torch.cuda.synchronize()
+    finally:
+        qsa.qsa_debug_set_wait_ns(0)
+    lib = qsa.load()
+    code = ctypes.c_int(0)
+    st = lib.qsa_sparse_decode_noalloc_status(ctypes.byref(code),
+                                              ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 5 and code.value != 0                     # QSA_ERR_DEVICE_TIMEOUT
+    assert qsa.qsa_sparse_decode_noalloc_status() == 0      # read and cleared
+    qsa.qsa_sparse_decode_noalloc(*args)
+    torch.cuda.synchronize()
+    assert qsa.qsa_sparse_decode_noalloc_status() == 0
+    _close(out, lse, step.out, step.lse)
