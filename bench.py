@@ -396,8 +396,14 @@ KERNEL_SOURCE = {"index_scores": "qsa_index_scores", "select_topk": "qsa_select_
                  "select_sparse_decode": "qsa_sparse_decode"}
 
 
+def bytes_key(name: str) -> str:
+    """The algorithmic-bytes entry of a timed call: the fused selection +
+    attention moves the attention's bytes."""
+    return {"select_sparse_decode": "sparse_decode"}.get(name, name)
+
+
 def source_of(name: str, case: qw.Case) -> str:
-    if name == "sparse_decode" and case.head_dim != 128:
+    if name == "sparse_decode" and (case.head_dim != 128 or case.rows_per_req > 1):
         return "qsa_sparse_decode"
     return KERNEL_SOURCE.get(name, "")
 
@@ -548,8 +554,7 @@ def measure(qsa, case, args, dev, rank, world, l2, peak_gbs, peak_kind, steps, h
     wl = "cfg%d" % case_index(case)
     kernels = {}
     for name, k in kern.items():
-        bkey = "sparse_decode" if name == "select_sparse_decode" else name
-        b = mean.get(bkey, 0.0)
+        b = mean.get(bytes_key(name), 0.0)
         t = k["stream_ms"]
         traffic, ncu_us = ncu_record(source_of(name, case), wl)
         kernels[name] = {"ms": t, "isolated_ms": k.get("isolated_ms"), "bytes": b,
@@ -557,7 +562,7 @@ def measure(qsa, case, args, dev, rank, world, l2, peak_gbs, peak_kind, steps, h
                          "ncu_us": ncu_us}
     dom = max(kern, key=lambda n: kern[n]["stream_ms"])
     dom_t = kern[dom]["stream_ms"]
-    dkey = "sparse_decode" if dom == "select_sparse_decode" else dom
+    dkey = bytes_key(dom)
     traffic, ncu_us = ncu_record(source_of(dom, case), wl)
     if dom == "sparse_prefill":
         # A contraction: useful FLOPs (4 * D per (row, head, attended token))

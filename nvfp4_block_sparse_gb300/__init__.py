@@ -45,10 +45,10 @@ class DecodeStep:
     """Device buffers for one QSA step of a fixed geometry, and the library
     calls that fill them: index scores -> top-k selection -> sparse decode,
     chained by programmatic dependent launch.  ``fused`` runs selection and
-    decode through qsa_select_sparse_decode instead (one launch for decode
-    rows; bit-identical results).  ``num_splits`` = 0 lets the library choose
-    the KV split count.  A geometry with more than MAX_DECODE_ROWS rows per
-    request (a context row group) runs qsa_sparse_prefill as its attention."""
+    decode through qsa_select_sparse_decode instead.  ``num_splits`` = 0 lets
+    the library choose the KV split count.  A geometry with more than
+    MAX_DECODE_ROWS rows per request (a context row group) runs
+    qsa_sparse_prefill as its attention."""
 
     def __init__(self, geom: dict, k: int, window: int, device="cuda", num_splits: int = 0,
                  fused: bool = False):
@@ -86,13 +86,19 @@ class DecodeStep:
         dev = self.scores.device
         ws = torch.empty_like(self.workspace)
         qsa_workspace_init(ws)
-        return dict(scores=torch.empty_like(self.scores), sel=torch.empty_like(self.sel),
-                    nsel=torch.empty_like(self.nsel), out=torch.empty_like(self.out),
-                    lse=torch.empty_like(self.lse), workspace=ws)
+        b = dict(scores=torch.empty_like(self.scores), sel=torch.empty_like(self.sel),
+                 nsel=torch.empty_like(self.nsel), out=torch.empty_like(self.out),
+                 lse=torch.empty_like(self.lse), workspace=ws)
+        return b
 
     def own_buffers(self) -> dict:
         return dict(scores=self.scores, sel=self.sel, nsel=self.nsel, out=self.out,
                     lse=self.lse, workspace=self.workspace)
+
+    def status(self) -> int:
+        """Device status word of this step's workspace: 0 when every bounded
+        wait completed."""
+        return qsa_workspace_status(self.workspace)
 
     def launches(self):
         """The step's library calls in order, as (name, fn) pairs; fn(w, bufs,

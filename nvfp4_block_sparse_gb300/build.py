@@ -16,7 +16,7 @@ SOURCES = ["qsa_api.cu", "qsa_index_scores.cu", "qsa_select_topk.cu", "qsa_spars
            "qsa_sparse_decode_noalloc.cu", "qsa_store_tokens.cu", "qsa_rollback.cu",
            "qsa_sparse_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
+FLAGS = ["-O3", "-lineinfo", "-std=c++20", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 
 
 def _nvcc() -> str:

@@ -1,20 +1,17 @@
-// qsa_attend.cu -- A3 at head_dim 128: split-KV sparse GQA over the selected
-// NVFP4 pages, each 64-token chunk dequantised ONCE for every query column of
-// the request (all R rows x the slice's query heads), partials merged by
-// log-sum-exp.
+// qsa_attend.cu -- A3 for decode rows at head_dim 128: split-KV sparse GQA
+// over the selected NVFP4 pages, each 64-token chunk shared by a group of
+// four warps, partials merged by log-sum-exp.
 //
 // TensorRT-LLM PR #20937 ("GB300 perf work on
 // qwen3_8_flash_next_nvfp4__sm_103__tp1"), What changes: NVFP4 sparse GQA
-// decode as split-K + merge, verify as request-grouped NVFP4 sparse GQA with a
-// per-row merge; Per-File QA: invalid-page handling and masking.  PR #20276
-// ("Qwen3.8-Flash-Next NVFP4 target"), Features table: uint8 e2m1 pages +
-// e4m3 block scales.
+// decode as split-K + merge with a lean one-split variant; Per-File QA:
+// invalid-page handling and masking.  PR #20276 ("Qwen3.8-Flash-Next NVFP4
+// target"), Features table: uint8 e2m1 pages + e4m3 block scales.
 //
-// One CTA = (request b, KV head g, head slice, KV split s).  Its query columns
-// are c = j * hs + hh: row j of the request, head hh of the slice (hs heads per
-// slice, so R * hs <= 32 columns, padded to NT tiles of 8).  The pages it reads
-// are the union of the rows' selections, in block order, each page with a mask
-// of the rows that selected it; split s takes union chunks s, s + splits, ...
+// One CTA = (request b, KV head g, head slice, KV split s); its query columns
+// are the slice's query heads (up to 32, padded to NT tiles of 8).  Split s
+// takes the row's selected chunks s, s + splits, ...  One CTA per SM: the
+// split count is planned so that the grid is one wave of clusters.
 //
 // Warp groups.  A group of four warps processes one chunk at a time:
 //   S^T = K . Q^T   warp w takes tokens [16w, 16w + 16) of the chunk, every
@@ -22,25 +19,25 @@
 //   P               fp16, written to a shared tile [column][token] (stmatrix)
 //   O^T += V^T.P^T  warp w takes dims [32w, 32w + 32) over all 64 tokens; V^T
 //                   fragments are built from two tokens' nibbles per byte
-// so each chunk's 16384 e2m1 values are converted once, whatever the number of
-// columns, and every warp's MMAs serve all columns (columns whose row did not
-// select the chunk are masked to -inf).  All warps of a group share one
-// softmax base per column, so O can be split by dims.  The base moves only
-// when a logit exceeds it by more than 2^8 (log2 domain): the common chunk
-// costs one group barrier (a barrier-reduction that also tells whether any
-// warp saw such a logit); the rare chunk that moves the base exchanges the
-// group's column maxima, rescales O and rewrites P.
+// so a chunk's last arrival is turned around by four warps, not one.  All
+// warps of a group share one softmax base per column, so O can be split by
+// dims.  The base moves only when a logit exceeds it by more than 2^8 (log2
+// domain): the common chunk costs one group barrier (a barrier-reduction
+// that also tells whether any warp saw such a logit); the rare chunk that
+// moves the base exchanges the group's column maxima, rescales O and
+// rewrites P.
 //
 // Chunks stream in with TMA bulk copies (K codes 4 KB, V codes 4 KB, K and V
 // scales 512 B each, contiguous in the pools) into per-group stages under
-// mbarriers; every stage of the CTA is requested before the first chunk is
-// processed, and a stage is refilled as soon as the group has finished it.
+// mbarriers; every group requests all of its stages before its first chunk
+// (four copy issuers per SM), and refills a stage as soon as it has finished
+// it.  Waits sleep in hardware instead of spinning.
 //
-// Merge: each group's state (m, l per warp, O) is a partial record.  Up to 8
+// Merge: each group's state (m, l per warp, O) is a partial record.  Up to 16
 // splits form a thread-block cluster and push their records into the merging
-// rank's shared memory (column c is merged by rank c mod splits); more splits
-// write records to the workspace and the last CTA of the unit to take its
-// ticket merges them.  Every merge runs in a fixed order (deterministic).
+// rank's shared memory (column c is merged by rank c mod splits); otherwise
+// records go to the workspace and the last CTA of the unit to take its ticket
+// merges them.  Every merge runs in a fixed order (deterministic).
 //
 // Every wait is bounded (2 s): a wait that gives up records a status word in
 // the workspace, stops further copies, lets the copies in flight land and the
@@ -196,6 +193,13 @@ __device__ __forceinline__ void stsm_x2_trans(uint32_t addr, uint32_t r0, uint32
                : "memory");
 }
 
+// Position of 16-byte unit j (dims 8j .. 8j + 7) in row c of the query tile:
+// a lane (gid, tig) reads unit 4 tig + wd of row nt*8 + gid, and the swizzle
+// gives the eight rows' reads of one quarter-warp distinct bank groups.
+__device__ __forceinline__ int qunit(int c, int j) {
+  return j ^ ((j >> 3) & 1) ^ (2 * (c & 1));
+}
+
 // Shared-memory layout (bytes), shared by host sizing and the kernel.
 template <int NT, int NG, int SG>
 struct Lay {
@@ -214,29 +218,25 @@ struct Lay {
     const int per = (kCols + cl - 1) / cl;
     return cl * NG * per * kRec;
   }
-  // sel rows + union (block|mask, page) for verify; chunk list for decode
-  __host__ __device__ static int list_ints(int R, int k, int mb, int list_cap) {
-    const int ver = R * k + 2 * (R * k < mb ? R * k : mb) + 4;
-    const int dec = 2 * list_cap + 4;
-    return R > 1 ? ver : dec;
-  }
-  static size_t bytes(int R, int k, int mb, int cl, int list_cap) {
+  // this CTA's chunk list: (page, first token) pairs
+  __host__ __device__ static int list_ints(int list_cap) { return 2 * list_cap + 4; }
+  static size_t bytes(int mb, int cl, int list_cap) {
     size_t off = (size_t)kStagesB + kBarB + kQB + kPB + kRedB + kColB + kMiscB;
     off += (size_t)rb_floats(cl) * 4;
-    off += (size_t)list_ints(R, k, mb, list_cap) * 4;
+    off += (size_t)list_ints(list_cap) * 4;
     off += mb <= kPtMax ? (size_t)mb * 4 : 0;
     return (off + 127) & ~(size_t)127;
   }
 };
 
-template <int NT, int NG>
-constexpr int min_blocks() {
-  return 1;
-}
 
-template <int NT, int NG, int SG>
-__global__ void __launch_bounds__(Lay<NT, NG, SG>::kThreads, (min_blocks<NT, NG>()))
-attend_kernel(Params p) {
+// One (request b, KV head kvh, head slice, split s) unit of work by the whole
+// CTA.  wait_before_list() runs after the prologue (the queries, the page-table
+// row and the length are in shared memory), before the row's selection is
+// read; after_list() once this CTA's chunk list is built.
+template <int NT, int NG, int SG, class Wait, class After>
+__device__ __forceinline__ void attend_cta(const Params& p, int s, int kvh, int slice, int b,
+                                           Wait&& wait_before_list, After&& after_list) {
   using L = Lay<NT, NG, SG>;
   constexpr int kCols = L::kCols;
   constexpr int kThreads = L::kThreads;
@@ -248,9 +248,6 @@ attend_kernel(Params p) {
   const int warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int grp = warp / kGW, wg = warp % kGW;
-  const int s = blockIdx.x;                            // KV split (= cluster rank)
-  const int kvh = blockIdx.y / p.slices, slice = blockIdx.y % p.slices;
-  const int b = blockIdx.z;
   const int hs = p.hs;
   const int h0 = slice * hs;
   const int hreal = min(hs, G - h0);
@@ -278,13 +275,8 @@ attend_kernel(Params p) {
   float* rb = reinterpret_cast<float*>(smem + off);
   off += (size_t)L::rb_floats(CL > 0 ? CL : 1) * 4;
   int32_t* lists = reinterpret_cast<int32_t*>(smem + off);
-  off += (size_t)L::list_ints(R, k, g.MB, p.list_cap) * 4;
+  off += (size_t)L::list_ints(p.list_cap) * 4;
   int32_t* s_pt = reinterpret_cast<int32_t*>(smem + off);
-  // verify: sel rows, then union entries (block | mask << 24) and pages
-  int32_t* s_sel = lists;
-  const int umax = R * k < g.MB ? R * k : g.MB;
-  int32_t* s_union = lists + R * k;
-  int32_t* s_upage = s_union + umax;
 
   if (tid == 0) {
     for (int i = 0; i < NG * SG; ++i) mbar_init(&full[i], 1);
@@ -328,7 +320,9 @@ attend_kernel(Params p) {
     sq = sq > 126 ? 126 : (sq < -126 ? -126 : sq);
     const float up = __uint_as_float((uint32_t)(sq + 127) << 23);
     const float down = __uint_as_float((uint32_t)(127 - sq) << 23);
-    __half2* dst = reinterpret_cast<__half2*>(qs + c * kD + 4 * lane);
+    // 16-byte unit j = lane / 2 of the row sits at qunit(c, j) (a swizzle
+    // that spreads the fragment reads below over all banks).
+    __half2* dst = reinterpret_cast<__half2*>(qs + c * kD + 8 * qunit(c, lane >> 1) + 4 * (lane & 1));
     dst[0] = __floats2half2_rn(v0 * up, v1 * up);
     dst[1] = __floats2half2_rn(v2 * up, v3 * up);
     if (lane == 0) {
@@ -337,114 +331,56 @@ attend_kernel(Params p) {
       col_row[c] = real ? j : -1;
     }
   }
-  // verify: per-block row masks (one byte per block) in the idle stages
-  uint32_t* s_rm = reinterpret_cast<uint32_t*>(stages);
-  if (R > 1)
-    for (int i = tid; i < (g.MB + 3) >> 2; i += kThreads) s_rm[i] = 0u;
   if (tid == 0) misc[1] = 0;   // set when a bounded wait gives up
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
-  pdl_wait();   // the selections come from the preceding kernel
+  wait_before_list();   // the selections come from an earlier kernel or CTA
 
   // ---- this CTA's chunks ----------------------------------------------------
-  int nch = 0;
-  if (R == 1) {
-    // Candidate chunk c of the row (entry c >> csh, part c & csh) belongs to
-    // split c mod splits; entries repeating their predecessor (the selection
-    // is ascending) or on an invalid page are dropped.
-    if (warp == 0) {
-      const int nc = k << csh;
-      const int32_t* selrow = p.sel + (size_t)b * k;
-      int cnt = 0;
-      for (int m0 = 0;; m0 += 32) {
-        if (s + (long long)p.splits * m0 >= nc) break;
-        const long long c = s + (long long)p.splits * (m0 + lane);
-        int page = -1, tok0 = 0;
-        if (c < nc) {
-          const int e = (int)(c >> csh);
-          const int beta = selrow[e];
-          const int prev = e > 0 ? selrow[e - 1] : -1;
-          if (beta >= 0 && beta < g.MB && beta != prev) {
-            const int pg = pt_smem ? s_pt[beta] : p.page_table[(size_t)b * g.MB + beta];
-            if (pg >= 0 && pg < g.NP) {
-              page = pg;
-              tok0 = beta * g.P + (int)(c & csh) * kChunk;
-            }
-          }
-        }
-        const unsigned vm = __ballot_sync(0xffffffffu, page >= 0);
-        if (page >= 0) {
-          const int q = cnt + __popc(vm & ((1u << lane) - 1u));
-          if (q < p.list_cap) {
-            lists[2 * q] = page;
-            lists[2 * q + 1] = tok0;
-          }
-        }
-        cnt += __popc(vm);
-      }
-      if (lane == 0) misc[0] = min(cnt, p.list_cap);
-    }
-    __syncthreads();
-    nch = misc[0];
-  } else {
-    // Row masks: every selection entry ors its row's bit into its block.
-    for (int i = tid; i < R * k; i += kThreads) {
-      const int v = p.sel[(size_t)b * R * k + i];
-      s_sel[i] = v;
-      if (v >= 0 && v < g.MB) atomicOr(&s_rm[v >> 2], (1u << (i / k)) << (8 * (v & 3)));
-    }
-    __syncthreads();
-    // Union = blocks with a mask and a valid page, compacted in block order.
-    const uint8_t* rm = reinterpret_cast<const uint8_t*>(s_rm);
-    const int per_b = (g.MB + kThreads - 1) / kThreads;
-    const int b_lo = min(g.MB, tid * per_b), b_hi = min(g.MB, b_lo + per_b);
+  // Candidate chunk c of the row (entry c >> csh, part c & csh) belongs to
+  // split c mod splits; entries repeating their predecessor (the selection is
+  // ascending) or on an invalid page are dropped.
+  if (warp == 0) {
+    const int nc = k << csh;
+    const int32_t* selrow = p.sel + (size_t)b * k;
     int cnt = 0;
-    for (int beta = b_lo; beta < b_hi; ++beta) {
-      if (rm[beta] == 0) continue;
-      const int page = pt_smem ? s_pt[beta] : p.page_table[(size_t)b * g.MB + beta];
-      cnt += (page >= 0 && page < g.NP) ? 1 : 0;
-    }
-    int x = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) misc[8 + warp] = x;
-    __syncthreads();
-    int pos = x - cnt;
-    for (int w = 0; w < warp; ++w) pos += misc[8 + w];
-    for (int beta = b_lo; beta < b_hi; ++beta) {
-      const int mask = rm[beta];
-      if (mask == 0) continue;
-      const int page = pt_smem ? s_pt[beta] : p.page_table[(size_t)b * g.MB + beta];
-      if (page >= 0 && page < g.NP) {
-        s_union[pos] = beta | (mask << 24);
-        s_upage[pos] = page;
-        ++pos;
+    for (int m0 = 0;; m0 += 32) {
+      if (s + (long long)p.splits * m0 >= nc) break;
+      const long long c = s + (long long)p.splits * (m0 + lane);
+      int page = -1, tok0 = 0;
+      if (c < nc) {
+        const int e = (int)(c >> csh);
+        const int beta = __ldcg(selrow + e);
+        const int prev = e > 0 ? __ldcg(selrow + e - 1) : -1;
+        if (beta >= 0 && beta < g.MB && beta != prev) {
+          const int pg = pt_smem ? s_pt[beta] : p.page_table[(size_t)b * g.MB + beta];
+          if (pg >= 0 && pg < g.NP) {
+            page = pg;
+            tok0 = beta * g.P + (int)(c & csh) * kChunk;
+          }
+        }
       }
+      const unsigned vm = __ballot_sync(0xffffffffu, page >= 0);
+      if (page >= 0) {
+        const int q = cnt + __popc(vm & ((1u << lane) - 1u));
+        if (q < p.list_cap) {
+          lists[2 * q] = page;
+          lists[2 * q + 1] = tok0;
+        }
+      }
+      cnt += __popc(vm);
     }
-    if (tid == kThreads - 1) misc[0] = pos;   // the last thread's end is the total
-    __syncthreads();
-    const int C = misc[0] << csh;
-    nch = C > s ? (C - s + p.splits - 1) / p.splits : 0;
+    if (lane == 0) misc[0] = min(cnt, p.list_cap);
   }
-  pdl_trigger();
+  __syncthreads();
+  const int nch = misc[0];
+  after_list();
 
-  // Chunk m of this CTA: union chunk c = s + m * splits.
+  // Chunk m of this CTA: candidate chunk s + m * splits of the row.
   auto chunk_of = [&](int m, int& page, int& tok0, int& mask) {
-    if (R == 1) {
-      page = lists[2 * m];
-      tok0 = lists[2 * m + 1];
-      mask = 1;
-    } else {
-      const int c = s + m * p.splits;
-      const int u = c >> csh;
-      const int e = s_union[u];
-      page = s_upage[u];
-      tok0 = (e & 0xFFFFFF) * g.P + (c & csh) * kChunk;
-      mask = (e >> 24) & 0xFF;
-    }
+    page = lists[2 * m];
+    tok0 = lists[2 * m + 1];
+    mask = 1;
   };
   const uint64_t pol = policy_evict_first();
   // Chunk m goes to group m % NG, its stage (m / NG) % SG.
@@ -468,25 +404,29 @@ attend_kernel(Params p) {
   }
 
   // ---- per-column state and fragments --------------------------------------
+  // Per lane column: cq, and the row (low 4 bits, 15 = padding) with the
+  // row's visible tokens (upper bits) in one word.
   float cq[NT][2];
-  int cn[NT][2], crow[NT][2];
+  int crn[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int c = nt * 8 + 2 * tig + e;
       cq[nt][e] = col_cq[c];
-      cn[nt][e] = col_n[c];
-      crow[nt][e] = col_row[c];
+      crn[nt][e] = (col_n[c] << 4) | (col_row[c] < 0 ? 15 : col_row[c]);
     }
-  // Q^T fragments: column nt*8 + gid, dims [32 tig, 32 tig + 32).
+  auto crow_of = [&](int nt, int e) { return crn[nt][e] & 15; };   // 15: padding
+  auto cn_of = [&](int nt, int e) { return crn[nt][e] >> 4; };
+  // Q^T fragments: column nt*8 + gid, dims [32 tig, 32 tig + 32) = units
+  // 4 tig .. 4 tig + 3 of the row.
   uint32_t qf[NT][16];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const uint4* src = reinterpret_cast<const uint4*>(qs + (nt * 8 + gid) * kD + 32 * tig);
+    const int c = nt * 8 + gid;
 #pragma unroll
     for (int v4 = 0; v4 < 4; ++v4) {
-      const uint4 x = src[v4];
+      const uint4 x = *reinterpret_cast<const uint4*>(qs + c * kD + 8 * qunit(c, 4 * tig + v4));
       qf[nt][4 * v4 + 0] = x.x; qf[nt][4 * v4 + 1] = x.y;
       qf[nt][4 * v4 + 2] = x.z; qf[nt][4 * v4 + 3] = x.w;
     }
@@ -514,9 +454,9 @@ attend_kernel(Params p) {
     int r = 0;
 #pragma unroll
     for (int e = 0; e < 2; ++e)
-      if (crow[nt][e] >= 0) {
-        r |= 1 << crow[nt][e];
-        nmin = min(nmin, cn[nt][e]);
+      if (crow_of(nt, e) != 15) {
+        r |= 1 << crow_of(nt, e);
+        nmin = min(nmin, cn_of(nt, e));
       }
     r |= __shfl_xor_sync(0xffffffffu, r, 1);
     r |= __shfl_xor_sync(0xffffffffu, r, 2);
@@ -613,13 +553,14 @@ attend_kernel(Params p) {
     const int tokA = tok0 + 16 * wg + rA, tokB = tokA + 8;
     const bool partial = tok0 + kChunk > nmin;
     bool exceed = false;
-    float tA[NT][2], tB[NT][2];
+    // From here sacc[nt][e] / sacc[nt][2 + e] hold the logits t of the
+    // lane's tokens A / B.
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       if (!act[nt]) continue;
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const bool on = crow[nt][e] >= 0 && ((mask >> crow[nt][e]) & 1);
+        const bool on = ((mask >> crow_of(nt, e)) & 1) != 0;   // padding: bit 15 is 0
         const bool nobase = base[nt][e] == -INFINITY;
         const float c = on ? cq[nt][e] : 0.f;
         const float nb = on ? (nobase ? 0.f : -base[nt][e]) : -INFINITY;
@@ -627,28 +568,30 @@ attend_kernel(Params p) {
         float za = fmaf(sacc[nt][e], c, nb);
         float zb = fmaf(sacc[nt][2 + e], c, nb);
         if (partial) {
-          const int lim = on ? cn[nt][e] : 0;
+          const int lim = on ? cn_of(nt, e) : 0;
           za = tokA < lim ? za : -INFINITY;
           zb = tokB < lim ? zb : -INFINITY;
         }
-        tA[nt][e] = za;
-        tB[nt][e] = zb;
+        sacc[nt][e] = za;
+        sacc[nt][2 + e] = zb;
         exceed |= (za > thr) | (zb > thr);
       }
     }
     __half* pt = ptile + (size_t)((grp * 2 + (l & 1)) * kCols) * kPRow;
-    float pA[NT][2], pB[NT][2];
+    float psum[NT][2];
     auto write_p = [&]() {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         if (!act[nt]) continue;
+        float pa[2], pb[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          pA[nt][e] = exp2f(tA[nt][e]);
-          pB[nt][e] = exp2f(tB[nt][e]);
+          pa[e] = exp2f(sacc[nt][e]);
+          pb[e] = exp2f(sacc[nt][2 + e]);
+          psum[nt][e] = pa[e] + pb[e];
         }
-        const uint32_t r0 = pack_half2(pA[nt][0], pA[nt][1]);
-        const uint32_t r1 = pack_half2(pB[nt][0], pB[nt][1]);
+        const uint32_t r0 = pack_half2(pa[0], pa[1]);
+        const uint32_t r1 = pack_half2(pb[0], pb[1]);
         // lanes 0-7: rows (columns) of positions 0-7, lanes 8-15: positions 8-15
         const int rr = lane & 7, half = (lane >> 3) & 1;
         stsm_x2_trans(smem_u32(pt + (nt * 8 + rr) * kPRow + 16 * wg + 8 * half), r0, r1);
@@ -663,7 +606,7 @@ attend_kernel(Params p) {
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          float v = act[nt] ? fmaxf(tA[nt][e], tB[nt][e]) : -INFINITY;
+          float v = act[nt] ? fmaxf(sacc[nt][e], sacc[nt][2 + e]) : -INFINITY;
           v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
           v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
           v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
@@ -689,8 +632,8 @@ attend_kernel(Params p) {
               o[dt][nt][e] *= alpha;
               o[dt][nt][2 + e] *= alpha;
             }
-            tA[nt][e] -= cm;
-            tB[nt][e] -= cm;
+            sacc[nt][e] -= cm;
+            sacc[nt][2 + e] -= cm;
             base[nt][e] = nbv;
           }
         }
@@ -702,7 +645,7 @@ attend_kernel(Params p) {
     for (int nt = 0; nt < NT; ++nt)
       if (act[nt])
 #pragma unroll
-        for (int e = 0; e < 2; ++e) lsum[nt][e] += pA[nt][e] + pB[nt][e];
+        for (int e = 0; e < 2; ++e) lsum[nt][e] += psum[nt][e];
 
     // The stage of the group's previous chunk is free: every warp has passed
     // this chunk's barrier, so their reads of it are done.
@@ -902,6 +845,14 @@ attend_kernel(Params p) {
   if (tid == 0) atomicExch(&p.tickets[unit], 0);
 }
 
+template <int NT, int NG, int SG>
+__global__ void __launch_bounds__(Lay<NT, NG, SG>::kThreads, 1)
+attend_kernel(Params p) {
+  attend_cta<NT, NG, SG>(
+      p, blockIdx.x, blockIdx.y / p.slices, blockIdx.y % p.slices, blockIdx.z,
+      [] { pdl_wait(); }, [] { pdl_trigger(); });
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -909,9 +860,16 @@ attend_kernel(Params p) {
 constexpr size_t kWsHeader = 256;
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Variants: (NT column tiles, NG warp groups, SG stages per group), one CTA
-// per SM with 16 stages (147 KB): 16 warps for one column tile, 8 warps for
-// wider ones (their fragments take 130 to 250 registers).
+// Kernel variants: one CTA per SM with 16 stages (147 KB), 16 warps for one
+// column tile and 8 warps for wider ones (their fragments take 160 to 240
+// registers).
+template <int NT_, int NG_, int SG_>
+struct Var {
+  static constexpr int NT = NT_, NG = NG_, SG = SG_;
+  using L = Lay<NT_, NG_, SG_>;
+  static constexpr auto kernel = attend_kernel<NT_, NG_, SG_>;
+};
+// X(NT, NG, SG)
 #define QSA_ATT_VARIANTS(X) \
   X(1, 4, 4)                \
   X(2, 2, 8)                \
@@ -930,23 +888,22 @@ int heads_per_slice(const Geom& g) {
 
 int ntiles(const Geom& g) { return (g.R * heads_per_slice(g) + 7) / 8; }
 
-
 int list_cap_for(const Geom& g, int k, int splits) {
   const int cpp = g.P / kChunk;
   return (k * cpp + splits - 1) / splits;
 }
 
-template <int NT, int NG, int SG>
+template <class V>
 size_t smem_for(const Geom& g, int k, int cl, int splits) {
-  return Lay<NT, NG, SG>::bytes(g.R, k, g.MB, cl, list_cap_for(g, k, splits));
+  return V::L::bytes(g.MB, cl, list_cap_for(g, k, splits));
 }
 
-template <int NT, int NG, int SG>
+template <class V>
 cudaLaunchConfig_t make_config(dim3 grid, size_t smem, cudaStream_t stream,
                                cudaLaunchAttribute* attr, bool pdl, int cluster) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(Lay<NT, NG, SG>::kThreads);
+  cfg.blockDim = dim3(V::L::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   int n = 0;
@@ -967,9 +924,15 @@ cudaLaunchConfig_t make_config(dim3 grid, size_t smem, cudaStream_t stream,
   return cfg;
 }
 
+template <class V>
+void set_smem_attr(size_t smem, int cl) {
+  cudaFuncSetAttribute(V::kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (cl > 8) cudaFuncSetAttribute(V::kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+}
+
 // Clusters of `cl` CTAs of this variant that can be resident at once (0 when
 // none can); sizes above 8 need the non-portable cluster attribute.
-template <int NT, int NG, int SG>
+template <class V>
 int cluster_capacity(int cl, size_t smem) {
   struct Entry { int dev, cl; size_t smem; int n; };
   static std::mutex mu;
@@ -982,15 +945,11 @@ int cluster_capacity(int cl, size_t smem) {
     for (const Entry& e : cache)
       if (e.dev == dev && e.cl == cl && e.smem == smem) return e.n;
   }
-  cudaFuncSetAttribute(attend_kernel<NT, NG, SG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)smem);
-  if (cl > 8)
-    cudaFuncSetAttribute(attend_kernel<NT, NG, SG>,
-                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  set_smem_attr<V>(smem, cl);
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = make_config<NT, NG, SG>(dim3(cl, 1, 1), smem, 0, attr, false, cl);
+  cudaLaunchConfig_t cfg = make_config<V>(dim3(cl, 1, 1), smem, 0, attr, false, cl);
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, attend_kernel<NT, NG, SG>, &cfg) != cudaSuccess) n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, V::kernel, &cfg) != cudaSuccess) n = 0;
   cudaGetLastError();
   std::lock_guard<std::mutex> lock(mu);
   cache.push_back({dev, cl, smem, n});
@@ -1000,67 +959,58 @@ int cluster_capacity(int cl, size_t smem) {
 // Largest split count (up to a 16-CTA cluster) that keeps the grid in one
 // wave: units * splits CTAs resident at once, every cluster of `splits`
 // co-resident, and at least one chunk per warp group.
-template <int NT, int NG, int SG>
+template <class V>
 int plan_splits(const Geom& g, int k, long long units, int max_chunks) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaGetLastError();
-  const size_t smem1 = smem_for<NT, NG, SG>(g, k, 1, 1);
-  cudaFuncSetAttribute(attend_kernel<NT, NG, SG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)smem1);
+  const size_t smem1 = smem_for<V>(g, k, 1, 1);
+  set_smem_attr<V>(smem1, 1);
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attend_kernel<NT, NG, SG>,
-                                                    Lay<NT, NG, SG>::kThreads, smem1) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, V::kernel, V::L::kThreads, smem1) !=
       cudaSuccess)
     per_sm = 1;
   cudaGetLastError();
   const long long slots = (long long)sms * (per_sm < 1 ? 1 : per_sm);
   int best = 1;
   for (int sp = 2; sp <= kMaxCl; ++sp) {
-    if (units * sp > slots || max_chunks / sp < NG) break;
-    const int cap = cluster_capacity<NT, NG, SG>(sp, smem_for<NT, NG, SG>(g, k, sp, sp));
-    if (cap >= units) best = sp;
+    if (units * sp > slots || max_chunks / sp < V::NG) break;
+    const int cap = cluster_capacity<V>(sp, smem_for<V>(g, k, sp, sp));
+    if (cap * sp >= units * sp && cap >= units) best = sp;
   }
   return best;
 }
 
-int variant_splits(const Geom& g, int k, long long units, int max_chunks) {
-  const int nt = ntiles(g);
-#define X(NT_, NG_, SG_) if (nt == NT_) return plan_splits<NT_, NG_, SG_>(g, k, units, max_chunks);
-  QSA_ATT_VARIANTS(X)
-#undef X
-  return 1;
-}
-
-template <int NT, int NG, int SG>
+template <class V>
 cudaError_t launch_t(Params prm, dim3 grid, const Geom& g, int k, bool pdl, cudaStream_t stream) {
   int cl = 1;
   if (prm.splits > 1 && prm.splits <= kMaxCl) {
-    const size_t smem_cl = smem_for<NT, NG, SG>(g, k, prm.splits, prm.splits);
-    if (cluster_capacity<NT, NG, SG>(prm.splits, smem_cl) > 0) cl = prm.splits;
+    const size_t smem_cl = smem_for<V>(g, k, prm.splits, prm.splits);
+    if (cluster_capacity<V>(prm.splits, smem_cl) > 0) cl = prm.splits;
   }
   prm.cluster = cl;
-  const size_t smem = smem_for<NT, NG, SG>(g, k, prm.splits == 1 ? 1 : (cl > 1 ? cl : 1),
-                                           prm.splits);
-  cudaError_t e = cudaFuncSetAttribute(attend_kernel<NT, NG, SG>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  if (cl > 8) {
-    e = cudaFuncSetAttribute(attend_kernel<NT, NG, SG>,
-                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-  }
+  const size_t smem = smem_for<V>(g, k, prm.splits == 1 ? 1 : (cl > 1 ? cl : 1), prm.splits);
+  set_smem_attr<V>(smem, cl);
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = make_config<NT, NG, SG>(grid, smem, stream, attr, pdl, cl);
-  return cudaLaunchKernelEx(&cfg, attend_kernel<NT, NG, SG>, prm);
+  cudaLaunchConfig_t cfg = make_config<V>(grid, smem, stream, attr, pdl, cl);
+  return cudaLaunchKernelEx(&cfg, V::kernel, prm);
+}
+
+// Runs fn.template operator()<V>() for the variant serving g.
+template <class F>
+auto with_variant(const Geom& g, F&& fn) -> decltype(fn.template operator()<Var<1, 4, 4>>()) {
+  const int nt = ntiles(g);
+#define X(NT_, NG_, SG_) \
+  if (nt == NT_) return fn.template operator()<Var<NT_, NG_, SG_>>();
+  QSA_ATT_VARIANTS(X)
+#undef X
+  return fn.template operator()<Var<1, 4, 4>>();
 }
 
 }  // namespace att
 
-// Whether this kernel serves the geometry: decode rows (one row per request)
-// at head_dim 128.  Verify rows run the per-row-warp kernel, which keeps more
-// independent warps per SM on their larger column sets.
+// Whether this kernel serves the geometry: decode rows at head_dim 128.
 bool attend_supports(const Geom& g) { return g.D == att::kD && g.R == 1; }
 
 DecodePlan plan_attend(const Geom& g, int k, int num_splits) {
@@ -1075,12 +1025,10 @@ DecodePlan plan_attend(const Geom& g, int k, int num_splits) {
   const int max_union = min(g.R * k, g.MB);
   const int max_chunks = max(1, max_union * cpp);
   int splits = num_splits;
-  if (splits <= 0) splits = att::variant_splits(g, k, units, max_chunks);
+  if (splits <= 0)
+    splits = att::with_variant(g, [&]<class V>() { return att::plan_splits<V>(g, k, units, max_chunks); });
   pl.splits = splits;
-  int ng = 1;
-#define X(NT_, NG_, SG_) if (nt == NT_) ng = NG_;
-  QSA_ATT_VARIANTS(X)
-#undef X
+  const int ng = att::with_variant(g, [&]<class V>() { return V::NG; });
   size_t ws = att::kWsHeader + att::align256((size_t)units * sizeof(int));
   if (splits > 1) ws += (size_t)units * splits * ng * pl.cols * att::kRec * sizeof(float);
   pl.ws_bytes = ws;
@@ -1114,12 +1062,9 @@ cudaError_t launch_attend(const Geom& g, const DecodePlan& plan, const void* q,
   prm.list_cap = att::list_cap_for(g, k, plan.splits);
   prm.wait_ns = wait_limit_ns();
   dim3 grid(plan.splits, g.Hkv * plan.qgroups, g.B);
-  const int nt = att::ntiles(g);
-#define X(NT_, NG_, SG_) \
-  if (nt == NT_) return att::launch_t<NT_, NG_, SG_>(prm, grid, g, k, pdl, stream);
-  QSA_ATT_VARIANTS(X)
-#undef X
-  return cudaErrorInvalidValue;
+  return att::with_variant(g, [&]<class V>() {
+    return att::launch_t<V>(prm, grid, g, k, pdl, stream);
+  });
 }
 
 }  // namespace qsa

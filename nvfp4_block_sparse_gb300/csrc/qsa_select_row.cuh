@@ -47,7 +47,9 @@ __device__ __forceinline__ uint32_t sel_order_key(int s) { return (uint32_t)s ^ 
 
 // Selects row `src` (nb visible blocks of which the last W are the window) into
 // out[0..k) and returns the count (also written to *nsel by thread 0).
-template <int NTHREADS>
+// kFromL2: read the row past L1 (it was just written by other CTAs of the
+// same kernel).
+template <int NTHREADS, bool kFromL2 = false>
 __device__ void select_row(const int32_t* __restrict__ src, int nb, int W, int k,
                            int32_t* __restrict__ out, int32_t* __restrict__ nsel,
                            uint8_t* smem) {
@@ -74,7 +76,7 @@ __device__ void select_row(const int32_t* __restrict__ src, int nb, int W, int k
   int nwin = 0, ncand = 0;
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
   for (int i = tid; i < nb; i += NTHREADS) {
-    const int s = src[i];
+    const int s = kFromL2 ? __ldcg(src + i) : src[i];
     row[i] = s;
     if (s == kSentinel) continue;
     if (i >= wlo) {

@@ -29,7 +29,7 @@ def run_gpu(qsa, w, num_splits=0, window=None, k=None):
     step.run(w)
     torch.cuda.synchronize()
     # A bounded wait that gave up leaves a status in the workspace.
-    assert qsa.qsa_workspace_status(step.workspace) == 0
+    assert step.status() == 0
     return step
 
 
@@ -219,7 +219,7 @@ def test_cuda_graph_replay_matches_eager(qsa):
 def test_workspace_status_clean(qsa):
     w = qw.make_workload(qw.small(qw.CONFIGS[1]), "cuda")
     step = run_gpu(qsa, w)
-    assert qsa.qsa_workspace_status(step.workspace) == 0
+    assert step.status() == 0
 
 
 def test_workspace_too_small_is_rejected(qsa):
@@ -301,7 +301,7 @@ def test_fused_selection_matches_composed(qsa, name, make, splits):
                             num_splits=splits, fused=True)
     step_f.run(w)
     torch.cuda.synchronize()
-    assert qsa.qsa_workspace_status(step_f.workspace) == 0
+    assert step_f.status() == 0
     ra, rc = host(step_f), host(c)
     for key in ("scores", "sel", "nsel", "out", "lse"):
         np.testing.assert_array_equal(ra[key], rc[key], err_msg=key)

@@ -26,7 +26,7 @@ def run_step(qsa, w):
     assert step.prefill
     step.run(w)
     torch.cuda.synchronize()
-    assert qsa.qsa_workspace_status(step.workspace) == 0
+    assert step.status() == 0
     return step
 
 

@@ -101,7 +101,7 @@ def test_store_then_step_matches_the_oracle(qsa, cfg):
     step = qsa.DecodeStep(qw.geometry(w), w["k"], w["window"], device=w["q"].device)
     step.run(w)
     torch.cuda.synchronize()
-    assert qsa.qsa_workspace_status(step.workspace) == 0
+    assert step.status() == 0
     ref = oracle.step(qw.to_numpy(w))
     np.testing.assert_array_equal(step.scores.cpu().numpy(), ref["scores"])
     np.testing.assert_array_equal(step.sel.cpu().numpy(), ref["sel"])
