@@ -415,6 +415,23 @@ qsa_status_t qsa_sparse_prefill(const qsa_geom_t *geom, const void *q_bf16,
 void qsa_debug_set_wait_ns(unsigned long long ns);
 
 /*
+ * Diagnostics: the bounds-checked build (compiled with QSA_DEBUG_BOUNDS)
+ * checks, in every kernel, the indices it derives from data before the access
+ * (page ids and token offsets of the copies it issues, chunk-list, union and
+ * selection slots in shared memory, output rows, workspace units); a failed
+ * check records its code in a device word -- the first failure per source
+ * file wins -- and skips the access, never trapping.  This call returns the
+ * first nonzero code over the library's source files on the current device
+ * and clears them all (it synchronises the device): 0 when every check held,
+ * -1 in a build without the checks (the normal library) or on a CUDA error.
+ * Codes are 0xF0S: F the source file (1 decode-row attention, 2 decode and
+ * verify attention, 3 index scores, 4 selection, 5 token store, 6 rollback,
+ * 7 row-tile attention), S the check.  Not thread-safe against concurrent
+ * calls of the library.
+ */
+int qsa_debug_bounds_status(void);
+
+/*
  * Reads the workspace's device status word (synchronising `stream`): 0 when
  * every bounded wait since qsa_workspace_init() completed, otherwise a
  * nonzero code and QSA_ERR_DEVICE_TIMEOUT is returned.  Diagnostic only.

@@ -16,6 +16,7 @@ from .binding import (EXPORTS, QsaError, load, make_geom, qsa_geom_t, qsa_index_
                       qsa_select_sparse_decode, qsa_select_sparse_decode_fused,
                       qsa_select_topk, qsa_sparse_decode, qsa_sparse_decode_ex, qsa_sparse_decode_noalloc,
                       qsa_sparse_decode_noalloc_status, qsa_debug_set_wait_ns,
+                      qsa_debug_bounds_status, bounds_checked, library_path,
                       qsa_sparse_decode_workspace_bytes, qsa_sparse_decode_workspace_bytes_ex,
                       qsa_rollback_gather, qsa_rollback_restore, qsa_rollback_state_bytes,
                       qsa_sparse_prefill, qsa_sparse_prefill_workspace_bytes,
@@ -26,7 +27,8 @@ __all__ = [
     "EXPORTS", "QsaError", "load", "make_geom", "qsa_geom_t", "qsa_index_scores",
     "qsa_select_sparse_decode", "qsa_select_sparse_decode_fused",
     "qsa_select_topk", "qsa_sparse_decode", "qsa_sparse_decode_ex", "qsa_sparse_decode_noalloc",
-    "qsa_sparse_decode_noalloc_status", "qsa_debug_set_wait_ns",
+    "qsa_sparse_decode_noalloc_status", "qsa_debug_set_wait_ns", "qsa_debug_bounds_status",
+    "bounds_checked", "library_path",
     "qsa_sparse_decode_workspace_bytes", "qsa_sparse_decode_workspace_bytes_ex",
     "qsa_rollback_gather", "qsa_rollback_restore", "qsa_rollback_state_bytes",
     "qsa_sparse_prefill", "qsa_sparse_prefill_workspace_bytes",

@@ -33,6 +33,7 @@ EXPORTS = (
     "qsa_sparse_decode_noalloc",
     "qsa_sparse_decode_noalloc_status",
     "qsa_debug_set_wait_ns",
+    "qsa_debug_bounds_status",
     "qsa_workspace_status",
     "qsa_store_kv_tokens",
     "qsa_select_sparse_decode",
@@ -61,20 +62,26 @@ _lib = None
 _vp = ctypes.c_void_p
 
 
+def bounds_checked() -> bool:
+    """True when QSA_BOUNDS_CHECKED=1 selects the bounds-checked library."""
+    return os.environ.get("QSA_BOUNDS_CHECKED", "") == "1"
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _build.BOUNDS_LIB if bounds_checked() else _build.LIB
 
 
 def load(build_if_missing: bool = False):
-    """Loads libqsa.so (building it first only when asked)."""
+    """Loads libqsa.so, or libqsa_bounds.so under QSA_BOUNDS_CHECKED=1
+    (building first only when asked)."""
     global _lib
     if _lib is not None:
         return _lib
-    path = _build.LIB
+    path = library_path()
     if not os.path.exists(path):
         if not build_if_missing:
-            raise ImportError("libqsa.so is not built (run __graft_entry__.build() or "
-                              "python -m nvfp4_block_sparse_gb300.build)")
+            raise ImportError("%s is not built (run __graft_entry__.build() or "
+                              "python -m nvfp4_block_sparse_gb300.build)" % os.path.basename(path))
         _build.build()
     lib = ctypes.CDLL(path)
     G = ctypes.POINTER(qsa_geom_t)
@@ -125,6 +132,8 @@ def load(build_if_missing: bool = False):
     lib.qsa_sparse_decode_noalloc_status.argtypes = [ctypes.POINTER(ctypes.c_int), _vp]
     lib.qsa_debug_set_wait_ns.restype = None
     lib.qsa_debug_set_wait_ns.argtypes = [ctypes.c_ulonglong]
+    lib.qsa_debug_bounds_status.restype = ctypes.c_int
+    lib.qsa_debug_bounds_status.argtypes = []
     lib.qsa_workspace_status.restype = st
     lib.qsa_workspace_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int), _vp]
     _lib = lib
@@ -320,6 +329,12 @@ def qsa_sparse_decode_noalloc_status(stream=None) -> int:
     if st not in (QSA_OK, QSA_ERR_DEVICE_TIMEOUT):
         _check("qsa_sparse_decode_noalloc_status", st)
     return int(code.value)
+
+
+def qsa_debug_bounds_status() -> int:
+    """First failed bounds-check code since the last call (clearing them), 0
+    when every check held, -1 when the loaded library has no checks."""
+    return int(load().qsa_debug_bounds_status())
 
 
 def qsa_debug_set_wait_ns(ns: int) -> None:

@@ -109,6 +109,25 @@ void qsa_debug_set_wait_ns(unsigned long long ns) {
   g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns, std::memory_order_relaxed);
 }
 
+int qsa_debug_bounds_status(void) {
+#ifdef QSA_DEBUG_BOUNDS
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  int first = 0;
+  for (int v : {qsa::bounds_word_attend(), qsa::bounds_word_decode(), qsa::bounds_word_index(),
+                qsa::bounds_word_select(), qsa::bounds_word_store(), qsa::bounds_word_rollback(),
+                qsa::bounds_word_prefill()}) {
+    if (v < 0) return -1;
+    if (first == 0) first = v;
+  }
+  return first;
+#else
+  return -1;
+#endif
+}
+
 const char* qsa_status_string(qsa_status_t s) {
   switch (s) {
     case QSA_OK: return "ok";

@@ -67,6 +67,12 @@ constexpr int kGT = kGW * 32;                 // threads per group
 constexpr int kPRow = 72;                     // halfs per P-tile row (64 tokens + pad)
 constexpr int kRec = 8 + kD;                  // record: m, l[4 warps], pad[3], O[D]
 constexpr int kMaxCols = 32;
+// Bounds-check codes (reported by bounds-checked builds only).
+constexpr int kChkList = 0x101;     // chunk-list slot past the list capacity
+constexpr int kChkChunk = 0x102;    // listed chunk: slot, page id or token offset out of range
+constexpr int kChkOut = 0x103;      // output row or dims out of range
+constexpr int kChkRecord = 0x104;   // cluster record slot out of range
+constexpr int kChkUnit = 0x105;     // workspace unit or split out of range
 constexpr int kMaxCl = 16;                    // cluster size (non-portable above 8)
 constexpr int kPtMax = 4096;                  // page-table rows up to this stay in smem
 constexpr float kLog2e = 1.4426950408889634f;
@@ -363,7 +369,7 @@ __device__ __forceinline__ void attend_cta(const Params& p, int s, int kvh, int 
       const unsigned vm = __ballot_sync(0xffffffffu, page >= 0);
       if (page >= 0) {
         const int q = cnt + __popc(vm & ((1u << lane) - 1u));
-        if (q < p.list_cap) {
+        if (QSA_GUARD(q < p.list_cap, kChkList)) {
           lists[2 * q] = page;
           lists[2 * q + 1] = tok0;
         }
@@ -388,6 +394,10 @@ __device__ __forceinline__ void attend_cta(const Params& p, int s, int kvh, int 
     int page, tok0, mask;
     chunk_of(m, page, tok0, mask);
     const int st = (m % NG) * SG + (m / NG) % SG;
+    if (!QSA_IN_BOUNDS(m >= 0 && m < p.list_cap && page >= 0 && page < g.NP && tok0 >= 0 &&
+                           tok0 < cap && (tok0 & (g.P - 1)) + kChunk <= g.P,
+                       kChkChunk))
+      return;
     const size_t row0 = ((size_t)page * g.Hkv + kvh) * g.P + (size_t)(tok0 & (g.P - 1));
     uint8_t* dst = stages + (size_t)st * kStage;
     mbar_arrive_expect_tx(&full[st], kStage);
@@ -752,6 +762,7 @@ __device__ __forceinline__ void attend_cta(const Params& p, int s, int kvh, int 
     if (j >= R || hh >= hreal) return;   // padding column
     const int h = kvh * G + h0 + hh;
     const size_t orow = (size_t)(b * R + j) * g.Hq + h;
+    if (!QSA_IN_BOUNDS(b < g.B && h < g.Hq && d4 + 4 <= kD, kChkOut)) return;
     const float sc = Lsum > 0.f ? p.v_scale / Lsum : 0.f;
     __nv_bfloat162 o01 = __floats2bfloat162_rn(O.x * sc, O.y * sc);
     __nv_bfloat162 o23 = __floats2bfloat162_rn(O.z * sc, O.w * sc);
@@ -795,7 +806,7 @@ __device__ __forceinline__ void attend_cta(const Params& p, int s, int kvh, int 
           const int c = nt * 8 + 2 * tig + e;
           float* dst = cluster.map_shared_rank(rb, c % CL) +
                        ((size_t)(s * NG + grp) * per + c / CL) * kRec;
-          write_record(dst, nt, e);
+          if (QSA_IN_BOUNDS(s < CL && c < kCols, kChkRecord)) write_record(dst, nt, e);
         }
       cluster_arrive_release();
       cluster_wait_acquire();
@@ -822,6 +833,8 @@ __device__ __forceinline__ void attend_cta(const Params& p, int s, int kvh, int 
   // Ticket merge: records to the workspace; the last split of this unit to
   // arrive merges them in split order and resets the ticket.
   const int unit = (b * g.Hkv + kvh) * p.slices + slice;
+  if (!QSA_IN_BOUNDS(b < g.B && kvh < g.Hkv && slice < p.slices && s < p.splits, kChkUnit))
+    return;
   float* mine = p.partials + ((size_t)(unit * p.splits + s) * NG + grp) * kCols * kRec;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
@@ -1068,3 +1081,5 @@ cudaError_t launch_attend(const Geom& g, const DecodePlan& plan, const void* q,
 }
 
 }  // namespace qsa
+
+QSA_BOUNDS_READER(bounds_word_attend)

@@ -34,6 +34,43 @@ __host__ __device__ __forceinline__ int visible_tokens(int L, int R, int j, int 
 }
 
 // ---------------------------------------------------------------------------
+// Bounds-checked builds.  Built with QSA_DEBUG_BOUNDS, every kernel checks the
+// indices it derives from data (page ids, token offsets, list and record
+// slots, output rows) before the access: a failed check records its code in
+// the translation unit's bounds word (the first failure wins) and the access
+// is skipped -- never a trap.  QSA_IN_BOUNDS(cond, code) is an invariant the
+// code relies on (plain `true` in normal builds, cond not evaluated);
+// QSA_GUARD(cond, code) is a test that normal builds also make, and that
+// bounds-checked builds also report.
+// ---------------------------------------------------------------------------
+#ifdef QSA_DEBUG_BOUNDS
+static __device__ int qsa_bounds_word = 0;
+__device__ __forceinline__ bool qsa_bounds_fail(int code) {
+  atomicCAS(&qsa_bounds_word, 0, code);
+  return false;
+}
+#define QSA_IN_BOUNDS(cond, code) ((cond) ? true : ::qsa::qsa_bounds_fail(code))
+#define QSA_GUARD(cond, code) ((cond) ? true : ::qsa::qsa_bounds_fail(code))
+// Defines `int fn()` reading and clearing this translation unit's word.
+#define QSA_BOUNDS_READER(fn)                                                    \
+  namespace qsa {                                                                \
+  int fn() {                                                                     \
+    int v = 0, z = 0;                                                            \
+    if (cudaMemcpyFromSymbol(&v, qsa_bounds_word, sizeof(int)) != cudaSuccess)   \
+      v = -1;                                                                    \
+    else if (cudaMemcpyToSymbol(qsa_bounds_word, &z, sizeof(int)) != cudaSuccess) \
+      v = -1;                                                                    \
+    cudaGetLastError();                                                          \
+    return v;                                                                    \
+  }                                                                              \
+  }
+#else
+#define QSA_IN_BOUNDS(cond, code) true
+#define QSA_GUARD(cond, code) (cond)
+#define QSA_BOUNDS_READER(fn)
+#endif
+
+// ---------------------------------------------------------------------------
 // mbarrier + bulk copy (TMA engine, non-tensor form)
 // ---------------------------------------------------------------------------
 
@@ -208,6 +245,17 @@ struct DecodePlan {
 
 DecodePlan plan_sparse_decode(const Geom& g, int k, int num_splits);
 bool decode_can_fuse_select(const Geom& g);
+
+#ifdef QSA_DEBUG_BOUNDS
+// Each file's bounds word, read and cleared (0 = no failed check).
+int bounds_word_attend();
+int bounds_word_decode();
+int bounds_word_index();
+int bounds_word_select();
+int bounds_word_store();
+int bounds_word_rollback();
+int bounds_word_prefill();
+#endif
 
 // Bound of the attention kernels' waits for their chunk copies, in ns
 // (qsa_debug_set_wait_ns; 2 s unless a diagnostic changed it).

@@ -26,6 +26,9 @@
 namespace qsa {
 namespace {
 
+// Bounds-check codes (reported by bounds-checked builds only).
+constexpr int kChkPage = 0x301;    // index-key page id out of range
+constexpr int kChkScore = 0x302;   // score row or block out of range
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
@@ -69,6 +72,7 @@ index_scores_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __restr
   };
   // Lane (token group lane>>2, part lane&3) loads 16 B of 8 tokens per step.
   auto load_keys = [&](int page, int4 (&kv)[P / 8]) {
+    if (!QSA_IN_BOUNDS(page >= 0 && page < g.NP, kChkPage)) return;
     const int4* src = reinterpret_cast<const int4*>(ik_pool + (size_t)page * P * kIndexDim) + lane;
 #pragma unroll
     for (int i = 0; i < P / 8; ++i) kv[i] = ld_stream_v4(src + 32 * i);
@@ -145,6 +149,7 @@ index_scores_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __restr
       live_n = block_of(it + 1, beta_n, page_n);
     }
     int32_t* dst = scores + (size_t)b * R * g.MB + beta;
+    if (!QSA_IN_BOUNDS(b < g.B && beta >= 0 && beta < g.MB, kChkScore)) break;
     if (!live) {
       if (lane < R) dst[(size_t)lane * g.MB] = kSentinel;
     } else {
@@ -254,6 +259,7 @@ index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __r
   };
   // Lane (gid, tig) loads 16 B (dims 16*tig..) of token 8*i + gid per step.
   auto load_keys = [&](int page, int4 (&kv)[P / 8]) {
+    if (!QSA_IN_BOUNDS(page >= 0 && page < g.NP, kChkPage)) return;
     const int4* src = reinterpret_cast<const int4*>(ik_pool + (size_t)page * P * kIndexDim) + lane;
 #pragma unroll
     for (int i = 0; i < P / 8; ++i) kv[i] = ld_stream_v4(src + 32 * i);
@@ -330,6 +336,7 @@ index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __r
       live_n = block_of(it + 1, beta_n, page_n);
     }
     int32_t* dst = scores + ((size_t)b * R + r0) * g.MB + beta;
+    if (!QSA_IN_BOUNDS(b < g.B && beta >= 0 && beta < g.MB, kChkScore)) break;
     if (!live) {
       if (lane < RB && r0 + lane < R) dst[(size_t)lane * g.MB] = kSentinel;
     } else {
@@ -466,12 +473,14 @@ index_scores_rows_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __
     const bool live = block_of(it, beta, page);
     if (beta >= g.MB) break;
     int32_t* dst = scores + ((size_t)b * R + r0) * g.MB + beta;
+    if (!QSA_IN_BOUNDS(b < g.B && beta >= 0 && beta < g.MB, kChkScore)) break;
     if (!live) {
       for (int jr = lane; jr < kGroupRows; jr += 32)
         if (r0 + jr < R) dst[(size_t)jr * g.MB] = kSentinel;
       continue;
     }
     int4 kv[P / 8];
+    if (!QSA_IN_BOUNDS(page >= 0 && page < g.NP, kChkPage)) break;
     const int4* src = reinterpret_cast<const int4*>(ik_pool + (size_t)page * P * kIndexDim) + lane;
 #pragma unroll
     for (int i = 0; i < P / 8; ++i) kv[i] = ld_stream_v4(src + 32 * i);
@@ -651,3 +660,5 @@ cudaError_t launch_index_scores(const Geom& g, const int8_t* iq, const int8_t* i
 }
 
 }  // namespace qsa
+
+QSA_BOUNDS_READER(bounds_word_index)

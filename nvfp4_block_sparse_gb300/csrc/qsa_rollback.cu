@@ -23,6 +23,8 @@
 namespace qsa {
 namespace {
 
+// Bounds-check code (reported by bounds-checked builds only): pool row out of range.
+constexpr int kChkRow = 0x601;
 constexpr int kWarpsPerCta = 8;
 constexpr int kIkWords = kIndexDim / 4;                              // 16
 
@@ -62,6 +64,9 @@ rollback_kernel(Geom g, const int32_t* __restrict__ page_table, const int32_t* _
   if (page < 0 || page >= g.NP) return;
   const int slot = (int)(pos % g.P);
   const size_t row = ((size_t)page * g.Hkv + kvh) * g.P + slot;
+  if (!QSA_IN_BOUNDS(b < g.B && slot >= 0 && slot < g.P && row < (size_t)g.NP * g.Hkv * g.P,
+                     kChkRow))
+    return;
   const int kw = kv_words(g.D), cw = g.D / 8, sw = g.D / 64;
   const size_t row_bytes = (size_t)g.Hkv * kw * 4 + kIkWords * 4;
   uint32_t* sv = reinterpret_cast<uint32_t*>(saved + (size_t)r * row_bytes) + kvh * kw;
@@ -102,3 +107,5 @@ cudaError_t launch_rollback(const Geom& g, bool restore, const int32_t* page_tab
 }
 
 }  // namespace qsa
+
+QSA_BOUNDS_READER(bounds_word_rollback)

@@ -32,6 +32,9 @@ namespace qsa {
 constexpr int kSelDigitBits = 11;
 constexpr int kSelBins = 1 << kSelDigitBits;
 constexpr int kSelMaxMembers = 256;   // boundary-bin members ranked directly
+// Bounds-check codes (reported by bounds-checked builds only).
+constexpr int kChkSelMember = 0x401;  // boundary-member list slot past its capacity
+constexpr int kChkSelOut = 0x402;     // selection slot at or past k
 
 // Shared memory a CTA of NTHREADS needs for rows of up to `mb` blocks.
 template <int NTHREADS>
@@ -47,9 +50,7 @@ __device__ __forceinline__ uint32_t sel_order_key(int s) { return (uint32_t)s ^ 
 
 // Selects row `src` (nb visible blocks of which the last W are the window) into
 // out[0..k) and returns the count (also written to *nsel by thread 0).
-// kFromL2: read the row past L1 (it was just written by other CTAs of the
-// same kernel).
-template <int NTHREADS, bool kFromL2 = false>
+template <int NTHREADS>
 __device__ void select_row(const int32_t* __restrict__ src, int nb, int W, int k,
                            int32_t* __restrict__ out, int32_t* __restrict__ nsel,
                            uint8_t* smem) {
@@ -76,7 +77,7 @@ __device__ void select_row(const int32_t* __restrict__ src, int nb, int W, int k
   int nwin = 0, ncand = 0;
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
   for (int i = tid; i < nb; i += NTHREADS) {
-    const int s = kFromL2 ? __ldcg(src + i) : src[i];
+    const int s = src[i];
     row[i] = s;
     if (s == kSentinel) continue;
     if (i >= wlo) {
@@ -193,10 +194,14 @@ __device__ void select_row(const int32_t* __restrict__ src, int nb, int W, int k
       const int s = row[i];
       if (s == kSentinel) continue;
       const uint32_t rel = sel_order_key(s) - kmin;
-      if ((rel >> shift) == prefix) mlist[atomicAdd(&sc[50], 1)] = make_uint2(rel, (uint32_t)i);
+      if ((rel >> shift) == prefix) {
+        const int slot = atomicAdd(&sc[50], 1);
+        if (QSA_IN_BOUNDS(slot < kSelMaxMembers, kChkSelMember))
+          mlist[slot] = make_uint2(rel, (uint32_t)i);
+      }
     }
     __syncthreads();
-    const int m = sc[50];
+    const int m = min(sc[50], kSelMaxMembers);
     for (int rd = 0; rd < rounds; ++rd) {
       const int i = rd * NTHREADS + tid;
       const int s = i < nb ? row[i] : kSentinel;
@@ -283,7 +288,8 @@ __device__ void select_row(const int32_t* __restrict__ src, int nb, int W, int k
       round_tot += cw;
       if (w < warp) in_round += cw;
     }
-    if (pick) out[below + in_round + __popc(pb & lt_mask)] = i;
+    const int pos = below + in_round + __popc(pb & lt_mask);
+    if (pick && QSA_IN_BOUNDS(pos < k, kChkSelOut)) out[pos] = i;
     below += round_tot;
   }
   const int total = below;

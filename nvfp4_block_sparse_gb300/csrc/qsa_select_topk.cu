@@ -65,3 +65,4 @@ cudaError_t launch_select_topk(const Geom& g, const int32_t* scores, const int32
 }
 
 }  // namespace qsa
+QSA_BOUNDS_READER(bounds_word_select)

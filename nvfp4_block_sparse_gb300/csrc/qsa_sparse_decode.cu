@@ -66,6 +66,12 @@ struct Hd {
   static constexpr int kDt = D / 16;                 // 16-dim tiles
   static constexpr int kRuns = D / 128;              // 16-byte runs of a row per lane
 };
+// Bounds-check codes (reported by bounds-checked builds only).
+constexpr int kChkList = 0x201;    // decode warp list slot past its capacity
+constexpr int kChkUnion = 0x202;   // verify union slot out of range
+constexpr int kChkChunk = 0x203;   // chunk: slot, page id or token offset out of range
+constexpr int kChkOut = 0x204;     // output row or dims out of range
+constexpr int kChkUnit = 0x205;    // workspace unit or split out of range
 constexpr int kStageBytes = 9216;
 static_assert(2 * Hd<128>::kKBytes + 2 * Hd<128>::kSfBytes == kStageBytes, "stage size");
 static_assert(2 * Hd<256>::kKBytes + 2 * Hd<256>::kSfBytes == kStageBytes, "stage size");
@@ -603,8 +609,10 @@ sparse_decode_kernel(Params p) {
       const unsigned vm = __ballot_sync(0xffffffffu, page >= 0);
       if (page >= 0) {
         const int q = wcnt + __popc(vm & ((1u << lane) - 1u));
-        wl[2 * q] = page;
-        wl[2 * q + 1] = tok0;
+        if (QSA_IN_BOUNDS(q < decode_list_cap(k, p.splits, W), kChkList)) {
+          wl[2 * q] = page;
+          wl[2 * q + 1] = tok0;
+        }
       }
       wcnt += __popc(vm);
     }
@@ -664,7 +672,7 @@ sparse_decode_kernel(Params p) {
     for (int beta = b_lo; beta < b_hi; ++beta) {
       const int mask = rm[beta];
       const int page = s_pt[beta];
-      if (mask != 0 && page >= 0 && page < g.NP) {
+      if (mask != 0 && page >= 0 && page < g.NP && QSA_IN_BOUNDS(pos < R * k, kChkUnion)) {
         s_union[pos] = beta | (mask << 24);
         s_upage[pos] = page;
         ++pos;
@@ -743,8 +751,10 @@ sparse_decode_kernel(Params p) {
         if (!ONE)
           for (int j2 = 0; j2 < R; ++j2)
             if (j2 != jj) pos += s_scan[j2 * k + lower(j2, beta)] - s_scan[j2 * k];
-        s_union[pos] = beta | ((flag & 0xFF) << 24);
-        s_upage[pos] = t_page[e];
+        if (QSA_IN_BOUNDS(pos >= 0 && pos < R * k, kChkUnion)) {
+          s_union[pos] = beta | ((flag & 0xFF) << 24);
+          s_upage[pos] = t_page[e];
+        }
       }
       if (++ii == k) { ii = 0; ++jj; }
     }
@@ -765,6 +775,7 @@ sparse_decode_kernel(Params p) {
     const int st = i % S;
     const int c = s + i * p.splits;
     const int u = c >> csh, sub = c & csh;
+    if (!QSA_IN_BOUNDS(u < U && s_upage[u] >= 0 && s_upage[u] < g.NP, kChkChunk)) return;
     const size_t row0 = ((size_t)s_upage[u] * g.Hkv + kvh) * g.P + (size_t)sub * kChunk;
     uint8_t* dst = region + st * kStageBytes;
     mbar_arrive_expect_tx(&full[st], kStageBytes);
@@ -827,6 +838,10 @@ sparse_decode_kernel(Params p) {
   auto issue_one = [&](int q) {
     const int st = warp + W * (q % kSpw);
     const int page = wl[2 * q], tok0 = wl[2 * q + 1];
+    if (!QSA_IN_BOUNDS(q < decode_list_cap(k, p.splits, W) && page >= 0 && page < g.NP &&
+                           tok0 >= 0 && tok0 < cap && (tok0 & (g.P - 1)) + kChunk <= g.P,
+                       kChkChunk))
+      return;
     const size_t row0 = ((size_t)page * g.Hkv + kvh) * g.P + (size_t)(tok0 & (g.P - 1));
     uint8_t* dst = region + st * kStageBytes;
     mbar_arrive_expect_tx(&full[st], kStageBytes);
@@ -967,6 +982,7 @@ sparse_decode_kernel(Params p) {
     if (hh >= hs) return;   // padding column
     const int h = kvh * G + hs0 + hh;
     const size_t orow = (size_t)(b * R + j) * g.Hq + h;
+    if (!QSA_IN_BOUNDS(j < R && b < g.B && h < g.Hq && d4 + 4 <= D, kChkOut)) return;
     const float sc = Lsum > 0.f ? p.v_scale / Lsum : 0.f;
     __nv_bfloat162 o01 = __floats2bfloat162_rn(O.x * sc, O.y * sc);
     __nv_bfloat162 o23 = __floats2bfloat162_rn(O.z * sc, O.w * sc);
@@ -1079,6 +1095,8 @@ sparse_decode_kernel(Params p) {
   // (request, KV head, slice) to arrive merges them in split order
   // (deterministic) and resets the ticket.
   const int units_idx = (b * g.Hkv + kvh) * p.slices + slice;
+  if (!QSA_IN_BOUNDS(b < g.B && kvh < g.Hkv && slice < p.slices && s < p.splits, kChkUnit))
+    return;
   const size_t split_floats = (size_t)ncols * kPartStride;
   float* part = p.partials + ((size_t)units_idx * p.splits + s) * split_floats;
   for (int idx = tid; idx < ncols * (kPartStride / 4); idx += kThreads)
@@ -1406,3 +1424,5 @@ cudaError_t launch_sparse_decode(const Geom& g, const DecodePlan& plan, const vo
 }
 
 }  // namespace qsa
+
+QSA_BOUNDS_READER(bounds_word_decode)

@@ -42,6 +42,10 @@
 namespace qsa {
 namespace {
 
+// Bounds-check codes (reported by bounds-checked builds only).
+constexpr int kChkUnion = 0x701;   // union slot past its capacity
+constexpr int kChkChunk = 0x702;   // chunk: union slot or page id out of range
+constexpr int kChkOut = 0x703;     // output row out of range
 constexpr int kThreads = 128;           // four warps: one thread per tile row
 constexpr int kStage = 9216;            // NVFP4 bytes of one chunk (8192 K and V values)
 
@@ -367,8 +371,10 @@ sparse_prefill_kernel(Params p) {
       while (m) {
         const int beta = (w << 5) + __ffs(m) - 1;
         m &= m - 1;
-        s_union[pos] = beta;
-        s_upage[pos] = pt[beta];
+        if (QSA_IN_BOUNDS(pos < p.ucap, kChkUnion)) {
+          s_union[pos] = beta;
+          s_upage[pos] = pt[beta];
+        }
         ++pos;
       }
     }
@@ -389,6 +395,8 @@ sparse_prefill_kernel(Params p) {
   auto issue = [&](int c) {
     uint8_t* dst = sStage + (c & 1) * kStage;
     const int u = c >> csh, sub = c & csh;
+    if (!QSA_IN_BOUNDS(u < U && u < p.ucap && s_upage[u] >= 0 && s_upage[u] < g.NP, kChkChunk))
+      return;
     const size_t row0 = ((size_t)s_upage[u] * g.Hkv + kvh) * g.P + (size_t)sub * kTok;
     mbar_arrive_expect_tx(&full[c & 1], kStage);
     bulk_g2s(dst, p.k_pool + row0 * (D / 2), kTok * D / 2, &full[c & 1], pol);
@@ -625,6 +633,7 @@ sparse_prefill_kernel(Params p) {
   // chunk was visited, and rows without a token write zeros)
   if (!dead) {
     const size_t orow = ((size_t)b * g.R + j) * g.Hq + (size_t)kvh * G + hh;
+    const bool out_ok = !vec || QSA_IN_BOUNDS(b < g.B && j < g.R && kvh * G + hh < g.Hq, kChkOut);
     uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D);
     const bool has = l_run > 0.f && C > 0;
     const float sc = has ? p.v_scale / l_run : 0.f;
@@ -642,12 +651,12 @@ sparse_prefill_kernel(Params p) {
                                                  has ? o16[2 * i + 1] * sc : 0.f);
         h[i] = *reinterpret_cast<uint32_t*>(&x);
       }
-      if (vec) {
+      if (vec && out_ok) {
         dst[2 * q8] = make_uint4(h[0], h[1], h[2], h[3]);
         dst[2 * q8 + 1] = make_uint4(h[4], h[5], h[6], h[7]);
       }
     }
-    if (vec) p.lse[orow] = has ? (m_base + log2f(l_run)) * kLn2 : -INFINITY;
+    if (vec && out_ok) p.lse[orow] = has ? (m_base + log2f(l_run)) * kLn2 : -INFINITY;
   }
   tc_fence_before();
   __syncthreads();
@@ -709,3 +718,5 @@ cudaError_t launch_sparse_prefill(const Geom& g, const void* q, const uint8_t* k
 }
 
 }  // namespace qsa
+
+QSA_BOUNDS_READER(bounds_word_prefill)

@@ -29,6 +29,8 @@ namespace qsa {
 namespace {
 
 constexpr int kWarpsPerCta = 8;
+// Bounds-check code (reported by bounds-checked builds only): pool row out of range.
+constexpr int kChkRow = 0x501;
 
 __device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi) {
   uint32_t r;
@@ -111,6 +113,9 @@ store_tokens_kernel(Geom g, const __nv_bfloat16* __restrict__ k_new,
                                           __fdiv_rn(x[2 * i + 1], den))) << (8 * i);
   }
   const size_t row = ((size_t)page * g.Hkv + kvh) * g.P + slot;   // token row in the pool
+  if (!QSA_IN_BOUNDS(b < g.B && slot >= 0 && slot < g.P && row < (size_t)g.NP * g.Hkv * g.P,
+                     kChkRow))
+    return;
   uint8_t* pool = is_v ? v_pool : k_pool;
   uint8_t* sfp = is_v ? v_sf : k_sf;
   if constexpr (E == 4)
@@ -150,3 +155,5 @@ cudaError_t launch_store_tokens(const Geom& g, const void* k_new, const void* v_
 }
 
 }  // namespace qsa
+
+QSA_BOUNDS_READER(bounds_word_store)

@@ -31,3 +31,16 @@ def pytest_collection_modifyitems(config, items):
 @pytest.fixture(scope="session")
 def golden_dir():
     return GOLDEN
+
+
+@pytest.fixture(autouse=True)
+def _bounds_checks_held(request):
+    """Under QSA_BOUNDS_CHECKED=1 (the bounds-checked library), every GPU test
+    also asserts that no in-kernel bounds check failed while it ran."""
+    yield
+    if os.environ.get("QSA_BOUNDS_CHECKED", "") != "1" or "gpu" not in request.keywords:
+        return
+    import nvfp4_block_sparse_gb300 as qsa
+    assert qsa.library_path().endswith("libqsa_bounds.so")
+    code = qsa.qsa_debug_bounds_status()
+    assert code == 0, "in-kernel bounds check failed: code 0x%x" % code

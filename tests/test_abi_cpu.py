@@ -34,6 +34,20 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_bounds_checked_library_exports_every_declared_symbol(lib):
+    # libqsa_bounds.so (built beside libqsa.so) has the same C ABI; the normal
+    # library answers the bounds query with -1 (no checks compiled in) without
+    # touching a device.
+    from nvfp4_block_sparse_gb300 import build
+    if not os.path.exists(build.BOUNDS_LIB):
+        build.build()
+    blib = ctypes.CDLL(build.BOUNDS_LIB)
+    for name in declared_functions():
+        assert hasattr(blib, name), name
+    if not qsa.bounds_checked():
+        assert qsa.qsa_debug_bounds_status() == -1
+
+
 def test_status_strings(lib):
     for s in range(6):
         assert qsa.qsa_status_string(s)
