@@ -162,7 +162,7 @@ struct Layout {
   static constexpr int kCoSz = W * kHsp * D * 4;
   static constexpr int kCmSz = W * kHsp * 4;
   static constexpr int kClSz = W * kHsp * 4;
-  __host__ __device__ static bool direct(int R) { return !ONE && W == R; }
+  __host__ __device__ static bool direct(int R) { return W == R; }
   __host__ __device__ static int cp_off(int R) { return direct(R) ? 0 : kCoSz + kCmSz + kClSz; }
   __host__ __device__ static int cp_bytes(int R) { return R * kHsp * kPartStride * 4; }
   __host__ __device__ static int region_bytes(int R, int k, int splits) {
@@ -190,7 +190,7 @@ struct Layout {
     // sel rows, union ids, pages, scan (verify) / per-warp chunk lists (decode)
     size_t sel_bytes = (size_t)R * k * 4 * 4 + 16;
     if (ONE) {   // per-warp chunk lists, then the fused selection's row
-      const size_t lists = ((size_t)W * 2 * decode_list_cap(k, splits, W) + k) * 4;
+      const size_t lists = ((size_t)W * 2 * decode_list_cap(k, splits, W / R) + k) * 4;
       if (lists > sel_bytes) sel_bytes = lists;
     }
     off += sel_bytes;
@@ -230,20 +230,24 @@ __device__ __forceinline__ void cluster_wait_acquire() {
 // covers dims D/4 * tig + 4*kk + {0..3} on both operands.  For PV it reads
 // bytes [D/16 * gid, D/16 * (gid+1)) of four token rows per k-step: dim tile
 // dt holds dims D/8 * gid + 2*dt (+1 in the upper eight rows).
+//
+// The work is two halves: consume_qk reads only the stage's K codes and
+// scales and leaves P^T in registers (pf), consume_pv reads only the V codes
+// and scales, so a warp that owns its stage can refill the K half while it
+// still works on the V half.
 template <int NTR, int D>
-__device__ __forceinline__ void consume_chunk(const uint8_t* __restrict__ sk, int tok0, int nrow,
-                                              const uint32_t (&qf)[NTR][D / 8],
-                                              const float (&cq)[NTR][2], float (&m_run)[NTR][2],
-                                              float (&l_run)[NTR][2],
-                                              float (&o_acc)[D / 16][NTR][4]) {
+__device__ __forceinline__ void consume_qk(const uint8_t* __restrict__ sk, int tok0, int nrow,
+                                           const uint32_t (&qf)[NTR][D / 8],
+                                           const float (&cq)[NTR][2], float (&m_run)[NTR][2],
+                                           float (&l_run)[NTR][2],
+                                           float (&o_acc)[D / 16][NTR][4],
+                                           uint32_t (&pf)[Hd<D>::kMt][NTR][2]) {
   using H = Hd<D>;
   constexpr int kMt = H::kMt;
   const int lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const bool partial = tok0 + H::kChunk > nrow;
-  const uint8_t* sv = sk + H::kKBytes;
   const uint8_t* sks = sk + 2 * H::kKBytes;
-  const uint8_t* svs = sks + H::kSfBytes;
 
   // ---- S^T = K . Q^T over the stage's 16-token tiles -----------------
   // Tiles go in pairs: k-steps outside and the pair inside, so
@@ -372,7 +376,6 @@ __device__ __forceinline__ void consume_chunk(const uint8_t* __restrict__ sk, in
     for (int e = 0; e < 2; ++e) m_run[nt][e] = fmaxf(m_run[nt][e], cmax[nt][e]);
 
   // P = exp2(z - base) -> fp16 -> transposed B fragments for P^T.
-  uint32_t pf[kMt][NTR][2];
 #pragma unroll
   for (int mt = 0; mt < kMt; ++mt)
 #pragma unroll
@@ -386,6 +389,18 @@ __device__ __forceinline__ void consume_chunk(const uint8_t* __restrict__ sk, in
       pf[mt][nt][0] = movmatrix_trans(pack_half2(p0, p1));
       pf[mt][nt][1] = movmatrix_trans(pack_half2(p2, p3));
     }
+}
+
+template <int NTR, int D>
+__device__ __forceinline__ void consume_pv(const uint8_t* __restrict__ sk,
+                                           const uint32_t (&pf)[Hd<D>::kMt][NTR][2],
+                                           float (&o_acc)[D / 16][NTR][4]) {
+  using H = Hd<D>;
+  constexpr int kMt = H::kMt;
+  const int lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const uint8_t* sv = sk + H::kKBytes;
+  const uint8_t* svs = sk + 2 * H::kKBytes + H::kSfBytes;
 
   // ---- O^T += V^T . P^T over the 16-dim tiles -------------------------
 #pragma unroll
@@ -433,6 +448,17 @@ __device__ __forceinline__ void consume_chunk(const uint8_t* __restrict__ sk, in
   }
 }
 
+template <int NTR, int D>
+__device__ __forceinline__ void consume_chunk(const uint8_t* __restrict__ sk, int tok0, int nrow,
+                                              const uint32_t (&qf)[NTR][D / 8],
+                                              const float (&cq)[NTR][2], float (&m_run)[NTR][2],
+                                              float (&l_run)[NTR][2],
+                                              float (&o_acc)[D / 16][NTR][4]) {
+  uint32_t pf[Hd<D>::kMt][NTR][2];
+  consume_qk<NTR, D>(sk, tok0, nrow, qf, cq, m_run, l_run, o_acc, pf);
+  consume_pv<NTR, D>(sk, pf, o_acc);
+}
+
 template <int NTR, int W, int S, bool ONE, int D>
 __global__ void __launch_bounds__(Layout<NTR, W, S, ONE, D>::kThreads,
                                   (decode_min_blocks<NTR, W, ONE, D>()))
@@ -447,12 +473,19 @@ sparse_decode_kernel(Params p) {
   static_assert(!ONE || S % W == 0, "a single-row stage must always belong to one consumer");
 
   const Geom& g = p.g;
-  const int R = ONE ? 1 : g.R;
+  const int R = g.R;
   const int G = g.Hq / g.Hkv;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const bool producer = !ONE && warp == W;
+  // Self-issued (ONE) variants: warp w owns row w % R and, of that row's
+  // chunks of this split, every (W / R)-th starting at the (w / R)-th; it
+  // lists, requests and consumes them itself.  Verify (union) variants: a
+  // producer warp streams the union and consumer w owns row w % R.
+  const int gper = W / R;                       // consumers per row
+  const int jw = warp % R;                      // the row this warp owns
+  const int gw = warp / R;
 
   const int s = blockIdx.x;                           // KV split (= cluster rank)
   const int kvh = blockIdx.y / p.slices, slice = blockIdx.y % p.slices;
@@ -481,7 +514,7 @@ sparse_decode_kernel(Params p) {
   int32_t* s_union = s_sel + R * k;
   int32_t* s_upage = s_union + R * k;
   int32_t* s_scan = s_upage + R * k;                  // [R * k + 1]
-  const int list_ints = ONE ? W * 2 * decode_list_cap(k, p.splits, W) + k : 0;
+  const int list_ints = ONE ? W * 2 * decode_list_cap(k, p.splits, gper) + k : 0;
   int32_t* s_pt = s_sel + (list_ints > R * k * 4 + 4 ? list_ints : R * k * 4 + 4);
 
   // full[st]: one arrival (the copy issuer) plus the copies' bytes.  empty[st]
@@ -489,7 +522,8 @@ sparse_decode_kernel(Params p) {
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);
-      if (!ONE) mbar_init(&empty[i], W);
+      // ONE: empty[st] is the V half's full barrier (see the consumers).
+      mbar_init(&empty[i], ONE ? 1 : W);
     }
     fence_mbar_init();
   }
@@ -512,13 +546,14 @@ sparse_decode_kernel(Params p) {
     // queries of any magnitude inside fp16 range.  2^sq and its inverse are
     // built from exponent bits (|sq| <= 126 keeps both normal).
     // Lane holds D/32 consecutive dims (4 or 8), read as D/128 8-byte words.
-    constexpr int kMaxCols = (ONE ? 1 : kMaxRows) * kHsp;
-    constexpr int kQPerWarp = (kMaxCols + kWarps - 1) / kWarps;
+    // Columns in passes of kQPerWarp per warp (one pass for decode rows).
+    constexpr int kQPerWarp = ONE ? (kHsp + kWarps - 1) / kWarps : (kMaxRows * kHsp + kWarps - 1) / kWarps;
     constexpr int kQw = D / 128;
+    for (int cb = 0; cb < ncols; cb += kQPerWarp * kWarps) {
     uint2 raw[kQPerWarp][kQw];
 #pragma unroll
     for (int ci = 0; ci < kQPerWarp; ++ci) {
-      const int c = warp + ci * kWarps;
+      const int c = cb + warp + ci * kWarps;
 #pragma unroll
       for (int u = 0; u < kQw; ++u) raw[ci][u] = make_uint2(0u, 0u);
       if (c < ncols && (c % kHsp) < hs) {
@@ -532,7 +567,7 @@ sparse_decode_kernel(Params p) {
     }
 #pragma unroll
     for (int ci = 0; ci < kQPerWarp; ++ci) {
-      const int c = warp + ci * kWarps;
+      const int c = cb + warp + ci * kWarps;
       if (c >= ncols) break;
       float v[4 * kQw];
 #pragma unroll
@@ -560,26 +595,30 @@ sparse_decode_kernel(Params p) {
         col_n[c] = visible_tokens(L, R, c / kHsp, cap);
       }
     }
+    }
   }
 
   __syncthreads();   // barriers, page-table row and queries visible to every warp
   pdl_wait();        // the selections come from the preceding kernel
 
   const int csh = (g.P == 2 * kChunk) ? 1 : 0;  // stages per page: 1 << csh
-  // Decode: each warp lists its own chunks straight from the selection (no
-  // union and no CTA-wide barrier before the first copies).  Candidate chunk c
-  // of the row (entry c >> csh, part c & csh) belongs to split c mod splits and,
-  // within it, to warp (c / splits) mod W.  An entry equal to its predecessor
-  // (the selection is ascending) or on an invalid page is dropped.
-  int* wl = s_sel + warp * 2 * decode_list_cap(k, p.splits, W);   // (page, tok0) pairs
+  // Self-issued: each warp lists its own chunks straight from its row's
+  // selection (no union and no CTA-wide barrier before the first copies).
+  // Candidate chunk c of the row (entry c >> csh, part c & csh) belongs to
+  // split c mod splits and, within it, to the row's warp (c / splits) mod
+  // (W / R).  An entry equal to its predecessor (the selection is ascending)
+  // or on an invalid page is dropped.
+  const int wcap = ONE ? decode_list_cap(k, p.splits, gper) : 0;
+  int* wl = s_sel + warp * 2 * wcap;            // (page, tok0) pairs
   int wcnt = 0;
   if constexpr (ONE) {
     const int nc = k << csh;
-    const int32_t* selrow = p.sel + (size_t)b * k;
+    const int32_t* selrow = p.sel + (size_t)(b * R + jw) * k;
     if (p.scores) {
-      // Fused selection: this CTA selects its row from the scores, with the
-      // (still idle) stage region as the selection's scratch.
-      int32_t* s_row = s_sel + W * 2 * decode_list_cap(k, p.splits, W);
+      // Fused selection (one row per request): this CTA selects its row from
+      // the scores, with the (still idle) stage region as the selection's
+      // scratch.
+      int32_t* s_row = s_sel + W * 2 * wcap;
       const int n = visible_tokens(L, 1, 0, cap);
       select_row<kThreads>(p.scores + (size_t)b * g.MB, (n + g.P - 1) / g.P, p.window, k, s_row,
                            misc + 20, region);
@@ -591,8 +630,8 @@ sparse_decode_kernel(Params p) {
       selrow = s_row;
     }
     for (int t0 = 0;; t0 += 32) {
-      if (s + (long long)p.splits * (warp + (long long)W * t0) >= nc) break;
-      const long long c = s + (long long)p.splits * (warp + (long long)W * (t0 + lane));
+      if (s + (long long)p.splits * (gw + (long long)gper * t0) >= nc) break;
+      const long long c = s + (long long)p.splits * (gw + (long long)gper * (t0 + lane));
       int page = -1, tok0 = 0;
       if (c < nc) {
         const int e = (int)(c >> csh);
@@ -609,7 +648,7 @@ sparse_decode_kernel(Params p) {
       const unsigned vm = __ballot_sync(0xffffffffu, page >= 0);
       if (page >= 0) {
         const int q = wcnt + __popc(vm & ((1u << lane) - 1u));
-        if (QSA_IN_BOUNDS(q < decode_list_cap(k, p.splits, W), kChkList)) {
+        if (QSA_IN_BOUNDS(q < wcap, kChkList)) {
           wl[2 * q] = page;
           wl[2 * q + 1] = tok0;
         }
@@ -769,7 +808,11 @@ sparse_decode_kernel(Params p) {
   // share of every row's pages.
   const int n_ch = (C > s) ? (C - s + p.splits - 1) / p.splits : 0;
 
-  const uint64_t pol = (ONE || producer) ? policy_evict_first() : 0ull;
+  // Chunks read by one warp only are evicted first; a verify row's chunk may
+  // be read again by another row's warp, so self-issued verify copies keep
+  // the normal policy.
+  const uint64_t pol = ((ONE && R == 1) || producer) ? policy_evict_first()
+                                                     : (ONE ? policy_evict_normal() : 0ull);
   // Chunk i of this split into stage i % S (one lane).
   auto issue = [&](int i) {
     const int st = i % S;
@@ -817,9 +860,6 @@ sparse_decode_kernel(Params p) {
   // with one consumer), so no warp waits on another.  Verify: consumer w owns
   // row w % R and, of the chunks of this split that its row selected, every
   // (W / R)-th starting at the (w / R)-th.
-  const int gper = ONE ? W : W / R;             // consumers per row
-  const int jw = ONE ? 0 : warp % R;            // the row this warp owns
-  const int gw = ONE ? 0 : warp / R;
   float m_run[NTR][2], l_run[NTR][2];
   float o_acc[H::kDt][NTR][4];
 #pragma unroll
@@ -833,27 +873,47 @@ sparse_decode_kernel(Params p) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) o_acc[dt][nt][e] = 0.f;
 
-  // Decode: this warp's q-th chunk goes to stage warp + W * (q mod S/W).
-  constexpr int kSpw = ONE ? S / W : 1;          // stages per decode warp
-  auto issue_one = [&](int q) {
-    const int st = warp + W * (q % kSpw);
+  // Self-issued: this warp's q-th chunk goes to stage warp + W * (q mod S/W).
+  // Its K half (codes and scales) completes on full[st] and its V half on
+  // empty[st], so the K half of chunk q + S/W is requested as soon as the
+  // logits of chunk q are done, and its V half once P.V is: one stage per
+  // warp is then already double-buffered by halves.
+  constexpr int kSpw = ONE ? S / W : 1;          // stages per self-issuing warp
+  auto chunk_row0 = [&](int q, size_t& row0) -> bool {
     const int page = wl[2 * q], tok0 = wl[2 * q + 1];
-    if (!QSA_IN_BOUNDS(q < decode_list_cap(k, p.splits, W) && page >= 0 && page < g.NP &&
-                           tok0 >= 0 && tok0 < cap && (tok0 & (g.P - 1)) + kChunk <= g.P,
+    if (!QSA_IN_BOUNDS(q < wcap && page >= 0 && page < g.NP && tok0 >= 0 && tok0 < cap &&
+                           (tok0 & (g.P - 1)) + kChunk <= g.P,
                        kChkChunk))
-      return;
-    const size_t row0 = ((size_t)page * g.Hkv + kvh) * g.P + (size_t)(tok0 & (g.P - 1));
-    uint8_t* dst = region + st * kStageBytes;
-    mbar_arrive_expect_tx(&full[st], kStageBytes);
-    bulk_g2s(dst, p.k_pool + row0 * H::kRow, H::kKBytes, &full[st], pol);
-    bulk_g2s(dst + H::kKBytes, p.v_pool + row0 * H::kRow, H::kKBytes, &full[st], pol);
-    bulk_g2s(dst + 2 * H::kKBytes, p.k_sf + row0 * H::kSfRow, H::kSfBytes, &full[st], pol);
-    bulk_g2s(dst + 2 * H::kKBytes + H::kSfBytes, p.v_sf + row0 * H::kSfRow, H::kSfBytes,
-             &full[st], pol);
+      return false;
+    row0 = ((size_t)page * g.Hkv + kvh) * g.P + (size_t)(tok0 & (g.P - 1));
+    return true;
   };
+  auto issue_k = [&](int q) {
+    const int st = warp + W * (q % kSpw);
+    size_t row0;
+    if (!chunk_row0(q, row0)) return;
+    uint8_t* dst = region + st * kStageBytes;
+    mbar_arrive_expect_tx(&full[st], H::kKBytes + H::kSfBytes);
+    bulk_g2s(dst, p.k_pool + row0 * H::kRow, H::kKBytes, &full[st], pol);
+    bulk_g2s(dst + 2 * H::kKBytes, p.k_sf + row0 * H::kSfRow, H::kSfBytes, &full[st], pol);
+  };
+  auto issue_v = [&](int q) {
+    const int st = warp + W * (q % kSpw);
+    size_t row0;
+    if (!chunk_row0(q, row0)) return;
+    uint8_t* dst = region + st * kStageBytes;
+    mbar_arrive_expect_tx(&empty[st], H::kKBytes + H::kSfBytes);
+    bulk_g2s(dst + H::kKBytes, p.v_pool + row0 * H::kRow, H::kKBytes, &empty[st], pol);
+    bulk_g2s(dst + 2 * H::kKBytes + H::kSfBytes, p.v_sf + row0 * H::kSfRow, H::kSfBytes,
+             &empty[st], pol);
+  };
+  const int n_first = ONE ? min(kSpw, wcnt) : 0;
   if (ONE && lane == 0) {
     fence_proxy_async_smem();   // after the fused selection's scratch in the region
-    for (int q = 0; q < min(kSpw, wcnt); ++q) issue_one(q);
+    for (int q = 0; q < n_first; ++q) {
+      issue_k(q);
+      issue_v(q);
+    }
   }
 
   if (!producer) {
@@ -879,27 +939,48 @@ sparse_decode_kernel(Params p) {
     }
 
     if (ONE) {
-      int q_dead = -1;
+      // K and V halves requested so far (chunks [0, nk) and [0, nv)) and the
+      // first ones not yet seen complete (a stage has at most one of each in
+      // flight: its next half is requested only after this one completed).
+      int nk = n_first, nv = n_first, k_seen = 0, v_seen = 0;
+      bool dead = false;
       for (int q = 0; q < wcnt; ++q) {
         const int st = warp + W * (q % kSpw);
-        if (!wait_bounded(&full[st], (q / kSpw) & 1)) {
-          q_dead = q;
-          if (lane == 0) atomicExch(p.status, kStatusWaitTimeout);
-          break;
+        const uint32_t ph = (q / kSpw) & 1;
+        const uint8_t* stage = region + st * kStageBytes;
+        if (!wait_bounded(&full[st], ph)) { dead = true; break; }
+        k_seen = q + 1;
+        uint32_t pf[H::kMt][NTR][2];
+        consume_qk<NTR, D>(stage, wl[2 * q + 1], nrow, qf, cq, m_run, l_run, o_acc, pf);
+        __syncwarp();   // every lane's reads of the K half are done
+        if (q + kSpw < wcnt) {
+          if (lane == 0) {
+            fence_proxy_async_smem();
+            issue_k(q + kSpw);
+          }
+          ++nk;
         }
-        consume_chunk<NTR, D>(region + st * kStageBytes, wl[2 * q + 1], nrow, qf, cq, m_run, l_run,
-                           o_acc);
-        __syncwarp();   // every lane's reads of the stage are done
-        if (lane == 0 && q + kSpw < wcnt) {
-          fence_proxy_async_smem();
-          issue_one(q + kSpw);
+        if (!wait_bounded(&empty[st], ph)) { dead = true; break; }
+        v_seen = q + 1;
+        consume_pv<NTR, D>(stage, pf, o_acc);
+        __syncwarp();   // every lane's reads of the V half are done
+        if (q + kSpw < wcnt) {
+          if (lane == 0) {
+            fence_proxy_async_smem();
+            issue_v(q + kSpw);
+          }
+          ++nv;
         }
       }
       // After a wait gave up, let this warp's copies still in flight land
       // before the stage memory is reused.
-      if (q_dead >= 0 && lane == 0)
-        for (int q = q_dead; q < min(wcnt, q_dead + kSpw); ++q)
+      if (dead && lane == 0) {
+        atomicExch(p.status, kStatusWaitTimeout);
+        for (int q = k_seen; q < nk; ++q)
           if (!wait_bounded(&full[warp + W * (q % kSpw)], (q / kSpw) & 1)) break;
+        for (int q = v_seen; q < nv; ++q)
+          if (!wait_bounded(&empty[warp + W * (q % kSpw)], (q / kSpw) & 1)) break;
+      }
     } else {
       bool dead = false;
       int rc = 0;                               // this row's chunks seen so far
@@ -1012,7 +1093,7 @@ sparse_decode_kernel(Params p) {
     float mx = -INFINITY;
 #pragma unroll
     for (int w = 0; w < W; ++w) {
-      mv[w] = (ONE || w % R == j) ? cm[w * kHsp + cc] : -INFINITY;
+      mv[w] = (w % R == j) ? cm[w * kHsp + cc] : -INFINITY;
       mx = fmaxf(mx, mv[w]);
     }
     const float M = (mx == -INFINITY) ? 0.f : mx;
@@ -1020,7 +1101,7 @@ sparse_decode_kernel(Params p) {
     float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int w = 0; w < W; ++w) {
-      if (ONE || w % R == j) {
+      if (w % R == j) {
         const float wt = exp2f(mv[w] - M);
         Lsum += cl[w * kHsp + cc] * wt;
         const float4 v =
@@ -1252,9 +1333,11 @@ int resident_ctas(int R, int k, int mb, int splits) {
   return n < 1 ? 1 : n;
 }
 
-// Variant by (tiles per row, rows): decode rows use W consumers sharing the
-// chunks (S a multiple of W); verify rows a producer warp and W / R
-// consumers per row.
+// Variant by (tiles per row, rows).  Self-issued variants (ONE = true): W
+// warps, each owning one row (two per row for two-row requests), S / W
+// stages per warp.  Union variants (ONE = false, head_dim 256 verify): a
+// producer warp streams the union of the rows' chunks through S stages and
+// W / R consumers per row take the chunks their row selected.
 #ifndef QSA_DECODE_STAGES_R1
 #define QSA_DECODE_STAGES_R1 8
 #endif
@@ -1264,28 +1347,20 @@ int resident_ctas(int R, int k, int mb, int splits) {
 #ifndef QSA_DECODE_STAGES_RN
 #define QSA_DECODE_STAGES_RN 4
 #endif
-#ifndef QSA_DECODE_WARPS_R2
-#define QSA_DECODE_WARPS_R2 4
+#ifndef QSA_VERIFY_STAGES_PER_WARP
+#define QSA_VERIFY_STAGES_PER_WARP 1
 #endif
-#ifndef QSA_DECODE_WARPS_R4
-#define QSA_DECODE_WARPS_R4 4
-#endif
-// head_dim 256: one 8-column tile per row (the output and query fragments are
-// twice as large; wider head groups take several slices), four decode
-// consumers.
+#define QSA_VSPW QSA_VERIFY_STAGES_PER_WARP
 #define QSA_DECODE_VARIANTS(X)                                            \
   X(1, 1, QSA_DECODE_WARPS_R1, QSA_DECODE_STAGES_R1, true, 128)           \
   X(2, 1, QSA_DECODE_WARPS_R1, QSA_DECODE_STAGES_R1, true, 128)           \
-  X(1, 2, QSA_DECODE_WARPS_R2, QSA_DECODE_STAGES_RN, false, 128)         \
-  X(2, 2, 4, QSA_DECODE_STAGES_RN, false, 128)                            \
-  X(1, 3, 6, QSA_DECODE_STAGES_RN, false, 128)                            \
-  X(2, 3, 6, QSA_DECODE_STAGES_RN, false, 128)                            \
-  X(1, 4, QSA_DECODE_WARPS_R4, QSA_DECODE_STAGES_RN, false, 128)         \
-  X(2, 4, 4, QSA_DECODE_STAGES_RN, false, 128)                            \
-  X(1, 5, 5, QSA_DECODE_STAGES_RN, false, 128) X(2, 5, 5, QSA_DECODE_STAGES_RN, false, 128) \
-  X(1, 6, 6, QSA_DECODE_STAGES_RN, false, 128) X(2, 6, 6, QSA_DECODE_STAGES_RN, false, 128) \
-  X(1, 7, 7, QSA_DECODE_STAGES_RN, false, 128) X(2, 7, 7, QSA_DECODE_STAGES_RN, false, 128) \
-  X(1, 8, 8, QSA_DECODE_STAGES_RN, false, 128) X(2, 8, 8, QSA_DECODE_STAGES_RN, false, 128) \
+  X(1, 2, 4, 4 * QSA_VSPW, true, 128) X(2, 2, 4, 4 * QSA_VSPW, true, 128) \
+  X(1, 3, 3, 3 * QSA_VSPW, true, 128) X(2, 3, 3, 3 * QSA_VSPW, true, 128) \
+  X(1, 4, 4, 4 * QSA_VSPW, true, 128) X(2, 4, 4, 4 * QSA_VSPW, true, 128) \
+  X(1, 5, 5, 5 * QSA_VSPW, true, 128) X(2, 5, 5, 5 * QSA_VSPW, true, 128) \
+  X(1, 6, 6, 6 * QSA_VSPW, true, 128) X(2, 6, 6, 6 * QSA_VSPW, true, 128) \
+  X(1, 7, 7, 7 * QSA_VSPW, true, 128) X(2, 7, 7, 7 * QSA_VSPW, true, 128) \
+  X(1, 8, 8, 8 * QSA_VSPW, true, 128) X(2, 8, 8, 8 * QSA_VSPW, true, 128) \
   X(1, 1, 4, 8, true, 256)                                                \
   X(1, 2, 4, QSA_DECODE_STAGES_RN, false, 256)                            \
   X(1, 3, 6, QSA_DECODE_STAGES_RN, false, 256)                            \
