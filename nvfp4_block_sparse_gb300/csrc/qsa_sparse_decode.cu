@@ -145,6 +145,13 @@ __host__ __device__ inline int decode_list_cap(int k, int splits, int W) {
   return (2 * k + splits * W - 1) / (splits * W);
 }
 
+// Rows of its request one CTA takes: all of them, except for self-issued
+// variants with fewer warps than rows (one warp per row, R / W CTAs per
+// request).
+__host__ __device__ inline int rows_per_cta(bool one, int W, int R) {
+  return (one && W < R) ? W : R;
+}
+
 // Shared-memory layout (bytes), shared by host sizing and the kernel.  ONE:
 // the single-row specialisation (no producer warp; W consumer warps).
 template <int NTR, int W, int S, bool ONE, int D>
@@ -155,18 +162,20 @@ struct Layout {
   static constexpr int kStagesSz = S * kStageBytes;
   static constexpr int kPartStride = Hd<D>::kPartStride;
   // After the main loop the stage region holds the consumers' partials (co,
-  // cm, cl) and the CTA partial (cp); the ticket merge then reuses it for its
-  // weights.  Before the main loop it holds the union's temporaries.  With one
-  // consumer per row (direct) each consumer writes its row's partial straight
-  // into cp and co, cm, cl are not used.
+  // cm, cl), the CTA partial (cp) and the cluster merge's receive buffer
+  // (rb); the ticket merge instead reuses it for its weights.  Before the
+  // main loop it holds the union's temporaries.  With one consumer per row
+  // (direct) each consumer writes its row's partial straight into cp and co,
+  // cm, cl are not used.
   static constexpr int kCoSz = W * kHsp * D * 4;
   static constexpr int kCmSz = W * kHsp * 4;
   static constexpr int kClSz = W * kHsp * 4;
   __host__ __device__ static bool direct(int R) { return W == R; }
   __host__ __device__ static int cp_off(int R) { return direct(R) ? 0 : kCoSz + kCmSz + kClSz; }
   __host__ __device__ static int cp_bytes(int R) { return R * kHsp * kPartStride * 4; }
+  __host__ __device__ static int rb_off(int R) { return (cp_off(R) + cp_bytes(R) + 15) & ~15; }
   __host__ __device__ static int region_bytes(int R, int k, int splits) {
-    const int combine = cp_off(R) + cp_bytes(R);
+    const int combine = rb_off(R) + rb_bytes(R, splits);
     const int merge = R * kHsp * (splits + 2) * 4;
     const int uni = R * k * 4 * 2;
     int r = kStagesSz;
@@ -182,7 +191,7 @@ struct Layout {
     return splits * per * kPartStride * 4;
   }
   static size_t bytes(int R, int k, int mb, int splits) {
-    size_t off = (size_t)region_bytes(R, k, splits) + rb_bytes(R, splits);
+    size_t off = (size_t)region_bytes(R, k, splits);
     off += 2 * S * 8;                                   // full + empty barriers
     off += (size_t)R * kHsp * D * 2;                    // q (fp16)
     off += (size_t)R * kHsp * 4 * 2;                    // cq, n per column
@@ -211,9 +220,6 @@ constexpr int decode_min_blocks() {
                               : (ONE ? (W <= 4 ? 4 : 2) : (W <= 4 ? 3 : 2)));
 }
 
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void cluster_arrive_release() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
@@ -479,43 +485,49 @@ sparse_decode_kernel(Params p) {
   const int warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const bool producer = !ONE && warp == W;
-  // Self-issued (ONE) variants: warp w owns row w % R and, of that row's
-  // chunks of this split, every (W / R)-th starting at the (w / R)-th; it
-  // lists, requests and consumes them itself.  Verify (union) variants: a
-  // producer warp streams the union and consumer w owns row w % R.
-  const int gper = W / R;                       // consumers per row
-  const int jw = warp % R;                      // the row this warp owns
-  const int gw = warp / R;
+  // A CTA takes RC consecutive rows of its request (all R rows, except for
+  // self-issued variants with fewer warps than rows: RC = W, one warp per
+  // row, and the request's rows are spread over R / RC CTAs).  Self-issued
+  // (ONE) variants: warp w owns row w % RC and, of that row's chunks of this
+  // split, every (W / RC)-th starting at the (w / RC)-th; it lists, requests
+  // and consumes them itself.  Union variants: a producer warp streams the
+  // union and consumer w owns row w % R.
+  const int RC = rows_per_cta(ONE, W, R);
+  const int nrg = R / RC;                       // row groups per request
+  const int gper = W / RC;                      // consumers per row
+  const int jw = warp % RC;                     // the row (of the CTA's) this warp owns
+  const int gw = warp / RC;
 
   const int s = blockIdx.x;                           // KV split (= cluster rank)
   const int kvh = blockIdx.y / p.slices, slice = blockIdx.y % p.slices;
-  const int b = blockIdx.z;
+  const int b = blockIdx.z / nrg;
+  const int rgi = blockIdx.z - b * nrg;               // row group of the request
+  const int r0 = rgi * RC;                            // its first row
   const int hs0 = slice * kHsp;                       // first head of the slice
   const int hs = min(kHsp, G - hs0);                  // real heads in the slice
-  const int ncols = R * kHsp;                         // padded columns (j, hh)
+  const int ncols = RC * kHsp;                        // padded columns (j, hh)
   const int k = p.k;
 
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* region = smem;
-  size_t off = (size_t)Lay::region_bytes(R, k, p.splits);
-  float* rb = reinterpret_cast<float*>(smem + off);   // cluster merge receive buffer
-  off += (size_t)Lay::rb_bytes(R, p.splits);
+  size_t off = (size_t)Lay::region_bytes(RC, k, p.splits);
+  float* rb = reinterpret_cast<float*>(region + Lay::rb_off(RC));   // cluster merge receive buffer
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + off);
   uint64_t* empty = full + S;
   off += 2 * S * 8;
   __half* qs = reinterpret_cast<__half*>(smem + off);
-  off += (size_t)R * kHsp * D * 2;
+  off += (size_t)RC * kHsp * D * 2;
   float* col_cq = reinterpret_cast<float*>(smem + off);
   int* col_n = reinterpret_cast<int*>(col_cq + ncols);
   off += (size_t)ncols * 4 * 2;
   int* misc = reinterpret_cast<int*>(smem + off);
   off += 64 * 4;
   int32_t* s_sel = reinterpret_cast<int32_t*>(smem + off);
-  int32_t* s_union = s_sel + R * k;
-  int32_t* s_upage = s_union + R * k;
-  int32_t* s_scan = s_upage + R * k;                  // [R * k + 1]
+  int32_t* s_union = s_sel + RC * k;                  // (union variants: RC = R)
+  int32_t* s_upage = s_union + RC * k;
+  int32_t* s_scan = s_upage + RC * k;                 // [R * k + 1]
   const int list_ints = ONE ? W * 2 * decode_list_cap(k, p.splits, gper) + k : 0;
-  int32_t* s_pt = s_sel + (list_ints > R * k * 4 + 4 ? list_ints : R * k * 4 + 4);
+  int32_t* s_pt = s_sel + (list_ints > RC * k * 4 + 4 ? list_ints : RC * k * 4 + 4);
 
   // full[st]: one arrival (the copy issuer) plus the copies' bytes.  empty[st]
   // (verify only): every row consumer arrives, so stage reuse waits for all.
@@ -527,9 +539,6 @@ sparse_decode_kernel(Params p) {
     }
     fence_mbar_init();
   }
-  // Cluster merge: this arrival is matched by the wait before the first
-  // remote write, which so only starts once every CTA of the cluster runs.
-  if (p.cluster > 1) cluster_arrive_relaxed();
 
   // ---- before the dependency wait: what does not depend on the selection ---
   // The queries, the request's page-table row and its length are step inputs
@@ -560,7 +569,7 @@ sparse_decode_kernel(Params p) {
         const int j = c / kHsp;
         const int h = kvh * G + hs0 + c % kHsp;
         const uint2* src = reinterpret_cast<const uint2*>(
-            p.q + ((size_t)(b * R + j) * g.Hq + h) * D + lane * (D / 32));
+            p.q + ((size_t)(b * R + r0 + j) * g.Hq + h) * D + lane * (D / 32));
 #pragma unroll
         for (int u = 0; u < kQw; ++u) raw[ci][u] = src[u];
       }
@@ -592,7 +601,7 @@ sparse_decode_kernel(Params p) {
       for (int i = 0; i < 2 * kQw; ++i) dst[i] = __floats2half2_rn(v[2 * i] * up, v[2 * i + 1] * up);
       if (lane == 0) {
         col_cq[c] = ((c % kHsp) < hs) ? p.k_scale * p.sm_scale * kLog2e * down : 0.f;
-        col_n[c] = visible_tokens(L, R, c / kHsp, cap);
+        col_n[c] = visible_tokens(L, R, r0 + c / kHsp, cap);
       }
     }
     }
@@ -613,7 +622,7 @@ sparse_decode_kernel(Params p) {
   int wcnt = 0;
   if constexpr (ONE) {
     const int nc = k << csh;
-    const int32_t* selrow = p.sel + (size_t)(b * R + jw) * k;
+    const int32_t* selrow = p.sel + (size_t)(b * R + r0 + jw) * k;
     if (p.scores) {
       // Fused selection (one row per request): this CTA selects its row from
       // the scores, with the (still idle) stage region as the selection's
@@ -800,7 +809,9 @@ sparse_decode_kernel(Params p) {
   }
   __syncthreads();
   }   // verify union
+#ifndef QSA_LATE_TRIGGER
   pdl_trigger();
+#endif
 
   const int U = ONE ? 0 : s_scan[R * k];
   const int C = U << csh;
@@ -1018,11 +1029,14 @@ sparse_decode_kernel(Params p) {
 
   // ---- combine the consumers of this CTA ------------------------------------
   __syncthreads();   // every copy landed and was consumed: reuse the stage region
-  const bool direct = Lay::direct(R);
+#ifdef QSA_LATE_TRIGGER
+  pdl_trigger();
+#endif
+  const bool direct = Lay::direct(RC);
   float* co = reinterpret_cast<float*>(region);                  // [W][kHsp][D]
   float* cm = co + W * kHsp * D;                                  // [W][kHsp]
   float* cl = cm + W * kHsp;                                      // [W][kHsp]
-  float* cp = reinterpret_cast<float*>(region + Lay::cp_off(R));  // [ncols][kPartStride]
+  float* cp = reinterpret_cast<float*>(region + Lay::cp_off(RC));  // [ncols][kPartStride]
   if (!producer) {
     // Direct: consumer `warp` is row `warp`'s only consumer, and its state is
     // the CTA partial of the row's columns.
@@ -1062,8 +1076,8 @@ sparse_decode_kernel(Params p) {
     const int j = c / kHsp, hh = c % kHsp;
     if (hh >= hs) return;   // padding column
     const int h = kvh * G + hs0 + hh;
-    const size_t orow = (size_t)(b * R + j) * g.Hq + h;
-    if (!QSA_IN_BOUNDS(j < R && b < g.B && h < g.Hq && d4 + 4 <= D, kChkOut)) return;
+    const size_t orow = (size_t)(b * R + r0 + j) * g.Hq + h;
+    if (!QSA_IN_BOUNDS(r0 + j < R && b < g.B && h < g.Hq && d4 + 4 <= D, kChkOut)) return;
     const float sc = Lsum > 0.f ? p.v_scale / Lsum : 0.f;
     __nv_bfloat162 o01 = __floats2bfloat162_rn(O.x * sc, O.y * sc);
     __nv_bfloat162 o23 = __floats2bfloat162_rn(O.z * sc, O.w * sc);
@@ -1084,7 +1098,7 @@ sparse_decode_kernel(Params p) {
     }
   } else {
   // CTA partial per column (j, hh): m (log2 domain, -inf when empty), l, O,
-  // merged over the consumers of row j (warps j, j + R, ...).  With one split
+  // merged over the consumers of row j (warps j, j + RC, ...).  With one split
   // it is the result.
   for (int idx = tid; idx < ncols * (D / 4); idx += kThreads) {
     const int c = idx / (D / 4), d4 = (idx % (D / 4)) * 4;
@@ -1093,7 +1107,7 @@ sparse_decode_kernel(Params p) {
     float mx = -INFINITY;
 #pragma unroll
     for (int w = 0; w < W; ++w) {
-      mv[w] = (w % R == j) ? cm[w * kHsp + cc] : -INFINITY;
+      mv[w] = (w % RC == j) ? cm[w * kHsp + cc] : -INFINITY;
       mx = fmaxf(mx, mv[w]);
     }
     const float M = (mx == -INFINITY) ? 0.f : mx;
@@ -1101,7 +1115,7 @@ sparse_decode_kernel(Params p) {
     float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int w = 0; w < W; ++w) {
-      if (w % R == j) {
+      if (w % RC == j) {
         const float wt = exp2f(mv[w] - M);
         Lsum += cl[w * kHsp + cc] * wt;
         const float4 v =
@@ -1134,7 +1148,10 @@ sparse_decode_kernel(Params p) {
     cg::cluster_group cluster = cg::this_cluster();
     const int CL = p.cluster;
     const int per = (ncols + CL - 1) / CL;
-    cluster_wait_acquire();   // pairs with the arrival at the start
+    // The receive buffers live in the stage regions: the first barrier lets
+    // every CTA of the cluster finish its main loop before any remote write.
+    cluster_arrive_release();
+    cluster_wait_acquire();
     for (int idx = tid; idx < ncols * (kPartStride / 4); idx += kThreads) {
       const int c = idx / (kPartStride / 4), w4 = (idx % (kPartStride / 4)) * 4;
       float* dst = cluster.map_shared_rank(rb, c % CL) +
@@ -1175,7 +1192,7 @@ sparse_decode_kernel(Params p) {
   // Ticket merge: partials go to the workspace; the last split of this
   // (request, KV head, slice) to arrive merges them in split order
   // (deterministic) and resets the ticket.
-  const int units_idx = (b * g.Hkv + kvh) * p.slices + slice;
+  const int units_idx = ((b * g.Hkv + kvh) * p.slices + slice) * nrg + rgi;
   if (!QSA_IN_BOUNDS(b < g.B && kvh < g.Hkv && slice < p.slices && s < p.splits, kChkUnit))
     return;
   const size_t split_floats = (size_t)ncols * kPartStride;
@@ -1333,11 +1350,13 @@ int resident_ctas(int R, int k, int mb, int splits) {
   return n < 1 ? 1 : n;
 }
 
-// Variant by (tiles per row, rows).  Self-issued variants (ONE = true): W
-// warps, each owning one row (two per row for two-row requests), S / W
-// stages per warp.  Union variants (ONE = false, head_dim 256 verify): a
-// producer warp streams the union of the rows' chunks through S stages and
-// W / R consumers per row take the chunks their row selected.
+// Variant by (tiles per row, rows, head_dim).  Self-issued variants (ONE =
+// true): W warps, each owning one row (two per row for two-row requests at
+// head_dim 128), S / W stages per warp; decode rows at head_dim 256 use four
+// warps per row.  Built with QSA_VERIFY_UNION, verify rows run the union
+// variants instead (ONE = false: a producer warp streams the union of the
+// rows' chunks through S stages, W / R consumers per row take the chunks
+// their row selected), kept for comparison.
 #ifndef QSA_DECODE_STAGES_R1
 #define QSA_DECODE_STAGES_R1 8
 #endif
@@ -1350,25 +1369,33 @@ int resident_ctas(int R, int k, int mb, int splits) {
 #ifndef QSA_VERIFY_STAGES_PER_WARP
 #define QSA_VERIFY_STAGES_PER_WARP 1
 #endif
+// Warps per verify CTA (0 = one per row, two per row for two-row requests at
+// head_dim 128; n > 0 = n warps, one row each, the request's rows spread over
+// R / n CTAs where n divides R).
+#ifndef QSA_VERIFY_CTA_WARPS
+#define QSA_VERIFY_CTA_WARPS 0
+#endif
 #define QSA_VSPW QSA_VERIFY_STAGES_PER_WARP
-#define QSA_DECODE_VARIANTS(X)                                            \
-  X(1, 1, QSA_DECODE_WARPS_R1, QSA_DECODE_STAGES_R1, true, 128)           \
-  X(2, 1, QSA_DECODE_WARPS_R1, QSA_DECODE_STAGES_R1, true, 128)           \
-  X(1, 2, 4, 4 * QSA_VSPW, true, 128) X(2, 2, 4, 4 * QSA_VSPW, true, 128) \
-  X(1, 3, 3, 3 * QSA_VSPW, true, 128) X(2, 3, 3, 3 * QSA_VSPW, true, 128) \
-  X(1, 4, 4, 4 * QSA_VSPW, true, 128) X(2, 4, 4, 4 * QSA_VSPW, true, 128) \
-  X(1, 5, 5, 5 * QSA_VSPW, true, 128) X(2, 5, 5, 5 * QSA_VSPW, true, 128) \
-  X(1, 6, 6, 6 * QSA_VSPW, true, 128) X(2, 6, 6, 6 * QSA_VSPW, true, 128) \
-  X(1, 7, 7, 7 * QSA_VSPW, true, 128) X(2, 7, 7, 7 * QSA_VSPW, true, 128) \
-  X(1, 8, 8, 8 * QSA_VSPW, true, 128) X(2, 8, 8, 8 * QSA_VSPW, true, 128) \
-  X(1, 1, 4, 8, true, 256)                                                \
-  X(1, 2, 4, QSA_DECODE_STAGES_RN, false, 256)                            \
-  X(1, 3, 6, QSA_DECODE_STAGES_RN, false, 256)                            \
-  X(1, 4, 4, QSA_DECODE_STAGES_RN, false, 256)                            \
-  X(1, 5, 5, QSA_DECODE_STAGES_RN, false, 256)                            \
-  X(1, 6, 6, QSA_DECODE_STAGES_RN, false, 256)                            \
-  X(1, 7, 7, QSA_DECODE_STAGES_RN, false, 256)                            \
-  X(1, 8, 8, QSA_DECODE_STAGES_RN, false, 256)
+#define QSA_VW(R_, DEF_) \
+  ((QSA_VERIFY_CTA_WARPS > 0 && (R_) % QSA_VERIFY_CTA_WARPS == 0) ? QSA_VERIFY_CTA_WARPS : (DEF_))
+#ifdef QSA_VERIFY_UNION
+#define QSA_V128(NTR_, R_, DEF_) X(NTR_, R_, (R_) == 2 ? 4 : (R_), QSA_DECODE_STAGES_RN, false, 128)
+#define QSA_V256(R_, W_) X(1, R_, W_, QSA_DECODE_STAGES_RN, false, 256)
+#else
+#define QSA_V128(NTR_, R_, DEF_) \
+  X(NTR_, R_, QSA_VW(R_, DEF_), QSA_VW(R_, DEF_) * QSA_VSPW, true, 128)
+#define QSA_V256(R_, W_) X(1, R_, QSA_VW(R_, R_), QSA_VW(R_, R_) * QSA_VSPW, true, 256)
+#endif
+#define QSA_DECODE_VARIANTS(X)                                                        \
+  X(1, 1, QSA_DECODE_WARPS_R1, QSA_DECODE_STAGES_R1, true, 128)                       \
+  X(2, 1, QSA_DECODE_WARPS_R1, QSA_DECODE_STAGES_R1, true, 128)                       \
+  QSA_V128(1, 2, 4) QSA_V128(2, 2, 4) QSA_V128(1, 3, 3) QSA_V128(2, 3, 3)             \
+  QSA_V128(1, 4, 4) QSA_V128(2, 4, 4) QSA_V128(1, 5, 5) QSA_V128(2, 5, 5)             \
+  QSA_V128(1, 6, 6) QSA_V128(2, 6, 6) QSA_V128(1, 7, 7) QSA_V128(2, 7, 7)             \
+  QSA_V128(1, 8, 8) QSA_V128(2, 8, 8)                                                 \
+  X(1, 1, 4, 8, true, 256)                                                            \
+  QSA_V256(2, 4) QSA_V256(3, 6) QSA_V256(4, 4) QSA_V256(5, 5) QSA_V256(6, 6)          \
+  QSA_V256(7, 7) QSA_V256(8, 8)
 
 int tiles_per_row(const Geom& g) {
   const int G = g.Hq / g.Hkv;
@@ -1377,9 +1404,19 @@ int tiles_per_row(const Geom& g) {
 
 int stage_tokens(const Geom& g) { return 8192 / g.D; }
 
-int variant_resident(int ntr, int R, int d, int k, int mb, int splits) {
+// Rows per CTA of the variant that serves (tiles per row, R, D).
+int variant_rows(int ntr, int R, int d) {
 #define X(NTR_, R_, W_, S_, ONE_, D_) \
-  if (ntr == NTR_ && R == R_ && d == D_) return resident_ctas<NTR_, W_, S_, ONE_, D_>(R, k, mb, splits);
+  if (ntr == NTR_ && R == R_ && d == D_) return rows_per_cta(ONE_, W_, R_);
+  QSA_DECODE_VARIANTS(X)
+#undef X
+  return R;
+}
+
+int variant_resident(int ntr, int R, int d, int k, int mb, int splits) {
+  const int rc = variant_rows(ntr, R, d);
+#define X(NTR_, R_, W_, S_, ONE_, D_) \
+  if (ntr == NTR_ && R == R_ && d == D_) return resident_ctas<NTR_, W_, S_, ONE_, D_>(rc, k, mb, splits);
   QSA_DECODE_VARIANTS(X)
 #undef X
   return 1;
@@ -1407,8 +1444,10 @@ DecodePlan plan_legacy_decode(const Geom& g, int k, int num_splits) {
   const int G = g.Hq / g.Hkv;
   const int ntr = tiles_per_row(g);
   pl.qgroups = (G + 8 * ntr - 1) / (8 * ntr);           // head slices per KV head
-  pl.cols = g.R * 8 * ntr;                               // padded columns per CTA
-  const long long units = (long long)g.B * g.Hkv * pl.qgroups;
+  const int rc = variant_rows(ntr, g.R, g.D);            // rows per CTA
+  pl.cols = rc * 8 * ntr;                                // padded columns per CTA
+  // units: (request, KV head, head slice, row group)
+  const long long units = (long long)g.B * g.Hkv * pl.qgroups * (g.R / rc);
   const int max_union = min(g.R * k, g.MB);
   const int max_chunks = max(1, max_union * (g.P / stage_tokens(g)));
   int splits = num_splits;
@@ -1459,18 +1498,19 @@ cudaError_t launch_legacy_decode(const Geom& g, const DecodePlan& plan, const vo
   prm.out = reinterpret_cast<__nv_bfloat16*>(out);
   prm.lse = lse;
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
-  const long long units = (long long)g.B * g.Hkv * plan.qgroups;
+  const int ntr = tiles_per_row(g);
+  const int rc = variant_rows(ntr, g.R, g.D);
+  const long long units = (long long)g.B * g.Hkv * plan.qgroups * (g.R / rc);
   prm.status = reinterpret_cast<int*>(ws);
   prm.tickets = reinterpret_cast<int*>(ws + kWsHeader);
   prm.partials = reinterpret_cast<float*>(ws + kWsHeader + align256((size_t)units * sizeof(int)));
   prm.splits = plan.splits;
   prm.slices = plan.qgroups;
   prm.cluster = 1;
-  dim3 grid(plan.splits, g.Hkv * plan.qgroups, g.B);
-  const int ntr = tiles_per_row(g);
+  dim3 grid(plan.splits, g.Hkv * plan.qgroups, g.B * (g.R / rc));
 #define X(NTR_, R_, W_, S_, ONE_, D_)                                \
   if (ntr == NTR_ && g.R == R_ && g.D == D_)                           \
-    return launch_t<NTR_, W_, S_, ONE_, D_>(prm, grid, g.R, k, g.MB, pdl, stream);
+    return launch_t<NTR_, W_, S_, ONE_, D_>(prm, grid, rc, k, g.MB, pdl, stream);
   QSA_DECODE_VARIANTS(X)
 #undef X
   return cudaErrorInvalidValue;
