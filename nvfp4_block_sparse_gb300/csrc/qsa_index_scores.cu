@@ -234,7 +234,7 @@ index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __r
                         const int32_t* __restrict__ seqlens, int32_t* __restrict__ scores,
                         int blocks_per_warp) {
   constexpr int RB = kMaxRows;                 // the 8 MMA columns hold the rows
-  __shared__ int32_t wpart[4][RB][kIndexDim];
+  static_assert(RB * 32 == kThreads, "one warp per row of the group for the head sums");
   __shared__ __half wsplit[2][RB][kIndexDim];   // a, b
 
   const int b = blockIdx.y;
@@ -270,33 +270,48 @@ index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __r
   int4 kv[P / 8];
   if (live0) load_keys(page0, kv);
 
-  // Head sums w[j][d], then the exact split w = 128*a + b.
-  for (int idx = threadIdx.x; idx < 4 * RB * kIndexDim; idx += kThreads) {
-    const int hg = idx / (RB * kIndexDim);
-    const int j = (idx / kIndexDim) % RB;
-    const int d = idx % kIndexDim;
-    int s = 0;
+  // Head sums w[j][d], then the exact split w = 128*a + b.  Thread pair
+  // (t >> 1) owns row j = t >> 5 and dims 4*d4..4*d4+3 (d4 = (t >> 1) & 15);
+  // the two threads of a pair take alternate heads, 4-byte loads, up to 16
+  // of them in flight per thread, then one shuffle adds the pair.
+  {
+    const int t = threadIdx.x;
+    const int j = t >> 5, d4 = (t >> 1) & 15, hs = t & 1;
+    int s0 = 0, s1 = 0, s2 = 0, s3 = 0;
     if (r0 + j < R) {
-      const int8_t* src = iq + ((size_t)((size_t)b * R + r0 + j) * g.Hq) * kIndexDim + d;
-      int h = hg;
-      for (; h + 28 < g.Hq; h += 32) {
-        int v[8];
+      const int8_t* src = iq + ((size_t)((size_t)b * R + r0 + j) * g.Hq) * kIndexDim + 4 * d4;
+      for (int h0 = hs; h0 < g.Hq; h0 += 32) {
+        uint32_t v[16];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = src[(size_t)(h + 4 * u) * kIndexDim];
+        for (int u = 0; u < 16; ++u) {
+          const int h = h0 + 2 * u;
+          v[u] = h < g.Hq ? __ldg(reinterpret_cast<const uint32_t*>(src + (size_t)h * kIndexDim))
+                          : 0u;
+        }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) s += v[u];
+        for (int u = 0; u < 16; ++u) {
+          // byte i sign-extended: prmt selector nibbles (i, 8|i, 8|i, 8|i)
+          s0 += (int)prmt(v[u], 0u, 0x8880);
+          s1 += (int)prmt(v[u], 0u, 0x9991);
+          s2 += (int)prmt(v[u], 0u, 0xAAA2);
+          s3 += (int)prmt(v[u], 0u, 0xBBB3);
+        }
       }
-      for (; h < g.Hq; h += 4) s += src[(size_t)h * kIndexDim];
     }
-    wpart[hg][j][d] = s;
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < RB * kIndexDim; idx += kThreads) {
-    const int j = idx / kIndexDim, d = idx % kIndexDim;
-    const int w = wpart[0][j][d] + wpart[1][j][d] + wpart[2][j][d] + wpart[3][j][d];
-    const int lo = ((w + 64) & 127) - 64;
-    wsplit[0][j][d] = __int2half_rn((w - lo) / 128);
-    wsplit[1][j][d] = __int2half_rn(lo);
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+    s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+    s3 += __shfl_xor_sync(0xffffffffu, s3, 1);
+    if (hs == 0) {
+      const int w4[4] = {s0, s1, s2, s3};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int w = w4[i];
+        const int lo = ((w + 64) & 127) - 64;
+        wsplit[0][j][4 * d4 + i] = __int2half_rn((w - lo) / 128);
+        wsplit[1][j][4 * d4 + i] = __int2half_rn(lo);
+      }
+    }
   }
   __syncthreads();
   pdl_trigger();
@@ -546,16 +561,22 @@ index_scores_rows_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __
   }
 }
 
-// Blocks each warp scores: one, unless the grid would exceed about four
-// resident CTAs per SM.
+// Blocks each warp scores: one, unless the grid would exceed about
+// QSA_INDEX_CTAS_PER_SM resident CTAs per SM (at most QSA_INDEX_BPW_MAX).
+#ifndef QSA_INDEX_CTAS_PER_SM
+#define QSA_INDEX_CTAS_PER_SM 8
+#endif
+#ifndef QSA_INDEX_BPW_MAX
+#define QSA_INDEX_BPW_MAX 4
+#endif
 int blocks_per_warp_for(const Geom& g) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long warps_needed = (long long)g.B * g.MB;
-  const long long warp_slots = (long long)sms * 4 * kWarps;
+  const long long warp_slots = (long long)sms * QSA_INDEX_CTAS_PER_SM * kWarps;
   int bpw = (int)((warps_needed + warp_slots - 1) / warp_slots);
-  return bpw < 1 ? 1 : (bpw > 4 ? 4 : bpw);
+  return bpw < 1 ? 1 : (bpw > QSA_INDEX_BPW_MAX ? QSA_INDEX_BPW_MAX : bpw);
 }
 
 template <int P, int RB, bool PIPE>
