@@ -68,11 +68,11 @@ constexpr int kPRow = 72;                     // halfs per P-tile row (64 tokens
 constexpr int kRec = 8 + kD;                  // record: m, l[4 warps], pad[3], O[D]
 constexpr int kMaxCols = 32;
 // Bounds-check codes (reported by bounds-checked builds only).
-constexpr int kChkList = 0x101;     // chunk-list slot past the list capacity
-constexpr int kChkChunk = 0x102;    // listed chunk: slot, page id or token offset out of range
-constexpr int kChkOut = 0x103;      // output row or dims out of range
-constexpr int kChkRecord = 0x104;   // cluster record slot out of range
-constexpr int kChkUnit = 0x105;     // workspace unit or split out of range
+[[maybe_unused]] constexpr int kChkList = 0x101;     // chunk-list slot past the list capacity
+[[maybe_unused]] constexpr int kChkChunk = 0x102;    // listed chunk: slot, page id or token offset out of range
+[[maybe_unused]] constexpr int kChkOut = 0x103;      // output row or dims out of range
+[[maybe_unused]] constexpr int kChkRecord = 0x104;   // cluster record slot out of range
+[[maybe_unused]] constexpr int kChkUnit = 0x105;     // workspace unit or split out of range
 constexpr int kMaxCl = 16;                    // cluster size (non-portable above 8)
 constexpr int kPtMax = 4096;                  // page-table rows up to this stay in smem
 constexpr float kLog2e = 1.4426950408889634f;

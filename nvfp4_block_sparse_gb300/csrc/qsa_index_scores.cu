@@ -27,8 +27,8 @@ namespace qsa {
 namespace {
 
 // Bounds-check codes (reported by bounds-checked builds only).
-constexpr int kChkPage = 0x301;    // index-key page id out of range
-constexpr int kChkScore = 0x302;   // score row or block out of range
+[[maybe_unused]] constexpr int kChkPage = 0x301;    // index-key page id out of range
+[[maybe_unused]] constexpr int kChkScore = 0x302;   // score row or block out of range
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 

@@ -24,7 +24,7 @@ namespace qsa {
 namespace {
 
 // Bounds-check code (reported by bounds-checked builds only): pool row out of range.
-constexpr int kChkRow = 0x601;
+[[maybe_unused]] constexpr int kChkRow = 0x601;
 constexpr int kWarpsPerCta = 8;
 constexpr int kIkWords = kIndexDim / 4;                              // 16
 

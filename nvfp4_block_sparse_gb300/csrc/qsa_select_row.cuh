@@ -33,8 +33,8 @@ constexpr int kSelDigitBits = 11;
 constexpr int kSelBins = 1 << kSelDigitBits;
 constexpr int kSelMaxMembers = 256;   // boundary-bin members ranked directly
 // Bounds-check codes (reported by bounds-checked builds only).
-constexpr int kChkSelMember = 0x401;  // boundary-member list slot past its capacity
-constexpr int kChkSelOut = 0x402;     // selection slot at or past k
+[[maybe_unused]] constexpr int kChkSelMember = 0x401;  // boundary-member list slot past its capacity
+[[maybe_unused]] constexpr int kChkSelOut = 0x402;     // selection slot at or past k
 
 // Shared memory a CTA of NTHREADS needs for rows of up to `mb` blocks.
 template <int NTHREADS>

@@ -67,11 +67,11 @@ struct Hd {
   static constexpr int kRuns = D / 128;              // 16-byte runs of a row per lane
 };
 // Bounds-check codes (reported by bounds-checked builds only).
-constexpr int kChkList = 0x201;    // decode warp list slot past its capacity
-constexpr int kChkUnion = 0x202;   // verify union slot out of range
-constexpr int kChkChunk = 0x203;   // chunk: slot, page id or token offset out of range
-constexpr int kChkOut = 0x204;     // output row or dims out of range
-constexpr int kChkUnit = 0x205;    // workspace unit or split out of range
+[[maybe_unused]] constexpr int kChkList = 0x201;    // decode warp list slot past its capacity
+[[maybe_unused]] constexpr int kChkUnion = 0x202;   // verify union slot out of range
+[[maybe_unused]] constexpr int kChkChunk = 0x203;   // chunk: slot, page id or token offset out of range
+[[maybe_unused]] constexpr int kChkOut = 0x204;     // output row or dims out of range
+[[maybe_unused]] constexpr int kChkUnit = 0x205;    // workspace unit or split out of range
 constexpr int kStageBytes = 9216;
 static_assert(2 * Hd<128>::kKBytes + 2 * Hd<128>::kSfBytes == kStageBytes, "stage size");
 static_assert(2 * Hd<256>::kKBytes + 2 * Hd<256>::kSfBytes == kStageBytes, "stage size");
@@ -182,6 +182,8 @@ struct Layout {
     r = r > combine ? r : combine;
     r = r > merge ? r : merge;
     r = r > uni ? r : uni;
+    const int qtile = R * kHsp * D * 2;   // the queries, before the main loop
+    r = r > qtile ? r : qtile;
     return (r + 15) & ~15;
   }
   // Receive buffer of the cluster merge: [splits][ceil(ncols / splits)] partials.
@@ -193,16 +195,12 @@ struct Layout {
   static size_t bytes(int R, int k, int mb, int splits) {
     size_t off = (size_t)region_bytes(R, k, splits);
     off += 2 * S * 8;                                   // full + empty barriers
-    off += (size_t)R * kHsp * D * 2;                    // q (fp16)
     off += (size_t)R * kHsp * 4 * 2;                    // cq, n per column
     off += 64 * 4;                                      // scalars
-    // sel rows, union ids, pages, scan (verify) / per-warp chunk lists (decode)
-    size_t sel_bytes = (size_t)R * k * 4 * 4 + 16;
-    if (ONE) {   // per-warp chunk lists, then the fused selection's row
-      const size_t lists = ((size_t)W * 2 * decode_list_cap(k, splits, W / R) + k) * 4;
-      if (lists > sel_bytes) sel_bytes = lists;
-    }
-    off += sel_bytes;
+    // union variants: sel rows, union ids, pages, scan; self-issued: the
+    // per-warp chunk lists, then the fused selection's row
+    off += ONE ? ((size_t)W * 2 * decode_list_cap(k, splits, W / R) + k) * 4
+               : (size_t)R * k * 4 * 4 + 16;
     off += mb <= kPtRowMax ? (size_t)mb * 4 : 0;        // page-table row
     return off;
   }
@@ -213,11 +211,14 @@ struct Layout {
 // verify CTAs with up to four row consumers, unconstrained otherwise; at
 // D = 256 (twice the output and query fragments) two CTAs per SM of up to
 // five warps, unconstrained for wider ones.
+#ifndef QSA_SELF_MIN_BLOCKS
+#define QSA_SELF_MIN_BLOCKS 4
+#endif
 template <int NTR, int W, bool ONE, int D>
 constexpr int decode_min_blocks() {
   return NTR != 1 ? 1
                   : (D != 128 ? (W <= 4 ? 2 : 1)
-                              : (ONE ? (W <= 4 ? 4 : 2) : (W <= 4 ? 3 : 2)));
+                              : (ONE ? (W <= 4 ? QSA_SELF_MIN_BLOCKS : 2) : (W <= 4 ? 3 : 2)));
 }
 
 __device__ __forceinline__ void cluster_arrive_release() {
@@ -515,8 +516,9 @@ sparse_decode_kernel(Params p) {
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + off);
   uint64_t* empty = full + S;
   off += 2 * S * 8;
-  __half* qs = reinterpret_cast<__half*>(smem + off);
-  off += (size_t)RC * kHsp * D * 2;
+  // The fp16 query tile sits in the stage region: every warp takes its
+  // fragments into registers before the region is first written.
+  __half* qs = reinterpret_cast<__half*>(region);
   float* col_cq = reinterpret_cast<float*>(smem + off);
   int* col_n = reinterpret_cast<int*>(col_cq + ncols);
   off += (size_t)ncols * 4 * 2;
@@ -527,7 +529,7 @@ sparse_decode_kernel(Params p) {
   int32_t* s_upage = s_union + RC * k;
   int32_t* s_scan = s_upage + RC * k;                 // [R * k + 1]
   const int list_ints = ONE ? W * 2 * decode_list_cap(k, p.splits, gper) + k : 0;
-  int32_t* s_pt = s_sel + (list_ints > RC * k * 4 + 4 ? list_ints : RC * k * 4 + 4);
+  int32_t* s_pt = s_sel + (ONE ? list_ints : RC * k * 4 + 4);
 
   // full[st]: one arrival (the copy issuer) plus the copies' bytes.  empty[st]
   // (verify only): every row consumer arrives, so stage reuse waits for all.
@@ -608,6 +610,32 @@ sparse_decode_kernel(Params p) {
   }
 
   __syncthreads();   // barriers, page-table row and queries visible to every warp
+
+  // Each consumer's query fragments and column constants, into registers.
+  const int cbase = jw * kHsp;
+  float cq[NTR][2];
+  int nrow = 0;                                 // tokens this row sees
+  // Q^T fragments: column nt*8+gid of the row, dims [D/4*tig, D/4*(tig+1)).
+  uint32_t qf[NTR][D / 8];
+  if (!producer) {
+#pragma unroll
+    for (int nt = 0; nt < NTR; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) cq[nt][e] = col_cq[cbase + nt * 8 + 2 * tig + e];
+    nrow = col_n[cbase];
+#pragma unroll
+    for (int nt = 0; nt < NTR; ++nt) {
+      const uint4* src =
+          reinterpret_cast<const uint4*>(qs + (cbase + nt * 8 + gid) * D + (D / 4) * tig);
+#pragma unroll
+      for (int v4 = 0; v4 < D / 32; ++v4) {
+        const uint4 x = src[v4];
+        qf[nt][4 * v4 + 0] = x.x; qf[nt][4 * v4 + 1] = x.y;
+        qf[nt][4 * v4 + 2] = x.z; qf[nt][4 * v4 + 3] = x.w;
+      }
+    }
+  }
+  __syncthreads();   // the query tile (in the stage region) is no longer read
   pdl_wait();        // the selections come from the preceding kernel
 
   const int csh = (g.P == 2 * kChunk) ? 1 : 0;  // stages per page: 1 << csh
@@ -809,9 +837,7 @@ sparse_decode_kernel(Params p) {
   }
   __syncthreads();
   }   // verify union
-#ifndef QSA_LATE_TRIGGER
   pdl_trigger();
-#endif
 
   const int U = ONE ? 0 : s_scan[R * k];
   const int C = U << csh;
@@ -928,27 +954,6 @@ sparse_decode_kernel(Params p) {
   }
 
   if (!producer) {
-    const int cbase = jw * kHsp;
-    float cq[NTR][2];
-#pragma unroll
-    for (int nt = 0; nt < NTR; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) cq[nt][e] = col_cq[cbase + nt * 8 + 2 * tig + e];
-    const int nrow = col_n[cbase];              // tokens this row sees
-    // Q^T fragments: column nt*8+gid of the row, dims [D/4*tig, D/4*(tig+1)).
-    uint32_t qf[NTR][D / 8];
-#pragma unroll
-    for (int nt = 0; nt < NTR; ++nt) {
-      const uint4* src =
-          reinterpret_cast<const uint4*>(qs + (cbase + nt * 8 + gid) * D + (D / 4) * tig);
-#pragma unroll
-      for (int v4 = 0; v4 < D / 32; ++v4) {
-        const uint4 x = src[v4];
-        qf[nt][4 * v4 + 0] = x.x; qf[nt][4 * v4 + 1] = x.y;
-        qf[nt][4 * v4 + 2] = x.z; qf[nt][4 * v4 + 3] = x.w;
-      }
-    }
-
     if (ONE) {
       // K and V halves requested so far (chunks [0, nk) and [0, nv)) and the
       // first ones not yet seen complete (a stage has at most one of each in
@@ -1029,9 +1034,7 @@ sparse_decode_kernel(Params p) {
 
   // ---- combine the consumers of this CTA ------------------------------------
   __syncthreads();   // every copy landed and was consumed: reuse the stage region
-#ifdef QSA_LATE_TRIGGER
-  pdl_trigger();
-#endif
+
   const bool direct = Lay::direct(RC);
   float* co = reinterpret_cast<float*>(region);                  // [W][kHsp][D]
   float* cm = co + W * kHsp * D;                                  // [W][kHsp]
@@ -1377,7 +1380,9 @@ int resident_ctas(int R, int k, int mb, int splits) {
 #endif
 #define QSA_VSPW QSA_VERIFY_STAGES_PER_WARP
 #define QSA_VW(R_, DEF_) \
-  ((QSA_VERIFY_CTA_WARPS > 0 && (R_) % QSA_VERIFY_CTA_WARPS == 0) ? QSA_VERIFY_CTA_WARPS : (DEF_))
+  ((QSA_VERIFY_CTA_WARPS > 0 && (R_) % (QSA_VERIFY_CTA_WARPS > 0 ? QSA_VERIFY_CTA_WARPS : 1) == 0) \
+       ? QSA_VERIFY_CTA_WARPS                                                        \
+       : (DEF_))
 #ifdef QSA_VERIFY_UNION
 #define QSA_V128(NTR_, R_, DEF_) X(NTR_, R_, (R_) == 2 ? 4 : (R_), QSA_DECODE_STAGES_RN, false, 128)
 #define QSA_V256(R_, W_) X(1, R_, W_, QSA_DECODE_STAGES_RN, false, 256)

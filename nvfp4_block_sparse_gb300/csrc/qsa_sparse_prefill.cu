@@ -43,9 +43,9 @@ namespace qsa {
 namespace {
 
 // Bounds-check codes (reported by bounds-checked builds only).
-constexpr int kChkUnion = 0x701;   // union slot past its capacity
-constexpr int kChkChunk = 0x702;   // chunk: union slot or page id out of range
-constexpr int kChkOut = 0x703;     // output row out of range
+[[maybe_unused]] constexpr int kChkUnion = 0x701;   // union slot past its capacity
+[[maybe_unused]] constexpr int kChkChunk = 0x702;   // chunk: union slot or page id out of range
+[[maybe_unused]] constexpr int kChkOut = 0x703;     // output row out of range
 constexpr int kThreads = 128;           // four warps: one thread per tile row
 constexpr int kStage = 9216;            // NVFP4 bytes of one chunk (8192 K and V values)
 

@@ -30,7 +30,7 @@ namespace {
 
 constexpr int kWarpsPerCta = 8;
 // Bounds-check code (reported by bounds-checked builds only): pool row out of range.
-constexpr int kChkRow = 0x501;
+[[maybe_unused]] constexpr int kChkRow = 0x501;
 
 __device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi) {
   uint32_t r;
