@@ -43,6 +43,23 @@ __device__ __forceinline__ int4 ld_stream_v4(const int4* p) {
 
 // RB: compile-time bound on rows per request (R <= RB).  PIPE: a warp owns
 // several blocks and loads the next block's keys while scoring the current.
+// A CTA none of whose blocks holds a token visible to its rows writes the
+// sentinel for all of them and leaves before the head sums (the blocks past
+// the shortest contexts of a batch are most of a wide grid).  Returns true
+// when the CTA is done.  Rows r0 .. r0 + nrows - 1 of request b.
+__device__ __forceinline__ bool only_invisible_blocks(const Geom& g, int P, int b, int r0,
+                                                      int nrows, int nmax, int blocks_per_warp,
+                                                      int32_t* scores) {
+  const int beta0 = blockIdx.x * blocks_per_warp * kWarps;
+  if (beta0 * P < nmax) return false;
+  const int nb = min(blocks_per_warp * kWarps, g.MB - beta0);
+  for (int i = threadIdx.x; i < nrows * nb; i += kThreads) {
+    const int j = i / nb, beta = beta0 + i % nb;
+    scores[((size_t)b * g.R + r0 + j) * g.MB + beta] = kSentinel;
+  }
+  return true;
+}
+
 template <int P, int RB, bool PIPE>
 __global__ void __launch_bounds__(kThreads)
 index_scores_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __restrict__ ik_pool,
@@ -61,6 +78,7 @@ index_scores_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __restr
   const int L = seqlens[b];
   const int cap = g.MB * P;
   const int nmax = visible_tokens(L, R, R - 1, cap);
+  if (only_invisible_blocks(g, P, b, 0, R, nmax, blocks_per_warp, scores)) return;
 
   // Block `it` of this warp: page id and whether it has a visible token.
   auto block_of = [&](int it, int& beta, int& page) -> bool {
@@ -228,7 +246,7 @@ __device__ __forceinline__ void s8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32
 }
 
 template <int P, bool PIPE>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, (P == 128 && PIPE) ? 1 : 2)
 index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __restrict__ ik_pool,
                         const int32_t* __restrict__ page_table,
                         const int32_t* __restrict__ seqlens, int32_t* __restrict__ scores,
@@ -249,6 +267,8 @@ index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __r
   const int L = seqlens[b];
   const int cap = g.MB * P;
   const int nmax = visible_tokens(L, R, min(R - 1, r0 + RB - 1), cap);
+  if (only_invisible_blocks(g, P, b, r0, min(RB, R - r0), nmax, blocks_per_warp, scores))
+    return;
 
   auto block_of = [&](int it, int& beta, int& page) -> bool {
     beta = (blockIdx.x * blocks_per_warp + it) * kWarps + warp;
@@ -431,6 +451,8 @@ index_scores_rows_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __
   const int L = seqlens[b];
   const int cap = g.MB * P;
   const int nmax = visible_tokens(L, R, min(R - 1, r0 + kGroupRows - 1), cap);
+  if (only_invisible_blocks(g, P, b, r0, min(kGroupRows, R - r0), nmax, blocks_per_warp, scores))
+    return;
 
   auto block_of = [&](int it, int& beta, int& page) -> bool {
     beta = (blockIdx.x * blocks_per_warp + it) * kWarps + warp;
