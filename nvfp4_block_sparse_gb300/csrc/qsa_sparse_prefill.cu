@@ -208,6 +208,10 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t s2) {
                     hmul2_u32(o[3], s2));
 }
 
+__device__ __forceinline__ void ws_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // Lower bound of beta in an ascending selection row padded with -1 (+inf).
 __device__ __forceinline__ bool row_holds(const int32_t* row, int k, int beta) {
   int lo = 0, hi = k;
@@ -665,6 +669,517 @@ sparse_prefill_kernel(Params p) {
                  "r"(T::kTmemCols));
 }
 
+// ---------------------------------------------------------------------------
+// Warp-specialised row tiles.  Nine warps: warps 0-3 own the tile's 128
+// tensor-memory lanes (queries, softmax, epilogue), warps 4-7 dequantise the
+// NVFP4 chunks into double-buffered fp16 K and V^T tiles, and one thread of
+// warp 8 issues the bulk copies and the MMAs.  S is double-buffered in tensor
+// memory and P in shared memory, so for chunk c the softmax of c, the
+// dequantisation of c + 1 and the MMAs S(c + 1) and O(c - 1) overlap.
+// Hand-overs are mbarriers (all waits bounded):
+//   full[x]   copy of a chunk into stage x landed       (1 arrival + bytes)
+//   empty[x]  the dequant warps are done with stage x    (4 arrivals)
+//   kready[x] K tile x written                           (128 arrivals)
+//   vready[x] V^T tile x written                         (128 arrivals)
+//   pready[x] P tile x written, O rescaled, S buffer x read (128 arrivals)
+//   barS[x]   S into tensor-memory buffer x complete     (commit)
+//   barO[x]   O += P(x) V(x) complete                    (commit)
+// Chunk c uses buffer x = c & 1; its phase on a buffer's barrier is c >> 1.
+constexpr int kWsThreads = 288;
+
+template <int D>
+struct WT {
+  using T = PT<D>;
+  static constexpr int kSCols = T::kTok;
+  static constexpr uint32_t kOCol = D == 128 ? 128 : 256;
+  static constexpr uint32_t kTmemCols = D == 128 ? 256 : 512;
+  static constexpr size_t kTiles = (size_t)T::kQBytes + 2 * ((size_t)T::kKBytes + T::kVBytes + T::kPBytes);
+};
+
+template <int D>
+__global__ void __launch_bounds__(kWsThreads, 1)
+sparse_prefill_ws_kernel(Params p) {
+  using T = PT<D>;
+  using W = WT<D>;
+  constexpr int kTok = T::kTok;
+  const Geom& g = p.g;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = g.Hq / g.Hkv;
+  const int TR = p.tr;
+  const int tile = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int r0 = tile * TR;                   // first row of the tile
+  const int rows = min(TR, g.R - r0);
+  const int k = p.k;
+  const bool soft = warp < 4, deq = warp >= 4 && warp < 8, iss = tid == 256;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK0 = sQ + T::kQBytes;                       // [2][kKBytes]
+  uint8_t* sV0 = sK0 + 2 * T::kKBytes;                  // [2][kVBytes]
+  uint8_t* sP0 = sV0 + 2 * T::kVBytes;                  // [2][kPBytes]
+  uint8_t* sStage = sP0 + 2 * T::kPBytes;               // [2][kStage]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + 2 * kStage);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + 2;
+  uint64_t* kready = bars + 4;
+  uint64_t* vready = bars + 6;
+  uint64_t* pready = bars + 8;
+  uint64_t* barS = bars + 10;
+  uint64_t* barO = bars + 12;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 14);
+  int* s_misc = reinterpret_cast<int*>(s_tmem + 1);            // [8]
+  int32_t* s_sel = s_misc + 8;                                  // [TR][k]
+  int32_t* s_union = s_sel + TR * k;                            // [ucap]
+  int32_t* s_upage = s_union + p.ucap;                          // [ucap]
+  uint32_t* s_bits = reinterpret_cast<uint32_t*>(s_upage + p.ucap);   // [ceil(MB/32)]
+  const int nwords = (g.MB + 31) >> 5;
+
+  if (tid == 0) {
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&full[x], 1);
+      mbar_init(&empty[x], 4);
+      mbar_init(&kready[x], 128);
+      mbar_init(&vready[x], 128);
+      mbar_init(&pready[x], 128);
+      mbar_init(&barS[x], 1);
+      mbar_init(&barO[x], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(s_tmem)),
+                 "r"(W::kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+
+  // ---- the softmax warps' query vectors into the swizzled Q tile -------------
+  const int jj = tid / G, hh = tid % G;
+  const bool vec = soft && jj < rows;           // a real (row, head) vector
+  const int j = r0 + jj;
+  const int L = p.seqlens[b];
+  const int cap = g.MB * g.P;
+  const int nrow = vec ? visible_tokens(L, g.R, j, cap) : 0;
+  float cq = 0.f;                               // logit scale, log2 domain
+  if (soft) {
+    const size_t qrow = ((size_t)b * g.R + j) * g.Hq + (size_t)kvh * G + hh;
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow * D);
+    float amax = 0.f;
+    if (vec) {
+#pragma unroll 4
+      for (int i = 0; i < D / 8; ++i) {
+        const uint4 r = src[i];
+        const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          amax = fmaxf(amax, fabsf(__uint_as_float(w4[u] << 16)));
+          amax = fmaxf(amax, fabsf(__uint_as_float(w4[u] & 0xFFFF0000u)));
+        }
+      }
+    }
+    const int ebits = (int)((__float_as_uint(amax) >> 23) & 0xFF);
+    int sq = (amax > 0.f) ? 135 - ebits : 0;
+    sq = sq > 126 ? 126 : (sq < -126 ? -126 : sq);
+    const float up = __uint_as_float((uint32_t)(sq + 127) << 23);
+    const float down = __uint_as_float((uint32_t)(127 - sq) << 23);
+    cq = p.k_scale * p.sm_scale * kLog2e * down;
+#pragma unroll 4
+    for (int i = 0; i < D / 8; ++i) {
+      uint4 h = make_uint4(0u, 0u, 0u, 0u);
+      if (vec) {
+        const uint4 r = src[i];
+        const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          o[u] = pack_half2(__uint_as_float(w4[u] << 16) * up,
+                            __uint_as_float(w4[u] & 0xFFFF0000u) * up);
+        h = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      *reinterpret_cast<uint4*>(sQ + (i >> 3) * 16384 + sw128(tid, i & 7)) = h;
+    }
+  }
+  // Token slots past a chunk (D = 256: 32 of the 64 slots of every V^T and P
+  // tile) stay zero: cleared once here, never written.
+  if (kTok < 64) {
+    for (int i = tid; i < 2 * (T::kVBytes + T::kPBytes) / 16; i += kWsThreads)
+      reinterpret_cast<uint4*>(sV0)[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+
+  // ---- the tile's rows' selections and their union (softmax warps) ------------
+  if (soft) {
+    auto soft_sync = [] { asm volatile("bar.sync 1, 128;" ::: "memory"); };
+    for (int i = tid; i < TR * k; i += 128) {
+      const int jr = i / k;
+      int v = -1;
+      if (jr < rows) {
+        v = p.sel[((size_t)b * g.R + r0 + jr) * k + (i - jr * k)];
+        if (v < 0 || v >= g.MB) v = -1;
+      }
+      s_sel[i] = v;
+    }
+    for (int i = tid; i < nwords; i += 128) s_bits[i] = 0u;
+    soft_sync();
+    for (int i = tid; i < rows * k; i += 128) {
+      const int v = s_sel[i];
+      if (v >= 0) atomicOr(&s_bits[v >> 5], 1u << (v & 31));
+    }
+    soft_sync();
+    // Blocks with a valid page, ascending: thread t scans words [t*per, ...).
+    const int per = (nwords + 127) / 128;
+    const int w0 = min(nwords, tid * per), w1 = min(nwords, w0 + per);
+    const int32_t* pt = p.page_table + (size_t)b * g.MB;
+    int cnt = 0;
+    for (int w = w0; w < w1; ++w) {
+      uint32_t m = s_bits[w];
+      while (m) {
+        const int beta = (w << 5) + __ffs(m) - 1;
+        m &= m - 1;
+        const int pg = pt[beta];
+        if (pg >= 0 && pg < g.NP) ++cnt; else s_bits[w] &= ~(1u << (beta & 31));
+      }
+    }
+    int x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_misc[warp] = x;
+    soft_sync();
+    int pos = x - cnt;
+    for (int w = 0; w < warp; ++w) pos += s_misc[w];
+    for (int w = w0; w < w1; ++w) {
+      uint32_t m = s_bits[w];
+      while (m) {
+        const int beta = (w << 5) + __ffs(m) - 1;
+        m &= m - 1;
+        if (QSA_IN_BOUNDS(pos < p.ucap, kChkUnion)) {
+          s_union[pos] = beta;
+          s_upage[pos] = pt[beta];
+        }
+        ++pos;
+      }
+    }
+    if (tid == 127) s_misc[4] = pos;
+  }
+  fence_proxy_async_smem();       // Q and zero tiles (generic stores) before the MMAs
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const int U = s_misc[4];
+  const int csh = (g.P == 2 * kTok) ? 1 : 0;    // chunks per block: 1 << csh
+  const int C = U << csh;
+  const int32_t* myrow = s_sel + (soft ? jj : 0) * k;
+  const uint32_t tO = tmem + W::kOCol;
+  auto tS = [&](int x) { return tmem + (uint32_t)(x * W::kSCols); };
+  auto sK = [&](int x) { return sK0 + x * T::kKBytes; };
+  auto sV = [&](int x) { return sV0 + x * T::kVBytes; };
+  auto sP = [&](int x) { return sP0 + x * T::kPBytes; };
+  bool dead = false;
+
+  // ---- copy and MMA issue (one thread of warp 8) -------------------------------
+  // S(c) once K(c) is dequantised and softmax(c - 2) has read S buffer c & 1;
+  // O(c - 1) once P(c - 1) and V(c - 1) are ready; stage c & 1 is refilled
+  // with chunk c + 2 once the dequantisation warps are done with chunk c.
+  if (iss) {
+    const uint64_t pol = policy_evict_first();
+    auto issue_copy = [&](int c) {
+      uint8_t* dst = sStage + (c & 1) * kStage;
+      const int u = c >> csh, sub = c & csh;
+      if (!QSA_IN_BOUNDS(u < U && u < p.ucap && s_upage[u] >= 0 && s_upage[u] < g.NP,
+                         kChkChunk))
+        return;
+      const size_t row0 = ((size_t)s_upage[u] * g.Hkv + kvh) * g.P + (size_t)sub * kTok;
+      mbar_arrive_expect_tx(&full[c & 1], kStage);
+      bulk_g2s(dst, p.k_pool + row0 * (D / 2), kTok * D / 2, &full[c & 1], pol);
+      bulk_g2s(dst + kTok * D / 2, p.v_pool + row0 * (D / 2), kTok * D / 2, &full[c & 1], pol);
+      bulk_g2s(dst + kTok * D, p.k_sf + row0 * (D / 16), kTok * D / 16, &full[c & 1], pol);
+      bulk_g2s(dst + kTok * D + kTok * D / 16, p.v_sf + row0 * (D / 16), kTok * D / 16,
+               &full[c & 1], pol);
+    };
+    auto issue_s = [&](int c) {
+      const int x = c & 1;
+      const uint32_t id = f16_idesc(128, kTok);
+#pragma unroll
+      for (int h = 0; h < D / 64; ++h)
+#pragma unroll
+        for (int ks2 = 0; ks2 < 4; ++ks2)
+          mma_f16(tS(x), sw128_desc(smem_u32(sQ + h * 16384) + 32 * ks2),
+                  sw128_desc(smem_u32(sK(x) + h * T::kKBlk) + 32 * ks2), id,
+                  (h | ks2) ? 1u : 0u);
+      mma_commit(&barS[x]);
+    };
+    auto issue_o = [&](int c) {
+      const int x = c & 1;
+      const uint32_t id = f16_idesc(128, D);
+#pragma unroll
+      for (int ks2 = 0; ks2 < 4; ++ks2)
+        mma_f16(tO, sw128_desc(smem_u32(sP(x)) + 32 * ks2),
+                sw128_desc(smem_u32(sV(x)) + 32 * ks2), id, (c | ks2) ? 1u : 0u);
+      mma_commit(&barO[x]);
+    };
+    int ncopy = min(C, 2), ns = 0, no = 0;
+    for (int c = 0; c < ncopy; ++c) issue_copy(c);
+    for (int c = 0; c <= C; ++c) {
+      if (c < C) {
+        if (!wait_bounded(&kready[c & 1], (c >> 1) & 1) ||
+            (c >= 2 && !wait_bounded(&pready[c & 1], ((c - 2) >> 1) & 1))) {
+          dead = true;
+          break;
+        }
+        tc_fence_after();
+        issue_s(c);
+        ns = c + 1;
+      }
+      if (c >= 1) {
+        const int o = c - 1;
+        if (!wait_bounded(&pready[o & 1], (o >> 1) & 1) ||
+            !wait_bounded(&vready[o & 1], (o >> 1) & 1)) {
+          dead = true;
+          break;
+        }
+        tc_fence_after();
+        issue_o(o);
+        no = o + 1;
+      }
+      if (c + 2 < C) {
+        if (!wait_bounded(&empty[c & 1], (c >> 1) & 1)) {
+          dead = true;
+          break;
+        }
+        fence_proxy_async_smem();   // the dequant warps' reads of the stage come first
+        issue_copy(c + 2);
+        ncopy = c + 3;
+      }
+    }
+    // Every copy and MMA this thread issued completes before the tiles and
+    // tensor memory are read or released (at once when nothing went wrong).
+    for (int c = max(0, ncopy - 2); c < ncopy; ++c) wait_bounded(&full[c & 1], (c >> 1) & 1);
+    for (int c = max(0, ns - 2); c < ns; ++c) wait_bounded(&barS[c & 1], (c >> 1) & 1);
+    for (int c = max(0, no - 2); c < no; ++c) wait_bounded(&barO[c & 1], (c >> 1) & 1);
+  }
+
+  // ---- dequantisation (warps 4-7) ----------------------------------------------
+  if (deq) {
+    const int dt = tid - 128, dw = warp - 4;
+    for (int c = 0; c < C; ++c) {
+      const int x = c & 1;
+      const uint8_t* st = sStage + x * kStage;
+      // Warp-uniform give-ups (the warp syncs below).
+      if (__any_sync(0xffffffffu, !wait_bounded(&full[x], (c >> 1) & 1) ||
+                                      (c >= 2 && !wait_bounded(&barS[x], ((c - 2) >> 1) & 1)))) {
+        dead = true;   // (barS: S(c - 2) has read K tile x)
+        break;
+      }
+      {
+        // K rows = tokens (D/64 blocks of 64 dims), 8 pieces per thread.
+        const uint8_t* kc = st;
+        const uint8_t* ks = st + kTok * D;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int pc = dt + 128 * i;      // (token, 8-dim group)
+          const int t = pc / (D / 8), c8 = pc % (D / 8);
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(kc + t * (D / 2) + c8 * 4);
+          const uint32_t s = e4m3x2_to_f16x2(ks[t * (D / 16) + (c8 >> 1)]);
+          *reinterpret_cast<uint4*>(sK(x) + (c8 >> 3) * T::kKBlk + sw128(t, c8 & 7)) =
+              dequant8(w, prmt(s, 0, 0x1010));
+        }
+      }
+      fence_proxy_async_smem();
+      ws_arrive(&kready[x]);
+      if (c >= 2 &&
+          __any_sync(0xffffffffu, !wait_bounded(&barO[x], ((c - 2) >> 1) & 1))) {
+        dead = true;   // (O(c - 2) has read V^T tile x)
+        break;
+      }
+      {
+        // V^T: 8 tokens x 8 dims per thread (the layout of the one-group kernel).
+        const uint8_t* vc = st + kTok * D / 2;
+        const uint8_t* vs = st + kTok * D + kTok * D / 16;
+        const int hw = D == 128 ? lane >> 4 : 0;
+        const int c8 = D == 128 ? lane & 15 : 8 * dw + (lane & 7);
+        const int tg = D == 128 ? 2 * dw + hw : lane >> 3;
+        uint32_t X[8], sf[8];   // X[u]: token 8*tg + (u ^ hw)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int t = 8 * tg + (u ^ hw);
+          X[u] = *reinterpret_cast<const uint32_t*>(vc + t * (D / 2) + c8 * 4);
+          sf[u] = vs[t * (D / 16) + (c8 >> 1)];
+        }
+        uint32_t rowv[8][4];   // [dim e][token pair]
+#pragma unroll
+        for (int pr = 0; pr < 4; ++pr) {
+          const uint32_t x0 = hw ? X[2 * pr + 1] : X[2 * pr];
+          const uint32_t x1 = hw ? X[2 * pr] : X[2 * pr + 1];
+          const uint32_t f0 = hw ? sf[2 * pr + 1] : sf[2 * pr];
+          const uint32_t f1 = hw ? sf[2 * pr] : sf[2 * pr + 1];
+          const uint32_t s2 = e4m3x2_to_f16x2(f0 | (f1 << 8));
+          const uint32_t LO = (x0 & 0x0F0F0F0Fu) | ((x1 << 4) & 0xF0F0F0F0u);
+          const uint32_t HI = ((x0 >> 4) & 0x0F0F0F0Fu) | (x1 & 0xF0F0F0F0u);
+          const uint4 el = dequant8(LO, s2), od = dequant8(HI, s2);
+          rowv[0][pr] = el.x; rowv[2][pr] = el.y; rowv[4][pr] = el.z; rowv[6][pr] = el.w;
+          rowv[1][pr] = od.x; rowv[3][pr] = od.y; rowv[5][pr] = od.z; rowv[7][pr] = od.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          *reinterpret_cast<uint4*>(sV(x) + sw128(8 * c8 + e, tg)) =
+              make_uint4(rowv[e][0], rowv[e][1], rowv[e][2], rowv[e][3]);
+      }
+      fence_proxy_async_smem();
+      ws_arrive(&vready[x]);
+      __syncwarp();
+      if (lane == 0) ws_arrive(&empty[x]);   // this warp is done with the stage
+    }
+  }
+
+  // ---- softmax (warps 0-3: thread = query vector = tensor-memory lane) ---------
+  float m_base = -INFINITY, l_run = 0.f;
+  const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+  if (soft) {
+    for (int c = 0; c < C; ++c) {
+      const int x = c & 1;
+      // Warp-uniform give-up: tensor-memory loads and stores are warp-wide.
+      if (__any_sync(0xffffffffu, !wait_bounded(&barS[x], (c >> 1) & 1))) {
+        dead = true;
+        break;
+      }
+      tc_fence_after();
+      const int ue = s_union[c >> csh];
+      const int tok0 = ue * g.P + (c & csh) * kTok;
+      const bool member = vec && tok0 < nrow && row_holds(myrow, k, ue);
+      float z[kTok];
+#pragma unroll
+      for (int q4 = 0; q4 < kTok / 16; ++q4) {
+        float v16[16];
+        tmem_ld16(tS(x) + lane_off + 16 * q4, v16);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) z[16 * q4 + i] = v16[i];
+      }
+      tmem_wait_ld();
+      float cmax = -INFINITY;   // log2 units
+      if (member) {
+        if (tok0 + kTok > nrow) {
+#pragma unroll
+          for (int i = 0; i < kTok; ++i)
+            if (tok0 + i >= nrow) z[i] = -INFINITY;
+        }
+        float mx8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = z[i];
+#pragma unroll
+        for (int i = 8; i < kTok; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], z[i]);
+#pragma unroll
+        for (int h = 4; h >= 1; h >>= 1)
+#pragma unroll
+          for (int i = 0; i < h; ++i) mx8[i] = fmaxf(mx8[i], mx8[i + h]);
+        cmax = mx8[0] * cq;     // cq > 0: the scale keeps the order
+      }
+      bool rescale = false;
+      float alpha = 1.f;
+      if (cmax != -INFINITY) {
+        if (m_base == -INFINITY) {
+          m_base = cmax;
+        } else if (cmax > m_base + kRescaleGap) {
+          alpha = exp2_approx(m_base - cmax);
+          m_base = cmax;
+          rescale = true;
+        }
+      }
+      uint32_t pk[kTok / 2];
+      if (member) {
+        float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < kTok / 2; ++i) {
+          const float p0 = exp2_approx(fmaf(z[2 * i], cq, -m_base));
+          const float p1 = exp2_approx(fmaf(z[2 * i + 1], cq, -m_base));
+          ls4[i & 3] += p0 + p1;
+          pk[i] = pack_half2(p0, p1);
+        }
+        l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < kTok / 2; ++i) pk[i] = 0u;
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+        // O holds every chunk before c once O(c - 1) completed (O(c) waits for
+        // this chunk's P); a warp rescales when any of its lanes must.
+        if (c >= 1 &&
+            __any_sync(0xffffffffu, !wait_bounded(&barO[(c - 1) & 1], ((c - 1) >> 1) & 1))) {
+          dead = true;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int q8 = 0; q8 < D / 16; ++q8) {
+          float o16[16];
+          tmem_ld16(tO + lane_off + 16 * q8, o16);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o16[i] *= alpha;
+          tmem_st16(tO + lane_off + 16 * q8, o16);
+        }
+        tmem_wait_st();
+      }
+      // P tile x is free once O(c - 2) completed.
+      if (c >= 2 &&
+          __any_sync(0xffffffffu, !wait_bounded(&barO[x], ((c - 2) >> 1) & 1))) {
+        dead = true;
+        break;
+      }
+#pragma unroll
+      for (int c16 = 0; c16 < kTok / 8; ++c16)
+        *reinterpret_cast<uint4*>(sP(x) + sw128(tid, c16)) =
+            make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      ws_arrive(&pready[x]);   // P(c) written, O rescaled, S buffer x read
+    }
+  }
+
+  // ---- epilogue: out = O / l * v_scale, lse -------------------------------------
+  // The issuer has seen its last O complete; the barrier publishes that.
+  if (dead) atomicExch(p.status, kStatusWaitTimeout);
+  tc_fence_before();
+  const bool any_dead = __syncthreads_or(dead);
+  tc_fence_after();
+  if (soft && !any_dead) {
+    const size_t orow = ((size_t)b * g.R + j) * g.Hq + (size_t)kvh * G + hh;
+    const bool out_ok = !vec || QSA_IN_BOUNDS(b < g.B && j < g.R && kvh * G + hh < g.Hq, kChkOut);
+    uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D);
+    const bool has = l_run > 0.f && C > 0;
+    const float sc = has ? p.v_scale / l_run : 0.f;
+#pragma unroll 4
+    for (int q8 = 0; q8 < D / 16; ++q8) {
+      float o16[16];
+      if (C > 0) {
+        tmem_ld16(tO + lane_off + 16 * q8, o16);
+        tmem_wait_ld();
+      }
+      uint32_t h[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        __nv_bfloat162 x2 = __floats2bfloat162_rn(has ? o16[2 * i] * sc : 0.f,
+                                                  has ? o16[2 * i + 1] * sc : 0.f);
+        h[i] = *reinterpret_cast<uint32_t*>(&x2);
+      }
+      if (vec && out_ok) {
+        dst[2 * q8] = make_uint4(h[0], h[1], h[2], h[3]);
+        dst[2 * q8 + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+      }
+    }
+    if (vec && out_ok) p.lse[orow] = has ? (m_base + log2f(l_run)) * kLn2 : -INFINITY;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(W::kTmemCols));
+}
+
 }  // namespace
 
 int prefill_rows_per_tile(const Geom& g) {
@@ -680,6 +1195,16 @@ size_t prefill_smem_bytes(const Geom& g, int k) {
                            : (size_t)PT<128>::kQBytes + PT<128>::kKBytes + PT<128>::kVBytes + PT<128>::kPBytes;
   return (size_t)1024 + tiles + 2 * kStage + 4 * 8 + 4 + 8 * 4 +
          (size_t)tr * k * 4 + (size_t)ucap * 8 + (size_t)((g.MB + 31) / 32) * 4;
+}
+
+// The warp-specialised kernel's shared memory (double-buffered tiles); the
+// four-warp kernel (single tiles) serves geometries where it does not fit.
+size_t prefill_ws_smem_bytes(const Geom& g, int k) {
+  const int tr = prefill_rows_per_tile(g);
+  const int ucap = min(g.MB, tr * k);
+  const size_t tiles = g.D == 256 ? WT<256>::kTiles : WT<128>::kTiles;
+  return (size_t)1024 + tiles + 2 * kStage + 14 * 8 + 4 + 8 * 4 + (size_t)tr * k * 4 +
+         (size_t)ucap * 8 + (size_t)((g.MB + 31) / 32) * 4;
 }
 
 cudaError_t launch_sparse_prefill(const Geom& g, const void* q, const uint8_t* k_pool,
@@ -699,14 +1224,20 @@ cudaError_t launch_sparse_prefill(const Geom& g, const void* q, const uint8_t* k
   prm.out = reinterpret_cast<__nv_bfloat16*>(out);
   prm.lse = lse;
   prm.status = status;
-  const size_t smem = prefill_smem_bytes(g, k);
-  auto* kern = g.D == 256 ? sparse_prefill_kernel<256> : sparse_prefill_kernel<128>;
+#ifdef QSA_PREFILL_FOUR_WARPS
+  const bool ws = false;
+#else
+  const bool ws = prefill_ws_smem_bytes(g, k) <= 227 * 1024;
+#endif
+  const size_t smem = ws ? prefill_ws_smem_bytes(g, k) : prefill_smem_bytes(g, k);
+  auto* kern = ws ? (g.D == 256 ? sparse_prefill_ws_kernel<256> : sparse_prefill_ws_kernel<128>)
+                  : (g.D == 256 ? sparse_prefill_kernel<256> : sparse_prefill_kernel<128>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((g.R + prm.tr - 1) / prm.tr, g.Hkv, g.B);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(ws ? kWsThreads : kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
