@@ -997,12 +997,16 @@ sparse_prefill_ws_kernel(Params p) {
         break;
       }
       {
-        // V^T: 8 tokens x 8 dims per thread (the layout of the one-group kernel).
+        // V^T: 8 tokens x 8 dims per thread.  The eight lanes of each store
+        // phase take eight different token groups (the 16-byte chunk of the
+        // swizzled row), so the V^T stores are conflict-free; lanes of odd
+        // token groups read their token pairs in swapped order, which halves
+        // the read conflicts (token rows share banks every 128 bytes).
         const uint8_t* vc = st + kTok * D / 2;
         const uint8_t* vs = st + kTok * D + kTok * D / 16;
-        const int hw = D == 128 ? lane >> 4 : 0;
-        const int c8 = D == 128 ? lane & 15 : 8 * dw + (lane & 7);
-        const int tg = D == 128 ? 2 * dw + hw : lane >> 3;
+        const int tg = D == 128 ? lane & 7 : lane & 3;
+        const int c8 = D == 128 ? (lane >> 3) + 4 * dw : (lane >> 2) + 8 * dw;
+        const int hw = D == 128 ? tg & 1 : 0;
         uint32_t X[8], sf[8];   // X[u]: token 8*tg + (u ^ hw)
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
