@@ -685,41 +685,50 @@ sparse_prefill_kernel(Params p) {
 //   barS[x]   S into tensor-memory buffer x complete     (commit)
 //   barO[x]   O += P(x) V(x) complete                    (commit)
 // Chunk c uses buffer x = c & 1; its phase on a buffer's barrier is c >> 1.
-constexpr int kWsThreads = 288;
-
+// At head_dim 128 a CTA holds two query tiles (NTL = 2: eight softmax warps,
+// 2 x TR consecutive rows) that share every dequantised chunk of the union of
+// their rows' selections; at head_dim 256 one (two Q tiles would not fit).
 template <int D>
 struct WT {
   using T = PT<D>;
+  static constexpr int kNtl = D == 128 ? 2 : 1;       // query tiles per CTA
+  static constexpr int kThreads = 128 * kNtl + 160;   // softmax, dequant, issuer
   static constexpr int kSCols = T::kTok;
-  static constexpr uint32_t kOCol = D == 128 ? 128 : 256;
-  static constexpr uint32_t kTmemCols = D == 128 ? 256 : 512;
-  static constexpr size_t kTiles = (size_t)T::kQBytes + 2 * ((size_t)T::kKBytes + T::kVBytes + T::kPBytes);
+  static constexpr uint32_t kOBase = 256;             // O of tile t at kOBase + t * D
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr size_t kTiles =
+      (size_t)kNtl * T::kQBytes + 2 * ((size_t)T::kKBytes + T::kVBytes + (size_t)kNtl * T::kPBytes);
 };
 
 template <int D>
-__global__ void __launch_bounds__(kWsThreads, 1)
+__global__ void __launch_bounds__(WT<D>::kThreads, 1)
 sparse_prefill_ws_kernel(Params p) {
   using T = PT<D>;
   using W = WT<D>;
+  constexpr int NTL = W::kNtl;
+  constexpr int kWsThreads = W::kThreads;
   constexpr int kTok = T::kTok;
   const Geom& g = p.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = g.Hq / g.Hkv;
   const int TR = p.tr;
   const int tile = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-  const int r0 = tile * TR;                   // first row of the tile
-  const int rows = min(TR, g.R - r0);
+  const int r0 = tile * NTL * TR;             // first row of the CTA's tiles
+  const int rows = min(NTL * TR, g.R - r0);   // rows of the CTA
   const int k = p.k;
-  const bool soft = warp < 4, deq = warp >= 4 && warp < 8, iss = tid == 256;
+  const bool soft = warp < 4 * NTL, deq = warp >= 4 * NTL && warp < 4 * NTL + 4;
+  const bool iss = tid == 128 * NTL + 128;
+  const int tt = soft ? warp >> 2 : 0;        // a softmax thread's tile
+  const int vi = tid & 127;                   // its query vector (tile row)
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sK0 = sQ + T::kQBytes;                       // [2][kKBytes]
+  uint8_t* sQ0 = smem;                                  // [NTL][kQBytes]
+  uint8_t* sK0 = sQ0 + NTL * T::kQBytes;                // [2][kKBytes]
   uint8_t* sV0 = sK0 + 2 * T::kKBytes;                  // [2][kVBytes]
   uint8_t* sP0 = sV0 + 2 * T::kVBytes;                  // [2][kPBytes]
-  uint8_t* sStage = sP0 + 2 * T::kPBytes;               // [2][kStage]
+  uint8_t* sStage = sP0 + 2 * NTL * T::kPBytes;         // [2][kStage]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + 2 * kStage);
   uint64_t* full = bars;
   uint64_t* empty = bars + 2;
@@ -730,8 +739,8 @@ sparse_prefill_ws_kernel(Params p) {
   uint64_t* barO = bars + 12;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 14);
   int* s_misc = reinterpret_cast<int*>(s_tmem + 1);            // [8]
-  int32_t* s_sel = s_misc + 8;                                  // [TR][k]
-  int32_t* s_union = s_sel + TR * k;                            // [ucap]
+  int32_t* s_sel = s_misc + 8;                                  // [NTL * TR][k]
+  int32_t* s_union = s_sel + NTL * TR * k;                      // [ucap]
   int32_t* s_upage = s_union + p.ucap;                          // [ucap]
   uint32_t* s_bits = reinterpret_cast<uint32_t*>(s_upage + p.ucap);   // [ceil(MB/32)]
   const int nwords = (g.MB + 31) >> 5;
@@ -742,7 +751,7 @@ sparse_prefill_ws_kernel(Params p) {
       mbar_init(&empty[x], 4);
       mbar_init(&kready[x], 128);
       mbar_init(&vready[x], 128);
-      mbar_init(&pready[x], 128);
+      mbar_init(&pready[x], 128 * NTL);
       mbar_init(&barS[x], 1);
       mbar_init(&barO[x], 1);
     }
@@ -755,9 +764,9 @@ sparse_prefill_ws_kernel(Params p) {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
 
-  // ---- the softmax warps' query vectors into the swizzled Q tile -------------
-  const int jj = tid / G, hh = tid % G;
-  const bool vec = soft && jj < rows;           // a real (row, head) vector
+  // ---- the softmax warps' query vectors into the swizzled Q tiles ------------
+  const int jj = tt * TR + vi / G, hh = vi % G; // row of the CTA, head
+  const bool vec = soft && vi / G < TR && jj < rows;   // a real (row, head) vector
   const int j = r0 + jj;
   const int L = p.seqlens[b];
   const int cap = g.MB * g.P;
@@ -798,20 +807,20 @@ sparse_prefill_ws_kernel(Params p) {
                             __uint_as_float(w4[u] & 0xFFFF0000u) * up);
         h = make_uint4(o[0], o[1], o[2], o[3]);
       }
-      *reinterpret_cast<uint4*>(sQ + (i >> 3) * 16384 + sw128(tid, i & 7)) = h;
+      *reinterpret_cast<uint4*>(sQ0 + tt * T::kQBytes + (i >> 3) * 16384 + sw128(vi, i & 7)) = h;
     }
   }
   // Token slots past a chunk (D = 256: 32 of the 64 slots of every V^T and P
   // tile) stay zero: cleared once here, never written.
   if (kTok < 64) {
-    for (int i = tid; i < 2 * (T::kVBytes + T::kPBytes) / 16; i += kWsThreads)
+    for (int i = tid; i < (2 * T::kVBytes + 2 * NTL * T::kPBytes) / 16; i += kWsThreads)
       reinterpret_cast<uint4*>(sV0)[i] = make_uint4(0u, 0u, 0u, 0u);
   }
 
   // ---- the tile's rows' selections and their union (softmax warps) ------------
   if (soft) {
-    auto soft_sync = [] { asm volatile("bar.sync 1, 128;" ::: "memory"); };
-    for (int i = tid; i < TR * k; i += 128) {
+    auto soft_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(128 * NTL) : "memory"); };
+    for (int i = tid; i < NTL * TR * k; i += 128 * NTL) {
       const int jr = i / k;
       int v = -1;
       if (jr < rows) {
@@ -820,15 +829,15 @@ sparse_prefill_ws_kernel(Params p) {
       }
       s_sel[i] = v;
     }
-    for (int i = tid; i < nwords; i += 128) s_bits[i] = 0u;
+    for (int i = tid; i < nwords; i += 128 * NTL) s_bits[i] = 0u;
     soft_sync();
-    for (int i = tid; i < rows * k; i += 128) {
+    for (int i = tid; i < rows * k; i += 128 * NTL) {
       const int v = s_sel[i];
       if (v >= 0) atomicOr(&s_bits[v >> 5], 1u << (v & 31));
     }
     soft_sync();
     // Blocks with a valid page, ascending: thread t scans words [t*per, ...).
-    const int per = (nwords + 127) / 128;
+    const int per = (nwords + 128 * NTL - 1) / (128 * NTL);
     const int w0 = min(nwords, tid * per), w1 = min(nwords, w0 + per);
     const int32_t* pt = p.page_table + (size_t)b * g.MB;
     int cnt = 0;
@@ -863,7 +872,7 @@ sparse_prefill_ws_kernel(Params p) {
         ++pos;
       }
     }
-    if (tid == 127) s_misc[4] = pos;
+    if (tid == 128 * NTL - 1) s_misc[4] = pos;
   }
   fence_proxy_async_smem();       // Q and zero tiles (generic stores) before the MMAs
   tc_fence_before();
@@ -874,11 +883,12 @@ sparse_prefill_ws_kernel(Params p) {
   const int csh = (g.P == 2 * kTok) ? 1 : 0;    // chunks per block: 1 << csh
   const int C = U << csh;
   const int32_t* myrow = s_sel + (soft ? jj : 0) * k;
-  const uint32_t tO = tmem + W::kOCol;
-  auto tS = [&](int x) { return tmem + (uint32_t)(x * W::kSCols); };
+  auto tO = [&](int t) { return tmem + W::kOBase + (uint32_t)(t * D); };
+  auto tS = [&](int t, int x) { return tmem + (uint32_t)((2 * t + x) * W::kSCols); };
+  auto sQ = [&](int t) { return sQ0 + t * T::kQBytes; };
   auto sK = [&](int x) { return sK0 + x * T::kKBytes; };
   auto sV = [&](int x) { return sV0 + x * T::kVBytes; };
-  auto sP = [&](int x) { return sP0 + x * T::kPBytes; };
+  auto sP = [&](int t, int x) { return sP0 + (2 * t + x) * T::kPBytes; };
   bool dead = false;
 
   // ---- copy and MMA issue (one thread of warp 8) -------------------------------
@@ -901,25 +911,29 @@ sparse_prefill_ws_kernel(Params p) {
       bulk_g2s(dst + kTok * D + kTok * D / 16, p.v_sf + row0 * (D / 16), kTok * D / 16,
                &full[c & 1], pol);
     };
-    auto issue_s = [&](int c) {
+    auto issue_s = [&](int c) {   // every tile's S(c), then one commit
       const int x = c & 1;
       const uint32_t id = f16_idesc(128, kTok);
 #pragma unroll
-      for (int h = 0; h < D / 64; ++h)
+      for (int t = 0; t < NTL; ++t)
 #pragma unroll
-        for (int ks2 = 0; ks2 < 4; ++ks2)
-          mma_f16(tS(x), sw128_desc(smem_u32(sQ + h * 16384) + 32 * ks2),
-                  sw128_desc(smem_u32(sK(x) + h * T::kKBlk) + 32 * ks2), id,
-                  (h | ks2) ? 1u : 0u);
+        for (int h = 0; h < D / 64; ++h)
+#pragma unroll
+          for (int ks2 = 0; ks2 < 4; ++ks2)
+            mma_f16(tS(t, x), sw128_desc(smem_u32(sQ(t) + h * 16384) + 32 * ks2),
+                    sw128_desc(smem_u32(sK(x) + h * T::kKBlk) + 32 * ks2), id,
+                    (h | ks2) ? 1u : 0u);
       mma_commit(&barS[x]);
     };
-    auto issue_o = [&](int c) {
+    auto issue_o = [&](int c) {   // every tile's O += P(c) V(c), then one commit
       const int x = c & 1;
       const uint32_t id = f16_idesc(128, D);
 #pragma unroll
-      for (int ks2 = 0; ks2 < 4; ++ks2)
-        mma_f16(tO, sw128_desc(smem_u32(sP(x)) + 32 * ks2),
-                sw128_desc(smem_u32(sV(x)) + 32 * ks2), id, (c | ks2) ? 1u : 0u);
+      for (int t = 0; t < NTL; ++t)
+#pragma unroll
+        for (int ks2 = 0; ks2 < 4; ++ks2)
+          mma_f16(tO(t), sw128_desc(smem_u32(sP(t, x)) + 32 * ks2),
+                  sw128_desc(smem_u32(sV(x)) + 32 * ks2), id, (c | ks2) ? 1u : 0u);
       mma_commit(&barO[x]);
     };
     int ncopy = min(C, 2), ns = 0, no = 0;
@@ -965,7 +979,7 @@ sparse_prefill_ws_kernel(Params p) {
 
   // ---- dequantisation (warps 4-7) ----------------------------------------------
   if (deq) {
-    const int dt = tid - 128, dw = warp - 4;
+    const int dt = tid - 128 * NTL, dw = warp - 4 * NTL;
     for (int c = 0; c < C; ++c) {
       const int x = c & 1;
       const uint8_t* st = sStage + x * kStage;
@@ -1059,7 +1073,7 @@ sparse_prefill_ws_kernel(Params p) {
 #pragma unroll
       for (int q4 = 0; q4 < kTok / 16; ++q4) {
         float v16[16];
-        tmem_ld16(tS(x) + lane_off + 16 * q4, v16);
+        tmem_ld16(tS(tt, x) + lane_off + 16 * q4, v16);
 #pragma unroll
         for (int i = 0; i < 16; ++i) z[16 * q4 + i] = v16[i];
       }
@@ -1120,11 +1134,11 @@ sparse_prefill_ws_kernel(Params p) {
 #pragma unroll
         for (int q8 = 0; q8 < D / 16; ++q8) {
           float o16[16];
-          tmem_ld16(tO + lane_off + 16 * q8, o16);
+          tmem_ld16(tO(tt) + lane_off + 16 * q8, o16);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 16; ++i) o16[i] *= alpha;
-          tmem_st16(tO + lane_off + 16 * q8, o16);
+          tmem_st16(tO(tt) + lane_off + 16 * q8, o16);
         }
         tmem_wait_st();
       }
@@ -1136,7 +1150,7 @@ sparse_prefill_ws_kernel(Params p) {
       }
 #pragma unroll
       for (int c16 = 0; c16 < kTok / 8; ++c16)
-        *reinterpret_cast<uint4*>(sP(x) + sw128(tid, c16)) =
+        *reinterpret_cast<uint4*>(sP(tt, x) + sw128(vi, c16)) =
             make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
       fence_proxy_async_smem();
       tc_fence_before();
@@ -1160,7 +1174,7 @@ sparse_prefill_ws_kernel(Params p) {
     for (int q8 = 0; q8 < D / 16; ++q8) {
       float o16[16];
       if (C > 0) {
-        tmem_ld16(tO + lane_off + 16 * q8, o16);
+        tmem_ld16(tO(tt) + lane_off + 16 * q8, o16);
         tmem_wait_ld();
       }
       uint32_t h[8];
@@ -1203,11 +1217,13 @@ size_t prefill_smem_bytes(const Geom& g, int k) {
 
 // The warp-specialised kernel's shared memory (double-buffered tiles); the
 // four-warp kernel (single tiles) serves geometries where it does not fit.
+int prefill_ws_tiles(const Geom& g) { return g.D == 256 ? WT<256>::kNtl : WT<128>::kNtl; }
+
 size_t prefill_ws_smem_bytes(const Geom& g, int k) {
-  const int tr = prefill_rows_per_tile(g);
-  const int ucap = min(g.MB, tr * k);
+  const int rows = prefill_ws_tiles(g) * prefill_rows_per_tile(g);   // rows per CTA
+  const int ucap = min(g.MB, rows * k);
   const size_t tiles = g.D == 256 ? WT<256>::kTiles : WT<128>::kTiles;
-  return (size_t)1024 + tiles + 2 * kStage + 14 * 8 + 4 + 8 * 4 + (size_t)tr * k * 4 +
+  return (size_t)1024 + tiles + 2 * kStage + 14 * 8 + 4 + 8 * 4 + (size_t)rows * k * 4 +
          (size_t)ucap * 8 + (size_t)((g.MB + 31) / 32) * 4;
 }
 
@@ -1234,14 +1250,16 @@ cudaError_t launch_sparse_prefill(const Geom& g, const void* q, const uint8_t* k
   const bool ws = prefill_ws_smem_bytes(g, k) <= 227 * 1024;
 #endif
   const size_t smem = ws ? prefill_ws_smem_bytes(g, k) : prefill_smem_bytes(g, k);
+  const int rows_per_cta = (ws ? prefill_ws_tiles(g) : 1) * prm.tr;
+  prm.ucap = min(g.MB, rows_per_cta * k);
   auto* kern = ws ? (g.D == 256 ? sparse_prefill_ws_kernel<256> : sparse_prefill_ws_kernel<128>)
                   : (g.D == 256 ? sparse_prefill_kernel<256> : sparse_prefill_kernel<128>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((g.R + prm.tr - 1) / prm.tr, g.Hkv, g.B);
-  cfg.blockDim = dim3(ws ? kWsThreads : kThreads);
+  cfg.gridDim = dim3((g.R + rows_per_cta - 1) / rows_per_cta, g.Hkv, g.B);
+  cfg.blockDim = dim3(ws ? (g.D == 256 ? WT<256>::kThreads : WT<128>::kThreads) : kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
