@@ -148,6 +148,34 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b,
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
+// tcgen05.mma with A (M x 16, fp16) in tensor memory reads lane m as row m,
+// column j as the elements 2j (low half) and 2j + 1.
+// The same MMAs issued by one elected lane of a converged warp (warp-uniform
+// operands), and their commit from that lane.
+__device__ __forceinline__ void mma_f16_elect(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_f16_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
@@ -185,6 +213,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
       "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
       "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
       "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+
+// 16 words into 16 consecutive columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
       : "memory");
 }
 
@@ -670,34 +709,53 @@ sparse_prefill_kernel(Params p) {
 }
 
 // ---------------------------------------------------------------------------
-// Warp-specialised row tiles.  Nine warps: warps 0-3 own the tile's 128
-// tensor-memory lanes (queries, softmax, epilogue), warps 4-7 dequantise the
-// NVFP4 chunks into double-buffered fp16 K and V^T tiles, and one thread of
-// warp 8 issues the bulk copies and the MMAs.  S is double-buffered in tensor
-// memory and P in shared memory, so for chunk c the softmax of c, the
-// dequantisation of c + 1 and the MMAs S(c + 1) and O(c - 1) overlap.
+// Warp-specialised row tiles.  Per query tile four softmax warps own its 128
+// tensor-memory lanes (queries, softmax, epilogue); four warps dequantise the
+// NVFP4 chunks into double-buffered fp16 K and V^T tiles in shared memory, and
+// one thread issues the bulk copies and the MMAs.  P goes from the softmax
+// into tensor memory (double-buffered) and feeds O += P V as the A operand
+// from there, so shared memory carries only the K and V^T operands.  S is
+// double-buffered in tensor memory at head_dim 256 and single-buffered at
+// head_dim 128 (two tiles' O fill half of it); the softmax releases its S
+// buffer as soon as it has loaded S into registers.  For chunk c the softmax
+// of c, the dequantisation of c + 1 and the MMAs S(c + 1) and O(c - 1) overlap.
 // Hand-overs are mbarriers (all waits bounded):
 //   full[x]   copy of a chunk into stage x landed       (1 arrival + bytes)
 //   empty[x]  the dequant warps are done with stage x    (4 arrivals)
 //   kready[x] K tile x written                           (128 arrivals)
 //   vready[x] V^T tile x written                         (128 arrivals)
-//   pready[x] P tile x written, O rescaled, S buffer x read (128 arrivals)
-//   barS[x]   S into tensor-memory buffer x complete     (commit)
+//   kfree[x]  S MMAs that read K tile x complete         (commit)
+//   barS[y]   S into tensor-memory buffer y complete     (commit)
+//   sfree[y]  S buffer y loaded by every softmax thread  (128 NTL arrivals)
+//   pready[x] P buffer x written, O rescaled             (128 NTL arrivals)
 //   barO[x]   O += P(x) V(x) complete                    (commit)
-// Chunk c uses buffer x = c & 1; its phase on a buffer's barrier is c >> 1.
+// Chunk c uses buffer x = c & 1 (phase c >> 1) and S buffer y = c % SB
+// (phase c / SB), SB the number of S buffers.
 // At head_dim 128 a CTA holds two query tiles (NTL = 2: eight softmax warps,
 // 2 x TR consecutive rows) that share every dequantised chunk of the union of
 // their rows' selections; at head_dim 256 one (two Q tiles would not fit).
+// Tensor memory (512 columns): S buffers from column 0, then the P buffers
+// (kTok / 2 columns each: two fp16 per column), O of tile t at 256 + t D.
+constexpr int kWsBars = 18;   // mbarriers of the warp-specialised kernel
+
+// Words of a row's membership bitmap over the union (odd, so the rows of one
+// warp fall on different banks).
+__host__ __device__ __forceinline__ int ws_member_words(int ucap) {
+  return ((ucap + 31) >> 5) | 1;
+}
+
 template <int D>
 struct WT {
   using T = PT<D>;
   static constexpr int kNtl = D == 128 ? 2 : 1;       // query tiles per CTA
-  static constexpr int kThreads = 128 * kNtl + 160;   // softmax, dequant, issuer
-  static constexpr int kSCols = T::kTok;
+  static constexpr int kThreads = 128 * kNtl + 192;   // softmax, dequant, MMA, copy
+  static constexpr int kSBuf = D == 128 ? 1 : 2;      // S buffers per tile
+  static constexpr uint32_t kPBase = kNtl * kSBuf * T::kTok;   // P of (t, x) after S
   static constexpr uint32_t kOBase = 256;             // O of tile t at kOBase + t * D
   static constexpr uint32_t kTmemCols = 512;
   static constexpr size_t kTiles =
-      (size_t)kNtl * T::kQBytes + 2 * ((size_t)T::kKBytes + T::kVBytes + (size_t)kNtl * T::kPBytes);
+      (size_t)kNtl * T::kQBytes + 2 * ((size_t)T::kKBytes + T::kVBytes);
+  static_assert(kPBase + 2 * kNtl * T::kTok / 2 <= kOBase, "tensor-memory columns");
 };
 
 template <int D>
@@ -706,8 +764,8 @@ sparse_prefill_ws_kernel(Params p) {
   using T = PT<D>;
   using W = WT<D>;
   constexpr int NTL = W::kNtl;
-  constexpr int kWsThreads = W::kThreads;
   constexpr int kTok = T::kTok;
+  constexpr int SB = W::kSBuf;
   const Geom& g = p.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = g.Hq / g.Hkv;
@@ -717,7 +775,8 @@ sparse_prefill_ws_kernel(Params p) {
   const int rows = min(NTL * TR, g.R - r0);   // rows of the CTA
   const int k = p.k;
   const bool soft = warp < 4 * NTL, deq = warp >= 4 * NTL && warp < 4 * NTL + 4;
-  const bool iss = tid == 128 * NTL + 128;
+  const bool mmaw = warp == 4 * NTL + 4;                 // the MMA warp
+  const bool cpy = warp == 4 * NTL + 5 && lane == 0;     // the copy thread
   const int tt = soft ? warp >> 2 : 0;        // a softmax thread's tile
   const int vi = tid & 127;                   // its query vector (tile row)
 
@@ -727,23 +786,27 @@ sparse_prefill_ws_kernel(Params p) {
   uint8_t* sQ0 = smem;                                  // [NTL][kQBytes]
   uint8_t* sK0 = sQ0 + NTL * T::kQBytes;                // [2][kKBytes]
   uint8_t* sV0 = sK0 + 2 * T::kKBytes;                  // [2][kVBytes]
-  uint8_t* sP0 = sV0 + 2 * T::kVBytes;                  // [2][kPBytes]
-  uint8_t* sStage = sP0 + 2 * NTL * T::kPBytes;         // [2][kStage]
+  uint8_t* sStage = sV0 + 2 * T::kVBytes;               // [2][kStage]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + 2 * kStage);
   uint64_t* full = bars;
   uint64_t* empty = bars + 2;
   uint64_t* kready = bars + 4;
   uint64_t* vready = bars + 6;
-  uint64_t* pready = bars + 8;
+  uint64_t* kfree = bars + 8;
   uint64_t* barS = bars + 10;
-  uint64_t* barO = bars + 12;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 14);
-  int* s_misc = reinterpret_cast<int*>(s_tmem + 1);            // [8]
-  int32_t* s_sel = s_misc + 8;                                  // [NTL * TR][k]
+  uint64_t* sfree = bars + 12;
+  uint64_t* pready = bars + 14;
+  uint64_t* barO = bars + 16;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + kWsBars);
+  int* s_misc = reinterpret_cast<int*>(s_tmem + 1);            // [12]: warp counts, total
+  int32_t* s_sel = s_misc + 12;                                 // [NTL * TR][k]
   int32_t* s_union = s_sel + NTL * TR * k;                      // [ucap]
   int32_t* s_upage = s_union + p.ucap;                          // [ucap]
-  uint32_t* s_bits = reinterpret_cast<uint32_t*>(s_upage + p.ucap);   // [ceil(MB/32)]
   const int nwords = (g.MB + 31) >> 5;
+  const int mwords = ws_member_words(p.ucap);
+  uint32_t* s_bits = reinterpret_cast<uint32_t*>(s_upage + p.ucap);   // [nwords]
+  int* s_wpre = reinterpret_cast<int*>(s_bits + nwords);              // [nwords]
+  uint32_t* s_mem = reinterpret_cast<uint32_t*>(s_wpre + nwords);     // [NTL * TR][mwords]
 
   if (tid == 0) {
     for (int x = 0; x < 2; ++x) {
@@ -751,8 +814,10 @@ sparse_prefill_ws_kernel(Params p) {
       mbar_init(&empty[x], 4);
       mbar_init(&kready[x], 128);
       mbar_init(&vready[x], 128);
-      mbar_init(&pready[x], 128 * NTL);
+      mbar_init(&kfree[x], 1);
       mbar_init(&barS[x], 1);
+      mbar_init(&sfree[x], 128 * NTL);
+      mbar_init(&pready[x], 128 * NTL);
       mbar_init(&barO[x], 1);
     }
     fence_mbar_init();
@@ -810,13 +875,6 @@ sparse_prefill_ws_kernel(Params p) {
       *reinterpret_cast<uint4*>(sQ0 + tt * T::kQBytes + (i >> 3) * 16384 + sw128(vi, i & 7)) = h;
     }
   }
-  // Token slots past a chunk (D = 256: 32 of the 64 slots of every V^T and P
-  // tile) stay zero: cleared once here, never written.
-  if (kTok < 64) {
-    for (int i = tid; i < (2 * T::kVBytes + 2 * NTL * T::kPBytes) / 16; i += kWsThreads)
-      reinterpret_cast<uint4*>(sV0)[i] = make_uint4(0u, 0u, 0u, 0u);
-  }
-
   // ---- the tile's rows' selections and their union (softmax warps) ------------
   if (soft) {
     auto soft_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(128 * NTL) : "memory"); };
@@ -830,6 +888,7 @@ sparse_prefill_ws_kernel(Params p) {
       s_sel[i] = v;
     }
     for (int i = tid; i < nwords; i += 128 * NTL) s_bits[i] = 0u;
+    for (int i = tid; i < NTL * TR * mwords; i += 128 * NTL) s_mem[i] = 0u;
     soft_sync();
     for (int i = tid; i < rows * k; i += 128 * NTL) {
       const int v = s_sel[i];
@@ -861,6 +920,7 @@ sparse_prefill_ws_kernel(Params p) {
     int pos = x - cnt;
     for (int w = 0; w < warp; ++w) pos += s_misc[w];
     for (int w = w0; w < w1; ++w) {
+      s_wpre[w] = pos;   // union position of the word's first block
       uint32_t m = s_bits[w];
       while (m) {
         const int beta = (w << 5) + __ffs(m) - 1;
@@ -872,30 +932,38 @@ sparse_prefill_ws_kernel(Params p) {
         ++pos;
       }
     }
-    if (tid == 128 * NTL - 1) s_misc[4] = pos;
+    if (tid == 128 * NTL - 1) s_misc[10] = pos;
+    soft_sync();
+    // Each row's membership bitmap over the union positions.
+    for (int i = tid; i < rows * k; i += 128 * NTL) {
+      const int v = s_sel[i];
+      if (v < 0 || !((s_bits[v >> 5] >> (v & 31)) & 1u)) continue;
+      const int u = s_wpre[v >> 5] + __popc(s_bits[v >> 5] & ((1u << (v & 31)) - 1u));
+      if (QSA_IN_BOUNDS(u < p.ucap, kChkUnion))
+        atomicOr(&s_mem[(i / k) * mwords + (u >> 5)], 1u << (u & 31));
+    }
   }
   fence_proxy_async_smem();       // Q and zero tiles (generic stores) before the MMAs
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  const int U = s_misc[4];
+  const int U = s_misc[10];
   const int csh = (g.P == 2 * kTok) ? 1 : 0;    // chunks per block: 1 << csh
   const int C = U << csh;
-  const int32_t* myrow = s_sel + (soft ? jj : 0) * k;
+  const uint32_t* mymem = s_mem + (vec ? jj : 0) * mwords;
   auto tO = [&](int t) { return tmem + W::kOBase + (uint32_t)(t * D); };
-  auto tS = [&](int t, int x) { return tmem + (uint32_t)((2 * t + x) * W::kSCols); };
+  auto tS = [&](int t, int c) { return tmem + (uint32_t)((t * SB + c % SB) * kTok); };
+  auto tP = [&](int t, int x) { return tmem + W::kPBase + (uint32_t)((2 * t + x) * (kTok / 2)); };
   auto sQ = [&](int t) { return sQ0 + t * T::kQBytes; };
   auto sK = [&](int x) { return sK0 + x * T::kKBytes; };
   auto sV = [&](int x) { return sV0 + x * T::kVBytes; };
-  auto sP = [&](int t, int x) { return sP0 + (2 * t + x) * T::kPBytes; };
   bool dead = false;
 
-  // ---- copy and MMA issue (one thread of warp 8) -------------------------------
-  // S(c) once K(c) is dequantised and softmax(c - 2) has read S buffer c & 1;
-  // O(c - 1) once P(c - 1) and V(c - 1) are ready; stage c & 1 is refilled
-  // with chunk c + 2 once the dequantisation warps are done with chunk c.
-  if (iss) {
+  // ---- bulk copies (lane 0 of the copy warp) ----------------------------------
+  // Stage c & 1 is refilled with chunk c + 2 once the dequantisation warps
+  // are done with chunk c.
+  if (cpy) {
     const uint64_t pol = policy_evict_first();
     auto issue_copy = [&](int c) {
       uint8_t* dst = sStage + (c & 1) * kStage;
@@ -911,37 +979,72 @@ sparse_prefill_ws_kernel(Params p) {
       bulk_g2s(dst + kTok * D + kTok * D / 16, p.v_sf + row0 * (D / 16), kTok * D / 16,
                &full[c & 1], pol);
     };
-    auto issue_s = [&](int c) {   // every tile's S(c), then one commit
+    int ncopy = min(C, 2);
+    for (int c = 0; c < ncopy; ++c) issue_copy(c);
+    for (int c = 2; c < C; ++c) {
+      if (!wait_bounded(&empty[c & 1], ((c - 2) >> 1) & 1)) {
+        dead = true;
+        break;
+      }
+      fence_proxy_async_smem();   // the dequant warps' reads of the stage come first
+      issue_copy(c);
+      ncopy = c + 1;
+    }
+    // Every copy issued lands before shared memory is released.
+    for (int c = max(0, ncopy - 2); c < ncopy; ++c) wait_bounded(&full[c & 1], (c >> 1) & 1);
+  }
+
+  // ---- MMA issue (the MMA warp; one elected lane issues) -----------------------
+  // S(c) once K(c) is dequantised and softmax(c - SB) has loaded S buffer
+  // c % SB; O(c - 1) once P(c - 1) and V(c - 1) are ready.  The whole warp
+  // runs the loop so descriptors stay warp-uniform; waits probe both of their
+  // barriers before blocking on either.
+  if (mmaw) {
+    const uint32_t id_s = f16_idesc(128, kTok), id_o = f16_idesc(128, D);
+    uint64_t dq[NTL];
+#pragma unroll
+    for (int t = 0; t < NTL; ++t) dq[t] = sw128_desc(smem_u32(sQ(t)));
+    const uint64_t dk0 = sw128_desc(smem_u32(sK(0))), dk1 = sw128_desc(smem_u32(sK(1)));
+    const uint64_t dv0 = sw128_desc(smem_u32(sV(0))), dv1 = sw128_desc(smem_u32(sV(1)));
+    auto issue_s = [&](int c) {   // every tile's S(c); S buffer and K tile commits
       const int x = c & 1;
-      const uint32_t id = f16_idesc(128, kTok);
+      const uint64_t dk = x ? dk1 : dk0;
 #pragma unroll
       for (int t = 0; t < NTL; ++t)
 #pragma unroll
         for (int h = 0; h < D / 64; ++h)
 #pragma unroll
           for (int ks2 = 0; ks2 < 4; ++ks2)
-            mma_f16(tS(t, x), sw128_desc(smem_u32(sQ(t) + h * 16384) + 32 * ks2),
-                    sw128_desc(smem_u32(sK(x) + h * T::kKBlk) + 32 * ks2), id,
-                    (h | ks2) ? 1u : 0u);
-      mma_commit(&barS[x]);
+            mma_f16_elect(tS(t, c), dq[t] + (uint64_t)((h * 16384 + 32 * ks2) >> 4),
+                          dk + (uint64_t)((h * T::kKBlk + 32 * ks2) >> 4), id_s,
+                          (h | ks2) ? 1u : 0u);
+      mma_commit_elect(&barS[c % SB]);
+      mma_commit_elect(&kfree[x]);
     };
-    auto issue_o = [&](int c) {   // every tile's O += P(c) V(c), then one commit
+    // Every tile's O += P(c) V(c): P from tensor memory (kTok / 16 steps of 16
+    // tokens, eight columns each), V^T from shared memory; then one commit.
+    auto issue_o = [&](int c) {
       const int x = c & 1;
-      const uint32_t id = f16_idesc(128, D);
+      const uint64_t dv = x ? dv1 : dv0;
 #pragma unroll
       for (int t = 0; t < NTL; ++t)
 #pragma unroll
-        for (int ks2 = 0; ks2 < 4; ++ks2)
-          mma_f16(tO(t), sw128_desc(smem_u32(sP(t, x)) + 32 * ks2),
-                  sw128_desc(smem_u32(sV(x)) + 32 * ks2), id, (c | ks2) ? 1u : 0u);
-      mma_commit(&barO[x]);
+        for (int ks2 = 0; ks2 < kTok / 16; ++ks2)
+          mma_f16_ts_elect(tO(t), tP(t, x) + 8 * ks2, dv + (uint64_t)((32 * ks2) >> 4), id_o,
+                           (c | ks2) ? 1u : 0u);
+      mma_commit_elect(&barO[x]);
     };
-    int ncopy = min(C, 2), ns = 0, no = 0;
-    for (int c = 0; c < ncopy; ++c) issue_copy(c);
+    auto wait_pair = [&](uint64_t* b1, uint32_t p1, bool two, uint64_t* b2, uint32_t p2) {
+      const bool r1 = mbar_try_wait(b1, p1);
+      const bool r2 = !two || mbar_try_wait(b2, p2);
+      const bool ok = (r1 || wait_bounded(b1, p1)) && (r2 || wait_bounded(b2, p2));
+      return __all_sync(0xffffffffu, ok);
+    };
+    int ns = 0, no = 0;
     for (int c = 0; c <= C; ++c) {
       if (c < C) {
-        if (!wait_bounded(&kready[c & 1], (c >> 1) & 1) ||
-            (c >= 2 && !wait_bounded(&pready[c & 1], ((c - 2) >> 1) & 1))) {
+        const int cf = max(c - SB, 0);   // the chunk whose S buffer S(c) reuses
+        if (!wait_pair(&kready[c & 1], (c >> 1) & 1, c >= SB, &sfree[cf % SB], (cf / SB) & 1)) {
           dead = true;
           break;
         }
@@ -951,8 +1054,7 @@ sparse_prefill_ws_kernel(Params p) {
       }
       if (c >= 1) {
         const int o = c - 1;
-        if (!wait_bounded(&pready[o & 1], (o >> 1) & 1) ||
-            !wait_bounded(&vready[o & 1], (o >> 1) & 1)) {
+        if (!wait_pair(&pready[o & 1], (o >> 1) & 1, true, &vready[o & 1], (o >> 1) & 1)) {
           dead = true;
           break;
         }
@@ -960,21 +1062,12 @@ sparse_prefill_ws_kernel(Params p) {
         issue_o(o);
         no = o + 1;
       }
-      if (c + 2 < C) {
-        if (!wait_bounded(&empty[c & 1], (c >> 1) & 1)) {
-          dead = true;
-          break;
-        }
-        fence_proxy_async_smem();   // the dequant warps' reads of the stage come first
-        issue_copy(c + 2);
-        ncopy = c + 3;
-      }
     }
-    // Every copy and MMA this thread issued completes before the tiles and
-    // tensor memory are read or released (at once when nothing went wrong).
-    for (int c = max(0, ncopy - 2); c < ncopy; ++c) wait_bounded(&full[c & 1], (c >> 1) & 1);
-    for (int c = max(0, ns - 2); c < ns; ++c) wait_bounded(&barS[c & 1], (c >> 1) & 1);
+    // Every MMA issued completes before the tiles and tensor memory are read
+    // or released (at once when nothing went wrong).
+    for (int c = max(0, ns - 2); c < ns; ++c) wait_bounded(&kfree[c & 1], (c >> 1) & 1);
     for (int c = max(0, no - 2); c < no; ++c) wait_bounded(&barO[c & 1], (c >> 1) & 1);
+    __syncwarp();
   }
 
   // ---- dequantisation (warps 4-7) ----------------------------------------------
@@ -985,8 +1078,8 @@ sparse_prefill_ws_kernel(Params p) {
       const uint8_t* st = sStage + x * kStage;
       // Warp-uniform give-ups (the warp syncs below).
       if (__any_sync(0xffffffffu, !wait_bounded(&full[x], (c >> 1) & 1) ||
-                                      (c >= 2 && !wait_bounded(&barS[x], ((c - 2) >> 1) & 1)))) {
-        dead = true;   // (barS: S(c - 2) has read K tile x)
+                                      (c >= 2 && !wait_bounded(&kfree[x], ((c - 2) >> 1) & 1)))) {
+        dead = true;   // (kfree: S(c - 2) has read K tile x)
         break;
       }
       {
@@ -1060,24 +1153,31 @@ sparse_prefill_ws_kernel(Params p) {
   if (soft) {
     for (int c = 0; c < C; ++c) {
       const int x = c & 1;
-      // Warp-uniform give-up: tensor-memory loads and stores are warp-wide.
-      if (__any_sync(0xffffffffu, !wait_bounded(&barS[x], (c >> 1) & 1))) {
+      const int u = c >> csh;                      // union position of the chunk
+      const uint32_t mword = mymem[u >> 5];
+      const int ue = s_union[u];
+      // First probes of S(c) and of O(c - 2) (P buffer x free) overlap; then a
+      // warp-uniform give-up (tensor-memory loads and stores are warp-wide).
+      const bool s_now = mbar_try_wait(&barS[c % SB], (c / SB) & 1);
+      const bool p_now = c < 2 || mbar_try_wait(&barO[x], ((c - 2) >> 1) & 1);
+      if (__any_sync(0xffffffffu, !(s_now || wait_bounded(&barS[c % SB], (c / SB) & 1)))) {
         dead = true;
         break;
       }
       tc_fence_after();
-      const int ue = s_union[c >> csh];
       const int tok0 = ue * g.P + (c & csh) * kTok;
-      const bool member = vec && tok0 < nrow && row_holds(myrow, k, ue);
+      const bool member = vec && tok0 < nrow && ((mword >> (u & 31)) & 1u);
       float z[kTok];
 #pragma unroll
       for (int q4 = 0; q4 < kTok / 16; ++q4) {
         float v16[16];
-        tmem_ld16(tS(tt, x) + lane_off + 16 * q4, v16);
+        tmem_ld16(tS(tt, c) + lane_off + 16 * q4, v16);
 #pragma unroll
         for (int i = 0; i < 16; ++i) z[16 * q4 + i] = v16[i];
       }
       tmem_wait_ld();
+      tc_fence_before();
+      ws_arrive(&sfree[c % SB]);   // S buffer loaded: S(c + SB) may overwrite it
       float cmax = -INFINITY;   // log2 units
       if (member) {
         if (tok0 + kTok > nrow) {
@@ -1142,19 +1242,18 @@ sparse_prefill_ws_kernel(Params p) {
         }
         tmem_wait_st();
       }
-      // P tile x is free once O(c - 2) completed.
-      if (c >= 2 &&
-          __any_sync(0xffffffffu, !wait_bounded(&barO[x], ((c - 2) >> 1) & 1))) {
+      // P buffer x is free once O(c - 2) completed.
+      if (__any_sync(0xffffffffu, !(p_now || wait_bounded(&barO[x], ((c - 2) >> 1) & 1)))) {
         dead = true;
         break;
       }
+      tc_fence_after();
+      // This lane's P row: token pair i in column i (the A-operand layout).
 #pragma unroll
-      for (int c16 = 0; c16 < kTok / 8; ++c16)
-        *reinterpret_cast<uint4*>(sP(tt, x) + sw128(vi, c16)) =
-            make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
-      fence_proxy_async_smem();
+      for (int q = 0; q < kTok / 32; ++q) tmem_st16u(tP(tt, x) + lane_off + 16 * q, pk + 16 * q);
+      tmem_wait_st();
       tc_fence_before();
-      ws_arrive(&pready[x]);   // P(c) written, O rescaled, S buffer x read
+      ws_arrive(&pready[x]);   // P(c) written, O rescaled
     }
   }
 
@@ -1223,8 +1322,8 @@ size_t prefill_ws_smem_bytes(const Geom& g, int k) {
   const int rows = prefill_ws_tiles(g) * prefill_rows_per_tile(g);   // rows per CTA
   const int ucap = min(g.MB, rows * k);
   const size_t tiles = g.D == 256 ? WT<256>::kTiles : WT<128>::kTiles;
-  return (size_t)1024 + tiles + 2 * kStage + 14 * 8 + 4 + 8 * 4 + (size_t)rows * k * 4 +
-         (size_t)ucap * 8 + (size_t)((g.MB + 31) / 32) * 4;
+  return (size_t)1024 + tiles + 2 * kStage + kWsBars * 8 + 4 + 12 * 4 + (size_t)rows * k * 4 +
+         (size_t)ucap * 8 + (size_t)((g.MB + 31) / 32) * 8 + (size_t)rows * ws_member_words(ucap) * 4;
 }
 
 cudaError_t launch_sparse_prefill(const Geom& g, const void* q, const uint8_t* k_pool,
