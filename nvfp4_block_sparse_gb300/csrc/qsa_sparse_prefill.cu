@@ -720,23 +720,27 @@ sparse_prefill_kernel(Params p) {
 // buffer as soon as it has loaded S into registers.  For chunk c the softmax
 // of c, the dequantisation of c + 1 and the MMAs S(c + 1) and O(c - 1) overlap.
 // Hand-overs are mbarriers (all waits bounded):
-//   full[x]   copy of a chunk into stage x landed       (1 arrival + bytes)
-//   empty[x]  the dequant warps are done with stage x    (4 arrivals)
-//   kready[x] K tile x written                           (128 arrivals)
-//   vready[x] V^T tile x written                         (128 arrivals)
-//   kfree[x]  S MMAs that read K tile x complete         (commit)
-//   barS[y]   S into tensor-memory buffer y complete     (commit)
-//   sfree[y]  S buffer y loaded by every softmax thread  (128 NTL arrivals)
-//   pready[x] P buffer x written, O rescaled             (128 NTL arrivals)
-//   barO[x]   O += P(x) V(x) complete                    (commit)
-// Chunk c uses buffer x = c & 1 (phase c >> 1) and S buffer y = c % SB
-// (phase c / SB), SB the number of S buffers.
+//   full[z]      copy of a chunk into stage z landed         (1 arrival + bytes)
+//   empty[z]     the dequant warps are done with stage z      (4 arrivals)
+//   kready[x]    K tile x written                             (128 arrivals)
+//   vready[x]    V^T tile x written                           (128 arrivals)
+//   kfree[x]     every tile's S MMAs that read K tile x done  (commit)
+//   vfree[x]     every tile's O MMAs that read V^T tile x done (commit)
+//   barS[t][y]   S of tile t into its buffer y complete       (commit)
+//   sfree[t][y]  tile t's softmax has loaded S buffer y       (128 arrivals)
+//   pready[t][x] P buffer x of tile t written, O rescaled     (128 arrivals)
+//   barO[t][x]   O_t += P_t(x) V(x) complete                  (commit)
+// Chunk c uses stage z = c % 4 (phase c / 4), tile buffer x = c & 1 (phase
+// c >> 1) and S buffer y = c % SB (phase c / SB), SB the S buffers per tile.
+// Each tile has its own S, P and O hand-overs, so the MMA warp can issue one
+// tile's MMAs while the other tile's softmax runs.
 // At head_dim 128 a CTA holds two query tiles (NTL = 2: eight softmax warps,
 // 2 x TR consecutive rows) that share every dequantised chunk of the union of
 // their rows' selections; at head_dim 256 one (two Q tiles would not fit).
 // Tensor memory (512 columns): S buffers from column 0, then the P buffers
 // (kTok / 2 columns each: two fp16 per column), O of tile t at 256 + t D.
-constexpr int kWsBars = 18;   // mbarriers of the warp-specialised kernel
+constexpr int kWsStages = 4;   // NVFP4 chunk stages of the warp-specialised kernel
+constexpr int kWsBars = 30;    // its mbarriers
 
 // Words of a row's membership bitmap over the union (odd, so the rows of one
 // warp fall on different banks).
@@ -748,7 +752,7 @@ template <int D>
 struct WT {
   using T = PT<D>;
   static constexpr int kNtl = D == 128 ? 2 : 1;       // query tiles per CTA
-  static constexpr int kThreads = 128 * kNtl + 192;   // softmax, dequant, MMA, copy
+  static constexpr int kThreads = 160 * kNtl + 160;   // softmax, dequant, MMA, copy
   static constexpr int kSBuf = D == 128 ? 1 : 2;      // S buffers per tile
   static constexpr uint32_t kPBase = kNtl * kSBuf * T::kTok;   // P of (t, x) after S
   static constexpr uint32_t kOBase = 256;             // O of tile t at kOBase + t * D
@@ -775,8 +779,9 @@ sparse_prefill_ws_kernel(Params p) {
   const int rows = min(NTL * TR, g.R - r0);   // rows of the CTA
   const int k = p.k;
   const bool soft = warp < 4 * NTL, deq = warp >= 4 * NTL && warp < 4 * NTL + 4;
-  const bool mmaw = warp == 4 * NTL + 4;                 // the MMA warp
-  const bool cpy = warp == 4 * NTL + 5 && lane == 0;     // the copy thread
+  const bool mmaw = warp >= 4 * NTL + 4 && warp < 5 * NTL + 4;   // one MMA warp per tile
+  const int mt = warp - (4 * NTL + 4);                            // its tile
+  const bool cpy = warp == 5 * NTL + 4 && lane == 0;              // the copy thread
   const int tt = soft ? warp >> 2 : 0;        // a softmax thread's tile
   const int vi = tid & 127;                   // its query vector (tile row)
 
@@ -786,17 +791,19 @@ sparse_prefill_ws_kernel(Params p) {
   uint8_t* sQ0 = smem;                                  // [NTL][kQBytes]
   uint8_t* sK0 = sQ0 + NTL * T::kQBytes;                // [2][kKBytes]
   uint8_t* sV0 = sK0 + 2 * T::kKBytes;                  // [2][kVBytes]
-  uint8_t* sStage = sV0 + 2 * T::kVBytes;               // [2][kStage]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + 2 * kStage);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + 2;
-  uint64_t* kready = bars + 4;
-  uint64_t* vready = bars + 6;
-  uint64_t* kfree = bars + 8;
-  uint64_t* barS = bars + 10;
-  uint64_t* sfree = bars + 12;
-  uint64_t* pready = bars + 14;
-  uint64_t* barO = bars + 16;
+  uint8_t* sStage = sV0 + 2 * T::kVBytes;               // [kWsStages][kStage]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + kWsStages * kStage);
+  uint64_t* full = bars;                 // [kWsStages]
+  uint64_t* empty = bars + 4;            // [kWsStages]
+  uint64_t* kready = bars + 8;           // [2]
+  uint64_t* vready = bars + 10;          // [2]
+  uint64_t* kfree = bars + 12;           // [2]
+  uint64_t* vfree = bars + 14;           // [2]
+  uint64_t* barS = bars + 16;            // [NTL][SB]
+  uint64_t* sfree = bars + 18;           // [NTL][SB]
+  uint64_t* pready = bars + 20;          // [NTL][2]
+  uint64_t* barO = bars + 24;            // [NTL][2]
+  uint64_t* mdone = bars + 28;           // [NTL] every MMA of tile t's warp completed
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + kWsBars);
   int* s_misc = reinterpret_cast<int*>(s_tmem + 1);            // [12]: warp counts, total
   int32_t* s_sel = s_misc + 12;                                 // [NTL * TR][k]
@@ -809,17 +816,24 @@ sparse_prefill_ws_kernel(Params p) {
   uint32_t* s_mem = reinterpret_cast<uint32_t*>(s_wpre + nwords);     // [NTL * TR][mwords]
 
   if (tid == 0) {
+    for (int z = 0; z < kWsStages; ++z) {
+      mbar_init(&full[z], 1);
+      mbar_init(&empty[z], 4);
+    }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&full[x], 1);
-      mbar_init(&empty[x], 4);
       mbar_init(&kready[x], 128);
       mbar_init(&vready[x], 128);
-      mbar_init(&kfree[x], 1);
+      mbar_init(&kfree[x], NTL);   // one commit per MMA warp
+      mbar_init(&vfree[x], NTL);
       mbar_init(&barS[x], 1);
-      mbar_init(&sfree[x], 128 * NTL);
-      mbar_init(&pready[x], 128 * NTL);
-      mbar_init(&barO[x], 1);
+      mbar_init(&sfree[x], 128);
     }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&pready[i], 128);
+      mbar_init(&barO[i], 1);
+    }
+    mbar_init(&mdone[0], 1);
+    mbar_init(&mdone[1], 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -961,28 +975,30 @@ sparse_prefill_ws_kernel(Params p) {
   bool dead = false;
 
   // ---- bulk copies (lane 0 of the copy warp) ----------------------------------
-  // Stage c & 1 is refilled with chunk c + 2 once the dequantisation warps
+  // Stage c % 4 is refilled with chunk c + 4 once the dequantisation warps
   // are done with chunk c.
   if (cpy) {
     const uint64_t pol = policy_evict_first();
     auto issue_copy = [&](int c) {
-      uint8_t* dst = sStage + (c & 1) * kStage;
+      const int z = c % kWsStages;
+      uint8_t* dst = sStage + z * kStage;
       const int u = c >> csh, sub = c & csh;
       if (!QSA_IN_BOUNDS(u < U && u < p.ucap && s_upage[u] >= 0 && s_upage[u] < g.NP,
                          kChkChunk))
         return;
       const size_t row0 = ((size_t)s_upage[u] * g.Hkv + kvh) * g.P + (size_t)sub * kTok;
-      mbar_arrive_expect_tx(&full[c & 1], kStage);
-      bulk_g2s(dst, p.k_pool + row0 * (D / 2), kTok * D / 2, &full[c & 1], pol);
-      bulk_g2s(dst + kTok * D / 2, p.v_pool + row0 * (D / 2), kTok * D / 2, &full[c & 1], pol);
-      bulk_g2s(dst + kTok * D, p.k_sf + row0 * (D / 16), kTok * D / 16, &full[c & 1], pol);
+      mbar_arrive_expect_tx(&full[z], kStage);
+      bulk_g2s(dst, p.k_pool + row0 * (D / 2), kTok * D / 2, &full[z], pol);
+      bulk_g2s(dst + kTok * D / 2, p.v_pool + row0 * (D / 2), kTok * D / 2, &full[z], pol);
+      bulk_g2s(dst + kTok * D, p.k_sf + row0 * (D / 16), kTok * D / 16, &full[z], pol);
       bulk_g2s(dst + kTok * D + kTok * D / 16, p.v_sf + row0 * (D / 16), kTok * D / 16,
-               &full[c & 1], pol);
+               &full[z], pol);
     };
-    int ncopy = min(C, 2);
+    int ncopy = min(C, kWsStages);
     for (int c = 0; c < ncopy; ++c) issue_copy(c);
-    for (int c = 2; c < C; ++c) {
-      if (!wait_bounded(&empty[c & 1], ((c - 2) >> 1) & 1)) {
+    for (int c = kWsStages; c < C; ++c) {
+      const int cp = c - kWsStages;   // the chunk that last used stage c % kWsStages
+      if (!wait_bounded(&empty[cp % kWsStages], (cp / kWsStages) & 1)) {
         dead = true;
         break;
       }
@@ -991,48 +1007,46 @@ sparse_prefill_ws_kernel(Params p) {
       ncopy = c + 1;
     }
     // Every copy issued lands before shared memory is released.
-    for (int c = max(0, ncopy - 2); c < ncopy; ++c) wait_bounded(&full[c & 1], (c >> 1) & 1);
+    for (int c = max(0, ncopy - kWsStages); c < ncopy; ++c)
+      wait_bounded(&full[c % kWsStages], (c / kWsStages) & 1);
   }
 
-  // ---- MMA issue (the MMA warp; one elected lane issues) -----------------------
-  // S(c) once K(c) is dequantised and softmax(c - SB) has loaded S buffer
-  // c % SB; O(c - 1) once P(c - 1) and V(c - 1) are ready.  The whole warp
-  // runs the loop so descriptors stay warp-uniform; waits probe both of their
-  // barriers before blocking on either.
+  // ---- MMA issue (one warp per tile; one elected lane issues) -----------------
+  // S(c) once K(c) is dequantised and the tile's softmax(c - SB) has loaded
+  // S buffer c % SB; O(c - 1) once P(c - 1) and V(c - 1) are ready.  The
+  // whole warp runs the loop so descriptors stay warp-uniform; waits probe
+  // both of their barriers before blocking on either.
   if (mmaw) {
+    const int t = mt;
     const uint32_t id_s = f16_idesc(128, kTok), id_o = f16_idesc(128, D);
-    uint64_t dq[NTL];
-#pragma unroll
-    for (int t = 0; t < NTL; ++t) dq[t] = sw128_desc(smem_u32(sQ(t)));
+    const uint64_t dq = sw128_desc(smem_u32(sQ(t)));
     const uint64_t dk0 = sw128_desc(smem_u32(sK(0))), dk1 = sw128_desc(smem_u32(sK(1)));
     const uint64_t dv0 = sw128_desc(smem_u32(sV(0))), dv1 = sw128_desc(smem_u32(sV(1)));
-    auto issue_s = [&](int c) {   // every tile's S(c); S buffer and K tile commits
+    auto issue_s = [&](int c) {   // the tile's S(c); then its S buffer and K tile x commits
       const int x = c & 1;
       const uint64_t dk = x ? dk1 : dk0;
 #pragma unroll
-      for (int t = 0; t < NTL; ++t)
+      for (int h = 0; h < D / 64; ++h)
 #pragma unroll
-        for (int h = 0; h < D / 64; ++h)
-#pragma unroll
-          for (int ks2 = 0; ks2 < 4; ++ks2)
-            mma_f16_elect(tS(t, c), dq[t] + (uint64_t)((h * 16384 + 32 * ks2) >> 4),
-                          dk + (uint64_t)((h * T::kKBlk + 32 * ks2) >> 4), id_s,
-                          (h | ks2) ? 1u : 0u);
-      mma_commit_elect(&barS[c % SB]);
+        for (int ks2 = 0; ks2 < 4; ++ks2)
+          mma_f16_elect(tS(t, c), dq + (uint64_t)((h * 16384 + 32 * ks2) >> 4),
+                        dk + (uint64_t)((h * T::kKBlk + 32 * ks2) >> 4), id_s,
+                        (h | ks2) ? 1u : 0u);
+      mma_commit_elect(&barS[t * SB + c % SB]);
       mma_commit_elect(&kfree[x]);
     };
-    // Every tile's O += P(c) V(c): P from tensor memory (kTok / 16 steps of 16
-    // tokens, eight columns each), V^T from shared memory; then one commit.
+    // The tile's O += P(c) V(c): P from tensor memory (kTok / 16 steps of 16
+    // tokens, eight columns each), V^T from shared memory; then the O and
+    // V^T tile x commits.
     auto issue_o = [&](int c) {
       const int x = c & 1;
       const uint64_t dv = x ? dv1 : dv0;
 #pragma unroll
-      for (int t = 0; t < NTL; ++t)
-#pragma unroll
-        for (int ks2 = 0; ks2 < kTok / 16; ++ks2)
-          mma_f16_ts_elect(tO(t), tP(t, x) + 8 * ks2, dv + (uint64_t)((32 * ks2) >> 4), id_o,
-                           (c | ks2) ? 1u : 0u);
-      mma_commit_elect(&barO[x]);
+      for (int ks2 = 0; ks2 < kTok / 16; ++ks2)
+        mma_f16_ts_elect(tO(t), tP(t, x) + 8 * ks2, dv + (uint64_t)((32 * ks2) >> 4), id_o,
+                         (c | ks2) ? 1u : 0u);
+      mma_commit_elect(&barO[t * 2 + x]);
+      mma_commit_elect(&vfree[x]);
     };
     auto wait_pair = [&](uint64_t* b1, uint32_t p1, bool two, uint64_t* b2, uint32_t p2) {
       const bool r1 = mbar_try_wait(b1, p1);
@@ -1040,33 +1054,32 @@ sparse_prefill_ws_kernel(Params p) {
       const bool ok = (r1 || wait_bounded(b1, p1)) && (r2 || wait_bounded(b2, p2));
       return __all_sync(0xffffffffu, ok);
     };
-    int ns = 0, no = 0;
     for (int c = 0; c <= C; ++c) {
       if (c < C) {
         const int cf = max(c - SB, 0);   // the chunk whose S buffer S(c) reuses
-        if (!wait_pair(&kready[c & 1], (c >> 1) & 1, c >= SB, &sfree[cf % SB], (cf / SB) & 1)) {
+        if (!wait_pair(&kready[c & 1], (c >> 1) & 1, c >= SB, &sfree[t * SB + cf % SB],
+                       (cf / SB) & 1)) {
           dead = true;
           break;
         }
         tc_fence_after();
         issue_s(c);
-        ns = c + 1;
       }
       if (c >= 1) {
         const int o = c - 1;
-        if (!wait_pair(&pready[o & 1], (o >> 1) & 1, true, &vready[o & 1], (o >> 1) & 1)) {
+        if (!wait_pair(&vready[o & 1], (o >> 1) & 1, true, &pready[t * 2 + (o & 1)],
+                       (o >> 1) & 1)) {
           dead = true;
           break;
         }
         tc_fence_after();
         issue_o(o);
-        no = o + 1;
       }
     }
-    // Every MMA issued completes before the tiles and tensor memory are read
-    // or released (at once when nothing went wrong).
-    for (int c = max(0, ns - 2); c < ns; ++c) wait_bounded(&kfree[c & 1], (c >> 1) & 1);
-    for (int c = max(0, no - 2); c < no; ++c) wait_bounded(&barO[c & 1], (c >> 1) & 1);
+    // Every MMA this warp issued completes before the tiles and tensor memory
+    // are read or released (at once when nothing went wrong).
+    mma_commit_elect(&mdone[t]);
+    wait_bounded(&mdone[t], 0);
     __syncwarp();
   }
 
@@ -1074,12 +1087,18 @@ sparse_prefill_ws_kernel(Params p) {
   if (deq) {
     const int dt = tid - 128 * NTL, dw = warp - 4 * NTL;
     for (int c = 0; c < C; ++c) {
-      const int x = c & 1;
-      const uint8_t* st = sStage + x * kStage;
-      // Warp-uniform give-ups (the warp syncs below).
-      if (__any_sync(0xffffffffu, !wait_bounded(&full[x], (c >> 1) & 1) ||
-                                      (c >= 2 && !wait_bounded(&kfree[x], ((c - 2) >> 1) & 1)))) {
-        dead = true;   // (kfree: S(c - 2) has read K tile x)
+      const int x = c & 1, z = c % kWsStages;
+      const uint8_t* st = sStage + z * kStage;
+      // First probes of the stage, the K tile and the V^T tile overlap; then
+      // warp-uniform give-ups (the warp syncs below).  kfree / vfree: every
+      // S(c - 2) / O(c - 2) has read tile x.
+      const bool f_now = mbar_try_wait(&full[z], (c / kWsStages) & 1);
+      const bool k_now = c < 2 || mbar_try_wait(&kfree[x], ((c - 2) >> 1) & 1);
+      const bool v_now = c < 2 || mbar_try_wait(&vfree[x], ((c - 2) >> 1) & 1);
+      if (__any_sync(0xffffffffu,
+                     !((f_now || wait_bounded(&full[z], (c / kWsStages) & 1)) &&
+                       (k_now || wait_bounded(&kfree[x], ((c - 2) >> 1) & 1))))) {
+        dead = true;
         break;
       }
       {
@@ -1098,9 +1117,8 @@ sparse_prefill_ws_kernel(Params p) {
       }
       fence_proxy_async_smem();
       ws_arrive(&kready[x]);
-      if (c >= 2 &&
-          __any_sync(0xffffffffu, !wait_bounded(&barO[x], ((c - 2) >> 1) & 1))) {
-        dead = true;   // (O(c - 2) has read V^T tile x)
+      if (__any_sync(0xffffffffu, !(v_now || wait_bounded(&vfree[x], ((c - 2) >> 1) & 1)))) {
+        dead = true;
         break;
       }
       {
@@ -1143,7 +1161,7 @@ sparse_prefill_ws_kernel(Params p) {
       fence_proxy_async_smem();
       ws_arrive(&vready[x]);
       __syncwarp();
-      if (lane == 0) ws_arrive(&empty[x]);   // this warp is done with the stage
+      if (lane == 0) ws_arrive(&empty[z]);   // this warp is done with the stage
     }
   }
 
@@ -1158,9 +1176,10 @@ sparse_prefill_ws_kernel(Params p) {
       const int ue = s_union[u];
       // First probes of S(c) and of O(c - 2) (P buffer x free) overlap; then a
       // warp-uniform give-up (tensor-memory loads and stores are warp-wide).
-      const bool s_now = mbar_try_wait(&barS[c % SB], (c / SB) & 1);
-      const bool p_now = c < 2 || mbar_try_wait(&barO[x], ((c - 2) >> 1) & 1);
-      if (__any_sync(0xffffffffu, !(s_now || wait_bounded(&barS[c % SB], (c / SB) & 1)))) {
+      const bool s_now = mbar_try_wait(&barS[tt * SB + c % SB], (c / SB) & 1);
+      const bool p_now = c < 2 || mbar_try_wait(&barO[tt * 2 + x], ((c - 2) >> 1) & 1);
+      if (__any_sync(0xffffffffu,
+                     !(s_now || wait_bounded(&barS[tt * SB + c % SB], (c / SB) & 1)))) {
         dead = true;
         break;
       }
@@ -1177,7 +1196,7 @@ sparse_prefill_ws_kernel(Params p) {
       }
       tmem_wait_ld();
       tc_fence_before();
-      ws_arrive(&sfree[c % SB]);   // S buffer loaded: S(c + SB) may overwrite it
+      ws_arrive(&sfree[tt * SB + c % SB]);   // S buffer loaded: S(c + SB) may overwrite it
       float cmax = -INFINITY;   // log2 units
       if (member) {
         if (tok0 + kTok > nrow) {
@@ -1226,7 +1245,8 @@ sparse_prefill_ws_kernel(Params p) {
         // O holds every chunk before c once O(c - 1) completed (O(c) waits for
         // this chunk's P); a warp rescales when any of its lanes must.
         if (c >= 1 &&
-            __any_sync(0xffffffffu, !wait_bounded(&barO[(c - 1) & 1], ((c - 1) >> 1) & 1))) {
+            __any_sync(0xffffffffu,
+                       !wait_bounded(&barO[tt * 2 + ((c - 1) & 1)], ((c - 1) >> 1) & 1))) {
           dead = true;
           break;
         }
@@ -1243,7 +1263,8 @@ sparse_prefill_ws_kernel(Params p) {
         tmem_wait_st();
       }
       // P buffer x is free once O(c - 2) completed.
-      if (__any_sync(0xffffffffu, !(p_now || wait_bounded(&barO[x], ((c - 2) >> 1) & 1)))) {
+      if (__any_sync(0xffffffffu,
+                     !(p_now || wait_bounded(&barO[tt * 2 + x], ((c - 2) >> 1) & 1)))) {
         dead = true;
         break;
       }
@@ -1253,7 +1274,7 @@ sparse_prefill_ws_kernel(Params p) {
       for (int q = 0; q < kTok / 32; ++q) tmem_st16u(tP(tt, x) + lane_off + 16 * q, pk + 16 * q);
       tmem_wait_st();
       tc_fence_before();
-      ws_arrive(&pready[x]);   // P(c) written, O rescaled
+      ws_arrive(&pready[tt * 2 + x]);   // P(c) written, O rescaled
     }
   }
 
@@ -1322,7 +1343,7 @@ size_t prefill_ws_smem_bytes(const Geom& g, int k) {
   const int rows = prefill_ws_tiles(g) * prefill_rows_per_tile(g);   // rows per CTA
   const int ucap = min(g.MB, rows * k);
   const size_t tiles = g.D == 256 ? WT<256>::kTiles : WT<128>::kTiles;
-  return (size_t)1024 + tiles + 2 * kStage + kWsBars * 8 + 4 + 12 * 4 + (size_t)rows * k * 4 +
+  return (size_t)1024 + tiles + kWsStages * kStage + kWsBars * 8 + 4 + 12 * 4 + (size_t)rows * k * 4 +
          (size_t)ucap * 8 + (size_t)((g.MB + 31) / 32) * 8 + (size_t)rows * ws_member_words(ucap) * 4;
 }
 
