@@ -107,10 +107,23 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
+// The same for an MN-major operand: rows of 64 N-elements (128 B, swizzled)
+// along K in 8-row groups 1024 B apart; consecutive 64-element groups along
+// N `lbo` bytes apart.
+__device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;   // leading byte offset: along N
+  d |= (uint64_t)(1024 >> 4) << 32;              // stride byte offset: along K
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
 // Instruction descriptor, kind::f16: fp16 A and B (K-major), fp32 D, M x N.
 __host__ __device__ constexpr uint32_t f16_idesc(int m, int n) {
   return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
+constexpr uint32_t kIdescBMn = 1u << 16;   // instruction descriptor: B is MN-major
 
 __device__ __forceinline__ unsigned long long now_ns() {
   unsigned long long t;
@@ -710,22 +723,23 @@ sparse_prefill_kernel(Params p) {
 
 // ---------------------------------------------------------------------------
 // Warp-specialised row tiles.  Per query tile four softmax warps own its 128
-// tensor-memory lanes (queries, softmax, epilogue); four warps dequantise the
-// NVFP4 chunks into double-buffered fp16 K and V^T tiles in shared memory, and
-// one thread issues the bulk copies and the MMAs.  P goes from the softmax
-// into tensor memory (double-buffered) and feeds O += P V as the A operand
-// from there, so shared memory carries only the K and V^T operands.  S is
+// tensor-memory lanes (queries, softmax, epilogue) and one warp issues its
+// MMAs; ND warps dequantise the NVFP4 chunks into double-buffered fp16 K and
+// V tiles in shared memory (both with token rows), and one thread issues the
+// bulk copies.  P goes from the softmax into tensor memory (double-buffered)
+// and feeds O += P V as the A operand from there, with V as an MN-major B
+// operand, so shared memory carries only the K and V operands.  S is
 // double-buffered in tensor memory at head_dim 256 and single-buffered at
 // head_dim 128 (two tiles' O fill half of it); the softmax releases its S
 // buffer as soon as it has loaded S into registers.  For chunk c the softmax
 // of c, the dequantisation of c + 1 and the MMAs S(c + 1) and O(c - 1) overlap.
 // Hand-overs are mbarriers (all waits bounded):
 //   full[z]      copy of a chunk into stage z landed         (1 arrival + bytes)
-//   empty[z]     the dequant warps are done with stage z      (4 arrivals)
-//   kready[x]    K tile x written                             (128 arrivals)
-//   vready[x]    V^T tile x written                           (128 arrivals)
+//   empty[z]     the dequant warps are done with stage z      (ND arrivals)
+//   kready[x]    K tile x written                             (32 ND arrivals)
+//   vready[x]    V tile x written                             (32 ND arrivals)
 //   kfree[x]     every tile's S MMAs that read K tile x done  (commit)
-//   vfree[x]     every tile's O MMAs that read V^T tile x done (commit)
+//   vfree[x]     every tile's O MMAs that read V tile x done  (commit)
 //   barS[t][y]   S of tile t into its buffer y complete       (commit)
 //   sfree[t][y]  tile t's softmax has loaded S buffer y       (128 arrivals)
 //   pready[t][x] P buffer x of tile t written, O rescaled     (128 arrivals)
@@ -740,7 +754,7 @@ sparse_prefill_kernel(Params p) {
 // Tensor memory (512 columns): S buffers from column 0, then the P buffers
 // (kTok / 2 columns each: two fp16 per column), O of tile t at 256 + t D.
 constexpr int kWsStages = 4;   // NVFP4 chunk stages of the warp-specialised kernel
-constexpr int kWsBars = 30;    // its mbarriers
+constexpr int kWsBars = 31;    // its mbarriers
 
 // Words of a row's membership bitmap over the union (odd, so the rows of one
 // warp fall on different banks).
@@ -752,13 +766,13 @@ template <int D>
 struct WT {
   using T = PT<D>;
   static constexpr int kNtl = D == 128 ? 2 : 1;       // query tiles per CTA
-  static constexpr int kThreads = 160 * kNtl + 160;   // softmax, dequant, MMA, copy
+  static constexpr int kDeq = D == 128 ? 4 : 8;       // dequantisation warps
+  static constexpr int kThreads = 128 * kNtl + 32 * kDeq + 96;   // softmax, dequant, 2 MMA, copy
   static constexpr int kSBuf = D == 128 ? 1 : 2;      // S buffers per tile
   static constexpr uint32_t kPBase = kNtl * kSBuf * T::kTok;   // P of (t, x) after S
   static constexpr uint32_t kOBase = 256;             // O of tile t at kOBase + t * D
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr size_t kTiles =
-      (size_t)kNtl * T::kQBytes + 2 * ((size_t)T::kKBytes + T::kVBytes);
+  static constexpr size_t kTiles = (size_t)kNtl * T::kQBytes + 4 * (size_t)T::kKBytes;   // Q, K, V
   static_assert(kPBase + 2 * kNtl * T::kTok / 2 <= kOBase, "tensor-memory columns");
 };
 
@@ -778,10 +792,15 @@ sparse_prefill_ws_kernel(Params p) {
   const int r0 = tile * NTL * TR;             // first row of the CTA's tiles
   const int rows = min(NTL * TR, g.R - r0);   // rows of the CTA
   const int k = p.k;
-  const bool soft = warp < 4 * NTL, deq = warp >= 4 * NTL && warp < 4 * NTL + 4;
-  const bool mmaw = warp >= 4 * NTL + 4 && warp < 5 * NTL + 4;   // one MMA warp per tile
-  const int mt = warp - (4 * NTL + 4);                            // its tile
-  const bool cpy = warp == 5 * NTL + 4 && lane == 0;              // the copy thread
+  constexpr int ND = W::kDeq;
+  const bool soft = warp < 4 * NTL, deq = warp >= 4 * NTL && warp < 4 * NTL + ND;
+  // Two MMA warps: one per tile (S and O) with two tiles; with one tile, one
+  // issues S and the other O.
+  const bool mmaw = warp >= 4 * NTL + ND && warp < 4 * NTL + ND + 2;
+  const int mw = warp - (4 * NTL + ND);
+  const int mt = NTL == 2 ? mw : 0;                                 // its tile
+  const bool does_s = NTL == 2 || mw == 0, does_o = NTL == 2 || mw == 1;
+  const bool cpy = warp == 4 * NTL + ND + 2 && lane == 0;           // the copy thread
   const int tt = soft ? warp >> 2 : 0;        // a softmax thread's tile
   const int vi = tid & 127;                   // its query vector (tile row)
 
@@ -790,8 +809,8 @@ sparse_prefill_ws_kernel(Params p) {
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sQ0 = smem;                                  // [NTL][kQBytes]
   uint8_t* sK0 = sQ0 + NTL * T::kQBytes;                // [2][kKBytes]
-  uint8_t* sV0 = sK0 + 2 * T::kKBytes;                  // [2][kVBytes]
-  uint8_t* sStage = sV0 + 2 * T::kVBytes;               // [kWsStages][kStage]
+  uint8_t* sV0 = sK0 + 2 * T::kKBytes;                  // [2][kKBytes] (V in K's layout)
+  uint8_t* sStage = sV0 + 2 * T::kKBytes;               // [kWsStages][kStage]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + kWsStages * kStage);
   uint64_t* full = bars;                 // [kWsStages]
   uint64_t* empty = bars + 4;            // [kWsStages]
@@ -804,6 +823,7 @@ sparse_prefill_ws_kernel(Params p) {
   uint64_t* pready = bars + 20;          // [NTL][2]
   uint64_t* barO = bars + 24;            // [NTL][2]
   uint64_t* mdone = bars + 28;           // [NTL] every MMA of tile t's warp completed
+  uint64_t* qbar = bars + 30;            // the CTA's query rows landed
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + kWsBars);
   int* s_misc = reinterpret_cast<int*>(s_tmem + 1);            // [12]: warp counts, total
   int32_t* s_sel = s_misc + 12;                                 // [NTL * TR][k]
@@ -814,15 +834,20 @@ sparse_prefill_ws_kernel(Params p) {
   uint32_t* s_bits = reinterpret_cast<uint32_t*>(s_upage + p.ucap);   // [nwords]
   int* s_wpre = reinterpret_cast<int*>(s_bits + nwords);              // [nwords]
   uint32_t* s_mem = reinterpret_cast<uint32_t*>(s_wpre + nwords);     // [NTL * TR][mwords]
+  int32_t* s_pt = reinterpret_cast<int32_t*>(s_mem + NTL * TR * mwords);   // [MB] page row
+  // The CTA's query rows (bf16, [tile][vector][D]) land in the K and V tiles,
+  // which stay unused until the chunk loop.
+  uint8_t* sQst = sK0;
+  static_assert(NTL * 128 * D * 2 <= 4 * T::kKBytes, "query staging");
 
   if (tid == 0) {
     for (int z = 0; z < kWsStages; ++z) {
       mbar_init(&full[z], 1);
-      mbar_init(&empty[z], 4);
+      mbar_init(&empty[z], ND);
     }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&kready[x], 128);
-      mbar_init(&vready[x], 128);
+      mbar_init(&kready[x], 32 * ND);
+      mbar_init(&vready[x], 32 * ND);
       mbar_init(&kfree[x], NTL);   // one commit per MMA warp
       mbar_init(&vfree[x], NTL);
       mbar_init(&barS[x], 1);
@@ -834,6 +859,7 @@ sparse_prefill_ws_kernel(Params p) {
     }
     mbar_init(&mdone[0], 1);
     mbar_init(&mdone[1], 1);
+    mbar_init(qbar, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -842,8 +868,22 @@ sparse_prefill_ws_kernel(Params p) {
                  "r"(W::kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
+  bool dead = false;
+  __syncthreads();   // the barriers are initialised
 
-  // ---- the softmax warps' query vectors into the swizzled Q tiles ------------
+  // ---- the CTA's query rows: one bulk copy per row (its G heads, contiguous) ---
+  if (cpy) {
+    const uint32_t row_bytes = (uint32_t)(G * D * 2);
+    mbar_arrive_expect_tx(qbar, (uint32_t)rows * row_bytes);
+    for (int jr = 0; jr < rows; ++jr) {
+      const int t = jr / TR, jq = jr - t * TR;
+      const size_t qrow = ((size_t)b * g.R + r0 + jr) * g.Hq + (size_t)kvh * G;
+      bulk_g2s(sQst + ((size_t)t * 128 + (size_t)jq * G) * D * 2, p.q + qrow * D, row_bytes, qbar,
+               policy_evict_first());
+    }
+  }
+
+  // ---- the softmax warps' query vectors -----------------------------------------
   const int jj = tt * TR + vi / G, hh = vi % G; // row of the CTA, head
   const bool vec = soft && vi / G < TR && jj < rows;   // a real (row, head) vector
   const int j = r0 + jj;
@@ -851,44 +891,6 @@ sparse_prefill_ws_kernel(Params p) {
   const int cap = g.MB * g.P;
   const int nrow = vec ? visible_tokens(L, g.R, j, cap) : 0;
   float cq = 0.f;                               // logit scale, log2 domain
-  if (soft) {
-    const size_t qrow = ((size_t)b * g.R + j) * g.Hq + (size_t)kvh * G + hh;
-    const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow * D);
-    float amax = 0.f;
-    if (vec) {
-#pragma unroll 4
-      for (int i = 0; i < D / 8; ++i) {
-        const uint4 r = src[i];
-        const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          amax = fmaxf(amax, fabsf(__uint_as_float(w4[u] << 16)));
-          amax = fmaxf(amax, fabsf(__uint_as_float(w4[u] & 0xFFFF0000u)));
-        }
-      }
-    }
-    const int ebits = (int)((__float_as_uint(amax) >> 23) & 0xFF);
-    int sq = (amax > 0.f) ? 135 - ebits : 0;
-    sq = sq > 126 ? 126 : (sq < -126 ? -126 : sq);
-    const float up = __uint_as_float((uint32_t)(sq + 127) << 23);
-    const float down = __uint_as_float((uint32_t)(127 - sq) << 23);
-    cq = p.k_scale * p.sm_scale * kLog2e * down;
-#pragma unroll 4
-    for (int i = 0; i < D / 8; ++i) {
-      uint4 h = make_uint4(0u, 0u, 0u, 0u);
-      if (vec) {
-        const uint4 r = src[i];
-        const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          o[u] = pack_half2(__uint_as_float(w4[u] << 16) * up,
-                            __uint_as_float(w4[u] & 0xFFFF0000u) * up);
-        h = make_uint4(o[0], o[1], o[2], o[3]);
-      }
-      *reinterpret_cast<uint4*>(sQ0 + tt * T::kQBytes + (i >> 3) * 16384 + sw128(vi, i & 7)) = h;
-    }
-  }
   // ---- the tile's rows' selections and their union (softmax warps) ------------
   if (soft) {
     auto soft_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(128 * NTL) : "memory"); };
@@ -901,6 +903,7 @@ sparse_prefill_ws_kernel(Params p) {
       }
       s_sel[i] = v;
     }
+    for (int i = tid; i < g.MB; i += 128 * NTL) s_pt[i] = p.page_table[(size_t)b * g.MB + i];
     for (int i = tid; i < nwords; i += 128 * NTL) s_bits[i] = 0u;
     for (int i = tid; i < NTL * TR * mwords; i += 128 * NTL) s_mem[i] = 0u;
     soft_sync();
@@ -912,7 +915,7 @@ sparse_prefill_ws_kernel(Params p) {
     // Blocks with a valid page, ascending: thread t scans words [t*per, ...).
     const int per = (nwords + 128 * NTL - 1) / (128 * NTL);
     const int w0 = min(nwords, tid * per), w1 = min(nwords, w0 + per);
-    const int32_t* pt = p.page_table + (size_t)b * g.MB;
+    const int32_t* pt = s_pt;
     int cnt = 0;
     for (int w = w0; w < w1; ++w) {
       uint32_t m = s_bits[w];
@@ -956,6 +959,48 @@ sparse_prefill_ws_kernel(Params p) {
       if (QSA_IN_BOUNDS(u < p.ucap, kChkUnion))
         atomicOr(&s_mem[(i / k) * mwords + (u >> 5)], 1u << (u & 31));
     }
+
+    // The query vector: per-vector power-of-two scale into fp16 (the largest
+    // magnitude near 2^8), swizzled into the tile.  Lanes start at different
+    // 16-byte pieces of their rows, so the staging reads avoid bank conflicts.
+    if (__any_sync(0xffffffffu, !wait_bounded(qbar, 0))) dead = true;
+    const uint8_t* src = sQst + ((size_t)tt * 128 + vi) * D * 2;
+    float amax = 0.f;
+    if (vec && !dead) {
+#pragma unroll 4
+      for (int i = 0; i < D / 8; ++i) {
+        const int ii = (i + lane) & (D / 8 - 1);
+        const uint4 r = *reinterpret_cast<const uint4*>(src + ii * 16);
+        const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          amax = fmaxf(amax, fabsf(__uint_as_float(w4[u] << 16)));
+          amax = fmaxf(amax, fabsf(__uint_as_float(w4[u] & 0xFFFF0000u)));
+        }
+      }
+    }
+    const int ebits = (int)((__float_as_uint(amax) >> 23) & 0xFF);
+    int sq = (amax > 0.f) ? 135 - ebits : 0;
+    sq = sq > 126 ? 126 : (sq < -126 ? -126 : sq);
+    const float up = __uint_as_float((uint32_t)(sq + 127) << 23);
+    const float down = __uint_as_float((uint32_t)(127 - sq) << 23);
+    cq = p.k_scale * p.sm_scale * kLog2e * down;
+#pragma unroll 4
+    for (int i = 0; i < D / 8; ++i) {
+      const int ii = (i + lane) & (D / 8 - 1);
+      uint4 h = make_uint4(0u, 0u, 0u, 0u);
+      if (vec && !dead) {
+        const uint4 r = *reinterpret_cast<const uint4*>(src + ii * 16);
+        const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          o[u] = pack_half2(__uint_as_float(w4[u] << 16) * up,
+                            __uint_as_float(w4[u] & 0xFFFF0000u) * up);
+        h = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      *reinterpret_cast<uint4*>(sQ0 + tt * T::kQBytes + (ii >> 3) * 16384 + sw128(vi, ii & 7)) = h;
+    }
   }
   fence_proxy_async_smem();       // Q and zero tiles (generic stores) before the MMAs
   tc_fence_before();
@@ -971,8 +1016,7 @@ sparse_prefill_ws_kernel(Params p) {
   auto tP = [&](int t, int x) { return tmem + W::kPBase + (uint32_t)((2 * t + x) * (kTok / 2)); };
   auto sQ = [&](int t) { return sQ0 + t * T::kQBytes; };
   auto sK = [&](int x) { return sK0 + x * T::kKBytes; };
-  auto sV = [&](int x) { return sV0 + x * T::kVBytes; };
-  bool dead = false;
+  auto sV = [&](int x) { return sV0 + x * T::kKBytes; };
 
   // ---- bulk copies (lane 0 of the copy warp) ----------------------------------
   // Stage c % 4 is refilled with chunk c + 4 once the dequantisation warps
@@ -1009,19 +1053,22 @@ sparse_prefill_ws_kernel(Params p) {
     // Every copy issued lands before shared memory is released.
     for (int c = max(0, ncopy - kWsStages); c < ncopy; ++c)
       wait_bounded(&full[c % kWsStages], (c / kWsStages) & 1);
+    wait_bounded(qbar, 0);
   }
 
-  // ---- MMA issue (one warp per tile; one elected lane issues) -----------------
+  // ---- MMA issue (two warps; one elected lane of each issues) -----------------
   // S(c) once K(c) is dequantised and the tile's softmax(c - SB) has loaded
-  // S buffer c % SB; O(c - 1) once P(c - 1) and V(c - 1) are ready.  The
-  // whole warp runs the loop so descriptors stay warp-uniform; waits probe
-  // both of their barriers before blocking on either.
+  // S buffer c % SB; O(c) once P(c) and V(c) are ready.  The whole warp runs
+  // the loop so descriptors stay warp-uniform.
   if (mmaw) {
     const int t = mt;
-    const uint32_t id_s = f16_idesc(128, kTok), id_o = f16_idesc(128, D);
+    // S: Q (A) and K (B) K-major.  O: P from tensor memory, V (B) MN-major:
+    // 64-dim blocks kKBlk bytes apart, 8-token row groups 1024 bytes apart.
+    const uint32_t id_s = f16_idesc(128, kTok), id_o = f16_idesc(128, D) | kIdescBMn;
     const uint64_t dq = sw128_desc(smem_u32(sQ(t)));
     const uint64_t dk0 = sw128_desc(smem_u32(sK(0))), dk1 = sw128_desc(smem_u32(sK(1)));
-    const uint64_t dv0 = sw128_desc(smem_u32(sV(0))), dv1 = sw128_desc(smem_u32(sV(1)));
+    const uint64_t dv0 = sw128_mn_desc(smem_u32(sV(0)), T::kKBlk);
+    const uint64_t dv1 = sw128_mn_desc(smem_u32(sV(1)), T::kKBlk);
     auto issue_s = [&](int c) {   // the tile's S(c); then its S buffer and K tile x commits
       const int x = c & 1;
       const uint64_t dk = x ? dk1 : dk0;
@@ -1036,128 +1083,102 @@ sparse_prefill_ws_kernel(Params p) {
       mma_commit_elect(&kfree[x]);
     };
     // The tile's O += P(c) V(c): P from tensor memory (kTok / 16 steps of 16
-    // tokens, eight columns each), V^T from shared memory; then the O and
-    // V^T tile x commits.
+    // tokens, eight columns each), V from shared memory (16 token rows per
+    // step); then the O and V tile x commits.
     auto issue_o = [&](int c) {
       const int x = c & 1;
       const uint64_t dv = x ? dv1 : dv0;
 #pragma unroll
       for (int ks2 = 0; ks2 < kTok / 16; ++ks2)
-        mma_f16_ts_elect(tO(t), tP(t, x) + 8 * ks2, dv + (uint64_t)((32 * ks2) >> 4), id_o,
+        mma_f16_ts_elect(tO(t), tP(t, x) + 8 * ks2, dv + (uint64_t)((2048 * ks2) >> 4), id_o,
                          (c | ks2) ? 1u : 0u);
       mma_commit_elect(&barO[t * 2 + x]);
       mma_commit_elect(&vfree[x]);
     };
-    auto wait_pair = [&](uint64_t* b1, uint32_t p1, bool two, uint64_t* b2, uint32_t p2) {
-      const bool r1 = mbar_try_wait(b1, p1);
-      const bool r2 = !two || mbar_try_wait(b2, p2);
-      const bool ok = (r1 || wait_bounded(b1, p1)) && (r2 || wait_bounded(b2, p2));
-      return __all_sync(0xffffffffu, ok);
-    };
-    for (int c = 0; c <= C; ++c) {
-      if (c < C) {
-        const int cf = max(c - SB, 0);   // the chunk whose S buffer S(c) reuses
-        if (!wait_pair(&kready[c & 1], (c >> 1) & 1, c >= SB, &sfree[t * SB + cf % SB],
-                       (cf / SB) & 1)) {
-          dead = true;
-          break;
-        }
-        tc_fence_after();
-        issue_s(c);
+    // Each pass probes every barrier the next O and the next S wait on (the
+    // probes overlap), then issues O(no) and S(ns) if they are ready: O(no)
+    // needs V(no) and P(no); S(ns) needs K(ns) and the softmax's release of
+    // S buffer ns % SB.  Neither barrier can run a phase ahead of the waiter
+    // (each next phase needs an MMA this warp has not issued yet).
+    int ns = does_s ? 0 : C, no = does_o ? 0 : C;
+    unsigned long long spin0 = 0;
+    bool spinning = false;
+    while (no < C || ns < C) {
+      bool s_ok = false, o_ok = false;
+      if (ns < C) {
+        const int cf = max(ns - SB, 0);   // the chunk whose S buffer S(ns) reuses
+        const bool k_ok = mbar_test_wait(&kready[ns & 1], (ns >> 1) & 1);
+        const bool f_ok = ns < SB || mbar_test_wait(&sfree[t * SB + cf % SB], (cf / SB) & 1);
+        s_ok = k_ok && f_ok;
       }
-      if (c >= 1) {
-        const int o = c - 1;
-        if (!wait_pair(&vready[o & 1], (o >> 1) & 1, true, &pready[t * 2 + (o & 1)],
-                       (o >> 1) & 1)) {
-          dead = true;
-          break;
-        }
+      if (no < C && (no < ns || !does_s)) {   // (P(no) implies S(no) was issued)
+        const bool v_ok = mbar_test_wait(&vready[no & 1], (no >> 1) & 1);
+        const bool p_ok = mbar_test_wait(&pready[t * 2 + (no & 1)], (no >> 1) & 1);
+        o_ok = v_ok && p_ok;
+      }
+      o_ok = __all_sync(0xffffffffu, o_ok);
+      s_ok = __all_sync(0xffffffffu, s_ok);
+      if (o_ok || s_ok) {
         tc_fence_after();
-        issue_o(o);
+        if (o_ok) issue_o(no++);
+        if (s_ok) issue_s(ns++);
+        spinning = false;
+      } else if (!spinning) {
+        spin0 = now_ns();
+        spinning = true;
+      } else if (__any_sync(0xffffffffu, now_ns() - spin0 > kWaitNs)) {
+        dead = true;
+        break;
       }
     }
     // Every MMA this warp issued completes before the tiles and tensor memory
     // are read or released (at once when nothing went wrong).
-    mma_commit_elect(&mdone[t]);
-    wait_bounded(&mdone[t], 0);
+    mma_commit_elect(&mdone[mw]);
+    wait_bounded(&mdone[mw], 0);
     __syncwarp();
   }
 
-  // ---- dequantisation (warps 4-7) ----------------------------------------------
+  // ---- dequantisation (ND warps) -----------------------------------------------
+  // K and V alike: rows = tokens, D/64 blocks of 64 dims (128-byte swizzled
+  // rows); thread dt converts pieces of eight values (one code word, one
+  // scale).  K feeds S as a K-major B operand, V feeds O as an MN-major one.
   if (deq) {
-    const int dt = tid - 128 * NTL, dw = warp - 4 * NTL;
+    const int dt = tid - 128 * NTL;
+    constexpr int kPieces = kTok * D / 8 / (32 * ND);
+    auto rows_tile = [&](const uint8_t* codes, const uint8_t* scales, uint8_t* tile) {
+#pragma unroll
+      for (int i = 0; i < kPieces; ++i) {
+        const int pc = dt + 32 * ND * i;   // (token, 8-dim group)
+        const int t = pc / (D / 8), c8 = pc % (D / 8);
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(codes + t * (D / 2) + c8 * 4);
+        const uint32_t sc = e4m3x2_to_f16x2(scales[t * (D / 16) + (c8 >> 1)]);
+        *reinterpret_cast<uint4*>(tile + (c8 >> 3) * T::kKBlk + sw128(t, c8 & 7)) =
+            dequant8(w, prmt(sc, 0, 0x1010));
+      }
+    };
     for (int c = 0; c < C; ++c) {
       const int x = c & 1, z = c % kWsStages;
       const uint8_t* st = sStage + z * kStage;
-      // First probes of the stage, the K tile and the V^T tile overlap; then
+      // First probes of the stage, the K tile and the V tile overlap; then
       // warp-uniform give-ups (the warp syncs below).  kfree / vfree: every
       // S(c - 2) / O(c - 2) has read tile x.
-      const bool f_now = mbar_try_wait(&full[z], (c / kWsStages) & 1);
-      const bool k_now = c < 2 || mbar_try_wait(&kfree[x], ((c - 2) >> 1) & 1);
-      const bool v_now = c < 2 || mbar_try_wait(&vfree[x], ((c - 2) >> 1) & 1);
+      const bool f_now = mbar_test_wait(&full[z], (c / kWsStages) & 1);
+      const bool k_now = c < 2 || mbar_test_wait(&kfree[x], ((c - 2) >> 1) & 1);
+      const bool v_now = c < 2 || mbar_test_wait(&vfree[x], ((c - 2) >> 1) & 1);
       if (__any_sync(0xffffffffu,
                      !((f_now || wait_bounded(&full[z], (c / kWsStages) & 1)) &&
                        (k_now || wait_bounded(&kfree[x], ((c - 2) >> 1) & 1))))) {
         dead = true;
         break;
       }
-      {
-        // K rows = tokens (D/64 blocks of 64 dims), 8 pieces per thread.
-        const uint8_t* kc = st;
-        const uint8_t* ks = st + kTok * D;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int pc = dt + 128 * i;      // (token, 8-dim group)
-          const int t = pc / (D / 8), c8 = pc % (D / 8);
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(kc + t * (D / 2) + c8 * 4);
-          const uint32_t s = e4m3x2_to_f16x2(ks[t * (D / 16) + (c8 >> 1)]);
-          *reinterpret_cast<uint4*>(sK(x) + (c8 >> 3) * T::kKBlk + sw128(t, c8 & 7)) =
-              dequant8(w, prmt(s, 0, 0x1010));
-        }
-      }
+      rows_tile(st, st + kTok * D, sK(x));
       fence_proxy_async_smem();
       ws_arrive(&kready[x]);
       if (__any_sync(0xffffffffu, !(v_now || wait_bounded(&vfree[x], ((c - 2) >> 1) & 1)))) {
         dead = true;
         break;
       }
-      {
-        // V^T: 8 tokens x 8 dims per thread.  The eight lanes of each store
-        // phase take eight different token groups (the 16-byte chunk of the
-        // swizzled row), so the V^T stores are conflict-free; lanes of odd
-        // token groups read their token pairs in swapped order, which halves
-        // the read conflicts (token rows share banks every 128 bytes).
-        const uint8_t* vc = st + kTok * D / 2;
-        const uint8_t* vs = st + kTok * D + kTok * D / 16;
-        const int tg = D == 128 ? lane & 7 : lane & 3;
-        const int c8 = D == 128 ? (lane >> 3) + 4 * dw : (lane >> 2) + 8 * dw;
-        const int hw = D == 128 ? tg & 1 : 0;
-        uint32_t X[8], sf[8];   // X[u]: token 8*tg + (u ^ hw)
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int t = 8 * tg + (u ^ hw);
-          X[u] = *reinterpret_cast<const uint32_t*>(vc + t * (D / 2) + c8 * 4);
-          sf[u] = vs[t * (D / 16) + (c8 >> 1)];
-        }
-        uint32_t rowv[8][4];   // [dim e][token pair]
-#pragma unroll
-        for (int pr = 0; pr < 4; ++pr) {
-          const uint32_t x0 = hw ? X[2 * pr + 1] : X[2 * pr];
-          const uint32_t x1 = hw ? X[2 * pr] : X[2 * pr + 1];
-          const uint32_t f0 = hw ? sf[2 * pr + 1] : sf[2 * pr];
-          const uint32_t f1 = hw ? sf[2 * pr] : sf[2 * pr + 1];
-          const uint32_t s2 = e4m3x2_to_f16x2(f0 | (f1 << 8));
-          const uint32_t LO = (x0 & 0x0F0F0F0Fu) | ((x1 << 4) & 0xF0F0F0F0u);
-          const uint32_t HI = ((x0 >> 4) & 0x0F0F0F0Fu) | (x1 & 0xF0F0F0F0u);
-          const uint4 el = dequant8(LO, s2), od = dequant8(HI, s2);
-          rowv[0][pr] = el.x; rowv[2][pr] = el.y; rowv[4][pr] = el.z; rowv[6][pr] = el.w;
-          rowv[1][pr] = od.x; rowv[3][pr] = od.y; rowv[5][pr] = od.z; rowv[7][pr] = od.w;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          *reinterpret_cast<uint4*>(sV(x) + sw128(8 * c8 + e, tg)) =
-              make_uint4(rowv[e][0], rowv[e][1], rowv[e][2], rowv[e][3]);
-      }
+      rows_tile(st + kTok * D / 2, st + kTok * D + kTok * D / 16, sV(x));
       fence_proxy_async_smem();
       ws_arrive(&vready[x]);
       __syncwarp();
@@ -1176,8 +1197,8 @@ sparse_prefill_ws_kernel(Params p) {
       const int ue = s_union[u];
       // First probes of S(c) and of O(c - 2) (P buffer x free) overlap; then a
       // warp-uniform give-up (tensor-memory loads and stores are warp-wide).
-      const bool s_now = mbar_try_wait(&barS[tt * SB + c % SB], (c / SB) & 1);
-      const bool p_now = c < 2 || mbar_try_wait(&barO[tt * 2 + x], ((c - 2) >> 1) & 1);
+      const bool s_now = mbar_test_wait(&barS[tt * SB + c % SB], (c / SB) & 1);
+      const bool p_now = c < 2 || mbar_test_wait(&barO[tt * 2 + x], ((c - 2) >> 1) & 1);
       if (__any_sync(0xffffffffu,
                      !(s_now || wait_bounded(&barS[tt * SB + c % SB], (c / SB) & 1)))) {
         dead = true;
@@ -1344,7 +1365,8 @@ size_t prefill_ws_smem_bytes(const Geom& g, int k) {
   const int ucap = min(g.MB, rows * k);
   const size_t tiles = g.D == 256 ? WT<256>::kTiles : WT<128>::kTiles;
   return (size_t)1024 + tiles + kWsStages * kStage + kWsBars * 8 + 4 + 12 * 4 + (size_t)rows * k * 4 +
-         (size_t)ucap * 8 + (size_t)((g.MB + 31) / 32) * 8 + (size_t)rows * ws_member_words(ucap) * 4;
+         (size_t)ucap * 8 + (size_t)((g.MB + 31) / 32) * 8 + (size_t)rows * ws_member_words(ucap) * 4 +
+         (size_t)g.MB * 4;
 }
 
 cudaError_t launch_sparse_prefill(const Geom& g, const void* q, const uint8_t* k_pool,
