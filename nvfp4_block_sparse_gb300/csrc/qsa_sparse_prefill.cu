@@ -165,6 +165,12 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b,
 // column j as the elements 2j (low half) and 2j + 1.
 // The same MMAs issued by one elected lane of a converged warp (warp-uniform
 // operands), and their commit from that lane.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ void mma_f16_elect(uint32_t d_tmem, uint64_t a, uint64_t b,
                                               uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -766,7 +772,7 @@ template <int D>
 struct WT {
   using T = PT<D>;
   static constexpr int kNtl = D == 128 ? 2 : 1;       // query tiles per CTA
-  static constexpr int kDeq = D == 128 ? 4 : 8;       // dequantisation warps
+  static constexpr int kDeq = D == 128 ? 4 : 8;       // dequantisation warps (registers)
   static constexpr int kThreads = 128 * kNtl + 32 * kDeq + 96;   // softmax, dequant, 2 MMA, copy
   static constexpr int kSBuf = D == 128 ? 1 : 2;      // S buffers per tile
   static constexpr uint32_t kPBase = kNtl * kSBuf * T::kTok;   // P of (t, x) after S
@@ -1225,16 +1231,14 @@ sparse_prefill_ws_kernel(Params p) {
           for (int i = 0; i < kTok; ++i)
             if (tok0 + i >= nrow) z[i] = -INFINITY;
         }
-        float mx8[8];
+        float mx8[8];   // three-input maxima: eight running maxima, then a tree
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx8[i] = z[i];
 #pragma unroll
-        for (int i = 8; i < kTok; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], z[i]);
-#pragma unroll
-        for (int h = 4; h >= 1; h >>= 1)
-#pragma unroll
-          for (int i = 0; i < h; ++i) mx8[i] = fmaxf(mx8[i], mx8[i + h]);
-        cmax = mx8[0] * cq;     // cq > 0: the scale keeps the order
+        for (int i = 8; i < kTok; i += 2) mx8[(i >> 1) & 7] = fmax3(mx8[(i >> 1) & 7], z[i], z[i + 1]);
+        const float m3 = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                               fmaxf(mx8[6], mx8[7]));
+        cmax = m3 * cq;     // cq > 0: the scale keeps the order
       }
       bool rescale = false;
       float alpha = 1.f;
@@ -1246,21 +1250,6 @@ sparse_prefill_ws_kernel(Params p) {
           m_base = cmax;
           rescale = true;
         }
-      }
-      uint32_t pk[kTok / 2];
-      if (member) {
-        float ls4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int i = 0; i < kTok / 2; ++i) {
-          const float p0 = exp2_approx(fmaf(z[2 * i], cq, -m_base));
-          const float p1 = exp2_approx(fmaf(z[2 * i + 1], cq, -m_base));
-          ls4[i & 3] += p0 + p1;
-          pk[i] = pack_half2(p0, p1);
-        }
-        l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
-      } else {
-#pragma unroll
-        for (int i = 0; i < kTok / 2; ++i) pk[i] = 0u;
       }
       if (__any_sync(0xffffffffu, rescale)) {
         // O holds every chunk before c once O(c - 1) completed (O(c) waits for
@@ -1290,9 +1279,27 @@ sparse_prefill_ws_kernel(Params p) {
         break;
       }
       tc_fence_after();
-      // This lane's P row: token pair i in column i (the A-operand layout).
+      // This lane's P row, 32 tokens at a time: token pair i in column i (the
+      // A-operand layout); the row sum from the same fp32 values.
+      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int q = 0; q < kTok / 32; ++q) tmem_st16u(tP(tt, x) + lane_off + 16 * q, pk + 16 * q);
+      for (int q = 0; q < kTok / 32; ++q) {
+        uint32_t pk[16];
+        if (member) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = exp2_approx(fmaf(z[32 * q + 2 * i], cq, -m_base));
+            const float p1 = exp2_approx(fmaf(z[32 * q + 2 * i + 1], cq, -m_base));
+            ls4[i & 3] += p0 + p1;
+            pk[i] = pack_half2(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = 0u;
+        }
+        tmem_st16u(tP(tt, x) + lane_off + 16 * q, pk);
+      }
+      if (member) l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
       tmem_wait_st();
       tc_fence_before();
       ws_arrive(&pready[tt * 2 + x]);   // P(c) written, O rescaled
