@@ -900,16 +900,33 @@ sparse_prefill_ws_kernel(Params p) {
   // ---- the tile's rows' selections and their union (softmax warps) ------------
   if (soft) {
     auto soft_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(128 * NTL) : "memory"); };
-    for (int i = tid; i < NTL * TR * k; i += 128 * NTL) {
-      const int jr = i / k;
-      int v = -1;
-      if (jr < rows) {
-        v = p.sel[((size_t)b * g.R + r0 + jr) * k + (i - jr * k)];
-        if (v < 0 || v >= g.MB) v = -1;
+    // Selections and the page-table row, eight loads in flight per thread.
+    constexpr int kNs = 128 * NTL, kLd = 8;
+    for (int i0 = tid; i0 < NTL * TR * k; i0 += kLd * kNs) {
+      int v[kLd];
+#pragma unroll
+      for (int u = 0; u < kLd; ++u) {
+        const int i = i0 + u * kNs, jr = i / k;
+        v[u] = (i < NTL * TR * k && jr < rows) ? p.sel[((size_t)b * g.R + r0 + jr) * k + (i - jr * k)]
+                                                : -1;
       }
-      s_sel[i] = v;
+#pragma unroll
+      for (int u = 0; u < kLd; ++u) {
+        const int i = i0 + u * kNs;
+        if (i < NTL * TR * k) s_sel[i] = (v[u] < 0 || v[u] >= g.MB) ? -1 : v[u];
+      }
     }
-    for (int i = tid; i < g.MB; i += 128 * NTL) s_pt[i] = p.page_table[(size_t)b * g.MB + i];
+    for (int i0 = tid; i0 < g.MB; i0 += kLd * kNs) {
+      int v[kLd];
+#pragma unroll
+      for (int u = 0; u < kLd; ++u) {
+        const int i = i0 + u * kNs;
+        v[u] = i < g.MB ? p.page_table[(size_t)b * g.MB + i] : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < kLd; ++u)
+        if (i0 + u * kNs < g.MB) s_pt[i0 + u * kNs] = v[u];
+    }
     for (int i = tid; i < nwords; i += 128 * NTL) s_bits[i] = 0u;
     for (int i = tid; i < NTL * TR * mwords; i += 128 * NTL) s_mem[i] = 0u;
     soft_sync();
