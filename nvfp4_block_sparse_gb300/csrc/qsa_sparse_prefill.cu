@@ -844,6 +844,7 @@ sparse_prefill_ws_kernel(Params p) {
   // The CTA's query rows (bf16, [tile][vector][D]) land in the K and V tiles,
   // which stay unused until the chunk loop.
   uint8_t* sQst = sK0;
+  float* s_cq = reinterpret_cast<float*>(s_pt + g.MB);   // [NTL * 128] logit scales
   static_assert(NTL * 128 * D * 2 <= 4 * T::kKBytes, "query staging");
 
   if (tid == 0) {
@@ -982,47 +983,64 @@ sparse_prefill_ws_kernel(Params p) {
       if (QSA_IN_BOUNDS(u < p.ucap, kChkUnion))
         atomicOr(&s_mem[(i / k) * mwords + (u >> 5)], 1u << (u & 31));
     }
+  }
 
-    // The query vector: per-vector power-of-two scale into fp16 (the largest
-    // magnitude near 2^8), swizzled into the tile.  Lanes start at different
-    // 16-byte pieces of their rows, so the staging reads avoid bank conflicts.
-    if (__any_sync(0xffffffffu, !wait_bounded(qbar, 0))) dead = true;
-    const uint8_t* src = sQst + ((size_t)tt * 128 + vi) * D * 2;
-    float amax = 0.f;
-    if (vec && !dead) {
+  // ---- the query vectors into the swizzled fp16 Q tiles ------------------------
+  // By the dequantisation warps (idle until the chunk loop) while the softmax
+  // warps build the union: a per-vector power-of-two scale (the largest
+  // magnitude near 2^8), with one or two threads per vector.  Lanes start at
+  // different 16-byte pieces of their rows, so the staging reads avoid bank
+  // conflicts.
+  if (deq) {
+    const int dt = tid - 128 * NTL;
+    constexpr int kNv = NTL * 128;                       // the CTA's vectors
+    constexpr int kGs = 32 * ND >= 2 * kNv ? 2 : 1;      // threads per vector
+    constexpr int kPer = D / 8 / kGs;                    // 16-byte pieces per thread
+    constexpr int kStride = 32 * ND / kGs;
+    const bool qok = __all_sync(0xffffffffu, wait_bounded(qbar, 0));
+    if (!qok) dead = true;
+    const int half = dt % kGs;
+    for (int v = dt / kGs; v < kNv; v += kStride) {
+      const int t = v >> 7, vv = v & 127, jr = t * TR + vv / G;
+      const bool valid = qok && vv / G < TR && jr < rows;
+      const uint8_t* src = sQst + (size_t)v * D * 2;
+      float amax = 0.f;
+      if (valid) {
 #pragma unroll 4
-      for (int i = 0; i < D / 8; ++i) {
-        const int ii = (i + lane) & (D / 8 - 1);
-        const uint4 r = *reinterpret_cast<const uint4*>(src + ii * 16);
-        const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+        for (int i = 0; i < kPer; ++i) {
+          const int ii = half * kPer + ((i + lane) & (kPer - 1));
+          const uint4 r = *reinterpret_cast<const uint4*>(src + ii * 16);
+          const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          amax = fmaxf(amax, fabsf(__uint_as_float(w4[u] << 16)));
-          amax = fmaxf(amax, fabsf(__uint_as_float(w4[u] & 0xFFFF0000u)));
+          for (int u = 0; u < 4; ++u) {
+            amax = fmaxf(amax, fabsf(__uint_as_float(w4[u] << 16)));
+            amax = fmaxf(amax, fabsf(__uint_as_float(w4[u] & 0xFFFF0000u)));
+          }
         }
       }
-    }
-    const int ebits = (int)((__float_as_uint(amax) >> 23) & 0xFF);
-    int sq = (amax > 0.f) ? 135 - ebits : 0;
-    sq = sq > 126 ? 126 : (sq < -126 ? -126 : sq);
-    const float up = __uint_as_float((uint32_t)(sq + 127) << 23);
-    const float down = __uint_as_float((uint32_t)(127 - sq) << 23);
-    cq = p.k_scale * p.sm_scale * kLog2e * down;
+      if (kGs == 2) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      const int ebits = (int)((__float_as_uint(amax) >> 23) & 0xFF);
+      int sq = (amax > 0.f) ? 135 - ebits : 0;
+      sq = sq > 126 ? 126 : (sq < -126 ? -126 : sq);
+      const float up = __uint_as_float((uint32_t)(sq + 127) << 23);
+      const float down = __uint_as_float((uint32_t)(127 - sq) << 23);
+      if (half == 0) s_cq[v] = valid ? p.k_scale * p.sm_scale * kLog2e * down : 0.f;
 #pragma unroll 4
-    for (int i = 0; i < D / 8; ++i) {
-      const int ii = (i + lane) & (D / 8 - 1);
-      uint4 h = make_uint4(0u, 0u, 0u, 0u);
-      if (vec && !dead) {
-        const uint4 r = *reinterpret_cast<const uint4*>(src + ii * 16);
-        const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
-        uint32_t o[4];
+      for (int i = 0; i < kPer; ++i) {
+        const int ii = half * kPer + ((i + lane) & (kPer - 1));
+        uint4 h = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) {
+          const uint4 r = *reinterpret_cast<const uint4*>(src + ii * 16);
+          const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+          uint32_t o[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          o[u] = pack_half2(__uint_as_float(w4[u] << 16) * up,
-                            __uint_as_float(w4[u] & 0xFFFF0000u) * up);
-        h = make_uint4(o[0], o[1], o[2], o[3]);
+          for (int u = 0; u < 4; ++u)
+            o[u] = pack_half2(__uint_as_float(w4[u] << 16) * up,
+                              __uint_as_float(w4[u] & 0xFFFF0000u) * up);
+          h = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        *reinterpret_cast<uint4*>(sQ0 + t * T::kQBytes + (ii >> 3) * 16384 + sw128(vv, ii & 7)) = h;
       }
-      *reinterpret_cast<uint4*>(sQ0 + tt * T::kQBytes + (ii >> 3) * 16384 + sw128(vi, ii & 7)) = h;
     }
   }
   fence_proxy_async_smem();       // Q and zero tiles (generic stores) before the MMAs
@@ -1031,6 +1049,7 @@ sparse_prefill_ws_kernel(Params p) {
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
   const int U = s_misc[10];
+  if (soft) cq = s_cq[tt * 128 + vi];
   const int csh = (g.P == 2 * kTok) ? 1 : 0;    // chunks per block: 1 << csh
   const int C = U << csh;
   const uint32_t* mymem = s_mem + (vec ? jj : 0) * mwords;
@@ -1390,7 +1409,7 @@ size_t prefill_ws_smem_bytes(const Geom& g, int k) {
   const size_t tiles = g.D == 256 ? WT<256>::kTiles : WT<128>::kTiles;
   return (size_t)1024 + tiles + kWsStages * kStage + kWsBars * 8 + 4 + 12 * 4 + (size_t)rows * k * 4 +
          (size_t)ucap * 8 + (size_t)((g.MB + 31) / 32) * 8 + (size_t)rows * ws_member_words(ucap) * 4 +
-         (size_t)g.MB * 4;
+         (size_t)g.MB * 4 + (size_t)prefill_ws_tiles(g) * 128 * 4;
 }
 
 cudaError_t launch_sparse_prefill(const Geom& g, const void* q, const uint8_t* k_pool,
