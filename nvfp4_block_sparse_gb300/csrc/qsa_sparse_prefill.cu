@@ -1250,14 +1250,16 @@ sparse_prefill_ws_kernel(Params p) {
       const int tok0 = ue * g.P + (c & csh) * kTok;
       const bool member = vec && tok0 < nrow && ((mword >> (u & 31)) & 1u);
       float z[kTok];
+      if (__any_sync(0xffffffffu, member)) {   // a warp with no member skips the load
 #pragma unroll
-      for (int q4 = 0; q4 < kTok / 16; ++q4) {
-        float v16[16];
-        tmem_ld16(tS(tt, c) + lane_off + 16 * q4, v16);
+        for (int q4 = 0; q4 < kTok / 16; ++q4) {
+          float v16[16];
+          tmem_ld16(tS(tt, c) + lane_off + 16 * q4, v16);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) z[16 * q4 + i] = v16[i];
+          for (int i = 0; i < 16; ++i) z[16 * q4 + i] = v16[i];
+        }
+        tmem_wait_ld();
       }
-      tmem_wait_ld();
       tc_fence_before();
       ws_arrive(&sfree[tt * SB + c % SB]);   // S buffer loaded: S(c + SB) may overwrite it
       float cmax = -INFINITY;   // log2 units
