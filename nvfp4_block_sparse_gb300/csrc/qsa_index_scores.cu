@@ -157,7 +157,7 @@ index_scores_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __restr
     // Next block's keys go out before this block is scored.
     int beta_n = g.MB, page_n = -1;
     bool live_n = false;
-    int4 kv_n[PIPE ? P / 8 : 1];
+    [[maybe_unused]] int4 kv_n[PIPE ? P / 8 : 1];
     if constexpr (PIPE) {
       if (it + 1 < blocks_per_warp) {
         live_n = block_of(it + 1, beta_n, page_n);
@@ -238,6 +238,17 @@ __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
 }
 
 // Four int8 -> two fp16 pairs (bytes 0,1 and bytes 2,3), exact.
+// Head-summed index weights up to this magnitude are exact fp16 integers,
+// and then every partial sum of a 64-dim dot product with int8 keys is an
+// integer below 2^24 (2047 * 128 * 64), exact in the fp32 accumulators: one
+// MMA per product and a float maximum.  Larger weights take the exact split
+// w = 128 a + b (two MMAs, integer combination per token).
+constexpr int kWholeMax = 2047;
+template <bool B>
+struct BoolTag {
+  static constexpr bool value = B;
+};
+
 __device__ __forceinline__ void s8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t u = w ^ 0x80808080u;                 // x + 128, as unsigned bytes
   const uint32_t bias = 0x64806480u;                  // fp16 pair (1152, 1152)
@@ -290,6 +301,7 @@ index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __r
   int4 kv[P / 8];
   if (live0) load_keys(page0, kv);
 
+  bool split = false;   // some |w| > kWholeMax: the exact two-part products
   // Head sums w[j][d], then the exact split w = 128*a + b.  Thread pair
   // (t >> 1) owns row j = t >> 5 and dims 4*d4..4*d4+3 (d4 = (t >> 1) & 15);
   // the two threads of a pair take alternate heads, 4-byte loads, up to 16
@@ -322,14 +334,18 @@ index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __r
     s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
     s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
     s3 += __shfl_xor_sync(0xffffffffu, s3, 1);
+    const int w4[4] = {s0, s1, s2, s3};
+    bool big = false;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) big |= w4[i] > kWholeMax || w4[i] < -kWholeMax;
+    split = __syncthreads_or(big) != 0;
     if (hs == 0) {
-      const int w4[4] = {s0, s1, s2, s3};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int w = w4[i];
         const int lo = ((w + 64) & 127) - 64;
-        wsplit[0][j][4 * d4 + i] = __int2half_rn((w - lo) / 128);
-        wsplit[1][j][4 * d4 + i] = __int2half_rn(lo);
+        wsplit[0][j][4 * d4 + i] = __int2half_rn(split ? (w - lo) / 128 : w);
+        if (split) wsplit[1][j][4 * d4 + i] = __int2half_rn(lo);
       }
     }
   }
@@ -340,7 +356,7 @@ index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __r
   // 16*tig + 4*kk + {0,1} / {2,3}.
   uint32_t bw[2][4][2];
 #pragma unroll
-  for (int q = 0; q < 2; ++q)
+  for (int q = 0; q < 2; ++q)   // (w[1] is unused without the split)
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const __half* src = &wsplit[q][gid][16 * tig + 4 * kk];
@@ -355,13 +371,15 @@ index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __r
     ncol[e] = (j < R) ? visible_tokens(L, R, j, cap) : 0;
   }
 
+  auto blocks = [&](auto split_tag) {
+  constexpr bool SPLIT = decltype(split_tag)::value;
   int beta = beta0, page = page0;
   bool live = live0;
   for (int it = 0; it < blocks_per_warp; ++it) {
     if (beta >= g.MB) break;
     int beta_n = g.MB, page_n = -1;
     bool live_n = false;
-    int4 kv_n[PIPE ? P / 8 : 1];
+    [[maybe_unused]] int4 kv_n[PIPE ? P / 8 : 1];
     if constexpr (PIPE) {
       if (it + 1 < blocks_per_warp) {
         live_n = block_of(it + 1, beta_n, page_n);
@@ -376,6 +394,7 @@ index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __r
       if (lane < RB && r0 + lane < R) dst[(size_t)lane * g.MB] = kSentinel;
     } else {
       int best[2] = {kSentinel, kSentinel};
+      float bestf[2] = {-INFINITY, -INFINITY};
 #pragma unroll
       for (int mt = 0; mt < P / 16; ++mt) {
         const int4 ka = kv[2 * mt], kb = kv[2 * mt + 1];   // tokens gid and gid + 8
@@ -388,23 +407,37 @@ index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __r
           s8x4_to_f16x2x2(wa[kk], a[0], a[2]);
           s8x4_to_f16x2x2(wb[kk], a[1], a[3]);
           mma_f16_16816(sa, a, bw[0][kk][0], bw[0][kk][1]);
-          mma_f16_16816(sb, a, bw[1][kk][0], bw[1][kk][1]);
+          if constexpr (SPLIT) mma_f16_16816(sb, a, bw[1][kk][0], bw[1][kk][1]);
         }
         const int tA = beta * P + 16 * mt + gid, tB = tA + 8;
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int vA = __float2int_rn(sa[e]) * 128 + __float2int_rn(sb[e]);
-          const int vB = __float2int_rn(sa[2 + e]) * 128 + __float2int_rn(sb[2 + e]);
-          if (tA < ncol[e]) best[e] = max(best[e], vA);
-          if (tB < ncol[e]) best[e] = max(best[e], vB);
+          if constexpr (SPLIT) {
+            const int vA = __float2int_rn(sa[e]) * 128 + __float2int_rn(sb[e]);
+            const int vB = __float2int_rn(sa[2 + e]) * 128 + __float2int_rn(sb[2 + e]);
+            if (tA < ncol[e]) best[e] = max(best[e], vA);
+            if (tB < ncol[e]) best[e] = max(best[e], vB);
+          } else {
+            if (tA < ncol[e]) bestf[e] = fmaxf(bestf[e], sa[e]);
+            if (tB < ncol[e]) bestf[e] = fmaxf(bestf[e], sa[2 + e]);
+          }
         }
       }
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        int v = best[e];
-        v = max(v, __shfl_xor_sync(0xffffffffu, v, 4));
-        v = max(v, __shfl_xor_sync(0xffffffffu, v, 8));
-        v = max(v, __shfl_xor_sync(0xffffffffu, v, 16));
+        int v;
+        if constexpr (SPLIT) {
+          v = best[e];
+          v = max(v, __shfl_xor_sync(0xffffffffu, v, 4));
+          v = max(v, __shfl_xor_sync(0xffffffffu, v, 8));
+          v = max(v, __shfl_xor_sync(0xffffffffu, v, 16));
+        } else {
+          float f = bestf[e];
+          f = fmaxf(f, __shfl_xor_sync(0xffffffffu, f, 4));
+          f = fmaxf(f, __shfl_xor_sync(0xffffffffu, f, 8));
+          f = fmaxf(f, __shfl_xor_sync(0xffffffffu, f, 16));
+          v = f == -INFINITY ? kSentinel : __float2int_rn(f);
+        }
         const int j = 2 * tig + e;
         if (gid == 0 && r0 + j < R) dst[(size_t)j * g.MB] = (beta * P < ncol[e]) ? v : kSentinel;
       }
@@ -420,6 +453,9 @@ index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __r
     }
   }
   (void)page;
+  };
+  if (split) blocks(BoolTag<true>{});
+  else blocks(BoolTag<false>{});
 }
 
 // ---- long row groups (R > 8): 64 rows per CTA ----------------------------
@@ -432,7 +468,7 @@ index_scores_mma_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __r
 constexpr int kGroupRows = 64;
 
 template <int P>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, P == 128 ? 1 : 2)
 index_scores_rows_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __restrict__ ik_pool,
                          const int32_t* __restrict__ page_table,
                          const int32_t* __restrict__ seqlens, int32_t* __restrict__ scores,
@@ -462,6 +498,7 @@ index_scores_rows_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __
     return page >= 0 && page < g.NP && beta * P < nmax;
   };
 
+  bool split = false;   // some |w| > kWholeMax: the exact two-part products
   {
     const int rr = threadIdx.x >> 2, part = threadIdx.x & 3;
     int acc[16];
@@ -493,18 +530,24 @@ index_scores_rows_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __
           for (int e = 0; e < 4; ++e) acc[4 * q + e] += (int)(int8_t)(w4[q] >> (8 * e));
       }
     }
+    bool big = false;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) big |= acc[i] > kWholeMax || acc[i] < -kWholeMax;
+    split = __syncthreads_or(big) != 0;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int w = acc[i];
       const int lo = ((w + 64) & 127) - 64;
-      wsplit[0][rr][16 * part + i] = __int2half_rn((w - lo) / 128);
-      wsplit[1][rr][16 * part + i] = __int2half_rn(lo);
+      wsplit[0][rr][16 * part + i] = __int2half_rn(split ? (w - lo) / 128 : w);
+      if (split) wsplit[1][rr][16 * part + i] = __int2half_rn(lo);
     }
   }
   __syncthreads();
   pdl_trigger();
 
   // This lane's columns in every group: rows r0 + 8*grp + 2*tig + e.
+  auto blocks = [&](auto split_tag) {
+  constexpr bool SPLIT = decltype(split_tag)::value;
   int beta = 0, page = -1;
   for (int it = 0; it < blocks_per_warp; ++it) {
     const bool live = block_of(it, beta, page);
@@ -539,7 +582,7 @@ index_scores_rows_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __
       if (r0 + jbase >= R) break;
       uint32_t bw[2][4][2];
 #pragma unroll
-      for (int q = 0; q < 2; ++q)
+      for (int q = 0; q < (SPLIT ? 2 : 1); ++q)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const __half* w = &wsplit[q][jbase + gid][16 * tig + 4 * kk];
@@ -553,34 +596,52 @@ index_scores_rows_kernel(Geom g, const int8_t* __restrict__ iq, const int8_t* __
         ncol[e] = (j < R) ? visible_tokens(L, R, j, cap) : 0;
       }
       int best[2] = {kSentinel, kSentinel};
+      float bestf[2] = {-INFINITY, -INFINITY};
 #pragma unroll
       for (int mt = 0; mt < P / 16; ++mt) {
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           mma_f16_16816(sa, af[mt][kk], bw[0][kk][0], bw[0][kk][1]);
-          mma_f16_16816(sb, af[mt][kk], bw[1][kk][0], bw[1][kk][1]);
+          if constexpr (SPLIT) mma_f16_16816(sb, af[mt][kk], bw[1][kk][0], bw[1][kk][1]);
         }
         const int tA = beta * P + 16 * mt + gid, tB = tA + 8;
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int vA = __float2int_rn(sa[e]) * 128 + __float2int_rn(sb[e]);
-          const int vB = __float2int_rn(sa[2 + e]) * 128 + __float2int_rn(sb[2 + e]);
-          if (tA < ncol[e]) best[e] = max(best[e], vA);
-          if (tB < ncol[e]) best[e] = max(best[e], vB);
+          if constexpr (SPLIT) {
+            const int vA = __float2int_rn(sa[e]) * 128 + __float2int_rn(sb[e]);
+            const int vB = __float2int_rn(sa[2 + e]) * 128 + __float2int_rn(sb[2 + e]);
+            if (tA < ncol[e]) best[e] = max(best[e], vA);
+            if (tB < ncol[e]) best[e] = max(best[e], vB);
+          } else {
+            if (tA < ncol[e]) bestf[e] = fmaxf(bestf[e], sa[e]);
+            if (tB < ncol[e]) bestf[e] = fmaxf(bestf[e], sa[2 + e]);
+          }
         }
       }
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        int v = best[e];
-        v = max(v, __shfl_xor_sync(0xffffffffu, v, 4));
-        v = max(v, __shfl_xor_sync(0xffffffffu, v, 8));
-        v = max(v, __shfl_xor_sync(0xffffffffu, v, 16));
+        int v;
+        if constexpr (SPLIT) {
+          v = best[e];
+          v = max(v, __shfl_xor_sync(0xffffffffu, v, 4));
+          v = max(v, __shfl_xor_sync(0xffffffffu, v, 8));
+          v = max(v, __shfl_xor_sync(0xffffffffu, v, 16));
+        } else {
+          float f = bestf[e];
+          f = fmaxf(f, __shfl_xor_sync(0xffffffffu, f, 4));
+          f = fmaxf(f, __shfl_xor_sync(0xffffffffu, f, 8));
+          f = fmaxf(f, __shfl_xor_sync(0xffffffffu, f, 16));
+          v = f == -INFINITY ? kSentinel : __float2int_rn(f);
+        }
         const int j = jbase + 2 * tig + e;
         if (gid == 0 && r0 + j < R) dst[(size_t)j * g.MB] = (beta * P < ncol[e]) ? v : kSentinel;
       }
     }
   }
+  };
+  if (split) blocks(BoolTag<true>{});
+  else blocks(BoolTag<false>{});
 }
 
 // Blocks each warp scores: one, unless the grid would exceed about
