@@ -144,6 +144,22 @@ def test_edge_cases(qsa, name):
     check_against_oracle(res, qw.to_numpy(w))
 
 
+@pytest.mark.parametrize("rows", [2, 4, 8])
+def test_index_large_head_sums(qsa, rows):
+    # The first request's rows at +-127 with one sign per (row, dim) for every
+    # head: head-summed weights of Hq * 127, beyond the single-product range of
+    # the tensor-core index kernel, so its CTAs take the exact two-part
+    # products while the other requests' CTAs take one product.
+    w = qw.make_workload(_case(rows_per_req=rows, num_q_heads=32, num_kv_heads=4), "cuda")
+    iq = w["iq"]
+    Di = iq.shape[-1]
+    gen = torch.Generator().manual_seed(11)
+    sign = torch.randint(0, 2, (rows, 1, Di), generator=gen) * 254 - 127
+    iq[:rows] = sign.to(torch.int8).to(iq.device).expand(-1, iq.shape[1], -1)
+    res = host(run_gpu(qsa, w))
+    check_against_oracle(res, qw.to_numpy(w))
+
+
 def test_all_pages_invalid(qsa):
     w = qw.make_workload(_case(rows_per_req=2), "cuda")
     w["page_table"].fill_(-1)

@@ -102,6 +102,26 @@ def test_prefill_matches_oracle(qsa, name):
     check(step, qw.to_numpy(w))
 
 
+def _saturate_iq(w, rows, seed):
+    """Index queries of the given rows at +-127 with one sign per (row, dim)
+    for every head: each head-summed weight is then Hq * 127 in magnitude,
+    beyond the single-product range of the tensor-core index kernels."""
+    iq = w["iq"]
+    Di = iq.shape[-1]
+    gen = torch.Generator().manual_seed(seed)
+    sign = torch.randint(0, 2, (len(rows), 1, Di), generator=gen) * 254 - 127
+    iq[rows] = sign.to(torch.int8).to(iq.device).expand(-1, iq.shape[1], -1)
+
+
+def test_prefill_large_head_sums(qsa):
+    # Rows 0-15 saturated (their 64-row group takes the exact two-part products),
+    # the next 64-row group left as drawn: both index paths in one step.
+    w = qw.make_workload(_case(rows_per_req=80, ctx_lo=4200, ctx_hi=4200, max_blocks=66), "cuda")
+    _saturate_iq(w, list(range(16)), 5)
+    step = run_step(qsa, w)
+    check(step, qw.to_numpy(w))
+
+
 def test_prefill_all_pages_invalid(qsa):
     w = qw.make_workload(_case(rows_per_req=20), "cuda")
     w["page_table"].fill_(-1)
