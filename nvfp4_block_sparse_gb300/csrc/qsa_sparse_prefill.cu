@@ -890,7 +890,7 @@ sparse_prefill_ws_kernel(Params p) {
     }
   }
 
-  // ---- the softmax warps' query vectors -----------------------------------------
+  // ---- each softmax thread's query vector: its row, head and visible tokens ----
   const int jj = tt * TR + vi / G, hh = vi % G; // row of the CTA, head
   const bool vec = soft && vi / G < TR && jj < rows;   // a real (row, head) vector
   const int j = r0 + jj;
@@ -1228,7 +1228,7 @@ sparse_prefill_ws_kernel(Params p) {
     }
   }
 
-  // ---- softmax (warps 0-3: thread = query vector = tensor-memory lane) ---------
+  // ---- softmax (four warps per tile: thread = query vector = tensor-memory lane)
   float m_base = -INFINITY, l_run = 0.f;
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
   if (soft) {
