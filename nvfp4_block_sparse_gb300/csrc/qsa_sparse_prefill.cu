@@ -1405,8 +1405,29 @@ size_t prefill_smem_bytes(const Geom& g, int k) {
 // four-warp kernel (single tiles) serves geometries where it does not fit.
 int prefill_ws_tiles(const Geom& g) { return g.D == 256 ? WT<256>::kNtl : WT<128>::kNtl; }
 
+// Rows per tile of the warp-specialised kernel (one CTA per SM): at most
+// 128 / G; among the heights down to half of that whose grid takes as many
+// waves as the tallest, the shortest, so that each CTA walks the smallest
+// union of selected blocks the wave count allows.
+int prefill_ws_rows_per_tile(const Geom& g) {
+  const int trmax = prefill_rows_per_tile(g);
+  if (trmax < 1) return trmax;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int ntl = prefill_ws_tiles(g);
+  auto waves = [&](int tr) {
+    const long long ctas = (long long)((g.R + ntl * tr - 1) / (ntl * tr)) * g.Hkv * g.B;
+    return (ctas + sms - 1) / sms;
+  };
+  const long long w0 = waves(trmax);
+  int tr = trmax;
+  while (tr - 1 >= (trmax + 1) / 2 && waves(tr - 1) == w0) --tr;
+  return tr;
+}
+
 size_t prefill_ws_smem_bytes(const Geom& g, int k) {
-  const int rows = prefill_ws_tiles(g) * prefill_rows_per_tile(g);   // rows per CTA
+  const int rows = prefill_ws_tiles(g) * prefill_ws_rows_per_tile(g);   // rows per CTA
   const int ucap = min(g.MB, rows * k);
   const size_t tiles = g.D == 256 ? WT<256>::kTiles : WT<128>::kTiles;
   return (size_t)1024 + tiles + kWsStages * kStage + kWsBars * 8 + 4 + 12 * 4 + (size_t)rows * k * 4 +
@@ -1426,8 +1447,6 @@ cudaError_t launch_sparse_prefill(const Geom& g, const void* q, const uint8_t* k
   prm.k_pool = k_pool; prm.k_sf = k_sf; prm.v_pool = v_pool; prm.v_sf = v_sf;
   prm.k_scale = k_scale; prm.v_scale = v_scale; prm.sm_scale = sm_scale;
   prm.page_table = page_table; prm.seqlens = seqlens; prm.sel = sel; prm.k = k;
-  prm.tr = prefill_rows_per_tile(g);
-  prm.ucap = min(g.MB, prm.tr * k);
   prm.out = reinterpret_cast<__nv_bfloat16*>(out);
   prm.lse = lse;
   prm.status = status;
@@ -1437,6 +1456,7 @@ cudaError_t launch_sparse_prefill(const Geom& g, const void* q, const uint8_t* k
   const bool ws = prefill_ws_smem_bytes(g, k) <= 227 * 1024;
 #endif
   const size_t smem = ws ? prefill_ws_smem_bytes(g, k) : prefill_smem_bytes(g, k);
+  prm.tr = ws ? prefill_ws_rows_per_tile(g) : prefill_rows_per_tile(g);
   const int rows_per_cta = (ws ? prefill_ws_tiles(g) : 1) * prm.tr;
   prm.ucap = min(g.MB, rows_per_cta * k);
   auto* kern = ws ? (g.D == 256 ? sparse_prefill_ws_kernel<256> : sparse_prefill_ws_kernel<128>)
