@@ -742,8 +742,8 @@ sparse_prefill_kernel(Params p) {
 // Hand-overs are mbarriers (all waits bounded):
 //   full[z]      copy of a chunk into stage z landed         (1 arrival + bytes)
 //   empty[z]     the dequant warps are done with stage z      (ND arrivals)
-//   kready[x]    K tile x written                             (32 ND arrivals)
-//   vready[x]    V tile x written                             (32 ND arrivals)
+//   kready[x]    K tile x written                             (its converting threads)
+//   vready[x]    V tile x written                             (its converting threads)
 //   kfree[x]     every tile's S MMAs that read K tile x done  (commit)
 //   vfree[x]     every tile's O MMAs that read V tile x done  (commit)
 //   barS[t][y]   S of tile t into its buffer y complete       (commit)
@@ -853,8 +853,8 @@ sparse_prefill_ws_kernel(Params p) {
       mbar_init(&empty[z], ND);
     }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&kready[x], 32 * ND);
-      mbar_init(&vready[x], 32 * ND);
+      mbar_init(&kready[x], ND >= 8 ? 16 * ND : 32 * ND);   // the threads converting K
+      mbar_init(&vready[x], ND >= 8 ? 16 * ND : 32 * ND);   // ... and V
       mbar_init(&kfree[x], NTL);   // one commit per MMA warp
       mbar_init(&vfree[x], NTL);
       mbar_init(&barS[x], 1);
@@ -1182,15 +1182,21 @@ sparse_prefill_ws_kernel(Params p) {
 
   // ---- dequantisation (ND warps) -----------------------------------------------
   // K and V alike: rows = tokens, D/64 blocks of 64 dims (128-byte swizzled
-  // rows); thread dt converts pieces of eight values (one code word, one
+  // rows); a thread converts pieces of eight values (one code word, one
   // scale).  K feeds S as a K-major B operand, V feeds O as an MN-major one.
+  // With eight warps, four convert K and four V, each group waiting only on
+  // its own tile's release; with four, every warp converts both.
   if (deq) {
     const int dt = tid - 128 * NTL;
-    constexpr int kPieces = kTok * D / 8 / (32 * ND);
+    constexpr bool kSplitKV = ND >= 8;
+    constexpr int kOpThreads = kSplitKV ? 16 * ND : 32 * ND;   // threads per operand
+    constexpr int kPieces = kTok * D / 8 / kOpThreads;
+    const bool do_k = !kSplitKV || dt < kOpThreads, do_v = !kSplitKV || dt >= kOpThreads;
+    const int ot = kSplitKV ? dt % kOpThreads : dt;            // thread within its operand
     auto rows_tile = [&](const uint8_t* codes, const uint8_t* scales, uint8_t* tile) {
 #pragma unroll
       for (int i = 0; i < kPieces; ++i) {
-        const int pc = dt + 32 * ND * i;   // (token, 8-dim group)
+        const int pc = ot + kOpThreads * i;   // (token, 8-dim group)
         const int t = pc / (D / 8), c8 = pc % (D / 8);
         const uint32_t w = *reinterpret_cast<const uint32_t*>(codes + t * (D / 2) + c8 * 4);
         const uint32_t sc = e4m3x2_to_f16x2(scales[t * (D / 16) + (c8 >> 1)]);
@@ -1205,24 +1211,28 @@ sparse_prefill_ws_kernel(Params p) {
       // warp-uniform give-ups (the warp syncs below).  kfree / vfree: every
       // S(c - 2) / O(c - 2) has read tile x.
       const bool f_now = mbar_test_wait(&full[z], (c / kWsStages) & 1);
-      const bool k_now = c < 2 || mbar_test_wait(&kfree[x], ((c - 2) >> 1) & 1);
-      const bool v_now = c < 2 || mbar_test_wait(&vfree[x], ((c - 2) >> 1) & 1);
+      const bool k_now = !do_k || c < 2 || mbar_test_wait(&kfree[x], ((c - 2) >> 1) & 1);
+      const bool v_now = !do_v || c < 2 || mbar_test_wait(&vfree[x], ((c - 2) >> 1) & 1);
       if (__any_sync(0xffffffffu,
                      !((f_now || wait_bounded(&full[z], (c / kWsStages) & 1)) &&
                        (k_now || wait_bounded(&kfree[x], ((c - 2) >> 1) & 1))))) {
         dead = true;
         break;
       }
-      rows_tile(st, st + kTok * D, sK(x));
-      fence_proxy_async_smem();
-      ws_arrive(&kready[x]);
-      if (__any_sync(0xffffffffu, !(v_now || wait_bounded(&vfree[x], ((c - 2) >> 1) & 1)))) {
-        dead = true;
-        break;
+      if (do_k) {
+        rows_tile(st, st + kTok * D, sK(x));
+        fence_proxy_async_smem();
+        ws_arrive(&kready[x]);
       }
-      rows_tile(st + kTok * D / 2, st + kTok * D + kTok * D / 16, sV(x));
-      fence_proxy_async_smem();
-      ws_arrive(&vready[x]);
+      if (do_v) {
+        if (__any_sync(0xffffffffu, !(v_now || wait_bounded(&vfree[x], ((c - 2) >> 1) & 1)))) {
+          dead = true;
+          break;
+        }
+        rows_tile(st + kTok * D / 2, st + kTok * D + kTok * D / 16, sV(x));
+        fence_proxy_async_smem();
+        ws_arrive(&vready[x]);
+      }
       __syncwarp();
       if (lane == 0) ws_arrive(&empty[z]);   // this warp is done with the stage
     }
