@@ -760,7 +760,7 @@ sparse_prefill_kernel(Params p) {
 // Tensor memory (512 columns): S buffers from column 0, then the P buffers
 // (kTok / 2 columns each: two fp16 per column), O of tile t at 256 + t D.
 constexpr int kWsStages = 4;   // NVFP4 chunk stages of the warp-specialised kernel
-constexpr int kWsBars = 31;    // its mbarriers
+constexpr int kWsBars = 32;    // its mbarriers
 
 // Words of a row's membership bitmap over the union (odd, so the rows of one
 // warp fall on different banks).
@@ -778,6 +778,12 @@ struct WT {
   static constexpr uint32_t kPBase = kNtl * kSBuf * T::kTok;   // P of (t, x) after S
   static constexpr uint32_t kOBase = 256;             // O of tile t at kOBase + t * D
   static constexpr uint32_t kTmemCols = 512;
+  // At head_dim 256 (one tile) Q also lives in tensor memory, so the S MMAs
+  // read only K from shared memory; at 128 two tiles' O leave no room.
+  static constexpr bool kQTmem = D == 256;
+  static constexpr uint32_t kQBase = 128;
+  static_assert(!kQTmem || (kPBase + 2 * kNtl * T::kTok / 2 <= kQBase && kQBase + D / 2 <= kOBase),
+                "tensor-memory columns for Q");
   static constexpr size_t kTiles = (size_t)kNtl * T::kQBytes + 4 * (size_t)T::kKBytes;   // Q, K, V
   static_assert(kPBase + 2 * kNtl * T::kTok / 2 <= kOBase, "tensor-memory columns");
 };
@@ -830,6 +836,7 @@ sparse_prefill_ws_kernel(Params p) {
   uint64_t* barO = bars + 24;            // [NTL][2]
   uint64_t* mdone = bars + 28;           // [NTL] every MMA of tile t's warp completed
   uint64_t* qbar = bars + 30;            // the CTA's query rows landed
+  uint64_t* qready = bars + 31;          // Q in tensor memory (head_dim 256)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + kWsBars);
   int* s_misc = reinterpret_cast<int*>(s_tmem + 1);            // [12]: warp counts, total
   int32_t* s_sel = s_misc + 12;                                 // [NTL * TR][k]
@@ -867,6 +874,7 @@ sparse_prefill_ws_kernel(Params p) {
     mbar_init(&mdone[0], 1);
     mbar_init(&mdone[1], 1);
     mbar_init(qbar, 1);
+    mbar_init(qready, 128 * NTL);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -1050,6 +1058,27 @@ sparse_prefill_ws_kernel(Params p) {
   const uint32_t tmem = *s_tmem;
   const int U = s_misc[10];
   if (soft) cq = s_cq[tt * 128 + vi];
+  if constexpr (W::kQTmem) {
+    // Each softmax thread copies its Q row (fp16, dims in order, two per
+    // column: the A-operand layout) into its tensor-memory lane.
+    if (soft) {
+      const uint32_t lane_q = (uint32_t)(32 * (warp & 3)) << 16;
+#pragma unroll
+      for (int q16 = 0; q16 < D / 32; ++q16) {   // 16 columns = 32 dims = 4 pieces
+        uint32_t v[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int pc = 4 * q16 + i;   // 8-dim piece
+          const uint4 r = *reinterpret_cast<const uint4*>(sQ0 + (pc >> 3) * 16384 + sw128(vi, pc & 7));
+          v[4 * i] = r.x; v[4 * i + 1] = r.y; v[4 * i + 2] = r.z; v[4 * i + 3] = r.w;
+        }
+        tmem_st16u(tmem + W::kQBase + lane_q + 16 * q16, v);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      ws_arrive(qready);
+    }
+  }
   const int csh = (g.P == 2 * kTok) ? 1 : 0;    // chunks per block: 1 << csh
   const int C = U << csh;
   const uint32_t* mymem = s_mem + (vec ? jj : 0) * mwords;
@@ -1117,10 +1146,15 @@ sparse_prefill_ws_kernel(Params p) {
 #pragma unroll
       for (int h = 0; h < D / 64; ++h)
 #pragma unroll
-        for (int ks2 = 0; ks2 < 4; ++ks2)
-          mma_f16_elect(tS(t, c), dq + (uint64_t)((h * 16384 + 32 * ks2) >> 4),
-                        dk + (uint64_t)((h * T::kKBlk + 32 * ks2) >> 4), id_s,
-                        (h | ks2) ? 1u : 0u);
+        for (int ks2 = 0; ks2 < 4; ++ks2) {
+          const uint64_t bk = dk + (uint64_t)((h * T::kKBlk + 32 * ks2) >> 4);
+          if constexpr (W::kQTmem)   // Q columns: 16 dims (one K step) per 8
+            mma_f16_ts_elect(tS(t, c), tmem + W::kQBase + 8 * (4 * h + ks2), bk, id_s,
+                             (h | ks2) ? 1u : 0u);
+          else
+            mma_f16_elect(tS(t, c), dq + (uint64_t)((h * 16384 + 32 * ks2) >> 4), bk, id_s,
+                          (h | ks2) ? 1u : 0u);
+        }
       mma_commit_elect(&barS[t * SB + c % SB]);
       mma_commit_elect(&kfree[x]);
     };
@@ -1143,6 +1177,13 @@ sparse_prefill_ws_kernel(Params p) {
     // S buffer ns % SB.  Neither barrier can run a phase ahead of the waiter
     // (each next phase needs an MMA this warp has not issued yet).
     int ns = does_s ? 0 : C, no = does_o ? 0 : C;
+    if (W::kQTmem && does_s && ns < C) {
+      if (!__all_sync(0xffffffffu, wait_bounded(qready, 0))) {
+        dead = true;
+        ns = no = C;
+      }
+      tc_fence_after();
+    }
     unsigned long long spin0 = 0;
     bool spinning = false;
     while (no < C || ns < C) {
