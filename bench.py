@@ -3,7 +3,7 @@ canonical top-k -> split-KV sparse attention over NVFP4 pages) on one GB300,
 as query rows/s and achieved HBM bandwidth.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--config C]
-                [--per-config 1,2,3,4] [--impl qsa|reference]
+                [--per-config 1,2,3,4,5,6,7] [--impl qsa|reference]
 
 Prints one JSON line (rank 0).  A step is one pass of the whole path over one
 batch of synthetic, seeded input; the headline workload is the wide
@@ -822,7 +822,7 @@ def main():
     # The largest single-GPU workload of the target set is the headline; the
     # others of the set are measured into per_config.
     ap.add_argument("--config", type=int, default=4)
-    ap.add_argument("--per-config", default="1,2,3,4",
+    ap.add_argument("--per-config", default="1,2,3,4,5,6,7",
                     help="comma-separated workload indices measured besides --config")
     ap.add_argument("--impl", default="qsa", choices=["qsa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
