@@ -758,7 +758,8 @@ sparse_prefill_kernel(Params p) {
 // 2 x TR consecutive rows) that share every dequantised chunk of the union of
 // their rows' selections; at head_dim 256 one (two Q tiles would not fit).
 // Tensor memory (512 columns): S buffers from column 0, then the P buffers
-// (kTok / 2 columns each: two fp16 per column), O of tile t at 256 + t D.
+// (kTok / 2 columns each: two fp16 per column), at head_dim 256 Q at 128
+// (D / 2 columns), O of tile t at 256 + t D.
 constexpr int kWsStages = 4;   // NVFP4 chunk stages of the warp-specialised kernel
 constexpr int kWsBars = 32;    // its mbarriers
 
