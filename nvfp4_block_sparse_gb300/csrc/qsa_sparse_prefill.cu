@@ -729,10 +729,11 @@ sparse_prefill_kernel(Params p) {
 
 // ---------------------------------------------------------------------------
 // Warp-specialised row tiles.  Per query tile four softmax warps own its 128
-// tensor-memory lanes (queries, softmax, epilogue) and one warp issues its
-// MMAs; ND warps dequantise the NVFP4 chunks into double-buffered fp16 K and
-// V tiles in shared memory (both with token rows), and one thread issues the
-// bulk copies.  P goes from the softmax into tensor memory (double-buffered)
+// tensor-memory lanes (queries, softmax, epilogue); two warps issue the MMAs
+// (one per tile with two tiles; with one tile one issues S and the other O);
+// ND warps dequantise the NVFP4 chunks into double-buffered fp16 K and V
+// tiles in shared memory (both with token rows; with eight warps four convert
+// K and four V), and one thread issues the bulk copies.  P goes from the softmax into tensor memory (double-buffered)
 // and feeds O += P V as the A operand from there, with V as an MN-major B
 // operand, so shared memory carries only the K and V operands.  S is
 // double-buffered in tensor memory at head_dim 256 and single-buffered at
@@ -750,10 +751,13 @@ sparse_prefill_kernel(Params p) {
 //   sfree[t][y]  tile t's softmax has loaded S buffer y       (128 arrivals)
 //   pready[t][x] P buffer x of tile t written, O rescaled     (128 arrivals)
 //   barO[t][x]   O_t += P_t(x) V(x) complete                  (commit)
+//   mdone[w]     every MMA of MMA warp w complete             (commit)
+//   qbar         the CTA's query rows landed                  (1 arrival + bytes)
+//   qready       Q in tensor memory (head_dim 256)            (128 arrivals)
 // Chunk c uses stage z = c % 4 (phase c / 4), tile buffer x = c & 1 (phase
 // c >> 1) and S buffer y = c % SB (phase c / SB), SB the S buffers per tile.
-// Each tile has its own S, P and O hand-overs, so the MMA warp can issue one
-// tile's MMAs while the other tile's softmax runs.
+// Each tile has its own S, P and O hand-overs, so one tile's MMAs issue
+// while the other tile's softmax runs.
 // At head_dim 128 a CTA holds two query tiles (NTL = 2: eight softmax warps,
 // 2 x TR consecutive rows) that share every dequantised chunk of the union of
 // their rows' selections; at head_dim 256 one (two Q tiles would not fit).
