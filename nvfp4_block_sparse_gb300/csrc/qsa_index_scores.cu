@@ -715,13 +715,15 @@ template <int P>
 cudaError_t launch_rows(const Geom& g, const int8_t* iq, const int8_t* ik_pool,
                         const int32_t* page_table, const int32_t* seqlens, int32_t* scores,
                         bool pdl, cudaStream_t stream) {
-  // Blocks per warp: about four resident CTAs per SM over the whole grid.
+  // Blocks per warp: the grid about fills the SMs at two resident CTAs each
+  // (the register cap), so each CTA's head sums serve as many blocks as that
+  // allows.
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long groups = (g.R + kGroupRows - 1) / kGroupRows;
   const long long warps_needed = (long long)g.B * g.MB * groups;
-  const long long warp_slots = (long long)sms * 4 * kWarps;
+  const long long warp_slots = (long long)sms * 2 * kWarps;
   int bpw = (int)((warps_needed + warp_slots - 1) / warp_slots);
   bpw = bpw < 1 ? 1 : (bpw > 8 ? 8 : bpw);
   cudaLaunchConfig_t cfg = {};
