@@ -616,7 +616,7 @@ def measure(qsa, case, args, dev, rank, world, l2, peak_gbs, peak_kind, steps, h
 
 
 def case_index(case: qw.Case) -> int:
-    for i, c in enumerate(qw.CONFIGS):
+    for i, c in enumerate(qw.WORKLOADS):
         if c.name == case.name and c.seed == case.seed:
             return i
     return -1
@@ -657,7 +657,7 @@ def run_qsa(args, case):
     for c in [int(x) for x in args.per_config.split(",") if x.strip() != ""]:
         if c == args.config:
             continue
-        r, _ = measure(qsa, qw.CONFIGS[c], args, dev, rank, world, l2, peak_gbs, peak_kind,
+        r, _ = measure(qsa, qw.WORKLOADS[c], args, dev, rank, world, l2, peak_gbs, peak_kind,
                        args.steps, headline=False)
         per_config[str(c)] = r
         torch.cuda.empty_cache()
@@ -829,7 +829,7 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    case = qw.CONFIGS[args.config]
+    case = qw.WORKLOADS[args.config]
     if args.impl == "reference":
         run_reference(args, case)
         return

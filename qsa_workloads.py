@@ -79,7 +79,7 @@ class Case:
 # The workloads the method is measured on: five at head_dim 128, then one in
 # the geometry the pages tune their kernels on (24 q / 2 KV heads, head_dim
 # 256, 32-token pages, four rows per request as in an MTP-3 verify step).
-CONFIGS = [
+WORKLOADS = [
     Case("tiny decode", seed=0, batch=1, rows_per_req=1, num_q_heads=8,
          num_kv_heads=1, page_size=64, ctx_lo=4096, ctx_hi=4096, k=16,
          window=2, max_blocks=64, pool="identity"),
@@ -111,7 +111,7 @@ CONFIGS = [
 ]
 
 # Workloads whose rows are context row groups (served by the row-tile path).
-PREFILL_CONFIGS = (6, 7)
+PREFILL_WORKLOADS = (6, 7)
 
 
 def small(case: Case, batch: Optional[int] = None, ctx_lo: Optional[int] = None,

@@ -51,13 +51,13 @@ def _check(case):
 
 
 def test_bytes_verify_workload_with_invalid_pages():
-    _check(qw.small(qw.CONFIGS[4], batch=2))
+    _check(qw.small(qw.WORKLOADS[4], batch=2))
 
 
 def test_bytes_head_dim_256():
-    _check(qw.small(qw.CONFIGS[5], batch=2))
+    _check(qw.small(qw.WORKLOADS[5], batch=2))
 
 
 def test_bytes_and_flops_context_rows():
-    _check(qw.CONFIGS[6].scaled(batch=1, rows_per_req=20, ctx_lo=1300, ctx_hi=1300,
+    _check(qw.WORKLOADS[6].scaled(batch=1, rows_per_req=20, ctx_lo=1300, ctx_hi=1300,
                                 max_blocks=21, k=8, window=2))

@@ -31,7 +31,7 @@ def _rank_main(rank, world, port, out):
         dist.barrier()
         ms = bench.max_over_ranks(1.5 + rank, world, torch.device("cpu"))
         rows = bench.job_rows_per_second(world, 8, 100, ms)
-        seeds = [bench.replica_seed(qw.CONFIGS[1], i, rank) for i in range(4)]
+        seeds = [bench.replica_seed(qw.WORKLOADS[1], i, rank) for i in range(4)]
         out[rank] = (ms, rows, seeds)
     finally:
         dist.destroy_process_group()
@@ -46,7 +46,7 @@ def test_two_gloo_ranks_aggregate_like_the_bench():
     (ms0, rows0, seeds0), (ms1, rows1, seeds1) = out[0], out[1]
     assert ms0 == ms1 == 2.5                       # the slower rank's time
     assert rows0 == rows1 == pytest.approx(2 * 8 * 100 / 0.0025)
-    assert seeds0[0] == qw.CONFIGS[1].seed         # rank 0, replica 0: the workload
+    assert seeds0[0] == qw.WORKLOADS[1].seed         # rank 0, replica 0: the workload
     assert not set(seeds0) & set(seeds1)           # ranks draw distinct inputs
 
 

@@ -70,9 +70,9 @@ def check_against_oracle(res, w_np, rows=None):
 # the workloads, reduced to oracle speed (several tiles + ragged tails)
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("cfg", range(len(qw.CONFIGS)))
+@pytest.mark.parametrize("cfg", range(len(qw.WORKLOADS)))
 def test_small_configs(qsa, cfg):
-    case = qw.small(qw.CONFIGS[cfg])
+    case = qw.small(qw.WORKLOADS[cfg])
     w = qw.make_workload(case, "cuda")
     res = host(run_gpu(qsa, w))
     check_against_oracle(res, qw.to_numpy(w))
@@ -82,7 +82,7 @@ def test_small_configs(qsa, cfg):
                                         (4, 1), (4, 5), (3, 1), (3, 16), (5, 1), (5, 2),
                                         (5, 8), (5, 24)])
 def test_forced_splits(qsa, cfg, splits):
-    case = qw.small(qw.CONFIGS[cfg])
+    case = qw.small(qw.WORKLOADS[cfg])
     w = qw.make_workload(case, "cuda")
     res = host(run_gpu(qsa, w, num_splits=splits))
     check_against_oracle(res, qw.to_numpy(w))
@@ -182,7 +182,7 @@ def test_all_equal_scores_select_highest_blocks(qsa):
 
 
 def test_page_permutation_leaves_outputs_bitwise_unchanged(qsa):
-    case = qw.small(qw.CONFIGS[4])
+    case = qw.small(qw.WORKLOADS[4])
     w = qw.make_workload(case, "cuda")
     res = host(run_gpu(qsa, w))
     NP = w["num_pages"]
@@ -200,7 +200,7 @@ def test_page_permutation_leaves_outputs_bitwise_unchanged(qsa):
 
 
 def test_selection_deterministic_over_50_launches(qsa):
-    case = qw.small(qw.CONFIGS[4], batch=6)
+    case = qw.small(qw.WORKLOADS[4], batch=6)
     w = qw.make_workload(case, "cuda")
     step = run_gpu(qsa, w)
     sel0, out0 = step.sel.clone(), step.out.clone()
@@ -211,7 +211,7 @@ def test_selection_deterministic_over_50_launches(qsa):
 
 
 def test_cuda_graph_replay_matches_eager(qsa):
-    case = qw.small(qw.CONFIGS[2])
+    case = qw.small(qw.WORKLOADS[2])
     w = qw.make_workload(case, "cuda")
     step = run_gpu(qsa, w)
     eager = host(step)
@@ -233,13 +233,13 @@ def test_cuda_graph_replay_matches_eager(qsa):
 
 
 def test_workspace_status_clean(qsa):
-    w = qw.make_workload(qw.small(qw.CONFIGS[1]), "cuda")
+    w = qw.make_workload(qw.small(qw.WORKLOADS[1]), "cuda")
     step = run_gpu(qsa, w)
     assert step.status() == 0
 
 
 def test_workspace_too_small_is_rejected(qsa):
-    w = qw.make_workload(qw.small(qw.CONFIGS[1]), "cuda")
+    w = qw.make_workload(qw.small(qw.WORKLOADS[1]), "cuda")
     step = run_gpu(qsa, w, num_splits=4)
     small_ws = step.workspace[:64]
     with pytest.raises(qsa.QsaError) as ei:
@@ -272,9 +272,9 @@ def _selection_properties(res, w_np):
         assert np.all(res["sel"][r, res["nsel"][r]:] == -1)
 
 
-@pytest.mark.parametrize("cfg", range(len(qw.CONFIGS)))
+@pytest.mark.parametrize("cfg", range(len(qw.WORKLOADS)))
 def test_full_size_sampled_rows(qsa, cfg):
-    case = qw.CONFIGS[cfg]
+    case = qw.WORKLOADS[cfg]
     w = qw.make_workload(case, "cuda")
     res = host(run_gpu(qsa, w))
     w_np = qw.to_numpy(w)
@@ -291,14 +291,14 @@ def test_full_size_sampled_rows(qsa, cfg):
 # fused selection + decode against the composed calls (bit for bit)
 # ---------------------------------------------------------------------------
 
-FUSED_CASES = [("cfg0", lambda: qw.small(qw.CONFIGS[0]), 0),
-               ("cfg1", lambda: qw.small(qw.CONFIGS[1]), 0),
-               ("cfg3", lambda: qw.small(qw.CONFIGS[3]), 0),
-               ("cfg1_full", lambda: qw.CONFIGS[1], 0),
-               ("cfg3_full", lambda: qw.CONFIGS[3], 0),
-               ("cfg1_split1", lambda: qw.small(qw.CONFIGS[1]), 1),
-               ("cfg1_split7", lambda: qw.small(qw.CONFIGS[1]), 7),
-               ("cfg1_split64", lambda: qw.small(qw.CONFIGS[1]), 64),
+FUSED_CASES = [("cfg0", lambda: qw.small(qw.WORKLOADS[0]), 0),
+               ("cfg1", lambda: qw.small(qw.WORKLOADS[1]), 0),
+               ("cfg3", lambda: qw.small(qw.WORKLOADS[3]), 0),
+               ("cfg1_full", lambda: qw.WORKLOADS[1], 0),
+               ("cfg3_full", lambda: qw.WORKLOADS[3], 0),
+               ("cfg1_split1", lambda: qw.small(qw.WORKLOADS[1]), 1),
+               ("cfg1_split7", lambda: qw.small(qw.WORKLOADS[1]), 7),
+               ("cfg1_split64", lambda: qw.small(qw.WORKLOADS[1]), 64),
                ("window0", lambda: EDGE_CASES["window_zero"], 0),
                ("k_one", lambda: EDGE_CASES["k_one"], 0),
                ("ties", lambda: _case(tie_frac=0.5), 0),
@@ -306,7 +306,7 @@ FUSED_CASES = [("cfg0", lambda: qw.small(qw.CONFIGS[0]), 0),
                ("gqa12", lambda: EDGE_CASES["gqa12_nt2"], 0),
                ("hd256_p32", lambda: EDGE_CASES["hd256_decode_p32"], 0),
                ("hd256_p64_split3", lambda: EDGE_CASES["hd256_decode_p64"], 3),
-               ("cfg2_composed_inside", lambda: qw.small(qw.CONFIGS[2]), 0)]
+               ("cfg2_composed_inside", lambda: qw.small(qw.WORKLOADS[2]), 0)]
 
 
 @pytest.mark.parametrize("name,make,splits", FUSED_CASES, ids=[c[0] for c in FUSED_CASES])

@@ -133,7 +133,7 @@ def test_prefill_all_pages_invalid(qsa):
 def test_prefill_on_verify_rows_matches_decode(qsa):
     # The row-tile kernel called directly on a verify geometry (R <= 8) gives
     # the decode kernel's results within the tolerance, and the oracle's.
-    w = qw.make_workload(qw.small(qw.CONFIGS[2]), "cuda")
+    w = qw.make_workload(qw.small(qw.WORKLOADS[2]), "cuda")
     step = qsa.DecodeStep(qw.geometry(w), w["k"], w["window"], device=w["q"].device)
     step.run(w)
     out = torch.empty_like(step.out)
@@ -152,9 +152,9 @@ def test_prefill_on_verify_rows_matches_decode(qsa):
     assert (lse[fin] - step.lse[fin]).abs().max().item() <= 2 * LSE_ABS
 
 
-@pytest.mark.parametrize("cfg", qw.PREFILL_CONFIGS)
+@pytest.mark.parametrize("cfg", qw.PREFILL_WORKLOADS)
 def test_prefill_full_size_sampled_rows(qsa, cfg):
-    case = qw.CONFIGS[cfg]
+    case = qw.WORKLOADS[cfg]
     w = qw.make_workload(case, "cuda")
     step = run_step(qsa, w)
     w_np = qw.to_numpy(w)

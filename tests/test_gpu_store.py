@@ -42,15 +42,15 @@ def check_store(qsa, w, new):
     return got
 
 
-@pytest.mark.parametrize("cfg", range(len(qw.CONFIGS)))
+@pytest.mark.parametrize("cfg", range(len(qw.WORKLOADS)))
 def test_store_small_configs(qsa, cfg):
-    w = qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cuda")
+    w = qw.make_workload(qw.small(qw.WORKLOADS[cfg]), "cuda")
     check_store(qsa, w, qw.make_new_tokens(w))
 
 
 @pytest.mark.parametrize("cfg", [1, 4, 5])
 def test_store_full_size(qsa, cfg):
-    w = qw.make_workload(qw.CONFIGS[cfg], "cuda")
+    w = qw.make_workload(qw.WORKLOADS[cfg], "cuda")
     check_store(qsa, w, qw.make_new_tokens(w))
 
 
@@ -84,7 +84,7 @@ def test_store_edge_cases(qsa, name):
 def test_store_saturation_underflow_and_zeros(qsa, mult, cfg):
     # Values far above the tensor scale saturate the block scale (448) and
     # the codes (6); values far below it flush the block to zero.
-    w = qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cuda")
+    w = qw.make_workload(qw.small(qw.WORKLOADS[cfg]), "cuda")
     new = qw.make_new_tokens(w)
     new["k_new"] = (new["k_new"].float() * mult).to(torch.bfloat16)
     new["v_new"] = (new["v_new"].float() * mult).to(torch.bfloat16)
@@ -93,7 +93,7 @@ def test_store_saturation_underflow_and_zeros(qsa, mult, cfg):
 
 @pytest.mark.parametrize("cfg", [2, 5])
 def test_store_then_step_matches_the_oracle(qsa, cfg):
-    w = qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cuda")
+    w = qw.make_workload(qw.small(qw.WORKLOADS[cfg]), "cuda")
     new = qw.make_new_tokens(w)
     got = store_gpu(qsa, w, new)
     for n in POOLS:
@@ -131,11 +131,11 @@ def restore_gpu(qsa, w, pools, rejected, saved):
     torch.cuda.synchronize()
 
 
-ROLLBACK_CASES = [("cfg2", lambda: qw.small(qw.CONFIGS[2])), ("cfg4", lambda: qw.small(qw.CONFIGS[4])),
+ROLLBACK_CASES = [("cfg2", lambda: qw.small(qw.WORKLOADS[2])), ("cfg4", lambda: qw.small(qw.WORKLOADS[4])),
                   ("tiny", lambda: STORE_CASES["tiny_contexts_verify"]),
                   ("invalid", lambda: STORE_CASES["mostly_invalid"]),
-                  ("full4", lambda: qw.CONFIGS[4]),
-                  ("cfg5", lambda: qw.small(qw.CONFIGS[5])),
+                  ("full4", lambda: qw.WORKLOADS[4]),
+                  ("cfg5", lambda: qw.small(qw.WORKLOADS[5])),
                   ("hd256_tiny", lambda: STORE_CASES["hd256_p64_tiny"])]
 
 

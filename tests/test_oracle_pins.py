@@ -261,7 +261,7 @@ def test_select_matches_brute_force():
 
 
 def test_select_properties_on_generated_case():
-    case = qw.small(qw.CONFIGS[4], batch=4)
+    case = qw.small(qw.WORKLOADS[4], batch=4)
     w = qw.to_numpy(qw.make_workload(case, "cpu"))
     sc = oracle.index_scores(w)
     sel, nsel = oracle.select(w, sc)
@@ -505,8 +505,8 @@ def test_quantize_matches_the_generators_encoder():
 
 @pytest.mark.parametrize("cfg", [2, 4, 5])
 def test_store_kv_writes_exactly_the_new_slots(cfg):
-    w = qw.to_numpy(qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cpu"))
-    new = qw.to_numpy(qw.make_new_tokens(qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cpu")))
+    w = qw.to_numpy(qw.make_workload(qw.small(qw.WORKLOADS[cfg]), "cpu"))
+    new = qw.to_numpy(qw.make_new_tokens(qw.make_workload(qw.small(qw.WORKLOADS[cfg]), "cpu")))
     out = oracle.store_kv(w, new)
     B, R, P, MB, Hkv = w["batch"], w["rows_per_req"], w["page_size"], w["max_blocks"], w["num_kv_heads"]
     D = w["head_dim"]
@@ -554,8 +554,8 @@ def _half_rejected(T):
 
 @pytest.mark.parametrize("cfg", [2, 4, 5])
 def test_rollback_round_trip(cfg):
-    w = qw.to_numpy(qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cpu"))
-    new = qw.to_numpy(qw.make_new_tokens(qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cpu")))
+    w = qw.to_numpy(qw.make_workload(qw.small(qw.WORKLOADS[cfg]), "cpu"))
+    new = qw.to_numpy(qw.make_new_tokens(qw.make_workload(qw.small(qw.WORKLOADS[cfg]), "cpu")))
     names = ("k_pool", "k_sf", "v_pool", "v_sf", "ik_pool")
     saved = oracle.rollback_gather(w, w)
     stored = oracle.store_kv(w, new)
@@ -594,7 +594,7 @@ def test_rollback_round_trip(cfg):
 @pytest.mark.parametrize("cfg", [2, 5])
 def test_rollback_saved_layout(cfg):
     # the saved bytes of a row are its slots' bytes in the documented order
-    w = qw.to_numpy(qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cpu"))
+    w = qw.to_numpy(qw.make_workload(qw.small(qw.WORKLOADS[cfg]), "cpu"))
     saved = oracle.rollback_gather(w, w)
     Hkv, P, R, D = w["num_kv_heads"], w["page_size"], w["rows_per_req"], w["head_dim"]
     c, f = D // 2, D // 16            # code and scale bytes per token row

@@ -43,7 +43,7 @@ def _close(out, lse, ref_out, ref_lse):
 
 @pytest.mark.parametrize("cfg", [1, 2, 4])
 def test_noalloc_matches_workspace_entry_point_twice(qsa, cfg):
-    w = qw.make_workload(qw.small(qw.CONFIGS[cfg]), "cuda")
+    w = qw.make_workload(qw.small(qw.WORKLOADS[cfg]), "cuda")
     step = qsa.DecodeStep(qw.geometry(w), w["k"], w["window"])
     step.run(w)                     # scores, selection and the reference output
     torch.cuda.synchronize()
@@ -136,7 +136,7 @@ def test_noalloc_reports_a_wait_that_gave_up(qsa):
     # (the copies still land before it finishes): the built-in array's status
     # word then reports QSA_ERR_DEVICE_TIMEOUT until it is read, and the next
     # call under the default bound is correct again.
-    w = qw.make_workload(qw.small(qw.CONFIGS[1]), "cuda")
+    w = qw.make_workload(qw.small(qw.WORKLOADS[1]), "cuda")
     step = qsa.DecodeStep(qw.geometry(w), w["k"], w["window"])
     step.run(w)
     torch.cuda.synchronize()
