@@ -704,6 +704,16 @@ def run_qsa(args, case):
     print(json.dumps(line), flush=True)
 
 
+# End-to-end loop shape: inputs travel in groups of up to E2E_GROUP_BYTES of
+# steps (at most an eighth of a graph's steps, so that groups overlap), and
+# one CUDA graph holds at least E2E_MIN_STEPS steps (a whole number of rounds
+# over the replicas) so that its start and end joins are shared by many
+# steps, as in a serving loop that never drains.
+E2E_GROUP_BYTES = 4 << 20
+E2E_MIN_STEPS = 64
+E2E_MAX_RESULT_BYTES = 256 << 20
+
+
 def run_e2e(qsa, step, reps, stream, args, dev, T, world):
     """Same metric through the public API with HOST buffers: each step copies
     its query-side inputs (q, iq, page table, seqlens) from pinned host memory
@@ -711,39 +721,41 @@ def run_e2e(qsa, step, reps, stream, args, dev, T, world):
     K/V pages and index keys are the cache: resident in HBM.
 
     Steps are pipelined as a serving loop runs them: the inputs of a group of
-    steps (about 1 MB) are copied in on an input stream ahead of the group,
-    and each step's results are copied out on an output stream as soon as it
-    is done, while the next steps compute; every step still moves its own
-    inputs in and its own results out inside the timed region.  The loop is
-    captured as CUDA graphs of 2 * replicas steps (forked and joined on the
-    compute stream) and replayed back to back."""
-    # A step's query-side inputs travel as one pinned host buffer into one
-    # device buffer whose 256-byte-aligned slices are the step's tensors; the
-    # results (out, then lse) come back in one copy of DecodeStep.results.
+    steps (up to 4 MB) are copied in on an input stream into one of two sets
+    of device slots while the previous group computes from the other set, and
+    each step's results are copied out on an output stream as soon as it is
+    done, while the next steps compute; every step still moves its own inputs
+    in and its own results out inside the timed region.  The loop is captured
+    as CUDA graphs of whole rounds over the replicas (at least E2E_MIN_STEPS
+    steps; forked and joined on the compute stream) and replayed back to
+    back."""
+    # A step's query-side inputs travel as one pinned host buffer (one per
+    # replica) into one device slot whose 256-byte-aligned slices are the
+    # step's tensors; the results (out, then lse) come back in one copy of
+    # DecodeStep.results.
     keys = ("q", "iq", "page_table", "seqlens")
     offs, total = {}, 0
     for k in keys:
         offs[k] = total
         nb = reps[0][k].numel() * reps[0][k].element_size()
         total += (nb + 255) // 256 * 256
-    host, dev_in = [], []
+    host = []
     for w in reps:
         hb = torch.empty((total,), dtype=torch.uint8).pin_memory()
-        db = torch.empty((total,), dtype=torch.uint8, device=w["q"].device)
         for k in keys:
             t = w[k]
             nb = t.numel() * t.element_size()
             hb[offs[k]:offs[k] + nb].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
-            w[k] = db[offs[k]:offs[k] + nb].view(t.dtype).view(t.shape)
-        db.copy_(hb)
         host.append(hb)
-        dev_in.append(db)
     nrep = len(reps)
-    per_graph = 2 * nrep                 # every replica twice per graph
-    # One device result span (out, then lse) and one pinned host span per step
-    # of a graph, so that no step waits for an earlier step's result copy.
+    # Result spans: one device span (out, then lse) and one pinned host span
+    # per step of a graph, so that no step waits for an earlier step's copy.
     rbytes = step.results.numel()
     rstride = (rbytes + 255) // 256 * 256    # every span 256-byte aligned
+    rounds = max(2, -(-E2E_MIN_STEPS // nrep))
+    while rounds > 2 and rounds * nrep * rstride > E2E_MAX_RESULT_BYTES:
+        rounds -= 1
+    per_graph = rounds * nrep                # step i runs replica i % nrep
     out_bytes = step.out.numel() * step.out.element_size()
     lse_off = (out_bytes + 255) // 256 * 256
     res_d = torch.empty((per_graph, rstride), dtype=torch.uint8, device=dev)[:, :rbytes]
@@ -755,32 +767,42 @@ def run_e2e(qsa, step, reps, stream, args, dev, T, world):
     s_in = torch.cuda.Stream(device=dev)
     s_out = torch.cuda.Stream(device=dev)
 
-    # Inputs go in groups of about 1 MB of steps: the compute stream waits once
+    # Groups of up to E2E_GROUP_BYTES of steps: the compute stream waits once
     # per group (consecutive steps of a group keep their programmatic-launch
-    # overlap), and a large step's inputs are not queued behind its group's.
-    grp = max(1, min(nrep, (1 << 20) // max(1, total)))
+    # overlap).  Group n's inputs go to slot set n % 2, once group n - 2 (the
+    # last user of that set) has finished.
+    grp = max(1, min(per_graph // 8, E2E_GROUP_BYTES // max(1, total)))
+    slots = torch.empty((2 * grp, total), dtype=torch.uint8, device=dev)
+
+    def inputs_in(slot, r):
+        v = dict(reps[r])
+        for k in keys:
+            t = reps[r][k]
+            nb = t.numel() * t.element_size()
+            v[k] = slots[slot, offs[k]:offs[k] + nb].view(t.dtype).view(t.shape)
+        return v
 
     def body():
         ev_run = [torch.cuda.Event() for _ in range(per_graph)]
         s_in.wait_stream(stream)
         s_out.wait_stream(stream)
-        for half in range(2):
-            for g0 in range(0, nrep, grp):
-                ev_in = torch.cuda.Event()
-                with torch.cuda.stream(s_in):
-                    for r in range(g0, min(nrep, g0 + grp)):
-                        if half:
-                            s_in.wait_event(ev_run[r])    # replica r's inputs are free
-                        dev_in[r].copy_(host[r], non_blocking=True)
-                    ev_in.record(s_in)
-                stream.wait_event(ev_in)
-                for r in range(g0, min(nrep, g0 + grp)):
-                    i = half * nrep + r
-                    step.run(reps[r], stream=stream, out=outs[i], lse=lses[i])
-                    ev_run[i].record(stream)
-                    with torch.cuda.stream(s_out):
-                        s_out.wait_event(ev_run[i])
-                        res_h[i].copy_(res_d[i], non_blocking=True)
+        for n, g0 in enumerate(range(0, per_graph, grp)):
+            idx = range(g0, min(per_graph, g0 + grp))
+            ev_in = torch.cuda.Event()
+            with torch.cuda.stream(s_in):
+                if n >= 2:
+                    s_in.wait_event(ev_run[g0 - grp - 1])   # group n - 2 is done
+                for i in idx:
+                    slots[(n % 2) * grp + i - g0].copy_(host[i % nrep], non_blocking=True)
+                ev_in.record(s_in)
+            stream.wait_event(ev_in)
+            for i in idx:
+                step.run(inputs_in((n % 2) * grp + i - g0, i % nrep), stream=stream,
+                         out=outs[i], lse=lses[i])
+                ev_run[i].record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_run[i])
+                    res_h[i].copy_(res_d[i], non_blocking=True)
         stream.wait_stream(s_in)
         stream.wait_stream(s_out)
 
@@ -809,9 +831,10 @@ def run_e2e(qsa, step, reps, stream, args, dev, T, world):
     ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     return {"value": job_rows_per_second(world, T, n, ms), "unit": "rows/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
-            "pipelined": "inputs copied in per ~1 MB group of steps ahead of the group; "
-                         "each step's results copied out while the next steps run",
-            "input_group_steps": grp}
+            "pipelined": "inputs copied in per group of steps (up to 4 MB) into one of two "
+                         "slot sets while the previous group computes; each step's "
+                         "results copied out while the next steps run",
+            "input_group_steps": grp, "steps_per_graph": per_graph}
 
 
 def main():
