@@ -12,8 +12,9 @@ workload of the set is measured the same way into ``per_config``.  Steps
 rotate over input replicas held in distinct HBM buffers whose touched bytes
 add up to at least 4x the L2 size, so every step reads HBM.
 
-Timing: exactly K steps as CUDA graph replays (one step per replica) with CUDA
-events on the launching stream between replays, a barrier and synchronize on
+Timing: exactly K steps as CUDA graph replays (whole rounds of steps over the
+replicas, at least 64 steps per graph) with CUDA events on the launching
+stream between replays, a barrier and synchronize on
 both sides; ``steady`` adds the median over many replays.  Per call: the call
 alone on every replica back to back in one graph (median over replays,
 divided by the replicas; the roofline uses this), and the same call isolated
@@ -41,6 +42,8 @@ import qsa_workloads as qw  # noqa: E402
 
 METRIC = "sparse decode query-rows/s per GPU; achieved HBM GB/s vs GB300 peak"
 L2_BYTES_DEFAULT = 129 * 1024 * 1024
+# Device-timed steps run as CUDA graphs of at least TIMED_MIN_STEPS steps.
+TIMED_MIN_STEPS = 64
 
 
 # ---------------------------------------------------------------------------
@@ -436,28 +439,33 @@ def measure(qsa, case, args, dev, rank, world, l2, peak_gbs, peak_kind, steps, h
 
     stream = torch.cuda.Stream(device=dev)
     stream.wait_stream(torch.cuda.current_stream(dev))
-    # Warm-up (eager), then graphs of one step per replica in turn.
+    # Warm-up (eager), then graphs of whole rounds over the replicas (step i
+    # runs replica i % nrep; at least TIMED_MIN_STEPS steps per graph, so that
+    # most step boundaries keep their programmatic-launch overlap, as in a
+    # serving loop).
+    rounds = max(1, -(-TIMED_MIN_STEPS // nrep))
+    per_graph = rounds * nrep
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             step.run(reps[i % nrep], stream=stream, bufs=bufs[i % nrep])
         stream.synchronize()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
-            for w, b in zip(reps, bufs):
-                step.run(w, stream=stream, bufs=b)
-        rem = steps % nrep
+            for i in range(per_graph):
+                step.run(reps[i % nrep], stream=stream, bufs=bufs[i % nrep])
+        rem = steps % per_graph
         graph_rem = None
         if rem:
             graph_rem = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph_rem, stream=stream):
-                for w, b in zip(reps[:rem], bufs[:rem]):
-                    step.run(w, stream=stream, bufs=b)
+                for i in range(rem):
+                    step.run(reps[i % nrep], stream=stream, bufs=bufs[i % nrep])
         for _ in range(2):
             graph.replay()
         stream.synchronize()
 
     # ---- timed region: exactly `steps` steps, events between graph replays --
-    full, rem = divmod(steps, nrep)
+    full, rem = divmod(steps, per_graph)
     nseg = full + (1 if rem else 0)
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(nseg + 1)]
     if world > 1:
@@ -481,12 +489,12 @@ def measure(qsa, case, args, dev, rank, world, l2, peak_gbs, peak_kind, steps, h
     if world > 1:
         torch.distributed.barrier()
     ms = max_over_ranks(evs[0].elapsed_time(evs[nseg]), world, dev)
-    seg_ms_per_step = [evs[i].elapsed_time(evs[i + 1]) / nrep for i in range(full)]
+    seg_ms_per_step = [evs[i].elapsed_time(evs[i + 1]) / per_graph for i in range(full)]
     ms_step = ms / steps
     rows_s = job_rows_per_second(world, T, steps, ms)
 
-    # ---- steady state: replays of the whole replica graph -------------------
-    n_steady = max(10, min(200, int(math.ceil(3000 / nrep))))
+    # ---- steady state: replays of the whole graph -----------------------------
+    n_steady = max(10, min(200, int(math.ceil(3000 / per_graph))))
     st_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_steady + 1)]
     with torch.cuda.stream(stream):
         st_ev[0].record(stream)
@@ -494,7 +502,7 @@ def measure(qsa, case, args, dev, rank, world, l2, peak_gbs, peak_kind, steps, h
             graph.replay()
             st_ev[i + 1].record(stream)
     stream.synchronize()
-    steady = [st_ev[i].elapsed_time(st_ev[i + 1]) / nrep for i in range(n_steady)]
+    steady = [st_ev[i].elapsed_time(st_ev[i + 1]) / per_graph for i in range(n_steady)]
     steady_med = statistics.median(steady)
 
     # ---- per call, in stream: the call alone on every replica back to back ---
@@ -594,7 +602,7 @@ def measure(qsa, case, args, dev, rank, world, l2, peak_gbs, peak_kind, steps, h
         "ms_per_step_segments_median": (statistics.median(seg_ms_per_step)
                                         if seg_ms_per_step else None),
         "steady": {"ms_per_step_median": steady_med, "rows_s": world * T / (steady_med / 1e3),
-                   "replays": n_steady, "steps_per_replay": nrep},
+                   "replays": n_steady, "steps_per_replay": per_graph},
         "step_hbm": {"bytes": mean["step"], "achieved_gbs": step_gbs, "peak_gbs": peak_gbs,
                      "frac": step_gbs / peak_gbs, "steady_gbs": steady_gbs,
                      "steady_frac": steady_gbs / peak_gbs, "peak_kind": peak_kind},
@@ -686,8 +694,9 @@ def run_qsa(args, case):
         "config": {"workload": head["workload"], "config_index": args.config,
                    "query_rows_per_step": head["query_rows_per_step"],
                    "replicas": head["replicas"], "l2_defeat": head["l2_defeat"],
-                   "timing": "CUDA graph replays of one step per replica; CUDA events on the "
-                   "launching stream between replays"},
+                   "timing": "CUDA graph replays of whole rounds of steps over the replicas "
+                   "(at least %d steps per graph); CUDA events on the launching stream "
+                   "between replays" % TIMED_MIN_STEPS},
         "ms_per_step_segments_median": head["ms_per_step_segments_median"],
         "steady": head["steady"],
         "step_hbm": head["step_hbm"],
