@@ -443,8 +443,7 @@ def measure(qsa, case, args, dev, rank, world, l2, peak_gbs, peak_kind, steps, h
     # runs replica i % nrep; at least TIMED_MIN_STEPS steps per graph, so that
     # most step boundaries keep their programmatic-launch overlap, as in a
     # serving loop).
-    rounds = max(1, -(-TIMED_MIN_STEPS // nrep))
-    per_graph = rounds * nrep
+    per_graph, full, rem = timed_plan(steps, nrep)
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             step.run(reps[i % nrep], stream=stream, bufs=bufs[i % nrep])
@@ -453,7 +452,6 @@ def measure(qsa, case, args, dev, rank, world, l2, peak_gbs, peak_kind, steps, h
         with torch.cuda.graph(graph, stream=stream):
             for i in range(per_graph):
                 step.run(reps[i % nrep], stream=stream, bufs=bufs[i % nrep])
-        rem = steps % per_graph
         graph_rem = None
         if rem:
             graph_rem = torch.cuda.CUDAGraph()
@@ -465,7 +463,6 @@ def measure(qsa, case, args, dev, rank, world, l2, peak_gbs, peak_kind, steps, h
         stream.synchronize()
 
     # ---- timed region: exactly `steps` steps, events between graph replays --
-    full, rem = divmod(steps, per_graph)
     nseg = full + (1 if rem else 0)
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(nseg + 1)]
     if world > 1:
@@ -723,6 +720,32 @@ E2E_MIN_STEPS = 64
 E2E_MAX_RESULT_BYTES = 256 << 20
 
 
+def e2e_schedule(nrep: int, input_bytes: int, result_stride: int):
+    """The end-to-end loop's plan: (steps per graph, steps per input group,
+    groups).  Step i of a graph runs replica i % nrep; group n is
+    (n, its steps, its first input slot, the step whose completion frees its
+    slots or None): its inputs go to slot set n % 2 (slots
+    (n % 2) * grp ..), last read by group n - 2."""
+    rounds = max(2, -(-E2E_MIN_STEPS // nrep))
+    while rounds > 2 and rounds * nrep * result_stride > E2E_MAX_RESULT_BYTES:
+        rounds -= 1
+    per_graph = rounds * nrep
+    grp = max(1, min(per_graph // 8, E2E_GROUP_BYTES // max(1, input_bytes)))
+    groups = []
+    for n, g0 in enumerate(range(0, per_graph, grp)):
+        steps = list(range(g0, min(per_graph, g0 + grp)))
+        groups.append((n, steps, (n % 2) * grp, g0 - grp - 1 if n >= 2 else None))
+    return per_graph, grp, groups
+
+
+def timed_plan(steps: int, nrep: int):
+    """Device-timed steps: (steps per graph, full graph replays, steps of the
+    remainder graph); step i of a graph runs replica i % nrep."""
+    per_graph = max(1, -(-TIMED_MIN_STEPS // nrep)) * nrep
+    full, rem = divmod(steps, per_graph)
+    return per_graph, full, rem
+
+
 def run_e2e(qsa, step, reps, stream, args, dev, T, world):
     """Same metric through the public API with HOST buffers: each step copies
     its query-side inputs (q, iq, page table, seqlens) from pinned host memory
@@ -761,10 +784,7 @@ def run_e2e(qsa, step, reps, stream, args, dev, T, world):
     # per step of a graph, so that no step waits for an earlier step's copy.
     rbytes = step.results.numel()
     rstride = (rbytes + 255) // 256 * 256    # every span 256-byte aligned
-    rounds = max(2, -(-E2E_MIN_STEPS // nrep))
-    while rounds > 2 and rounds * nrep * rstride > E2E_MAX_RESULT_BYTES:
-        rounds -= 1
-    per_graph = rounds * nrep                # step i runs replica i % nrep
+    per_graph, grp, groups = e2e_schedule(nrep, total, rstride)
     out_bytes = step.out.numel() * step.out.element_size()
     lse_off = (out_bytes + 255) // 256 * 256
     res_d = torch.empty((per_graph, rstride), dtype=torch.uint8, device=dev)[:, :rbytes]
@@ -780,7 +800,6 @@ def run_e2e(qsa, step, reps, stream, args, dev, T, world):
     # per group (consecutive steps of a group keep their programmatic-launch
     # overlap).  Group n's inputs go to slot set n % 2, once group n - 2 (the
     # last user of that set) has finished.
-    grp = max(1, min(per_graph // 8, E2E_GROUP_BYTES // max(1, total)))
     slots = torch.empty((2 * grp, total), dtype=torch.uint8, device=dev)
 
     def inputs_in(slot, r):
@@ -795,18 +814,17 @@ def run_e2e(qsa, step, reps, stream, args, dev, T, world):
         ev_run = [torch.cuda.Event() for _ in range(per_graph)]
         s_in.wait_stream(stream)
         s_out.wait_stream(stream)
-        for n, g0 in enumerate(range(0, per_graph, grp)):
-            idx = range(g0, min(per_graph, g0 + grp))
+        for _, idx, slot0, free_after in groups:
             ev_in = torch.cuda.Event()
             with torch.cuda.stream(s_in):
-                if n >= 2:
-                    s_in.wait_event(ev_run[g0 - grp - 1])   # group n - 2 is done
+                if free_after is not None:
+                    s_in.wait_event(ev_run[free_after])   # group n - 2 is done
                 for i in idx:
-                    slots[(n % 2) * grp + i - g0].copy_(host[i % nrep], non_blocking=True)
+                    slots[slot0 + i - idx[0]].copy_(host[i % nrep], non_blocking=True)
                 ev_in.record(s_in)
             stream.wait_event(ev_in)
             for i in idx:
-                step.run(inputs_in((n % 2) * grp + i - g0, i % nrep), stream=stream,
+                step.run(inputs_in(slot0 + i - idx[0], i % nrep), stream=stream,
                          out=outs[i], lse=lses[i])
                 ev_run[i].record(stream)
                 with torch.cuda.stream(s_out):
